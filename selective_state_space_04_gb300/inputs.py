@@ -1,0 +1,100 @@
+"""Seeded synthetic inputs for the SSD forward scan.
+
+This module only draws random numbers and lays them out; it holds none of the
+scan's arithmetic.  The same tensors (same bytes) feed the CUDA path and the
+fp64 oracle.
+
+Workloads are shaped like the Mamba layers that the source pages build
+(@seanhogg/builderforce-memory-engine ``Mamba2BlockConfig``: multi-head SSM
+with scalar A per head, state size N, head groups G, chunk length Q).
+
+Distributions (one recipe for every workload):
+  x ~ N(0, 1)                          [B, L, H, P]   storage dtype
+  dt_raw ~ N(0, 0.1^2)                 [B, L, H]      fp32
+  dt0 = exp(U[ln 1e-3, ln 1e-1]),  dt_bias = log(expm1(dt0))   [H] fp32
+      (the inverse of softplus, so that softplus(dt_bias) = dt0)
+  A_log = log(U[1, 16])                [H]            fp32
+  B, C ~ N(0, 1)                       [B, L, G, N]   storage dtype
+  D ~ N(0, 1)                          [H]            fp32
+  init_state ~ N(0, 0.1^2)             [B, H, P, N]   fp32 (only where used)
+Draw order is fixed: x, dt_raw, dt0, A_log, B, C, D, init_state, from one
+numpy PCG64 stream seeded with ``seed``.  Values are drawn in float32 and
+cast once to the storage dtype (bf16: round to nearest even).
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    seqlen: int
+    nheads: int
+    headdim: int
+    dstate: int
+    ngroups: int
+    chunk: int
+    dtype: str          # storage dtype of x, B, C, y: "bf16" or "f32"
+    init_state: bool    # whether a non-zero initial state is passed
+
+    @property
+    def token_heads(self) -> int:
+        return self.batch * self.seqlen * self.nheads
+
+    def with_(self, **kw) -> "Workload":
+        return replace(self, **kw)
+
+
+WORKLOADS = {
+    # tiny fp32 case that the oracle finishes in milliseconds
+    "tiny_fp32": Workload("tiny_fp32", 1, 64, 2, 8, 16, 1, 16, "f32", False),
+    # Mamba-2 130M layer: d_model 768, expand 2 -> H = 24 heads of P = 64
+    "mamba2_130m_layer": Workload("mamba2_130m_layer", 4, 2048, 24, 64, 128, 1, 256, "bf16", False),
+    # Mamba-2 2.7B layer: d_model 2560, expand 2 -> H = 80 heads of P = 64
+    "mamba2_2p7b_layer": Workload("mamba2_2p7b_layer", 8, 4096, 80, 64, 128, 1, 256, "bf16", False),
+    # one 64k-token sequence, 8 groups of 4 heads, carried-in and returned state
+    "long_context_64k": Workload("long_context_64k", 1, 65536, 32, 64, 128, 8, 256, "bf16", True),
+    # many 64-token sequences with per-sequence state in and out
+    "many_short_seqs": Workload("many_short_seqs", 256, 64, 48, 64, 128, 1, 64, "bf16", True),
+}
+
+_TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
+
+
+def torch_dtype(dtype: str) -> torch.dtype:
+    return _TORCH_DTYPE[dtype]
+
+
+def make_inputs(w: Workload, seed: int = 0) -> dict:
+    """Draw one seeded input set for workload ``w`` as CPU torch tensors.
+
+    Keys: x, dt_raw, dt_bias, A_log, B, C, D, init_state (None when
+    ``w.init_state`` is False).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    Bt, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    sd = _TORCH_DTYPE[w.dtype]
+
+    def normal(shape, std=1.0):
+        a = rng.standard_normal(size=shape, dtype=np.float32)
+        if std != 1.0:
+            a *= np.float32(std)
+        return a
+
+    x = torch.from_numpy(normal((Bt, L, H, P))).to(sd)
+    dt_raw = torch.from_numpy(normal((Bt, L, H), 0.1))
+    dt0 = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=H))
+    dt_bias = torch.from_numpy(np.log(np.expm1(dt0)).astype(np.float32))
+    A_log = torch.from_numpy(np.log(rng.uniform(1.0, 16.0, size=H)).astype(np.float32))
+    Bm = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    Cm = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    D = torch.from_numpy(normal((H,)))
+    init = torch.from_numpy(normal((Bt, H, P, N), 0.1)) if w.init_state else None
+    return dict(x=x, dt_raw=dt_raw, dt_bias=dt_bias, A_log=A_log, B=Bm, C=Cm, D=D,
+                init_state=init)
