@@ -1,0 +1,143 @@
+/*
+ * libssd -- forward Mamba-2 SSD (structured state-space duality) scan on one
+ * NVIDIA GB300 (sm_103a).  Plain C ABI: host or device pointers, sizes and a
+ * CUDA stream handle; no framework types.
+ *
+ * The operation (per batch row b and head h, for t = 0 .. L-1):
+ *
+ *   dt_t  = softplus(dt_raw[b,t,h] + dt_bias[h])
+ *   A_h   = -exp(A_log[h])                        A_log stores log(-A)
+ *   h_t   = exp(dt_t * A_h) * h_{t-1} + dt_t * B[b,t,g] x[b,t,h]^T      (N x P)
+ *   y[b,t,h] = C[b,t,g]^T h_t + D[h] * x[b,t,h]
+ *
+ * with g = h * G / H (contiguous blocks of H/G heads share a group) and h_{-1}
+ * the initial state (zero when none is given).  Defined by the SSD module of
+ * @seanhogg/builderforce-memory-engine 2026.6.18 (package/dist/kernels/
+ * ssd.js and ssd.d.ts, module header: scalar decay per head, MIMO state per
+ * head, chunked evaluation with a carried state, buffer layouts), taken with
+ * A = -exp(A_log), input term dt * B x^T and a readout per channel p.  The
+ * chunked evaluation (chunks of Q steps, chunk states passed from chunk to
+ * chunk) follows the chunked-scan structure of mamba-rs 0.2.1
+ * src/mamba3_siso/gpu/mamba3_gpu.rs (parallel branch of the forward layer:
+ * decay cumsum, chunk state, state passing, chunk scan) applied to the
+ * Mamba-2 recurrence above.
+ *
+ * Layouts: row-major and contiguous.
+ *   x, y                   [B, L, H, P]   dtype (bf16 or fp32)
+ *   dt_raw                 [B, L, H]      fp32
+ *   B, C                   [B, L, G, N]   dtype
+ *   dt_bias, A_log, D      [H]            fp32
+ *   init_state, final_state [B, H, P, N]  fp32 (state stored P-major, N-minor)
+ */
+#ifndef LIBSSD_SSD_H
+#define LIBSSD_SSD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SSD_ABI_VERSION 1
+
+typedef enum ssd_dtype {
+    SSD_DTYPE_F32 = 0,   /* x, B, C, y are fp32 */
+    SSD_DTYPE_BF16 = 1   /* x, B, C, y are bf16; arithmetic accumulates in fp32 */
+} ssd_dtype_t;
+
+typedef enum ssd_status {
+    SSD_OK = 0,
+    SSD_ERR_INVALID_DIMS = 1,   /* a size is negative/zero where it may not be, H % G != 0, overflow */
+    SSD_ERR_NULL_PTR = 2,       /* a required pointer is NULL */
+    SSD_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
+    SSD_ERR_UNSUPPORTED = 4,    /* dtype, shape or requested path not supported */
+    SSD_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed; nothing further enqueued */
+    SSD_ERR_TIMEOUT = 6,        /* a kernel gave up a bounded wait (read via ssd_get_device_error) */
+    SSD_ERR_ALIASING = 7        /* y overlaps an input, or the two states overlap partially */
+} ssd_status_t;
+
+/* Kernel path selection, in ssd_dims_t.flags (low 4 bits). */
+#define SSD_PATH_AUTO 0u        /* chunked tensor-core path where supported, else sequential */
+#define SSD_PATH_SEQUENTIAL 1u  /* direct recurrence, fp32 FFMA (any P, N up to 2048; fp32 or bf16) */
+#define SSD_PATH_CHUNKED 2u     /* chunked tcgen05 path: bf16, P = 64, N = 128, Q % 64 == 0, (H/G) even */
+#define SSD_PATH_MASK 0xFu
+
+typedef struct ssd_dims {
+    int64_t batch;     /* B >= 0 */
+    int64_t seqlen;    /* L >= 0; need not be a multiple of chunk (ragged last chunk) */
+    int32_t nheads;    /* H >= 1 */
+    int32_t headdim;   /* P >= 1 */
+    int32_t dstate;    /* N >= 1 */
+    int32_t ngroups;   /* G >= 1, H % G == 0 */
+    int32_t chunk;     /* Q >= 1: chunk length of the chunked evaluation (ignored by the sequential path) */
+    int32_t dtype;     /* ssd_dtype_t of x, B, C and y */
+    uint32_t flags;    /* SSD_PATH_* */
+    uint32_t reserved; /* must be 0 */
+} ssd_dims_t;
+
+/*
+ * ssd_scan_fwd -- the forward scan on device memory.
+ *
+ * All array arguments are DEVICE pointers of the current device, owned by the
+ * caller, contiguous in the layouts above and 16-byte aligned.  init_state may
+ * be NULL (zero initial state); final_state may be NULL (not returned).
+ * init_state and final_state may be the same pointer (in-place state update)
+ * but must not overlap otherwise; y must not overlap any input.
+ * `stream` is a cudaStream_t (NULL = legacy default stream).  The call only
+ * enqueues work on `stream`: it never synchronises, and returns before the
+ * results are ready.  Scratch memory (chunk-handoff flags, and chunk states
+ * when final_state is NULL) is taken stream-ordered from a library-owned
+ * memory pool and released stream-ordered after the kernel.
+ * Errors: returns a status; on any status other than SSD_OK nothing was
+ * enqueued, except SSD_ERR_CUDA raised by a launch itself.  A kernel that
+ * exceeds a bounded wait (about 2 s) records SSD_ERR_TIMEOUT in a device
+ * error word, stops, and leaves y undefined; read it with
+ * ssd_get_device_error.
+ */
+ssd_status_t ssd_scan_fwd(const void *x, const float *dt_raw, const float *dt_bias,
+                          const float *A_log, const void *B, const void *C, const float *D,
+                          const float *init_state, void *y, float *final_state,
+                          const ssd_dims_t *dims, void *stream);
+
+/*
+ * ssd_scan_fwd_host -- the same scan on HOST buffers (end-to-end use).
+ *
+ * Arguments as ssd_scan_fwd but every array is a host pointer (pinned memory
+ * gives asynchronous copies; pageable works).  The call allocates device
+ * buffers stream-ordered, copies the inputs in, runs the scan, copies y (and
+ * final_state when non-NULL) back, releases the buffers, and synchronises
+ * `stream` before returning, so the host outputs are ready on SSD_OK.
+ */
+ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *dt_bias,
+                               const float *A_log, const void *B, const void *C,
+                               const float *D, const float *init_state, void *y,
+                               float *final_state, const ssd_dims_t *dims, void *stream);
+
+/* Which path SSD_PATH_AUTO resolves to for these dims on the current device
+ * (SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED), or -(ssd_status_t) if the dims are
+ * invalid or unsupported.  Host only; launches nothing. */
+int32_t ssd_select_path(const ssd_dims_t *dims);
+
+/* Kernel launches one ssd_scan_fwd call makes for these dims (0 for empty
+ * work), or -(ssd_status_t).  Host only. */
+int32_t ssd_launches_per_call(const ssd_dims_t *dims);
+
+/* Total kernel launches this library has made in this process. */
+uint64_t ssd_launch_count(void);
+
+/* Synchronises `stream`, then reads and clears the device error word of the
+ * current device into *code (0 = none, else an ssd_status_t such as
+ * SSD_ERR_TIMEOUT).  Returns SSD_OK, or SSD_ERR_CUDA if the read failed. */
+ssd_status_t ssd_get_device_error(void *stream, uint32_t *code);
+
+/* Static description of a status code.  Never NULL. */
+const char *ssd_status_string(int32_t status);
+
+/* SSD_ABI_VERSION of the loaded library. */
+int32_t ssd_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBSSD_SSD_H */

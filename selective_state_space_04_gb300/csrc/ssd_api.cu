@@ -1,0 +1,365 @@
+// ssd_api.cu -- the C ABI of libssd: validation, path choice, scratch memory,
+// launches.  Every entry point only enqueues on the caller's stream (except
+// the host-buffer variant, which synchronises it at the end).
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "ssd.h"
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+std::atomic<uint64_t> g_launches{0};
+
+size_t elem_size(int dtype) { return dtype == SSD_DTYPE_BF16 ? 2 : 4; }
+
+bool mul_ok(int64_t a, int64_t b, int64_t *out)
+{
+    if (a < 0 || b < 0)
+        return false;
+    if (a != 0 && b > INT64_MAX / a)
+        return false;
+    *out = a * b;
+    return true;
+}
+
+struct Sizes {
+    int64_t x, dt, bc, par, state;  // bytes
+};
+
+ssd_status_t check_dims(const ssd_dims_t *d, Sizes *sz)
+{
+    if (!d)
+        return SSD_ERR_NULL_PTR;
+    if (d->reserved != 0 || d->batch < 0 || d->seqlen < 0 || d->nheads < 1 || d->headdim < 1 ||
+        d->dstate < 1 || d->ngroups < 1 || d->chunk < 1 || d->nheads % d->ngroups != 0)
+        return SSD_ERR_INVALID_DIMS;
+    if (d->dtype != SSD_DTYPE_F32 && d->dtype != SSD_DTYPE_BF16)
+        return SSD_ERR_UNSUPPORTED;
+    const uint32_t path = d->flags & SSD_PATH_MASK;
+    if ((d->flags & ~SSD_PATH_MASK) != 0 || path > SSD_PATH_CHUNKED)
+        return SSD_ERR_INVALID_DIMS;
+    int64_t bl, blh, t;
+    const int64_t es = (int64_t)elem_size(d->dtype);
+    if (!mul_ok(d->batch, d->seqlen, &bl) || !mul_ok(bl, d->nheads, &blh) ||
+        !mul_ok(blh, d->headdim, &t) || !mul_ok(t, es, &sz->x) || !mul_ok(blh, 4, &sz->dt))
+        return SSD_ERR_INVALID_DIMS;
+    if (!mul_ok(bl, d->ngroups, &t) || !mul_ok(t, d->dstate, &t) || !mul_ok(t, es, &sz->bc))
+        return SSD_ERR_INVALID_DIMS;
+    sz->par = (int64_t)d->nheads * 4;
+    if (!mul_ok(d->batch, d->nheads, &t) || !mul_ok(t, d->headdim, &t) ||
+        !mul_ok(t, d->dstate, &t) || !mul_ok(t, 4, &sz->state))
+        return SSD_ERR_INVALID_DIMS;
+    if (sz->x > (INT64_C(1) << 46) || sz->state > (INT64_C(1) << 46) || d->seqlen >= (INT64_C(1) << 31))
+        return SSD_ERR_INVALID_DIMS;
+    return SSD_OK;
+}
+
+ScanArgs make_args(const void *x, const float *dt_raw, const float *dt_bias, const float *A_log,
+                   const void *B, const void *C, const float *D, const float *init_state, void *y,
+                   float *final_state, const ssd_dims_t *d)
+{
+    ScanArgs a;
+    a.x = x;
+    a.dt_raw = dt_raw;
+    a.dt_bias = dt_bias;
+    a.A_log = A_log;
+    a.B = B;
+    a.C = C;
+    a.D = D;
+    a.init_state = init_state;
+    a.y = y;
+    a.final_state = final_state;
+    a.batch = d->batch;
+    a.seqlen = d->seqlen;
+    a.nheads = d->nheads;
+    a.headdim = d->headdim;
+    a.dstate = d->dstate;
+    a.ngroups = d->ngroups;
+    a.chunk = d->chunk;
+    a.dtype = d->dtype;
+    return a;
+}
+
+bool overlaps(const void *p, int64_t pn, const void *q, int64_t qn)
+{
+    if (!p || !q || pn <= 0 || qn <= 0)
+        return false;
+    const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+    return a < b + (uintptr_t)qn && b < a + (uintptr_t)pn;
+}
+
+bool aligned16(const void *p) { return p == nullptr || ((uintptr_t)p & 15u) == 0; }
+
+bool device_is_gb300_class()
+{
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return false;
+    return major == 10 && minor == 3;
+}
+
+// Resolves the path for validated dims.  Returns SSD_PATH_* or -status.
+int32_t resolve_path(const ScanArgs &a, uint32_t requested, bool probe_device)
+{
+    const bool seq_ok = seq_supported(a.headdim, a.dstate);
+    const bool chunk_ok = chunk_supported(a) && (!probe_device || device_is_gb300_class());
+    if (requested == SSD_PATH_SEQUENTIAL)
+        return seq_ok ? (int32_t)SSD_PATH_SEQUENTIAL : -(int32_t)SSD_ERR_UNSUPPORTED;
+    if (requested == SSD_PATH_CHUNKED)
+        return chunk_ok ? (int32_t)SSD_PATH_CHUNKED : -(int32_t)SSD_ERR_UNSUPPORTED;
+    if (chunk_ok)
+        return SSD_PATH_CHUNKED;
+    if (seq_ok)
+        return SSD_PATH_SEQUENTIAL;
+    return -(int32_t)SSD_ERR_UNSUPPORTED;
+}
+
+// Library-owned stream-ordered memory pool per device (kept cached so that
+// repeated calls do not go back to the driver).
+cudaMemPool_t scratch_pool(int dev)
+{
+    static std::mutex mu;
+    static cudaMemPool_t pools[64] = {};
+    if (dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!pools[dev]) {
+        cudaMemPoolProps props;
+        std::memset(&props, 0, sizeof(props));
+        props.allocType = cudaMemAllocationTypePinned;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        cudaMemPool_t p = nullptr;
+        if (cudaMemPoolCreate(&p, &props) != cudaSuccess)
+            return nullptr;
+        uint64_t keep = UINT64_MAX;
+        cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
+        pools[dev] = p;
+    }
+    return pools[dev];
+}
+
+ssd_status_t run_device(const ScanArgs &a, uint32_t requested, cudaStream_t st)
+{
+    const int32_t path = resolve_path(a, requested, true);
+    if (path < 0)
+        return (ssd_status_t)(-path);
+    if (path == SSD_PATH_SEQUENTIAL) {
+        return seq_launch(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    const size_t ws_bytes = chunk_workspace_bytes(a);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool)
+        return SSD_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, ws_bytes, pool, st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    const ssd_status_t s = chunk_launch(a, ws, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && s == SSD_OK)
+        return SSD_ERR_CUDA;
+    return s;
+}
+
+ssd_status_t validate(const void *x, const float *dt_raw, const float *dt_bias, const float *A_log,
+                      const void *B, const void *C, const float *D, const float *init_state,
+                      const void *y, const float *final_state, const ssd_dims_t *dims, Sizes *sz)
+{
+    ssd_status_t s = check_dims(dims, sz);
+    if (s != SSD_OK)
+        return s;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!x || !dt_raw || !dt_bias || !A_log || !B || !C || !D || !y))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state};
+    for (const void *p : ptrs)
+        if (!aligned16(p))
+            return SSD_ERR_MISALIGNED;
+    if (work) {
+        const void *ins[] = {x, dt_raw, dt_bias, A_log, B, C, D, init_state};
+        const int64_t inb[] = {sz->x, sz->dt, sz->par, sz->par, sz->bc, sz->bc, sz->par, sz->state};
+        for (int i = 0; i < 8; ++i) {
+            if (overlaps(y, sz->x, ins[i], inb[i]))
+                return SSD_ERR_ALIASING;
+            if (overlaps(final_state, sz->state, ins[i], inb[i]) && !(i == 7 && final_state == init_state))
+                return SSD_ERR_ALIASING;
+        }
+        if (overlaps(final_state, sz->state, y, sz->x))
+            return SSD_ERR_ALIASING;
+    } else if (init_state && final_state && init_state != final_state &&
+               overlaps(final_state, sz->state, init_state, sz->state)) {
+        return SSD_ERR_ALIASING;
+    }
+    return SSD_OK;
+}
+
+}  // namespace
+
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace ssd
+
+using namespace ssd;
+
+extern "C" {
+
+ssd_status_t ssd_scan_fwd(const void *x, const float *dt_raw, const float *dt_bias,
+                          const float *A_log, const void *B, const void *C, const float *D,
+                          const float *init_state, void *y, float *final_state,
+                          const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->batch == 0)
+        return SSD_OK;
+    if (dims->seqlen == 0) {
+        // no steps: the final state is the initial state (zero when none)
+        if (!final_state || sz.state == 0)
+            return SSD_OK;
+        cudaError_t e = init_state ? (init_state == final_state
+                                          ? cudaSuccess
+                                          : cudaMemcpyAsync(final_state, init_state, (size_t)sz.state,
+                                                            cudaMemcpyDeviceToDevice, st))
+                                   : cudaMemsetAsync(final_state, 0, (size_t)sz.state, st);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    const ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
+    return run_device(a, dims->flags & SSD_PATH_MASK, st);
+}
+
+ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *dt_bias,
+                               const float *A_log, const void *B, const void *C,
+                               const float *D, const float *init_state, void *y,
+                               float *final_state, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if (dims->batch == 0 || (dims->seqlen == 0 && !final_state))
+        return SSD_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->seqlen == 0) {
+        if (init_state)
+            std::memmove(final_state, init_state, (size_t)sz.state);
+        else
+            std::memset(final_state, 0, (size_t)sz.state);
+        return SSD_OK;
+    }
+    auto up = [](int64_t v) { return (v + 255) & ~(int64_t)255; };
+    const int64_t off_x = 0, off_dt = off_x + up(sz.x), off_bias = off_dt + up(sz.dt),
+                  off_alog = off_bias + up(sz.par), off_B = off_alog + up(sz.par),
+                  off_C = off_B + up(sz.bc), off_D = off_C + up(sz.bc), off_h0 = off_D + up(sz.par),
+                  off_y = off_h0 + (init_state ? up(sz.state) : 0),
+                  off_hf = off_y + up(sz.x), total = off_hf + (final_state ? up(sz.state) : 0);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool)
+        return SSD_ERR_CUDA;
+    char *buf = nullptr;
+    if (cudaMallocFromPoolAsync((void **)&buf, (size_t)total, pool, st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    bool ok = true;
+    auto h2d = [&](int64_t off, const void *src, int64_t n) {
+        if (ok && src && n > 0)
+            ok = cudaMemcpyAsync(buf + off, src, (size_t)n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+    };
+    h2d(off_x, x, sz.x);
+    h2d(off_dt, dt_raw, sz.dt);
+    h2d(off_bias, dt_bias, sz.par);
+    h2d(off_alog, A_log, sz.par);
+    h2d(off_B, B, sz.bc);
+    h2d(off_C, C, sz.bc);
+    h2d(off_D, D, sz.par);
+    h2d(off_h0, init_state, init_state ? sz.state : 0);
+    ssd_status_t rs = SSD_ERR_CUDA;
+    if (ok) {
+        const ScanArgs a = make_args(buf + off_x, (const float *)(buf + off_dt),
+                                     (const float *)(buf + off_bias), (const float *)(buf + off_alog),
+                                     buf + off_B, buf + off_C, (const float *)(buf + off_D),
+                                     init_state ? (const float *)(buf + off_h0) : nullptr,
+                                     buf + off_y, final_state ? (float *)(buf + off_hf) : nullptr, dims);
+        rs = run_device(a, dims->flags & SSD_PATH_MASK, st);
+    }
+    if (rs == SSD_OK) {
+        ok = cudaMemcpyAsync(y, buf + off_y, (size_t)sz.x, cudaMemcpyDeviceToHost, st) == cudaSuccess;
+        if (ok && final_state)
+            ok = cudaMemcpyAsync(final_state, buf + off_hf, (size_t)sz.state, cudaMemcpyDeviceToHost,
+                                 st) == cudaSuccess;
+        if (!ok)
+            rs = SSD_ERR_CUDA;
+    }
+    cudaFreeAsync(buf, st);
+    if (cudaStreamSynchronize(st) != cudaSuccess && rs == SSD_OK)
+        rs = SSD_ERR_CUDA;
+    return rs;
+}
+
+int32_t ssd_select_path(const ssd_dims_t *dims)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return -(int32_t)s;
+    const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, dims);
+    return resolve_path(a, dims->flags & SSD_PATH_MASK, true);
+}
+
+int32_t ssd_launches_per_call(const ssd_dims_t *dims)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return -(int32_t)s;
+    if (dims->batch == 0 || dims->seqlen == 0)
+        return 0;
+    const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, dims);
+    const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
+    return path < 0 ? path : 1;
+}
+
+uint64_t ssd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+ssd_status_t ssd_get_device_error(void *stream, uint32_t *code)
+{
+    if (!code)
+        return SSD_ERR_NULL_PTR;
+    return chunk_read_device_error(static_cast<cudaStream_t>(stream), code);
+}
+
+const char *ssd_status_string(int32_t status)
+{
+    switch (status) {
+    case SSD_OK: return "ok";
+    case SSD_ERR_INVALID_DIMS: return "invalid dimensions";
+    case SSD_ERR_NULL_PTR: return "required pointer is null";
+    case SSD_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+    case SSD_ERR_UNSUPPORTED: return "dtype, shape or path not supported";
+    case SSD_ERR_CUDA: return "CUDA call failed";
+    case SSD_ERR_TIMEOUT: return "kernel exceeded a bounded wait";
+    case SSD_ERR_ALIASING: return "output overlaps an input";
+    default: return "unknown status";
+    }
+}
+
+int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// ssd_internal.h -- shared declarations between the host layer (ssd_api.cu)
+// and the kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ssd.h"
+
+namespace ssd {
+
+// Everything one scan needs, after validation.  Device pointers.
+struct ScanArgs {
+    const void *x;
+    const float *dt_raw;
+    const float *dt_bias;
+    const float *A_log;
+    const void *B;
+    const void *C;
+    const float *D;
+    const float *init_state;   // may be null
+    void *y;
+    float *final_state;        // may be null
+    int64_t batch, seqlen;
+    int nheads, headdim, dstate, ngroups, chunk;
+    int dtype;                 // ssd_dtype_t
+};
+
+// ---- sequential (direct recurrence) path: ssd_seq.cu
+bool seq_supported(int headdim, int dstate);
+cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);
+
+// ---- chunked tcgen05 path: ssd_chunk.cu
+bool chunk_supported(const ScanArgs &a);
+// Bytes of scratch the chunked path needs for these sizes (flags and, when
+// final_state is null, the chunk-handoff states).
+size_t chunk_workspace_bytes(const ScanArgs &a);
+// `workspace` must hold chunk_workspace_bytes(a) bytes, 16-byte aligned;
+// its contents on entry do not matter.
+ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t stream);
+ssd_status_t chunk_read_device_error(cudaStream_t stream, uint32_t *code);
+
+// launch accounting
+void note_launches(int n);
+
+}  // namespace ssd

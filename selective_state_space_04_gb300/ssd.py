@@ -1,0 +1,176 @@
+"""ctypes binding for libssd (argument marshalling only).
+
+Every step of the scan runs in libssd's CUDA kernels.  If the shared library
+has not been built, importing this module raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH
+
+PATH_AUTO = 0
+PATH_SEQUENTIAL = 1
+PATH_CHUNKED = 2
+_PATHS = {"auto": PATH_AUTO, "sequential": PATH_SEQUENTIAL, "seq": PATH_SEQUENTIAL,
+          "chunked": PATH_CHUNKED}
+
+DTYPE_F32 = 0
+DTYPE_BF16 = 1
+
+STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_DIMS", 2: "SSD_ERR_NULL_PTR", 3: "SSD_ERR_MISALIGNED",
+          4: "SSD_ERR_UNSUPPORTED", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_TIMEOUT", 7: "SSD_ERR_ALIASING"}
+
+
+class SsdError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{STATUS.get(status, status)}: {what}")
+
+
+class SsdDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int64), ("seqlen", ctypes.c_int64),
+                ("nheads", ctypes.c_int32), ("headdim", ctypes.c_int32),
+                ("dstate", ctypes.c_int32), ("ngroups", ctypes.c_int32),
+                ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32), ("reserved", ctypes.c_uint32)]
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libssd is not built ({path} missing); run "
+                          "`python -c 'import __graft_entry__ as g; g.build()'`")
+    lib = ctypes.CDLL(path)
+    vp, fp = ctypes.c_void_p, ctypes.c_void_p
+    sig = [vp, fp, fp, fp, vp, vp, fp, fp, vp, fp, ctypes.POINTER(SsdDims), vp]
+    for name in ("ssd_scan_fwd", "ssd_scan_fwd_host"):
+        f = getattr(lib, name)
+        f.restype = ctypes.c_int
+        f.argtypes = sig
+    lib.ssd_select_path.restype = ctypes.c_int32
+    lib.ssd_select_path.argtypes = [ctypes.POINTER(SsdDims)]
+    lib.ssd_launches_per_call.restype = ctypes.c_int32
+    lib.ssd_launches_per_call.argtypes = [ctypes.POINTER(SsdDims)]
+    lib.ssd_launch_count.restype = ctypes.c_uint64
+    lib.ssd_launch_count.argtypes = []
+    lib.ssd_get_device_error.restype = ctypes.c_int
+    lib.ssd_get_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    lib.ssd_status_string.restype = ctypes.c_char_p
+    lib.ssd_status_string.argtypes = [ctypes.c_int32]
+    lib.ssd_abi_version.restype = ctypes.c_int32
+    lib.ssd_abi_version.argtypes = []
+    return lib
+
+
+_lib = load_library()
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype, path="auto") -> SsdDims:
+    d = SsdDims()
+    d.batch, d.seqlen, d.nheads, d.headdim = batch, seqlen, nheads, headdim
+    d.dstate, d.ngroups, d.chunk = dstate, ngroups, chunk
+    d.dtype = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
+    d.flags = _PATHS[path] if isinstance(path, str) else int(path)
+    d.reserved = 0
+    return d
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(status: int, what: str):
+    if status != 0:
+        raise SsdError(status, what)
+
+
+def _dims_from(x, B, chunk, path):
+    Bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    return make_dims(Bt, L, H, P, N, G, chunk, x.dtype, path)
+
+
+def select_path(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+    Bt, L, H, P = x_shape
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    return _lib.ssd_select_path(ctypes.byref(d))
+
+
+def launches_per_call(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+    Bt, L, H, P = x_shape
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    return _lib.ssd_launches_per_call(ctypes.byref(d))
+
+
+def launch_count() -> int:
+    return int(_lib.ssd_launch_count())
+
+
+def device_error(stream=None) -> int:
+    st = torch.cuda.current_stream() if stream is None else stream
+    code = ctypes.c_uint32(0)
+    _check(_lib.ssd_get_device_error(ctypes.c_void_p(st.cuda_stream), ctypes.byref(code)),
+           "ssd_get_device_error")
+    return int(code.value)
+
+
+def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
+                 path="auto", return_final_state=True, y=None, final_state=None, stream=None):
+    """Forward SSD scan on CUDA tensors.  Returns ``(y, final_state)``.
+
+    ``x [B,L,H,P]`` and ``B, C [B,L,G,N]`` share one dtype (bf16 or fp32);
+    ``dt_raw [B,L,H]``, ``dt_bias, A_log, D [H]`` and the states
+    ``[B,H,P,N]`` are fp32.  Work is enqueued on ``stream`` (default: the
+    current torch stream); the call does not synchronise.
+    """
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        Bt, L, H, P = x.shape
+        final_state = torch.empty((Bt, H, P, B.shape[3]), dtype=torch.float32, device=x.device)
+    for name, t in (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log),
+                    ("B", B), ("C", C), ("D", D), ("init_state", init_state), ("y", y),
+                    ("final_state", final_state)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    d = _dims_from(x, B, chunk, path)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    _check(_lib.ssd_scan_fwd(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B), _ptr(C),
+                             _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state),
+                             ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)),
+           "ssd_scan_fwd")
+    return y, final_state
+
+
+def ssd_scan_fwd_host(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
+                      path="auto", return_final_state=True, y=None, final_state=None,
+                      stream=None, device=None):
+    """Same scan on CPU tensors (pinned for asynchronous copies).  The library
+    copies in, runs, copies out and synchronises before returning."""
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        Bt, L, H, P = x.shape
+        final_state = torch.empty((Bt, H, P, B.shape[3]), dtype=torch.float32)
+    for name, t in (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log),
+                    ("B", B), ("C", C), ("D", D), ("init_state", init_state), ("y", y),
+                    ("final_state", final_state)):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CPU tensor")
+    d = _dims_from(x, B, chunk, path)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    with torch.cuda.device(dev):
+        st = torch.cuda.current_stream(dev) if stream is None else stream
+        _check(_lib.ssd_scan_fwd_host(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B),
+                                      _ptr(C), _ptr(D), _ptr(init_state), _ptr(y),
+                                      _ptr(final_state), ctypes.byref(d),
+                                      ctypes.c_void_p(st.cuda_stream)),
+               "ssd_scan_fwd_host")
+    return y, final_state

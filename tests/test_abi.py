@@ -1,0 +1,122 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every symbol
+that include/ssd.h declares, and rejects bad arguments before touching a GPU.
+
+No call here launches a kernel (validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def libssd():
+    from selective_state_space_04_gb300 import build
+    path = build.build()
+    from selective_state_space_04_gb300 import ssd
+    return ssd
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "ssd.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"\b(ssd_[a-z_0-9]+)\s*\(", src)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ssd_scan_fwd", "ssd_scan_fwd_host", "ssd_status_string",
+                     "ssd_get_device_error", "ssd_select_path"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(libssd):
+    lib = libssd.lib()
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} declared in ssd.h but not exported"
+
+
+def test_abi_version_and_status_strings(libssd):
+    lib = libssd.lib()
+    assert lib.ssd_abi_version() == 1
+    for code in range(8):
+        s = lib.ssd_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.ssd_status_string(99) == b"unknown status"
+
+
+def call(libssd, dims, ptrs=None):
+    lib = libssd.lib()
+    p = ptrs or {}
+    fake = ctypes.c_void_p(0x10000)   # aligned, never dereferenced on these paths
+    args = [p.get(k, fake) for k in ("x", "dt_raw", "dt_bias", "A_log", "B", "C", "D")]
+    args += [p.get("init_state", None), p.get("y", ctypes.c_void_p(0x90000000)),
+             p.get("final_state", None)]
+    return lib.ssd_scan_fwd(*args, ctypes.byref(dims) if dims is not None else None, None)
+
+
+def dims(libssd, **kw):
+    base = dict(batch=1, seqlen=8, nheads=2, headdim=8, dstate=16, ngroups=1, chunk=16,
+                dtype="bf16", path="auto")
+    base.update(kw)
+    return libssd.make_dims(**base)
+
+
+@pytest.mark.parametrize("kw", [dict(nheads=3, ngroups=2), dict(nheads=0), dict(headdim=0),
+                                dict(dstate=0), dict(ngroups=0), dict(chunk=0), dict(batch=-1),
+                                dict(seqlen=-5), dict(path=7)])
+def test_invalid_dims_rejected(libssd, kw):
+    assert call(libssd, dims(libssd, **kw)) == 1
+
+
+def test_reserved_must_be_zero(libssd):
+    d = dims(libssd)
+    d.reserved = 1
+    assert call(libssd, d) == 1
+
+
+def test_null_dims_and_pointers(libssd):
+    assert call(libssd, None) == 2
+    assert call(libssd, dims(libssd), {"x": None}) == 2
+    assert call(libssd, dims(libssd), {"y": None}) == 2
+
+
+def test_misaligned_pointer(libssd):
+    assert call(libssd, dims(libssd), {"x": ctypes.c_void_p(0x10002)}) == 3
+
+
+def test_output_aliasing_input(libssd):
+    d = dims(libssd)
+    assert call(libssd, d, {"x": ctypes.c_void_p(0x90000000), "y": ctypes.c_void_p(0x90000000)}) == 7
+    # final_state overlapping B
+    assert call(libssd, d, {"B": ctypes.c_void_p(0xA0000000),
+                            "final_state": ctypes.c_void_p(0xA0000000)}) == 7
+
+
+def test_chunked_path_needs_bf16_64_128(libssd):
+    lib = libssd.lib()
+    d = dims(libssd, dtype="f32", path="chunked", headdim=64, dstate=128, chunk=256)
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    d = dims(libssd, path="chunked", headdim=32, dstate=128, chunk=256)
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    d = dims(libssd, path="chunked", headdim=64, dstate=128, chunk=100)
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    d = dims(libssd, path="chunked", nheads=3, ngroups=1, headdim=64, dstate=128, chunk=256)
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+
+
+def test_sequential_path_limits(libssd):
+    lib = libssd.lib()
+    assert lib.ssd_select_path(ctypes.byref(dims(libssd, path="sequential"))) == 1
+    assert lib.ssd_select_path(ctypes.byref(dims(libssd, path="sequential", headdim=1024))) == -4
+
+
+def test_empty_work_launches_nothing(libssd):
+    lib = libssd.lib()
+    assert lib.ssd_launches_per_call(ctypes.byref(dims(libssd, batch=0))) == 0
+    assert lib.ssd_launches_per_call(ctypes.byref(dims(libssd, seqlen=0))) == 0
+    # batch == 0 is a no-op that returns OK without any device access
+    assert call(libssd, dims(libssd, batch=0)) == 0

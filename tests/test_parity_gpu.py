@@ -1,0 +1,265 @@
+"""GPU parity: libssd (through the C ABI) against the fp64 oracle.
+
+Metric (the method's stated bar): max|y - y_ref| / max|y_ref| over the whole
+output, applied to y and to the final state separately; <= 2e-2 for bf16
+inputs with fp32 accumulation, <= 1e-4 for the fp32 path.
+
+Small cases (oracle in seconds) are compared element by element; they span
+several 128-step sub-chunks, several chunks and a ragged tail.  Full-size
+workloads are run in the launch configuration the benchmark times and
+compared on sampled (batch, head) chains that the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from selective_state_space_04_gb300.inputs import WORKLOADS, Workload, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd as mod
+    return mod
+
+
+def to_dev(inp):
+    return {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
+
+
+def run(ssd, inp, w, path="auto", chunk=None, init=True):
+    d = to_dev(inp)
+    y, fin = ssd.ssd_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
+                              d["init_state"] if init else None, chunk=chunk or w.chunk, path=path)
+    torch.cuda.synchronize()
+    assert ssd.device_error() == 0
+    return y, fin
+
+
+def relerr(a, ref):
+    a = a.double().cpu().numpy() if hasattr(a, "cpu") else a
+    return float(np.max(np.abs(a - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def check(y, fin, ref_y, ref_fin, dtype):
+    ey, ef = relerr(y, ref_y), relerr(fin, ref_fin)
+    assert ey <= TOL[dtype], f"y rel err {ey:.3e} > {TOL[dtype]}"
+    assert ef <= TOL[dtype], f"final state rel err {ef:.3e} > {TOL[dtype]}"
+    return ey, ef
+
+
+def small(**kw):
+    base = dict(name="t", batch=2, seqlen=640, nheads=4, headdim=64, dstate=128, ngroups=1,
+                chunk=256, dtype="bf16", init_state=True)
+    base.update(kw)
+    return Workload(**base)
+
+
+# ----------------------------------------------------------- small, exact
+def test_tiny_fp32_sequential(ssd):
+    w = WORKLOADS["tiny_fp32"]
+    inp = make_inputs(w, seed=0)
+    ref = oracle.ssd_fwd(**inp)
+    assert ssd.select_path((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups, w.dstate,
+                           w.chunk, "f32") == ssd.PATH_SEQUENTIAL
+    y, fin = run(ssd, inp, w)
+    check(y, fin, *ref, "f32")
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 2, 8, 16, 1), (2, 37, 4, 8, 16, 2), (1, 200, 3, 5, 7, 1),
+                                   (2, 130, 4, 64, 128, 1), (1, 70, 2, 32, 256, 2)])
+def test_sequential_fp32_shapes(ssd, shape):
+    Bt, L, H, P, N, G = shape
+    w = small(batch=Bt, seqlen=L, nheads=H, headdim=P, dstate=N, ngroups=G, chunk=16, dtype="f32")
+    inp = make_inputs(w, seed=1)
+    y, fin = run(ssd, inp, w, path="sequential")
+    check(y, fin, *oracle.ssd_fwd(**inp), "f32")
+
+
+def test_sequential_bf16(ssd):
+    w = small(seqlen=300)
+    inp = make_inputs(w, seed=2)
+    y, fin = run(ssd, inp, w, path="sequential")
+    check(y, fin, *oracle.ssd_fwd(**inp), "bf16")
+
+
+@pytest.mark.parametrize("init", [False, True])
+def test_chunked_small(ssd, init):
+    w = small(init_state=init)
+    inp = make_inputs(w, seed=3)
+    assert ssd.select_path((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups, w.dstate,
+                           w.chunk) == ssd.PATH_CHUNKED
+    y, fin = run(ssd, inp, w, path="chunked")
+    check(y, fin, *oracle.ssd_fwd(**inp), "bf16")
+
+
+@pytest.mark.parametrize("chunk", [64, 128, 192, 256, 512])
+def test_chunked_chunk_lengths_ragged(ssd, chunk):
+    w = small(seqlen=700, chunk=chunk)
+    inp = make_inputs(w, seed=4)
+    y, fin = run(ssd, inp, w, path="chunked")
+    check(y, fin, *oracle.ssd_fwd(**inp), "bf16")
+
+
+@pytest.mark.parametrize("L", [1, 2, 63, 127, 128, 129, 255, 257])
+def test_chunked_short_and_boundary_lengths(ssd, L):
+    w = small(seqlen=L, batch=1, nheads=2)
+    inp = make_inputs(w, seed=5)
+    y, fin = run(ssd, inp, w, path="chunked")
+    check(y, fin, *oracle.ssd_fwd(**inp), "bf16")
+
+
+@pytest.mark.parametrize("H,G", [(8, 2), (8, 4), (16, 8), (6, 3)])
+def test_chunked_groups(ssd, H, G):
+    w = small(nheads=H, ngroups=G, seqlen=384)
+    inp = make_inputs(w, seed=6)
+    y, fin = run(ssd, inp, w, path="chunked")
+    check(y, fin, *oracle.ssd_fwd(**inp), "bf16")
+
+
+def test_many_short_sequences_reduced(ssd):
+    w = WORKLOADS["many_short_seqs"].with_(batch=16, nheads=8)
+    inp = make_inputs(w, seed=7)
+    ref = oracle.ssd_fwd(**inp)
+    for path in ("chunked", "sequential"):
+        y, fin = run(ssd, inp, w, path=path)
+        check(y, fin, *ref, "bf16")
+
+
+def test_paths_agree(ssd):
+    w = small(seqlen=520)
+    inp = make_inputs(w, seed=8)
+    y1, f1 = run(ssd, inp, w, path="chunked")
+    y2, f2 = run(ssd, inp, w, path="sequential")
+    ref = oracle.ssd_fwd(**inp)
+    check(y1, f1, *ref, "bf16")
+    check(y2, f2, *ref, "bf16")
+    assert relerr(y1, y2.double().cpu().numpy()) < 2e-2
+
+
+def test_chunk_length_invariance(ssd):
+    w = small(seqlen=1024, init_state=True)
+    inp = make_inputs(w, seed=9)
+    outs = [run(ssd, inp, w, path="chunked", chunk=q) for q in (64, 128, 256, 512, 1024)]
+    y0 = outs[0][0].double().cpu().numpy()
+    f0 = outs[0][1].double().cpu().numpy()
+    for y, f in outs[1:]:
+        assert relerr(y, y0) < 1e-2
+        assert relerr(f, f0) < 1e-2
+
+
+def test_split_and_resume(ssd):
+    w = small(seqlen=768)
+    inp = make_inputs(w, seed=10)
+    y, fin = run(ssd, inp, w, path="chunked")
+    L1 = 256
+    first = dict(inp)
+    second = dict(inp)
+    for k in ("x", "dt_raw", "B", "C"):
+        first[k] = inp[k][:, :L1].contiguous()
+        second[k] = inp[k][:, L1:].contiguous()
+    y1, f1 = run(ssd, first, w.with_(seqlen=L1), path="chunked")
+    second["init_state"] = f1.cpu()
+    y2, f2 = run(ssd, second, w.with_(seqlen=w.seqlen - L1), path="chunked")
+    ycat = torch.cat([y1, y2], dim=1)
+    assert relerr(ycat, y.double().cpu().numpy()) < 1e-2
+    assert relerr(f2, fin.double().cpu().numpy()) < 1e-2
+
+
+def test_deterministic_bitwise(ssd):
+    w = small(seqlen=900)
+    inp = make_inputs(w, seed=11)
+    for path in ("chunked", "sequential"):
+        a = run(ssd, inp, w, path=path)
+        b = run(ssd, inp, w, path=path)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_in_place_state_update(ssd):
+    w = small(seqlen=400)
+    inp = make_inputs(w, seed=12)
+    d = to_dev(inp)
+    state = d["init_state"].clone()
+    y, _ = ssd.ssd_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
+                            state, chunk=256, path="chunked", final_state=state)
+    torch.cuda.synchronize()
+    ry, rf = oracle.ssd_fwd(**inp)
+    check(y, state, ry, rf, "bf16")
+
+
+def test_host_entry_point_matches_device(ssd):
+    w = small(seqlen=333)
+    inp = make_inputs(w, seed=13)
+    yd, fd = run(ssd, inp, w)
+    pinned = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
+    yh, fh = ssd.ssd_scan_fwd_host(pinned["x"], pinned["dt_raw"], pinned["dt_bias"], pinned["A_log"],
+                                   pinned["B"], pinned["C"], pinned["D"], pinned["init_state"],
+                                   chunk=w.chunk)
+    assert torch.equal(yh, yd.cpu()) and torch.equal(fh, fd.cpu())
+
+
+def test_empty_batch_and_sequence(ssd):
+    w = small(batch=0)
+    inp = make_inputs(w, seed=14)
+    y, fin = run(ssd, inp, w)
+    assert y.numel() == 0
+    w = small(seqlen=0)
+    inp = make_inputs(w, seed=15)
+    y, fin = run(ssd, inp, w)
+    assert torch.equal(fin.cpu(), inp["init_state"])
+    y, fin = run(ssd, inp, w, init=False)
+    assert torch.count_nonzero(fin).item() == 0
+
+
+def test_rejects_wrong_dtype_for_chunked(ssd):
+    w = small(dtype="f32")
+    inp = make_inputs(w, seed=16)
+    with pytest.raises(ssd.SsdError) as ei:
+        run(ssd, inp, w, path="chunked")
+    assert ei.value.status == 4
+
+
+# --------------------------------------------- full size, sampled chains
+def sample_pairs(w, n, seed):
+    rng = np.random.default_rng(seed)
+    pairs = {(0, 0), (w.batch - 1, w.nheads - 1)}
+    while len(pairs) < min(n, w.batch * w.nheads):
+        pairs.add((int(rng.integers(w.batch)), int(rng.integers(w.nheads))))
+    return sorted(pairs)
+
+
+def oracle_pair(inp, w, b, h):
+    g = h // (w.nheads // w.ngroups)
+    sl = dict(x=inp["x"][b:b + 1, :, h:h + 1], dt_raw=inp["dt_raw"][b:b + 1, :, h:h + 1],
+              dt_bias=inp["dt_bias"][h:h + 1], A_log=inp["A_log"][h:h + 1],
+              B=inp["B"][b:b + 1, :, g:g + 1], C=inp["C"][b:b + 1, :, g:g + 1], D=inp["D"][h:h + 1],
+              init_state=None if inp["init_state"] is None else inp["init_state"][b:b + 1, h:h + 1])
+    y, f = oracle.ssd_fwd(**sl)
+    return y[0, :, 0], f[0, 0]
+
+
+@pytest.mark.parametrize("name,npairs", [("mamba2_130m_layer", 6), ("mamba2_2p7b_layer", 6),
+                                         ("long_context_64k", 3), ("many_short_seqs", 40)])
+def test_full_size_workloads_sampled(ssd, name, npairs):
+    w = WORKLOADS[name]
+    inp = make_inputs(w, seed=0)
+    y, fin = run(ssd, inp, w)       # auto path, as the benchmark runs it
+    assert torch.isfinite(y.float()).all() and torch.isfinite(fin).all()
+    yc, fc = y.cpu(), fin.cpu()
+    num_y = den_y = num_f = den_f = 0.0
+    for b, h in sample_pairs(w, npairs, seed=1):
+        ry, rf = oracle_pair(inp, w, b, h)
+        num_y = max(num_y, float(np.max(np.abs(yc[b, :, h].double().numpy() - ry))))
+        den_y = max(den_y, float(np.max(np.abs(ry))))
+        num_f = max(num_f, float(np.max(np.abs(fc[b, h].double().numpy() - rf))))
+        den_f = max(den_f, float(np.max(np.abs(rf))))
+    assert num_y / den_y <= TOL["bf16"], f"{name}: y rel err {num_y / den_y:.3e}"
+    assert num_f / den_f <= TOL["bf16"], f"{name}: final rel err {num_f / den_f:.3e}"
