@@ -1,0 +1,423 @@
+#!/usr/bin/env python3
+"""Benchmark of the forward SSD scan (libssd) on GB300.
+
+Prints one JSON line.  Metric: SSD scan forward tokens*heads per second on
+one GPU (B*L*H / time), with the achieved fraction of the HBM roofline of the
+dominant kernel.  A step is one full forward scan (all steps of the method)
+over one batch of synthetic input that is already resident in HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the fp64 CPU oracle on host cores
+
+Under torchrun (N > 1) every rank runs its own copy of the workload on its own
+GPU (the scan shards over batch rows and heads with no exchange, so this is
+weak scaling); the step time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_04_gb300.inputs import WORKLOADS, Workload, make_inputs  # noqa: E402
+
+METRIC = "SSD scan fwd tokens·heads/s at 1 GB300; % of HBM/tensor roofline"
+UNIT = "tokens·heads/s"
+DEFAULT_WORKLOAD = "mamba2_2p7b_layer"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ accounting
+def algorithmic_bytes(w: Workload, final_state: bool = True) -> int:
+    """Bytes a scan must move at least once: read x, dt_raw, B, C, the three
+    per-head parameter vectors and the initial state (when given); write y
+    and the final state.  Chunk states and scratch are not counted."""
+    es = 2 if w.dtype == "bf16" else 4
+    BL = w.batch * w.seqlen
+    x = BL * w.nheads * w.headdim * es
+    dt = BL * w.nheads * 4
+    bc = 2 * BL * w.ngroups * w.dstate * es
+    par = 3 * w.nheads * 4
+    state = w.batch * w.nheads * w.headdim * w.dstate * 4
+    return x + dt + bc + par + (state if w.init_state else 0) + x + (state if final_state else 0)
+
+
+def algorithmic_flops(w: Workload) -> int:
+    """Tensor FLOPs of the chunked method at its stated chunk length Q:
+    causal C B^T per (chunk, group), causal masked M x, chunk state and C P
+    per (chunk, head), state passing per (chunk, head)."""
+    Q, N, P = w.chunk, w.dstate, w.headdim
+    nc = -(-w.seqlen // Q)
+    tri = Q * (Q + 1) // 2
+    per_cg = 2 * tri * N
+    per_ch = 2 * tri * P + 2 * Q * N * P + 2 * Q * N * P + 2 * N * P
+    return w.batch * nc * (w.ngroups * per_cg + w.nheads * per_ch)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_digest() -> str:
+    """Digest of the kernel sources, to tell whether stored ncu counters still
+    describe the kernel that runs."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "selective_state_space_04_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def stored_traffic(workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(workload)
+    if not e or e.get("source_digest") != source_digest():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ clocks
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.thread:
+                self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def init_dist(world: int, backend: str):
+    if world <= 1:
+        return None
+    import torch.distributed as dist
+    if not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+def cpu_oracle_sample(w: Workload, inp: dict, budget_pairs: int | None = None):
+    """Times the fp64 oracle on a bounded sample of the workload: the first
+    `budget_pairs` (batch, head) chains, full sequence length each.  Returns
+    (tokens*heads per second, cores, description)."""
+    import oracle
+    H = w.nheads
+    if budget_pairs is None:
+        # about 10-30 s of host work: roughly 4*N*P flop per token*head in fp64
+        per_pair = 4.0 * w.dstate * w.headdim * w.seqlen
+        cores = oracle.max_threads()
+        budget_pairs = int(max(1, min(w.batch * H, cores * 2.5e9 * 4 / per_pair)))
+    b_rows = -(-budget_pairs // H)
+    nb = min(w.batch, b_rows)
+    sl = {k: (v[:nb] if (v is not None and k in ("x", "dt_raw", "B", "C", "init_state")) else v)
+          for k, v in inp.items()}
+    f64 = {k: (None if v is None else v.double().numpy()) for k, v in sl.items()}
+    t0 = time.perf_counter()
+    oracle.ssd_fwd(**f64)
+    dt = time.perf_counter() - t0
+    th = nb * w.seqlen * H
+    return th / dt, oracle.max_threads(), f"{nb} of {w.batch} batch rows x all {H} heads x L={w.seqlen} ({th} token*heads) in {dt:.2f} s"
+
+
+# ------------------------------------------------------------ GPU arm
+def run_gpu(args, w: Workload):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd
+
+    inp = make_inputs(w, seed=args.seed + rank)
+    d = {k: (None if v is None else v.to(dev)) for k, v in inp.items()}
+    y = torch.empty_like(d["x"])
+    fin = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    path = ssd.select_path((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups, w.dstate, w.chunk,
+                           w.dtype, args.path)
+    if path < 0:
+        raise SystemExit(f"workload {w.name} not supported: status {-path}")
+
+    def step():
+        ssd.ssd_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
+                         d["init_state"], chunk=w.chunk, path=args.path, y=y, final_state=fin,
+                         stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if ssd.device_error() != 0:
+        raise SystemExit("device error during warm-up")
+
+    # timed region: K back-to-back steps, per-step CUDA events on the launching stream
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    launches0 = ssd.launch_count()
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+    launches = ssd.launch_count() - launches0
+    if ssd.device_error() != 0:
+        raise SystemExit("device error during the timed region")
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    total_ms = max_over_ranks(dist, total_ms, dev)
+    ms_per_step = total_ms / args.steps
+    th = w.token_heads
+    value = world * th * args.steps / (total_ms / 1e3)
+
+    # end-to-end through the host-buffer entry point: pinned inputs in, y and
+    # final state out, every step
+    pin = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
+    yh = torch.empty_like(pin["x"]).pin_memory()
+    fh = torch.empty(tuple(fin.shape), dtype=torch.float32).pin_memory()
+
+    def step_host():
+        ssd.ssd_scan_fwd_host(pin["x"], pin["dt_raw"], pin["dt_bias"], pin["A_log"], pin["B"],
+                              pin["C"], pin["D"], pin["init_state"], chunk=w.chunk, path=args.path,
+                              y=yh, final_state=fh, stream=stream)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    step_host()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_host()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev)
+    h2d = sum(v.numel() * v.element_size() for v in pin.values() if v is not None)
+    d2h = yh.numel() * yh.element_size() + fh.numel() * fh.element_size()
+    e2e_value = world * th * e2e_steps / e2e_s
+
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    alg_bytes = algorithmic_bytes(w, final_state=True)
+    alg_flops = algorithmic_flops(w)
+    avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved_gbs = alg_bytes / avg_launch_s / 1e9
+    t_hbm = alg_bytes / (hbm_peak * 1e9)
+    t_tensor = alg_flops / (float(peaks["bf16_tflops"]) * 1e12)
+    traffic = stored_traffic(w.name)
+    kernel = "ssd_chunk_fused_kernel" if path == ssd.PATH_CHUNKED else "ssd_seq_kernel"
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "chunk": w.chunk, "init_state": w.init_state, "final_state": True,
+                   "path": "chunked" if path == ssd.PATH_CHUNKED else "sequential",
+                   "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "roofline": {
+            "bound": "hbm" if t_hbm >= t_tensor else "tensor",
+            "kernel": kernel,
+            "achieved": achieved_gbs,
+            "peak": hbm_peak,
+            "unit": "GB/s",
+            "frac": achieved_gbs / hbm_peak,
+            "peak_source": peak_src,
+            "traffic": traffic,
+            "algorithmic_bytes_per_launch": alg_bytes,
+            "algorithmic_tensor_flops_per_launch": alg_flops,
+            "avg_launch_ms": avg_launch_s * 1e3,
+            "roofline_ms": max(t_hbm, t_tensor) * 1e3,
+            "frac_of_nominal_8TBs": alg_bytes / avg_launch_s / 8.0e12,
+        },
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "ssd_scan_fwd_host (pinned host buffers)"},
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, cores, sample = cpu_oracle_sample(w, inp)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------ reference arm
+def run_reference(args, w: Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    inp = make_inputs(w, seed=args.seed)
+    cores = oracle.max_threads()
+    per_pair = 4.0 * w.dstate * w.headdim * w.seqlen
+    # each step: a bounded sample sized for ~5 s of host work
+    pairs = int(max(1, min(w.batch * w.nheads, cores * 2.5e9 * 2 / per_pair)))
+    for _ in range(args.warmup):
+        cpu_oracle_sample(w, inp, budget_pairs=pairs)
+    times, th_total, sample = 0.0, 0, ""
+    for _ in range(args.steps):
+        v, cores, sample = cpu_oracle_sample(w, inp, budget_pairs=pairs)
+        nb = min(w.batch, -(-pairs // w.nheads))
+        th = nb * w.seqlen * w.nheads
+        times += th / v
+        th_total += th
+    value = th_total / times
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": UNIT,
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": times / args.steps * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "chunk": w.chunk, "init_state": w.init_state, "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": "per step: " + sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="libssd", choices=["libssd", "reference"])
+    ap.add_argument("--path", default="auto", choices=["auto", "chunked", "sequential"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()
