@@ -1,13 +1,15 @@
 // ssd_chunk.cu -- chunked SSD forward scan on the sm_103a tensor cores.
 //
-// One persistent kernel evaluates the whole scan.  Work unit = (chunk c,
-// batch row b, pair of heads h0, h0+1 of one group).  Units are ordered
-// chunk-major, so the CTAs running at any moment work on the same chunk of
-// many head pairs (the group's B/C tiles are shared through L2), and the unit
-// that needs the state left by chunk c-1 of its chain was scheduled about one
-// round of the grid earlier.
+// One persistent cooperative kernel evaluates the whole scan.  A work unit is
+// a range of R consecutive chunks (R*Q steps) of one chain, a chain being a
+// batch row b and a pair of heads h0, h0+1 of one group.  Units are ordered
+// range-major (all chains' first ranges, then all second ranges, ...): the
+// CTAs running at any moment share the group's B/C tiles through L2, and the
+// unit that needs the state left by the previous range of its chain was
+// scheduled about one grid round earlier.  R is chosen on the host to balance
+// the grid against the cost of handing a state from unit to unit.
 //
-// Inside a unit the chunk is walked in sub-chunks of T = 128 steps.  For a
+// Inside a unit the steps are walked in sub-chunks of T = 128.  For a
 // sub-chunk with carried-in state P (N x P per head) and the sub-chunk-local
 // inclusive cumulative sum cs_t = sum_{k<=t} dt_k A:
 //
@@ -16,26 +18,26 @@
 //   y_t    = (M x)_t + exp(cs_t) (C P)_t
 //   P     <- exp(cs_{T-1}) P + B^T (w o x),   w_s = exp(cs_{T-1} - cs_s) dt_s
 //
-// This is the quadratic ("dual") form inside the sub-chunk and the linear
-// recurrence between sub-chunks; chunk boundaries are where the state is
-// handed from one unit to the next through global memory.  Source: the SSD
-// module of @seanhogg/builderforce-memory-engine 2026.6.18 (chunked evaluation
-// with a carried state) and the chunked-scan pipeline of mamba-rs 0.2.1
+// This is the quadratic ("dual") form inside a sub-chunk and the linear
+// recurrence between sub-chunks and chunks.  Source: the SSD module of
+// @seanhogg/builderforce-memory-engine 2026.6.18 (chunked evaluation with a
+// carried state) and the chunked-scan pipeline of mamba-rs 0.2.1
 // mamba3_siso/gpu/mamba3_gpu.rs (decay cumsum, chunk state, state passing,
 // chunk scan), applied to the Mamba-2 recurrence.
 //
-// Roles (10 warps):
-//   warps 0-7  "math": cumulative sums and decay factors, the masked decay
-//              matrix M (written to tensor memory as a bf16 MMA operand), the
-//              w-scaling of x, the state rescale, the output epilogue and the
-//              state handoff.
-//   warp 8     TMA producer: B/C tiles (2 stages) and x tiles (2 stages).
-//   warp 9     tcgen05 MMA issuer (one lane) and TMEM owner.
+// Roles (18 warps):
+//   warps 0-7   decay group: dt, cumulative sums and decay factors; the masked
+//               decay matrix M, built in tensor memory as a bf16 MMA operand
+//   warps 8-15  state group: w-scaling of x, state rescale, output epilogue,
+//               state handoff between units
+//   warp 16     TMA producer: B/C tiles (2 stages), x tiles (2 stages)
+//   warp 17     tcgen05 MMA issuer (one lane) and TMEM owner
+// The decay group prepares sub-chunk j+1 while the state group finishes j.
 // Tensor memory (512 columns x 128 lanes, fp32):
-//   [  0,128)  Y_diag = M x            lanes t, columns (head, p)
-//   [128,256)  S = C B^T, then Y_off = C P   (lanes t)
-//   [256,384)  M for both heads (bf16 pairs, MMA A operand)
-//   [384,512)  P, the carried state, fp32    lanes n, columns (head, p)
+//   [  0,128)  Y_diag = M x            lanes t, columns head*64 + p
+//   [128,256)  Y_off  = C P            lanes t, columns head*64 + p
+//   [256,384)  S = C B^T, then in place M of both heads (bf16 pairs)
+//   [384,512)  P, the carried state    lanes n, columns head*64 + p
 // Every wait is bounded (about 2 s); on expiry the kernel records
 // SSD_ERR_TIMEOUT, stops issuing work, drains its own copies and MMAs, frees
 // tensor memory and returns.
@@ -62,11 +64,11 @@ using namespace ssd::ptx;
 constexpr int kT = 128;          // sub-chunk length (MMA M)
 constexpr int kP = 64;           // head dimension
 constexpr int kN = 128;          // state size
-constexpr int kMathWarps = 8;
-constexpr int kMathThreads = kMathWarps * 32;
-constexpr int kProducerWarp = 8;
-constexpr int kMmaWarp = 9;
-constexpr int kThreads = 320;
+constexpr int kGroupWarps = 8;   // warps per math group
+constexpr int kStateWarp0 = 8;   // first warp of the state group
+constexpr int kProducerWarp = 16;
+constexpr int kMmaWarp = 17;
+constexpr int kThreads = 18 * 32;
 
 constexpr uint32_t kTileBytes = 16384;              // 128 rows x 128 bytes
 constexpr uint32_t kBCStageBytes = 4 * kTileBytes;  // C lo/hi, B lo/hi
@@ -75,16 +77,23 @@ constexpr uint32_t kXStageBytes = 2 * kTileBytes;   // x of two heads
 // dynamic shared memory layout (offsets from a 1024-aligned base)
 constexpr uint32_t kOffBC = 0;
 constexpr uint32_t kOffX = kOffBC + 2 * kBCStageBytes;
-constexpr uint32_t kOffSmall = kOffX + 2 * kXStageBytes;
-constexpr uint32_t kSmallFloats = 2 /*parity*/ * 2 /*head*/ * kT * 3 /*cs2, dt, colf*/;
-constexpr uint32_t kOffWsum = kOffSmall + kSmallFloats * 4;
-constexpr uint32_t kOffBars = kOffWsum + 64;
+// decay arrays, 3 buffers (sub-chunk j uses buffer j % 3), each:
+//   cs2 [2][T], dt [2][T], colf [2][T], ecs [2][T], wsc [2][T], dtot [2] (+pad)
+constexpr int kDecayFloats = 5 * 2 * kT + 4;
+constexpr uint32_t kOffDecay = kOffX + 2 * kXStageBytes;
+constexpr uint32_t kOffWsum = kOffDecay + 3 * kDecayFloats * 4;
+constexpr int kMaxHeads = 512;                       // per-head parameters staged in shared memory
+constexpr uint32_t kOffHead = kOffWsum + 64;          // A*log2(e), dt_bias, D  (3 x kMaxHeads floats)
+constexpr uint32_t kOffBars = kOffHead + 3 * kMaxHeads * 4;
 constexpr int kNumBars = 20;
 constexpr uint32_t kOffTmemHolder = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemHolder + 16 + 1024;  // + alignment slack
 
-// tensor memory columns
-constexpr uint32_t kColYd = 0, kColSY = 128, kColM = 256, kColP = 384;
+// tensor memory columns (128 lanes each)
+//   SM: S = C B^T (fp32, column s), then, in place, M of both heads as bf16
+//       pairs: for each 16-step group s0, columns s0 + 8*head + c hold
+//       s = s0 + 2c, s0 + 2c + 1 (so M is built group by group in place)
+constexpr uint32_t kColYd = 0, kColYo = 128, kColSM = 256, kColP = 384;
 
 // barrier indices
 enum {
@@ -101,7 +110,7 @@ enum {
     BAR_PB_READY,
     BAR_EPI_DONE,
     BAR_DRAIN,
-    BAR_MSYNC,   // math-warp group barrier (bounded, unlike bar.sync)
+    BAR_MSYNC,   // decay-group barrier (bounded, unlike bar.sync)
 };
 
 struct ChunkParams {
@@ -109,16 +118,17 @@ struct ChunkParams {
     const float *dt_bias;
     const float *A_log;
     const float *D;
-    const float *init_state;          // may be null
+    const float *init_state;          // [B,H,P,N] or null
     __nv_bfloat16 *y;
-    float *slot;                      // [B, H, P, N] fp32: handoff states, final state
-    unsigned long long *flags;        // [nunits]
+    float *final_state;               // [B,H,P,N] or null
+    float *slots;                     // [chains][N][2P] handoff states (null if one unit per chain)
+    unsigned long long *flags;        // [nunits][state-group warps]: warp w of a unit publishes its rows
     unsigned long long *abort_word;
     unsigned long long epoch;
     unsigned long long timeout_ns;
     long long L;
     long long nunits;
-    int H, Q, nchunks, nhp, nchains, hpg;
+    int H, span, nranges, nhp, nchains, hpg;   // span = steps per unit (R*Q)
 };
 
 struct Maps {
@@ -154,30 +164,38 @@ __device__ __forceinline__ bool aborted(const ChunkParams &p)
     return *reinterpret_cast<volatile unsigned long long *>(p.abort_word) == p.epoch;
 }
 
-// Bounded wait for the phase of `bar` with the given parity.
+// Bounded wait for the phase of `bar` with the given parity.  Each probe
+// suspends the thread for up to 1 ms (it resumes as soon as the phase
+// completes), so waiting warps do not take issue slots from working ones.
 __device__ bool wait_bar(uint64_t *bar, uint32_t parity, const ChunkParams &p)
 {
-    if (mbar_test(bar, parity))
+    if (mbar_wait_for(bar, parity, 1000000u))
         return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_test(bar, parity))
+    for (;;) {
+        if (mbar_wait_for(bar, parity, 1000000u))
             return true;
-        if ((it & 255u) == 0) {
-            if (aborted(p))
-                return false;
-            if (globaltimer_ns() - t0 > p.timeout_ns) {
-                raise_timeout(p);
-                return false;
-            }
+        if (aborted(p))
+            return false;
+        if (globaltimer_ns() - t0 > p.timeout_ns) {
+            raise_timeout(p);
+            return false;
         }
     }
 }
 
-// Group barrier of the math warps on an mbarrier, so that it is bounded too.
-__device__ __forceinline__ bool math_sync(uint64_t *bar, uint32_t &phase, const ChunkParams &p)
+// One arrival per warp (lane 0, after the warp's own writes are ordered).
+__device__ __forceinline__ void warp_arrive(uint64_t *bar)
 {
-    mbar_arrive(bar);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(bar);
+}
+
+// Group barrier of the decay warps on an mbarrier, so that it is bounded too.
+__device__ __forceinline__ bool group_sync(uint64_t *bar, uint32_t &phase, const ChunkParams &p)
+{
+    warp_arrive(bar);
     const bool ok = wait_bar(bar, phase, p);
     phase ^= 1u;
     return ok;
@@ -190,7 +208,7 @@ __device__ bool wait_flag(const unsigned long long *flag, const ChunkParams &p)
         return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        __nanosleep(64);
+        __nanosleep(128);
         if (ld_acquire_u64(flag) == p.epoch)
             return true;
         if ((it & 63u) == 0) {
@@ -205,23 +223,57 @@ __device__ bool wait_flag(const unsigned long long *flag, const ChunkParams &p)
 }
 
 struct Unit {
-    int c, b, h0, g, nsub, clen;
-    long long cstart;
+    int rg, b, hp, h0, g, nsub, len;   // rg: index of the unit's step range in its chain
+    long long start;                   // first step
 };
 
 __device__ __forceinline__ Unit decode_unit(long long u, const ChunkParams &p)
 {
     Unit w;
-    w.c = (int)(u / p.nchains);
-    const int chain = (int)(u - (long long)w.c * p.nchains);
+    w.rg = (int)(u / p.nchains);
+    const int chain = (int)(u - (long long)w.rg * p.nchains);
     w.b = chain / p.nhp;
-    const int hp = chain - w.b * p.nhp;
-    w.h0 = 2 * hp;
+    w.hp = chain - w.b * p.nhp;
+    w.h0 = 2 * w.hp;
     w.g = w.h0 / p.hpg;
-    w.cstart = (long long)w.c * p.Q;
-    w.clen = (int)min((long long)p.Q, p.L - w.cstart);
-    w.nsub = (w.clen + kT - 1) / kT;
+    w.start = (long long)w.rg * p.span;
+    w.len = (int)min((long long)p.span, p.L - w.start);
+    w.nsub = (w.len + kT - 1) / kT;
     return w;
+}
+
+// Position in this CTA's sequence of sub-chunks: units blockIdx.x,
+// blockIdx.x + gridDim.x, ... each walked in sub-chunks of kT steps.
+struct Cursor {
+    long long u;
+    int k;
+    Unit w;
+    __device__ __forceinline__ int valid() const { return min(kT, w.len - k * kT); }
+    __device__ __forceinline__ long long t0() const { return w.start + (long long)k * kT; }
+};
+
+__device__ __forceinline__ bool cursor_first(Cursor &c, const ChunkParams &p)
+{
+    c.u = blockIdx.x;
+    c.k = 0;
+    if (c.u >= p.nunits)
+        return false;
+    c.w = decode_unit(c.u, p);
+    return true;
+}
+
+__device__ __forceinline__ bool cursor_next(Cursor &c, const ChunkParams &p)
+{
+    if (c.k + 1 < c.w.nsub) {
+        ++c.k;
+        return true;
+    }
+    c.u += gridDim.x;
+    c.k = 0;
+    if (c.u >= p.nunits)
+        return false;
+    c.w = decode_unit(c.u, p);
+    return true;
 }
 
 __device__ __forceinline__ float softplus_f32(float z)
@@ -235,6 +287,81 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }
 
+__device__ __forceinline__ uint4 pack8(const uint32_t *v)
+{
+    uint4 o;
+    o.x = pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1]));
+    o.y = pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3]));
+    o.z = pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5]));
+    o.w = pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7]));
+    return o;
+}
+
+// One 16-column group of M for both heads, from S values sv[0..15]
+// (columns s = s0 .. s0+15 of row r; s0 is a multiple of 16).  Writes 8
+// packed bf16 pairs per head.  Decay exp(cs_t - cs_s) dt_s for s <= t:
+//   * s in an earlier 32-step block than t: the row factor exp(cs_t - cs_e)
+//     times the column factor exp(cs_e - cs_s) dt_s (e = end of s's block),
+//     both <= 1;
+//   * s in t's own 32-step block: evaluated directly;
+// and D_h is added on the diagonal.
+__device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8],
+                                            int s0, int r, const float *cs2, const float *dtv,
+                                            const float *colf, float D0, float D1)
+{
+    const int J = s0 >> 5, rb = r >> 5;
+    if (J > rb) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            m0[i] = 0u;
+            m1[i] = 0u;
+        }
+    } else if (J < rb) {
+        const float rf0 = ex2_approx(cs2[r] - cs2[J * 32 + 31]);
+        const float rf1 = ex2_approx(cs2[kT + r] - cs2[kT + J * 32 + 31]);
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int s = s0 + 4 * i4;
+            const float4 c0 = *reinterpret_cast<const float4 *>(colf + s);
+            const float4 c1 = *reinterpret_cast<const float4 *>(colf + kT + s);
+            const float a0 = __uint_as_float(sv[4 * i4 + 0]), a1 = __uint_as_float(sv[4 * i4 + 1]);
+            const float a2 = __uint_as_float(sv[4 * i4 + 2]), a3 = __uint_as_float(sv[4 * i4 + 3]);
+            m0[2 * i4 + 0] = pack_bf16x2(a0 * rf0 * c0.x, a1 * rf0 * c0.y);
+            m0[2 * i4 + 1] = pack_bf16x2(a2 * rf0 * c0.z, a3 * rf0 * c0.w);
+            m1[2 * i4 + 0] = pack_bf16x2(a0 * rf1 * c1.x, a1 * rf1 * c1.y);
+            m1[2 * i4 + 1] = pack_bf16x2(a2 * rf1 * c1.z, a3 * rf1 * c1.w);
+        }
+    } else {
+        const float cr0 = cs2[r], cr1 = cs2[kT + r];
+#pragma unroll
+        for (int i4 = 0; i4 < 4; ++i4) {
+            const int s = s0 + 4 * i4;
+            const float4 q0 = *reinterpret_cast<const float4 *>(cs2 + s);
+            const float4 d0 = *reinterpret_cast<const float4 *>(dtv + s);
+            const float4 q1 = *reinterpret_cast<const float4 *>(cs2 + kT + s);
+            const float4 d1 = *reinterpret_cast<const float4 *>(dtv + kT + s);
+            const float qa0[4] = {q0.x, q0.y, q0.z, q0.w}, da0[4] = {d0.x, d0.y, d0.z, d0.w};
+            const float qa1[4] = {q1.x, q1.y, q1.z, q1.w}, da1[4] = {d1.x, d1.y, d1.z, d1.w};
+            float e0[4], e1[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float sv_e = __uint_as_float(sv[4 * i4 + e]);
+                const bool keep = (s + e) <= r;
+                e0[e] = keep ? sv_e * ex2_approx(cr0 - qa0[e]) * da0[e] : 0.f;
+                e1[e] = keep ? sv_e * ex2_approx(cr1 - qa1[e]) * da1[e] : 0.f;
+                if (s + e == r) {
+                    e0[e] += D0;
+                    e1[e] += D1;
+                }
+            }
+            m0[2 * i4 + 0] = pack_bf16x2(e0[0], e0[1]);
+            m0[2 * i4 + 1] = pack_bf16x2(e0[2], e0[3]);
+            m1[2 * i4 + 0] = pack_bf16x2(e1[0], e1[1]);
+            m1[2 * i4 + 1] = pack_bf16x2(e1[2], e1[3]);
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
@@ -243,11 +370,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                 ~static_cast<uintptr_t>(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(smem + kOffTmemHolder);
-    float *small = reinterpret_cast<float *>(smem + kOffSmall);
+    float *decay_base = reinterpret_cast<float *>(smem + kOffDecay);
     float *wsum = reinterpret_cast<float *>(smem + kOffWsum);
+    float *hA2 = reinterpret_cast<float *>(smem + kOffHead);   // -exp(A_log) * log2(e)
+    float *hBias = hA2 + kMaxHeads;
+    float *hD = hBias + kMaxHeads;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
+        hA2[h] = -expf(p.A_log[h]) * 1.4426950408889634f;
+        hBias[h] = p.dt_bias[h];
+        hD[h] = p.D[h];
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
@@ -257,15 +392,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars[BAR_X_EMPTY + i], 1);
         }
         mbar_init(&bars[BAR_S_DONE], 1);
-        mbar_init(&bars[BAR_M_READY], kMathThreads);
+        mbar_init(&bars[BAR_M_READY], kGroupWarps);
         mbar_init(&bars[BAR_YD_DONE], 1);
-        mbar_init(&bars[BAR_XS_READY], kMathThreads);
+        mbar_init(&bars[BAR_XS_READY], kGroupWarps);
         mbar_init(&bars[BAR_YOFF_DONE], 1);
         mbar_init(&bars[BAR_STATE_DONE], 1);
-        mbar_init(&bars[BAR_PB_READY], kMathThreads);
-        mbar_init(&bars[BAR_EPI_DONE], kMathThreads);
+        mbar_init(&bars[BAR_PB_READY], kGroupWarps);
+        mbar_init(&bars[BAR_EPI_DONE], kGroupWarps);
         mbar_init(&bars[BAR_DRAIN], 1);
-        mbar_init(&bars[BAR_MSYNC], kMathThreads);
+        mbar_init(&bars[BAR_MSYNC], kGroupWarps);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -290,39 +425,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t j = 0;
             bool ok = true;
             int last_bc[2] = {-1, -1}, last_x[2] = {-1, -1};  // last sub-chunk loaded per stage
-            for (long long u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
-                const Unit w = decode_unit(u, p);
-                for (int k = 0; k < w.nsub; ++k, ++j) {
-                    const int s = j & 1;
-                    const int t0 = (int)(w.cstart + (long long)k * kT);
-                    if (j >= 2 && !(ok = wait_bar(&bars[BAR_BC_EMPTY + s], ((j >> 1) + 1) & 1, p)))
-                        break;
-                    uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
-                    mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
-                    tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], w.g * kN, t0, w.b, pol_keep);
-                    tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], w.g * kN + 64, t0, w.b, pol_keep);
-                    tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], w.g * kN, t0, w.b, pol_keep);
-                    tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], w.g * kN + 64, t0, w.b, pol_keep);
-                    last_bc[s] = (int)j;
-                    if (j >= 1 && !(ok = wait_bar(&bars[BAR_X_EMPTY + s], ((j - 1) >> 1) & 1, p)))
-                        break;
-                    uint8_t *xs = smem + kOffX + s * kXStageBytes;
-                    mbar_arrive_expect_tx(&bars[BAR_X_FULL + s], kXStageBytes);
-                    tma_load_3d(xs, &maps.x, &bars[BAR_X_FULL + s], w.h0 * kP, t0, w.b, pol_stream);
-                    tma_load_3d(xs + kTileBytes, &maps.x, &bars[BAR_X_FULL + s], (w.h0 + 1) * kP, t0, w.b, pol_stream);
-                    last_x[s] = (int)j;
-                }
+            Cursor cur;
+            for (bool has = cursor_first(cur, p); has; has = cursor_next(cur, p), ++j) {
+                const int s = j & 1;
+                const int t0 = (int)cur.t0();
+                if (j >= 2 && !(ok = wait_bar(&bars[BAR_BC_EMPTY + s], ((j >> 1) + 1) & 1, p)))
+                    break;
+                uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
+                const int gc = cur.w.g * kN;
+                mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
+                tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
+                tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
+                tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
+                tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
+                last_bc[s] = (int)j;
+                if (j >= 1 && !(ok = wait_bar(&bars[BAR_X_EMPTY + s], ((j - 1) >> 1) & 1, p)))
+                    break;
+                uint8_t *xs = smem + kOffX + s * kXStageBytes;
+                mbar_arrive_expect_tx(&bars[BAR_X_FULL + s], kXStageBytes);
+                tma_load_3d(xs, &maps.x, &bars[BAR_X_FULL + s], cur.w.h0 * kP, t0, cur.w.b, pol_stream);
+                tma_load_3d(xs + kTileBytes, &maps.x, &bars[BAR_X_FULL + s], (cur.w.h0 + 1) * kP, t0, cur.w.b,
+                            pol_stream);
+                last_x[s] = (int)j;
             }
             if (!ok) {
                 // every load issued by this thread must land before the CTA exits
                 const uint64_t t0 = globaltimer_ns();
                 for (int st = 0; st < 2; ++st) {
                     if (last_bc[st] >= 0)
-                        while (!mbar_test(&bars[BAR_BC_FULL + st], (last_bc[st] >> 1) & 1) &&
+                        while (!mbar_wait_for(&bars[BAR_BC_FULL + st], (last_bc[st] >> 1) & 1, 1000000u) &&
                                globaltimer_ns() - t0 < p.timeout_ns) {
                         }
                     if (last_x[st] >= 0)
-                        while (!mbar_test(&bars[BAR_X_FULL + st], (last_x[st] >> 1) & 1) &&
+                        while (!mbar_wait_for(&bars[BAR_X_FULL + st], (last_x[st] >> 1) & 1, 1000000u) &&
                                globaltimer_ns() - t0 < p.timeout_ns) {
                         }
                 }
@@ -330,315 +465,363 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
+        // order per sub-chunk j:  Y_diag(j), Y_off(j), S(j+1), state(j)
         if (lane == 0) {
             const uint32_t id_S = idesc_bf16_f32(128, 128, 0, 0);      // C (K-major) x B (K-major)
             const uint32_t id_Yd = idesc_bf16_f32(128, 64, 0, 1);      // M (TMEM) x x (MN-major)
             const uint32_t id_Yoff = idesc_bf16_f32(128, 128, 0, 1);   // C (K-major) x P (MN-major)
             const uint32_t id_St = idesc_bf16_f32(128, 128, 1, 1);     // B^T (MN-major) x wx (MN-major)
+            auto issue_S = [&](int stage) {
+                const uint32_t bc = smem_u32(smem + kOffBC + stage * kBCStageBytes);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+                    mma_ss(tmem + kColSM, sdesc_sw128(bc + ko, 16, 1024),
+                           sdesc_sw128(bc + 2 * kTileBytes + ko, 16, 1024), id_S, kk > 0);
+                }
+                mma_commit(&bars[BAR_S_DONE]);
+            };
             uint32_t j = 0;
             bool ok = true;
-            for (long long u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
-                const Unit w = decode_unit(u, p);
-                for (int k = 0; k < w.nsub; ++k, ++j) {
-                    const int s = j & 1;
-                    const uint32_t par = j & 1;
-                    const uint32_t bc = smem_u32(smem + kOffBC + s * kBCStageBytes);
-                    const uint32_t cA = bc, bB = bc + 2 * kTileBytes;
-                    const uint32_t xs = smem_u32(smem + kOffX + s * kXStageBytes);
-                    const uint32_t pb = smem_u32(smem + kOffX + (s ^ 1) * kXStageBytes);
-                    // 1. S = C B^T
-                    if (!(ok = wait_bar(&bars[BAR_BC_FULL + s], (j >> 1) & 1, p)))
-                        break;
-                    if (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p)))
-                        break;
+            Cursor cur;
+            bool has = cursor_first(cur, p);
+            if (has) {
+                if ((ok = wait_bar(&bars[BAR_BC_FULL + 0], 0, p))) {
                     tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                        mma_ss(tmem + kColSY, sdesc_sw128(cA + ko, 16, 1024), sdesc_sw128(bB + ko, 16, 1024),
-                               id_S, kk > 0);
-                    }
-                    mma_commit(&bars[BAR_S_DONE]);
-                    // 2. Y_diag[h] = M[h] x[h]
-                    if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)))
-                        break;
-                    if (!(ok = wait_bar(&bars[BAR_M_READY], par, p)))
-                        break;
-                    tc_fence_after();
-                    for (int h = 0; h < 2; ++h)
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_ts(tmem + kColYd + 64 * h, tmem + kColM + 64 * h + 8 * kk,
-                                   sdesc_sw128(xs + h * kTileBytes + kk * 2048, kTileBytes, 1024), id_Yd, kk > 0);
-                    mma_commit(&bars[BAR_YD_DONE]);
-                    // 3. Y_off = C P   (P as bf16 in the other x stage)
-                    if (!(ok = wait_bar(&bars[BAR_PB_READY], par, p)))
-                        break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                        mma_ss(tmem + kColSY, sdesc_sw128(cA + ko, 16, 1024),
-                               sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
-                    }
-                    mma_commit(&bars[BAR_YOFF_DONE]);
-                    mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
-                    // 4. P += B^T (w o x)   (P already rescaled by the math warps)
-                    if (!(ok = wait_bar(&bars[BAR_XS_READY], par, p)))
-                        break;
-                    tc_fence_after();
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + kColP, sdesc_sw128(bB + kk * 2048, kTileBytes, 1024),
-                               sdesc_sw128(xs + kk * 2048, kTileBytes, 1024), id_St, 1);
-                    mma_commit(&bars[BAR_STATE_DONE]);
-                    mma_commit(&bars[BAR_BC_EMPTY + s]);
+                    issue_S(0);
                 }
+            }
+            while (ok && has) {
+                Cursor nxt = cur;
+                const bool has_next = cursor_next(nxt, p);
+                const int s = j & 1;
+                const uint32_t par = j & 1;
+                const uint32_t bc = smem_u32(smem + kOffBC + s * kBCStageBytes);
+                const uint32_t cA = bc, bB = bc + 2 * kTileBytes;
+                const uint32_t xs = smem_u32(smem + kOffX + s * kXStageBytes);
+                const uint32_t pb = smem_u32(smem + kOffX + (s ^ 1) * kXStageBytes);
+                // Y_diag[h] = M[h] x[h]
+                if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)) ||
+                    !(ok = wait_bar(&bars[BAR_M_READY], par, p)) ||
+                    (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p))))
+                    break;
+                tc_fence_after();
+                for (int h = 0; h < 2; ++h)
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColYd + 64 * h, tmem + kColSM + 16 * kk + 8 * h,
+                               sdesc_sw128(xs + h * kTileBytes + kk * 2048, kTileBytes, 1024), id_Yd, kk > 0);
+                mma_commit(&bars[BAR_YD_DONE]);
+                // Y_off = C P   (P as bf16 in the other x stage)
+                if (!(ok = wait_bar(&bars[BAR_PB_READY], par, p)))
+                    break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+                    mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024),
+                           sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
+                }
+                mma_commit(&bars[BAR_YOFF_DONE]);
+                mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
+                // S of the next sub-chunk, in place of M (after Y_diag has read M)
+                if (has_next) {
+                    if (!(ok = wait_bar(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1, p)) ||
+                        !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
+                        break;
+                    tc_fence_after();
+                    issue_S(s ^ 1);
+                }
+                // P += B^T (w o x)   (P already rescaled by the state group)
+                if (!(ok = wait_bar(&bars[BAR_XS_READY], par, p)))
+                    break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColP, sdesc_sw128(bB + kk * 2048, kTileBytes, 1024),
+                           sdesc_sw128(xs + kk * 2048, kTileBytes, 1024), id_St, 1);
+                mma_commit(&bars[BAR_STATE_DONE]);
+                mma_commit(&bars[BAR_BC_EMPTY + s]);
+                cur = nxt;
+                has = has_next;
+                ++j;
             }
             // make sure no MMA is in flight before tensor memory is released
             mma_commit(&bars[BAR_DRAIN]);
             const uint64_t t0 = globaltimer_ns();
-            while (!mbar_test(&bars[BAR_DRAIN], 0) && globaltimer_ns() - t0 < p.timeout_ns) {
+            while (!mbar_wait_for(&bars[BAR_DRAIN], 0, 1000000u) && globaltimer_ns() - t0 < p.timeout_ns) {
             }
         }
-    } else {
-        // ------------------------------------------------------------ math
+    } else if (warp < kStateWarp0) {
+        // ------------------------------------------------------------ decay group
+        // per sub-chunk j: dt and the local cumulative sum of dt*A (thread: step r,
+        // head hd), decay factors for both groups, then M from S (thread: row r,
+        // s-half hd, both heads)
         const int q = warp & 3;        // TMEM lane quarter
-        const int hf = warp >> 2;      // head of this thread for per-head work; column half for M
-        const int r = q * 32 + lane;   // row: token t / state row n
+        const int hd = warp >> 2;      // head (decay) / s-half (M)
+        const int r = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        const float LOG2E = 1.4426950408889634f;
-        uint32_t j = 0, msync = 0;
+        uint32_t msync = 0;
+        Cursor cur;
+        bool has = cursor_first(cur, p);
+        float dt_raw = 0.f;
+        if (has && r < cur.valid())
+            dt_raw = __ldg(p.dt_raw + ((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + cur.w.h0 + hd);
+        for (uint32_t j = 0; has; ++j) {
+            Cursor nxt = cur;
+            const bool has_next = cursor_next(nxt, p);
+            float dt_next = 0.f;   // issued one sub-chunk ahead
+            if (has_next && r < nxt.valid())
+                dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
+            const int hh = cur.w.h0 + hd;
+            float *dk = decay_base + (j % 3) * kDecayFloats;
+            float *cs2 = dk, *dtv = dk + 2 * kT, *colf = dk + 4 * kT, *ecs = dk + 6 * kT,
+                  *wsc = dk + 8 * kT, *dtot = dk + 10 * kT;
+            float dt = 0.f;
+            if (r < cur.valid())
+                dt = softplus_f32(dt_raw + hBias[hh]);
+            float l = dt * hA2[hh];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float nb = __shfl_up_sync(0xffffffffu, l, o);
+                if (lane >= o)
+                    l += nb;
+            }
+            if (lane == 31)
+                wsum[hd * 4 + q] = l;
+            if (!group_sync(&bars[BAR_MSYNC], msync, p))
+                break;
+            float pre = 0.f, tot = 0.f;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const float v = wsum[hd * 4 + qq];
+                pre += qq < q ? v : 0.f;
+                tot += v;
+            }
+            l += pre;
+            const float l_end = __shfl_sync(0xffffffffu, l, 31);   // cs at the end of this 32-step block
+            cs2[hd * kT + r] = l;
+            dtv[hd * kT + r] = dt;
+            colf[hd * kT + r] = ex2_approx(l_end - l) * dt;
+            ecs[hd * kT + r] = ex2_approx(l);                 // exp(cs_t), scales C P
+            wsc[hd * kT + r] = ex2_approx(tot - l) * dt;      // state input weight
+            if (r == 0)
+                dtot[hd] = ex2_approx(tot);                   // state decay over the sub-chunk
+            if (!group_sync(&bars[BAR_MSYNC], msync, p))
+                break;
+            // ---- M from S, in place, 16 columns at a time (row r, s-half hd, both heads)
+            if (!wait_bar(&bars[BAR_S_DONE], j & 1, p))
+                break;
+            tc_fence_after();
+            {
+                const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
+#pragma unroll 1
+                for (int g = 0; g < 4; ++g) {
+                    const int s0 = 64 * hd + 16 * g;
+                    const uint32_t ta = tmem + lane_addr + kColSM + s0;
+                    uint32_t sv[16], m0[8], m1[8];
+                    tmem_ld16(ta, sv);
+                    tmem_wait_ld();
+                    build_group(sv, m0, m1, s0, r, cs2, dtv, colf, D0, D1);
+                    tmem_st8(ta, m0);
+                    tmem_st8(ta + 8, m1);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            // M(j) is published only after the state group has passed its wait on
+            // M(j-1) (it signals XS_READY(j-1) after that wait), so M_READY never
+            // runs two phases ahead of that group's parity wait
+            if (j >= 1 && !wait_bar(&bars[BAR_XS_READY], (j - 1) & 1, p))
+                break;
+            warp_arrive(&bars[BAR_M_READY]);
+            cur = nxt;
+            has = has_next;
+            dt_raw = dt_next;
+        }
+    } else if (warp < kProducerWarp) {
+        // ------------------------------------------------------------ state group
+        // per sub-chunk j (thread: row r, head hf):
+        //   [carried-in state](j) at a unit start, [x <- w o x, P <- dtot P](j),
+        //   [y](j), [state handoff or bf16 P](j)
+        const int sw = warp - kStateWarp0;   // 0..7
+        const int q = warp & 3;              // TMEM lane quarter
+        const int hf = sw >> 2;              // this thread's head
+        const int r = q * 32 + lane;         // row: token t, or state row n
+        const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
+        const uint32_t ta = tmem + lane_addr + kColP + hf * 64;
         bool ok = true;
-        for (long long u = blockIdx.x; ok && u < p.nunits; u += gridDim.x) {
-            const Unit w = decode_unit(u, p);
-            const int hh = w.h0 + hf;  // this thread's head
-            const float A2 = -expf(p.A_log[hh]) * LOG2E;
-            const float bias = p.dt_bias[hh];
-            const float Dh0 = p.D[w.h0], Dh1 = p.D[w.h0 + 1];
-            // state slot of (b, hh): [P][N], this thread's row n = r
-            const size_t slot_base = ((size_t)w.b * p.H + hh) * (size_t)(kP * kN) + r;
-            for (int k = 0; k < w.nsub; ++k, ++j) {
-                const int s = j & 1;
-                const uint32_t par = j & 1;
-                const long long t0 = w.cstart + (long long)k * kT;
-                const int valid = min(kT, w.clen - k * kT);
-                float *cs2 = small + ((s * 2) * kT) * 3;          // [2 heads][T]
-                float *dtv = cs2 + 2 * kT;
-                float *colf = dtv + 2 * kT;
-                // ---- 0a. unit start: carried-in state into TMEM (fp32) and bf16 operand
-                if (k == 0) {
-                    if (w.c > 0) {
-                        if (threadIdx.x == 0 && !(ok = wait_flag(p.flags + (u - p.nchains), p)))
-                            break;
-                        if (!(ok = math_sync(&bars[BAR_MSYNC], msync, p)))
-                            break;
-                    }
+        Cursor cur;
+        bool has = cursor_first(cur, p);
+        for (uint32_t j = 0; ok && has; ++j) {
+            Cursor nxt = cur;
+            const bool has_next = cursor_next(nxt, p);
+            const int s = j & 1;
+            const uint32_t par = j & 1;
+            const int hh = cur.w.h0 + hf;
+            if (cur.k == 0) {
+                // ---- carried-in state at a unit start: TMEM (fp32) and the bf16 operand of
+                //      C P in x stage (j-1)&1
+                if (cur.w.rg > 0) {
+                    // rows n of this warp were written by the same warp of the predecessor unit
+                    bool okf = true;
+                    if (lane == 0)
+                        okf = wait_flag(p.flags + (size_t)(cur.u - p.nchains) * kGroupWarps + sw, p);
+                    if (!(ok = __shfl_sync(0xffffffffu, okf ? 1 : 0, 0) != 0))
+                        break;
+                }
+                uint8_t *pb = smem + kOffX + (s ^ 1) * kXStageBytes + hf * kTileBytes;
+                for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    uint8_t *pb = smem + kOffX + (s ^ 1) * kXStageBytes + hf * kTileBytes;
-                    for (int half = 0; half < 2; ++half) {
-                        for (int i = 0; i < 32; ++i) {
-                            const size_t off = slot_base + (size_t)(half * 32 + i) * kN;
-                            float val = 0.f;
-                            if (w.c > 0)
-                                val = __ldcg(p.slot + off);
-                            else if (p.init_state)
-                                val = __ldg(p.init_state + off);
-                            v[i] = __float_as_uint(val);
+                    if (cur.w.rg > 0) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.slots + ((size_t)(cur.w.b * p.nhp + cur.w.hp) * kN + r) * (2 * kP) + hf * kP) +
+                            8 * half;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 f = __ldcg(src + i);
+                            v[4 * i + 0] = __float_as_uint(f.x);
+                            v[4 * i + 1] = __float_as_uint(f.y);
+                            v[4 * i + 2] = __float_as_uint(f.z);
+                            v[4 * i + 3] = __float_as_uint(f.w);
                         }
-                        tmem_st32(tmem + lane_addr + kColP + hf * 64 + half * 32, v);
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[c8 * 8 + 0]), __uint_as_float(v[c8 * 8 + 1]));
-                            o.y = pack_bf16x2(__uint_as_float(v[c8 * 8 + 2]), __uint_as_float(v[c8 * 8 + 3]));
-                            o.z = pack_bf16x2(__uint_as_float(v[c8 * 8 + 4]), __uint_as_float(v[c8 * 8 + 5]));
-                            o.w = pack_bf16x2(__uint_as_float(v[c8 * 8 + 6]), __uint_as_float(v[c8 * 8 + 7]));
-                            *reinterpret_cast<uint4 *>(pb + sw128(r, half * 4 + c8)) = o;
-                        }
+                    } else if (p.init_state) {
+                        const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = __float_as_uint(__ldg(src + (size_t)(32 * half + i) * kN));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            v[i] = 0u;
                     }
-                    tmem_wait_st();
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(&bars[BAR_PB_READY]);
+                    tmem_st32(ta + 32 * half, v);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v + 8 * c8);
                 }
-                // ---- 0b. dt, sub-chunk-local cumulative sum of dt*A (base 2), decay factors
-                float dt = 0.f;
-                if (r < valid)
-                    dt = softplus_f32(p.dt_raw[((size_t)w.b * p.L + t0 + r) * p.H + hh] + bias);
-                float l = dt * A2;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float nb = __shfl_up_sync(0xffffffffu, l, o);
-                    if (lane >= o)
-                        l += nb;
-                }
-                if (lane == 31)
-                    wsum[hf * 4 + q] = l;
-                if (!(ok = math_sync(&bars[BAR_MSYNC], msync, p)))
-                    break;
-                for (int qq = 0; qq < q; ++qq)
-                    l += wsum[hf * 4 + qq];
-                cs2[hf * kT + r] = l;
-                dtv[hf * kT + r] = dt;
-                if (!(ok = math_sync(&bars[BAR_MSYNC], msync, p)))
-                    break;
-                colf[hf * kT + r] = ex2_approx(cs2[hf * kT + (r | 31)] - l) * dt;
-                const float cs_last = cs2[hf * kT + kT - 1];
-                const float ecs = ex2_approx(l);                  // exp(cs_t), for C P
-                const float wsc = ex2_approx(cs_last - l) * dt;   // state input weight
-                const float dtot = ex2_approx(cs_last);           // state decay over the sub-chunk
-                if (!(ok = math_sync(&bars[BAR_MSYNC], msync, p)))
-                    break;
-                // ---- 1. masked decay matrix M (both heads) from S
-                if (!(ok = wait_bar(&bars[BAR_S_DONE], par, p)))
-                    break;
-                tc_fence_after();
-                {
-                    uint32_t m0[32], m1[32];
-                    const int rb = r >> 5;
-                    for (int jb = 0; jb < 2; ++jb) {
-                        const int J = hf * 2 + jb;   // 32-column block of s
-                        uint32_t sv[32];
-                        tmem_ld32(tmem + lane_addr + kColSY + J * 32, sv);
-                        tmem_wait_ld();
-                        for (int hh2 = 0; hh2 < 2; ++hh2) {
-                            uint32_t *mo = (hh2 == 0 ? m0 : m1) + jb * 16;
-                            const float *cs = cs2 + hh2 * kT;
-                            const float *dd = dtv + hh2 * kT;
-                            const float *cf = colf + hh2 * kT;
-                            const float Dh = hh2 == 0 ? Dh0 : Dh1;
-                            if (J > rb) {
-#pragma unroll
-                                for (int i = 0; i < 16; ++i)
-                                    mo[i] = 0u;
-                            } else if (J == rb) {
-                                const float csr = cs[r];
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int s0 = J * 32 + 2 * i, s1 = s0 + 1;
-                                    float a = 0.f, b2 = 0.f;
-                                    if (s0 <= r)
-                                        a = __uint_as_float(sv[2 * i]) * ex2_approx(csr - cs[s0]) * dd[s0];
-                                    if (s1 <= r)
-                                        b2 = __uint_as_float(sv[2 * i + 1]) * ex2_approx(csr - cs[s1]) * dd[s1];
-                                    if (s0 == r)
-                                        a += Dh;
-                                    if (s1 == r)
-                                        b2 += Dh;
-                                    mo[i] = pack_bf16x2(a, b2);
-                                }
-                            } else {
-                                const float rf = ex2_approx(cs[r] - cs[J * 32 + 31]);
-#pragma unroll
-                                for (int i = 0; i < 16; ++i) {
-                                    const int s0 = J * 32 + 2 * i;
-                                    mo[i] = pack_bf16x2(__uint_as_float(sv[2 * i]) * rf * cf[s0],
-                                                        __uint_as_float(sv[2 * i + 1]) * rf * cf[s0 + 1]);
-                                }
-                            }
-                        }
-                    }
-                    tmem_st32(tmem + lane_addr + kColM + 0 * 64 + hf * 32, m0);
-                    tmem_st32(tmem + lane_addr + kColM + 1 * 64 + hf * 32, m1);
-                    tmem_wait_st();
-                }
+                tmem_wait_st();
+                fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bars[BAR_M_READY]);
-                // ---- 2. x <- w o x in place (row r of head hf), P <- dtot P
-                if (!(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
-                    break;
-                tc_fence_after();
-                {
-                    uint8_t *xrow = smem + kOffX + s * kXStageBytes + hf * kTileBytes + r * 128;
+                warp_arrive(&bars[BAR_PB_READY]);
+            }
+            // ---- x <- w o x in place (row r, head hf); P <- dtot P
+            if (!(ok = wait_bar(&bars[BAR_M_READY], par, p)) || !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
+                break;
+            tc_fence_after();
+            const float *dk = decay_base + (j % 3) * kDecayFloats;
+            const float ecs = dk[6 * kT + hf * kT + r];
+            const float wsc = dk[8 * kT + hf * kT + r];
+            const float dtot = dk[10 * kT + hf];
+            {
+                uint8_t *xrow = smem + kOffX + s * kXStageBytes + hf * kTileBytes + r * 128;
+                // every chunk of the row gets the same weight, so the chunks are
+                // visited in swizzled order: 8 consecutive rows hit 8 distinct banks
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
-                        uint4 v4 = *reinterpret_cast<uint4 *>(xrow + c8 * 16);
-                        v4.x = pack_bf16x2(bf16lo_to_f32(v4.x) * wsc, bf16hi_to_f32(v4.x) * wsc);
-                        v4.y = pack_bf16x2(bf16lo_to_f32(v4.y) * wsc, bf16hi_to_f32(v4.y) * wsc);
-                        v4.z = pack_bf16x2(bf16lo_to_f32(v4.z) * wsc, bf16hi_to_f32(v4.z) * wsc);
-                        v4.w = pack_bf16x2(bf16lo_to_f32(v4.w) * wsc, bf16hi_to_f32(v4.w) * wsc);
-                        *reinterpret_cast<uint4 *>(xrow + c8 * 16) = v4;
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    const int cc = c8 ^ (r & 7);
+                    uint4 v4 = *reinterpret_cast<uint4 *>(xrow + cc * 16);
+                    v4.x = pack_bf16x2(bf16lo_to_f32(v4.x) * wsc, bf16hi_to_f32(v4.x) * wsc);
+                    v4.y = pack_bf16x2(bf16lo_to_f32(v4.y) * wsc, bf16hi_to_f32(v4.y) * wsc);
+                    v4.z = pack_bf16x2(bf16lo_to_f32(v4.z) * wsc, bf16hi_to_f32(v4.z) * wsc);
+                    v4.w = pack_bf16x2(bf16lo_to_f32(v4.w) * wsc, bf16hi_to_f32(v4.w) * wsc);
+                    *reinterpret_cast<uint4 *>(xrow + cc * 16) = v4;
+                }
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(ta + 32 * half, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        v[i] = __float_as_uint(__uint_as_float(v[i]) * dtot);
+                    tmem_st32(ta + 32 * half, v);
+                }
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bars[BAR_XS_READY]);
+            // ---- y = Y_diag + exp(cs_t) Y_off   (row t = r, head hf)
+            if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
+                break;
+            tc_fence_after();
+            {
+                const int valid = cur.valid();
+                __nv_bfloat16 *yrow = p.y + (((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + hh) * kP;
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t yd[32], yo[32];
+                    tmem_ld32(tmem + lane_addr + kColYd + hf * 64 + 32 * half, yd);
+                    tmem_ld32(tmem + lane_addr + kColYo + hf * 64 + 32 * half, yo);
+                    tmem_wait_ld();
+                    if (half == 1) {
+                        tc_fence_before();
+                        warp_arrive(&bars[BAR_EPI_DONE]);
                     }
+                    if (r < valid) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int i = c8 * 8 + 2 * e;
+                                o[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
+                                                   fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
+                            }
+                            st_global_cs_v4(yrow + 32 * half + c8 * 8, o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            }
+            // ---- carried state after sub-chunk j
+            if (!(ok = wait_bar(&bars[BAR_STATE_DONE], par, p)))
+                break;
+            tc_fence_after();
+            if (cur.k == cur.w.nsub - 1) {
+                // end of the unit: hand the state to the next unit of this chain, or
+                // write the final state
+                if (cur.w.rg < p.nranges - 1) {
+                    float4 *dst = reinterpret_cast<float4 *>(
+                        p.slots + ((size_t)(cur.w.b * p.nhp + cur.w.hp) * kN + r) * (2 * kP) + hf * kP);
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
-                        const uint32_t ta = tmem + lane_addr + kColP + hf * 64 + half * 32;
-                        tmem_ld32(ta, v);
+                        tmem_ld32(ta + 32 * half, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            __stcg(dst + 8 * half + i,
+                                   make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                               __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
+                    }
+                    __syncwarp();
+                    if (lane == 0) {
+                        __threadfence();
+                        st_release_u64(p.flags + (size_t)cur.u * kGroupWarps + sw, p.epoch);
+                    }
+                } else if (p.final_state) {
+                    float *dst = p.final_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
+                    for (int half = 0; half < 2; ++half) {
+                        uint32_t v[32];
+                        tmem_ld32(ta + 32 * half, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__uint_as_float(v[i]) * dtot);
-                        tmem_st32(ta, v);
+                            dst[(size_t)(32 * half + i) * kN] = __uint_as_float(v[i]);
                     }
-                    tmem_wait_st();
+                }
+                tc_fence_before();
+            } else {
+                // bf16 copy of P for the next sub-chunk's C P, in this sub-chunk's x stage
+                uint8_t *pb = smem + kOffX + s * kXStageBytes + hf * kTileBytes;
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t v[32];
+                    tmem_ld32(ta + 32 * half, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8)
+                        *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v + 8 * c8);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
-                mbar_arrive(&bars[BAR_XS_READY]);
-                // ---- 3. y = Y_diag + exp(cs_t) Y_off   (row t = r, head hf)
-                if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
-                    break;
-                tc_fence_after();
-                {
-                    __nv_bfloat16 *yrow = p.y + (((size_t)w.b * p.L + t0 + r) * p.H + hh) * kP;
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t yd[32], yo[32];
-                        tmem_ld32(tmem + lane_addr + kColYd + hf * 64 + half * 32, yd);
-                        tmem_ld32(tmem + lane_addr + kColSY + hf * 64 + half * 32, yo);
-                        tmem_wait_ld();
-                        if (r < valid) {
-#pragma unroll
-                            for (int c8 = 0; c8 < 4; ++c8) {
-                                uint32_t o[4];
-#pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    const int i = c8 * 8 + 2 * e;
-                                    o[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
-                                                       fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
-                                }
-                                st_global_cs_v4(yrow + half * 32 + c8 * 8, o[0], o[1], o[2], o[3]);
-                            }
-                        }
-                    }
-                }
-                tc_fence_before();
-                mbar_arrive(&bars[BAR_EPI_DONE]);
-                // ---- 4. carried state: hand off (end of unit) or bf16 operand for the next sub-chunk
-                if (!(ok = wait_bar(&bars[BAR_STATE_DONE], par, p)))
-                    break;
-                tc_fence_after();
-                const bool last = (k == w.nsub - 1);
-                if (last) {
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_addr + kColP + hf * 64 + half * 32, v);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            p.slot[slot_base + (size_t)(half * 32 + i) * kN] = __uint_as_float(v[i]);
-                    }
-                    tc_fence_before();
-                    if (!(ok = math_sync(&bars[BAR_MSYNC], msync, p)))
-                        break;
-                    if (threadIdx.x == 0 && w.c < p.nchunks - 1) {
-                        __threadfence();
-                        st_release_u64(p.flags + u, p.epoch);
-                    }
-                } else {
-                    uint8_t *pb = smem + kOffX + s * kXStageBytes + hf * kTileBytes;
-                    for (int half = 0; half < 2; ++half) {
-                        uint32_t v[32];
-                        tmem_ld32(tmem + lane_addr + kColP + hf * 64 + half * 32, v);
-                        tmem_wait_ld();
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint4 o;
-                            o.x = pack_bf16x2(__uint_as_float(v[c8 * 8 + 0]), __uint_as_float(v[c8 * 8 + 1]));
-                            o.y = pack_bf16x2(__uint_as_float(v[c8 * 8 + 2]), __uint_as_float(v[c8 * 8 + 3]));
-                            o.z = pack_bf16x2(__uint_as_float(v[c8 * 8 + 4]), __uint_as_float(v[c8 * 8 + 5]));
-                            o.w = pack_bf16x2(__uint_as_float(v[c8 * 8 + 6]), __uint_as_float(v[c8 * 8 + 7]));
-                            *reinterpret_cast<uint4 *>(pb + sw128(r, half * 4 + c8)) = o;
-                        }
-                    }
-                    fence_proxy_async_smem();
-                    tc_fence_before();
-                    mbar_arrive(&bars[BAR_PB_READY]);
-                }
+                warp_arrive(&bars[BAR_PB_READY]);
             }
+            cur = nxt;
+            has = has_next;
         }
     }
 
@@ -667,20 +850,63 @@ unsigned long long next_epoch()
     return e == 0 ? next_epoch() : e;
 }
 
+int sm_count()
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    return sms;
+}
+
 struct Geometry {
-    long long nchunks, nchains, nunits;
+    long long nchunks, nchains, chunks_per_unit, nranges, nunits, grid;
     size_t flags_off, slot_off, total;
 };
+
+// Chunks per unit R.  The schedule runs ceil(units / grid) rounds of units of
+// R chunks, every unit boundary costs about one sub-chunk of handoff latency,
+// and the units of one chain run one after another, so the makespan is at
+// least one chain's length.  R is the candidate with the smallest estimate.
+long long pick_chunks_per_unit(long long nchunks, long long nchains, int Q, long long grid)
+{
+    const double subs_per_chunk = (double)Q / kT;
+    const double handoff = 1.0;   // in sub-chunk times
+    long long best_r = 1;
+    double best = 1e300;
+    long long cand[64];
+    int nc = 0;
+    for (long long R = 1; R < nchunks && nc < 62; R = (R < 4 ? R + 1 : R * 2))
+        cand[nc++] = R;
+    cand[nc++] = nchunks;
+    for (int i = 0; i < nc; ++i) {
+        const long long R = cand[i];
+        const long long ranges = (nchunks + R - 1) / R;
+        const long long units = ranges * nchains;
+        const long long rounds = (units + grid - 1) / grid;
+        const double unit_time = R * subs_per_chunk + handoff;
+        const double est = std::max(rounds * unit_time, ranges * unit_time);
+        if (est < best * 0.999) {
+            best = est;
+            best_r = R;
+        }
+    }
+    return best_r;
+}
 
 Geometry geometry(const ScanArgs &a)
 {
     Geometry g;
     g.nchunks = (a.seqlen + a.chunk - 1) / a.chunk;
     g.nchains = a.batch * (a.nheads / 2);
-    g.nunits = g.nchunks * g.nchains;
+    const int sms = std::max(1, sm_count());
+    g.chunks_per_unit = pick_chunks_per_unit(g.nchunks, g.nchains, a.chunk, sms);
+    g.nranges = (g.nchunks + g.chunks_per_unit - 1) / g.chunks_per_unit;
+    g.nunits = g.nranges * g.nchains;
+    g.grid = std::min<long long>(sms, g.nunits);
     g.flags_off = 256;
-    g.slot_off = (g.flags_off + (size_t)g.nunits * 8 + 255) & ~(size_t)255;
-    const size_t slot_bytes = a.final_state ? 0 : (size_t)a.batch * a.nheads * kP * kN * 4;
+    g.slot_off = (g.flags_off + (size_t)g.nunits * kGroupWarps * 8 + 255) & ~(size_t)255;
+    const size_t slot_bytes = g.nranges > 1 ? (size_t)g.nchains * kN * 2 * kP * 4 : 0;
     g.total = g.slot_off + slot_bytes;
     return g;
 }
@@ -689,6 +915,8 @@ Geometry geometry(const ScanArgs &a)
 
 bool chunk_supported(const ScanArgs &a)
 {
+    if (a.nheads > kMaxHeads)
+        return false;
     if (a.dtype != SSD_DTYPE_BF16 || a.headdim != kP || a.dstate != kN)
         return false;
     if (a.chunk % 64 != 0 || a.chunk <= 0)
@@ -721,28 +949,24 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     char *ws = static_cast<char *>(workspace);
     p.abort_word = reinterpret_cast<unsigned long long *>(ws);
     p.flags = reinterpret_cast<unsigned long long *>(ws + geo.flags_off);
-    p.slot = a.final_state ? a.final_state : reinterpret_cast<float *>(ws + geo.slot_off);
+    p.final_state = a.final_state;
+    p.slots = geo.nranges > 1 ? reinterpret_cast<float *>(ws + geo.slot_off) : nullptr;
     p.epoch = next_epoch();
     p.timeout_ns = 2000000000ull;
     p.L = a.seqlen;
     p.nunits = geo.nunits;
     p.H = a.nheads;
-    p.Q = a.chunk;
-    p.nchunks = (int)geo.nchunks;
+    p.span = (int)(geo.chunks_per_unit * a.chunk);
+    p.nranges = (int)geo.nranges;
     p.nhp = a.nheads / 2;
     p.nchains = (int)geo.nchains;
     p.hpg = a.nheads / a.ngroups;
 
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-        return SSD_ERR_CUDA;
     if (cudaFuncSetAttribute(ssd_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;
-    const long long grid = std::min<long long>(sms, geo.nunits);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)grid);
+    cfg.gridDim = dim3((unsigned)geo.grid);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
