@@ -114,6 +114,31 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *map, uin
         : "memory");
 }
 
+// 3-D tiled store from this CTA's shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const void *map, const void *smem_src, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
+                 "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until every committed bulk group of this thread has finished reading
+// shared memory (the source may then be reused).
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until every committed bulk group of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Prefetch a 3-D tile into L2 (no shared memory involved).
+__device__ __forceinline__ void tma_prefetch_3d(const void *map, int c0, int c1, int c2)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *map, uint64_t *bar, int c0,
                                             int c1)
 {
@@ -275,6 +300,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Elementwise product of two bf16 pairs, rounded to nearest even.
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b)
+{
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
     return r;
 }
 

@@ -85,7 +85,7 @@ constexpr uint32_t kOffWsum = kOffDecay + 3 * kDecayFloats * 4;
 constexpr int kMaxHeads = 512;                       // per-head parameters staged in shared memory
 constexpr uint32_t kOffHead = kOffWsum + 64;          // A*log2(e), dt_bias, D  (3 x kMaxHeads floats)
 constexpr uint32_t kOffBars = kOffHead + 3 * kMaxHeads * 4;
-constexpr int kNumBars = 20;
+constexpr int kNumBars = 22;
 constexpr uint32_t kOffTmemHolder = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemHolder + 16 + 1024;  // + alignment slack
 
@@ -111,6 +111,7 @@ enum {
     BAR_EPI_DONE,
     BAR_DRAIN,
     BAR_MSYNC,   // decay-group barrier (bounded, unlike bar.sync)
+    BAR_Y_STAGED,  // 2: y of sub-chunk j staged in shared memory (barrier j & 1)
 };
 
 struct ChunkParams {
@@ -121,7 +122,7 @@ struct ChunkParams {
     const float *init_state;          // [B,H,P,N] or null
     __nv_bfloat16 *y;
     float *final_state;               // [B,H,P,N] or null
-    float *slots;                     // [chains][N][2P] handoff states (null if one unit per chain)
+    float *slots;                     // [chains][2][16][N][4] handoff states (null if one unit per chain)
     unsigned long long *flags;        // [nunits][state-group warps]: warp w of a unit publishes its rows
     unsigned long long *abort_word;
     unsigned long long epoch;
@@ -132,7 +133,8 @@ struct ChunkParams {
 };
 
 struct Maps {
-    CUtensorMap x, B, C;
+    CUtensorMap x, B, C;   // C boxes are 8 steps high (rows placed in row_step order)
+    CUtensorMap y;         // store boxes of 64 steps x 64 channels
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
@@ -145,12 +147,6 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __device__ __forceinline__ void st_release_u64(unsigned long long *p, unsigned long long v)
 {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void st_global_cs_v4(void *ptr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(ptr), "r"(a), "r"(b), "r"(c), "r"(d)
-                 : "memory");
 }
 
 __device__ void raise_timeout(const ChunkParams &p)
@@ -287,6 +283,18 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }
 
+// Row order of the C tile (and so of S, M, Y_diag and Y_off in tensor memory):
+// TMEM lane quarter q holds the 8-step groups {q, 7-q, 8+q, 15-q} of the
+// sub-chunk, so that every quarter (which only its own SM sub-partition can
+// access) gets the same share of the causal triangle.  Lane r holds step
+// row_step(r).
+__device__ __forceinline__ int row_step(int r)
+{
+    const int gi = r >> 3, q = gi >> 2, k = gi & 3;
+    const int grp = k == 0 ? q : (k == 1 ? 7 - q : (k == 2 ? 8 + q : 15 - q));
+    return (grp << 3) | (r & 7);
+}
+
 __device__ __forceinline__ uint4 pack8(const uint32_t *v)
 {
     uint4 o;
@@ -298,27 +306,27 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *v)
 }
 
 // One 16-column group of M for both heads, from S values sv[0..15]
-// (columns s = s0 .. s0+15 of row r; s0 is a multiple of 16).  Writes 8
-// packed bf16 pairs per head.  Decay exp(cs_t - cs_s) dt_s for s <= t:
-//   * s in an earlier 32-step block than t: the row factor exp(cs_t - cs_e)
-//     times the column factor exp(cs_e - cs_s) dt_s (e = end of s's block),
-//     both <= 1;
-//   * s in t's own 32-step block: evaluated directly;
+// (columns s = s0 .. s0+15 of the row of step t; s0 is a multiple of 16).
+// Writes 8 packed bf16 pairs per head.  Decay exp(cs_t - cs_s) dt_s for s <= t:
+//   * s in an earlier 16-step group than t: the row factor exp(cs_t - cs_e)
+//     times the column factor colf[s] = exp(cs_e - cs_s) dt_s (e = last step of
+//     s's group), both <= 1;
+//   * s in t's own group: evaluated directly;
 // and D_h is added on the diagonal.
 __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8],
-                                            int s0, int r, const float *cs2, const float *dtv,
+                                            int s0, int t, const float *cs2, const float *dtv,
                                             const float *colf, float D0, float D1)
 {
-    const int J = s0 >> 5, rb = r >> 5;
-    if (J > rb) {
+    const int G = s0 >> 4, tg = t >> 4;
+    if (G > tg) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             m0[i] = 0u;
             m1[i] = 0u;
         }
-    } else if (J < rb) {
-        const float rf0 = ex2_approx(cs2[r] - cs2[J * 32 + 31]);
-        const float rf1 = ex2_approx(cs2[kT + r] - cs2[kT + J * 32 + 31]);
+    } else if (G < tg) {
+        const float rf0 = ex2_approx(cs2[t] - cs2[s0 + 15]);
+        const float rf1 = ex2_approx(cs2[kT + t] - cs2[kT + s0 + 15]);
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4) {
             const int s = s0 + 4 * i4;
@@ -332,7 +340,7 @@ __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (
             m1[2 * i4 + 1] = pack_bf16x2(a2 * rf1 * c1.z, a3 * rf1 * c1.w);
         }
     } else {
-        const float cr0 = cs2[r], cr1 = cs2[kT + r];
+        const float cr0 = cs2[t], cr1 = cs2[kT + t];
 #pragma unroll
         for (int i4 = 0; i4 < 4; ++i4) {
             const int s = s0 + 4 * i4;
@@ -346,10 +354,10 @@ __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float sv_e = __uint_as_float(sv[4 * i4 + e]);
-                const bool keep = (s + e) <= r;
+                const bool keep = (s + e) <= t;
                 e0[e] = keep ? sv_e * ex2_approx(cr0 - qa0[e]) * da0[e] : 0.f;
                 e1[e] = keep ? sv_e * ex2_approx(cr1 - qa1[e]) * da1[e] : 0.f;
-                if (s + e == r) {
+                if (s + e == t) {
                     e0[e] += D0;
                     e1[e] += D1;
                 }
@@ -401,6 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[BAR_EPI_DONE], kGroupWarps);
         mbar_init(&bars[BAR_DRAIN], 1);
         mbar_init(&bars[BAR_MSYNC], kGroupWarps);
+        mbar_init(&bars[BAR_Y_STAGED + 0], kGroupWarps);
+        mbar_init(&bars[BAR_Y_STAGED + 1], kGroupWarps);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -411,6 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tmap(&maps.x);
         prefetch_tmap(&maps.B);
         prefetch_tmap(&maps.C);
+        prefetch_tmap(&maps.y);
     }
     tc_fence_before();
     __syncthreads();
@@ -425,17 +436,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t j = 0;
             bool ok = true;
             int last_bc[2] = {-1, -1}, last_x[2] = {-1, -1};  // last sub-chunk loaded per stage
-            Cursor cur;
+            // y of sub-chunk jj is staged (by the state group) in the C area of its
+            // B/C stage; store it with TMA before that stage is reloaded
+            auto store_y = [&](const Cursor &c, uint32_t jj) -> bool {
+                if (!wait_bar(&bars[BAR_Y_STAGED + (jj & 1)], (jj >> 1) & 1, p))
+                    return false;
+                const uint8_t *stg = smem + kOffBC + (jj & 1) * kBCStageBytes;
+                const int ty = (int)c.t0();
+                const int nbox = c.valid() > 64 ? 2 : 1;
+                for (int h = 0; h < 2; ++h)
+                    for (int bx = 0; bx < nbox; ++bx)
+                        tma_store_3d(&maps.y, stg + h * kTileBytes + bx * (kTileBytes / 2), (c.w.h0 + h) * kP,
+                                     ty + 64 * bx, c.w.b);
+                bulk_commit_group();
+                bulk_wait_read_all();
+                return true;
+            };
+            Cursor cur, back1, back2;   // back1/back2: the previous two sub-chunks
             for (bool has = cursor_first(cur, p); has; has = cursor_next(cur, p), ++j) {
                 const int s = j & 1;
                 const int t0 = (int)cur.t0();
+                if (j >= 2 && !(ok = store_y(back2, j - 2)))
+                    break;
                 if (j >= 2 && !(ok = wait_bar(&bars[BAR_BC_EMPTY + s], ((j >> 1) + 1) & 1, p)))
                     break;
                 uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
                 const int gc = cur.w.g * kN;
                 mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
-                tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
-                tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
+                for (int gi = 0; gi < 16; ++gi) {
+                    const int ts = t0 + row_step(gi << 3);   // first step of the group placed at rows 8gi..
+                    tma_load_3d(bc + gi * 1024, &maps.C, &bars[BAR_BC_FULL + s], gc, ts, cur.w.b, pol_keep);
+                    tma_load_3d(bc + kTileBytes + gi * 1024, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, ts, cur.w.b,
+                                pol_keep);
+                }
                 tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
                 last_bc[s] = (int)j;
@@ -447,7 +480,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(xs + kTileBytes, &maps.x, &bars[BAR_X_FULL + s], (cur.w.h0 + 1) * kP, t0, cur.w.b,
                             pol_stream);
                 last_x[s] = (int)j;
+                back2 = back1;
+                back1 = cur;
             }
+            // the last two sub-chunks' outputs
+            if (ok && j >= 2)
+                ok = store_y(back2, j - 2);
+            if (ok && j >= 1)
+                ok = store_y(back1, j - 1);
+            bulk_wait_all();
             if (!ok) {
                 // every load issued by this thread must land before the CTA exits
                 const uint64_t t0 = globaltimer_ns();
@@ -595,7 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tot += v;
             }
             l += pre;
-            const float l_end = __shfl_sync(0xffffffffu, l, 31);   // cs at the end of this 32-step block
+            const float l_end = __shfl_sync(0xffffffffu, l, lane | 15);   // cs at the end of this 16-step group
             cs2[hd * kT + r] = l;
             dtv[hd * kT + r] = dt;
             colf[hd * kT + r] = ex2_approx(l_end - l) * dt;
@@ -611,6 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             {
                 const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
+                const int t_row = row_step(r);
 #pragma unroll 1
                 for (int g = 0; g < 4; ++g) {
                     const int s0 = 64 * hd + 16 * g;
@@ -618,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t sv[16], m0[8], m1[8];
                     tmem_ld16(ta, sv);
                     tmem_wait_ld();
-                    build_group(sv, m0, m1, s0, r, cs2, dtv, colf, D0, D1);
+                    build_group(sv, m0, m1, s0, t_row, cs2, dtv, colf, D0, D1);
                     tmem_st8(ta, m0);
                     tmem_st8(ta + 8, m1);
                 }
@@ -670,12 +712,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
                     if (cur.w.rg > 0) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.slots + ((size_t)(cur.w.b * p.nhp + cur.w.hp) * kN + r) * (2 * kP) + hf * kP) +
-                            8 * half;
+                        const float4 *src = reinterpret_cast<const float4 *>(p.slots) +
+                                            ((size_t)(cur.w.b * p.nhp + cur.w.hp) * 2 + hf) * 16 * kN + r;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
-                            const float4 f = __ldcg(src + i);
+                            const float4 f = __ldcg(src + (size_t)(8 * half + i) * kN);
                             v[4 * i + 0] = __float_as_uint(f.x);
                             v[4 * i + 1] = __float_as_uint(f.y);
                             v[4 * i + 2] = __float_as_uint(f.z);
@@ -706,21 +747,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             const float *dk = decay_base + (j % 3) * kDecayFloats;
-            const float ecs = dk[6 * kT + hf * kT + r];
+            const int t_row = row_step(r);                 // step held by TMEM lane r in Y
+            const float ecs = dk[6 * kT + hf * kT + t_row];
             const float wsc = dk[8 * kT + hf * kT + r];
             const float dtot = dk[10 * kT + hf];
             {
                 uint8_t *xrow = smem + kOffX + s * kXStageBytes + hf * kTileBytes + r * 128;
+                const uint32_t w2 = pack_bf16x2(wsc, wsc);
                 // every chunk of the row gets the same weight, so the chunks are
                 // visited in swizzled order: 8 consecutive rows hit 8 distinct banks
 #pragma unroll
                 for (int c8 = 0; c8 < 8; ++c8) {
                     const int cc = c8 ^ (r & 7);
                     uint4 v4 = *reinterpret_cast<uint4 *>(xrow + cc * 16);
-                    v4.x = pack_bf16x2(bf16lo_to_f32(v4.x) * wsc, bf16hi_to_f32(v4.x) * wsc);
-                    v4.y = pack_bf16x2(bf16lo_to_f32(v4.y) * wsc, bf16hi_to_f32(v4.y) * wsc);
-                    v4.z = pack_bf16x2(bf16lo_to_f32(v4.z) * wsc, bf16hi_to_f32(v4.z) * wsc);
-                    v4.w = pack_bf16x2(bf16lo_to_f32(v4.w) * wsc, bf16hi_to_f32(v4.w) * wsc);
+                    v4.x = mul_bf16x2(v4.x, w2);
+                    v4.y = mul_bf16x2(v4.y, w2);
+                    v4.z = mul_bf16x2(v4.z, w2);
+                    v4.w = mul_bf16x2(v4.w, w2);
                     *reinterpret_cast<uint4 *>(xrow + cc * 16) = v4;
                 }
                 for (int half = 0; half < 2; ++half) {
@@ -737,13 +780,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             warp_arrive(&bars[BAR_XS_READY]);
-            // ---- y = Y_diag + exp(cs_t) Y_off   (row t = r, head hf)
+            // ---- y = Y_diag + exp(cs_t) Y_off   (TMEM lane r = step t_row, head hf), staged
+            //      in the C area of this sub-chunk's B/C stage (C is dead after Y_off) for the
+            //      producer's TMA store
             if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
                 break;
             tc_fence_after();
             {
-                const int valid = cur.valid();
-                __nv_bfloat16 *yrow = p.y + (((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + hh) * kP;
+                uint8_t *stg = smem + kOffBC + s * kBCStageBytes + hf * kTileBytes;
                 for (int half = 0; half < 2; ++half) {
                     uint32_t yd[32], yo[32];
                     tmem_ld32(tmem + lane_addr + kColYd + hf * 64 + 32 * half, yd);
@@ -753,20 +797,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tc_fence_before();
                         warp_arrive(&bars[BAR_EPI_DONE]);
                     }
-                    if (r < valid) {
 #pragma unroll
-                        for (int c8 = 0; c8 < 4; ++c8) {
-                            uint32_t o[4];
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        uint4 o;
+                        uint32_t *ov = reinterpret_cast<uint32_t *>(&o);
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int i = c8 * 8 + 2 * e;
-                                o[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
-                                                   fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
-                            }
-                            st_global_cs_v4(yrow + 32 * half + c8 * 8, o[0], o[1], o[2], o[3]);
+                        for (int e = 0; e < 4; ++e) {
+                            const int i = c8 * 8 + 2 * e;
+                            ov[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
+                                                fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
                         }
+                        *reinterpret_cast<uint4 *>(stg + sw128(t_row, 4 * half + c8)) = o;
                     }
                 }
+                fence_proxy_async_smem();
+                warp_arrive(&bars[BAR_Y_STAGED + s]);
             }
             // ---- carried state after sub-chunk j
             if (!(ok = wait_bar(&bars[BAR_STATE_DONE], par, p)))
@@ -776,15 +821,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // end of the unit: hand the state to the next unit of this chain, or
                 // write the final state
                 if (cur.w.rg < p.nranges - 1) {
-                    float4 *dst = reinterpret_cast<float4 *>(
-                        p.slots + ((size_t)(cur.w.b * p.nhp + cur.w.hp) * kN + r) * (2 * kP) + hf * kP);
+                    // slot layout [chain][head][16-byte chunk c][row n]: a warp writes 512
+                    // contiguous bytes per chunk
+                    float4 *dst = reinterpret_cast<float4 *>(p.slots) +
+                                  ((size_t)(cur.w.b * p.nhp + cur.w.hp) * 2 + hf) * 16 * kN + r;
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
                         tmem_ld32(ta + 32 * half, v);
                         tmem_wait_ld();
 #pragma unroll
                         for (int i = 0; i < 8; ++i)
-                            __stcg(dst + 8 * half + i,
+                            __stcg(dst + (size_t)(8 * half + i) * kN,
                                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
                     }
@@ -937,7 +984,8 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
     if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
-        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128))
+        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 8) ||
+        !make_tmap_bf16_3d(&maps.y, a.y, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 64))
         return SSD_ERR_CUDA;
     ChunkParams p;
     p.dt_raw = a.dt_raw;
