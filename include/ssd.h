@@ -53,7 +53,8 @@ typedef enum ssd_status {
     SSD_ERR_UNSUPPORTED = 4,    /* dtype, shape or requested path not supported */
     SSD_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed; nothing further enqueued */
     SSD_ERR_TIMEOUT = 6,        /* a kernel gave up a bounded wait (read via ssd_get_device_error) */
-    SSD_ERR_ALIASING = 7        /* y overlaps an input, or the two states overlap partially */
+    SSD_ERR_ALIASING = 7,       /* y overlaps an input, or the two states overlap partially */
+    SSD_ERR_SCRATCH_LIMIT = 8   /* ssd_scan_fwd_noalloc: scratch needed exceeds its fixed array */
 } ssd_status_t;
 
 /* Kernel path selection, in ssd_dims_t.flags (low 4 bits). */
@@ -112,6 +113,36 @@ ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *
                                const float *A_log, const void *B, const void *C,
                                const float *D, const float *init_state, void *y,
                                float *final_state, const ssd_dims_t *dims, void *stream);
+
+/*
+ * ssd_scan_fwd_noalloc -- ssd_scan_fwd on the chunked path without any
+ * device-memory allocation.
+ *
+ * No counterpart in the paper: an engineering variant for callers that cannot
+ * let a library allocate device memory during a call (a process that reserves
+ * the device up front in an arena of its own, or a driver or virtualised
+ * device without stream-ordered memory pools).
+ *
+ * Arguments, layouts and ownership as ssd_scan_fwd.  Runs the same chunked
+ * tcgen05 kernel with its scratch in a fixed 32 MiB array that the library
+ * module holds per device, whose address is looked up once per device.  The
+ * call calls no allocator.
+ * Errors as ssd_scan_fwd, plus:
+ *   SSD_ERR_UNSUPPORTED    the chunked path does not support these dims, or
+ *                          SSD_PATH_SEQUENTIAL was requested in dims->flags;
+ *   SSD_ERR_SCRATCH_LIMIT  the kernel would need more than 32 MiB of scratch
+ *                          (about 500 batch-row x head-pair chains when chains
+ *                          are split); nothing is enqueued;
+ *   SSD_ERR_CUDA           the array's address could not be obtained.
+ * Concurrency: the array is shared by all calls on a device.  Calls whose
+ * kernels may overlap in time on one device (different streams, or threads
+ * without ordering between them) race on it and give wrong results or time
+ * out; calls ordered on one stream are safe.
+ */
+ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const float *dt_bias,
+                                  const float *A_log, const void *B, const void *C,
+                                  const float *D, const float *init_state, void *y,
+                                  float *final_state, const ssd_dims_t *dims, void *stream);
 
 /* Which path SSD_PATH_AUTO resolves to for these dims on the current device
  * (SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED), or -(ssd_status_t) if the dims are

@@ -204,6 +204,53 @@ ssd_status_t validate(const void *x, const float *dt_raw, const float *dt_bias, 
     return SSD_OK;
 }
 
+// ---- allocation-free variant of the chunked path ------------------------
+//
+// Some callers cannot let a library allocate device memory during a call:
+// processes that reserve the whole device up front in an arena of their own
+// (a serving stack that sizes weights, caches and activations at start-up)
+// leave a library pool nothing to grow into, so a first-call allocation fails
+// with out-of-memory; and drivers or virtualised devices without stream-ordered
+// memory pools (cudaDevAttrMemoryPoolsSupported == 0) cannot serve
+// cudaMallocFromPoolAsync at all.  For them ssd_scan_fwd_noalloc runs the
+// chunked kernel with its scratch (abort word, handoff flags, chunk-handoff
+// states) in this fixed module-scope array instead of a pool allocation.
+//
+// Limit: 32 MiB.  The kernel needs 256 B for the abort word, 64 B of flags
+// per unit, and, when a batch-row x head-pair chain is split into several
+// units, 64 KiB of handoff state per chain: about 20 MiB for batch 8 x 80
+// heads at L = 4096, so roughly 500 split chains fit.  Larger needs are
+// rejected with SSD_ERR_SCRATCH_LIMIT before anything is enqueued.
+//
+// Nothing in the array has to start at zero: every flag and the abort word
+// are compared against a per-call tag that is never zero and never repeats
+// within a process, so values left by an earlier call never match.
+//
+// The array is one per device and shared by every call: two calls whose
+// kernels overlap in time on the same device (different streams, or threads
+// without ordering between them) race on it and give wrong results or
+// time out.  Calls ordered on one stream are safe.
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (with that device current) and cached; null on failure.
+void *noalloc_scratch(int dev)
+{
+    static std::mutex mu;
+    static void *addr[64] = {};
+    if (dev < 0 || dev >= 64)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return nullptr;
+        addr[dev] = p;
+    }
+    return addr[dev];
+}
+
 }  // namespace
 
 void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
@@ -311,6 +358,36 @@ ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *
     return rs;
 }
 
+ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const float *dt_bias,
+                                  const float *A_log, const void *B, const void *C,
+                                  const float *D, const float *init_state, void *y,
+                                  float *final_state, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    // empty work: ssd_scan_fwd launches nothing and allocates nothing here
+    if (dims->batch == 0 || dims->seqlen == 0)
+        return ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims,
+                            stream);
+    if ((dims->flags & SSD_PATH_MASK) == SSD_PATH_SEQUENTIAL)
+        return SSD_ERR_UNSUPPORTED;
+    const ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
+    const int32_t path = resolve_path(a, SSD_PATH_CHUNKED, true);
+    if (path < 0)
+        return (ssd_status_t)(-path);
+    if (chunk_workspace_bytes(a) > kNoAllocScratchBytes)
+        return SSD_ERR_SCRATCH_LIMIT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    void *ws = noalloc_scratch(dev);
+    if (!ws)
+        return SSD_ERR_CUDA;
+    return chunk_launch(a, ws, static_cast<cudaStream_t>(stream));
+}
+
 int32_t ssd_select_path(const ssd_dims_t *dims)
 {
     Sizes sz;
@@ -356,6 +433,7 @@ const char *ssd_status_string(int32_t status)
     case SSD_ERR_CUDA: return "CUDA call failed";
     case SSD_ERR_TIMEOUT: return "kernel exceeded a bounded wait";
     case SSD_ERR_ALIASING: return "output overlaps an input";
+    case SSD_ERR_SCRATCH_LIMIT: return "scratch needed exceeds the fixed no-allocation array";
     default: return "unknown status";
     }
 }

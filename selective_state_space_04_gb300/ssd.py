@@ -22,7 +22,8 @@ DTYPE_F32 = 0
 DTYPE_BF16 = 1
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_DIMS", 2: "SSD_ERR_NULL_PTR", 3: "SSD_ERR_MISALIGNED",
-          4: "SSD_ERR_UNSUPPORTED", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_TIMEOUT", 7: "SSD_ERR_ALIASING"}
+          4: "SSD_ERR_UNSUPPORTED", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_TIMEOUT", 7: "SSD_ERR_ALIASING",
+          8: "SSD_ERR_SCRATCH_LIMIT"}
 
 
 class SsdError(RuntimeError):
@@ -46,7 +47,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     vp, fp = ctypes.c_void_p, ctypes.c_void_p
     sig = [vp, fp, fp, fp, vp, vp, fp, fp, vp, fp, ctypes.POINTER(SsdDims), vp]
-    for name in ("ssd_scan_fwd", "ssd_scan_fwd_host"):
+    for name in ("ssd_scan_fwd", "ssd_scan_fwd_host", "ssd_scan_fwd_noalloc"):
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = sig
@@ -173,4 +174,31 @@ def ssd_scan_fwd_host(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, ch
                                       _ptr(final_state), ctypes.byref(d),
                                       ctypes.c_void_p(st.cuda_stream)),
                "ssd_scan_fwd_host")
+    return y, final_state
+
+
+def ssd_scan_fwd_noalloc(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
+                         path="auto", y=None, final_state=None, return_final_state=True,
+                         stream=None):
+    """``ssd_scan_fwd`` on the chunked path with the library's fixed scratch
+    array instead of a pool allocation (the library allocates nothing; outputs
+    not passed in are created here by torch).  Calls that may overlap on one
+    device share that array and race; calls ordered on one stream are safe."""
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        Bt, L, H, P = x.shape
+        final_state = torch.empty((Bt, H, P, B.shape[3]), dtype=torch.float32, device=x.device)
+    for name, t in (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log),
+                    ("B", B), ("C", C), ("D", D), ("init_state", init_state), ("y", y),
+                    ("final_state", final_state)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    d = _dims_from(x, B, chunk, path)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    _check(_lib.ssd_scan_fwd_noalloc(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B),
+                                     _ptr(C), _ptr(D), _ptr(init_state), _ptr(y),
+                                     _ptr(final_state), ctypes.byref(d),
+                                     ctypes.c_void_p(st.cuda_stream)),
+           "ssd_scan_fwd_noalloc")
     return y, final_state

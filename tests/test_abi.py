@@ -42,7 +42,7 @@ def test_every_declared_symbol_is_exported(libssd):
 def test_abi_version_and_status_strings(libssd):
     lib = libssd.lib()
     assert lib.ssd_abi_version() == 1
-    for code in range(8):
+    for code in range(9):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
     assert lib.ssd_status_string(99) == b"unknown status"

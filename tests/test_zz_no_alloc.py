@@ -1,0 +1,66 @@
+"""GPU check of ssd_scan_fwd_noalloc, the allocation-free variant of the
+chunked path that keeps its scratch in a fixed module-scope array.
+
+Two consecutive calls (the second finds the first call's flags and handoff
+states still in the array) must match ssd_scan_fwd, which takes its scratch
+from a pool, exactly: both run the same kernel with the same schedule.  The
+batch 4 x 80 heads x 2048 steps case splits every chain into several units,
+so the handoff states in the array are used.  A request above the array's
+32 MiB is rejected before anything is enqueued.
+"""
+import pytest
+import torch
+
+from selective_state_space_04_gb300.inputs import WORKLOADS, make_inputs
+
+pytestmark = pytest.mark.gpu
+
+SCRATCH_LIMIT = 8
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd as mod
+    return mod
+
+
+def _dev(seed, init):
+    w = WORKLOADS["mamba2_2p7b_layer"].with_(batch=4, seqlen=2048, init_state=init)
+    inp = make_inputs(w, seed)
+    return {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
+
+
+def _args(d):
+    return (d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"], d["init_state"])
+
+
+def test_two_consecutive_calls_match_pool_path(ssd):
+    for seed, init in ((11, False), (12, True)):
+        d = _dev(seed, init)
+        y_ref, f_ref = ssd.ssd_scan_fwd(*_args(d), chunk=256)
+        y_na, f_na = ssd.ssd_scan_fwd_noalloc(*_args(d), chunk=256)
+        torch.cuda.synchronize()
+        assert ssd.device_error() == 0
+        assert torch.isfinite(y_na.float()).all()
+        assert torch.equal(y_na, y_ref), f"seed {seed}: y differs"
+        assert torch.equal(f_na, f_ref), f"seed {seed}: final state differs"
+
+
+def test_oversize_request_rejected(ssd):
+    # batch 16 x 80 heads x 4096 steps: 640 split chains need 40 MiB of handoff state
+    Bt, L, H, P, G, N = 16, 4096, 80, 64, 1, 128
+    dev = torch.device("cuda")
+    x = torch.zeros((Bt, L, H, P), dtype=torch.bfloat16, device=dev)
+    dt = torch.zeros((Bt, L, H), dtype=torch.float32, device=dev)
+    par = torch.zeros((H,), dtype=torch.float32, device=dev)
+    Bm = torch.zeros((Bt, L, G, N), dtype=torch.bfloat16, device=dev)
+    Cm = torch.zeros_like(Bm)
+    before = ssd.launch_count()
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_scan_fwd_noalloc(x, dt, par, par, Bm, Cm, par, chunk=256)
+    assert e.value.status == SCRATCH_LIMIT
+    assert ssd.launch_count() == before
