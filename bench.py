@@ -76,12 +76,15 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+KERNEL_SOURCES = ("ssd_chunk.cu", "ptx.cuh", "tmap.h")
+
+
 def source_digest() -> str:
-    """Digest of the kernel sources, to tell whether stored ncu counters still
-    describe the kernel that runs."""
+    """Digest of the chunked kernel's sources, to tell whether stored ncu
+    counters still describe the kernel that runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_04_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -190,27 +193,63 @@ def max_over_ranks(dist, value: float, device) -> float:
 
 
 # ------------------------------------------------------------ CPU oracle
-def cpu_oracle_sample(w: Workload, inp: dict, budget_pairs: int | None = None):
-    """Times the fp64 oracle on a bounded sample of the workload: the first
-    `budget_pairs` (batch, head) chains, full sequence length each.  Returns
-    (tokens*heads per second, cores, description)."""
+def oracle_sample(w: Workload, inp: dict, nb: int, hp: int, ls: int) -> dict:
+    """fp64 inputs for a sample of the workload: the first `nb` batch rows, the
+    first `hp` heads (all heads, or heads of group 0 only when fewer) and the
+    first `ls` steps."""
+    if hp >= w.nheads:
+        hs, gs = slice(None), slice(None)
+    else:
+        hp = min(hp, w.nheads // w.ngroups)
+        hs, gs = slice(0, hp), slice(0, 1)
+    cut = {"x": (slice(0, nb), slice(0, ls), hs), "dt_raw": (slice(0, nb), slice(0, ls), hs),
+           "B": (slice(0, nb), slice(0, ls), gs), "C": (slice(0, nb), slice(0, ls), gs),
+           "init_state": (slice(0, nb), hs), "dt_bias": (hs,), "A_log": (hs,), "D": (hs,)}
+    return {k: (None if v is None else v[cut[k]].double().numpy()) for k, v in inp.items()}
+
+
+def size_oracle_sample(w: Workload, inp: dict, target_s: float):
+    """(nb, hp, ls) for an oracle run of about `target_s` seconds, from the
+    time of one calibration chain; the whole workload when that fits."""
     import oracle
-    H = w.nheads
-    if budget_pairs is None:
-        # about 10-30 s of host work: roughly 4*N*P flop per token*head in fp64
-        per_pair = 4.0 * w.dstate * w.headdim * w.seqlen
-        cores = oracle.max_threads()
-        budget_pairs = int(max(1, min(w.batch * H, cores * 2.5e9 * 4 / per_pair)))
-    b_rows = -(-budget_pairs // H)
-    nb = min(w.batch, b_rows)
-    sl = {k: (v[:nb] if (v is not None and k in ("x", "dt_raw", "B", "C", "init_state")) else v)
-          for k, v in inp.items()}
-    f64 = {k: (None if v is None else v.double().numpy()) for k, v in sl.items()}
+    cores = oracle.max_threads()
+    lc = min(w.seqlen, 512)
+    f64 = oracle_sample(w, inp, 1, 1, lc)
     t0 = time.perf_counter()
     oracle.ssd_fwd(**f64)
-    dt = time.perf_counter() - t0
-    th = nb * w.seqlen * H
-    return th / dt, oracle.max_threads(), f"{nb} of {w.batch} batch rows x all {H} heads x L={w.seqlen} ({th} token*heads) in {dt:.2f} s"
+    per_step = max((time.perf_counter() - t0) / lc, 1e-9)   # one chain, one thread
+    chains = w.batch * w.nheads
+    full = -(-chains // cores) * w.seqlen * per_step
+    if full <= target_s:
+        return w.batch, w.nheads, w.seqlen
+    ls = w.seqlen
+    fit = int(target_s / (ls * per_step)) * cores          # chains that fit at full length
+    if fit < 1:
+        return 1, 1, max(16, min(w.seqlen, int(target_s / per_step)))
+    if fit >= w.nheads:
+        return min(w.batch, fit // w.nheads), w.nheads, ls
+    return 1, min(fit, w.nheads // w.ngroups), ls
+
+
+def cpu_oracle_sample(w: Workload, inp: dict, shape, min_seconds: float = 0.0):
+    """Times the fp64 oracle on the sample `shape` = (nb, hp, ls), repeated
+    until `min_seconds` have passed.  Returns (tokens*heads per second, cores,
+    description)."""
+    import oracle
+    nb, hp, ls = shape
+    f64 = oracle_sample(w, inp, nb, hp, ls)
+    hp = f64["x"].shape[2]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.ssd_fwd(**f64)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    th = nb * ls * hp
+    return (th * reps / dt, oracle.max_threads(),
+            f"{nb} of {w.batch} batch rows x {hp} of {w.nheads} heads x {ls} of {w.seqlen} steps "
+            f"({th} token*heads), {reps} run(s) in {dt:.2f} s")
 
 
 # ------------------------------------------------------------ GPU arm
@@ -349,7 +388,8 @@ def run_gpu(args, w: Workload):
         "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
-        v, cores, sample = cpu_oracle_sample(w, inp)
+        shape = size_oracle_sample(w, inp, 10.0)
+        v, cores, sample = cpu_oracle_sample(w, inp, shape, min_seconds=10.0)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
                                 "sample": sample}
     print(json.dumps(line), flush=True)
@@ -360,19 +400,19 @@ def run_reference(args, w: Workload):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    import oracle
     inp = make_inputs(w, seed=args.seed)
-    cores = oracle.max_threads()
-    per_pair = 4.0 * w.dstate * w.headdim * w.seqlen
-    # each step: a bounded sample sized for ~5 s of host work
-    pairs = int(max(1, min(w.batch * w.nheads, cores * 2.5e9 * 2 / per_pair)))
+    # each step is one oracle run on a sample sized so that the whole run
+    # (warm-up and timed steps) takes about two minutes of host time
+    per_step_s = min(10.0, max(0.02, 120.0 / (args.steps + args.warmup)))
+    shape = size_oracle_sample(w, inp, per_step_s)
     for _ in range(args.warmup):
-        cpu_oracle_sample(w, inp, budget_pairs=pairs)
-    times, th_total, sample = 0.0, 0, ""
+        cpu_oracle_sample(w, inp, shape)
+    times, th_total, sample, cores = 0.0, 0, "", 0
     for _ in range(args.steps):
-        v, cores, sample = cpu_oracle_sample(w, inp, budget_pairs=pairs)
-        nb = min(w.batch, -(-pairs // w.nheads))
-        th = nb * w.seqlen * w.nheads
+        v, cores, sample = cpu_oracle_sample(w, inp, shape)
+        th = shape[0] * min(shape[1], w.nheads) * shape[2]
+        if shape[1] < w.nheads:
+            th = shape[0] * min(shape[1], w.nheads // w.ngroups) * shape[2]
         times += th / v
         th_total += th
     value = th_total / times
