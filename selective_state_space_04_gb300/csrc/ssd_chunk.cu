@@ -133,7 +133,7 @@ struct ChunkParams {
 };
 
 struct Maps {
-    CUtensorMap x, B, C;   // C boxes are 8 steps high (rows placed in row_step order)
+    CUtensorMap x, B, C;
     CUtensorMap y;         // store boxes of 64 steps x 64 channels
 };
 
@@ -283,18 +283,6 @@ __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c)
     return r * 128u + ((c ^ (r & 7u)) << 4);
 }
 
-// Row order of the C tile (and so of S, M, Y_diag and Y_off in tensor memory):
-// TMEM lane quarter q holds the 8-step groups {q, 7-q, 8+q, 15-q} of the
-// sub-chunk, so that every quarter (which only its own SM sub-partition can
-// access) gets the same share of the causal triangle.  Lane r holds step
-// row_step(r).
-__device__ __forceinline__ int row_step(int r)
-{
-    const int gi = r >> 3, q = gi >> 2, k = gi & 3;
-    const int grp = k == 0 ? q : (k == 1 ? 7 - q : (k == 2 ? 8 + q : 15 - q));
-    return (grp << 3) | (r & 7);
-}
-
 __device__ __forceinline__ uint4 pack8(const uint32_t *v)
 {
     uint4 o;
@@ -305,68 +293,86 @@ __device__ __forceinline__ uint4 pack8(const uint32_t *v)
     return o;
 }
 
-// One 16-column group of M for both heads, from S values sv[0..15]
-// (columns s = s0 .. s0+15 of the row of step t; s0 is a multiple of 16).
-// Writes 8 packed bf16 pairs per head.  Decay exp(cs_t - cs_s) dt_s for s <= t:
-//   * s in an earlier 16-step group than t: the row factor exp(cs_t - cs_e)
-//     times the column factor colf[s] = exp(cs_e - cs_s) dt_s (e = last step of
-//     s's group), both <= 1;
-//   * s in t's own group: evaluated directly;
-// and D_h is added on the diagonal.
-__device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8],
-                                            int s0, int t, const float *cs2, const float *dtv,
-                                            const float *colf, float D0, float D1)
+__device__ __forceinline__ uint32_t pack_pair(uint64_t v)
 {
-    const int G = s0 >> 4, tg = t >> 4;
-    if (G > tg) {
+    float lo, hi;
+    f32x2_split(v, lo, hi);
+    return pack_bf16x2(lo, hi);
+}
+
+// Largest decay span (log2 units) of one 16-step group for which the factored
+// form below is used inside the group; beyond it the direct form is.
+constexpr float kSpanMax = 64.f;
+
+// One 16-column group of M for both heads: columns s0 .. s0+15 of row t, from
+// the S values sv[0..15], as 8 packed bf16 pairs per head.
+//   M[t,s] = S[t,s] exp(cs_t - cs_s) dt_s  (s <= t, else 0),   M[t,t] += D
+// is evaluated as S[t,s] rf colf[s] with the row factor rf = exp(cs_t - cs_e)
+// and the column factor colf[s] = exp(cs_e - cs_s) dt_s, e = s0 + 15 the
+// group's last step (the caller passes rf and colf + s0).  For rows below the
+// group both factors are <= 1.  For a row inside the group rf >= 1 is at most
+// exp(span of the group) and colf >= exp(-span) dt, so the product is exact to
+// rounding while the span stays below kSpanMax (checked by the caller).
+// kMask: some rows are inside or above the group (k = t - s0 < 15): entries
+// with s > t are zeroed and D lands on s == t.
+template <bool kMask>
+__device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8], int k,
+                                            float rf0, float rf1, const float *colf, float D0, float D1)
+{
+    const uint64_t r0 = f32x2(rf0, rf0), r1 = f32x2(rf1, rf1);
+    const uint64_t dd0 = f32x2(D0, D0), dd1 = f32x2(D1, D1);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            m0[i] = 0u;
-            m1[i] = 0u;
-        }
-    } else if (G < tg) {
-        const float rf0 = ex2_approx(cs2[t] - cs2[s0 + 15]);
-        const float rf1 = ex2_approx(cs2[kT + t] - cs2[kT + s0 + 15]);
+    for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 c0 = *reinterpret_cast<const float4 *>(colf + 4 * i4);
+        const float4 c1 = *reinterpret_cast<const float4 *>(colf + kT + 4 * i4);
+        const uint64_t rc0[2] = {mul_f32x2(r0, f32x2(c0.x, c0.y)), mul_f32x2(r0, f32x2(c0.z, c0.w))};
+        const uint64_t rc1[2] = {mul_f32x2(r1, f32x2(c1.x, c1.y)), mul_f32x2(r1, f32x2(c1.z, c1.w))};
 #pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-            const int s = s0 + 4 * i4;
-            const float4 c0 = *reinterpret_cast<const float4 *>(colf + s);
-            const float4 c1 = *reinterpret_cast<const float4 *>(colf + kT + s);
-            const float a0 = __uint_as_float(sv[4 * i4 + 0]), a1 = __uint_as_float(sv[4 * i4 + 1]);
-            const float a2 = __uint_as_float(sv[4 * i4 + 2]), a3 = __uint_as_float(sv[4 * i4 + 3]);
-            m0[2 * i4 + 0] = pack_bf16x2(a0 * rf0 * c0.x, a1 * rf0 * c0.y);
-            m0[2 * i4 + 1] = pack_bf16x2(a2 * rf0 * c0.z, a3 * rf0 * c0.w);
-            m1[2 * i4 + 0] = pack_bf16x2(a0 * rf1 * c1.x, a1 * rf1 * c1.y);
-            m1[2 * i4 + 1] = pack_bf16x2(a2 * rf1 * c1.z, a3 * rf1 * c1.w);
-        }
-    } else {
-        const float cr0 = cs2[t], cr1 = cs2[kT + t];
-#pragma unroll
-        for (int i4 = 0; i4 < 4; ++i4) {
-            const int s = s0 + 4 * i4;
-            const float4 q0 = *reinterpret_cast<const float4 *>(cs2 + s);
-            const float4 d0 = *reinterpret_cast<const float4 *>(dtv + s);
-            const float4 q1 = *reinterpret_cast<const float4 *>(cs2 + kT + s);
-            const float4 d1 = *reinterpret_cast<const float4 *>(dtv + kT + s);
-            const float qa0[4] = {q0.x, q0.y, q0.z, q0.w}, da0[4] = {d0.x, d0.y, d0.z, d0.w};
-            const float qa1[4] = {q1.x, q1.y, q1.z, q1.w}, da1[4] = {d1.x, d1.y, d1.z, d1.w};
-            float e0[4], e1[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float sv_e = __uint_as_float(sv[4 * i4 + e]);
-                const bool keep = (s + e) <= t;
-                e0[e] = keep ? sv_e * ex2_approx(cr0 - qa0[e]) * da0[e] : 0.f;
-                e1[e] = keep ? sv_e * ex2_approx(cr1 - qa1[e]) * da1[e] : 0.f;
-                if (s + e == t) {
-                    e0[e] += D0;
-                    e1[e] += D1;
-                }
+        for (int e = 0; e < 2; ++e) {
+            const int i = 4 * i4 + 2 * e;   // columns s0+i, s0+i+1
+            float a = __uint_as_float(sv[i]), b = __uint_as_float(sv[i + 1]);
+            if (kMask) {
+                a = i <= k ? a : 0.f;
+                b = i + 1 <= k ? b : 0.f;
             }
-            m0[2 * i4 + 0] = pack_bf16x2(e0[0], e0[1]);
-            m0[2 * i4 + 1] = pack_bf16x2(e0[2], e0[3]);
-            m1[2 * i4 + 0] = pack_bf16x2(e1[0], e1[1]);
-            m1[2 * i4 + 1] = pack_bf16x2(e1[2], e1[3]);
+            const uint64_t ab = f32x2(a, b);
+            uint64_t v0 = mul_f32x2(ab, rc0[e]);
+            uint64_t v1 = mul_f32x2(ab, rc1[e]);
+            if (kMask) {
+                const uint64_t ind = f32x2(i == k ? 1.f : 0.f, i + 1 == k ? 1.f : 0.f);
+                v0 = fma_f32x2(ind, dd0, v0);
+                v1 = fma_f32x2(ind, dd1, v1);
+            }
+            m0[2 * i4 + e] = pack_pair(v0);
+            m1[2 * i4 + e] = pack_pair(v1);
         }
+    }
+}
+
+// The same group in the direct form exp(cs_t - cs_s) dt_s per entry, for a
+// group whose decay span is too large for the factored form.
+__device__ __forceinline__ void build_group_direct(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8],
+                                                   int s0, int t, const float *cs2, const float *dtv, float D0,
+                                                   float D1)
+{
+    const float cr0 = cs2[t], cr1 = cs2[kT + t];
+#pragma unroll
+    for (int i = 0; i < 16; i += 2) {
+        float e0[2], e1[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int s = s0 + i + u;
+            const float v = __uint_as_float(sv[i + u]);
+            const bool keep = s <= t;
+            e0[u] = keep ? v * ex2_approx(cr0 - cs2[s]) * dtv[s] : 0.f;
+            e1[u] = keep ? v * ex2_approx(cr1 - cs2[kT + s]) * dtv[kT + s] : 0.f;
+            if (s == t) {
+                e0[u] += D0;
+                e1[u] += D1;
+            }
+        }
+        m0[i >> 1] = pack_bf16x2(e0[0], e0[1]);
+        m1[i >> 1] = pack_bf16x2(e1[0], e1[1]);
     }
 }
 
@@ -463,12 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
                 const int gc = cur.w.g * kN;
                 mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
-                for (int gi = 0; gi < 16; ++gi) {
-                    const int ts = t0 + row_step(gi << 3);   // first step of the group placed at rows 8gi..
-                    tma_load_3d(bc + gi * 1024, &maps.C, &bars[BAR_BC_FULL + s], gc, ts, cur.w.b, pol_keep);
-                    tma_load_3d(bc + kTileBytes + gi * 1024, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, ts, cur.w.b,
-                                pol_keep);
-                }
+                tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
+                tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
                 last_bc[s] = (int)j;
@@ -551,24 +553,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mma_ts(tmem + kColYd + 64 * h, tmem + kColSM + 16 * kk + 8 * h,
                                sdesc_sw128(xs + h * kTileBytes + kk * 2048, kTileBytes, 1024), id_Yd, kk > 0);
                 mma_commit(&bars[BAR_YD_DONE]);
-                // Y_off = C P   (P as bf16 in the other x stage)
-                if (!(ok = wait_bar(&bars[BAR_PB_READY], par, p)))
-                    break;
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                    mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024),
-                           sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
-                }
-                mma_commit(&bars[BAR_YOFF_DONE]);
-                mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
-                // S of the next sub-chunk, in place of M (after Y_diag has read M)
-                if (has_next) {
-                    if (!(ok = wait_bar(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1, p)) ||
-                        !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
+                // Y_off(j) = C P (P as bf16 in the other x stage) and S(j+1), in place of
+                // M once Y_diag has read it: whichever is ready first goes first, S first
+                // when both are (the next M build waits on it)
+                {
+                    bool yo_done = false, s_done = !has_next;
+                    const uint64_t tw = globaltimer_ns();
+                    uint32_t spins = 0;
+                    while (!(yo_done && s_done)) {
+                        bool progressed = false;
+                        if (!s_done && mbar_poll(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1) &&
+                            mbar_poll(&bars[BAR_YD_DONE], par)) {
+                            tc_fence_after();
+                            issue_S(s ^ 1);
+                            s_done = progressed = true;
+                        }
+                        if (!yo_done && mbar_poll(&bars[BAR_PB_READY], par)) {
+                            tc_fence_after();
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+                                mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024),
+                                       sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
+                            }
+                            mma_commit(&bars[BAR_YOFF_DONE]);
+                            mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
+                            yo_done = progressed = true;
+                        }
+                        if (!progressed) {
+                            __nanosleep(32);
+                            if ((++spins & 255u) == 0) {
+                                if (aborted(p)) {
+                                    ok = false;
+                                    break;
+                                }
+                                if (globaltimer_ns() - tw > p.timeout_ns) {
+                                    raise_timeout(p);
+                                    ok = false;
+                                    break;
+                                }
+                            }
+                        }
+                    }
+                    if (!ok)
                         break;
-                    tc_fence_after();
-                    issue_S(s ^ 1);
                 }
                 // P += B^T (w o x)   (P already rescaled by the state group)
                 if (!(ok = wait_bar(&bars[BAR_XS_READY], par, p)))
@@ -593,9 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ decay group
         // per sub-chunk j: dt and the local cumulative sum of dt*A (thread: step r,
         // head hd), decay factors for both groups, then M from S (thread: row r,
-        // s-half hd, both heads)
+        // both heads)
         const int q = warp & 3;        // TMEM lane quarter
-        const int hd = warp >> 2;      // head (decay) / s-half (M)
+        const int hd = warp >> 2;      // head (decay) / column-group parity (M)
         const int r = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         uint32_t msync = 0;
@@ -646,21 +673,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dtot[hd] = ex2_approx(tot);                   // state decay over the sub-chunk
             if (!group_sync(&bars[BAR_MSYNC], msync, p))
                 break;
-            // ---- M from S, in place, 16 columns at a time (row r, s-half hd, both heads)
+            // ---- M from S, in place, 16 columns at a time (row r, both heads).  The
+            //      rows 32q .. 32q+31 of this lane quarter lie below every column
+            //      group G < 2q, hold the diagonal in G = 2q, 2q+1 and lie above
+            //      G > 2q+1 (M = 0 there); the quarter's two warps take alternate groups.
             if (!wait_bar(&bars[BAR_S_DONE], j & 1, p))
                 break;
             tc_fence_after();
             {
                 const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
-                const int t_row = row_step(r);
+                const float ct0 = cs2[r], ct1 = cs2[kT + r];
 #pragma unroll 1
-                for (int g = 0; g < 4; ++g) {
-                    const int s0 = 64 * hd + 16 * g;
-                    const uint32_t ta = tmem + lane_addr + kColSM + s0;
-                    uint32_t sv[16], m0[8], m1[8];
-                    tmem_ld16(ta, sv);
-                    tmem_wait_ld();
-                    build_group(sv, m0, m1, s0, t_row, cs2, dtv, colf, D0, D1);
+                for (int G = hd; G < 8; G += 2) {
+                    const uint32_t ta = tmem + lane_addr + kColSM + 16 * G;
+                    uint32_t m0[8], m1[8];
+                    if (G > 2 * q + 1) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            m0[i] = 0u;
+                            m1[i] = 0u;
+                        }
+                    } else {
+                        const int s0 = 16 * G;
+                        uint32_t sv[16];
+                        tmem_ld16(ta, sv);
+                        const float e0 = cs2[s0 + 15], e1 = cs2[kT + s0 + 15];
+                        const float rf0 = ex2_approx(fminf(ct0 - e0, kSpanMax));
+                        const float rf1 = ex2_approx(fminf(ct1 - e1, kSpanMax));
+                        tmem_wait_ld();
+                        if (G < 2 * q)
+                            build_group<false>(sv, m0, m1, 0, rf0, rf1, colf + s0, 0.f, 0.f);
+                        else if (cs2[s0] - e0 <= kSpanMax && cs2[kT + s0] - e1 <= kSpanMax)
+                            build_group<true>(sv, m0, m1, r - s0, rf0, rf1, colf + s0, D0, D1);
+                        else
+                            build_group_direct(sv, m0, m1, s0, r, cs2, dtv, D0, D1);
+                    }
                     tmem_st8(ta, m0);
                     tmem_st8(ta + 8, m1);
                 }
@@ -747,8 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             const float *dk = decay_base + (j % 3) * kDecayFloats;
-            const int t_row = row_step(r);                 // step held by TMEM lane r in Y
-            const float ecs = dk[6 * kT + hf * kT + t_row];
+            const float ecs = dk[6 * kT + hf * kT + r];
             const float wsc = dk[8 * kT + hf * kT + r];
             const float dtot = dk[10 * kT + hf];
             {
@@ -780,7 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             warp_arrive(&bars[BAR_XS_READY]);
-            // ---- y = Y_diag + exp(cs_t) Y_off   (TMEM lane r = step t_row, head hf), staged
+            // ---- y = Y_diag + exp(cs_t) Y_off   (TMEM lane r = step r, head hf), staged
             //      in the C area of this sub-chunk's B/C stage (C is dead after Y_off) for the
             //      producer's TMA store
             if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
@@ -807,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ov[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
                                                 fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
                         }
-                        *reinterpret_cast<uint4 *>(stg + sw128(t_row, 4 * half + c8)) = o;
+                        *reinterpret_cast<uint4 *>(stg + sw128(r, 4 * half + c8)) = o;
                     }
                 }
                 fence_proxy_async_smem();
@@ -984,7 +1030,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
     if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
-        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 8) ||
+        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.y, a.y, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 64))
         return SSD_ERR_CUDA;
     ChunkParams p;
