@@ -31,6 +31,7 @@
 //   warps 8-15  state group: w-scaling of x, state rescale, output epilogue,
 //               state handoff between units
 //   warp 16     TMA producer: B/C tiles (2 stages), x tiles (2 stages)
+//               (the state warps issue the TMA stores of y themselves)
 //   warp 17     tcgen05 MMA issuer (one lane) and TMEM owner
 // The decay group prepares sub-chunk j+1 while the state group finishes j.
 // Tensor memory (512 columns x 128 lanes, fp32):
@@ -111,7 +112,6 @@ enum {
     BAR_EPI_DONE,
     BAR_DRAIN,
     BAR_MSYNC,   // decay-group barrier (bounded, unlike bar.sync)
-    BAR_Y_STAGED,  // 2: y of sub-chunk j staged in shared memory (barrier j & 1)
 };
 
 struct ChunkParams {
@@ -134,7 +134,7 @@ struct ChunkParams {
 
 struct Maps {
     CUtensorMap x, B, C;
-    CUtensorMap y;         // store boxes of 64 steps x 64 channels
+    CUtensorMap y;         // store boxes of 32 steps x 64 channels
 };
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long *p)
@@ -401,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars[BAR_BC_FULL + i], 1);
-            mbar_init(&bars[BAR_BC_EMPTY + i], 1);
+            // the state MMA's commit (B read) and the state warps (their y stores have read the C area)
+            mbar_init(&bars[BAR_BC_EMPTY + i], 1 + kGroupWarps);
             mbar_init(&bars[BAR_X_FULL + i], 1);
             mbar_init(&bars[BAR_X_EMPTY + i], 1);
         }
@@ -415,8 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[BAR_EPI_DONE], kGroupWarps);
         mbar_init(&bars[BAR_DRAIN], 1);
         mbar_init(&bars[BAR_MSYNC], kGroupWarps);
-        mbar_init(&bars[BAR_Y_STAGED + 0], kGroupWarps);
-        mbar_init(&bars[BAR_Y_STAGED + 1], kGroupWarps);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -442,28 +441,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t j = 0;
             bool ok = true;
             int last_bc[2] = {-1, -1}, last_x[2] = {-1, -1};  // last sub-chunk loaded per stage
-            // y of sub-chunk jj is staged (by the state group) in the C area of its
-            // B/C stage; store it with TMA before that stage is reloaded
-            auto store_y = [&](const Cursor &c, uint32_t jj) -> bool {
-                if (!wait_bar(&bars[BAR_Y_STAGED + (jj & 1)], (jj >> 1) & 1, p))
-                    return false;
-                const uint8_t *stg = smem + kOffBC + (jj & 1) * kBCStageBytes;
-                const int ty = (int)c.t0();
-                const int nbox = c.valid() > 64 ? 2 : 1;
-                for (int h = 0; h < 2; ++h)
-                    for (int bx = 0; bx < nbox; ++bx)
-                        tma_store_3d(&maps.y, stg + h * kTileBytes + bx * (kTileBytes / 2), (c.w.h0 + h) * kP,
-                                     ty + 64 * bx, c.w.b);
-                bulk_commit_group();
-                bulk_wait_read_all();
-                return true;
-            };
-            Cursor cur, back1, back2;   // back1/back2: the previous two sub-chunks
+            Cursor cur;
             for (bool has = cursor_first(cur, p); has; has = cursor_next(cur, p), ++j) {
                 const int s = j & 1;
                 const int t0 = (int)cur.t0();
-                if (j >= 2 && !(ok = store_y(back2, j - 2)))
-                    break;
                 if (j >= 2 && !(ok = wait_bar(&bars[BAR_BC_EMPTY + s], ((j >> 1) + 1) & 1, p)))
                     break;
                 uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
@@ -482,15 +463,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(xs + kTileBytes, &maps.x, &bars[BAR_X_FULL + s], (cur.w.h0 + 1) * kP, t0, cur.w.b,
                             pol_stream);
                 last_x[s] = (int)j;
-                back2 = back1;
-                back1 = cur;
             }
-            // the last two sub-chunks' outputs
-            if (ok && j >= 2)
-                ok = store_y(back2, j - 2);
-            if (ok && j >= 1)
-                ok = store_y(back1, j - 1);
-            bulk_wait_all();
             if (!ok) {
                 // every load issued by this thread must land before the CTA exits
                 const uint64_t t0 = globaltimer_ns();
@@ -826,14 +799,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             warp_arrive(&bars[BAR_XS_READY]);
-            // ---- y = Y_diag + exp(cs_t) Y_off   (TMEM lane r = step r, head hf), staged
-            //      in the C area of this sub-chunk's B/C stage (C is dead after Y_off) for the
-            //      producer's TMA store
+            // ---- y = Y_diag + exp(cs_t) Y_off   (TMEM lane r = step r, head hf).  Each warp
+            //      stages its 32 rows in its own 4 KB of the C area of this sub-chunk's B/C
+            //      stage (C is dead after Y_off) and stores them with one TMA store; the
+            //      warp releases the C area once that store has read it
             if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
                 break;
             tc_fence_after();
             {
-                uint8_t *stg = smem + kOffBC + s * kBCStageBytes + hf * kTileBytes;
+                uint8_t *stg = smem + kOffBC + s * kBCStageBytes + sw * 4096;   // this warp's 32 rows
                 for (int half = 0; half < 2; ++half) {
                     uint32_t yd[32], yo[32];
                     tmem_ld32(tmem + lane_addr + kColYd + hf * 64 + 32 * half, yd);
@@ -853,11 +827,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             ov[e] = pack_bf16x2(fmaf(ecs, __uint_as_float(yo[i]), __uint_as_float(yd[i])),
                                                 fmaf(ecs, __uint_as_float(yo[i + 1]), __uint_as_float(yd[i + 1])));
                         }
-                        *reinterpret_cast<uint4 *>(stg + sw128(r, 4 * half + c8)) = o;
+                        *reinterpret_cast<uint4 *>(stg + sw128(lane, 4 * half + c8)) = o;
                     }
                 }
                 fence_proxy_async_smem();
-                warp_arrive(&bars[BAR_Y_STAGED + s]);
+                __syncwarp();
+                if (lane == 0 && 32 * q < cur.valid()) {
+                    tma_store_3d(&maps.y, stg, hh * kP, (int)cur.t0() + 32 * q, cur.w.b);
+                    bulk_commit_group();
+                }
             }
             // ---- carried state after sub-chunk j
             if (!(ok = wait_bar(&bars[BAR_STATE_DONE], par, p)))
@@ -913,9 +891,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bars[BAR_PB_READY]);
             }
+            if (lane == 0)
+                bulk_wait_read_all();
+            warp_arrive(&bars[BAR_BC_EMPTY + s]);
             cur = nxt;
             has = has_next;
         }
+        if (lane == 0)
+            bulk_wait_all();
     }
 
     tc_fence_before();
@@ -1031,7 +1014,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
-        !make_tmap_bf16_3d(&maps.y, a.y, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 64))
+        !make_tmap_bf16_3d(&maps.y, a.y, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 32))
         return SSD_ERR_CUDA;
     ChunkParams p;
     p.dt_raw = a.dt_raw;
