@@ -223,11 +223,13 @@ struct Unit {
     long long start;                   // first step
 };
 
+// (units number fewer than 2^31: 32-bit index arithmetic)
 __device__ __forceinline__ Unit decode_unit(long long u, const ChunkParams &p)
 {
     Unit w;
-    w.rg = (int)(u / p.nchains);
-    const int chain = (int)(u - (long long)w.rg * p.nchains);
+    const int ui = (int)u;
+    w.rg = ui / p.nchains;
+    const int chain = ui - w.rg * p.nchains;
     w.b = chain / p.nhp;
     w.hp = chain - w.b * p.nhp;
     w.h0 = 2 * w.hp;
@@ -350,11 +352,14 @@ __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (
 }
 
 // The same group in the direct form exp(cs_t - cs_s) dt_s per entry, for a
-// group whose decay span is too large for the factored form.
-__device__ __forceinline__ void build_group_direct(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8],
-                                                   int s0, int t, const float *cs2, const float *dtv, float D0,
-                                                   float D1)
+// group whose decay span is too large for the factored form (rare: kept out
+// of line; it reads S from and writes M to tensor memory at `ta` itself).
+__device__ __noinline__ void build_group_direct(uint32_t ta, int s0, int t, const float *cs2, const float *dtv,
+                                                float D0, float D1)
 {
+    uint32_t sv[16], m0[8], m1[8];
+    tmem_ld16(ta, sv);
+    tmem_wait_ld();
     const float cr0 = cs2[t], cr1 = cs2[kT + t];
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
@@ -374,6 +379,8 @@ __device__ __forceinline__ void build_group_direct(const uint32_t (&sv)[16], uin
         m0[i >> 1] = pack_bf16x2(e0[0], e0[1]);
         m1[i >> 1] = pack_bf16x2(e1[0], e1[1]);
     }
+    tmem_st8(ta, m0);
+    tmem_st8(ta + 8, m1);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -660,6 +667,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int G = hd; G < 8; G += 2) {
                     const uint32_t ta = tmem + lane_addr + kColSM + 16 * G;
                     uint32_t m0[8], m1[8];
+                    const int s0 = 16 * G;
+                    if (G <= 2 * q + 1 && G >= 2 * q &&
+                        !(cs2[s0] - cs2[s0 + 15] <= kSpanMax && cs2[kT + s0] - cs2[kT + s0 + 15] <= kSpanMax)) {
+                        build_group_direct(ta, s0, r, cs2, dtv, D0, D1);
+                        continue;
+                    }
                     if (G > 2 * q + 1) {
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
@@ -667,7 +680,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                             m1[i] = 0u;
                         }
                     } else {
-                        const int s0 = 16 * G;
                         uint32_t sv[16];
                         tmem_ld16(ta, sv);
                         const float e0 = cs2[s0 + 15], e1 = cs2[kT + s0 + 15];
@@ -676,10 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_ld();
                         if (G < 2 * q)
                             build_group<false>(sv, m0, m1, 0, rf0, rf1, colf + s0, 0.f, 0.f);
-                        else if (cs2[s0] - e0 <= kSpanMax && cs2[kT + s0] - e1 <= kSpanMax)
-                            build_group<true>(sv, m0, m1, r - s0, rf0, rf1, colf + s0, D0, D1);
                         else
-                            build_group_direct(sv, m0, m1, s0, r, cs2, dtv, D0, D1);
+                            build_group<true>(sv, m0, m1, r - s0, rf0, rf1, colf + s0, D0, D1);
                     }
                     tmem_st8(ta, m0);
                     tmem_st8(ta + 8, m1);
@@ -1000,6 +1010,10 @@ bool chunk_supported(const ScanArgs &a)
     if ((a.nheads / a.ngroups) % 2 != 0)
         return false;
     if (a.batch >= (1LL << 31) || a.seqlen >= (1LL << 31))
+        return false;
+    // work units (at most chunks x chains) are indexed with 32-bit arithmetic
+    const long long nchunks = (a.seqlen + a.chunk - 1) / a.chunk, nchains = a.batch * (a.nheads / 2);
+    if (nchains > 0 && nchunks > ((1LL << 31) - 1) / nchains)
         return false;
     return true;
 }
