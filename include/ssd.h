@@ -54,7 +54,8 @@ typedef enum ssd_status {
     SSD_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed; nothing further enqueued */
     SSD_ERR_TIMEOUT = 6,        /* a kernel gave up a bounded wait (read via ssd_get_device_error) */
     SSD_ERR_ALIASING = 7,       /* y overlaps an input, or the two states overlap partially */
-    SSD_ERR_SCRATCH_LIMIT = 8   /* ssd_scan_fwd_noalloc: scratch needed exceeds its fixed array */
+    SSD_ERR_SCRATCH_LIMIT = 8   /* the scratch needed exceeds the buffer the call may use (the fixed
+                                   array of ssd_scan_fwd_noalloc, the workspace of ssd_scan_fwd_ws) */
 } ssd_status_t;
 
 /* Kernel path selection, in ssd_dims_t.flags (low 4 bits). */
@@ -113,6 +114,39 @@ ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *
                                const float *A_log, const void *B, const void *C,
                                const float *D, const float *init_state, void *y,
                                float *final_state, const ssd_dims_t *dims, void *stream);
+
+/*
+ * ssd_scan_fwd_workspace_size -- bytes of scratch that ssd_scan_fwd_ws needs for
+ * these dims on the current device, in *bytes (0 when the call needs none:
+ * empty work or the sequential path).  The chunked path's scratch holds the
+ * chunk-unit handoff flags and, when a chain is split into several units,
+ * the handed-over states (the inter-chunk state passing of the chunked
+ * evaluation; @seanhogg/builderforce-memory-engine, dist/kernels/ssd.js, module
+ * header: chunked evaluation with a carried state).  The schedule, and so the
+ * size, depends on the device's SM count.  Host only; launches nothing.
+ * Returns SSD_OK, or an error for invalid or unsupported dims (as
+ * ssd_select_path), or SSD_ERR_NULL_PTR.
+ */
+ssd_status_t ssd_scan_fwd_workspace_size(const ssd_dims_t *dims, uint64_t *bytes);
+
+/*
+ * ssd_scan_fwd_ws -- ssd_scan_fwd with caller-provided scratch.
+ *
+ * Arguments as ssd_scan_fwd, plus `workspace`: a DEVICE buffer of
+ * `workspace_bytes` bytes, owned by the caller, 16-byte aligned, overlapping
+ * no other argument.  It must hold ssd_scan_fwd_workspace_size(dims) bytes
+ * (it may be NULL when that is 0); its contents on entry do not matter and
+ * are undefined afterwards.  The call allocates nothing.  Two calls whose
+ * kernels may overlap in time must not share a workspace.
+ * Errors as ssd_scan_fwd, plus SSD_ERR_SCRATCH_LIMIT when workspace_bytes is
+ * smaller than needed (nothing enqueued); a misaligned or overlapping
+ * workspace gives SSD_ERR_MISALIGNED or SSD_ERR_ALIASING before any CUDA call.
+ */
+ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt_bias,
+                             const float *A_log, const void *B, const void *C, const float *D,
+                             const float *init_state, void *y, float *final_state,
+                             void *workspace, uint64_t workspace_bytes, const ssd_dims_t *dims,
+                             void *stream);
 
 /*
  * ssd_scan_fwd_noalloc -- ssd_scan_fwd on the chunked path without any

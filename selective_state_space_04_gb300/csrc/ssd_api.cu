@@ -388,6 +388,65 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
     return chunk_launch(a, ws, static_cast<cudaStream_t>(stream));
 }
 
+ssd_status_t ssd_scan_fwd_workspace_size(const ssd_dims_t *dims, uint64_t *bytes)
+{
+    if (!bytes)
+        return SSD_ERR_NULL_PTR;
+    Sizes sz;
+    const ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    *bytes = 0;
+    if (dims->batch == 0 || dims->seqlen == 0)
+        return SSD_OK;
+    const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, dims);
+    const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
+    if (path < 0)
+        return (ssd_status_t)(-path);
+    if (path == SSD_PATH_CHUNKED)
+        *bytes = chunk_workspace_bytes(a);
+    return SSD_OK;
+}
+
+ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt_bias,
+                             const float *A_log, const void *B, const void *C, const float *D,
+                             const float *init_state, void *y, float *final_state, void *workspace,
+                             uint64_t workspace_bytes, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if (!aligned16(workspace))
+        return SSD_ERR_MISALIGNED;
+    if (workspace && workspace_bytes > 0) {
+        const void *args[] = {x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state};
+        const int64_t argb[] = {sz.x, sz.dt, sz.par, sz.par, sz.bc, sz.bc, sz.par, sz.state, sz.x, sz.state};
+        const int64_t wb = workspace_bytes > (uint64_t)INT64_MAX ? INT64_MAX : (int64_t)workspace_bytes;
+        for (int i = 0; i < 10; ++i)
+            if (overlaps(workspace, wb, args[i], argb[i]))
+                return SSD_ERR_ALIASING;
+    }
+    // empty work needs no scratch: ssd_scan_fwd allocates nothing here
+    if (dims->batch == 0 || dims->seqlen == 0)
+        return ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims,
+                            stream);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
+    const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
+    if (path < 0)
+        return (ssd_status_t)(-path);
+    if (path == SSD_PATH_SEQUENTIAL)
+        return seq_launch(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    const size_t need = chunk_workspace_bytes(a);
+    if (workspace_bytes < need)
+        return SSD_ERR_SCRATCH_LIMIT;
+    if (!workspace)
+        return SSD_ERR_NULL_PTR;
+    return chunk_launch(a, workspace, st);
+}
+
 int32_t ssd_select_path(const ssd_dims_t *dims)
 {
     Sizes sz;
@@ -433,7 +492,7 @@ const char *ssd_status_string(int32_t status)
     case SSD_ERR_CUDA: return "CUDA call failed";
     case SSD_ERR_TIMEOUT: return "kernel exceeded a bounded wait";
     case SSD_ERR_ALIASING: return "output overlaps an input";
-    case SSD_ERR_SCRATCH_LIMIT: return "scratch needed exceeds the fixed no-allocation array";
+    case SSD_ERR_SCRATCH_LIMIT: return "scratch needed exceeds the buffer the call may use";
     default: return "unknown status";
     }
 }

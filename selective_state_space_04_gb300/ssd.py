@@ -51,6 +51,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         f = getattr(lib, name)
         f.restype = ctypes.c_int
         f.argtypes = sig
+    lib.ssd_scan_fwd_ws.restype = ctypes.c_int
+    lib.ssd_scan_fwd_ws.argtypes = sig[:10] + [vp, ctypes.c_uint64, ctypes.POINTER(SsdDims), vp]
+    lib.ssd_scan_fwd_workspace_size.restype = ctypes.c_int
+    lib.ssd_scan_fwd_workspace_size.argtypes = [ctypes.POINTER(SsdDims), ctypes.POINTER(ctypes.c_uint64)]
     lib.ssd_select_path.restype = ctypes.c_int32
     lib.ssd_select_path.argtypes = [ctypes.POINTER(SsdDims)]
     lib.ssd_launches_per_call.restype = ctypes.c_int32
@@ -108,6 +112,15 @@ def launches_per_call(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto"
     Bt, L, H, P = x_shape
     d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
     return _lib.ssd_launches_per_call(ctypes.byref(d))
+
+
+def workspace_size(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+    """Bytes of scratch ``ssd_scan_fwd_ws`` needs for these sizes on the current device."""
+    Bt, L, H, P = x_shape
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    n = ctypes.c_uint64(0)
+    _check(_lib.ssd_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n)), "ssd_scan_fwd_workspace_size")
+    return int(n.value)
 
 
 def launch_count() -> int:
@@ -201,4 +214,32 @@ def ssd_scan_fwd_noalloc(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *,
                                      _ptr(final_state), ctypes.byref(d),
                                      ctypes.c_void_p(st.cuda_stream)),
            "ssd_scan_fwd_noalloc")
+    return y, final_state
+
+
+def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, workspace,
+                    chunk=256, path="auto", y=None, final_state=None, return_final_state=True,
+                    stream=None):
+    """``ssd_scan_fwd`` with caller-provided scratch: ``workspace`` is a CUDA
+    tensor of at least ``workspace_size(...)`` bytes (or None when that is 0).
+    The library allocates nothing; calls that may overlap must not share a
+    workspace."""
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_final_state:
+        Bt, L, H, P = x.shape
+        final_state = torch.empty((Bt, H, P, B.shape[3]), dtype=torch.float32, device=x.device)
+    for name, t in (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log),
+                    ("B", B), ("C", C), ("D", D), ("init_state", init_state), ("y", y),
+                    ("final_state", final_state), ("workspace", workspace)):
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    d = _dims_from(x, B, chunk, path)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    _check(_lib.ssd_scan_fwd_ws(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B), _ptr(C),
+                                _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state),
+                                _ptr(workspace), ctypes.c_uint64(nbytes), ctypes.byref(d),
+                                ctypes.c_void_p(st.cuda_stream)),
+           "ssd_scan_fwd_ws")
     return y, final_state

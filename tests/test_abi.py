@@ -120,3 +120,30 @@ def test_empty_work_launches_nothing(libssd):
     assert lib.ssd_launches_per_call(ctypes.byref(dims(libssd, seqlen=0))) == 0
     # batch == 0 is a no-op that returns OK without any device access
     assert call(libssd, dims(libssd, batch=0)) == 0
+
+
+def test_workspace_size_of_empty_and_sequential_work(libssd):
+    assert libssd.workspace_size((2, 0, 4, 64), 1, 128, 256) == 0
+    assert libssd.workspace_size((0, 64, 4, 64), 1, 128, 256) == 0
+    # fp32 always takes the sequential path, which needs no scratch
+    assert libssd.workspace_size((1, 64, 2, 8), 1, 16, 16, dtype="f32") == 0
+
+
+def test_workspace_size_rejects_bad_dims(libssd):
+    with pytest.raises(libssd.SsdError) as e:
+        libssd.workspace_size((1, 64, 3, 64), 2, 128, 256)    # H % G != 0
+    assert e.value.status == 1
+
+
+def _ws_call(libssd, ws, ws_bytes):
+    lib = libssd.lib()
+    d = libssd.make_dims(1, 64, 2, 64, 128, 1, 64, "bf16")
+    fake = ctypes.c_void_p(0x10000)
+    args = [fake] * 7 + [None, ctypes.c_void_p(0x90000000), None]
+    return lib.ssd_scan_fwd_ws(*args, ws, ctypes.c_uint64(ws_bytes), ctypes.byref(d), None)
+
+
+def test_workspace_misaligned_or_overlapping_rejected_before_cuda(libssd):
+    assert _ws_call(libssd, ctypes.c_void_p(0x20008), 4096) == 3   # SSD_ERR_MISALIGNED
+    # overlaps y at 0x90000000
+    assert _ws_call(libssd, ctypes.c_void_p(0x90000000 - 256), 4096) == 7   # SSD_ERR_ALIASING
