@@ -63,6 +63,13 @@ typedef enum ssd_status {
 #define SSD_PATH_SEQUENTIAL 1u  /* direct recurrence, fp32 FFMA (any P, N up to 2048; fp32 or bf16) */
 #define SSD_PATH_CHUNKED 2u     /* chunked tcgen05 path: bf16, P = 64, N = 128, Q % 64 == 0, (H/G) even */
 #define SSD_PATH_MASK 0xFu
+/* Diagnostic, in ssd_dims_t.flags: on the chunked path, the first unit of every
+ * chain waits for a state handoff that nothing publishes, with the bounded waits
+ * shortened to 20 ms.  The launch then records SSD_ERR_TIMEOUT (read with
+ * ssd_get_device_error), stops every warp, drains its own copies and MMAs and
+ * returns; y and final_state are undefined.  It exercises the failure path
+ * without faulting the GPU.  Ignored by the sequential path. */
+#define SSD_DIAG_STALL_HANDOFF 0x100u
 
 typedef struct ssd_dims {
     int64_t batch;     /* B >= 0 */
@@ -73,7 +80,7 @@ typedef struct ssd_dims {
     int32_t ngroups;   /* G >= 1, H % G == 0 */
     int32_t chunk;     /* Q >= 1: chunk length of the chunked evaluation (ignored by the sequential path) */
     int32_t dtype;     /* ssd_dtype_t of x, B, C and y */
-    uint32_t flags;    /* SSD_PATH_* */
+    uint32_t flags;    /* SSD_PATH_* | optional SSD_DIAG_STALL_HANDOFF */
     uint32_t reserved; /* must be 0 */
 } ssd_dims_t;
 

@@ -42,7 +42,7 @@ ssd_status_t check_dims(const ssd_dims_t *d, Sizes *sz)
     if (d->dtype != SSD_DTYPE_F32 && d->dtype != SSD_DTYPE_BF16)
         return SSD_ERR_UNSUPPORTED;
     const uint32_t path = d->flags & SSD_PATH_MASK;
-    if ((d->flags & ~SSD_PATH_MASK) != 0 || path > SSD_PATH_CHUNKED)
+    if ((d->flags & ~(SSD_PATH_MASK | SSD_DIAG_STALL_HANDOFF)) != 0 || path > SSD_PATH_CHUNKED)
         return SSD_ERR_INVALID_DIMS;
     int64_t bl, blh, t;
     const int64_t es = (int64_t)elem_size(d->dtype);
@@ -83,6 +83,7 @@ ScanArgs make_args(const void *x, const float *dt_raw, const float *dt_bias, con
     a.ngroups = d->ngroups;
     a.chunk = d->chunk;
     a.dtype = d->dtype;
+    a.diag_stall = (d->flags & SSD_DIAG_STALL_HANDOFF) != 0;
     return a;
 }
 

@@ -130,6 +130,7 @@ struct ChunkParams {
     long long L;
     long long nunits;
     int H, span, nranges, nhp, nchains, hpg;   // span = steps per unit (R*Q)
+    int diag_stall;                   // first units wait for a handoff nobody publishes
 };
 
 struct Maps {
@@ -728,6 +729,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t par = j & 1;
             const int hh = cur.w.h0 + hf;
             if (cur.k == 0) {
+                if (p.diag_stall && cur.w.rg == 0) {
+                    // diagnostic: a handoff that never comes (the word stays 0, never the epoch)
+                    bool okf = true;
+                    if (lane == 0)
+                        okf = wait_flag(p.abort_word + 8, p);
+                    if (!(ok = __shfl_sync(0xffffffffu, okf ? 1 : 0, 0) != 0))
+                        break;
+                }
                 // ---- carried-in state at a unit start: TMEM (fp32) and the bf16 operand of
                 //      C P in x stage (j-1)&1
                 if (cur.w.rg > 0) {
@@ -1043,7 +1052,10 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.final_state = a.final_state;
     p.slots = geo.nranges > 1 ? reinterpret_cast<float *>(ws + geo.slot_off) : nullptr;
     p.epoch = next_epoch();
-    p.timeout_ns = 2000000000ull;
+    p.timeout_ns = a.diag_stall ? 20000000ull : 2000000000ull;
+    p.diag_stall = a.diag_stall ? 1 : 0;
+    if (a.diag_stall && cudaMemsetAsync(ws + 64, 0, 8, stream) != cudaSuccess)
+        return SSD_ERR_CUDA;
     p.L = a.seqlen;
     p.nunits = geo.nunits;
     p.H = a.nheads;

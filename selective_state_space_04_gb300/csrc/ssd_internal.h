@@ -25,6 +25,7 @@ struct ScanArgs {
     int64_t batch, seqlen;
     int nheads, headdim, dstate, ngroups, chunk;
     int dtype;                 // ssd_dtype_t
+    bool diag_stall;           // SSD_DIAG_STALL_HANDOFF
 };
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu

@@ -13,6 +13,7 @@ import torch
 from .build import LIB_PATH
 
 PATH_AUTO = 0
+DIAG_STALL_HANDOFF = 0x100
 PATH_SEQUENTIAL = 1
 PATH_CHUNKED = 2
 _PATHS = {"auto": PATH_AUTO, "sequential": PATH_SEQUENTIAL, "seq": PATH_SEQUENTIAL,
@@ -136,7 +137,8 @@ def device_error(stream=None) -> int:
 
 
 def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
-                 path="auto", return_final_state=True, y=None, final_state=None, stream=None):
+                 path="auto", return_final_state=True, y=None, final_state=None, stream=None,
+                 diag_stall_handoff=False):
     """Forward SSD scan on CUDA tensors.  Returns ``(y, final_state)``.
 
     ``x [B,L,H,P]`` and ``B, C [B,L,G,N]`` share one dtype (bf16 or fp32);
@@ -155,6 +157,8 @@ def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=2
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     d = _dims_from(x, B, chunk, path)
+    if diag_stall_handoff:
+        d.flags |= DIAG_STALL_HANDOFF
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     _check(_lib.ssd_scan_fwd(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B), _ptr(C),
                              _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state),

@@ -147,3 +147,12 @@ def test_workspace_misaligned_or_overlapping_rejected_before_cuda(libssd):
     assert _ws_call(libssd, ctypes.c_void_p(0x20008), 4096) == 3   # SSD_ERR_MISALIGNED
     # overlaps y at 0x90000000
     assert _ws_call(libssd, ctypes.c_void_p(0x90000000 - 256), 4096) == 7   # SSD_ERR_ALIASING
+
+
+def test_diagnostic_flag_accepted_other_flags_rejected(libssd):
+    lib = libssd.lib()
+    d = libssd.make_dims(1, 64, 2, 8, 16, 1, 16, "f32")
+    d.flags = libssd.DIAG_STALL_HANDOFF
+    assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
+    d.flags = 0x200
+    assert lib.ssd_select_path(ctypes.byref(d)) == -1

@@ -51,6 +51,7 @@ def relerr(a, ref):
 
 def check(y, fin, ref_y, ref_fin, dtype):
     ey, ef = relerr(y, ref_y), relerr(fin, ref_fin)
+    print(f"rel err y {ey:.3e}  final state {ef:.3e}")
     assert ey <= TOL[dtype], f"y rel err {ey:.3e} > {TOL[dtype]}"
     assert ef <= TOL[dtype], f"final state rel err {ef:.3e} > {TOL[dtype]}"
     return ey, ef
