@@ -374,7 +374,8 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
                             stream);
     if ((dims->flags & SSD_PATH_MASK) == SSD_PATH_SEQUENTIAL)
         return SSD_ERR_UNSUPPORTED;
-    const ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
+    ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
+    a.allow_split = false;   // the chained schedule keeps the scratch within the array
     const int32_t path = resolve_path(a, SSD_PATH_CHUNKED, true);
     if (path < 0)
         return (ssd_status_t)(-path);
@@ -470,7 +471,9 @@ int32_t ssd_launches_per_call(const ssd_dims_t *dims)
     const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                                  nullptr, nullptr, nullptr, dims);
     const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
-    return path < 0 ? path : 1;
+    if (path < 0)
+        return path;
+    return path == SSD_PATH_CHUNKED ? chunk_launches(a) : 1;
 }
 
 uint64_t ssd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

@@ -122,7 +122,9 @@ struct ChunkParams {
     const float *init_state;          // [B,H,P,N] or null
     __nv_bfloat16 *y;
     float *final_state;               // [B,H,P,N] or null
-    float *slots;                     // [chains][2][16][N][4] handoff states (null if one unit per chain)
+    float *slots;                     // handoff states, [chains][2][16][N][4] (chained) or [units][2][16][N][4]
+                                      // (split); null when no unit hands a state on
+    float *unit_decay;                // split pass 1: exp(sum dt A) over each unit, [units][2]
     unsigned long long *flags;        // [nunits][state-group warps]: warp w of a unit publishes its rows
     unsigned long long *abort_word;
     unsigned long long epoch;
@@ -131,7 +133,17 @@ struct ChunkParams {
     long long nunits;
     int H, span, nranges, nhp, nchains, hpg;   // span = steps per unit (R*Q)
     int diag_stall;                   // first units wait for a handoff nobody publishes
+    int mode;                         // kChained, kSplitLocal or kSplitEntering
 };
+
+// How the units of a chain get their entering state:
+//   kChained        from the preceding unit of the chain, through a slot per chain
+//                   and a release/acquire flag (one launch)
+//   kSplitLocal     split pass 1: every unit starts from zero and stores its end
+//                   state and its total decay in a slot of its own (no y)
+//   kSplitEntering  split pass 3: every unit reads its entering state, combined
+//                   between the passes, from its own slot
+enum { kChained = 0, kSplitLocal = 1, kSplitEntering = 2 };
 
 struct Maps {
     CUtensorMap x, B, C;
@@ -719,6 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int r = q * 32 + lane;         // row: token t, or state row n
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t ta = tmem + lane_addr + kColP + hf * 64;
+        float unit_decay = 1.f;
         bool ok = true;
         Cursor cur;
         bool has = cursor_first(cur, p);
@@ -729,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t par = j & 1;
             const int hh = cur.w.h0 + hf;
             if (cur.k == 0) {
-                if (p.diag_stall && cur.w.rg == 0) {
+                if (p.mode == kChained && p.diag_stall && cur.w.rg == 0) {
                     // diagnostic: a handoff that never comes (the word stays 0, never the epoch)
                     bool okf = true;
                     if (lane == 0)
@@ -739,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // ---- carried-in state at a unit start: TMEM (fp32) and the bf16 operand of
                 //      C P in x stage (j-1)&1
-                if (cur.w.rg > 0) {
+                if (p.mode == kChained && cur.w.rg > 0) {
                     // rows n of this warp were written by the same warp of the predecessor unit
                     bool okf = true;
                     if (lane == 0)
@@ -748,11 +761,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                 }
                 uint8_t *pb = smem + kOffX + (s ^ 1) * kXStageBytes + hf * kTileBytes;
+                // chained: the chain's slot; split pass 3: this unit's own slot; split pass 1
+                // starts every unit from zero (the combine adds the initial state)
+                const size_t slot_of = p.mode == kChained ? (size_t)(cur.w.b * p.nhp + cur.w.hp) : (size_t)cur.u;
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
-                    if (cur.w.rg > 0) {
-                        const float4 *src = reinterpret_cast<const float4 *>(p.slots) +
-                                            ((size_t)(cur.w.b * p.nhp + cur.w.hp) * 2 + hf) * 16 * kN + r;
+                    if (cur.w.rg > 0 && p.mode != kSplitLocal) {
+                        const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float4 f = __ldcg(src + (size_t)(8 * half + i) * kN);
@@ -761,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             v[4 * i + 2] = __float_as_uint(f.z);
                             v[4 * i + 3] = __float_as_uint(f.w);
                         }
-                    } else if (p.init_state) {
+                    } else if (p.init_state && p.mode != kSplitLocal) {
                         const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
 #pragma unroll
                         for (int i = 0; i < 32; ++i)
@@ -789,6 +804,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float ecs = dk[6 * kT + hf * kT + r];
             const float wsc = dk[8 * kT + hf * kT + r];
             const float dtot = dk[10 * kT + hf];
+            unit_decay = (cur.k == 0 ? 1.f : unit_decay) * dtot;   // decay of the state over the unit so far
             {
                 uint8_t *xrow = smem + kOffX + s * kXStageBytes + hf * kTileBytes + r * 128;
                 const uint32_t w2 = pack_bf16x2(wsc, wsc);
@@ -851,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && 32 * q < cur.valid()) {
+                if (lane == 0 && 32 * q < cur.valid() && p.mode != kSplitLocal) {
                     tma_store_3d(&maps.y, stg, hh * kP, (int)cur.t0() + 32 * q, cur.w.b);
                     bulk_commit_group();
                 }
@@ -862,12 +878,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             if (cur.k == cur.w.nsub - 1) {
                 // end of the unit: hand the state to the next unit of this chain, or
-                // write the final state
-                if (cur.w.rg < p.nranges - 1) {
-                    // slot layout [chain][head][16-byte chunk c][row n]: a warp writes 512
+                // write the final state; split pass 1 stores every unit's end state and
+                // total decay in its own slot
+                const bool to_slot = p.mode == kSplitLocal || (p.mode == kChained && cur.w.rg < p.nranges - 1);
+                if (to_slot) {
+                    // slot layout [slot][head][16-byte chunk c][row n]: a warp writes 512
                     // contiguous bytes per chunk
-                    float4 *dst = reinterpret_cast<float4 *>(p.slots) +
-                                  ((size_t)(cur.w.b * p.nhp + cur.w.hp) * 2 + hf) * 16 * kN + r;
+                    const size_t slot_of = p.mode == kChained ? (size_t)(cur.w.b * p.nhp + cur.w.hp) : (size_t)cur.u;
+                    float4 *dst = reinterpret_cast<float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
                         tmem_ld32(ta + 32 * half, v);
@@ -878,12 +896,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
                                                __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3])));
                     }
-                    __syncwarp();
-                    if (lane == 0) {
-                        __threadfence();
-                        st_release_u64(p.flags + (size_t)cur.u * kGroupWarps + sw, p.epoch);
+                    if (p.mode == kSplitLocal) {
+                        if (q == 0 && lane == 0)
+                            p.unit_decay[(size_t)cur.u * 2 + hf] = unit_decay;
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) {
+                            __threadfence();
+                            st_release_u64(p.flags + (size_t)cur.u * kGroupWarps + sw, p.epoch);
+                        }
                     }
-                } else if (p.final_state) {
+                } else if (p.final_state && cur.w.rg == p.nranges - 1) {
                     float *dst = p.final_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
@@ -927,6 +950,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem, 512);
 }
 
+// Entering states of the split evaluation, between its two passes.  For each
+// chain, range by range: E_0 = the initial state (or 0) and
+// E_{k+1} = Lambda_k E_k + S_k, where S_k is the end state of the chain's unit k
+// started from zero and Lambda_k = exp(sum of dt A over that unit) (the linear
+// recurrence between chunks, applied to whole unit ranges).  E_k replaces S_k in
+// unit k's slot for k >= 1.  One thread per (chain, head, 4 channels, state row).
+__global__ void __launch_bounds__(256) ssd_split_combine_kernel(float *slots, const float *unit_decay,
+                                                                const float *init_state, int nchains,
+                                                                int nranges, int nhp, int H)
+{
+    constexpr int kPerChain = 2 * 16 * kN;   // float4 per slot
+    const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (tid >= (long long)nchains * kPerChain)
+        return;
+    const int chain = (int)(tid / kPerChain);
+    const int e = (int)(tid % kPerChain);   // (hf * 16 + c) * N + n
+    const int hf = e / (16 * kN), c = (e / kN) % 16, n = e % kN;
+    const int b = chain / nhp, h = 2 * (chain % nhp) + hf;
+    float4 E = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (init_state) {
+        const float *src = init_state + ((size_t)b * H + h) * (size_t)(kP * kN) + (size_t)(4 * c) * kN + n;
+        E = make_float4(src[0], src[kN], src[2 * kN], src[3 * kN]);
+    }
+    float4 *sl = reinterpret_cast<float4 *>(slots);
+    float4 S = __ldcg(sl + (size_t)chain * kPerChain + e);   // unit (range 0, chain)
+    for (int k = 0; k + 1 < nranges; ++k) {
+        const size_t u = (size_t)k * nchains + chain;
+        const float lam = unit_decay[u * 2 + hf];
+        E = make_float4(fmaf(lam, E.x, S.x), fmaf(lam, E.y, S.y), fmaf(lam, E.z, S.z), fmaf(lam, E.w, S.w));
+        float4 *dst = sl + (u + nchains) * kPerChain + e;
+        S = __ldcg(dst);   // the next unit's own end state, before it is replaced
+        __stcg(dst, E);
+    }
+}
+
 std::atomic<unsigned long long> g_epoch{0};
 
 unsigned long long next_epoch()
@@ -956,37 +1014,47 @@ int sm_count()
 
 struct Geometry {
     long long nchunks, nchains, chunks_per_unit, nranges, nunits, grid;
-    size_t flags_off, slot_off, total;
+    bool split;   // two passes with a combine in between, instead of chained units
+    size_t flags_off, slot_off, decay_off, total;
 };
 
-// Chunks per unit R.  The schedule runs ceil(units / grid) rounds of units of
-// R chunks, every unit boundary costs about one sub-chunk of handoff latency,
-// and the units of one chain run one after another, so the makespan is at
-// least one chain's length.  R is the candidate with the smallest estimate.
-long long pick_chunks_per_unit(long long nchunks, long long nchains, int Q, long long grid)
+// Candidate chunks-per-unit values: 1, 2, 3, 4, 8, 16, ... and all chunks.
+int unit_candidates(long long nchunks, long long *cand)
 {
-    const double subs_per_chunk = (double)Q / kT;
-    const double handoff = 1.0;   // in sub-chunk times
-    long long best_r = 1;
-    double best = 1e300;
-    long long cand[64];
     int nc = 0;
     for (long long R = 1; R < nchunks && nc < 62; R = (R < 4 ? R + 1 : R * 2))
         cand[nc++] = R;
     cand[nc++] = nchunks;
-    for (int i = 0; i < nc; ++i) {
-        const long long R = cand[i];
-        const long long ranges = (nchunks + R - 1) / R;
-        const long long units = ranges * nchains;
-        const long long rounds = (units + grid - 1) / grid;
-        const double unit_time = R * subs_per_chunk + handoff;
-        const double est = std::max(rounds * unit_time, ranges * unit_time);
-        if (est < best * 0.999) {
-            best = est;
-            best_r = R;
-        }
-    }
-    return best_r;
+    return nc;
+}
+
+// Estimated time (in 128-step sub-chunk times) of the chained schedule with R
+// chunks per unit: ceil(units / grid) rounds of units of R chunks, each unit
+// boundary costing about one sub-chunk of handoff latency, and never less than
+// one chain's ranges run one after another.
+double chained_estimate(long long R, long long nchunks, long long nchains, int Q, long long grid)
+{
+    const double subs_per_chunk = (double)Q / kT;
+    const long long ranges = (nchunks + R - 1) / R;
+    const long long rounds = (ranges * nchains + grid - 1) / grid;
+    const double unit_time = R * subs_per_chunk + 1.0;
+    return std::max(rounds * unit_time, ranges * unit_time);
+}
+
+// Estimated time of the split schedule: two passes over independent units
+// (no handoff wait, about half a sub-chunk to refill the pipeline per unit)
+// plus the combine, which streams every unit's state (64 KB) in and out
+// (about 40 ns per unit and chain at HBM speed, in sub-chunk times of about 3 us)
+// and two more launches.
+double split_estimate(long long R, long long nchunks, long long nchains, int Q, long long grid)
+{
+    const double subs_per_chunk = (double)Q / kT;
+    const long long ranges = (nchunks + R - 1) / R;
+    const long long units = ranges * nchains;
+    const long long rounds = (units + grid - 1) / grid;
+    const double pass = rounds * (R * subs_per_chunk + 0.5);
+    const double combine = units * 0.04 / 3.0 + 2.0;
+    return 2.0 * pass + combine;
 }
 
 Geometry geometry(const ScanArgs &a)
@@ -995,14 +1063,43 @@ Geometry geometry(const ScanArgs &a)
     g.nchunks = (a.seqlen + a.chunk - 1) / a.chunk;
     g.nchains = a.batch * (a.nheads / 2);
     const int sms = std::max(1, sm_count());
-    g.chunks_per_unit = pick_chunks_per_unit(g.nchunks, g.nchains, a.chunk, sms);
+    long long cand[64];
+    const int nc = unit_candidates(g.nchunks, cand);
+    double best = 1e300;
+    g.chunks_per_unit = 1;
+    for (int i = 0; i < nc; ++i) {
+        const double est = chained_estimate(cand[i], g.nchunks, g.nchains, a.chunk, sms);
+        if (est < best * 0.999) {
+            best = est;
+            g.chunks_per_unit = cand[i];
+        }
+    }
+    g.split = false;
+    if (a.allow_split && g.nchunks > 1) {
+        double best_split = 1e300;
+        long long r_split = 1;
+        for (int i = 0; i + 1 < nc; ++i) {   // at least two ranges
+            const double est = split_estimate(cand[i], g.nchunks, g.nchains, a.chunk, sms);
+            if (est < best_split * 0.999) {
+                best_split = est;
+                r_split = cand[i];
+            }
+        }
+        if (best_split < 0.8 * best) {
+            g.split = true;
+            g.chunks_per_unit = r_split;
+        }
+    }
     g.nranges = (g.nchunks + g.chunks_per_unit - 1) / g.chunks_per_unit;
     g.nunits = g.nranges * g.nchains;
     g.grid = std::min<long long>(sms, g.nunits);
     g.flags_off = 256;
     g.slot_off = (g.flags_off + (size_t)g.nunits * kGroupWarps * 8 + 255) & ~(size_t)255;
-    const size_t slot_bytes = g.nranges > 1 ? (size_t)g.nchains * kN * 2 * kP * 4 : 0;
-    g.total = g.slot_off + slot_bytes;
+    const size_t slot_state = (size_t)kN * 2 * kP * 4;   // one head pair, fp32
+    const size_t slot_bytes = g.split ? (size_t)g.nunits * slot_state
+                                      : (g.nranges > 1 ? (size_t)g.nchains * slot_state : 0);
+    g.decay_off = g.slot_off + slot_bytes;
+    g.total = g.decay_off + (g.split ? (((size_t)g.nunits * 2 * 4 + 255) & ~(size_t)255) : 0);
     return g;
 }
 
@@ -1050,7 +1147,9 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.abort_word = reinterpret_cast<unsigned long long *>(ws);
     p.flags = reinterpret_cast<unsigned long long *>(ws + geo.flags_off);
     p.final_state = a.final_state;
-    p.slots = geo.nranges > 1 ? reinterpret_cast<float *>(ws + geo.slot_off) : nullptr;
+    p.slots = (geo.split || geo.nranges > 1) ? reinterpret_cast<float *>(ws + geo.slot_off) : nullptr;
+    p.unit_decay = geo.split ? reinterpret_cast<float *>(ws + geo.decay_off) : nullptr;
+    p.mode = kChained;
     p.epoch = next_epoch();
     p.timeout_ns = a.diag_stall ? 20000000ull : 2000000000ull;
     p.diag_stall = a.diag_stall ? 1 : 0;
@@ -1078,11 +1177,33 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (!geo.split) {
+        if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        note_launches(1);
+        return SSD_OK;
+    }
+    // split: pass 1 (end state of every unit from zero), combine (entering state of
+    // every unit), pass 3 (the scan itself, all units independent)
+    p.mode = kSplitLocal;
+    if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    note_launches(1);
+    const long long threads = geo.nchains * 2 * 16 * kN;
+    ssd_split_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
+        p.slots, p.unit_decay, a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2, a.nheads);
+    if (cudaGetLastError() != cudaSuccess)
+        return SSD_ERR_CUDA;
+    note_launches(1);
+    p.mode = kSplitEntering;
+    p.epoch = next_epoch();
     if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     return SSD_OK;
 }
+
+int chunk_launches(const ScanArgs &a) { return geometry(a).split ? 3 : 1; }
 
 ssd_status_t chunk_read_device_error(cudaStream_t stream, uint32_t *code)
 {

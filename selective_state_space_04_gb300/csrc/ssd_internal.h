@@ -26,6 +26,7 @@ struct ScanArgs {
     int nheads, headdim, dstate, ngroups, chunk;
     int dtype;                 // ssd_dtype_t
     bool diag_stall;           // SSD_DIAG_STALL_HANDOFF
+    bool allow_split = true;   // the chunked path may use its two-pass split schedule
 };
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu
@@ -40,6 +41,8 @@ size_t chunk_workspace_bytes(const ScanArgs &a);
 // `workspace` must hold chunk_workspace_bytes(a) bytes, 16-byte aligned;
 // its contents on entry do not matter.
 ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t stream);
+// kernel launches chunk_launch makes for these sizes (1, or 3 for the split schedule)
+int chunk_launches(const ScanArgs &a);
 ssd_status_t chunk_read_device_error(cudaStream_t stream, uint32_t *code);
 
 // launch accounting
