@@ -365,6 +365,8 @@ def run_gpu(args, w: Workload):
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
                    "chunk": w.chunk, "init_state": w.init_state, "final_state": True,
                    "path": "chunked" if path == ssd.PATH_CHUNKED else "sequential",
+                   "schedule": ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups,
+                                                  w.dstate, w.chunk, w.dtype),
                    "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
         "roofline": {
             "bound": "hbm" if t_hbm >= t_tensor else "tensor",

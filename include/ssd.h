@@ -71,6 +71,18 @@ typedef enum ssd_status {
  * without faulting the GPU.  Ignored by the sequential path. */
 #define SSD_DIAG_STALL_HANDOFF 0x100u
 
+/* Schedules of the chunked path (see ssd_chunk_schedule).  One may be requested
+ * in ssd_dims_t.flags as (SSD_SCHEDULE_x << SSD_SCHEDULE_SHIFT); 0 there lets
+ * the library choose.  A split request for a sequence of a single chunk runs
+ * the range schedule (there is nothing to split).  Ignored by the sequential
+ * path. */
+#define SSD_SCHEDULE_NONE 0
+#define SSD_SCHEDULE_RANGES 1
+#define SSD_SCHEDULE_PIECES 2
+#define SSD_SCHEDULE_SPLIT 3
+#define SSD_SCHEDULE_SHIFT 4
+#define SSD_SCHEDULE_REQUEST_MASK 0x30u
+
 typedef struct ssd_dims {
     int64_t batch;     /* B >= 0 */
     int64_t seqlen;    /* L >= 0; need not be a multiple of chunk (ragged last chunk) */
@@ -80,7 +92,7 @@ typedef struct ssd_dims {
     int32_t ngroups;   /* G >= 1, H % G == 0 */
     int32_t chunk;     /* Q >= 1: chunk length of the chunked evaluation (ignored by the sequential path) */
     int32_t dtype;     /* ssd_dtype_t of x, B, C and y */
-    uint32_t flags;    /* SSD_PATH_* | optional SSD_DIAG_STALL_HANDOFF */
+    uint32_t flags;    /* SSD_PATH_* | optional schedule request | optional SSD_DIAG_STALL_HANDOFF */
     uint32_t reserved; /* must be 0 */
 } ssd_dims_t;
 
@@ -171,9 +183,13 @@ ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt
  * Errors as ssd_scan_fwd, plus:
  *   SSD_ERR_UNSUPPORTED    the chunked path does not support these dims, or
  *                          SSD_PATH_SEQUENTIAL was requested in dims->flags;
- *   SSD_ERR_SCRATCH_LIMIT  the kernel would need more than 32 MiB of scratch
- *                          (about 500 batch-row x head-pair chains when chains
- *                          are split); nothing is enqueued;
+ *   SSD_ERR_SCRATCH_LIMIT  the kernel would need more than 32 MiB of scratch;
+ *                          nothing is enqueued.  The call never takes
+ *                          SSD_SCHEDULE_SPLIT, and takes SSD_SCHEDULE_PIECES
+ *                          (one 64 KiB state slot and 64 B of flags per SM)
+ *                          wherever the schedule ssd_scan_fwd would take needs
+ *                          more than the array, so only a device of more than
+ *                          about 500 SMs gets this error;
  *   SSD_ERR_CUDA           the array's address could not be obtained.
  * Concurrency: the array is shared by all calls on a device.  Calls whose
  * kernels may overlap in time on one device (different streams, or threads
@@ -193,6 +209,25 @@ int32_t ssd_select_path(const ssd_dims_t *dims);
 /* Kernel launches one ssd_scan_fwd call makes for these dims (0 for empty
  * work), or -(ssd_status_t).  Host only. */
 int32_t ssd_launches_per_call(const ssd_dims_t *dims);
+
+/* How the chunked path orders its work for these dims and flags on the
+ * current device (the SM count enters the choice), as ssd_scan_fwd would run
+ * it:
+ *   SSD_SCHEDULE_NONE    no chunked work (empty, or the sequential path);
+ *   SSD_SCHEDULE_RANGES  chains cut into units of whole chunks, dealt to the CTAs
+ *                        in turn; a unit takes its entering state from the unit
+ *                        before it in its chain (one launch);
+ *   SSD_SCHEDULE_PIECES  the chains' 128-step sub-chunks, chain after chain, cut
+ *                        into one run of equal length per CTA; a chain cut
+ *                        between two CTAs hands its state across (one launch);
+ *   SSD_SCHEDULE_SPLIT   every unit's end state from zero, a combine of those
+ *                        states along each chain, then every unit from its
+ *                        combined entering state (three launches).
+ * All three evaluate the chunked recurrence with the state carried from chunk
+ * to chunk; they differ only in which CTA computes what, and when.
+ * ssd_scan_fwd_noalloc may choose differently (see there).  Returns -(ssd_status_t)
+ * for invalid or unsupported dims.  Host only; launches nothing. */
+int32_t ssd_chunk_schedule(const ssd_dims_t *dims);
 
 /* Total kernel launches this library has made in this process. */
 uint64_t ssd_launch_count(void);

@@ -42,7 +42,8 @@ ssd_status_t check_dims(const ssd_dims_t *d, Sizes *sz)
     if (d->dtype != SSD_DTYPE_F32 && d->dtype != SSD_DTYPE_BF16)
         return SSD_ERR_UNSUPPORTED;
     const uint32_t path = d->flags & SSD_PATH_MASK;
-    if ((d->flags & ~(SSD_PATH_MASK | SSD_DIAG_STALL_HANDOFF)) != 0 || path > SSD_PATH_CHUNKED)
+    if ((d->flags & ~(SSD_PATH_MASK | SSD_SCHEDULE_REQUEST_MASK | SSD_DIAG_STALL_HANDOFF)) != 0 ||
+        path > SSD_PATH_CHUNKED)
         return SSD_ERR_INVALID_DIMS;
     int64_t bl, blh, t;
     const int64_t es = (int64_t)elem_size(d->dtype);
@@ -84,6 +85,7 @@ ScanArgs make_args(const void *x, const float *dt_raw, const float *dt_bias, con
     a.chunk = d->chunk;
     a.dtype = d->dtype;
     a.diag_stall = (d->flags & SSD_DIAG_STALL_HANDOFF) != 0;
+    a.sched_req = (int)((d->flags & SSD_SCHEDULE_REQUEST_MASK) >> SSD_SCHEDULE_SHIFT);
     return a;
 }
 
@@ -375,7 +377,9 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
     if ((dims->flags & SSD_PATH_MASK) == SSD_PATH_SEQUENTIAL)
         return SSD_ERR_UNSUPPORTED;
     ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
-    a.allow_split = false;   // the chained schedule keeps the scratch within the array
+    if (a.sched_req == SSD_SCHEDULE_SPLIT)
+        return SSD_ERR_UNSUPPORTED;
+    a.scratch_cap = kNoAllocScratchBytes;
     const int32_t path = resolve_path(a, SSD_PATH_CHUNKED, true);
     if (path < 0)
         return (ssd_status_t)(-path);
@@ -474,6 +478,22 @@ int32_t ssd_launches_per_call(const ssd_dims_t *dims)
     if (path < 0)
         return path;
     return path == SSD_PATH_CHUNKED ? chunk_launches(a) : 1;
+}
+
+int32_t ssd_chunk_schedule(const ssd_dims_t *dims)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return -(int32_t)s;
+    if (dims->batch == 0 || dims->seqlen == 0)
+        return SSD_SCHEDULE_NONE;
+    const ScanArgs a = make_args(nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                                 nullptr, nullptr, nullptr, dims);
+    const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
+    if (path < 0)
+        return path;
+    return path == SSD_PATH_CHUNKED ? chunk_schedule(a) : SSD_SCHEDULE_NONE;
 }
 
 uint64_t ssd_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }

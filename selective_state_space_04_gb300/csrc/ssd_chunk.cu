@@ -130,8 +130,10 @@ struct ChunkParams {
     unsigned long long epoch;
     unsigned long long timeout_ns;
     long long L;
-    long long nunits;
+    long long nunits;                 // range schedule: units
+    long long total_subs;             // piece schedule: sub-chunks of all chains
     int H, span, nranges, nhp, nchains, hpg;   // span = steps per unit (R*Q)
+    int nsub_chain;                   // sub-chunks per chain
     int diag_stall;                   // first units wait for a handoff nobody publishes
     int mode;                         // kChained, kSplitLocal or kSplitEntering
 };
@@ -231,60 +233,142 @@ __device__ bool wait_flag(const unsigned long long *flag, const ChunkParams &p)
     }
 }
 
+// A run of consecutive sub-chunks of one chain (one batch row, one head pair).
+// Kept small: every warp role holds two of them (this sub-chunk's, the next).
 struct Unit {
-    int rg, b, hp, h0, g, nsub, len;   // rg: index of the unit's step range in its chain
-    long long start;                   // first step
+    int b, h0, nsub, len, start;   // start: first step (sequences are shorter than 2^31)
+    int flags;                     // kFirst: begins its chain; kLast: ends it
 };
+constexpr int kFirst = 1, kLast = 2;
 
-// (units number fewer than 2^31: 32-bit index arithmetic)
-__device__ __forceinline__ Unit decode_unit(long long u, const ChunkParams &p)
+// Range schedule: unit u is step range u / nchains of chain u % nchains (units
+// number fewer than 2^31: 32-bit index arithmetic).
+__device__ __forceinline__ Unit decode_unit(int u, const ChunkParams &p)
 {
     Unit w;
-    const int ui = (int)u;
-    w.rg = ui / p.nchains;
-    const int chain = ui - w.rg * p.nchains;
+    const int rg = u / p.nchains;
+    const int chain = u - rg * p.nchains;
     w.b = chain / p.nhp;
-    w.hp = chain - w.b * p.nhp;
-    w.h0 = 2 * w.hp;
-    w.g = w.h0 / p.hpg;
-    w.start = (long long)w.rg * p.span;
-    w.len = (int)min((long long)p.span, p.L - w.start);
+    w.h0 = 2 * (chain - w.b * p.nhp);
+    w.start = rg * p.span;
+    w.len = min(p.span, (int)(p.L - w.start));
     w.nsub = (w.len + kT - 1) / kT;
+    w.flags = (rg == 0 ? kFirst : 0) | (rg == p.nranges - 1 ? kLast : 0);
+    return w;
+}
+
+// Piece schedule: the chains' sub-chunks, chain after chain, are cut into
+// gridDim.x runs of equal length (to one sub-chunk), CTA i taking run i.  A
+// run is at least one chain long, so it holds at most: the head of a chain
+// that the next CTA finishes, whole chains, and the tail of a chain that the
+// previous CTA began.  It takes them in that order, so a head is handed on
+// first and a tail is taken up last.  The state crossing the boundary between
+// CTAs i and i+1 goes through slot i.  Unit e of this CTA's run (nsub == 0
+// past its end).
+__device__ __forceinline__ Unit decode_piece(int e, const ChunkParams &p)
+{
+    Unit w;
+    const long long T = p.total_subs, G = gridDim.x, i = blockIdx.x, ns = p.nsub_chain;
+    const long long lo = i * T / G, hi = (i + 1) * T / G;
+    const int head = hi % ns != 0 ? 1 : 0;
+    const int tail = lo % ns != 0 ? 1 : 0;
+    const long long f0 = (lo + ns - 1) / ns;
+    const int nfull = (int)(hi / ns - f0);
+    long long chain, kb, ke;
+    if (e < head) {
+        chain = hi / ns;
+        kb = 0;
+        ke = hi - chain * ns;
+        w.flags = kFirst;
+    } else if (e < head + nfull) {
+        chain = f0 + (e - head);
+        kb = 0;
+        ke = ns;
+        w.flags = kFirst | kLast;
+    } else if (e < head + nfull + tail) {
+        chain = lo / ns;
+        kb = lo - chain * ns;
+        ke = ns;
+        w.flags = kLast;
+    } else {
+        w.nsub = 0;
+        return w;
+    }
+    w.b = (int)(chain / p.nhp);
+    w.h0 = 2 * (int)(chain - (long long)w.b * p.nhp);
+    w.start = (int)(kb * kT);
+    w.len = (int)(min(ke * kT, p.L) - w.start);
+    w.nsub = (int)(ke - kb);
     return w;
 }
 
 // Position in this CTA's sequence of sub-chunks: units blockIdx.x,
-// blockIdx.x + gridDim.x, ... each walked in sub-chunks of kT steps.
+// blockIdx.x + gridDim.x, ... (range schedule) or units 0, 1, ... of the
+// CTA's run (piece schedule), each walked in sub-chunks of kT steps.
 struct Cursor {
-    long long u;
+    int u;
     int k;
     Unit w;
     __device__ __forceinline__ int valid() const { return min(kT, w.len - k * kT); }
-    __device__ __forceinline__ long long t0() const { return w.start + (long long)k * kT; }
+    __device__ __forceinline__ long long t0() const { return (long long)w.start + k * kT; }
+    __device__ __forceinline__ bool first() const { return (w.flags & kFirst) != 0; }
+    __device__ __forceinline__ bool last() const { return (w.flags & kLast) != 0; }
 };
 
-__device__ __forceinline__ bool cursor_first(Cursor &c, const ChunkParams &p)
+template <bool kPieces>
+__device__ __forceinline__ bool cursor_load(Cursor &c, const ChunkParams &p)
 {
-    c.u = blockIdx.x;
     c.k = 0;
+    if constexpr (kPieces) {
+        c.w = decode_piece(c.u, p);
+        return c.w.nsub > 0;
+    }
     if (c.u >= p.nunits)
         return false;
     c.w = decode_unit(c.u, p);
     return true;
 }
 
+template <bool kPieces>
+__device__ __forceinline__ bool cursor_first(Cursor &c, const ChunkParams &p)
+{
+    c.u = kPieces ? 0 : (int)blockIdx.x;
+    return cursor_load<kPieces>(c, p);
+}
+
+template <bool kPieces>
 __device__ __forceinline__ bool cursor_next(Cursor &c, const ChunkParams &p)
 {
     if (c.k + 1 < c.w.nsub) {
         ++c.k;
         return true;
     }
-    c.u += gridDim.x;
-    c.k = 0;
-    if (c.u >= p.nunits)
-        return false;
-    c.w = decode_unit(c.u, p);
-    return true;
+    c.u += kPieces ? 1 : (int)gridDim.x;
+    return cursor_load<kPieces>(c, p);
+}
+
+// Handoff slot of the unit's entering and/or end state: chained range schedule,
+// one per chain; piece schedule, one per boundary between CTAs (a head hands on
+// through this CTA's, a tail takes up through the previous CTA's); split, one
+// per unit.
+template <bool kPieces>
+__device__ __forceinline__ int unit_slot(const Cursor &c, const ChunkParams &p)
+{
+    if (kPieces)
+        return c.first() ? (int)blockIdx.x : (int)blockIdx.x - 1;
+    return p.mode == kChained ? c.w.b * p.nhp + (c.w.h0 >> 1) : c.u;
+}
+
+// Flag rows (chained only): the one the predecessor publishes, and this unit's.
+template <bool kPieces>
+__device__ __forceinline__ int wait_row(const Cursor &c, const ChunkParams &p)
+{
+    return kPieces ? (int)blockIdx.x - 1 : c.u - p.nchains;
+}
+template <bool kPieces>
+__device__ __forceinline__ int post_row_of(const Cursor &c, const ChunkParams &p)
+{
+    return kPieces ? (int)blockIdx.x : c.u;
 }
 
 __device__ __forceinline__ float softplus_f32(float z)
@@ -396,6 +480,8 @@ __device__ __noinline__ void build_group_direct(uint32_t ta, int s0, int t, cons
     tmem_st8(ta + 8, m1);
 }
 
+// kPieces: the piece schedule (else the range schedule, or a split pass)
+template <bool kPieces>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
@@ -462,13 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             int last_bc[2] = {-1, -1}, last_x[2] = {-1, -1};  // last sub-chunk loaded per stage
             Cursor cur;
-            for (bool has = cursor_first(cur, p); has; has = cursor_next(cur, p), ++j) {
+            for (bool has = cursor_first<kPieces>(cur, p); has; has = cursor_next<kPieces>(cur, p), ++j) {
                 const int s = j & 1;
                 const int t0 = (int)cur.t0();
                 if (j >= 2 && !(ok = wait_bar(&bars[BAR_BC_EMPTY + s], ((j >> 1) + 1) & 1, p)))
                     break;
                 uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
-                const int gc = cur.w.g * kN;
+                const int gc = (cur.w.h0 / p.hpg) * kN;
                 mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
                 tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
@@ -519,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t j = 0;
             bool ok = true;
             Cursor cur;
-            bool has = cursor_first(cur, p);
+            bool has = cursor_first<kPieces>(cur, p);
             if (has) {
                 if ((ok = wait_bar(&bars[BAR_BC_FULL + 0], 0, p))) {
                     tc_fence_after();
@@ -528,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             while (ok && has) {
                 Cursor nxt = cur;
-                const bool has_next = cursor_next(nxt, p);
+                const bool has_next = cursor_next<kPieces>(nxt, p);
                 const int s = j & 1;
                 const uint32_t par = j & 1;
                 const uint32_t bc = smem_u32(smem + kOffBC + s * kBCStageBytes);
@@ -620,13 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         uint32_t msync = 0;
         Cursor cur;
-        bool has = cursor_first(cur, p);
+        bool has = cursor_first<kPieces>(cur, p);
         float dt_raw = 0.f;
         if (has && r < cur.valid())
             dt_raw = __ldg(p.dt_raw + ((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + cur.w.h0 + hd);
         for (uint32_t j = 0; has; ++j) {
             Cursor nxt = cur;
-            const bool has_next = cursor_next(nxt, p);
+            const bool has_next = cursor_next<kPieces>(nxt, p);
             float dt_next = 0.f;   // issued one sub-chunk ahead
             if (has_next && r < nxt.valid())
                 dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
@@ -734,15 +820,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         float unit_decay = 1.f;
         bool ok = true;
         Cursor cur;
-        bool has = cursor_first(cur, p);
+        bool has = cursor_first<kPieces>(cur, p);
         for (uint32_t j = 0; ok && has; ++j) {
             Cursor nxt = cur;
-            const bool has_next = cursor_next(nxt, p);
+            const bool has_next = cursor_next<kPieces>(nxt, p);
             const int s = j & 1;
             const uint32_t par = j & 1;
             const int hh = cur.w.h0 + hf;
             if (cur.k == 0) {
-                if (p.mode == kChained && p.diag_stall && cur.w.rg == 0) {
+                if (p.mode == kChained && p.diag_stall && cur.first()) {
                     // diagnostic: a handoff that never comes (the word stays 0, never the epoch)
                     bool okf = true;
                     if (lane == 0)
@@ -752,44 +838,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // ---- carried-in state at a unit start: TMEM (fp32) and the bf16 operand of
                 //      C P in x stage (j-1)&1
-                if (p.mode == kChained && cur.w.rg > 0) {
+                if (p.mode == kChained && !cur.first()) {
                     // rows n of this warp were written by the same warp of the predecessor unit
                     bool okf = true;
                     if (lane == 0)
-                        okf = wait_flag(p.flags + (size_t)(cur.u - p.nchains) * kGroupWarps + sw, p);
+                        okf = wait_flag(p.flags + (size_t)wait_row<kPieces>(cur, p) * kGroupWarps + sw, p);
                     if (!(ok = __shfl_sync(0xffffffffu, okf ? 1 : 0, 0) != 0))
                         break;
                 }
                 uint8_t *pb = smem + kOffX + (s ^ 1) * kXStageBytes + hf * kTileBytes;
-                // chained: the chain's slot; split pass 3: this unit's own slot; split pass 1
-                // starts every unit from zero (the combine adds the initial state)
-                const size_t slot_of = p.mode == kChained ? (size_t)(cur.w.b * p.nhp + cur.w.hp) : (size_t)cur.u;
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t v[32];
-                    if (cur.w.rg > 0 && p.mode != kSplitLocal) {
-                        const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
+                // chained: the slot the predecessor filled; split pass 3: this unit's own
+                // slot; split pass 1 starts every unit from zero (the combine adds the
+                // initial state)
+                // all 64 loads of the row are issued before the first use (one round trip)
+                const size_t slot_of = (size_t)unit_slot<kPieces>(cur, p);
+                uint32_t v[2][32];
+                if (!cur.first() && p.mode != kSplitLocal) {
+                    const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            const float4 f = __ldcg(src + (size_t)(8 * half + i) * kN);
-                            v[4 * i + 0] = __float_as_uint(f.x);
-                            v[4 * i + 1] = __float_as_uint(f.y);
-                            v[4 * i + 2] = __float_as_uint(f.z);
-                            v[4 * i + 3] = __float_as_uint(f.w);
-                        }
-                    } else if (p.init_state && p.mode != kSplitLocal) {
-                        const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = __float_as_uint(__ldg(src + (size_t)(32 * half + i) * kN));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            v[i] = 0u;
+                    for (int i = 0; i < 16; ++i) {
+                        const float4 f = __ldcg(src + (size_t)i * kN);
+                        v[i >> 3][4 * (i & 7) + 0] = __float_as_uint(f.x);
+                        v[i >> 3][4 * (i & 7) + 1] = __float_as_uint(f.y);
+                        v[i >> 3][4 * (i & 7) + 2] = __float_as_uint(f.z);
+                        v[i >> 3][4 * (i & 7) + 3] = __float_as_uint(f.w);
                     }
-                    tmem_st32(ta + 32 * half, v);
+                } else if (p.init_state && p.mode != kSplitLocal) {
+                    const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        v[i >> 5][i & 31] = __float_as_uint(__ldg(src + (size_t)i * kN));
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 64; ++i)
+                        v[i >> 5][i & 31] = 0u;
+                }
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    tmem_st32(ta + 32 * half, v[half]);
 #pragma unroll
                     for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v + 8 * c8);
+                        *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v[half] + 8 * c8);
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
@@ -880,11 +969,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // end of the unit: hand the state to the next unit of this chain, or
                 // write the final state; split pass 1 stores every unit's end state and
                 // total decay in its own slot
-                const bool to_slot = p.mode == kSplitLocal || (p.mode == kChained && cur.w.rg < p.nranges - 1);
+                const bool to_slot = p.mode == kSplitLocal || (p.mode == kChained && !cur.last());
                 if (to_slot) {
                     // slot layout [slot][head][16-byte chunk c][row n]: a warp writes 512
                     // contiguous bytes per chunk
-                    const size_t slot_of = p.mode == kChained ? (size_t)(cur.w.b * p.nhp + cur.w.hp) : (size_t)cur.u;
+                    const size_t slot_of = (size_t)unit_slot<kPieces>(cur, p);
                     float4 *dst = reinterpret_cast<float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
@@ -903,10 +992,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         __syncwarp();
                         if (lane == 0) {
                             __threadfence();
-                            st_release_u64(p.flags + (size_t)cur.u * kGroupWarps + sw, p.epoch);
+                            st_release_u64(p.flags + (size_t)post_row_of<kPieces>(cur, p) * kGroupWarps + sw, p.epoch);
                         }
                     }
-                } else if (p.final_state && cur.w.rg == p.nranges - 1) {
+                } else if (p.final_state && cur.last()) {
                     float *dst = p.final_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
                     for (int half = 0; half < 2; ++half) {
                         uint32_t v[32];
@@ -1014,7 +1103,9 @@ int sm_count()
 
 struct Geometry {
     long long nchunks, nchains, chunks_per_unit, nranges, nunits, grid;
-    bool split;   // two passes with a combine in between, instead of chained units
+    bool split;    // two passes with a combine in between, instead of chained units
+    bool pieces;   // chained, one run of equal length per CTA (see decode_piece)
+    long long nsub_chain, total_subs;
     size_t flags_off, slot_off, decay_off, total;
 };
 
@@ -1057,11 +1148,15 @@ double split_estimate(long long R, long long nchunks, long long nchains, int Q, 
     return 2.0 * pass + combine;
 }
 
+void layout(Geometry &g, long long grid_p, int sms);
+
 Geometry geometry(const ScanArgs &a)
 {
     Geometry g;
     g.nchunks = (a.seqlen + a.chunk - 1) / a.chunk;
     g.nchains = a.batch * (a.nheads / 2);
+    g.nsub_chain = (a.seqlen + kT - 1) / kT;
+    g.total_subs = g.nsub_chain * g.nchains;
     const int sms = std::max(1, sm_count());
     long long cand[64];
     const int nc = unit_candidates(g.nchunks, cand);
@@ -1074,8 +1169,20 @@ Geometry geometry(const ScanArgs &a)
             g.chunks_per_unit = cand[i];
         }
     }
+    // piece schedule: every run must hold at least one whole chain, so at most
+    // nchains runs.  Only on request, or to bound the scratch: with all CTAs in
+    // step (the range schedule) neighbouring head pairs read and write the same
+    // rows of x and y at the same time, which measured faster on the 2.7B layer
+    // than the better balance of the pieces.
+    g.pieces = false;
+    const long long grid_p = std::min<long long>(sms, g.nchains);
+    const bool pieces_ok = g.nsub_chain > 0 && grid_p > 0 && g.total_subs / grid_p >= g.nsub_chain &&
+                           g.total_subs < (1LL << 40);
+    if (pieces_ok && a.sched_req == SSD_SCHEDULE_PIECES)
+        g.pieces = true;
     g.split = false;
-    if (a.allow_split && g.nchunks > 1) {
+    const bool split_allowed = a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0);
+    if (split_allowed && g.nchunks > 1) {
         double best_split = 1e300;
         long long r_split = 1;
         for (int i = 0; i + 1 < nc; ++i) {   // at least two ranges
@@ -1085,22 +1192,44 @@ Geometry geometry(const ScanArgs &a)
                 r_split = cand[i];
             }
         }
-        if (best_split < 0.8 * best) {
+        if (best_split < 0.8 * best || a.sched_req == SSD_SCHEDULE_SPLIT) {
             g.split = true;
+            g.pieces = false;
             g.chunks_per_unit = r_split;
         }
     }
-    g.nranges = (g.nchunks + g.chunks_per_unit - 1) / g.chunks_per_unit;
-    g.nunits = g.nranges * g.nchains;
-    g.grid = std::min<long long>(sms, g.nunits);
-    g.flags_off = 256;
-    g.slot_off = (g.flags_off + (size_t)g.nunits * kGroupWarps * 8 + 255) & ~(size_t)255;
+    layout(g, grid_p, sms);
+    if (a.sched_req == 0 && a.scratch_cap != 0 && g.total > a.scratch_cap && pieces_ok && !g.pieces) {
+        g.pieces = true;   // at most one state slot per CTA
+        layout(g, grid_p, sms);
+    }
+    return g;
+}
+
+// Grid and scratch layout of the chosen schedule.
+void layout(Geometry &g, long long grid_p, int sms)
+{
     const size_t slot_state = (size_t)kN * 2 * kP * 4;   // one head pair, fp32
-    const size_t slot_bytes = g.split ? (size_t)g.nunits * slot_state
-                                      : (g.nranges > 1 ? (size_t)g.nchains * slot_state : 0);
+    size_t flag_rows, slot_bytes;
+    if (g.pieces) {
+        g.chunks_per_unit = g.nchunks;
+        g.nranges = 1;
+        g.grid = grid_p;
+        g.nunits = 0;
+        flag_rows = (size_t)g.grid;   // one per boundary between CTAs
+        slot_bytes = g.grid > 1 ? (size_t)g.grid * slot_state : 0;
+    } else {
+        g.nranges = (g.nchunks + g.chunks_per_unit - 1) / g.chunks_per_unit;
+        g.nunits = g.nranges * g.nchains;
+        g.grid = std::min<long long>(sms, g.nunits);
+        flag_rows = (size_t)g.nunits;
+        slot_bytes = g.split ? (size_t)g.nunits * slot_state
+                             : (g.nranges > 1 ? (size_t)g.nchains * slot_state : 0);
+    }
+    g.flags_off = 256;
+    g.slot_off = (g.flags_off + flag_rows * kGroupWarps * 8 + 255) & ~(size_t)255;
     g.decay_off = g.slot_off + slot_bytes;
     g.total = g.decay_off + (g.split ? (((size_t)g.nunits * 2 * 4 + 255) & ~(size_t)255) : 0);
-    return g;
 }
 
 }  // namespace
@@ -1147,7 +1276,8 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.abort_word = reinterpret_cast<unsigned long long *>(ws);
     p.flags = reinterpret_cast<unsigned long long *>(ws + geo.flags_off);
     p.final_state = a.final_state;
-    p.slots = (geo.split || geo.nranges > 1) ? reinterpret_cast<float *>(ws + geo.slot_off) : nullptr;
+    p.slots = (geo.split || geo.nranges > 1 || (geo.pieces && geo.grid > 1)) ? reinterpret_cast<float *>(ws + geo.slot_off)
+                                                                            : nullptr;
     p.unit_decay = geo.split ? reinterpret_cast<float *>(ws + geo.decay_off) : nullptr;
     p.mode = kChained;
     p.epoch = next_epoch();
@@ -1160,11 +1290,14 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.H = a.nheads;
     p.span = (int)(geo.chunks_per_unit * a.chunk);
     p.nranges = (int)geo.nranges;
+    p.nsub_chain = (int)geo.nsub_chain;
+    p.total_subs = geo.total_subs;
     p.nhp = a.nheads / 2;
     p.nchains = (int)geo.nchains;
     p.hpg = a.nheads / a.ngroups;
 
-    if (cudaFuncSetAttribute(ssd_chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kernel = geo.pieces ? ssd_chunk_fused_kernel<true> : ssd_chunk_fused_kernel<false>;
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
@@ -1178,7 +1311,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (!geo.split) {
-        if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
             return SSD_ERR_CUDA;
         note_launches(1);
         return SSD_OK;
@@ -1186,7 +1319,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     // split: pass 1 (end state of every unit from zero), combine (entering state of
     // every unit), pass 3 (the scan itself, all units independent)
     p.mode = kSplitLocal;
-    if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     const long long threads = geo.nchains * 2 * 16 * kN;
@@ -1197,13 +1330,19 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     note_launches(1);
     p.mode = kSplitEntering;
     p.epoch = next_epoch();
-    if (cudaLaunchKernelEx(&cfg, ssd_chunk_fused_kernel, maps, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     return SSD_OK;
 }
 
 int chunk_launches(const ScanArgs &a) { return geometry(a).split ? 3 : 1; }
+
+int chunk_schedule(const ScanArgs &a)
+{
+    const Geometry g = geometry(a);
+    return g.split ? SSD_SCHEDULE_SPLIT : (g.pieces ? SSD_SCHEDULE_PIECES : SSD_SCHEDULE_RANGES);
+}
 
 ssd_status_t chunk_read_device_error(cudaStream_t stream, uint32_t *code)
 {

@@ -26,7 +26,10 @@ struct ScanArgs {
     int nheads, headdim, dstate, ngroups, chunk;
     int dtype;                 // ssd_dtype_t
     bool diag_stall;           // SSD_DIAG_STALL_HANDOFF
-    bool allow_split = true;   // the chunked path may use its two-pass split schedule
+    int sched_req;             // requested SSD_SCHEDULE_*, or 0: the library chooses
+    size_t scratch_cap = 0;   // nonzero: the chunked path takes no split schedule and, when it
+                              // chooses, the piece schedule (at most one state slot per SM)
+                              // if the one it would choose needs more scratch than this
 };
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu
@@ -43,6 +46,8 @@ size_t chunk_workspace_bytes(const ScanArgs &a);
 ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t stream);
 // kernel launches chunk_launch makes for these sizes (1, or 3 for the split schedule)
 int chunk_launches(const ScanArgs &a);
+// SSD_SCHEDULE_RANGES, _PIECES or _SPLIT for these sizes
+int chunk_schedule(const ScanArgs &a);
 ssd_status_t chunk_read_device_error(cudaStream_t stream, uint32_t *code);
 
 // launch accounting

@@ -60,6 +60,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_select_path.argtypes = [ctypes.POINTER(SsdDims)]
     lib.ssd_launches_per_call.restype = ctypes.c_int32
     lib.ssd_launches_per_call.argtypes = [ctypes.POINTER(SsdDims)]
+    lib.ssd_chunk_schedule.restype = ctypes.c_int32
+    lib.ssd_chunk_schedule.argtypes = [ctypes.POINTER(SsdDims)]
     lib.ssd_launch_count.restype = ctypes.c_uint64
     lib.ssd_launch_count.argtypes = []
     lib.ssd_get_device_error.restype = ctypes.c_int
@@ -78,12 +80,18 @@ def lib() -> ctypes.CDLL:
     return _lib
 
 
-def make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype, path="auto") -> SsdDims:
+SCHEDULE_SHIFT = 4
+_SCHEDULE_REQUESTS = {"auto": 0, "ranges": 1, "pieces": 2, "split": 3}
+
+
+def make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype, path="auto",
+              schedule="auto") -> SsdDims:
     d = SsdDims()
     d.batch, d.seqlen, d.nheads, d.headdim = batch, seqlen, nheads, headdim
     d.dstate, d.ngroups, d.chunk = dstate, ngroups, chunk
     d.dtype = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
-    d.flags = _PATHS[path] if isinstance(path, str) else int(path)
+    d.flags = (_PATHS[path] if isinstance(path, str) else int(path)) | \
+        (_SCHEDULE_REQUESTS[schedule] << SCHEDULE_SHIFT)
     d.reserved = 0
     return d
 
@@ -97,28 +105,41 @@ def _check(status: int, what: str):
         raise SsdError(status, what)
 
 
-def _dims_from(x, B, chunk, path):
+def _dims_from(x, B, chunk, path, schedule="auto"):
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
-    return make_dims(Bt, L, H, P, N, G, chunk, x.dtype, path)
+    return make_dims(Bt, L, H, P, N, G, chunk, x.dtype, path, schedule)
 
 
-def select_path(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+def select_path(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto", schedule="auto") -> int:
     Bt, L, H, P = x_shape
-    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path, schedule)
     return _lib.ssd_select_path(ctypes.byref(d))
 
 
-def launches_per_call(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+def launches_per_call(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto", schedule="auto") -> int:
     Bt, L, H, P = x_shape
-    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path, schedule)
     return _lib.ssd_launches_per_call(ctypes.byref(d))
 
 
-def workspace_size(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto") -> int:
+SCHEDULES = {0: "none", 1: "ranges", 2: "pieces", 3: "split"}
+
+
+def chunk_schedule(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto", schedule="auto") -> str:
+    """How ``ssd_scan_fwd`` orders the chunked path's work for these sizes on the current device."""
+    Bt, L, H, P = x_shape
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path, schedule)
+    v = _lib.ssd_chunk_schedule(ctypes.byref(d))
+    if v < 0:
+        _check(-v, "ssd_chunk_schedule")
+    return SCHEDULES[v]
+
+
+def workspace_size(x_shape, ngroups, dstate, chunk, dtype="bf16", path="auto", schedule="auto") -> int:
     """Bytes of scratch ``ssd_scan_fwd_ws`` needs for these sizes on the current device."""
     Bt, L, H, P = x_shape
-    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path)
+    d = make_dims(Bt, L, H, P, dstate, ngroups, chunk, dtype, path, schedule)
     n = ctypes.c_uint64(0)
     _check(_lib.ssd_scan_fwd_workspace_size(ctypes.byref(d), ctypes.byref(n)), "ssd_scan_fwd_workspace_size")
     return int(n.value)
@@ -138,13 +159,15 @@ def device_error(stream=None) -> int:
 
 def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
                  path="auto", return_final_state=True, y=None, final_state=None, stream=None,
-                 diag_stall_handoff=False):
+                 diag_stall_handoff=False, schedule="auto"):
     """Forward SSD scan on CUDA tensors.  Returns ``(y, final_state)``.
 
     ``x [B,L,H,P]`` and ``B, C [B,L,G,N]`` share one dtype (bf16 or fp32);
     ``dt_raw [B,L,H]``, ``dt_bias, A_log, D [H]`` and the states
     ``[B,H,P,N]`` are fp32.  Work is enqueued on ``stream`` (default: the
-    current torch stream); the call does not synchronise.
+    current torch stream); the call does not synchronise.  ``schedule``
+    requests the chunked path's schedule ("ranges", "pieces", "split"), or
+    lets the library choose ("auto").
     """
     if y is None:
         y = torch.empty_like(x)
@@ -156,7 +179,7 @@ def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=2
                     ("final_state", final_state)):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    d = _dims_from(x, B, chunk, path)
+    d = _dims_from(x, B, chunk, path, schedule)
     if diag_stall_handoff:
         d.flags |= DIAG_STALL_HANDOFF
     st = torch.cuda.current_stream(x.device) if stream is None else stream
@@ -169,7 +192,7 @@ def ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=2
 
 def ssd_scan_fwd_host(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
                       path="auto", return_final_state=True, y=None, final_state=None,
-                      stream=None, device=None):
+                      stream=None, device=None, schedule="auto"):
     """Same scan on CPU tensors (pinned for asynchronous copies).  The library
     copies in, runs, copies out and synchronises before returning."""
     if y is None:
@@ -182,7 +205,7 @@ def ssd_scan_fwd_host(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, ch
                     ("final_state", final_state)):
         if t is not None and (t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CPU tensor")
-    d = _dims_from(x, B, chunk, path)
+    d = _dims_from(x, B, chunk, path, schedule)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
     with torch.cuda.device(dev):
         st = torch.cuda.current_stream(dev) if stream is None else stream
@@ -196,7 +219,7 @@ def ssd_scan_fwd_host(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, ch
 
 def ssd_scan_fwd_noalloc(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, chunk=256,
                          path="auto", y=None, final_state=None, return_final_state=True,
-                         stream=None):
+                         stream=None, schedule="auto"):
     """``ssd_scan_fwd`` on the chunked path with the library's fixed scratch
     array instead of a pool allocation (the library allocates nothing; outputs
     not passed in are created here by torch).  Calls that may overlap on one
@@ -211,7 +234,7 @@ def ssd_scan_fwd_noalloc(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *,
                     ("final_state", final_state)):
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    d = _dims_from(x, B, chunk, path)
+    d = _dims_from(x, B, chunk, path, schedule)
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     _check(_lib.ssd_scan_fwd_noalloc(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B),
                                      _ptr(C), _ptr(D), _ptr(init_state), _ptr(y),
@@ -223,7 +246,7 @@ def ssd_scan_fwd_noalloc(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *,
 
 def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, workspace,
                     chunk=256, path="auto", y=None, final_state=None, return_final_state=True,
-                    stream=None):
+                    stream=None, schedule="auto"):
     """``ssd_scan_fwd`` with caller-provided scratch: ``workspace`` is a CUDA
     tensor of at least ``workspace_size(...)`` bytes (or None when that is 0).
     The library allocates nothing; calls that may overlap must not share a
@@ -239,7 +262,7 @@ def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, work
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    d = _dims_from(x, B, chunk, path)
+    d = _dims_from(x, B, chunk, path, schedule)
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     _check(_lib.ssd_scan_fwd_ws(_ptr(x), _ptr(dt_raw), _ptr(dt_bias), _ptr(A_log), _ptr(B), _ptr(C),
                                 _ptr(D), _ptr(init_state), _ptr(y), _ptr(final_state),

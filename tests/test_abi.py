@@ -156,3 +156,24 @@ def test_diagnostic_flag_accepted_other_flags_rejected(libssd):
     assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
     d.flags = 0x200
     assert lib.ssd_select_path(ctypes.byref(d)) == -1
+
+
+def test_chunk_schedule_query(libssd):
+    # no chunked work: empty, or fp32 (sequential path)
+    assert libssd.chunk_schedule((0, 64, 4, 64), 1, 128, 256) == "none"
+    assert libssd.chunk_schedule((1, 64, 2, 8), 1, 16, 16, dtype="f32") == "none"
+    # "none" without a GB300-class device (the auto path is then sequential)
+    assert libssd.chunk_schedule((2, 640, 4, 64), 1, 128, 256) in ("none", "ranges", "pieces", "split")
+    with pytest.raises(libssd.SsdError) as e:
+        libssd.chunk_schedule((1, 64, 3, 64), 2, 128, 256)    # H % G != 0
+    assert e.value.status == 1
+
+
+def test_schedule_request_bits(libssd):
+    lib = libssd.lib()
+    for sched in ("auto", "ranges", "pieces", "split"):
+        d = libssd.make_dims(1, 64, 2, 8, 16, 1, 16, "f32", schedule=sched)
+        assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
+    d = libssd.make_dims(1, 64, 2, 8, 16, 1, 16, "f32")
+    d.flags = 0x40     # beyond the schedule request field
+    assert lib.ssd_select_path(ctypes.byref(d)) == -1

@@ -35,10 +35,11 @@ def to_dev(inp):
     return {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
 
 
-def run(ssd, inp, w, path="auto", chunk=None, init=True):
+def run(ssd, inp, w, path="auto", chunk=None, init=True, schedule="auto"):
     d = to_dev(inp)
     y, fin = ssd.ssd_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
-                              d["init_state"] if init else None, chunk=chunk or w.chunk, path=path)
+                              d["init_state"] if init else None, chunk=chunk or w.chunk, path=path,
+                              schedule=schedule)
     torch.cuda.synchronize()
     assert ssd.device_error() == 0
     return y, fin
@@ -318,3 +319,50 @@ def test_weak_decay_state_passing(ssd, seqlen, H):
                              None, chunk=w.chunk)
     torch.cuda.synchronize()
     assert relerr(y0, ref_y) > 10 * 2e-2
+
+
+# ----------------------------------------------------------- piece schedule
+# On request: each CTA takes one run of equal length over the chains' sub-chunks
+# laid end to end; with more chains than SMs some chains are cut between two
+# CTAs and their state crosses the cut through a slot.  Weak decay makes that
+# state matter.
+def _cut_chains(nchains, nsub, sms):
+    grid = min(sms, nchains)
+    total = nchains * nsub
+    return sum(1 for i in range(grid - 1) if ((i + 1) * total // grid) % nsub)
+
+
+@pytest.mark.parametrize("batch,seqlen,H,init", [(2, 1000, 160, True), (2, 1024, 160, False),
+                                                 (4, 2048, 80, True), (3, 4000, 112, True)])
+def test_piece_schedule_weak_decay(ssd, batch, seqlen, H, init):
+    w = small(batch=batch, seqlen=seqlen, nheads=H, chunk=256, init_state=init)
+    shape = (w.batch, w.seqlen, w.nheads, w.headdim)
+    assert ssd.chunk_schedule(shape, w.ngroups, w.dstate, w.chunk, schedule="pieces") == "pieces"
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert _cut_chains(batch * H // 2, -(-seqlen // 128), sms) > 0
+    inp = _weak_decay(make_inputs(w, seed=70 + H), H)
+    ref_y, ref_f = oracle.ssd_fwd(**inp)
+    y, fin = run(ssd, inp, w, path="chunked", init=init, schedule="pieces")
+    check(y, fin, ref_y, ref_f, "bf16")
+
+
+@pytest.mark.parametrize("schedule", ["pieces", "ranges"])
+def test_schedules_match_sliced_calls(ssd, schedule):
+    # the scan over 512-step slices, one call each, the final state of one call
+    # entering the next: the cuts between CTAs fall elsewhere
+    w = small(batch=2, seqlen=1000, nheads=160, chunk=256, init_state=True)
+    inp = _weak_decay(make_inputs(w, seed=80), w.nheads)
+    y1, f1 = run(ssd, inp, w, path="chunked", schedule=schedule)
+    d = to_dev(inp)
+    y2 = torch.empty_like(y1)
+    state = d["init_state"]
+    for t0 in range(0, w.seqlen, 512):
+        sl = slice(t0, min(w.seqlen, t0 + 512))
+        ys, state = ssd.ssd_scan_fwd(d["x"][:, sl].contiguous(), d["dt_raw"][:, sl].contiguous(), d["dt_bias"],
+                                     d["A_log"], d["B"][:, sl].contiguous(), d["C"][:, sl].contiguous(), d["D"],
+                                     state, chunk=w.chunk, path="chunked", schedule=schedule)
+        y2[:, sl] = ys
+    torch.cuda.synchronize()
+    assert ssd.device_error() == 0
+    print("bitwise equal:", bool(torch.equal(y1, y2)), bool(torch.equal(f1, state)))
+    check(y1, f1, y2.double().cpu().numpy(), state.double().cpu().numpy(), "bf16")
