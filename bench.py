@@ -76,22 +76,26 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-KERNEL_SOURCES = ("ssd_chunk.cu", "ptx.cuh", "tmap.h")
+KERNEL_SOURCES = {
+    "ssd_chunk_fused_kernel": ("ssd_chunk.cu", "ptx.cuh", "tmap.h"),
+    "ssd_decode_kernel": ("ssd_decode.cu",),
+    "ssd_seq_kernel": ("ssd_seq.cu",),
+}
 
 
-def source_digest() -> str:
-    """Digest of the chunked kernel's sources, to tell whether stored ncu
-    counters still describe the kernel that runs."""
+def source_digest(kernel: str = "ssd_chunk_fused_kernel") -> str:
+    """Digest of a kernel's sources, to tell whether stored ncu counters
+    still describe the kernel that runs."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "selective_state_space_04_gb300", "csrc")
-    for name in KERNEL_SOURCES:
+    for name in KERNEL_SOURCES[kernel]:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def stored_traffic(workload: str):
+def stored_traffic(workload: str, kernel: str):
     """Per-launch DRAM bytes from the committed ncu summary, if it was taken
     on the current kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -101,7 +105,9 @@ def stored_traffic(workload: str):
     except (OSError, ValueError):
         return None
     e = d.get(workload)
-    if not e or e.get("source_digest") != source_digest():
+    if not e or e.get("kernel", "ssd_chunk_fused_kernel") != kernel:
+        return None
+    if e.get("source_digest") != source_digest(kernel):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -339,14 +345,17 @@ def run_gpu(args, w: Workload):
         return
     peaks, peak_src = load_peaks()
     alg_bytes = algorithmic_bytes(w, final_state=True)
-    alg_flops = algorithmic_flops(w)
+    # the decode step has no tensor work: its arithmetic is a few fp32 operations
+    # per state entry, far below what the state's bytes take to stream
+    alg_flops = 0 if path == ssd.PATH_DECODE else algorithmic_flops(w)
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
     hbm_peak = float(peaks["hbm_gbs"])
     achieved_gbs = alg_bytes / avg_launch_s / 1e9
     t_hbm = alg_bytes / (hbm_peak * 1e9)
     t_tensor = alg_flops / (float(peaks["bf16_tflops"]) * 1e12)
-    traffic = stored_traffic(w.name)
-    kernel = "ssd_chunk_fused_kernel" if path == ssd.PATH_CHUNKED else "ssd_seq_kernel"
+    kernel = {ssd.PATH_CHUNKED: "ssd_chunk_fused_kernel", ssd.PATH_DECODE: "ssd_decode_kernel"}.get(
+        path, "ssd_seq_kernel")
+    traffic = stored_traffic(w.name, kernel)
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -364,7 +373,7 @@ def run_gpu(args, w: Workload):
         "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
                    "chunk": w.chunk, "init_state": w.init_state, "final_state": True,
-                   "path": "chunked" if path == ssd.PATH_CHUNKED else "sequential",
+                   "path": {ssd.PATH_CHUNKED: "chunked", ssd.PATH_DECODE: "decode"}.get(path, "sequential"),
                    "schedule": ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups,
                                                   w.dstate, w.chunk, w.dtype),
                    "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
@@ -449,7 +458,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="libssd", choices=["libssd", "reference"])
-    ap.add_argument("--path", default="auto", choices=["auto", "chunked", "sequential"])
+    ap.add_argument("--path", default="auto", choices=["auto", "chunked", "sequential", "decode"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -59,9 +59,12 @@ typedef enum ssd_status {
 } ssd_status_t;
 
 /* Kernel path selection, in ssd_dims_t.flags (low 4 bits). */
-#define SSD_PATH_AUTO 0u        /* chunked tensor-core path where supported, else sequential */
+#define SSD_PATH_AUTO 0u        /* decode step for seqlen 1, else the chunked tensor-core path where
+                                   supported, else sequential */
 #define SSD_PATH_SEQUENTIAL 1u  /* direct recurrence, fp32 FFMA (any P, N up to 2048; fp32 or bf16) */
 #define SSD_PATH_CHUNKED 2u     /* chunked tcgen05 path: bf16, P = 64, N = 128, Q % 64 == 0, (H/G) even */
+#define SSD_PATH_DECODE 3u      /* one step (seqlen 1), fp32 FFMA: any P, N % 4 == 0 and N <= 512; fp32 or
+                                   bf16.  SSD_PATH_AUTO takes it whenever seqlen == 1 and it applies */
 #define SSD_PATH_MASK 0xFu
 /* Diagnostic, in ssd_dims_t.flags: on the chunked path, the first unit of every
  * chain waits for a state handoff that nothing publishes, with the bounded waits
@@ -202,7 +205,8 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
                                   float *final_state, const ssd_dims_t *dims, void *stream);
 
 /* Which path SSD_PATH_AUTO resolves to for these dims on the current device
- * (SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED), or -(ssd_status_t) if the dims are
+ * (SSD_PATH_SEQUENTIAL, SSD_PATH_CHUNKED or SSD_PATH_DECODE), or
+ * -(ssd_status_t) if the dims are
  * invalid or unsupported.  Host only; launches nothing. */
 int32_t ssd_select_path(const ssd_dims_t *dims);
 

@@ -43,7 +43,7 @@ ssd_status_t check_dims(const ssd_dims_t *d, Sizes *sz)
         return SSD_ERR_UNSUPPORTED;
     const uint32_t path = d->flags & SSD_PATH_MASK;
     if ((d->flags & ~(SSD_PATH_MASK | SSD_SCHEDULE_REQUEST_MASK | SSD_DIAG_STALL_HANDOFF)) != 0 ||
-        path > SSD_PATH_CHUNKED)
+        path > SSD_PATH_DECODE)
         return SSD_ERR_INVALID_DIMS;
     int64_t bl, blh, t;
     const int64_t es = (int64_t)elem_size(d->dtype);
@@ -114,6 +114,11 @@ bool device_is_gb300_class()
 int32_t resolve_path(const ScanArgs &a, uint32_t requested, bool probe_device)
 {
     const bool seq_ok = seq_supported(a.headdim, a.dstate);
+    const bool decode_ok = decode_supported(a);
+    if (requested == SSD_PATH_DECODE)
+        return decode_ok ? (int32_t)SSD_PATH_DECODE : -(int32_t)SSD_ERR_UNSUPPORTED;
+    if (requested == SSD_PATH_AUTO && decode_ok)
+        return SSD_PATH_DECODE;
     const bool chunk_ok = chunk_supported(a) && (!probe_device || device_is_gb300_class());
     if (requested == SSD_PATH_SEQUENTIAL)
         return seq_ok ? (int32_t)SSD_PATH_SEQUENTIAL : -(int32_t)SSD_ERR_UNSUPPORTED;
@@ -151,14 +156,20 @@ cudaMemPool_t scratch_pool(int dev)
     return pools[dev];
 }
 
+// The paths that need no scratch: the sequential scan and the decode step.
+ssd_status_t launch_direct(const ScanArgs &a, int32_t path, cudaStream_t st)
+{
+    const cudaError_t e = path == SSD_PATH_DECODE ? decode_launch(a, st) : seq_launch(a, st);
+    return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 ssd_status_t run_device(const ScanArgs &a, uint32_t requested, cudaStream_t st)
 {
     const int32_t path = resolve_path(a, requested, true);
     if (path < 0)
         return (ssd_status_t)(-path);
-    if (path == SSD_PATH_SEQUENTIAL) {
-        return seq_launch(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
-    }
+    if (path != SSD_PATH_CHUNKED)
+        return launch_direct(a, path, st);
     const size_t ws_bytes = chunk_workspace_bytes(a);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess)
@@ -443,8 +454,8 @@ ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt
     const int32_t path = resolve_path(a, dims->flags & SSD_PATH_MASK, true);
     if (path < 0)
         return (ssd_status_t)(-path);
-    if (path == SSD_PATH_SEQUENTIAL)
-        return seq_launch(a, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (path != SSD_PATH_CHUNKED)
+        return launch_direct(a, path, st);
     const size_t need = chunk_workspace_bytes(a);
     if (workspace_bytes < need)
         return SSD_ERR_SCRATCH_LIMIT;

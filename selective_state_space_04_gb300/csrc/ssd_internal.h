@@ -36,6 +36,10 @@ struct ScanArgs {
 bool seq_supported(int headdim, int dstate);
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);
 
+// ---- decode step (seqlen 1): ssd_decode.cu
+bool decode_supported(const ScanArgs &a);
+cudaError_t decode_launch(const ScanArgs &a, cudaStream_t stream);
+
 // ---- chunked tcgen05 path: ssd_chunk.cu
 bool chunk_supported(const ScanArgs &a);
 // Bytes of scratch the chunked path needs for these sizes (flags and, when

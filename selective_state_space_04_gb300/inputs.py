@@ -62,6 +62,9 @@ WORKLOADS = {
     "long_context_64k": Workload("long_context_64k", 1, 65536, 32, 64, 128, 8, 256, "bf16", True),
     # many 64-token sequences with per-sequence state in and out
     "many_short_seqs": Workload("many_short_seqs", 256, 64, 48, 64, 128, 1, 64, "bf16", True),
+    # one decode step of the 2.7B layer's SSM for 128 sequences: one token each,
+    # the carried state in and the updated state out
+    "decode_2p7b_128seq": Workload("decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 256, "bf16", True),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}

@@ -16,8 +16,9 @@ PATH_AUTO = 0
 DIAG_STALL_HANDOFF = 0x100
 PATH_SEQUENTIAL = 1
 PATH_CHUNKED = 2
+PATH_DECODE = 3
 _PATHS = {"auto": PATH_AUTO, "sequential": PATH_SEQUENTIAL, "seq": PATH_SEQUENTIAL,
-          "chunked": PATH_CHUNKED}
+          "chunked": PATH_CHUNKED, "decode": PATH_DECODE}
 
 DTYPE_F32 = 0
 DTYPE_BF16 = 1

@@ -177,3 +177,24 @@ def test_schedule_request_bits(libssd):
     d = libssd.make_dims(1, 64, 2, 8, 16, 1, 16, "f32")
     d.flags = 0x40     # beyond the schedule request field
     assert lib.ssd_select_path(ctypes.byref(d)) == -1
+
+
+def test_decode_path_selection(libssd):
+    lib = libssd.lib()
+    # one step: the decode path, with no scratch and one launch
+    for dtype in ("bf16", "f32"):
+        d = libssd.make_dims(4, 1, 8, 64, 128, 2, 256, dtype)
+        assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_DECODE
+        assert lib.ssd_launches_per_call(ctypes.byref(d)) == 1
+    assert libssd.workspace_size((4, 1, 8, 64), 2, 128, 256) == 0
+    assert libssd.chunk_schedule((4, 1, 8, 64), 2, 128, 256) == "none"
+    # N not a multiple of 4: the auto path falls back; an explicit request is refused
+    d = libssd.make_dims(4, 1, 8, 64, 126, 1, 256, "f32")
+    assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
+    d = libssd.make_dims(4, 1, 8, 64, 126, 1, 256, "f32", path="decode")
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    # more than one step: never the decode path
+    d = libssd.make_dims(4, 2, 8, 64, 128, 1, 256, "f32", path="decode")
+    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    d = libssd.make_dims(4, 2, 8, 64, 128, 1, 256, "f32")
+    assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
