@@ -101,3 +101,40 @@ def make_inputs(w: Workload, seed: int = 0) -> dict:
     init = torch.from_numpy(normal((Bt, H, P, N), 0.1)) if w.init_state else None
     return dict(x=x, dt_raw=dt_raw, dt_bias=dt_bias, A_log=A_log, B=Bm, C=Cm, D=D,
                 init_state=init)
+
+
+def make_trap_inputs(w: Workload, seed: int = 0) -> dict:
+    """One seeded input set for the trapezoidal (Mamba-3 SISO) scan of
+    workload ``w``, as CPU torch tensors.
+
+    Keys (draw order): v [B,L,H,P] ~ N(0,1), k [B,L,G,N] ~ N(0,1),
+    q [B,L,G,N] ~ N(0,1) (storage dtype); dt [B,L,H] = exp(U[ln 1e-3, ln 1e-1]),
+    a [B,L,H] ~ -U[1, 16] (a per-token decay rate), trap [B,L,H] ~ U[0, 1]
+    (a post-sigmoid mixing weight), D [H] ~ N(0,1) (fp32); when
+    ``w.init_state``: h0 [B,H,P,N] ~ N(0, 0.1^2) fp32, k0 [B,H,N] and
+    v0 [B,H,P] ~ N(0,1) in the storage dtype; else None.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    Bt, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    sd = _TORCH_DTYPE[w.dtype]
+
+    def normal(shape, std=1.0):
+        a = rng.standard_normal(size=shape, dtype=np.float32)
+        if std != 1.0:
+            a *= np.float32(std)
+        return a
+
+    v = torch.from_numpy(normal((Bt, L, H, P))).to(sd)
+    k = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    q = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    dt = torch.from_numpy(np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=(Bt, L, H))).astype(np.float32))
+    a = torch.from_numpy((-rng.uniform(1.0, 16.0, size=(Bt, L, H))).astype(np.float32))
+    trap = torch.from_numpy(rng.uniform(0.0, 1.0, size=(Bt, L, H)).astype(np.float32))
+    D = torch.from_numpy(normal((H,)))
+    if w.init_state:
+        h0 = torch.from_numpy(normal((Bt, H, P, N), 0.1))
+        k0 = torch.from_numpy(normal((Bt, H, N))).to(sd)
+        v0 = torch.from_numpy(normal((Bt, H, P))).to(sd)
+    else:
+        h0 = k0 = v0 = None
+    return dict(v=v, k=k, q=q, dt=dt, a=a, trap=trap, D=D, h0=h0, k0=k0, v0=v0)
