@@ -80,6 +80,7 @@ KERNEL_SOURCES = {
     "ssd_chunk_fused_kernel": ("ssd_chunk.cu", "ptx.cuh", "tmap.h"),
     "ssd_decode_kernel": ("ssd_decode.cu",),
     "ssd_seq_kernel": ("ssd_seq.cu",),
+    "ssd_trap_seq_kernel": ("ssd_trap.cu",),
 }
 
 
@@ -451,6 +452,185 @@ def run_reference(args, w: Workload):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ trapezoidal scan
+TRAP_KEYS = ("v", "k", "q", "dt", "a", "trap", "D", "h0", "k0", "v0")
+
+
+def trap_algorithmic_bytes(w: Workload) -> int:
+    """Bytes the trapezoidal scan must move at least once: read v, k, q, dt, a,
+    trap, D and the carried states (when given); write y and the states."""
+    es = 2 if w.dtype == "bf16" else 4
+    BL, BH = w.batch * w.seqlen, w.batch * w.nheads
+    vy = 2 * BL * w.nheads * w.headdim * es
+    kq = 2 * BL * w.ngroups * w.dstate * es
+    coef = 3 * BL * w.nheads * 4
+    states = BH * (w.headdim * w.dstate * 4 + (w.dstate + w.headdim) * es)
+    return vy + kq + coef + w.nheads * 4 + (states if w.init_state else 0) + states
+
+
+def trap_oracle_rate(w: Workload, inp: dict, nb: int, min_seconds: float = 0.0):
+    """token*heads/s of the fp64 trapezoidal oracle on the first nb batch rows
+    (all heads, all steps), repeated until min_seconds have passed."""
+    from oracle.trap import trap_fwd
+    sl = {n: (None if inp[n] is None else (inp[n] if n == "D" else inp[n][:nb])) for n in TRAP_KEYS}
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        trap_fwd(**sl)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    th = nb * w.seqlen * w.nheads
+    return th * reps / dt, (f"{nb} of {w.batch} batch rows x {w.nheads} heads x {w.seqlen} steps "
+                            f"({th} token*heads), {reps} run(s) in {dt:.2f} s")
+
+
+def trap_sample_rows(w: Workload, inp: dict, target_s: float) -> int:
+    rate, _ = trap_oracle_rate(w, inp, 1)
+    return max(1, min(w.batch, int(target_s * rate / (w.seqlen * w.nheads))))
+
+def run_gpu_trap(args, w: Workload):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd
+    from selective_state_space_04_gb300.inputs import make_trap_inputs
+
+    inp = make_trap_inputs(w, seed=args.seed + rank)
+    d = {n: (None if inp[n] is None else inp[n].to(dev)) for n in TRAP_KEYS}
+    y = torch.empty_like(d["v"])
+    hf = torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32, device=dev)
+    kf = torch.empty((w.batch, w.nheads, w.dstate), dtype=d["v"].dtype, device=dev)
+    vf = torch.empty((w.batch, w.nheads, w.headdim), dtype=d["v"].dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        ssd.ssd_trap_scan_fwd(*(d[n] for n in TRAP_KEYS), y=y, h_final=hf, k_final=kf, v_final=vf,
+                              stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    launches0 = ssd.launch_count()
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+    launches = ssd.launch_count() - launches0
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    th = w.token_heads
+    value = world * th * args.steps / (total_ms / 1e3)
+
+    # end to end: every step copies its inputs from pinned host memory, runs the
+    # scan through the public call and copies y and the states back
+    pin = {n: (None if inp[n] is None else inp[n].contiguous().pin_memory()) for n in TRAP_KEYS}
+    outs = [(y, torch.empty(tuple(y.shape), dtype=y.dtype).pin_memory()),
+            (hf, torch.empty(tuple(hf.shape), dtype=hf.dtype).pin_memory()),
+            (kf, torch.empty(tuple(kf.shape), dtype=kf.dtype).pin_memory()),
+            (vf, torch.empty(tuple(vf.shape), dtype=vf.dtype).pin_memory())]
+
+    def step_e2e():
+        for n in TRAP_KEYS:
+            if pin[n] is not None:
+                d[n].copy_(pin[n], non_blocking=True)
+        step()
+        for dv, hv in outs:
+            hv.copy_(dv, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    step_e2e()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_e2e()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev)
+    h2d = sum(t.numel() * t.element_size() for t in pin.values() if t is not None)
+    d2h = sum(hv.numel() * hv.element_size() for _, hv in outs)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    alg_bytes = trap_algorithmic_bytes(w)
+    avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = alg_bytes / avg_launch_s / 1e9
+    kernel = "ssd_trap_seq_kernel"
+    line = {
+        "metric": "trapezoidal (Mamba-3 SISO) scan fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "op": "trap", "batch": w.batch, "seqlen": w.seqlen,
+                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "init_state": w.init_state, "path": "sequential",
+                   "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
+                     "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3},
+        "e2e": {"value": world * th * e2e_steps / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                "api": "ssd_trap_scan_fwd with pinned host copies in and out"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        nb = trap_sample_rows(w, inp, 10.0)
+        v, sample = trap_oracle_rate(w, inp, nb, min_seconds=10.0)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_trap(args, w: Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from selective_state_space_04_gb300.inputs import make_trap_inputs
+    inp = make_trap_inputs(w, seed=args.seed)
+    nb = trap_sample_rows(w, inp, min(10.0, max(0.02, 120.0 / (args.steps + args.warmup))))
+    for _ in range(args.warmup):
+        trap_oracle_rate(w, inp, nb)
+    secs, th_total, sample = 0.0, 0, ""
+    for _ in range(args.steps):
+        v, sample = trap_oracle_rate(w, inp, nb)
+        th = nb * w.seqlen * w.nheads
+        secs += th / v
+        th_total += th
+    value = th_total / secs
+    line = {
+        "impl": "reference",
+        "metric": "trapezoidal (Mamba-3 SISO) scan fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "op": "trap", "batch": w.batch, "seqlen": w.seqlen,
+                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "init_state": w.init_state, "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "per step: " + sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -464,7 +644,9 @@ def main():
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least 3 untimed warm-up steps
     w = WORKLOADS[args.workload]
-    if args.impl == "reference":
+    if w.op == "trap":
+        (run_reference_trap if args.impl == "reference" else run_gpu_trap)(args, w)
+    elif args.impl == "reference":
         run_reference(args, w)
     else:
         run_gpu(args, w)

@@ -204,6 +204,51 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
                                   const float *D, const float *init_state, void *y,
                                   float *final_state, const ssd_dims_t *dims, void *stream);
 
+/*
+ * ssd_trap_scan_fwd -- the trapezoidal (Mamba-3 SISO) scan, forward.
+ *
+ * The Mamba-3 SISO GPU forward of the pages replaces the exponential
+ * recurrence by a trapezoidal one (module header of its forward pass: "Trapezoidal
+ * recurrence (alpha/beta/gamma)", "additional persistent state: k_state,
+ * v_state"; step F5b: alpha = exp(a dt), beta = alpha dt (1 - trap),
+ * gamma = trap dt).  Per batch row b and head h, with v = x, k = B, q = C of
+ * the head's group g = h / (H/G):
+ *   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
+ *   y_t = q_t^T h_t + D_h v_t
+ * where k_{-1}, v_{-1} are the carried k_state and v_state.  The pages print
+ * the coefficients and the k/v states but not the recurrence; the form above
+ * is the reading they support.  The coefficient step is fused: the call takes
+ * dt, a and trap per token.
+ *
+ * Arguments are DEVICE pointers of the current device, owned by the caller,
+ * contiguous, 16-byte aligned; dims as for ssd_scan_fwd (dtype: x, B, C, y
+ * and the k/v states; chunk is ignored; flags: SSD_PATH_AUTO or
+ * SSD_PATH_SEQUENTIAL only, both the sequential kernel).
+ *   v     [B,L,H,P]   k, q [B,L,G,N]   (dtype)
+ *   dt, a, trap [B,L,H] fp32: step size (> 0), per-token decay rate (a <= 0 for
+ *                       a decaying state), mixing weight in [0, 1]
+ *   D [H] fp32
+ *   h0, h_final [B,H,P,N] fp32; k0, k_final [B,H,N] (dtype); v0, v_final
+ *                       [B,H,P] (dtype).  Inputs may be NULL (zero), outputs
+ *                       NULL (not written).  Each output may be the same
+ *                       pointer as its input (in place) but must not
+ *                       overlap anything else.  k_final[b,h] = k[b,L-1,g] and
+ *                       v_final[b,h] = v[b,L-1,h]: the next call continues
+ *                       from (h_final, k_final, v_final).
+ *   y [B,L,H,P] (dtype), overlapping no input.
+ * Supported: N % 4 == 0, N <= 512; P <= 128 for N <= 128, P <= 64 for
+ * N <= 256, P <= 32 for N <= 512; fp32 or bf16.
+ * Returns SSD_OK, or an error as ssd_scan_fwd (SSD_ERR_INVALID_DIMS also for
+ * flags other than a path; SSD_ERR_UNSUPPORTED for another path or an
+ * unsupported shape); nothing is enqueued on error.  seqlen 0 passes the
+ * states through.  Enqueues on `stream` only; never synchronises.
+ */
+ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, const float *dt,
+                               const float *a, const float *trap, const float *D,
+                               const float *h0, const void *k0, const void *v0, void *y,
+                               float *h_final, void *k_final, void *v_final,
+                               const ssd_dims_t *dims, void *stream);
+
 /* Which path SSD_PATH_AUTO resolves to for these dims on the current device
  * (SSD_PATH_SEQUENTIAL, SSD_PATH_CHUNKED or SSD_PATH_DECODE), or
  * -(ssd_status_t) if the dims are

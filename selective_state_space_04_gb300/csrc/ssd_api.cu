@@ -534,4 +534,87 @@ const char *ssd_status_string(int32_t status)
 
 int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
+ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, const float *dt, const float *a,
+                               const float *trap, const float *D, const float *h0, const void *k0,
+                               const void *v0, void *y, float *h_final, void *k_final, void *v_final,
+                               const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    const uint32_t path = dims->flags & SSD_PATH_MASK;
+    if ((dims->flags & ~SSD_PATH_MASK) != 0)
+        return SSD_ERR_INVALID_DIMS;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+        return SSD_ERR_UNSUPPORTED;
+    const int64_t es = dims->dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    const int64_t kst = dims->batch * dims->nheads * dims->dstate * es;   // k_state bytes
+    const int64_t vst = dims->batch * dims->nheads * dims->headdim * es;  // v_state bytes
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!v || !k || !q || !dt || !a || !trap || !D || !y))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {v, k, q, dt, a, trap, D, h0, k0, v0, y, h_final, k_final, v_final};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    // outputs overlap no input (each state may be updated in place) and no other output
+    const void *ins[] = {v, k, q, dt, a, trap, D, h0, k0, v0};
+    const int64_t inb[] = {sz.x, sz.bc, sz.bc, sz.dt, sz.dt, sz.dt, sz.par, sz.state, kst, vst};
+    const void *outs[] = {work ? y : nullptr, h_final, k_final, v_final};
+    const int64_t outb[] = {sz.x, sz.state, kst, vst};
+    const void *same[] = {nullptr, h0, k0, v0};   // the input each output may replace exactly
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 10; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i]) && !(outs[o] == same[o] && ins[i] == same[o]))
+                return SSD_ERR_ALIASING;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlaps(outs[o], outb[o], outs[o2], outb[o2]))
+                return SSD_ERR_ALIASING;
+    }
+    if (dims->batch == 0)
+        return SSD_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->seqlen == 0) {
+        // no steps: every carried state passes through unchanged (zero when not given)
+        const void *src[] = {h0, k0, v0};
+        void *dst[] = {h_final, k_final, v_final};
+        const int64_t nb[] = {sz.state, kst, vst};
+        for (int i = 0; i < 3; ++i) {
+            if (!dst[i] || nb[i] == 0 || src[i] == dst[i])
+                continue;
+            const cudaError_t e = src[i] ? cudaMemcpyAsync(dst[i], src[i], (size_t)nb[i], cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(dst[i], 0, (size_t)nb[i], st);
+            if (e != cudaSuccess)
+                return SSD_ERR_CUDA;
+        }
+        return SSD_OK;
+    }
+    TrapArgs ta;
+    ta.v = v;
+    ta.k = k;
+    ta.q = q;
+    ta.dt = dt;
+    ta.a = a;
+    ta.trap = trap;
+    ta.D = D;
+    ta.h0 = h0;
+    ta.k0 = k0;
+    ta.v0 = v0;
+    ta.y = y;
+    ta.h_final = h_final;
+    ta.k_final = k_final;
+    ta.v_final = v_final;
+    ta.batch = dims->batch;
+    ta.seqlen = dims->seqlen;
+    ta.nheads = dims->nheads;
+    ta.headdim = dims->headdim;
+    ta.dstate = dims->dstate;
+    ta.ngroups = dims->ngroups;
+    ta.dtype = dims->dtype;
+    if (!trap_supported(ta))
+        return SSD_ERR_UNSUPPORTED;
+    return trap_launch(ta, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 }  // extern "C"

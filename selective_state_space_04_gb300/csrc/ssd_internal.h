@@ -32,6 +32,24 @@ struct ScanArgs {
                               // if the one it would choose needs more scratch than this
 };
 
+// The trapezoidal (Mamba-3 SISO) scan, after validation.  Device pointers.
+struct TrapArgs {
+    const void *v, *k, *q;               // x [B,L,H,P]; B, C [B,L,G,N] (storage dtype)
+    const float *dt, *a, *trap, *D;       // [B,L,H] x3, [H]
+    const float *h0;                      // [B,H,P,N] or null
+    const void *k0, *v0;                  // [B,H,N], [B,H,P] (storage dtype) or null
+    void *y;                              // [B,L,H,P]
+    float *h_final;                       // or null
+    void *k_final, *v_final;              // or null
+    int64_t batch, seqlen;
+    int nheads, headdim, dstate, ngroups;
+    int dtype;
+};
+
+// ---- trapezoidal scan: ssd_trap.cu
+bool trap_supported(const TrapArgs &a);
+cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream);
+
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);

@@ -1,0 +1,328 @@
+// ssd_trap.cu -- the trapezoidal (Mamba-3 SISO) scan, sequential in time.
+//
+// Per batch row b and head h, with v = x, k = B, q = C of the head's group
+// (the Mamba-3 SISO GPU forward of the pages: "trapezoidal recurrence
+// (alpha/beta/gamma) instead of exponential", step F5b for the coefficients,
+// and the persistent k_state / v_state):
+//   alpha_t = exp(a_t dt_t),  beta_t = alpha_t dt_t (1 - trap_t),  gamma_t = trap_t dt_t
+//   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
+//   y_t = q_t^T h_t + D v_t
+// k_{-1}, v_{-1} are the carried k/v states; the state is stored [P, N].
+//
+// One CTA per (b, h), one warp per block of state rows p: lane l holds
+// n = 4l .. 4l+3 (+128 per further float4) of each of the warp's rows, so the
+// state in and out are coalesced 512-byte rows (at seqlen 1 the kernel is a
+// stream of the state, like the decode step), and the state stays in
+// registers for the whole sequence.  Time is walked in blocks whose k, q, v and
+// coefficients are staged in shared memory by the whole CTA; the readout
+// y_t[p] is a warp shuffle reduction.  The coefficient step (F5b) is fused:
+// alpha, beta, gamma are computed from dt, a, trap as they are staged.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+struct TrapParams {
+    const void *v, *k, *q;
+    const float *dt, *a, *trap, *D;
+    const float *h0;
+    const void *k0, *v0;
+    void *y;
+    float *h_final;
+    void *k_final, *v_final;
+    long long L;
+    int H, P, N, G, tblk;
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v)
+{
+    return __float2bfloat16_rn(v);
+}
+
+// rows of one warp: RPW * NV = 8 float4 of state per lane stay in registers,
+// and a CTA has at most 16 warps (so at most 128 registers per thread)
+constexpr int kStateFloat4PerLane = 8;
+constexpr int kMaxWarps = 16;
+
+// Sums each of the R values over the warp's 32 lanes at once (R a power of two
+// <= 32): each butterfly stage exchanges half of the values still held, so R
+// rows take R - 1 + log2(32 / R) shuffles instead of 5 R.  Afterwards vals[0]
+// of lane l is the total of row trap_row<R>(l).
+template <int R>
+__device__ __forceinline__ void warp_sum_rows(float (&vals)[R], int lane)
+{
+    int cnt = R;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        if (cnt > 1) {
+            const int half = cnt >> 1;
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int j = 0; j < R / 2; ++j) {
+                if (j < half) {
+                    const float send = upper ? vals[j] : vals[j + half];
+                    const float keep = upper ? vals[j + half] : vals[j];
+                    vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            cnt = half;
+        } else {
+            vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], o);
+        }
+    }
+}
+
+template <int R>
+__device__ __forceinline__ int trap_row(int lane)
+{
+    int row = 0, half = R >> 1;
+#pragma unroll
+    for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
+        if (lane & o)
+            row += half;
+    return row;
+}
+
+// NV: float4 chunks of a state row per lane (N <= 128 NV); RPW: rows per warp
+template <typename T, int NV>
+__global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams p)
+{
+    constexpr int RPW = kStateFloat4PerLane / NV;
+    extern __shared__ float sm[];
+    const int P = p.P, N = p.N, H = p.H, TB = p.tblk;
+    const long long L = p.L;
+    float *ks = sm;                  // [TB][N]
+    float *qs = ks + TB * N;         // [TB][N]
+    float *vs = qs + TB * N;         // [TB][P]
+    float *cf = vs + TB * P;         // [TB][3]: alpha, beta, gamma
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
+    const long long bh = blockIdx.x;
+    const long long b = bh / H;
+    const int h = (int)(bh - b * H);
+    const int g = h / (H / p.G);
+    const int p0 = warp * RPW;
+
+    const T *vg = static_cast<const T *>(p.v);
+    const T *kg = static_cast<const T *>(p.k);
+    const T *qg = static_cast<const T *>(p.q);
+    T *yg = static_cast<T *>(p.y);
+    const size_t sbase = (size_t)bh * P * N;
+
+    // state rows of this warp, and the previous step's k (lane's n) and v (rows)
+    float4 hs[RPW][NV];
+    float kp[NV][4], vp[RPW];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int pr = p0 + r;
+#pragma unroll
+        for (int c = 0; c < NV; ++c) {
+            const int n = 4 * lane + 128 * c;
+            hs[r][c] = (p.h0 && pr < P && n < N)
+                           ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)pr * N + n))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        vp[r] = (p.v0 && pr < P) ? to_f32<T>(static_cast<const T *>(p.v0)[bh * P + pr]) : 0.f;
+    }
+#pragma unroll
+    for (int c = 0; c < NV; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = 4 * lane + 128 * c + e;
+            kp[c][e] = (p.k0 && n < N) ? to_f32<T>(static_cast<const T *>(p.k0)[bh * N + n]) : 0.f;
+        }
+
+    for (long long t0 = 0; t0 < L; t0 += TB) {
+        const int nt = (int)min((long long)TB, L - t0);
+        __syncthreads();   // the previous block is consumed
+        for (int i = threadIdx.x; i < nt * N; i += nthr) {
+            const int tt = i / N, n = i - tt * N;
+            const size_t gi = ((size_t)(b * L + t0 + tt) * p.G + g) * N + n;
+            ks[i] = to_f32<T>(kg[gi]);
+            qs[i] = to_f32<T>(qg[gi]);
+        }
+        for (int i = threadIdx.x; i < nt * P; i += nthr) {
+            const int tt = i / P, pp = i - tt * P;
+            vs[i] = to_f32<T>(vg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]);
+        }
+        for (int i = threadIdx.x; i < nt; i += nthr) {
+            const size_t ci = (size_t)(b * L + t0 + i) * H + h;
+            const float dt = p.dt[ci];
+            const float alpha = expf(p.a[ci] * dt);
+            cf[3 * i + 0] = alpha;
+            cf[3 * i + 1] = alpha * dt * (1.f - p.trap[ci]);
+            cf[3 * i + 2] = p.trap[ci] * dt;
+        }
+        __syncthreads();
+        for (int i = 0; i < nt; ++i) {
+            const float alpha = cf[3 * i], beta = cf[3 * i + 1], gamma = cf[3 * i + 2];
+            float kt[NV][4], qt[NV][4];
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const int n = 4 * lane + 128 * c;
+                const bool in = n < N;   // N % 4 == 0: whole float4 chunks
+                const float4 k4 = in ? *reinterpret_cast<const float4 *>(ks + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 q4 = in ? *reinterpret_cast<const float4 *>(qs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                kt[c][0] = k4.x; kt[c][1] = k4.y; kt[c][2] = k4.z; kt[c][3] = k4.w;
+                qt[c][0] = q4.x; qt[c][1] = q4.y; qt[c][2] = q4.z; qt[c][3] = q4.w;
+            }
+            float acc[RPW];
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const int pr = p0 + r;
+                const float vt = pr < P ? vs[i * P + pr] : 0.f;
+                const float bv = beta * vp[r], gv = gamma * vt;
+                float s = 0.f;
+#pragma unroll
+                for (int c = 0; c < NV; ++c) {
+                    float4 &x = hs[r][c];
+                    x.x = fmaf(alpha, x.x, fmaf(bv, kp[c][0], gv * kt[c][0]));
+                    x.y = fmaf(alpha, x.y, fmaf(bv, kp[c][1], gv * kt[c][1]));
+                    x.z = fmaf(alpha, x.z, fmaf(bv, kp[c][2], gv * kt[c][2]));
+                    x.w = fmaf(alpha, x.w, fmaf(bv, kp[c][3], gv * kt[c][3]));
+                    s = fmaf(qt[c][0], x.x, s);
+                    s = fmaf(qt[c][1], x.y, s);
+                    s = fmaf(qt[c][2], x.z, s);
+                    s = fmaf(qt[c][3], x.w, s);
+                }
+                acc[r] = s;
+                vp[r] = vt;
+            }
+#pragma unroll
+            for (int c = 0; c < NV; ++c)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    kp[c][e] = kt[c][e];
+            warp_sum_rows<RPW>(acc, lane);
+            const int pr = p0 + trap_row<RPW>(lane);
+            if ((lane & (32 / RPW - 1)) == 0 && pr < P)
+                yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] =
+                    from_f32<T>(fmaf(p.D[h], vs[i * P + pr], acc[0]));
+        }
+    }
+
+    // updated state, and the last step's k and v for the next call
+    if (p.h_final) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const int pr = p0 + r;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const int n = 4 * lane + 128 * c;
+                if (pr < P && n < N)
+                    __stcs(reinterpret_cast<float4 *>(p.h_final + sbase + (size_t)pr * N + n), hs[r][c]);
+            }
+        }
+    }
+    if (p.v_final && lane == 0) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r)
+            if (p0 + r < P)
+                static_cast<T *>(p.v_final)[bh * P + p0 + r] = from_f32<T>(vp[r]);
+    }
+    if (p.k_final && warp == 0) {
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < NV; ++c)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int n = 4 * lane + 128 * c + e;
+                if (n < N)
+                    static_cast<T *>(p.k_final)[bh * N + n] = from_f32<T>(kp[c][e]);
+            }
+    }
+}
+
+int trap_nv(int N) { return N <= 128 ? 1 : (N <= 256 ? 2 : 4); }
+
+// warps per CTA: each holds kStateFloat4PerLane / NV rows
+int trap_warps(int P, int N)
+{
+    const int rpw = kStateFloat4PerLane / trap_nv(N);
+    return (P + rpw - 1) / rpw;
+}
+
+// time steps per staged block: k, q (2N), v (P) and three coefficients per step
+int trap_tblk(int P, int N)
+{
+    const size_t per_step = (size_t)(2 * N + P + 3) * sizeof(float);
+    return (int)std::max<size_t>(1, std::min<size_t>(64, (48u * 1024u) / per_step));
+}
+
+size_t trap_smem(int P, int N, int tb) { return (size_t)tb * (2 * N + P + 3) * sizeof(float); }
+
+template <typename T, int NV>
+cudaError_t trap_launch_nv(const TrapParams &tp, long long grid, int threads, size_t smem, cudaStream_t st)
+{
+    ssd_trap_seq_kernel<T, NV><<<(unsigned)grid, threads, smem, st>>>(tp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t trap_launch_t(int nv, const TrapParams &tp, long long grid, int threads, size_t smem, cudaStream_t st)
+{
+    switch (nv) {
+    case 1: return trap_launch_nv<T, 1>(tp, grid, threads, smem, st);
+    case 2: return trap_launch_nv<T, 2>(tp, grid, threads, smem, st);
+    case 4: return trap_launch_nv<T, 4>(tp, grid, threads, smem, st);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+bool trap_supported(const TrapArgs &a)
+{
+    // whole float4 chunks of a state row, at most 512 states, at most kMaxWarps warps
+    // (P <= 128 for N <= 128, P <= 64 for N <= 256, P <= 32 for N <= 512)
+    return a.dstate % 4 == 0 && a.dstate <= 512 && a.headdim >= 1 && trap_warps(a.headdim, a.dstate) <= kMaxWarps &&
+           a.batch * (long long)a.nheads <= 0x7FFFFFFFLL;
+}
+
+cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream)
+{
+    if (!trap_supported(a))
+        return cudaErrorInvalidValue;
+    TrapParams tp;
+    tp.v = a.v;
+    tp.k = a.k;
+    tp.q = a.q;
+    tp.dt = a.dt;
+    tp.a = a.a;
+    tp.trap = a.trap;
+    tp.D = a.D;
+    tp.h0 = a.h0;
+    tp.k0 = a.k0;
+    tp.v0 = a.v0;
+    tp.y = a.y;
+    tp.h_final = a.h_final;
+    tp.k_final = a.k_final;
+    tp.v_final = a.v_final;
+    tp.L = a.seqlen;
+    tp.H = a.nheads;
+    tp.P = a.headdim;
+    tp.N = a.dstate;
+    tp.G = a.ngroups;
+    tp.tblk = trap_tblk(a.headdim, a.dstate);
+    const size_t smem = trap_smem(a.headdim, a.dstate, tp.tblk);
+    const int threads = 32 * trap_warps(a.headdim, a.dstate);
+    const long long grid = a.batch * (long long)a.nheads;
+    const int nv = trap_nv(a.dstate);
+    cudaError_t e = a.dtype == SSD_DTYPE_BF16 ? trap_launch_t<__nv_bfloat16>(nv, tp, grid, threads, smem, stream)
+                                              : trap_launch_t<float>(nv, tp, grid, threads, smem, stream);
+    if (e == cudaSuccess)
+        note_launches(1);
+    return e;
+}
+
+}  // namespace ssd

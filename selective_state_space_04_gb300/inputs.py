@@ -42,6 +42,7 @@ class Workload:
     chunk: int
     dtype: str          # storage dtype of x, B, C, y: "bf16" or "f32"
     init_state: bool    # whether a non-zero initial state is passed
+    op: str = "ssd"     # "ssd": the Mamba-2 SSD scan; "trap": the trapezoidal (Mamba-3 SISO) scan
 
     @property
     def token_heads(self) -> int:
@@ -65,6 +66,12 @@ WORKLOADS = {
     # one decode step of the 2.7B layer's SSM for 128 sequences: one token each,
     # the carried state in and the updated state out
     "decode_2p7b_128seq": Workload("decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 256, "bf16", True),
+    # trapezoidal (Mamba-3 SISO) scan: many 64-token sequences with the carried
+    # state and k/v states in and out (the short-sequence regime the pages run
+    # sequentially), and one decode step of 128 sequences
+    "trap_many_short_seqs": Workload("trap_many_short_seqs", 256, 64, 48, 64, 128, 1, 1, "bf16", True, "trap"),
+    "trap_decode_2p7b_128seq": Workload("trap_decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 1, "bf16", True,
+                                        "trap"),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}

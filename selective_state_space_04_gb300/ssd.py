@@ -71,6 +71,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_status_string.argtypes = [ctypes.c_int32]
     lib.ssd_abi_version.restype = ctypes.c_int32
     lib.ssd_abi_version.argtypes = []
+    lib.ssd_trap_scan_fwd.restype = ctypes.c_int
+    lib.ssd_trap_scan_fwd.argtypes = [vp] * 14 + [ctypes.POINTER(SsdDims), vp]
     return lib
 
 
@@ -271,3 +273,35 @@ def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, work
                                 ctypes.c_void_p(st.cuda_stream)),
            "ssd_scan_fwd_ws")
     return y, final_state
+
+
+def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, path="auto", y=None,
+                      h_final=None, k_final=None, v_final=None, return_states=True, stream=None):
+    """Trapezoidal (Mamba-3 SISO) scan on CUDA tensors.  Returns
+    ``(y, h_final, k_final, v_final)`` (the states None when not returned).
+
+    ``v [B,L,H,P]``, ``k, q [B,L,G,N]``, ``k0/k_final [B,H,N]`` and
+    ``v0/v_final [B,H,P]`` share one dtype (bf16 or fp32); ``dt, a, trap
+    [B,L,H]``, ``D [H]`` and ``h0/h_final [B,H,P,N]`` are fp32.
+    """
+    Bt, L, H, P = v.shape
+    G, N = k.shape[2], k.shape[3]
+    if y is None:
+        y = torch.empty_like(v)
+    if return_states:
+        if h_final is None:
+            h_final = torch.empty((Bt, H, P, N), dtype=torch.float32, device=v.device)
+        if k_final is None:
+            k_final = torch.empty((Bt, H, N), dtype=v.dtype, device=v.device)
+        if v_final is None:
+            v_final = torch.empty((Bt, H, P), dtype=v.dtype, device=v.device)
+    named = (("v", v), ("k", k), ("q", q), ("dt", dt), ("a", a), ("trap", trap), ("D", D), ("h0", h0),
+             ("k0", k0), ("v0", v0), ("y", y), ("h_final", h_final), ("k_final", k_final), ("v_final", v_final))
+    for name, t in named:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    d = make_dims(Bt, L, H, P, N, G, 1, v.dtype, path)
+    st = torch.cuda.current_stream(v.device) if stream is None else stream
+    _check(_lib.ssd_trap_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
+                                  ctypes.c_void_p(st.cuda_stream)), "ssd_trap_scan_fwd")
+    return y, h_final, k_final, v_final

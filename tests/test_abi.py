@@ -198,3 +198,30 @@ def test_decode_path_selection(libssd):
     assert lib.ssd_select_path(ctypes.byref(d)) == -4
     d = libssd.make_dims(4, 2, 8, 64, 128, 1, 256, "f32")
     assert lib.ssd_select_path(ctypes.byref(d)) == libssd.PATH_SEQUENTIAL
+
+
+def _trap_call(libssd, dims_, **override):
+    lib = libssd.lib()
+    base = 0x10000000
+    # 14 distinct, 16-byte aligned, widely spaced fake addresses (validation only)
+    names = ["v", "k", "q", "dt", "a", "trap", "D", "h0", "k0", "v0", "y", "h_final", "k_final", "v_final"]
+    ptrs = {n: ctypes.c_void_p(base + i * 0x1000000) for i, n in enumerate(names)}
+    ptrs.update(override)
+    return lib.ssd_trap_scan_fwd(*(ptrs[n] for n in names), ctypes.byref(dims_), None)
+
+
+def test_trap_entry_validation_before_cuda(libssd):
+    d = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32")
+    assert _trap_call(libssd, d, v=None) == 2                                  # SSD_ERR_NULL_PTR
+    assert _trap_call(libssd, d, dt=ctypes.c_void_p(0x30000008)) == 3          # SSD_ERR_MISALIGNED
+    assert _trap_call(libssd, d, y=ctypes.c_void_p(0x10000000 + 0x100)) == 7   # y inside v: SSD_ERR_ALIASING
+    # h_final overlapping h0 without being it
+    assert _trap_call(libssd, d, h_final=ctypes.c_void_p(0x10000000 + 7 * 0x1000000 + 0x10)) == 7
+    d2 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="chunked")
+    assert _trap_call(libssd, d2) == 4                                         # SSD_ERR_UNSUPPORTED
+    d3 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", schedule="pieces")
+    assert _trap_call(libssd, d3) == 1                                         # SSD_ERR_INVALID_DIMS
+    d4 = libssd.make_dims(2, 8, 4, 16, 30, 2, 1, "f32")                        # N % 4 != 0
+    assert _trap_call(libssd, d4) == 4
+    # empty batch: nothing to do, no device access
+    assert _trap_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0

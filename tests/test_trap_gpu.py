@@ -1,0 +1,107 @@
+"""GPU parity of the trapezoidal (Mamba-3 SISO) scan against its fp64 oracle.
+
+Metric as for the SSD scan: max|out - ref| / max|ref| over the whole tensor,
+for y and for the updated state; 1e-4 for fp32, 2e-2 for bf16.  The carried
+k and v states are copies of inputs and must match exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle.trap import trap_fwd
+from selective_state_space_04_gb300.inputs import WORKLOADS, Workload, make_trap_inputs
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"bf16": 2e-2, "f32": 1e-4}
+KEYS = ("v", "k", "q", "dt", "a", "trap", "D", "h0", "k0", "v0")
+
+
+@pytest.fixture(scope="module")
+def ssd():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd as mod
+    return mod
+
+
+def relerr(a, ref):
+    a = a.double().cpu().numpy()
+    return float(np.max(np.abs(a - ref)) / max(np.max(np.abs(ref)), 1e-30))
+
+
+def _dev(inp):
+    return {n: (None if inp[n] is None else inp[n].cuda().contiguous()) for n in KEYS}
+
+
+def _run(ssd, d):
+    out = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS))
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("B,L,H,P,N,G,dtype,init", [
+    (1, 64, 2, 8, 16, 1, "f32", False),      # the tiny fp32 shape
+    (2, 100, 4, 64, 128, 2, "f32", True),    # ragged against the 38-step time block
+    (2, 77, 4, 64, 128, 1, "bf16", True),
+    (1, 50, 2, 128, 64, 1, "bf16", True),    # 16 warps of 8 rows
+    (2, 33, 2, 64, 256, 2, "f32", True),     # two float4 per lane
+    (1, 20, 2, 32, 512, 1, "f32", False),    # four float4 per lane
+    (1, 9, 3, 17, 44, 1, "f32", True),       # ragged P and N
+])
+def test_trap_against_oracle(ssd, B, L, H, P, N, G, dtype, init):
+    w = Workload("t", B, L, H, P, N, G, 1, dtype, init)
+    inp = make_trap_inputs(w, seed=120 + N + L)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    y, h, k, v = _run(ssd, _dev(inp))
+    ey, eh = relerr(y, ry), relerr(h, rh)
+    print(f"trap rel err y {ey:.3e} state {eh:.3e}")
+    assert ey <= TOL[dtype] and eh <= TOL[dtype]
+    assert np.array_equal(k.double().cpu().numpy(), rk)
+    assert np.array_equal(v.double().cpu().numpy(), rv)
+
+
+def test_trap_one_step_in_place(ssd):
+    w = Workload("t", 16, 1, 8, 64, 128, 1, 1, "bf16", True)
+    inp = make_trap_inputs(w, seed=131)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    d = _dev(inp)
+    h, k, v = d["h0"].clone(), d["k0"].clone(), d["v0"].clone()
+    y, h2, k2, v2 = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS[:7]), h, k, v, h_final=h, k_final=k, v_final=v)
+    torch.cuda.synchronize()
+    assert h2.data_ptr() == h.data_ptr()
+    assert relerr(y, ry) <= TOL["bf16"] and relerr(h, rh) <= TOL["bf16"]
+    assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
+
+
+def test_trap_split_and_resume_bitwise(ssd):
+    # the carried (h, k, v) are exact, and each step is the same arithmetic
+    w = Workload("t", 2, 90, 4, 64, 128, 2, 1, "bf16", True)
+    d = _dev(make_trap_inputs(w, seed=132))
+    y, h, k, v = _run(ssd, d)
+    cut = 41
+    first = {n: (t[:, :cut].contiguous() if n in KEYS[:6] else t) for n, t in d.items()}
+    y1, h1, k1, v1 = _run(ssd, first)
+    second = {n: (t[:, cut:].contiguous() if n in KEYS[:6] else t) for n, t in d.items()}
+    second.update(h0=h1, k0=k1, v0=v1)
+    y2, h2, k2, v2 = _run(ssd, second)
+    assert torch.equal(torch.cat([y1, y2], dim=1), y)
+    assert torch.equal(h2, h) and torch.equal(k2, k) and torch.equal(v2, v)
+
+
+def test_trap_one_equals_ssd_scan(ssd):
+    # trap = 1 and a = -exp(A_log): the Mamba-2 scan on the sequential path (both fp32)
+    w = WORKLOADS["tiny_fp32"].with_(batch=2, seqlen=70, nheads=4, init_state=True)
+    from selective_state_space_04_gb300.inputs import make_inputs
+    s = {n: (None if t is None else t.cuda()) for n, t in make_inputs(w, seed=133).items()}
+    y_ref, h_ref = ssd.ssd_scan_fwd(s["x"], s["dt_raw"], s["dt_bias"], s["A_log"], s["B"], s["C"], s["D"],
+                                    s["init_state"], chunk=w.chunk, path="sequential")
+    dt = torch.nn.functional.softplus(s["dt_raw"] + s["dt_bias"])
+    a = (-torch.exp(s["A_log"])).expand_as(dt).contiguous()
+    y, h, _, _ = ssd.ssd_trap_scan_fwd(s["x"], s["B"], s["C"], dt.contiguous(), a, torch.ones_like(dt),
+                                       s["D"], s["init_state"])
+    torch.cuda.synchronize()
+    assert float((y - y_ref).abs().max()) <= 1e-5 * float(y_ref.abs().max())
+    assert float((h - h_ref).abs().max()) <= 1e-5 * float(h_ref.abs().max())
