@@ -222,8 +222,12 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
  *
  * Arguments are DEVICE pointers of the current device, owned by the caller,
  * contiguous, 16-byte aligned; dims as for ssd_scan_fwd (dtype: x, B, C, y
- * and the k/v states; chunk is ignored; flags: SSD_PATH_AUTO or
- * SSD_PATH_SEQUENTIAL only, both the sequential kernel).
+ * and the k/v states).  flags: a path only.  SSD_PATH_CHUNKED is the chunked
+ * tcgen05 kernel in a trapezoidal mode (same limits as for ssd_scan_fwd: bf16,
+ * P = 64, N = 128, chunk % 64 == 0, (H/G) even; scratch from the library pool;
+ * one more small launch writes k_final / v_final).  SSD_PATH_SEQUENTIAL is a
+ * sequential kernel (fp32 arithmetic).  SSD_PATH_AUTO takes the chunked kernel
+ * where it applies and seqlen > 1, else the sequential one.
  *   v     [B,L,H,P]   k, q [B,L,G,N]   (dtype)
  *   dt, a, trap [B,L,H] fp32: step size (> 0), per-token decay rate (a <= 0 for
  *                       a decaying state), mixing weight in [0, 1]
@@ -236,8 +240,8 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
  *                       v_final[b,h] = v[b,L-1,h]: the next call continues
  *                       from (h_final, k_final, v_final).
  *   y [B,L,H,P] (dtype), overlapping no input.
- * Supported: N % 4 == 0, N <= 512; P <= 128 for N <= 128, P <= 64 for
- * N <= 256, P <= 32 for N <= 512; fp32 or bf16.
+ * The sequential kernel supports N % 4 == 0, N <= 512; P <= 128 for
+ * N <= 128, P <= 64 for N <= 256, P <= 32 for N <= 512; fp32 or bf16.
  * Returns SSD_OK, or an error as ssd_scan_fwd (SSD_ERR_INVALID_DIMS also for
  * flags other than a path; SSD_ERR_UNSUPPORTED for another path or an
  * unsupported shape); nothing is enqueued on error.  seqlen 0 passes the

@@ -546,7 +546,7 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     const uint32_t path = dims->flags & SSD_PATH_MASK;
     if ((dims->flags & ~SSD_PATH_MASK) != 0)
         return SSD_ERR_INVALID_DIMS;
-    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
         return SSD_ERR_UNSUPPORTED;
     const int64_t es = dims->dtype == SSD_DTYPE_BF16 ? 2 : 4;
     const int64_t kst = dims->batch * dims->nheads * dims->dstate * es;   // k_state bytes
@@ -612,9 +612,43 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     ta.dstate = dims->dstate;
     ta.ngroups = dims->ngroups;
     ta.dtype = dims->dtype;
-    if (!trap_supported(ta))
+    // the chunked tcgen05 kernel in its trapezoidal mode, or the sequential kernel
+    ScanArgs ca = make_args(v, nullptr, nullptr, nullptr, k, q, D, h0, y, h_final, dims);
+    ca.trap = true;
+    ca.tdt = dt;
+    ca.ta = a;
+    ca.ttrap = trap;
+    ca.k0 = k0;
+    ca.v0 = v0;
+    ca.sched_req = 0;
+    const bool chunk_ok = chunk_supported(ca) && device_is_gb300_class();
+    const bool seq_ok = trap_supported(ta);
+    bool chunked;
+    if (path == SSD_PATH_CHUNKED)
+        chunked = true;
+    else if (path == SSD_PATH_SEQUENTIAL)
+        chunked = false;
+    else   // one step is a stream of the state: the sequential kernel
+        chunked = chunk_ok && (dims->seqlen > 1 || !seq_ok);
+    if (chunked ? !chunk_ok : !seq_ok)
         return SSD_ERR_UNSUPPORTED;
-    return trap_launch(ta, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (!chunked)
+        return trap_launch(ta, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool)
+        return SSD_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, chunk_workspace_bytes(ca), pool, st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    ssd_status_t rs = chunk_launch(ca, ws, st);
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rs == SSD_OK)
+        rs = SSD_ERR_CUDA;
+    if (rs == SSD_OK && trap_carry_launch(ta, st) != cudaSuccess)
+        rs = SSD_ERR_CUDA;
+    return rs;
 }
 
 }  // extern "C"

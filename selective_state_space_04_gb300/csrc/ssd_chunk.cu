@@ -79,8 +79,9 @@ constexpr uint32_t kXStageBytes = 2 * kTileBytes;   // x of two heads
 constexpr uint32_t kOffBC = 0;
 constexpr uint32_t kOffX = kOffBC + 2 * kBCStageBytes;
 // decay arrays, 3 buffers (sub-chunk j uses buffer j % 3), each:
-//   cs2 [2][T], dt [2][T], colf [2][T], ecs [2][T], wsc [2][T], dtot [2] (+pad)
-constexpr int kDecayFloats = 5 * 2 * kT + 4;
+//   cs2 [2][T], dt [2][T], colf [2][T], ecs [2][T], wsc [2][T], dtot [2] (+pad),
+//   dcr [2][T] (trapezoidal mode: diagonal weight minus input weight)
+constexpr int kDecayFloats = 6 * 2 * kT + 4;
 constexpr uint32_t kOffDecay = kOffX + 2 * kXStageBytes;
 constexpr uint32_t kOffWsum = kOffDecay + 3 * kDecayFloats * 4;
 constexpr int kMaxHeads = 512;                       // per-head parameters staged in shared memory
@@ -135,6 +136,9 @@ struct ChunkParams {
     int H, span, nranges, nhp, nchains, hpg;   // span = steps per unit (R*Q)
     int nsub_chain;                   // sub-chunks per chain
     int diag_stall;                   // first units wait for a handoff nobody publishes
+    // trapezoidal mode: per-token dt, a, trap [B,L,H]; carried k0 [B,H,N], v0 [B,H,P] (bf16, or null)
+    const float *tdt, *ta, *ttrap;
+    const __nv_bfloat16 *k0, *v0;
     int mode;                         // kChained, kSplitLocal or kSplitEntering
 };
 
@@ -414,12 +418,16 @@ constexpr float kSpanMax = 64.f;
 // rounding while the span stays below kSpanMax (checked by the caller).
 // kMask: some rows are inside or above the group (k = t - s0 < 15): entries
 // with s > t are zeroed and D lands on s == t.
-template <bool kMask>
+// kTrap (the trapezoidal mode): the diagonal entry also gets S[t,t] dc, where
+// dc (dc0, dc1 per head) is the diagonal weight of row t minus its input weight.
+template <bool kMask, bool kTrap = false>
 __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (&m0)[8], uint32_t (&m1)[8], int k,
-                                            float rf0, float rf1, const float *colf, float D0, float D1)
+                                            float rf0, float rf1, const float *colf, float D0, float D1,
+                                            float dc0 = 0.f, float dc1 = 0.f)
 {
     const uint64_t r0 = f32x2(rf0, rf0), r1 = f32x2(rf1, rf1);
     const uint64_t dd0 = f32x2(D0, D0), dd1 = f32x2(D1, D1);
+    const uint64_t cc0 = f32x2(dc0, dc0), cc1 = f32x2(dc1, dc1);
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4) {
         const float4 c0 = *reinterpret_cast<const float4 *>(colf + 4 * i4);
@@ -439,8 +447,13 @@ __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (
             uint64_t v1 = mul_f32x2(ab, rc1[e]);
             if (kMask) {
                 const uint64_t ind = f32x2(i == k ? 1.f : 0.f, i + 1 == k ? 1.f : 0.f);
-                v0 = fma_f32x2(ind, dd0, v0);
-                v1 = fma_f32x2(ind, dd1, v1);
+                if (kTrap) {
+                    v0 = fma_f32x2(ind, fma_f32x2(ab, cc0, dd0), v0);
+                    v1 = fma_f32x2(ind, fma_f32x2(ab, cc1, dd1), v1);
+                } else {
+                    v0 = fma_f32x2(ind, dd0, v0);
+                    v1 = fma_f32x2(ind, dd1, v1);
+                }
             }
             m0[2 * i4 + e] = pack_pair(v0);
             m1[2 * i4 + e] = pack_pair(v1);
@@ -451,8 +464,9 @@ __device__ __forceinline__ void build_group(const uint32_t (&sv)[16], uint32_t (
 // The same group in the direct form exp(cs_t - cs_s) dt_s per entry, for a
 // group whose decay span is too large for the factored form (rare: kept out
 // of line; it reads S from and writes M to tensor memory at `ta` itself).
+// dc0, dc1: diagonal correction as in build_group (0 outside the trapezoidal mode).
 __device__ __noinline__ void build_group_direct(uint32_t ta, int s0, int t, const float *cs2, const float *dtv,
-                                                float D0, float D1)
+                                                float D0, float D1, float dc0, float dc1)
 {
     uint32_t sv[16], m0[8], m1[8];
     tmem_ld16(ta, sv);
@@ -469,8 +483,8 @@ __device__ __noinline__ void build_group_direct(uint32_t ta, int s0, int t, cons
             e0[u] = keep ? v * ex2_approx(cr0 - cs2[s]) * dtv[s] : 0.f;
             e1[u] = keep ? v * ex2_approx(cr1 - cs2[kT + s]) * dtv[kT + s] : 0.f;
             if (s == t) {
-                e0[u] += D0;
-                e1[u] += D1;
+                e0[u] += fmaf(v, dc0, D0);
+                e1[u] += fmaf(v, dc1, D1);
             }
         }
         m0[i >> 1] = pack_bf16x2(e0[0], e0[1]);
@@ -480,8 +494,30 @@ __device__ __noinline__ void build_group_direct(uint32_t ta, int s0, int t, cons
     tmem_st8(ta + 8, m1);
 }
 
-// kPieces: the piece schedule (else the range schedule, or a split pass)
-template <bool kPieces>
+// Trapezoidal mode, per-token values of thread row r of sub-chunk c: dt_t, a_t,
+// trap_t, and dt, trap of the next step (0 and 1 past the end of the sequence,
+// so that the last step's input weight is its own gamma only).
+__device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, const ChunkParams &p, float (&o)[5])
+{
+    const long long t = c.t0() + r;
+    const size_t idx = ((size_t)c.w.b * p.L + t) * p.H + c.w.h0 + hd;
+    o[0] = __ldg(p.tdt + idx);
+    o[1] = __ldg(p.ta + idx);
+    o[2] = __ldg(p.ttrap + idx);
+    const bool more = t + 1 < p.L;
+    o[3] = more ? __ldg(p.tdt + idx + p.H) : 0.f;
+    o[4] = more ? __ldg(p.ttrap + idx + p.H) : 1.f;
+}
+
+// kPieces: the piece schedule (else the range schedule, or a split pass).
+// kTrap: the trapezoidal (Mamba-3 SISO) recurrence
+//   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
+// (alpha = exp(a dt), beta = alpha dt (1 - trap), gamma = trap dt) evaluated as
+// this kernel's SSD recurrence on h~_t = h_t + (beta_{t+1}/alpha_{t+1}) k_t v_t^T:
+// decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
+// alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
+// (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
+template <bool kPieces, bool kTrap>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
@@ -499,8 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     for (int h = threadIdx.x; h < p.H; h += blockDim.x) {
-        hA2[h] = -expf(p.A_log[h]) * 1.4426950408889634f;
-        hBias[h] = p.dt_bias[h];
+        if constexpr (!kTrap) {   // the trapezoidal mode has per-token a and dt instead
+            hA2[h] = -expf(p.A_log[h]) * 1.4426950408889634f;
+            hBias[h] = p.dt_bias[h];
+        }
         hD[h] = p.D[h];
     }
 
@@ -708,22 +746,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         Cursor cur;
         bool has = cursor_first<kPieces>(cur, p);
         float dt_raw = 0.f;
-        if (has && r < cur.valid())
-            dt_raw = __ldg(p.dt_raw + ((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + cur.w.h0 + hd);
+        float tq[5] = {0.f, 0.f, 0.f, 0.f, 0.f};   // trapezoidal mode: see load_trap_tok
+        if (has && r < cur.valid()) {
+            if constexpr (kTrap)
+                load_trap_tok(cur, r, hd, p, tq);
+            else
+                dt_raw = __ldg(p.dt_raw + ((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + cur.w.h0 + hd);
+        }
         for (uint32_t j = 0; has; ++j) {
             Cursor nxt = cur;
             const bool has_next = cursor_next<kPieces>(nxt, p);
             float dt_next = 0.f;   // issued one sub-chunk ahead
-            if (has_next && r < nxt.valid())
-                dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
+            float tn[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+            if (has_next && r < nxt.valid()) {
+                if constexpr (kTrap)
+                    load_trap_tok(nxt, r, hd, p, tn);
+                else
+                    dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
+            }
             const int hh = cur.w.h0 + hd;
             float *dk = decay_base + (j % 3) * kDecayFloats;
             float *cs2 = dk, *dtv = dk + 2 * kT, *colf = dk + 4 * kT, *ecs = dk + 6 * kT,
                   *wsc = dk + 8 * kT, *dtot = dk + 10 * kT;
-            float dt = 0.f;
-            if (r < cur.valid())
-                dt = softplus_f32(dt_raw + hBias[hh]);
-            float l = dt * hA2[hh];
+            // log2 decay l and input weight wgt of this step; dcv: diagonal weight minus wgt
+            float l, wgt, dcv = 0.f;
+            if constexpr (kTrap) {
+                const float carried = tq[3] * (1.f - tq[4]);   // dt_{t+1} (1 - trap_{t+1})
+                l = tq[1] * tq[0] * 1.4426950408889634f;
+                wgt = fmaf(tq[2], tq[0], carried);
+                dcv = -carried;
+            } else {
+                float dt = 0.f;
+                if (r < cur.valid())
+                    dt = softplus_f32(dt_raw + hBias[hh]);
+                l = dt * hA2[hh];
+                wgt = dt;
+            }
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float nb = __shfl_up_sync(0xffffffffu, l, o);
@@ -744,10 +802,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             l += pre;
             const float l_end = __shfl_sync(0xffffffffu, l, lane | 15);   // cs at the end of this 16-step group
             cs2[hd * kT + r] = l;
-            dtv[hd * kT + r] = dt;
-            colf[hd * kT + r] = ex2_approx(l_end - l) * dt;
+            dtv[hd * kT + r] = wgt;
+            colf[hd * kT + r] = ex2_approx(l_end - l) * wgt;
             ecs[hd * kT + r] = ex2_approx(l);                 // exp(cs_t), scales C P
-            wsc[hd * kT + r] = ex2_approx(tot - l) * dt;      // state input weight
+            wsc[hd * kT + r] = ex2_approx(tot - l) * wgt;     // state input weight
+            if constexpr (kTrap)
+                dk[10 * kT + 4 + hd * kT + r] = dcv;
             if (r == 0)
                 dtot[hd] = ex2_approx(tot);                   // state decay over the sub-chunk
             if (!group_sync(&bars[BAR_MSYNC], msync, p))
@@ -762,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
                 const float ct0 = cs2[r], ct1 = cs2[kT + r];
+                const float dc0 = kTrap ? dk[10 * kT + 4 + r] : 0.f, dc1 = kTrap ? dk[11 * kT + 4 + r] : 0.f;
 #pragma unroll 1
                 for (int G = hd; G < 8; G += 2) {
                     const uint32_t ta = tmem + lane_addr + kColSM + 16 * G;
@@ -769,7 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s0 = 16 * G;
                     if (G <= 2 * q + 1 && G >= 2 * q &&
                         !(cs2[s0] - cs2[s0 + 15] <= kSpanMax && cs2[kT + s0] - cs2[kT + s0 + 15] <= kSpanMax)) {
-                        build_group_direct(ta, s0, r, cs2, dtv, D0, D1);
+                        build_group_direct(ta, s0, r, cs2, dtv, D0, D1, dc0, dc1);
                         continue;
                     }
                     if (G > 2 * q + 1) {
@@ -788,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (G < 2 * q)
                             build_group<false>(sv, m0, m1, 0, rf0, rf1, colf + s0, 0.f, 0.f);
                         else
-                            build_group<true>(sv, m0, m1, r - s0, rf0, rf1, colf + s0, D0, D1);
+                            build_group<true, kTrap>(sv, m0, m1, r - s0, rf0, rf1, colf + s0, D0, D1, dc0, dc1);
                     }
                     tmem_st8(ta, m0);
                     tmem_st8(ta + 8, m1);
@@ -805,6 +866,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             cur = nxt;
             has = has_next;
             dt_raw = dt_next;
+#pragma unroll
+            for (int i = 0; i < 5; ++i)
+                tq[i] = tn[i];
         }
     } else if (warp < kProducerWarp) {
         // ------------------------------------------------------------ state group
@@ -872,6 +936,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
                         v[i >> 5][i & 31] = 0u;
+                }
+                if constexpr (kTrap) {
+                    // the chain's first step also takes the carried k0 v0^T, weighted
+                    // dt_0 (1 - trap_0) before the decay (see the kernel's comment)
+                    if (cur.first() && p.k0 && p.v0 && p.mode != kSplitLocal) {
+                        const size_t i0 = (size_t)cur.w.b * p.L * p.H + hh;   // step 0
+                        const float c = __ldg(p.tdt + i0) * (1.f - __ldg(p.ttrap + i0));
+                        const float ck = c * __bfloat162float(p.k0[((size_t)cur.w.b * p.H + hh) * kN + r]);
+                        const __nv_bfloat16 *v0 = p.v0 + ((size_t)cur.w.b * p.H + hh) * kP;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            v[i >> 5][i & 31] = __float_as_uint(
+                                fmaf(ck, __bfloat162float(v0[i]), __uint_as_float(v[i >> 5][i & 31])));
+                    }
                 }
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
@@ -1181,7 +1259,10 @@ Geometry geometry(const ScanArgs &a)
     if (pieces_ok && a.sched_req == SSD_SCHEDULE_PIECES)
         g.pieces = true;
     g.split = false;
-    const bool split_allowed = a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0);
+    // (the trapezoidal mode has no split schedule: its combine would need the
+    // entering-state correction too)
+    const bool split_allowed =
+        !a.trap && (a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0));
     if (split_allowed && g.nchunks > 1) {
         double best_split = 1e300;
         long long r_split = 1;
@@ -1283,6 +1364,11 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.epoch = next_epoch();
     p.timeout_ns = a.diag_stall ? 20000000ull : 2000000000ull;
     p.diag_stall = a.diag_stall ? 1 : 0;
+    p.tdt = a.tdt;
+    p.ta = a.ta;
+    p.ttrap = a.ttrap;
+    p.k0 = static_cast<const __nv_bfloat16 *>(a.k0);
+    p.v0 = static_cast<const __nv_bfloat16 *>(a.v0);
     if (a.diag_stall && cudaMemsetAsync(ws + 64, 0, 8, stream) != cudaSuccess)
         return SSD_ERR_CUDA;
     p.L = a.seqlen;
@@ -1296,7 +1382,8 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.nchains = (int)geo.nchains;
     p.hpg = a.nheads / a.ngroups;
 
-    auto kernel = geo.pieces ? ssd_chunk_fused_kernel<true> : ssd_chunk_fused_kernel<false>;
+    auto kernel = a.trap ? (geo.pieces ? ssd_chunk_fused_kernel<true, true> : ssd_chunk_fused_kernel<false, true>)
+                         : (geo.pieces ? ssd_chunk_fused_kernel<true, false> : ssd_chunk_fused_kernel<false, false>);
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;

@@ -27,6 +27,12 @@ struct ScanArgs {
     int dtype;                 // ssd_dtype_t
     bool diag_stall;           // SSD_DIAG_STALL_HANDOFF
     int sched_req;             // requested SSD_SCHEDULE_*, or 0: the library chooses
+    // trapezoidal (Mamba-3 SISO) mode of the chunked path: x = v, B = k, C = q,
+    // init_state = h0, final_state = h_final; per-token dt, a, trap replace
+    // dt_raw, dt_bias, A_log; k0, v0 ([B,H,N], [B,H,P], bf16) may be null
+    bool trap = false;
+    const float *tdt = nullptr, *ta = nullptr, *ttrap = nullptr;
+    const void *k0 = nullptr, *v0 = nullptr;
     size_t scratch_cap = 0;   // nonzero: the chunked path takes no split schedule and, when it
                               // chooses, the piece schedule (at most one state slot per SM)
                               // if the one it would choose needs more scratch than this
@@ -49,6 +55,8 @@ struct TrapArgs {
 // ---- trapezoidal scan: ssd_trap.cu
 bool trap_supported(const TrapArgs &a);
 cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream);
+// k_final, v_final (the last step's k and v) after a chunked-path run
+cudaError_t trap_carry_launch(const TrapArgs &a, cudaStream_t stream);
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);

@@ -243,6 +243,21 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
     }
 }
 
+// The carried k and v states after a scan run by the chunked kernel: the last
+// step's k of the head's group and v of the head.  One CTA per (b, h).
+template <typename T>
+__global__ void __launch_bounds__(128) ssd_trap_carry_kernel(const T *v, const T *k, T *k_final, T *v_final,
+                                                             long long L, int H, int P, int N, int G)
+{
+    const long long bh = blockIdx.x;
+    const long long b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / G);
+    for (int i = threadIdx.x; i < N && k_final; i += blockDim.x)
+        k_final[bh * N + i] = k[((b * L + L - 1) * G + g) * N + i];
+    for (int i = threadIdx.x; i < P && v_final; i += blockDim.x)
+        v_final[bh * P + i] = v[((b * L + L - 1) * H + h) * P + i];
+}
+
 int trap_nv(int N) { return N <= 128 ? 1 : (N <= 256 ? 2 : 4); }
 
 // warps per CTA: each holds kStateFloat4PerLane / NV rows
@@ -287,6 +302,26 @@ bool trap_supported(const TrapArgs &a)
     // (P <= 128 for N <= 128, P <= 64 for N <= 256, P <= 32 for N <= 512)
     return a.dstate % 4 == 0 && a.dstate <= 512 && a.headdim >= 1 && trap_warps(a.headdim, a.dstate) <= kMaxWarps &&
            a.batch * (long long)a.nheads <= 0x7FFFFFFFLL;
+}
+
+cudaError_t trap_carry_launch(const TrapArgs &a, cudaStream_t stream)
+{
+    if (!a.k_final && !a.v_final)
+        return cudaSuccess;
+    const long long grid = a.batch * (long long)a.nheads;
+    if (a.dtype == SSD_DTYPE_BF16)
+        ssd_trap_carry_kernel<__nv_bfloat16><<<(unsigned)grid, 128, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(a.v), static_cast<const __nv_bfloat16 *>(a.k),
+            static_cast<__nv_bfloat16 *>(a.k_final), static_cast<__nv_bfloat16 *>(a.v_final), a.seqlen, a.nheads,
+            a.headdim, a.dstate, a.ngroups);
+    else
+        ssd_trap_carry_kernel<float><<<(unsigned)grid, 128, 0, stream>>>(
+            static_cast<const float *>(a.v), static_cast<const float *>(a.k), static_cast<float *>(a.k_final),
+            static_cast<float *>(a.v_final), a.seqlen, a.nheads, a.headdim, a.dstate, a.ngroups);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        note_launches(1);
+    return e;
 }
 
 cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream)

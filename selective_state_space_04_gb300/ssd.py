@@ -275,7 +275,7 @@ def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, work
     return y, final_state
 
 
-def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, path="auto", y=None,
+def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, chunk=256, path="auto", y=None,
                       h_final=None, k_final=None, v_final=None, return_states=True, stream=None):
     """Trapezoidal (Mamba-3 SISO) scan on CUDA tensors.  Returns
     ``(y, h_final, k_final, v_final)`` (the states None when not returned).
@@ -300,7 +300,7 @@ def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, pat
     for name, t in named:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    d = make_dims(Bt, L, H, P, N, G, 1, v.dtype, path)
+    d = make_dims(Bt, L, H, P, N, G, chunk, v.dtype, path)
     st = torch.cuda.current_stream(v.device) if stream is None else stream
     _check(_lib.ssd_trap_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
                                   ctypes.c_void_p(st.cuda_stream)), "ssd_trap_scan_fwd")

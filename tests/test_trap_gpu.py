@@ -36,8 +36,8 @@ def _dev(inp):
     return {n: (None if inp[n] is None else inp[n].cuda().contiguous()) for n in KEYS}
 
 
-def _run(ssd, d):
-    out = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS))
+def _run(ssd, d, path="sequential"):
+    out = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS), path=path)
     torch.cuda.synchronize()
     return out
 
@@ -69,7 +69,8 @@ def test_trap_one_step_in_place(ssd):
     ry, rh, rk, rv = trap_fwd(**inp)
     d = _dev(inp)
     h, k, v = d["h0"].clone(), d["k0"].clone(), d["v0"].clone()
-    y, h2, k2, v2 = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS[:7]), h, k, v, h_final=h, k_final=k, v_final=v)
+    y, h2, k2, v2 = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS[:7]), h, k, v, h_final=h, k_final=k, v_final=v,
+                                          path="sequential")
     torch.cuda.synchronize()
     assert h2.data_ptr() == h.data_ptr()
     assert relerr(y, ry) <= TOL["bf16"] and relerr(h, rh) <= TOL["bf16"]
@@ -101,7 +102,73 @@ def test_trap_one_equals_ssd_scan(ssd):
     dt = torch.nn.functional.softplus(s["dt_raw"] + s["dt_bias"])
     a = (-torch.exp(s["A_log"])).expand_as(dt).contiguous()
     y, h, _, _ = ssd.ssd_trap_scan_fwd(s["x"], s["B"], s["C"], dt.contiguous(), a, torch.ones_like(dt),
-                                       s["D"], s["init_state"])
+                                       s["D"], s["init_state"], path="sequential")
     torch.cuda.synchronize()
     assert float((y - y_ref).abs().max()) <= 1e-5 * float(y_ref.abs().max())
     assert float((h - h_ref).abs().max()) <= 1e-5 * float(h_ref.abs().max())
+
+
+# ------------------------------------------------ chunked tcgen05 kernel, trapezoidal mode
+def _weak(inp):
+    # a = -0.05, dt = 0.01: the state carries across hundreds of steps
+    inp = dict(inp)
+    inp["a"] = torch.full_like(inp["a"], -0.05)
+    inp["dt"] = torch.full_like(inp["dt"], 0.01)
+    return inp
+
+
+@pytest.mark.parametrize("B,L,H,G,init,weak", [
+    (2, 1000, 4, 1, True, False),    # ragged against 128-step sub-chunks
+    (1, 2048, 4, 2, False, True),
+    (2, 3000, 2, 1, True, True),     # several units per chain
+    (3, 1, 4, 1, True, False),       # one step
+    (4, 300, 8, 4, True, False),
+])
+def test_trap_chunked_against_oracle(ssd, B, L, H, G, init, weak):
+    w = Workload("t", B, L, H, 64, 128, G, 256, "bf16", init, "trap")
+    inp = make_trap_inputs(w, seed=140 + L + H)
+    if weak:
+        inp = _weak(inp)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    d = _dev(inp)
+    y, h, k, v = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS), path="chunked")
+    torch.cuda.synchronize()
+    assert ssd.device_error() == 0
+    ey, eh = relerr(y, ry), relerr(h, rh)
+    print(f"trap chunked rel err y {ey:.3e} state {eh:.3e}")
+    assert ey <= TOL["bf16"] and eh <= TOL["bf16"]
+    assert np.array_equal(k.double().cpu().numpy(), rk)
+    assert np.array_equal(v.double().cpu().numpy(), rv)
+    if weak and init:
+        # the carried state matters: without it the output is far off
+        d0 = dict(d, h0=None, k0=None, v0=None)
+        y0, _, _, _ = ssd.ssd_trap_scan_fwd(*(d0[n] for n in KEYS), path="chunked")
+        torch.cuda.synchronize()
+        assert relerr(y0, ry) > 10 * TOL["bf16"]
+
+
+def test_trap_auto_path_is_chunked_and_matches_sequential(ssd):
+    w = Workload("t", 2, 500, 4, 64, 128, 1, 256, "bf16", True, "trap")
+    d = _dev(make_trap_inputs(w, seed=150))
+    launches = ssd.launch_count()
+    y1, h1, k1, v1 = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS))            # auto
+    torch.cuda.synchronize()
+    assert ssd.launch_count() - launches == 2                                 # chunked kernel + k/v carry
+    y2, h2, k2, v2 = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS), path="sequential")
+    torch.cuda.synchronize()
+    assert relerr(y1, y2.double().cpu().numpy()) <= TOL["bf16"]
+    assert relerr(h1, h2.double().cpu().numpy()) <= TOL["bf16"]
+    assert torch.equal(k1, k2) and torch.equal(v1, v2)
+
+
+def test_trap_chunked_in_place_states(ssd):
+    w = Workload("t", 2, 700, 4, 64, 128, 1, 256, "bf16", True, "trap")
+    inp = make_trap_inputs(w, seed=151)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    d = _dev(inp)
+    h, k, v = d["h0"].clone(), d["k0"].clone(), d["v0"].clone()
+    y, _, _, _ = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS[:7]), h, k, v, h_final=h, k_final=k, v_final=v,
+                                       path="chunked")
+    torch.cuda.synchronize()
+    assert relerr(y, ry) <= TOL["bf16"] and relerr(h, rh) <= TOL["bf16"]
+    assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
