@@ -258,6 +258,100 @@ __global__ void __launch_bounds__(128) ssd_trap_carry_kernel(const T *v, const T
         v_final[bh * P + i] = v[((b * L + L - 1) * H + h) * P + i];
 }
 
+// One step (seqlen 1): the state is only streamed in and out, so the layout of
+// the SSD decode step is used: one CTA of 4 warps per (b, h), 8 rows of a warp
+// in flight, each state row one coalesced 512-byte load and store, no staging.
+constexpr int kDecWarps = 4, kDecRows = 8;
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kDecWarps * 32) ssd_trap_decode_kernel(TrapParams p)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, P = p.P, N = p.N;
+    const long long bh = blockIdx.x;   // b * H + h (seqlen 1: also the token index)
+    const long long b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / p.G);
+    const float dt = p.dt[bh], trap = p.trap[bh];
+    const float alpha = expf(p.a[bh] * dt), beta = alpha * dt * (1.f - trap), gamma = trap * dt;
+    const float Dh = p.D[h];
+    const T *kg = static_cast<const T *>(p.k) + (b * p.G + g) * (long long)N;
+    const T *qg = static_cast<const T *>(p.q) + (b * p.G + g) * (long long)N;
+    const T *k0 = p.k0 ? static_cast<const T *>(p.k0) + bh * N : nullptr;
+    float kv[NV][4], qv[NV][4], kp[NV][4];
+#pragma unroll
+    for (int c = 0; c < NV; ++c)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int n = 4 * lane + 128 * c + e;
+            kv[c][e] = n < N ? to_f32<T>(kg[n]) : 0.f;
+            qv[c][e] = n < N ? to_f32<T>(qg[n]) : 0.f;
+            kp[c][e] = (k0 && n < N) ? to_f32<T>(k0[n]) : 0.f;
+        }
+    const T *vg = static_cast<const T *>(p.v) + bh * P;
+    const T *v0 = p.v0 ? static_cast<const T *>(p.v0) + bh * P : nullptr;
+    T *yg = static_cast<T *>(p.y) + bh * P;
+    const size_t sbase = (size_t)bh * P * N;
+    for (int p0 = warp * kDecRows; p0 < P; p0 += kDecWarps * kDecRows) {
+        float4 hv[kDecRows][NV];
+        float vt[kDecRows], vp[kDecRows];
+#pragma unroll
+        for (int i = 0; i < kDecRows; ++i) {
+            const int pr = p0 + i;
+            vt[i] = pr < P ? to_f32<T>(vg[pr]) : 0.f;
+            vp[i] = (v0 && pr < P) ? to_f32<T>(v0[pr]) : 0.f;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const int n = 4 * lane + 128 * c;
+                hv[i][c] = (p.h0 && pr < P && n < N)
+                               ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)pr * N + n))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kDecRows; ++i) {
+            const int pr = p0 + i;
+            const float bv = beta * vp[i], gv = gamma * vt[i];
+            float acc = 0.f;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                float4 &x = hv[i][c];
+                x.x = fmaf(alpha, x.x, fmaf(bv, kp[c][0], gv * kv[c][0]));
+                x.y = fmaf(alpha, x.y, fmaf(bv, kp[c][1], gv * kv[c][1]));
+                x.z = fmaf(alpha, x.z, fmaf(bv, kp[c][2], gv * kv[c][2]));
+                x.w = fmaf(alpha, x.w, fmaf(bv, kp[c][3], gv * kv[c][3]));
+                acc = fmaf(qv[c][0], x.x, acc);
+                acc = fmaf(qv[c][1], x.y, acc);
+                acc = fmaf(qv[c][2], x.z, acc);
+                acc = fmaf(qv[c][3], x.w, acc);
+                const int n = 4 * lane + 128 * c;
+                if (p.h_final && pr < P && n < N)
+                    __stcs(reinterpret_cast<float4 *>(p.h_final + sbase + (size_t)pr * N + n), x);
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0 && pr < P) {
+                yg[pr] = from_f32<T>(fmaf(Dh, vt[i], acc));
+                if (p.v_final)
+                    static_cast<T *>(p.v_final)[bh * P + pr] = vg[pr];
+            }
+        }
+    }
+    if (p.k_final) {   // uniform over the CTA
+        __syncthreads();   // every warp has read k0, which k_final may be
+        if (warp == 0) {
+#pragma unroll
+            for (int c = 0; c < NV; ++c)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int n = 4 * lane + 128 * c + e;
+                    if (n < N)
+                        static_cast<T *>(p.k_final)[bh * N + n] = from_f32<T>(kv[c][e]);
+                }
+        }
+    }
+}
+
 int trap_nv(int N) { return N <= 128 ? 1 : (N <= 256 ? 2 : 4); }
 
 // warps per CTA: each holds kStateFloat4PerLane / NV rows
@@ -279,7 +373,10 @@ size_t trap_smem(int P, int N, int tb) { return (size_t)tb * (2 * N + P + 3) * s
 template <typename T, int NV>
 cudaError_t trap_launch_nv(const TrapParams &tp, long long grid, int threads, size_t smem, cudaStream_t st)
 {
-    ssd_trap_seq_kernel<T, NV><<<(unsigned)grid, threads, smem, st>>>(tp);
+    if (tp.L == 1)
+        ssd_trap_decode_kernel<T, NV><<<(unsigned)grid, kDecWarps * 32, 0, st>>>(tp);
+    else
+        ssd_trap_seq_kernel<T, NV><<<(unsigned)grid, threads, smem, st>>>(tp);
     return cudaGetLastError();
 }
 

@@ -172,3 +172,22 @@ def test_trap_chunked_in_place_states(ssd):
     torch.cuda.synchronize()
     assert relerr(y, ry) <= TOL["bf16"] and relerr(h, rh) <= TOL["bf16"]
     assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("B,H,P,N,G,dtype,init", [
+    (4, 4, 64, 128, 1, "bf16", True),
+    (3, 6, 64, 128, 2, "f32", False),
+    (2, 4, 100, 64, 1, "f32", True),     # P not a multiple of a warp's 8 rows
+    (2, 2, 8, 16, 1, "f32", True),
+    (2, 4, 64, 256, 4, "bf16", True),
+    (1, 2, 32, 512, 1, "f32", True),
+    (1, 3, 17, 44, 1, "f32", False),
+])
+def test_trap_one_step_against_oracle(ssd, B, H, P, N, G, dtype, init):
+    # seqlen 1 runs the decode-layout kernel
+    w = Workload("t", B, 1, H, P, N, G, 256, dtype, init)
+    inp = make_trap_inputs(w, seed=160 + N + P)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    y, h, k, v = _run(ssd, _dev(inp))
+    assert relerr(y, ry) <= TOL[dtype] and relerr(h, rh) <= TOL[dtype]
+    assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
