@@ -145,3 +145,37 @@ def make_trap_inputs(w: Workload, seed: int = 0) -> dict:
     else:
         h0 = k0 = v0 = None
     return dict(v=v, k=k, q=q, dt=dt, a=a, trap=trap, D=D, h0=h0, k0=k0, v0=v0)
+
+
+def make_conv_inputs(w: Workload, K: int = 4, seed: int = 0) -> dict:
+    """Seeded inputs of the causal conv1d + SiLU over the fused x | B | C
+    channels (C = H*P + 2*G*N), as CPU torch tensors.
+
+    Keys (draw order): xbc [B,L,C] ~ N(0,1) (storage dtype); weight [C,K] ~
+    U[-0.5, 0.5], bias [C] ~ U[-0.5, 0.5] (fp32); conv_state [B,K-1,C] ~ N(0,1)
+    (storage dtype) when ``w.init_state``, else None.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sd = _TORCH_DTYPE[w.dtype]
+    C = w.nheads * w.headdim + 2 * w.ngroups * w.dstate
+    xbc = torch.from_numpy(rng.standard_normal(size=(w.batch, w.seqlen, C), dtype=np.float32)).to(sd)
+    weight = torch.from_numpy(rng.uniform(-0.5, 0.5, size=(C, K)).astype(np.float32))
+    bias = torch.from_numpy(rng.uniform(-0.5, 0.5, size=C).astype(np.float32))
+    state = (torch.from_numpy(rng.standard_normal(size=(w.batch, K - 1, C), dtype=np.float32)).to(sd)
+             if w.init_state else None)
+    return dict(xbc=xbc, weight=weight, bias=bias, conv_state=state)
+
+
+def make_gnorm_inputs(w: Workload, seed: int = 0) -> dict:
+    """Seeded inputs of the gated RMSNorm over the H*P channels of a token.
+
+    Keys (draw order): y, z [B,L,H,P] ~ N(0,1) (storage dtype); weight [H*P] ~
+    1 + 0.1 N(0,1) (fp32).
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    sd = _TORCH_DTYPE[w.dtype]
+    shape = (w.batch, w.seqlen, w.nheads, w.headdim)
+    y = torch.from_numpy(rng.standard_normal(size=shape, dtype=np.float32)).to(sd)
+    z = torch.from_numpy(rng.standard_normal(size=shape, dtype=np.float32)).to(sd)
+    weight = torch.from_numpy((1.0 + 0.1 * rng.standard_normal(size=w.nheads * w.headdim)).astype(np.float32))
+    return dict(y=y, z=z, weight=weight)
