@@ -81,6 +81,8 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("ssd_decode.cu",),
     "ssd_seq_kernel": ("ssd_seq.cu",),
     "ssd_trap_seq_kernel": ("ssd_trap.cu",),
+    "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
+    "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
 }
 
 
@@ -637,6 +639,187 @@ def run_reference_trap(args, w: Workload):
     print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------ steps around the scan
+CONV_TAPS = 4
+
+
+def neighbor_setup(w: Workload, dev, seed: int):
+    """(host inputs, device inputs, device outputs, step function, algorithmic
+    bytes, kernel name, oracle function of the first nb batch rows) of the
+    conv1d + SiLU or gated RMSNorm workload ``w``."""
+    from selective_state_space_04_gb300 import ssd
+    from selective_state_space_04_gb300.inputs import make_conv_inputs, make_gnorm_inputs
+    import oracle.neighbors as on
+    es = 2 if w.dtype == "bf16" else 4
+    BL, HP, GN = w.batch * w.seqlen, w.nheads * w.headdim, w.ngroups * w.dstate
+    if w.op == "conv":
+        inp = make_conv_inputs(w, K=CONV_TAPS, seed=seed)
+        d = {n: (None if t is None else t.to(dev)) for n, t in inp.items()}
+        Cc = HP + 2 * GN
+        outs = {"x": torch.empty((w.batch, w.seqlen, w.nheads, w.headdim), dtype=d["xbc"].dtype, device=dev),
+                "B": torch.empty((w.batch, w.seqlen, w.ngroups, w.dstate), dtype=d["xbc"].dtype, device=dev),
+                "C": torch.empty((w.batch, w.seqlen, w.ngroups, w.dstate), dtype=d["xbc"].dtype, device=dev),
+                "conv_state_out": torch.empty((w.batch, CONV_TAPS - 1, Cc), dtype=d["xbc"].dtype, device=dev)}
+
+        def step(stream):
+            ssd.conv1d_silu_fwd(d["xbc"], d["weight"], d["bias"], d["conv_state"], nheads=w.nheads,
+                                headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate, stream=stream, **outs)
+
+        state = w.batch * (CONV_TAPS - 1) * Cc * es
+        nbytes = 2 * BL * Cc * es + Cc * (CONV_TAPS + 1) * 4 + (state if w.init_state else 0) + state
+
+        def ref(nb):
+            on.conv1d_silu(inp["xbc"][:nb], inp["weight"], inp["bias"],
+                           None if inp["conv_state"] is None else inp["conv_state"][:nb],
+                           w.nheads, w.headdim, w.ngroups, w.dstate)
+        return inp, d, outs, step, nbytes, "ssd_conv1d_silu_kernel", ref
+    inp = make_gnorm_inputs(w, seed=seed)
+    d = {n: t.to(dev) for n, t in inp.items()}
+    outs = {"out": torch.empty_like(d["y"])}
+
+    def step(stream):
+        ssd.gated_rmsnorm_fwd(d["y"], d["z"], d["weight"], 1e-6, out=outs["out"], stream=stream)
+
+    def ref(nb):
+        on.gated_rmsnorm(inp["y"][:nb], inp["z"][:nb], inp["weight"])
+    return inp, d, outs, step, 3 * BL * HP * es + HP * 4, "ssd_gated_rmsnorm_kernel", ref
+
+
+def neighbor_oracle_rate(w: Workload, ref, target_s: float, min_seconds: float = 0.0):
+    """(token*heads/s, description) of the fp64 oracle on enough batch rows
+    (whole sequences) for about target_s seconds per run."""
+    t0 = time.perf_counter()
+    ref(1)
+    per_row = max(time.perf_counter() - t0, 1e-6)
+    nb = max(1, min(w.batch, int(target_s / per_row)))
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        ref(nb)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds:
+            break
+    th = nb * w.seqlen * w.nheads
+    return th * reps / dt, (f"{nb} of {w.batch} batch rows x {w.seqlen} steps x {w.nheads} heads "
+                            f"({th} token*heads), {reps} run(s) in {dt:.2f} s")
+
+def run_gpu_neighbor(args, w: Workload):
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, "nccl")
+    from selective_state_space_04_gb300 import build
+    build.build()
+    from selective_state_space_04_gb300 import ssd
+    inp, d, outs, step, alg_bytes, kernel, ref = neighbor_setup(w, dev, args.seed + rank)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(args.warmup):
+        step(stream)
+    torch.cuda.synchronize(dev)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    launches0 = ssd.launch_count()
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            evs[i][0].record(stream)
+            step(stream)
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+    launches = ssd.launch_count() - launches0
+    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
+    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    th = w.token_heads
+    value = world * th * args.steps / (total_ms / 1e3)
+    # end to end: pinned host copies of the inputs in and of the outputs back, every step
+    pin = {n: (None if t is None else t.contiguous().pin_memory()) for n, t in inp.items()}
+    back = {n: torch.empty(tuple(t.shape), dtype=t.dtype).pin_memory() for n, t in outs.items()}
+
+    def step_e2e():
+        for n, t in pin.items():
+            if t is not None:
+                d[n].copy_(t, non_blocking=True)
+        step(stream)
+        for n, t in outs.items():
+            back[n].copy_(t, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    e2e_steps = max(1, min(args.steps, 5))
+    step_e2e()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        step_e2e()
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t0, dev)
+    if rank != 0:
+        return
+    peaks, peak_src = load_peaks()
+    avg_launch_s = statistics.mean(per_launch_ms) / 1e3
+    hbm_peak = float(peaks["hbm_gbs"])
+    achieved = alg_bytes / avg_launch_s / 1e9
+    name = {"conv": "causal conv1d + SiLU", "gnorm": "gated RMSNorm"}[w.op]
+    line = {
+        "metric": f"{name} fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
+                   "init_state": w.init_state, "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_source": peak_src,
+                     "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
+                     "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3},
+        "e2e": {"value": world * th * e2e_steps / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values() if t is not None),
+                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in back.values()),
+                "steps": e2e_steps, "api": "the public call with pinned host copies in and out"},
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, sample = neighbor_oracle_rate(w, ref, 10.0, min_seconds=10.0)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def run_reference_neighbor(args, w: Workload):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    _, _, _, _, _, _, ref = neighbor_setup(w, torch.device("cpu"), args.seed)
+    per_step = min(10.0, max(0.02, 120.0 / (args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        neighbor_oracle_rate(w, ref, per_step)
+    secs, th_total, sample = 0.0, 0, ""
+    for _ in range(args.steps):
+        v, sample = neighbor_oracle_rate(w, ref, per_step)
+        th = int(sample.split("(")[1].split(" ")[0])
+        secs += th / v
+        th_total += th
+    value = th_total / secs
+    name = {"conv": "causal conv1d + SiLU", "gnorm": "gated RMSNorm"}[w.op]
+    line = {
+        "impl": "reference", "metric": f"{name} fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "op": w.op, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
+                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "seed": args.seed},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "per step: " + sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -652,6 +835,8 @@ def main():
     w = WORKLOADS[args.workload]
     if w.op == "trap":
         (run_reference_trap if args.impl == "reference" else run_gpu_trap)(args, w)
+    elif w.op in ("conv", "gnorm"):
+        (run_reference_neighbor if args.impl == "reference" else run_gpu_neighbor)(args, w)
     elif args.impl == "reference":
         run_reference(args, w)
     else:

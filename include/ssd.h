@@ -253,6 +253,46 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
                                float *h_final, void *k_final, void *v_final,
                                const ssd_dims_t *dims, void *stream);
 
+/*
+ * ssd_conv1d_silu_fwd -- the causal depthwise conv1d + SiLU that precedes the
+ * scan in the Mamba blocks of the pages ("causal conv1d over x + B_proj +
+ * C_proj (fused, convD channels)"; the conv1d kernel page:
+ * y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d], zero before the
+ * sequence; "conv1d burnin + fused SiLU" with a carried conv state).  Over
+ * the fused channels c of xbc = [x (H*P) | B (G*N) | C (G*N)]:
+ *   u[b,t,c] = SiLU(bias[c] + sum_{k<K} weight[c,k] xbc[b,t-k,c])
+ * with xbc before t = 0 taken from conv_state (zero when NULL), and u written
+ * split into the scan's x [B,L,H,P], B and C [B,L,G,N].
+ *   xbc [B,L,C], conv_state and conv_state_out [B,K-1,C] (oldest step
+ *     first) in dims->dtype; weight [C,K] and bias [C] (NULL: none) fp32.
+ *   conv_state_out (NULL: not written) receives the last K-1 inputs, from
+ *     which a following call continues; it must not overlap conv_state.
+ * DEVICE pointers, 16-byte aligned, caller-owned; outputs overlap no input.
+ * dims: batch, seqlen, nheads, headdim, dstate, ngroups, dtype as for
+ * ssd_scan_fwd; chunk is ignored (>= 1); flags must be 0.  Supported:
+ * kernel_size 2..4, H*P and G*N multiples of 8, batch <= 65535.  Errors as
+ * ssd_scan_fwd (SSD_ERR_UNSUPPORTED for an unsupported size).  seqlen 0
+ * passes the conv state through.  Enqueues on `stream` only.
+ */
+ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const float *bias,
+                                 const void *conv_state, void *x, void *B, void *C,
+                                 void *conv_state_out, int32_t kernel_size,
+                                 const ssd_dims_t *dims, void *stream);
+
+/*
+ * ssd_gated_rmsnorm_fwd -- the gated output norm after the scan (the Mamba-3
+ * forward of the pages, step F7 with its norm: RMSNorm(y) * weight * SiLU(z)),
+ * per token over its H*P channels:
+ *   out = y / sqrt(mean_c(y^2) + eps) * weight * SiLU(z)
+ *   y, z, out [B,L,H,P] (dims->dtype); weight [H*P] fp32; eps >= 0.
+ * DEVICE pointers, 16-byte aligned, caller-owned; out overlaps no input.
+ * dims as for ssd_conv1d_silu_fwd (dstate, ngroups, chunk ignored beyond their
+ * validation).  Supported: H*P a multiple of 8, at most 16384.  Errors as
+ * ssd_scan_fwd.
+ */
+ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *weight, float eps,
+                                   void *out, const ssd_dims_t *dims, void *stream);
+
 /* Which path SSD_PATH_AUTO resolves to for these dims on the current device
  * (SSD_PATH_SEQUENTIAL, SSD_PATH_CHUNKED or SSD_PATH_DECODE), or
  * -(ssd_status_t) if the dims are

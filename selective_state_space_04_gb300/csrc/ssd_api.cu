@@ -651,4 +651,108 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     return rs;
 }
 
+ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const float *bias,
+                                 const void *conv_state, void *x, void *B, void *C, void *conv_state_out,
+                                 int32_t kernel_size, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if (dims->flags != 0 || kernel_size < 1)
+        return SSD_ERR_INVALID_DIMS;
+    const int64_t es = dims->dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    const int64_t Cc = (int64_t)dims->nheads * dims->headdim + 2 * (int64_t)dims->ngroups * dims->dstate;
+    int64_t xbcb, stb;
+    if (!mul_ok(dims->batch * dims->seqlen, Cc * es, &xbcb) || !mul_ok(dims->batch * (kernel_size - 1), Cc * es, &stb))
+        return SSD_ERR_INVALID_DIMS;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!xbc || !weight || !x || !B || !C))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {xbc, weight, bias, conv_state, x, B, C, conv_state_out};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    const void *ins[] = {xbc, weight, bias, conv_state};
+    const int64_t inb[] = {xbcb, Cc * kernel_size * 4, Cc * 4, stb};
+    const void *outs[] = {work ? x : nullptr, work ? B : nullptr, work ? C : nullptr, conv_state_out};
+    const int64_t outb[] = {sz.x, sz.bc, sz.bc, stb};
+    for (int o = 0; o < 4; ++o) {
+        for (int i = 0; i < 4; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i]))
+                return SSD_ERR_ALIASING;
+        for (int o2 = o + 1; o2 < 4; ++o2)
+            if (overlaps(outs[o], outb[o], outs[o2], outb[o2]))
+                return SSD_ERR_ALIASING;
+    }
+    NeighborArgs na;
+    na.xbc = xbc;
+    na.w = weight;
+    na.bias = bias;
+    na.state_in = conv_state;
+    na.x = x;
+    na.B = B;
+    na.C = C;
+    na.state_out = conv_state_out;
+    na.kernel_size = kernel_size;
+    na.batch = dims->batch;
+    na.seqlen = dims->seqlen;
+    na.nheads = dims->nheads;
+    na.headdim = dims->headdim;
+    na.dstate = dims->dstate;
+    na.ngroups = dims->ngroups;
+    na.dtype = dims->dtype;
+    if (!conv_supported(na))
+        return SSD_ERR_UNSUPPORTED;
+    if (dims->batch == 0)
+        return SSD_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->seqlen == 0) {   // no steps: the conv state passes through (zero when not given)
+        if (!conv_state_out || stb == 0)
+            return SSD_OK;
+        const cudaError_t e = conv_state ? cudaMemcpyAsync(conv_state_out, conv_state, (size_t)stb,
+                                                           cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(conv_state_out, 0, (size_t)stb, st);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    return conv_launch(na, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
+ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *weight, float eps, void *out,
+                                   const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if (dims->flags != 0 || !(eps >= 0.f))
+        return SSD_ERR_INVALID_DIMS;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!y || !z || !weight || !out))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {y, z, weight, out};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    if (work && (overlaps(out, sz.x, y, sz.x) || overlaps(out, sz.x, z, sz.x) ||
+                 overlaps(out, sz.x, weight, (int64_t)dims->nheads * dims->headdim * 4)))
+        return SSD_ERR_ALIASING;
+    NeighborArgs na;
+    na.y = y;
+    na.z = z;
+    na.w = weight;
+    na.out = out;
+    na.eps = eps;
+    na.batch = dims->batch;
+    na.seqlen = dims->seqlen;
+    na.nheads = dims->nheads;
+    na.headdim = dims->headdim;
+    na.dtype = dims->dtype;
+    if (!gnorm_supported(na))
+        return SSD_ERR_UNSUPPORTED;
+    if (!work)
+        return SSD_OK;
+    return gnorm_launch(na, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 }  // extern "C"

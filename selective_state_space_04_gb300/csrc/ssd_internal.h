@@ -58,6 +58,28 @@ cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream);
 // k_final, v_final (the last step's k and v) after a chunked-path run
 cudaError_t trap_carry_launch(const TrapArgs &a, cudaStream_t stream);
 
+// The steps on either side of the scan (ssd_neighbors.cu), after validation.
+struct NeighborArgs {
+    // causal conv1d + SiLU over the fused x | B | C channels
+    const void *xbc = nullptr;                        // [B,L,H*P + 2*G*N]
+    const float *w = nullptr, *bias = nullptr;        // [C,K] (also the norm weight [H*P]), [C] or null
+    const void *state_in = nullptr;                   // [B,K-1,C] or null
+    void *x = nullptr, *B = nullptr, *C = nullptr;    // [B,L,H,P], [B,L,G,N] x2
+    void *state_out = nullptr;                        // [B,K-1,C] or null
+    int kernel_size = 0;
+    // gated RMSNorm
+    const void *y = nullptr, *z = nullptr;            // [B,L,H,P]
+    void *out = nullptr;                              // [B,L,H,P]
+    float eps = 0.f;
+    int64_t batch = 0, seqlen = 0;
+    int nheads = 0, headdim = 0, dstate = 0, ngroups = 0;
+    int dtype = 0;
+};
+bool conv_supported(const NeighborArgs &a);
+cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t stream);
+bool gnorm_supported(const NeighborArgs &a);
+cudaError_t gnorm_launch(const NeighborArgs &a, cudaStream_t stream);
+
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);

@@ -73,6 +73,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_abi_version.argtypes = []
     lib.ssd_trap_scan_fwd.restype = ctypes.c_int
     lib.ssd_trap_scan_fwd.argtypes = [vp] * 14 + [ctypes.POINTER(SsdDims), vp]
+    lib.ssd_conv1d_silu_fwd.restype = ctypes.c_int
+    lib.ssd_conv1d_silu_fwd.argtypes = [vp] * 8 + [ctypes.c_int32, ctypes.POINTER(SsdDims), vp]
+    lib.ssd_gated_rmsnorm_fwd.restype = ctypes.c_int
+    lib.ssd_gated_rmsnorm_fwd.argtypes = [vp, vp, vp, ctypes.c_float, vp, ctypes.POINTER(SsdDims), vp]
     return lib
 
 
@@ -305,3 +309,49 @@ def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, chu
     _check(_lib.ssd_trap_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
                                   ctypes.c_void_p(st.cuda_stream)), "ssd_trap_scan_fwd")
     return y, h_final, k_final, v_final
+
+
+def _require_cuda(named):
+    for name, t in named:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def conv1d_silu_fwd(xbc, weight, bias=None, conv_state=None, *, nheads, headdim, ngroups, dstate,
+                    x=None, B=None, C=None, conv_state_out=None, return_state=True, stream=None):
+    """Causal depthwise conv1d + SiLU over the fused x | B | C channels of
+    ``xbc [B,L,C]`` (``weight [C,K]``, ``bias [C]``, ``conv_state [B,K-1,C]``).
+    Returns ``(x [B,L,H,P], B [B,L,G,N], C [B,L,G,N], conv_state_out)``."""
+    Bt, L, Cc = xbc.shape
+    K = weight.shape[1]
+    if x is None:
+        x = torch.empty((Bt, L, nheads, headdim), dtype=xbc.dtype, device=xbc.device)
+    if B is None:
+        B = torch.empty((Bt, L, ngroups, dstate), dtype=xbc.dtype, device=xbc.device)
+    if C is None:
+        C = torch.empty((Bt, L, ngroups, dstate), dtype=xbc.dtype, device=xbc.device)
+    if conv_state_out is None and return_state:
+        conv_state_out = torch.empty((Bt, K - 1, Cc), dtype=xbc.dtype, device=xbc.device)
+    named = (("xbc", xbc), ("weight", weight), ("bias", bias), ("conv_state", conv_state), ("x", x),
+             ("B", B), ("C", C), ("conv_state_out", conv_state_out))
+    _require_cuda(named)
+    d = make_dims(Bt, L, nheads, headdim, dstate, ngroups, 1, xbc.dtype)
+    st = torch.cuda.current_stream(xbc.device) if stream is None else stream
+    _check(_lib.ssd_conv1d_silu_fwd(*(_ptr(t) for _, t in named), ctypes.c_int32(K), ctypes.byref(d),
+                                    ctypes.c_void_p(st.cuda_stream)), "ssd_conv1d_silu_fwd")
+    return x, B, C, conv_state_out
+
+
+def gated_rmsnorm_fwd(y, z, weight, eps=1e-6, *, out=None, stream=None):
+    """RMSNorm(y) * weight * SiLU(z) per token over the H*P channels of
+    ``y, z [B,L,H,P]`` (``weight [H*P]`` fp32)."""
+    Bt, L, H, P = y.shape
+    if out is None:
+        out = torch.empty_like(y)
+    named = (("y", y), ("z", z), ("weight", weight), ("out", out))
+    _require_cuda(named)
+    d = make_dims(Bt, L, H, P, 1, 1, 1, y.dtype)
+    st = torch.cuda.current_stream(y.device) if stream is None else stream
+    _check(_lib.ssd_gated_rmsnorm_fwd(_ptr(y), _ptr(z), _ptr(weight), ctypes.c_float(eps), _ptr(out),
+                                      ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)), "ssd_gated_rmsnorm_fwd")
+    return out
