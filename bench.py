@@ -81,6 +81,7 @@ KERNEL_SOURCES = {
     "ssd_decode_kernel": ("ssd_decode.cu",),
     "ssd_seq_kernel": ("ssd_seq.cu",),
     "ssd_trap_seq_kernel": ("ssd_trap.cu",),
+    "ssd_trap_decode_kernel": ("ssd_trap.cu",),
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
 }
@@ -578,7 +579,8 @@ def run_gpu_trap(args, w: Workload):
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
     hbm_peak = float(peaks["hbm_gbs"])
     achieved = alg_bytes / avg_launch_s / 1e9
-    kernel = "ssd_chunk_fused_kernel" if chunked else "ssd_trap_seq_kernel"
+    kernel = ("ssd_chunk_fused_kernel" if chunked
+              else ("ssd_trap_decode_kernel" if w.seqlen == 1 else "ssd_trap_seq_kernel"))
     line = {
         "metric": "trapezoidal (Mamba-3 SISO) scan fwd tokens·heads/s at 1 GB300; % of HBM roofline",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
