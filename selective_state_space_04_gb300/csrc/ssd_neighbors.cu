@@ -157,7 +157,7 @@ struct ConvParams {
 // thread: 4 consecutive channels (vector v) over kConvTile steps of one batch
 // row; the K-1 inputs before the current step stay in registers
 template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads) ssd_conv1d_silu_kernel(ConvParams p)
+__global__ void __launch_bounds__(kConvThreads, 6) ssd_conv1d_silu_kernel(ConvParams p)
 {
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= p.nvec)

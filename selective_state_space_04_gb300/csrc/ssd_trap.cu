@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(128) ssd_trap_carry_kernel(const T *v, const T
 constexpr int kDecWarps = 4, kDecRows = 8;
 
 template <typename T, int NV>
-__global__ void __launch_bounds__(kDecWarps * 32) ssd_trap_decode_kernel(TrapParams p)
+__global__ void __launch_bounds__(kDecWarps * 32, NV == 1 ? 5 : 1) ssd_trap_decode_kernel(TrapParams p)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, P = p.P, N = p.N;
