@@ -84,6 +84,7 @@ KERNEL_SOURCES = {
     "ssd_trap_decode_kernel": ("ssd_trap.cu",),
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
+    "ssd_bwd_kernel": ("ssd_bwd.cu",),
 }
 
 
@@ -675,6 +676,36 @@ def neighbor_setup(w: Workload, dev, seed: int):
                            None if inp["conv_state"] is None else inp["conv_state"][:nb],
                            w.nheads, w.headdim, w.ngroups, w.dstate)
         return inp, d, outs, step, nbytes, "ssd_conv1d_silu_kernel", ref
+    if w.op == "bwd":
+        inp = make_inputs(w, seed=seed)
+        rng = np.random.Generator(np.random.PCG64(seed + 1))
+        inp["dy"] = torch.from_numpy(rng.standard_normal((w.batch, w.seqlen, w.nheads, w.headdim),
+                                                          dtype=np.float32)).to(inp["x"].dtype)
+        inp["d_final"] = torch.from_numpy(0.1 * rng.standard_normal((w.batch, w.nheads, w.headdim, w.dstate),
+                                                                    dtype=np.float32))
+        d = {n: (None if t is None else t.to(dev)) for n, t in inp.items()}
+        outs = {}
+
+        def step(stream):
+            outs.update(ssd.ssd_scan_bwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
+                                         d["init_state"], d["dy"], d["d_final"], stream=stream))
+        f32 = 4
+        BH = w.batch * w.nheads
+        state = BH * w.headdim * w.dstate * f32
+        nbytes = (2 * BL * HP * es + BL * w.nheads * f32 + 2 * BL * GN * es + 3 * w.nheads * f32
+                  + (state if w.init_state else 0) + state                        # inputs, dy, d_final
+                  + BL * HP * f32 + BL * w.nheads * f32 + 2 * BL * GN * f32 + 3 * w.nheads * f32 + state)  # grads
+
+        def ref(nb):   # nb batch rows, the first 4 heads (the oracle keeps every state)
+            import oracle.backward as ob
+            hp = min(4, w.nheads // w.ngroups)
+            sl = inp
+            ob.ssd_bwd(sl["x"][:nb, :, :hp], sl["dt_raw"][:nb, :, :hp], sl["dt_bias"][:hp], sl["A_log"][:hp],
+                       sl["B"][:nb, :, :1], sl["C"][:nb, :, :1], sl["D"][:hp],
+                       None if sl["init_state"] is None else sl["init_state"][:nb, :hp], sl["dy"][:nb, :, :hp],
+                       sl["d_final"][:nb, :hp])
+        ref.heads = min(4, w.nheads // w.ngroups)
+        return inp, d, outs, step, nbytes, "ssd_bwd_kernel", ref
     inp = make_gnorm_inputs(w, seed=seed)
     d = {n: t.to(dev) for n, t in inp.items()}
     outs = {"out": torch.empty_like(d["y"])}
@@ -701,8 +732,9 @@ def neighbor_oracle_rate(w: Workload, ref, target_s: float, min_seconds: float =
         dt = time.perf_counter() - t0
         if dt >= min_seconds:
             break
-    th = nb * w.seqlen * w.nheads
-    return th * reps / dt, (f"{nb} of {w.batch} batch rows x {w.seqlen} steps x {w.nheads} heads "
+    heads = getattr(ref, "heads", w.nheads)
+    th = nb * w.seqlen * heads
+    return th * reps / dt, (f"{nb} of {w.batch} batch rows x {w.seqlen} steps x {heads} of {w.nheads} heads "
                             f"({th} token*heads), {reps} run(s) in {dt:.2f} s")
 
 def run_gpu_neighbor(args, w: Workload):
@@ -766,9 +798,9 @@ def run_gpu_neighbor(args, w: Workload):
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
     hbm_peak = float(peaks["hbm_gbs"])
     achieved = alg_bytes / avg_launch_s / 1e9
-    name = {"conv": "causal conv1d + SiLU", "gnorm": "gated RMSNorm"}[w.op]
+    name = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward"}[w.op]
     line = {
-        "metric": f"{name} fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "metric": f"{name} tokens·heads/s at 1 GB300; % of HBM roofline",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
@@ -808,9 +840,9 @@ def run_reference_neighbor(args, w: Workload):
         secs += th / v
         th_total += th
     value = th_total / secs
-    name = {"conv": "causal conv1d + SiLU", "gnorm": "gated RMSNorm"}[w.op]
+    name = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward"}[w.op]
     line = {
-        "impl": "reference", "metric": f"{name} fwd tokens·heads/s at 1 GB300; % of HBM roofline",
+        "impl": "reference", "metric": f"{name} tokens·heads/s at 1 GB300; % of HBM roofline",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -837,7 +869,7 @@ def main():
     w = WORKLOADS[args.workload]
     if w.op == "trap":
         (run_reference_trap if args.impl == "reference" else run_gpu_trap)(args, w)
-    elif w.op in ("conv", "gnorm"):
+    elif w.op in ("conv", "gnorm", "bwd"):
         (run_reference_neighbor if args.impl == "reference" else run_gpu_neighbor)(args, w)
     elif args.impl == "reference":
         run_reference(args, w)

@@ -293,6 +293,36 @@ ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const flo
 ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *weight, float eps,
                                    void *out, const ssd_dims_t *dims, void *stream);
 
+/*
+ * ssd_scan_bwd -- the backward of ssd_scan_fwd: the gradients of a loss with
+ * respect to every input, given dy = dL/dy and d_final = dL/d final_state.
+ * They are the derivatives of the recurrence ssd_scan_fwd evaluates (the
+ * SSD module's forward, direct form).  The gradient of the state runs in
+ * reverse:
+ *   G_{L-1} = d_final + C_{L-1} dy_{L-1}^T,  G_t = dA_{t+1} G_{t+1} + C_t dy_t^T
+ *   dx_t = D dy_t + dt_t G_t^T B_t,  dB_t = dt_t G_t x_t,  dC_t = h_t dy_t
+ *   ddt_raw_t = sigmoid(dt_raw_t + dt_bias) sum G_t o (a dA_t h_{t-1} + B_t x_t^T)
+ *   dA_log = a sum_t sum G_t o (dt_t dA_t h_{t-1}),  dD = sum_t dy_t . x_t,
+ *   d_init = dA_0 G_0
+ * with dB, dC summed over the heads of each group and the per-head gradients
+ * over batch rows and steps, in a fixed order (deterministic).
+ * Inputs as ssd_scan_fwd, plus dy [B,L,H,P] (dims->dtype) and d_final
+ * [B,H,P,N] fp32 (NULL: zero).  Outputs, all fp32, caller-owned, overlapping
+ * no input and each other: dx [B,L,H,P], ddt_raw [B,L,H], ddt_bias [H],
+ * dA_log [H], dB and dC [B,L,G,N], dD [H], d_init [B,H,P,N] (NULL: not
+ * written).  DEVICE pointers, 16-byte aligned.  flags: SSD_PATH_AUTO or
+ * SSD_PATH_SEQUENTIAL (a sequential kernel that recomputes the forward
+ * states segment by segment).  Supported: N % 4 == 0, N <= 128, P <= 128.
+ * Scratch (checkpoints every 64 steps, one segment of states, per-head
+ * partials) comes stream-ordered from the library pool.  Errors as
+ * ssd_scan_fwd.  Empty work writes nothing.
+ */
+ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bias, const float *A_log,
+                          const void *B, const void *C, const float *D, const float *init_state,
+                          const void *dy, const float *d_final, float *dx, float *ddt_raw,
+                          float *ddt_bias, float *dA_log, float *dB, float *dC, float *dD,
+                          float *d_init, const ssd_dims_t *dims, void *stream);
+
 /* Which path SSD_PATH_AUTO resolves to for these dims on the current device
  * (SSD_PATH_SEQUENTIAL, SSD_PATH_CHUNKED or SSD_PATH_DECODE), or
  * -(ssd_status_t) if the dims are

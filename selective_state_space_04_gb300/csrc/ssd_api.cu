@@ -755,4 +755,89 @@ ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *we
     return gnorm_launch(na, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bias, const float *A_log,
+                          const void *B, const void *C, const float *D, const float *init_state, const void *dy,
+                          const float *d_final, float *dx, float *ddt_raw, float *ddt_bias, float *dA_log,
+                          float *dB, float *dC, float *dD, float *d_init, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if ((dims->flags & ~SSD_PATH_MASK) != 0)
+        return SSD_ERR_INVALID_DIMS;
+    const uint32_t path = dims->flags & SSD_PATH_MASK;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+        return SSD_ERR_UNSUPPORTED;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!x || !dt_raw || !dt_bias || !A_log || !B || !C || !D || !dy || !dx || !ddt_raw || !ddt_bias ||
+                 !dA_log || !dB || !dC || !dD))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final,
+                          dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    // fp32 gradients: dx [B,L,H,P], ddt_raw [B,L,H], dB/dC [B,L,G,N], per-head [H], d_init [B,H,P,N]
+    const int64_t es = dims->dtype == SSD_DTYPE_BF16 ? 2 : 4;
+    const int64_t x32 = sz.x / es * 4, bc32 = sz.bc / es * 4;
+    const void *ins[] = {x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final};
+    const int64_t inb[] = {sz.x, sz.dt, sz.par, sz.par, sz.bc, sz.bc, sz.par, sz.state, sz.x, sz.state};
+    const void *outs[] = {dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init};
+    const int64_t outb[] = {x32, sz.dt, sz.par, sz.par, bc32, bc32, sz.par, sz.state};
+    if (work)
+        for (int o = 0; o < 8; ++o) {
+            for (int i = 0; i < 10; ++i)
+                if (overlaps(outs[o], outb[o], ins[i], inb[i]))
+                    return SSD_ERR_ALIASING;
+            for (int o2 = o + 1; o2 < 8; ++o2)
+                if (overlaps(outs[o], outb[o], outs[o2], outb[o2]))
+                    return SSD_ERR_ALIASING;
+        }
+    BwdArgs ba;
+    ba.x = x;
+    ba.B = B;
+    ba.C = C;
+    ba.dy = dy;
+    ba.dt_raw = dt_raw;
+    ba.dt_bias = dt_bias;
+    ba.A_log = A_log;
+    ba.D = D;
+    ba.init_state = init_state;
+    ba.d_final = d_final;
+    ba.dx = dx;
+    ba.ddt_raw = ddt_raw;
+    ba.ddt_bias = ddt_bias;
+    ba.dA_log = dA_log;
+    ba.dB = dB;
+    ba.dC = dC;
+    ba.dD = dD;
+    ba.d_init = d_init;
+    ba.batch = dims->batch;
+    ba.seqlen = dims->seqlen;
+    ba.nheads = dims->nheads;
+    ba.headdim = dims->headdim;
+    ba.dstate = dims->dstate;
+    ba.ngroups = dims->ngroups;
+    ba.dtype = dims->dtype;
+    if (!bwd_supported(ba))
+        return SSD_ERR_UNSUPPORTED;
+    if (!work)
+        return SSD_OK;   // (empty work: nothing is written)
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool)
+        return SSD_ERR_CUDA;
+    void *ws = nullptr;
+    if (cudaMallocFromPoolAsync(&ws, bwd_workspace_bytes(ba), pool, st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    ssd_status_t rs = bwd_launch(ba, ws, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (cudaFreeAsync(ws, st) != cudaSuccess && rs == SSD_OK)
+        rs = SSD_ERR_CUDA;
+    return rs;
+}
+
 }  // extern "C"

@@ -80,6 +80,22 @@ cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t stream);
 bool gnorm_supported(const NeighborArgs &a);
 cudaError_t gnorm_launch(const NeighborArgs &a, cudaStream_t stream);
 
+// The backward of the SSD scan (ssd_bwd.cu), after validation.
+struct BwdArgs {
+    const void *x, *B, *C, *dy;                 // [B,L,H,P], [B,L,G,N] x2, [B,L,H,P] (dtype)
+    const float *dt_raw, *dt_bias, *A_log, *D;
+    const float *init_state, *d_final;          // [B,H,P,N] or null
+    float *dx, *ddt_raw, *ddt_bias, *dA_log;    // [B,L,H,P], [B,L,H], [H], [H]
+    float *dB, *dC, *dD;                        // [B,L,G,N] x2, [H]
+    float *d_init;                              // [B,H,P,N] or null
+    int64_t batch, seqlen;
+    int nheads, headdim, dstate, ngroups;
+    int dtype;
+};
+bool bwd_supported(const BwdArgs &a);
+size_t bwd_workspace_bytes(const BwdArgs &a);
+cudaError_t bwd_launch(const BwdArgs &a, void *workspace, cudaStream_t stream);
+
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);

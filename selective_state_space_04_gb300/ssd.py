@@ -77,6 +77,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_conv1d_silu_fwd.argtypes = [vp] * 8 + [ctypes.c_int32, ctypes.POINTER(SsdDims), vp]
     lib.ssd_gated_rmsnorm_fwd.restype = ctypes.c_int
     lib.ssd_gated_rmsnorm_fwd.argtypes = [vp, vp, vp, ctypes.c_float, vp, ctypes.POINTER(SsdDims), vp]
+    lib.ssd_scan_bwd.restype = ctypes.c_int
+    lib.ssd_scan_bwd.argtypes = [vp] * 18 + [ctypes.POINTER(SsdDims), vp]
     return lib
 
 
@@ -354,4 +356,25 @@ def gated_rmsnorm_fwd(y, z, weight, eps=1e-6, *, out=None, stream=None):
     st = torch.cuda.current_stream(y.device) if stream is None else stream
     _check(_lib.ssd_gated_rmsnorm_fwd(_ptr(y), _ptr(z), _ptr(weight), ctypes.c_float(eps), _ptr(out),
                                       ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)), "ssd_gated_rmsnorm_fwd")
+    return out
+
+
+def ssd_scan_bwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final=None, *, path="auto",
+                 stream=None):
+    """Gradients of ``ssd_scan_fwd`` given ``dy`` (and ``d_final``).  Returns a
+    dict of fp32 CUDA tensors: dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init."""
+    Bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    f32 = dict(dtype=torch.float32, device=x.device)
+    out = dict(dx=torch.empty((Bt, L, H, P), **f32), ddt_raw=torch.empty((Bt, L, H), **f32),
+               ddt_bias=torch.empty((H,), **f32), dA_log=torch.empty((H,), **f32),
+               dB=torch.empty((Bt, L, G, N), **f32), dC=torch.empty((Bt, L, G, N), **f32),
+               dD=torch.empty((H,), **f32), d_init=torch.empty((Bt, H, P, N), **f32))
+    named = (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log), ("B", B), ("C", C), ("D", D),
+             ("init_state", init_state), ("dy", dy), ("d_final", d_final)) + tuple(out.items())
+    _require_cuda(named)
+    d = make_dims(Bt, L, H, P, N, G, 1, x.dtype, path)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    _check(_lib.ssd_scan_bwd(*(_ptr(t) for _, t in named), ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)),
+           "ssd_scan_bwd")
     return out
