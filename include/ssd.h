@@ -310,12 +310,17 @@ ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *we
  * [B,H,P,N] fp32 (NULL: zero).  Outputs, all fp32, caller-owned, overlapping
  * no input and each other: dx [B,L,H,P], ddt_raw [B,L,H], ddt_bias [H],
  * dA_log [H], dB and dC [B,L,G,N], dD [H], d_init [B,H,P,N] (NULL: not
- * written).  DEVICE pointers, 16-byte aligned.  flags: SSD_PATH_AUTO or
- * SSD_PATH_SEQUENTIAL (a sequential kernel that recomputes the forward
- * states segment by segment).  Supported: N % 4 == 0, N <= 128, P <= 128.
- * Scratch (checkpoints every 64 steps, one segment of states, per-head
- * partials) comes stream-ordered from the library pool.  Errors as
- * ssd_scan_fwd.  Empty work writes nothing.
+ * written).  DEVICE pointers, 16-byte aligned.  flags: a path only.
+ * SSD_PATH_CHUNKED: the chunk form (chunks of 64 steps in parallel: local
+ * chunk states and state gradients, a pass over the chunks that links them,
+ * then every gradient of a chunk as dense fp32 contractions); supported for
+ * P <= 64, N <= 128, B*H <= 65535.  SSD_PATH_SEQUENTIAL: one sequential
+ * kernel per (b, h) that recomputes the forward states segment by segment;
+ * supported for N % 4 == 0, N <= 128, P <= 128.  SSD_PATH_AUTO takes the
+ * chunk form where it applies, else the sequential kernel.  Scratch (chunk
+ * states and gradients, or checkpoints; per-head gradients of B and C; the
+ * per-head partial sums) comes stream-ordered from the library pool.  Errors
+ * as ssd_scan_fwd.  Empty work writes nothing.
  */
 ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bias, const float *A_log,
                           const void *B, const void *C, const float *D, const float *init_state,

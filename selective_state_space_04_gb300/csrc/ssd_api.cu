@@ -767,7 +767,7 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
     if ((dims->flags & ~SSD_PATH_MASK) != 0)
         return SSD_ERR_INVALID_DIMS;
     const uint32_t path = dims->flags & SSD_PATH_MASK;
-    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
         return SSD_ERR_UNSUPPORTED;
     const bool work = dims->batch > 0 && dims->seqlen > 0;
     if (work && (!x || !dt_raw || !dt_bias || !A_log || !B || !C || !D || !dy || !dx || !ddt_raw || !ddt_bias ||
@@ -820,6 +820,9 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
     ba.dstate = dims->dstate;
     ba.ngroups = dims->ngroups;
     ba.dtype = dims->dtype;
+    ba.path = path;
+    if (path == SSD_PATH_AUTO)
+        ba.path = bwd_chunk_supported(ba) ? SSD_PATH_CHUNKED : SSD_PATH_SEQUENTIAL;
     if (!bwd_supported(ba))
         return SSD_ERR_UNSUPPORTED;
     if (!work)

@@ -324,19 +324,23 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce_kernel(const float *dB_hea
     dC[i] = sc;
 }
 
-// dA_log, d dt_bias, dD [H]: the per-(b, h) partials summed over batch rows in order
-__global__ void ssd_bwd_heads_kernel(const float *part, float *dA_log, float *ddt_bias, float *dD, int Bt, int H)
+// dA_log, d dt_bias, dD [H]: the partials of each (b, h) (nper of them, one
+// per chunk or one per sequence) summed over batch rows and partials in order
+__global__ void ssd_bwd_heads_kernel(const float *part, float *dA_log, float *ddt_bias, float *dD, int Bt, int H,
+                                     int nper)
 {
     const int h = blockIdx.x * blockDim.x + threadIdx.x;
     if (h >= H)
         return;
-    const size_t BH = (size_t)Bt * H;
+    const size_t BHC = (size_t)Bt * H * nper;
     float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-    for (int b = 0; b < Bt; ++b) {
-        s0 += part[(size_t)b * H + h];
-        s1 += part[BH + (size_t)b * H + h];
-        s2 += part[2 * BH + (size_t)b * H + h];
-    }
+    for (int b = 0; b < Bt; ++b)
+        for (int c = 0; c < nper; ++c) {
+            const size_t i = ((size_t)b * H + h) * nper + c;
+            s0 += part[i];
+            s1 += part[BHC + i];
+            s2 += part[2 * BHC + i];
+        }
     dA_log[h] = s0;
     ddt_bias[h] = s1;
     dD[h] = s2;
@@ -346,14 +350,21 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 }  // namespace
 
-bool bwd_supported(const BwdArgs &a)
+bool bwd_seq_supported(const BwdArgs &a)
 {
     return a.dstate % 4 == 0 && a.dstate <= 128 && a.headdim >= 1 && a.headdim <= kMaxWarps * kRows &&
            a.batch * (long long)a.nheads <= 0x7FFFFFFFLL && a.seqlen < (1LL << 31);
 }
 
+bool bwd_supported(const BwdArgs &a)
+{
+    return a.path == SSD_PATH_CHUNKED ? bwd_chunk_supported(a) : bwd_seq_supported(a);
+}
+
 size_t bwd_workspace_bytes(const BwdArgs &a)
 {
+    if (a.path == SSD_PATH_CHUNKED)
+        return bwd_chunk_workspace_bytes(a);
     const size_t BH = (size_t)a.batch * a.nheads, PN = (size_t)a.headdim * a.dstate;
     const size_t nseg = (size_t)((a.seqlen + kSeg - 1) / kSeg);
     const size_t BLHN = (size_t)a.batch * a.seqlen * a.nheads * a.dstate;
@@ -361,10 +372,26 @@ size_t bwd_workspace_bytes(const BwdArgs &a)
            align256(3 * BH * 4);
 }
 
+cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const float *dC_head, const float *part,
+                              int nper, cudaStream_t st)
+{
+    const long long total = (long long)a.batch * a.seqlen * a.ngroups * a.dstate;
+    ssd_bwd_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(dB_head, dC_head, a.dB, a.dC, total,
+                                                                          a.nheads, a.ngroups, a.dstate);
+    ssd_bwd_heads_kernel<<<(a.nheads + 127) / 128, 128, 0, st>>>(part, a.dA_log, a.ddt_bias, a.dD, (int)a.batch,
+                                                                 a.nheads, nper);
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess)
+        note_launches(2);
+    return e;
+}
+
 cudaError_t bwd_launch(const BwdArgs &a, void *ws, cudaStream_t st)
 {
     if (!bwd_supported(a))
         return cudaErrorInvalidValue;
+    if (a.path == SSD_PATH_CHUNKED)
+        return bwd_chunk_launch(a, ws, st);
     const size_t BH = (size_t)a.batch * a.nheads, PN = (size_t)a.headdim * a.dstate;
     const int nseg = (int)((a.seqlen + kSeg - 1) / kSeg);
     const size_t BLHN = (size_t)a.batch * a.seqlen * a.nheads * a.dstate;
@@ -403,18 +430,11 @@ cudaError_t bwd_launch(const BwdArgs &a, void *ws, cudaStream_t st)
         ssd_bwd_kernel<__nv_bfloat16><<<(unsigned)BH, threads, 0, st>>>(p);
     else
         ssd_bwd_kernel<float><<<(unsigned)BH, threads, 0, st>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    const long long total = (long long)a.batch * a.seqlen * a.ngroups * a.dstate;
-    ssd_bwd_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(p.dB_head, p.dC_head, a.dB, a.dC, total,
-                                                                          a.nheads, a.ngroups, a.dstate);
-    ssd_bwd_heads_kernel<<<(a.nheads + 127) / 128, 128, 0, st>>>(p.part, a.dA_log, a.ddt_bias, a.dD, (int)a.batch,
-                                                                 a.nheads);
-    e = cudaGetLastError();
-    if (e == cudaSuccess)
-        note_launches(3);
-    return e;
+    note_launches(1);
+    return bwd_finish_launch(a, p.dB_head, p.dC_head, p.part, 1, st);
 }
 
 }  // namespace ssd

@@ -1,0 +1,684 @@
+// ssd_bwd_chunk.cu -- the backward of the SSD scan in chunk form (chunks of
+// kQ = 64 steps processed in parallel), the chunk structure of the Mamba-2 SSD
+// algorithm run in reverse.
+//
+// Per batch row b and head h, within one chunk (local steps i = 0 .. Q-1,
+// cs_i = sum_{k <= i} dt_k a the inclusive cumsum of the log decays, h_in the
+// state entering the chunk, G_out = dL/dh at the chunk's last step through
+// the later steps only):
+//   h_i  = e^{cs_i} h_in + sum_{j <= i} e^{cs_i - cs_j} dt_j B_j x_j^T
+//   G_i  = sum_{s >= i} e^{cs_s - cs_i} C_s dy_s^T + e^{cs_last - cs_i} G_out
+// and the chunks are linked by
+//   h_in(c+1)  = e^{cs_last(c)} h_in(c) + S(c),   S(c) = sum_j e^{cs_last - cs_j} dt_j B_j x_j^T
+//   G_out(c-1) = e^{cs_last(c)} G_out(c) + R(c),  R(c) = sum_s e^{cs_s} C_s dy_s^T
+// (G_out(-1) = dA_0 G_0 is d init).  Three launches:
+//   1. ssd_bwd_local_kernel: S(c), R(c) and e^{cs_last(c)} for every chunk;
+//   2. ssd_bwd_pass_kernel: the two chains above, element-wise over the state,
+//      overwriting S(c) by h_in(c) (and the slot past the last by the final
+//      state) and R(c) by G_out(c);
+//   3. ssd_bwd_grad_kernel: every gradient of one chunk from h_in, G_out and
+//      the chunk's inputs, as dense contractions (CB = C B^T, DX = dy x^T,
+//      E = causal e^{cs_s - cs_j}):
+//        dx_j = D dy_j + dt_j (sum_s E CB [s,j] dy_s + e^{cs_last-cs_j} G_out^T B_j)
+//        dB_j = dt_j (sum_s E DX [s,j] C_s + e^{cs_last-cs_j} G_out x_j)
+//        dC_s = sum_j E DX [s,j] dt_j B_j + e^{cs_s} h_in dy_s
+//      and d log dA_j = sum_{k >= j} dL/dcs_k, with dL/dcs_k the row-minus-
+//      column sum of W = E CB DX dt_j, plus e^{cs_k} dy_k . (h_in^T C_k), minus
+//      e^{cs_last-cs_k} dt_k x_k . (G_out^T B_k), plus <G_out, h_last> at the
+//      chunk's last step; ddt = x . (G^T B) + a d log dA, dA_log = a sum dt d log dA.
+// The contractions are shared-memory tiled fp32 FFMA: every operand sits in
+// shared memory with an odd row stride, each thread owns a 4 x 4 or 4 x 8
+// output tile strided by 16, so both orientations of every operand read
+// without bank conflicts.  Sums over chunks, batch rows and a group's heads
+// are left to the fixed-order reduction kernels (deterministic gradients).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ssd_internal.h"
+
+namespace ssd {
+namespace {
+
+constexpr int kQ = 64;        // steps per chunk
+constexpr int kPM = 64;       // largest headdim of this path
+constexpr int kNM = 128;      // largest dstate of this path
+constexpr int kLP = kPM + 1;  // shared-memory row strides (odd: conflict-free columns)
+constexpr int kLN = kNM + 1;
+constexpr int kLQ = kQ + 1;
+constexpr int kThreads = 256; // 16 x 16 threads, output tiles strided by 16
+
+struct ChunkBwdParams {
+    const void *x, *B, *C, *dy;          // x, dy [B,L,H,P]; B, C [B,L,G,N]
+    const float *dt_raw, *dt_bias, *A_log, *D;
+    const float *init_state, *d_final;   // [B,H,P,N] or null
+    float *dx, *ddt_raw, *d_init;        // [B,L,H,P], [B,L,H], [B,H,P,N] or null
+    float *S;                            // [B*H][nc+1][N][P]: S(c), then h_in(c); slot nc the final state
+    float *R;                            // [B*H][nc][N][P]: R(c), then G_out(c)
+    float *dec;                          // [B*H][nc]: e^{cs_last(c)}
+    float *dB_head, *dC_head;            // [B,L,H,N]
+    float *part;                         // [3][B*H*nc]: a * sum dt dlogdA, sum ddt_raw, sum dy.x per chunk
+    long long L;
+    int H, P, N, G, nc;
+};
+
+template <typename T> __device__ __forceinline__ float to_f32(T v);
+template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+__device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
+
+// acc[i][j] += sum_k fa(i, k) fb(k, j) for k < K; fa / fb read shared memory
+template <int TM, int TN, int K, typename FA, typename FB>
+__device__ __forceinline__ void contract(float (&acc)[TM][TN], FA fa, FB fb)
+{
+#pragma unroll 4
+    for (int k = 0; k < K; ++k) {
+        float av[TM], bv[TN];
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+            av[i] = fa(i, k);
+#pragma unroll
+        for (int j = 0; j < TN; ++j)
+            bv[j] = fb(k, j);
+#pragma unroll
+        for (int i = 0; i < TM; ++i)
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+}
+
+template <int TM, int TN>
+__device__ __forceinline__ void zero(float (&acc)[TM][TN])
+{
+#pragma unroll
+    for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int j = 0; j < TN; ++j)
+            acc[i][j] = 0.f;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// sum over the 16 threads of a half warp (the threads sharing a tile row)
+__device__ __forceinline__ float half_warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// the chunk's dt, z = dt_raw + bias and inclusive cumsum of dt a, in shared
+// memory (zero dt past the sequence's end, so cs stays flat there)
+__device__ __forceinline__ void chunk_decays(const ChunkBwdParams &p, long long b, int h, long long t0, int nq,
+                                             float a, float *dt_s, float *z_s, float *cs_s)
+{
+    const int tid = threadIdx.x;
+    if (tid < kQ) {
+        float dt = 0.f, z = 0.f;
+        if (tid < nq) {
+            z = p.dt_raw[(size_t)(b * p.L + t0 + tid) * p.H + h] + p.dt_bias[h];
+            dt = softplus_f32(z);
+        }
+        dt_s[tid] = dt;
+        z_s[tid] = z;
+        float v = dt * a;   // inclusive scan within each of the two warps
+        const int lane = tid & 31;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o)
+                v += u;
+        }
+        cs_s[tid] = v;
+    }
+    __syncthreads();
+    if (tid >= 32 && tid < kQ)
+        cs_s[tid] += cs_s[31];
+    __syncthreads();
+}
+
+// the V = 16 / sizeof(T) values of a 16-byte vector as fp32
+__device__ __forceinline__ void unpack(const uint4 &u, float (&v)[4]) {
+    v[0] = __uint_as_float(u.x);
+    v[1] = __uint_as_float(u.y);
+    v[2] = __uint_as_float(u.z);
+    v[3] = __uint_as_float(u.w);
+}
+__device__ __forceinline__ void unpack(const uint4 &u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // little-endian: the lower half is the earlier element
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+// rows r < nrows (of ROWS) and columns c < cols (of CMAX) of a row-major
+// tensor (row stride row_stride elements) into shared memory as fp32, row
+// stride ld, each row times scale[r] when scale is given; zero elsewhere.
+// Where rows are 16-byte aligned every thread issues all of its 16-byte
+// loads before the first shared-memory store (one round trip of latency).
+template <typename T, int ROWS, int CMAX>
+__device__ __forceinline__ void stage(float *dst, int ld, const T *src, size_t row_stride, int nrows, int cols,
+                                      const float *scale = nullptr)
+{
+    constexpr int V = 16 / sizeof(T), VPR = CMAX / V, IT = ROWS * VPR / kThreads;
+    static_assert(ROWS * VPR % kThreads == 0, "whole vectors per thread");
+    const bool vec = cols % V == 0 && row_stride % V == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+    if (vec) {
+        uint4 buf[IT];
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int idx = it * kThreads + threadIdx.x, r = idx / VPR, cv = idx % VPR;
+            buf[it] = (r < nrows && cv * V < cols)
+                          ? *reinterpret_cast<const uint4 *>(src + (size_t)r * row_stride + cv * V)
+                          : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            const int idx = it * kThreads + threadIdx.x, r = idx / VPR, cv = idx % VPR;
+            float v[V];
+            unpack(buf[it], v);
+            const float s = scale ? scale[r] : 1.f;
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                dst[r * ld + cv * V + e] = s * v[e];
+        }
+    } else {
+        for (int i = threadIdx.x; i < ROWS * CMAX; i += kThreads) {
+            const int r = i / CMAX, c = i % CMAX;
+            dst[r * ld + c] =
+                (r < nrows && c < cols) ? (scale ? scale[r] : 1.f) * to_f32<T>(src[(size_t)r * row_stride + c]) : 0.f;
+        }
+    }
+}
+
+// 1. S(c) = sum_j e^{cs_last - cs_j} dt_j B_j x_j^T and R(c) = sum_s e^{cs_s} C_s dy_s^T
+//    ([N,P] each) and e^{cs_last(c)}.  Grid (nc, B*H).  Thread tile: 8 rows n
+//    (ty + 16 i) x 4 columns p (tx + 16 j).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams p)
+{
+    extern __shared__ float smem[];
+    float *Bs = smem, *Cs = Bs + kQ * kLN, *xw = Cs + kQ * kLN, *dyw = xw + kQ * kLP;
+    float *dt_s = dyw + kQ * kLP, *z_s = dt_s + kQ, *cs_s = z_s + kQ, *w_s = cs_s + kQ, *e_s = w_s + kQ;
+    const int H = p.H, P = p.P, N = p.N, Gg = p.G, nc = p.nc;
+    const long long bh = blockIdx.y, b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / Gg), c = blockIdx.x;
+    const long long t0 = (long long)c * kQ;
+    const int nq = (int)min((long long)kQ, p.L - t0);
+    const float a = -expf(p.A_log[h]);
+    chunk_decays(p, b, h, t0, nq, a, dt_s, z_s, cs_s);
+    if (threadIdx.x < kQ) {
+        const int j = threadIdx.x;
+        w_s[j] = expf(cs_s[kQ - 1] - cs_s[j]) * dt_s[j];
+        e_s[j] = expf(cs_s[j]);
+    }
+    __syncthreads();
+    const T *xg = static_cast<const T *>(p.x) + ((size_t)(b * p.L + t0) * H + h) * P;
+    const T *dyg = static_cast<const T *>(p.dy) + ((size_t)(b * p.L + t0) * H + h) * P;
+    const T *Bg = static_cast<const T *>(p.B) + ((size_t)(b * p.L + t0) * Gg + g) * N;
+    const T *Cg = static_cast<const T *>(p.C) + ((size_t)(b * p.L + t0) * Gg + g) * N;
+    stage<T, kQ, kNM>(Bs, kLN, Bg, (size_t)Gg * N, nq, N);
+    stage<T, kQ, kNM>(Cs, kLN, Cg, (size_t)Gg * N, nq, N);
+    stage<T, kQ, kPM>(xw, kLP, xg, (size_t)H * P, nq, P, w_s);
+    stage<T, kQ, kPM>(dyw, kLP, dyg, (size_t)H * P, nq, P, e_s);
+    __syncthreads();
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const size_t NP = (size_t)N * P;
+    float acc[8][4];
+    zero(acc);
+    contract<8, 4, kQ>(acc, [&](int i, int k) { return Bs[k * kLN + ty + 16 * i]; },
+                       [&](int k, int j) { return xw[k * kLP + tx + 16 * j]; });
+    float *Sd = p.S + ((size_t)bh * (nc + 1) + c) * NP;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = ty + 16 * i, col = tx + 16 * j;
+            if (n < N && col < P)
+                Sd[(size_t)n * P + col] = acc[i][j];
+        }
+    zero(acc);
+    contract<8, 4, kQ>(acc, [&](int i, int k) { return Cs[k * kLN + ty + 16 * i]; },
+                       [&](int k, int j) { return dyw[k * kLP + tx + 16 * j]; });
+    float *Rd = p.R + ((size_t)bh * nc + c) * NP;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int n = ty + 16 * i, col = tx + 16 * j;
+            if (n < N && col < P)
+                Rd[(size_t)n * P + col] = acc[i][j];
+        }
+    if (threadIdx.x == 0)
+        p.dec[bh * nc + c] = expf(cs_s[kQ - 1]);
+}
+
+// 2. The chains over chunks.  blockIdx.z = 0: S(c) <- h_in(c) (slot nc <- the
+//    final state); blockIdx.z = 1: R(c) <- G_out(c), d init <- G_out(-1).  Each
+//    thread runs one chain over kVec consecutive state elements (n, p) of one
+//    (b, h), loading kBatch chunks ahead so that the loads of a batch are all
+//    in flight together (the stores of a batch go to other addresses).
+constexpr int kVec = 4, kBatch = 8;
+template <int V>
+__device__ __forceinline__ void chain(float *buf, size_t stride, const float *dec, int nc, bool reverse,
+                                      float (&v)[V])
+{
+    for (int c0 = 0; c0 < nc; c0 += kBatch) {
+        float x[kBatch][V], d[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int c = reverse ? nc - 1 - (c0 + k) : c0 + k;
+            if (c0 + k < nc) {
+                d[k] = dec[c];
+                if constexpr (V == 4) {
+                    const float4 t = *reinterpret_cast<const float4 *>(buf + c * stride);
+                    x[k][0] = t.x; x[k][1] = t.y; x[k][2] = t.z; x[k][3] = t.w;
+                } else {
+                    x[k][0] = buf[c * stride];
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const int c = reverse ? nc - 1 - (c0 + k) : c0 + k;
+            if (c0 + k < nc) {
+                if constexpr (V == 4)
+                    *reinterpret_cast<float4 *>(buf + c * stride) = make_float4(v[0], v[1], v[2], v[3]);
+                else
+                    buf[c * stride] = v[0];
+#pragma unroll
+                for (int e = 0; e < V; ++e)
+                    v[e] = fmaf(d[k], v[e], x[k][e]);
+            }
+        }
+    }
+}
+
+template <int V>
+__global__ void __launch_bounds__(kThreads) ssd_bwd_pass_kernel(ChunkBwdParams p)
+{
+    const int P = p.P, N = p.N, nc = p.nc;
+    const long long bh = blockIdx.y;
+    const int NP = N * P, e0 = (blockIdx.x * kThreads + threadIdx.x) * V;
+    if (e0 >= NP)
+        return;
+    const float *dec = p.dec + bh * nc;
+    const bool fwd = blockIdx.z == 0;
+    const float *in = fwd ? p.init_state : p.d_final;   // [B,H,P,N] or null
+    float v[V];
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const int n = (e0 + e) / P, col = (e0 + e) - n * P;
+        v[e] = in ? in[(size_t)bh * NP + (size_t)col * N + n] : 0.f;
+    }
+    if (fwd) {
+        float *S = p.S + (size_t)bh * (nc + 1) * NP + e0;
+        chain<V>(S, (size_t)NP, dec, nc, false, v);
+        if constexpr (V == 4)
+            *reinterpret_cast<float4 *>(S + (size_t)nc * NP) = make_float4(v[0], v[1], v[2], v[3]);
+        else
+            S[(size_t)nc * NP] = v[0];
+    } else {
+        chain<V>(p.R + (size_t)bh * nc * NP + e0, (size_t)NP, dec, nc, true, v);
+        if (p.d_init) {
+#pragma unroll
+            for (int e = 0; e < V; ++e) {
+                const int n = (e0 + e) / P, col = (e0 + e) - n * P;
+                p.d_init[(size_t)bh * NP + (size_t)col * N + n] = v[e];
+            }
+        }
+    }
+}
+
+// a [N,P] fp32 state into shared memory, row stride kLP, zero past N, P
+__device__ __forceinline__ void stage_state(float *dst, const float *src, int N, int P)
+{
+    stage<float, kNM, kPM>(dst, kLP, src, (size_t)P, N, P);
+}
+
+// 3. Every gradient of one chunk.  Grid (nc, B*H).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p)
+{
+    extern __shared__ float smem[];
+    float *xs = smem, *dys = xs + kQ * kLP, *Bs = dys + kQ * kLP, *Cs = Bs + kQ * kLN;
+    float *Mt = Cs + kQ * kLN, *A2 = Mt + kQ * kLQ, *St = A2 + kQ * kLQ;
+    float *rowp = St + kNM * kLP, *colp = rowp + 16 * kQ;
+    float *dt_s = colp + 16 * kQ, *z_s = dt_s + kQ, *cs_s = z_s + kQ;
+    float *ddir = cs_s + kQ, *vv = ddir + kQ, *uu = vv + kQ, *dcs = uu + kQ;
+    float *red = dcs + kQ;   // [32]: per-warp sums (fixed order: deterministic)
+    const int H = p.H, P = p.P, N = p.N, Gg = p.G, nc = p.nc;
+    const long long bh = blockIdx.y, b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / Gg), c = blockIdx.x;
+    const long long t0 = (long long)c * kQ;
+    const int nq = (int)min((long long)kQ, p.L - t0);
+    const float a = -expf(p.A_log[h]), Dh = p.D[h];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4, lane = tid & 31, warp = tid >> 5;
+    const size_t NP = (size_t)N * P;
+    const float *Gout = p.R + ((size_t)bh * nc + c) * NP;
+    const float *hin = p.S + ((size_t)bh * (nc + 1) + c) * NP, *hlast = hin + NP;
+
+    chunk_decays(p, b, h, t0, nq, a, dt_s, z_s, cs_s);
+    const size_t rowx = (size_t)(b * p.L + t0) * H + h, rowb = (size_t)(b * p.L + t0) * Gg + g;
+    stage<T, kQ, kPM>(xs, kLP, static_cast<const T *>(p.x) + rowx * P, (size_t)H * P, nq, P);
+    stage<T, kQ, kPM>(dys, kLP, static_cast<const T *>(p.dy) + rowx * P, (size_t)H * P, nq, P);
+    stage<T, kQ, kNM>(Bs, kLN, static_cast<const T *>(p.B) + rowb * N, (size_t)Gg * N, nq, N);
+    stage<T, kQ, kNM>(Cs, kLN, static_cast<const T *>(p.C) + rowb * N, (size_t)Gg * N, nq, N);
+    stage_state(St, Gout, N, P);
+    float gh = 0.f;   // <G_out, h_last>, this thread's share
+    if ((NP & 3) == 0) {
+        const float4 *g4 = reinterpret_cast<const float4 *>(Gout), *h4 = reinterpret_cast<const float4 *>(hlast);
+#pragma unroll 4
+        for (size_t e = tid; e < NP / 4; e += kThreads) {
+            const float4 gv = g4[e], hv = h4[e];
+            gh = fmaf(gv.x, hv.x, fmaf(gv.y, hv.y, fmaf(gv.z, hv.z, fmaf(gv.w, hv.w, gh))));
+        }
+    } else {
+        for (size_t e = tid; e < NP; e += kThreads)
+            gh = fmaf(Gout[e], hlast[e], gh);
+    }
+    gh = warp_sum(gh);
+    if (lane == 0)
+        red[warp] = gh;
+    __syncthreads();
+    const float cs_last = cs_s[kQ - 1];
+    float dd = 0.f;   // sum dy . x, this thread's share
+    for (int i = tid; i < kQ * kPM; i += kThreads)
+        dd = fmaf(dys[(i / kPM) * kLP + i % kPM], xs[(i / kPM) * kLP + i % kPM], dd);
+    dd = warp_sum(dd);
+    if (lane == 0)
+        red[8 + warp] = dd;
+
+    // CB = C B^T, DX = dy x^T; Mt = E CB, A2 = E DX; row / column sums of W = Mt DX dt_j
+    {
+        float cb[4][4], dx[4][4];
+        zero(cb);
+        zero(dx);
+        contract<4, 4, kNM>(cb, [&](int i, int k) { return Cs[(ty + 16 * i) * kLN + k]; },
+                            [&](int k, int j) { return Bs[(tx + 16 * j) * kLN + k]; });
+        contract<4, 4, kPM>(dx, [&](int i, int k) { return dys[(ty + 16 * i) * kLP + k]; },
+                            [&](int k, int j) { return xs[(tx + 16 * j) * kLP + k]; });
+        float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int s = ty + 16 * i, jj = tx + 16 * j;
+                const float E = (jj <= s && s < nq) ? expf(cs_s[s] - cs_s[jj]) : 0.f;
+                const float mt = E * cb[i][j], a2 = E * dx[i][j];
+                Mt[s * kLQ + jj] = mt;
+                A2[s * kLQ + jj] = a2;
+                const float w = mt * dt_s[jj] * dx[i][j];
+                rp[i] += w;
+                cp[j] += w;
+            }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            rowp[tx * kQ + ty + 16 * i] = rp[i];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            colp[ty * kQ + tx + 16 * j] = cp[j];
+    }
+    __syncthreads();
+
+    // dx_j = D dy_j + dt_j (Mt^T dy + e^{cs_last - cs_j} B G_out)_j; x . (G^T B) and v
+    {
+        float in[4][4], out[4][4];
+        zero(in);
+        zero(out);
+        contract<4, 4, kQ>(in, [&](int i, int k) { return Mt[k * kLQ + ty + 16 * i]; },
+                           [&](int k, int j) { return dys[k * kLP + tx + 16 * j]; });
+        contract<4, 4, kNM>(out, [&](int i, int k) { return Bs[(ty + 16 * i) * kLN + k]; },
+                            [&](int k, int j) { return St[k * kLP + tx + 16 * j]; });
+        float *dxg = p.dx + rowx * P;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = ty + 16 * i;
+            const float eo = expf(cs_last - cs_s[j]), dtj = dt_s[j];
+            float dsum = 0.f, vsum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int col = tx + 16 * q;
+                const float gx = fmaf(eo, out[i][q], in[i][q]);
+                const float xv = xs[j * kLP + col];
+                dsum = fmaf(xv, gx, dsum);
+                vsum = fmaf(xv, out[i][q], vsum);
+                if (j < nq && col < P)
+                    dxg[(size_t)j * H * P + col] = fmaf(Dh, dys[j * kLP + col], dtj * gx);
+            }
+            dsum = half_warp_sum(dsum);
+            vsum = half_warp_sum(vsum);
+            if (tx == 0) {
+                ddir[j] = dsum;
+                vv[j] = dtj * eo * vsum;
+            }
+        }
+    }
+
+    // dB_j = dt_j (A2^T C + e^{cs_last - cs_j} x G_out^T)_j
+    {
+        float in[4][8], out[4][8];
+        zero(in);
+        zero(out);
+        contract<4, 8, kQ>(in, [&](int i, int k) { return A2[k * kLQ + ty + 16 * i]; },
+                           [&](int k, int j) { return Cs[k * kLN + tx + 16 * j]; });
+        contract<4, 8, kPM>(out, [&](int i, int k) { return xs[(ty + 16 * i) * kLP + k]; },
+                            [&](int k, int j) { return St[(tx + 16 * j) * kLP + k]; });
+        float *dbg = p.dB_head + rowx * N;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = ty + 16 * i;
+            const float eo = expf(cs_last - cs_s[j]), dtj = dt_s[j];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int n = tx + 16 * q;
+                if (j < nq && n < N)
+                    dbg[(size_t)j * H * N + n] = dtj * fmaf(eo, out[i][q], in[i][q]);
+            }
+        }
+    }
+    __syncthreads();
+    stage_state(St, hin, N, P);
+    __syncthreads();
+
+    // dC_s = (A2 dt) B + e^{cs_s} dy h_in^T; u_s = C_s . (e^{cs_s} h_in dy_s)
+    {
+        float in[4][8], out[4][8];
+        zero(in);
+        zero(out);
+        contract<4, 8, kQ>(in, [&](int i, int k) { return A2[(ty + 16 * i) * kLQ + k] * dt_s[k]; },
+                           [&](int k, int j) { return Bs[k * kLN + tx + 16 * j]; });
+        contract<4, 8, kPM>(out, [&](int i, int k) { return dys[(ty + 16 * i) * kLP + k]; },
+                            [&](int k, int j) { return St[(tx + 16 * j) * kLP + k]; });
+        float *dcg = p.dC_head + rowx * N;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int s = ty + 16 * i;
+            const float es = expf(cs_s[s]);
+            float usum = 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int n = tx + 16 * q;
+                const float inter = es * out[i][q];
+                usum = fmaf(Cs[s * kLN + n], inter, usum);
+                if (s < nq && n < N)
+                    dcg[(size_t)s * H * N + n] = in[i][q] + inter;
+            }
+            usum = half_warp_sum(usum);
+            if (tx == 0)
+                uu[s] = usum;
+        }
+    }
+    __syncthreads();
+
+    // dL/dcs_k, its suffix sums d log dA_j, ddt_raw and the chunk's per-head partials
+    if (tid < kQ) {
+        float r = 0.f, cl = 0.f;
+        for (int q = 0; q < 16; ++q) {
+            r += rowp[q * kQ + tid];
+            cl += colp[q * kQ + tid];
+        }
+        dcs[tid] = r - cl + uu[tid] - vv[tid];
+    }
+    __syncthreads();
+    if (warp == 0) {   // suffix sums over the 64 steps, two per lane; <G_out, h_last> enters at the last
+        float ghs = 0.f;
+        for (int q = 0; q < 8; ++q)
+            ghs += red[q];
+        const float v0 = dcs[2 * lane], v1 = dcs[2 * lane + 1];
+        float s = v0 + v1;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_down_sync(0xffffffffu, s, o);
+            if (lane + o < 32)
+                s += t;
+        }
+        float after = __shfl_down_sync(0xffffffffu, s, 1);   // sum over the lanes past this one
+        if (lane == 31)
+            after = 0.f;
+        const float s1 = ghs + after + v1;
+        dcs[2 * lane + 1] = s1;
+        dcs[2 * lane] = s1 + v0;
+    }
+    __syncthreads();
+    if (warp < 2) {
+        float cda = 0.f, cdb = 0.f;
+        if (tid < nq) {
+            const float ddt = fmaf(a, dcs[tid], ddir[tid]);
+            cdb = ddt / (1.f + expf(-z_s[tid]));
+            p.ddt_raw[(size_t)(b * p.L + t0 + tid) * H + h] = cdb;
+            cda = dt_s[tid] * dcs[tid];
+        }
+        cda = warp_sum(cda);
+        cdb = warp_sum(cdb);
+        if (lane == 0) {
+            red[16 + warp] = cda;
+            red[18 + warp] = cdb;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const float sa = red[16] + red[17], sb = red[18] + red[19];
+        float sd = 0.f;
+        for (int q = 0; q < 8; ++q)
+            sd += red[8 + q];
+        const size_t BHC = (size_t)gridDim.y * nc, i = (size_t)bh * nc + c;
+        p.part[i] = a * sa;
+        p.part[BHC + i] = sb;
+        p.part[2 * BHC + i] = sd;
+    }
+}
+
+constexpr size_t kLocalSmem = (size_t)(2 * kQ * kLN + 2 * kQ * kLP + 5 * kQ) * sizeof(float);
+constexpr size_t kGradSmem =
+    (size_t)(2 * kQ * kLP + 2 * kQ * kLN + 2 * kQ * kLQ + kNM * kLP + 32 * kQ + 7 * kQ + 32) * sizeof(float);
+static_assert(kGradSmem <= 227 * 1024, "grad kernel shared memory");
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+}  // namespace
+
+bool bwd_chunk_supported(const BwdArgs &a)
+{
+    return a.headdim >= 1 && a.headdim <= kPM && a.dstate >= 1 && a.dstate <= kNM &&
+           a.batch * (long long)a.nheads <= 65535 && a.seqlen < (1LL << 31) &&
+           (a.seqlen + kQ - 1) / kQ <= 0x7FFFFFFFLL;
+}
+
+size_t bwd_chunk_workspace_bytes(const BwdArgs &a)
+{
+    const size_t BH = (size_t)a.batch * a.nheads, NP = (size_t)a.headdim * a.dstate;
+    const size_t nc = (size_t)((a.seqlen + kQ - 1) / kQ);
+    const size_t BLHN = (size_t)a.batch * a.seqlen * a.nheads * a.dstate;
+    return align256(BH * (nc + 1) * NP * 4) + align256(BH * nc * NP * 4) + align256(BH * nc * 4) +
+           2 * align256(BLHN * 4) + align256(3 * BH * nc * 4);
+}
+
+cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
+{
+    if (!bwd_chunk_supported(a))
+        return cudaErrorInvalidValue;
+    const size_t BH = (size_t)a.batch * a.nheads, NP = (size_t)a.headdim * a.dstate;
+    const int nc = (int)((a.seqlen + kQ - 1) / kQ);
+    const size_t BLHN = (size_t)a.batch * a.seqlen * a.nheads * a.dstate;
+    char *w = static_cast<char *>(ws);
+    ChunkBwdParams p;
+    p.x = a.x;
+    p.B = a.B;
+    p.C = a.C;
+    p.dy = a.dy;
+    p.dt_raw = a.dt_raw;
+    p.dt_bias = a.dt_bias;
+    p.A_log = a.A_log;
+    p.D = a.D;
+    p.init_state = a.init_state;
+    p.d_final = a.d_final;
+    p.dx = a.dx;
+    p.ddt_raw = a.ddt_raw;
+    p.d_init = a.d_init;
+    p.S = reinterpret_cast<float *>(w);
+    w += align256(BH * (nc + 1) * NP * 4);
+    p.R = reinterpret_cast<float *>(w);
+    w += align256(BH * nc * NP * 4);
+    p.dec = reinterpret_cast<float *>(w);
+    w += align256(BH * nc * 4);
+    p.dB_head = reinterpret_cast<float *>(w);
+    w += align256(BLHN * 4);
+    p.dC_head = reinterpret_cast<float *>(w);
+    w += align256(BLHN * 4);
+    p.part = reinterpret_cast<float *>(w);
+    p.L = a.seqlen;
+    p.H = a.nheads;
+    p.P = a.headdim;
+    p.N = a.dstate;
+    p.G = a.ngroups;
+    p.nc = nc;
+    const dim3 grid((unsigned)nc, (unsigned)BH);
+    const bool bf = a.dtype == SSD_DTYPE_BF16;
+    cudaError_t e;
+    if (bf) {
+        e = cudaFuncSetAttribute(ssd_bwd_local_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kLocalSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ssd_bwd_grad_kernel<__nv_bfloat16>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGradSmem);
+    } else {
+        e = cudaFuncSetAttribute(ssd_bwd_local_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kLocalSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(ssd_bwd_grad_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGradSmem);
+    }
+    if (e != cudaSuccess)
+        return e;
+    if (bf)
+        ssd_bwd_local_kernel<__nv_bfloat16><<<grid, kThreads, kLocalSmem, st>>>(p);
+    else
+        ssd_bwd_local_kernel<float><<<grid, kThreads, kLocalSmem, st>>>(p);
+    if (NP % kVec == 0)
+        ssd_bwd_pass_kernel<kVec><<<dim3((unsigned)((NP / kVec + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads,
+                                    0, st>>>(p);
+    else
+        ssd_bwd_pass_kernel<1><<<dim3((unsigned)((NP + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
+    if (bf)
+        ssd_bwd_grad_kernel<__nv_bfloat16><<<grid, kThreads, kGradSmem, st>>>(p);
+    else
+        ssd_bwd_grad_kernel<float><<<grid, kThreads, kGradSmem, st>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    note_launches(3);
+    return bwd_finish_launch(a, p.dB_head, p.dC_head, p.part, nc, st);
+}
+
+}  // namespace ssd

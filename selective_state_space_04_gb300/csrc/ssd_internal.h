@@ -91,10 +91,20 @@ struct BwdArgs {
     int64_t batch, seqlen;
     int nheads, headdim, dstate, ngroups;
     int dtype;
+    uint32_t path;                              // SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED (resolved)
 };
+// ssd_bwd.cu: dispatch, the sequential kernel and the fixed-order reductions
+bool bwd_seq_supported(const BwdArgs &a);
 bool bwd_supported(const BwdArgs &a);
 size_t bwd_workspace_bytes(const BwdArgs &a);
 cudaError_t bwd_launch(const BwdArgs &a, void *workspace, cudaStream_t stream);
+// dB, dC from the per-head buffers; dA_log, ddt_bias, dD from nper partials per (b, h)
+cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const float *dC_head, const float *part,
+                              int nper, cudaStream_t stream);
+// ssd_bwd_chunk.cu: the chunk-parallel backward (P <= 64, N <= 128)
+bool bwd_chunk_supported(const BwdArgs &a);
+size_t bwd_chunk_workspace_bytes(const BwdArgs &a);
+cudaError_t bwd_chunk_launch(const BwdArgs &a, void *workspace, cudaStream_t stream);
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);

@@ -225,3 +225,28 @@ def test_trap_entry_validation_before_cuda(libssd):
     assert _trap_call(libssd, d4) == 4
     # empty batch: nothing to do, no device access
     assert _trap_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0
+
+
+def _bwd_call(libssd, dims_, **override):
+    lib = libssd.lib()
+    base = 0x10000000
+    # 18 distinct, 16-byte aligned, widely spaced fake addresses (validation only)
+    names = ["x", "dt_raw", "dt_bias", "A_log", "B", "C", "D", "init_state", "dy", "d_final",
+             "dx", "ddt_raw", "ddt_bias", "dA_log", "dB", "dC", "dD", "d_init"]
+    ptrs = {n: ctypes.c_void_p(base + i * 0x1000000) for i, n in enumerate(names)}
+    ptrs.update(override)
+    return lib.ssd_scan_bwd(*(ptrs[n] for n in names), ctypes.byref(dims_), None)
+
+
+def test_bwd_entry_validation_before_cuda(libssd):
+    d = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32")
+    assert _bwd_call(libssd, d, dy=None) == 2                                   # SSD_ERR_NULL_PTR
+    assert _bwd_call(libssd, d, dB=ctypes.c_void_p(0x30000008)) == 3            # SSD_ERR_MISALIGNED
+    assert _bwd_call(libssd, d, dx=ctypes.c_void_p(0x10000000 + 0x100)) == 7    # dx inside x: SSD_ERR_ALIASING
+    assert _bwd_call(libssd, libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="decode")) == 4
+    assert _bwd_call(libssd, libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", schedule="pieces")) == 1
+    # the chunk-parallel kernels take P <= 64, N <= 128; the sequential kernel P <= 128, N % 4 == 0
+    assert _bwd_call(libssd, libssd.make_dims(1, 8, 2, 96, 32, 1, 1, "f32", path="chunked")) == 4
+    assert _bwd_call(libssd, libssd.make_dims(1, 8, 2, 16, 30, 1, 1, "f32", path="sequential")) == 4
+    assert _bwd_call(libssd, libssd.make_dims(1, 8, 2, 16, 160, 1, 1, "f32")) == 4
+    assert _bwd_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0   # empty: no device access

@@ -1,5 +1,6 @@
-"""GPU parity of the SSD backward (ssd_scan_bwd) against the fp64 backward
-oracle, which is itself pinned by finite differences of the forward oracle.
+"""GPU parity of the SSD backward (ssd_scan_bwd), both paths (the chunk-
+parallel kernels and the sequential kernel), against the fp64 backward oracle,
+which is itself pinned by finite differences of the forward oracle.
 
 Metric: max|g - g_ref| / max|g_ref| per gradient tensor.  The backward's
 arithmetic is fp32 for bf16 and fp32 inputs alike (the inputs are exact in
@@ -37,38 +38,97 @@ def _grads_in(w, seed):
     return inp, dy, dfin
 
 
-def _run(ssd, inp, dy, dfin):
+def _run(ssd, inp, dy, dfin, path="auto"):
     d = {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
     out = ssd.ssd_scan_bwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"], d["init_state"],
-                           dy.cuda(), None if dfin is None else dfin.cuda())
+                           dy.cuda(), None if dfin is None else dfin.cuda(), path=path)
     torch.cuda.synchronize()
     return out
 
 
-@pytest.mark.parametrize("B,L,H,P,N,G,dtype,init,dfinal", [
-    (2, 100, 4, 64, 128, 1, "f32", True, True),     # two checkpoint segments
-    (2, 70, 4, 64, 128, 2, "bf16", True, False),
-    (1, 130, 3, 17, 44, 1, "f32", False, True),     # ragged P, N; three segments
-    (1, 1, 2, 8, 16, 1, "f32", True, True),         # one step
-    (3, 64, 8, 32, 64, 4, "bf16", False, False),    # exactly one segment
-])
-def test_backward_against_oracle(ssd, B, L, H, P, N, G, dtype, init, dfinal):
-    w = Workload("t", B, L, H, P, N, G, 16, dtype, init)
-    inp, dy, dfin = _grads_in(w, seed=210 + L)
-    dfin = dfin if dfinal else None
-    ref = ssd_bwd(**inp, dy=dy, d_final=dfin)
-    out = _run(ssd, inp, dy, dfin)
-    for k in NAMES:
+def _check(out, ref, names=NAMES):
+    for k in names:
         r = ref[k]
         err = float(np.max(np.abs(out[k].double().cpu().numpy() - r)) / max(np.max(np.abs(r)), 1e-30))
         print(f"{k}: rel err {err:.2e}")
         assert err <= TOL, f"{k}: rel err {err:.2e}"
 
 
-def test_backward_is_deterministic(ssd):
+CASES = [
+    (2, 100, 4, 64, 128, 1, "f32", True, True),     # two chunks / checkpoint segments, ragged tail
+    (2, 70, 4, 64, 128, 2, "bf16", True, False),
+    (1, 130, 3, 17, 44, 1, "f32", False, True),     # ragged P, N; three chunks
+    (1, 1, 2, 8, 16, 1, "f32", True, True),         # one step
+    (3, 64, 8, 32, 64, 4, "bf16", False, False),    # exactly one chunk
+    (2, 300, 6, 64, 128, 3, "bf16", True, True),    # five chunks, the last of 44 steps
+    (1, 257, 2, 64, 128, 1, "f32", True, True),     # one step past four full chunks
+]
+
+
+@pytest.mark.parametrize("path", ["chunked", "sequential"])
+@pytest.mark.parametrize("B,L,H,P,N,G,dtype,init,dfinal", CASES)
+def test_backward_against_oracle(ssd, path, B, L, H, P, N, G, dtype, init, dfinal):
+    w = Workload("t", B, L, H, P, N, G, 16, dtype, init)
+    inp, dy, dfin = _grads_in(w, seed=210 + L)
+    dfin = dfin if dfinal else None
+    ref = ssd_bwd(**inp, dy=dy, d_final=dfin)
+    _check(_run(ssd, inp, dy, dfin, path), ref)
+
+
+def test_backward_strong_decay(ssd):
+    # large dt and |a|: per-step decays down to about e^-7, chunk decays to about e^-110
+    w = Workload("t", 1, 200, 4, 64, 128, 1, 16, "f32", True)
+    inp, dy, dfin = _grads_in(w, seed=230)
+    inp["dt_raw"] = inp["dt_raw"] + 1.5
+    inp["A_log"] = torch.log(torch.tensor([0.5, 2.0, 8.0, 16.0]))
+    ref = ssd_bwd(**inp, dy=dy, d_final=dfin)
+    for path in ("chunked", "sequential"):
+        _check(_run(ssd, inp, dy, dfin, path), ref)
+
+
+def test_auto_takes_the_chunked_path_up_to_p64(ssd):
+    w = Workload("t", 2, 150, 4, 64, 128, 2, 16, "bf16", True)
+    inp, dy, dfin = _grads_in(w, seed=240)
+    a, c = _run(ssd, inp, dy, dfin, "auto"), _run(ssd, inp, dy, dfin, "chunked")
+    for k in NAMES:
+        assert torch.equal(a[k], c[k]), k
+    # P = 96 is past the chunked kernels: auto takes the sequential kernel, chunked is refused
+    w = Workload("t", 1, 70, 2, 96, 64, 1, 16, "f32", True)
+    inp, dy, dfin = _grads_in(w, seed=241)
+    _check(_run(ssd, inp, dy, dfin, "auto"), ssd_bwd(**inp, dy=dy, d_final=dfin))
+    with pytest.raises(RuntimeError):
+        _run(ssd, inp, dy, dfin, "chunked")
+
+
+@pytest.mark.parametrize("path", ["chunked", "sequential"])
+def test_backward_is_deterministic(ssd, path):
     w = Workload("t", 2, 150, 8, 64, 128, 2, 16, "bf16", True)
     inp, dy, dfin = _grads_in(w, seed=220)
-    o1 = _run(ssd, inp, dy, dfin)
-    o2 = _run(ssd, inp, dy, dfin)
+    o1 = _run(ssd, inp, dy, dfin, path)
+    o2 = _run(ssd, inp, dy, dfin, path)
     for k in NAMES:
         assert torch.equal(o1[k], o2[k]), k
+
+
+def test_backward_full_size_sampled_heads(ssd):
+    # the bench's workload (2 x 1024 steps, 80 heads, P 64, N 128, bf16, one group) in one call;
+    # the oracle takes two sampled heads, whose per-head gradients do not depend on the others.
+    # dB and dC sum over all heads of the group: they are checked by a call on the two heads alone.
+    from selective_state_space_04_gb300.inputs import WORKLOADS
+    w = WORKLOADS["bwd_2p7b_2x1024"]
+    inp, dy, dfin = _grads_in(w, seed=250)
+    out = _run(ssd, inp, dy, dfin)
+    heads = [7, 61]
+    sub = {k: (None if v is None else v) for k, v in inp.items()}
+    for k in ("x", "dt_raw"):
+        sub[k] = inp[k][:, :, heads].contiguous()
+    for k in ("dt_bias", "A_log", "D"):
+        sub[k] = inp[k][heads].contiguous()
+    if inp["init_state"] is not None:
+        sub["init_state"] = inp["init_state"][:, heads].contiguous()
+    dy_s, dfin_s = dy[:, :, heads].contiguous(), dfin[:, heads].contiguous()
+    ref = ssd_bwd(**sub, dy=dy_s, d_final=dfin_s)
+    sliced = dict(dx=out["dx"][:, :, heads], ddt_raw=out["ddt_raw"][:, :, heads], ddt_bias=out["ddt_bias"][heads],
+                  dA_log=out["dA_log"][heads], dD=out["dD"][heads], d_init=out["d_init"][:, heads])
+    _check(sliced, ref, names=tuple(sliced))
+    _check(_run(ssd, sub, dy_s, dfin_s), ref, names=("dB", "dC"))
