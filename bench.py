@@ -85,7 +85,23 @@ KERNEL_SOURCES = {
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
     "ssd_bwd_kernel": ("ssd_bwd.cu",),
+    "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu"),
 }
+
+# fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
+# (the maximum SM clock), for kernels bound by plain fp32 arithmetic
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def bwd_chunk_flops(w: Workload) -> int:
+    """fp32 flops of the chunk-form backward (chunks of 64 steps) per call:
+    per (b, h, chunk) the local states 2 N P Q, and the gradients C B^T (Q^2 N),
+    dy x^T (Q^2 P), dx (Q^2 P + Q N P), dB (Q^2 N + Q P N), dC (Q^2 N + Q P N)
+    multiply-adds, 2 flops each."""
+    Q, N, P = 64, w.dstate, w.headdim
+    nc = (w.seqlen + Q - 1) // Q
+    fma = 5 * N * P * Q + 3 * Q * Q * N + 2 * Q * Q * P
+    return 2 * fma * w.batch * w.nheads * nc
 
 
 def source_digest(kernel: str = "ssd_chunk_fused_kernel") -> str:
@@ -705,7 +721,7 @@ def neighbor_setup(w: Workload, dev, seed: int):
                        None if sl["init_state"] is None else sl["init_state"][:nb, :hp], sl["dy"][:nb, :, :hp],
                        sl["d_final"][:nb, :hp])
         ref.heads = min(4, w.nheads // w.ngroups)
-        return inp, d, outs, step, nbytes, "ssd_bwd_kernel", ref
+        return inp, d, outs, step, nbytes, "ssd_scan_bwd", ref
     inp = make_gnorm_inputs(w, seed=seed)
     d = {n: t.to(dev) for n, t in inp.items()}
     outs = {"out": torch.empty_like(d["y"])}
@@ -798,6 +814,23 @@ def run_gpu_neighbor(args, w: Workload):
     avg_launch_s = statistics.mean(per_launch_ms) / 1e3
     hbm_peak = float(peaks["hbm_gbs"])
     achieved = alg_bytes / avg_launch_s / 1e9
+    roof = {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+            "frac": achieved / hbm_peak, "peak_source": peak_src,
+            "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,
+            "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
+            "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3}
+    if w.op == "bwd" and w.headdim <= 64 and w.dstate <= 128:
+        # the chunk-form backward: fp32 FFMA contractions dominate its time, so
+        # its roofline is the fp32 pipe; the whole call (5 launches) is timed
+        flops = bwd_chunk_flops(w)
+        tf = flops / avg_launch_s / 1e12
+        roof = {"bound": "alu", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_local_kernel, ssd_bwd_pass_kernel, "
+                                          "ssd_bwd_grad_kernel, ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
+                "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_PEAK_TFLOPS,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
+                "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
     name = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward"}[w.op]
     line = {
         "metric": f"{name} tokens·heads/s at 1 GB300; % of HBM roofline",
@@ -807,11 +840,7 @@ def run_gpu_neighbor(args, w: Workload):
         "config": {"workload": w.name, "op": w.op, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
                    "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
                    "init_state": w.init_state, "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
-        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "peak_source": peak_src,
-                     "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,
-                     "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
-                     "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3},
+        "roofline": roof,
         "e2e": {"value": world * th * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values() if t is not None),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in back.values()),

@@ -27,10 +27,11 @@
 //      e^{cs_last-cs_k} dt_k x_k . (G_out^T B_k), plus <G_out, h_last> at the
 //      chunk's last step; ddt = x . (G^T B) + a d log dA, dA_log = a sum dt d log dA.
 // The contractions are shared-memory tiled fp32 FFMA: every operand sits in
-// shared memory with an odd row stride, each thread owns a 4 x 4 or 4 x 8
-// output tile strided by 16, so both orientations of every operand read
-// without bank conflicts.  Sums over chunks, batch rows and a group's heads
-// are left to the fixed-order reduction kernels (deterministic gradients).
+// shared memory (the states also transposed) with rows of 4 mod 32 words,
+// each thread owns a 4 x 4, 4 x 8 or 8 x 4 output tile, and every operand
+// read is a conflict-free 16-byte load (see contract()).  Sums over chunks,
+// batch rows and a group's heads are left to the fixed-order reduction
+// kernels (deterministic gradients).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -42,9 +43,9 @@ namespace {
 constexpr int kQ = 64;        // steps per chunk
 constexpr int kPM = 64;       // largest headdim of this path
 constexpr int kNM = 128;      // largest dstate of this path
-constexpr int kLP = kPM + 1;  // shared-memory row strides (odd: conflict-free columns)
-constexpr int kLN = kNM + 1;
-constexpr int kLQ = kQ + 1;
+constexpr int kLP = kPM + 4;  // shared-memory row strides: 16-byte rows, = 4 mod 32 words
+constexpr int kLN = kNM + 4;
+constexpr int kLQ = kQ + 4;
 constexpr int kThreads = 256; // 16 x 16 threads, output tiles strided by 16
 
 struct ChunkBwdParams {
@@ -67,24 +68,90 @@ template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16
 
 __device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
 
-// acc[i][j] += sum_k fa(i, k) fb(k, j) for k < K; fa / fb read shared memory
-template <int TM, int TN, int K, typename FA, typename FB>
-__device__ __forceinline__ void contract(float (&acc)[TM][TN], FA fa, FB fb)
+// Thread (ty, tx) = (tid / 16, tid % 16) owns a TM x TN output tile.  Its
+// rows are TM ty + i (contiguous, RC) or ty + 16 i; its columns 4 tx + j % 4
+// + 64 (j / 4) (contiguous groups of four) when B is k-major, else tx + 16 j.
+template <int TM, bool RC>
+__device__ __forceinline__ int tile_row(int i) { return RC ? TM * (threadIdx.x >> 4) + i : (threadIdx.x >> 4) + 16 * i; }
+template <bool BK>
+__device__ __forceinline__ int tile_col(int j) { return BK ? 4 * (threadIdx.x & 15) + (j & 3) + 64 * (j >> 2) : (threadIdx.x & 15) + 16 * j; }
+
+// acc[i][j] += sum_{k < K} A(row_i, k) B(k, col_j) (times kscale[k] if given),
+// operands in shared memory, rows 16-byte aligned, K % 4 == 0.  A is k-major
+// (A[k * lda + m]; needs RC) when AK, else m-major (A[m * lda + k]); B is
+// k-major (B[k * ldb + n]) when BK, else n-major (B[n * ldb + k]; ldb = 4 mod
+// 32).  Every read is a 16-byte load: along m or n for a k-major operand,
+// along k otherwise.  Within a warp A reads hit two addresses (broadcast) and
+// B reads 16 distinct 16-byte words in distinct banks: no conflicts.
+template <int TM, int TN, int K, bool AK, bool RC, bool BK>
+__device__ __forceinline__ void contract(float (&acc)[TM][TN], const float *A, int lda, const float *B, int ldb,
+                                         const float *kscale = nullptr)
 {
-#pragma unroll 4
-    for (int k = 0; k < K; ++k) {
-        float av[TM], bv[TN];
+    static_assert(!AK || RC, "a k-major A needs contiguous rows");
+    static_assert(TM % 4 == 0 && TN % 4 == 0 && K % 4 == 0, "whole 16-byte words");
+    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+#pragma unroll 2
+    for (int k = 0; k < K; k += 4) {
+        float av[TM][4], bv[4][TN];
+        if constexpr (AK) {
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
-            av[i] = fa(i, k);
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-        for (int j = 0; j < TN; ++j)
-            bv[j] = fb(k, j);
+                for (int iv = 0; iv < TM / 4; ++iv) {
+                    const float4 t = *reinterpret_cast<const float4 *>(A + (k + kk) * lda + TM * ty + 4 * iv);
+                    av[4 * iv][kk] = t.x;
+                    av[4 * iv + 1][kk] = t.y;
+                    av[4 * iv + 2][kk] = t.z;
+                    av[4 * iv + 3][kk] = t.w;
+                }
+        } else {
 #pragma unroll
-        for (int i = 0; i < TM; ++i)
+            for (int i = 0; i < TM; ++i) {
+                const float4 t = *reinterpret_cast<const float4 *>(A + tile_row<TM, RC>(i) * lda + k);
+                av[i][0] = t.x;
+                av[i][1] = t.y;
+                av[i][2] = t.z;
+                av[i][3] = t.w;
+            }
+        }
+        if (kscale) {
+            const float4 s = *reinterpret_cast<const float4 *>(kscale + k);
 #pragma unroll
-            for (int j = 0; j < TN; ++j)
-                acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            for (int i = 0; i < TM; ++i) {
+                av[i][0] *= s.x;
+                av[i][1] *= s.y;
+                av[i][2] *= s.z;
+                av[i][3] *= s.w;
+            }
+        }
+        if constexpr (BK) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+                for (int jv = 0; jv < TN / 4; ++jv) {
+                    const float4 t = *reinterpret_cast<const float4 *>(B + (k + kk) * ldb + 4 * tx + 64 * jv);
+                    bv[kk][4 * jv] = t.x;
+                    bv[kk][4 * jv + 1] = t.y;
+                    bv[kk][4 * jv + 2] = t.z;
+                    bv[kk][4 * jv + 3] = t.w;
+                }
+        } else {
+#pragma unroll
+            for (int j = 0; j < TN; ++j) {
+                const float4 t = *reinterpret_cast<const float4 *>(B + (tx + 16 * j) * ldb + k);
+                bv[0][j] = t.x;
+                bv[1][j] = t.y;
+                bv[2][j] = t.z;
+                bv[3][j] = t.w;
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+            for (int i = 0; i < TM; ++i)
+#pragma unroll
+                for (int j = 0; j < TN; ++j)
+                    acc[i][j] = fmaf(av[i][kk], bv[kk][j], acc[i][j]);
     }
 }
 
@@ -104,6 +171,21 @@ __device__ __forceinline__ float warp_sum(float v)
     for (int o = 16; o > 0; o >>= 1)
         v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
+}
+
+// v[0..3] to row[c0 .. c0 + 3], the columns below cols only (one 16-byte
+// store where the row and cols allow it)
+__device__ __forceinline__ void store4(float *row, int c0, int cols, const float (&v)[4])
+{
+    if (cols % 4 == 0 && (reinterpret_cast<uintptr_t>(row) & 15) == 0) {
+        if (c0 < cols)
+            *reinterpret_cast<float4 *>(row + c0) = make_float4(v[0], v[1], v[2], v[3]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (c0 + e < cols)
+                row[c0 + e] = v[e];
+    }
 }
 
 // sum over the 16 threads of a half warp (the threads sharing a tile row)
@@ -161,20 +243,30 @@ __device__ __forceinline__ void unpack(const uint4 &u, float (&v)[8]) {
     }
 }
 
-// rows r < nrows (of ROWS) and columns c < cols (of CMAX) of a row-major
+// Rows r < nrows (of ROWS) and columns c < cols (of CMAX) of a row-major
 // tensor (row stride row_stride elements) into shared memory as fp32, row
 // stride ld, each row times scale[r] when scale is given; zero elsewhere.
-// Where rows are 16-byte aligned every thread issues all of its 16-byte
-// loads before the first shared-memory store (one round trip of latency).
+// load() issues this thread's 16-byte loads and store() writes them, so a
+// kernel can have the loads of several tiles in flight at once.  Where rows
+// are not 16-byte aligned, store() falls back to scalar loads.
 template <typename T, int ROWS, int CMAX>
-__device__ __forceinline__ void stage(float *dst, int ld, const T *src, size_t row_stride, int nrows, int cols,
-                                      const float *scale = nullptr)
-{
-    constexpr int V = 16 / sizeof(T), VPR = CMAX / V, IT = ROWS * VPR / kThreads;
+struct RowTile {
+    static constexpr int V = 16 / sizeof(T), VPR = CMAX / V, IT = ROWS * VPR / kThreads;
     static_assert(ROWS * VPR % kThreads == 0, "whole vectors per thread");
-    const bool vec = cols % V == 0 && row_stride % V == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
-    if (vec) {
-        uint4 buf[IT];
+    uint4 buf[IT];
+    const T *src;
+    size_t row_stride;
+    int nrows, cols;
+    bool vec;
+    __device__ __forceinline__ void load(const T *src_, size_t row_stride_, int nrows_, int cols_)
+    {
+        src = src_;
+        row_stride = row_stride_;
+        nrows = nrows_;
+        cols = cols_;
+        vec = cols % V == 0 && row_stride % V == 0 && (reinterpret_cast<uintptr_t>(src) & 15) == 0;
+        if (!vec)
+            return;
 #pragma unroll
         for (int it = 0; it < IT; ++it) {
             const int idx = it * kThreads + threadIdx.x, r = idx / VPR, cv = idx % VPR;
@@ -182,23 +274,37 @@ __device__ __forceinline__ void stage(float *dst, int ld, const T *src, size_t r
                           ? *reinterpret_cast<const uint4 *>(src + (size_t)r * row_stride + cv * V)
                           : make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+    __device__ __forceinline__ void store(float *dst, int ld, const float *scale = nullptr) const
+    {
+        if (vec) {
 #pragma unroll
-        for (int it = 0; it < IT; ++it) {
-            const int idx = it * kThreads + threadIdx.x, r = idx / VPR, cv = idx % VPR;
-            float v[V];
-            unpack(buf[it], v);
-            const float s = scale ? scale[r] : 1.f;
+            for (int it = 0; it < IT; ++it) {
+                const int idx = it * kThreads + threadIdx.x, r = idx / VPR, cv = idx % VPR;
+                float v[V];
+                unpack(buf[it], v);
+                const float s = scale ? scale[r] : 1.f;
 #pragma unroll
-            for (int e = 0; e < V; ++e)
-                dst[r * ld + cv * V + e] = s * v[e];
-        }
-    } else {
-        for (int i = threadIdx.x; i < ROWS * CMAX; i += kThreads) {
-            const int r = i / CMAX, c = i % CMAX;
-            dst[r * ld + c] =
-                (r < nrows && c < cols) ? (scale ? scale[r] : 1.f) * to_f32<T>(src[(size_t)r * row_stride + c]) : 0.f;
+                for (int e = 0; e < V; ++e)
+                    dst[r * ld + cv * V + e] = s * v[e];
+            }
+        } else {
+            for (int i = threadIdx.x; i < ROWS * CMAX; i += kThreads) {
+                const int r = i / CMAX, c = i % CMAX;
+                dst[r * ld + c] = (r < nrows && c < cols)
+                                      ? (scale ? scale[r] : 1.f) * to_f32<T>(src[(size_t)r * row_stride + c])
+                                      : 0.f;
+            }
         }
     }
+};
+
+template <typename T, int ROWS, int CMAX>
+__device__ __forceinline__ void stage(float *dst, int ld, const T *src, size_t row_stride, int nrows, int cols)
+{
+    RowTile<T, ROWS, CMAX> t;
+    t.load(src, row_stride, nrows, cols);
+    t.store(dst, ld);
 }
 
 // 1. S(c) = sum_j e^{cs_last - cs_j} dt_j B_j x_j^T and R(c) = sum_s e^{cs_s} C_s dy_s^T
@@ -207,7 +313,7 @@ __device__ __forceinline__ void stage(float *dst, int ld, const T *src, size_t r
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams p)
 {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *Bs = smem, *Cs = Bs + kQ * kLN, *xw = Cs + kQ * kLN, *dyw = xw + kQ * kLP;
     float *dt_s = dyw + kQ * kLP, *z_s = dt_s + kQ, *cs_s = z_s + kQ, *w_s = cs_s + kQ, *e_s = w_s + kQ;
     const int H = p.H, P = p.P, N = p.N, Gg = p.G, nc = p.nc;
@@ -216,6 +322,16 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams 
     const long long t0 = (long long)c * kQ;
     const int nq = (int)min((long long)kQ, p.L - t0);
     const float a = -expf(p.A_log[h]);
+    const T *xg = static_cast<const T *>(p.x) + ((size_t)(b * p.L + t0) * H + h) * P;
+    const T *dyg = static_cast<const T *>(p.dy) + ((size_t)(b * p.L + t0) * H + h) * P;
+    const T *Bg = static_cast<const T *>(p.B) + ((size_t)(b * p.L + t0) * Gg + g) * N;
+    const T *Cg = static_cast<const T *>(p.C) + ((size_t)(b * p.L + t0) * Gg + g) * N;
+    RowTile<T, kQ, kNM> tB, tC;
+    RowTile<T, kQ, kPM> tx, tdy;
+    tB.load(Bg, (size_t)Gg * N, nq, N);   // every load in flight before the first store
+    tC.load(Cg, (size_t)Gg * N, nq, N);
+    tx.load(xg, (size_t)H * P, nq, P);
+    tdy.load(dyg, (size_t)H * P, nq, P);
     chunk_decays(p, b, h, t0, nq, a, dt_s, z_s, cs_s);
     if (threadIdx.x < kQ) {
         const int j = threadIdx.x;
@@ -223,42 +339,32 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams 
         e_s[j] = expf(cs_s[j]);
     }
     __syncthreads();
-    const T *xg = static_cast<const T *>(p.x) + ((size_t)(b * p.L + t0) * H + h) * P;
-    const T *dyg = static_cast<const T *>(p.dy) + ((size_t)(b * p.L + t0) * H + h) * P;
-    const T *Bg = static_cast<const T *>(p.B) + ((size_t)(b * p.L + t0) * Gg + g) * N;
-    const T *Cg = static_cast<const T *>(p.C) + ((size_t)(b * p.L + t0) * Gg + g) * N;
-    stage<T, kQ, kNM>(Bs, kLN, Bg, (size_t)Gg * N, nq, N);
-    stage<T, kQ, kNM>(Cs, kLN, Cg, (size_t)Gg * N, nq, N);
-    stage<T, kQ, kPM>(xw, kLP, xg, (size_t)H * P, nq, P, w_s);
-    stage<T, kQ, kPM>(dyw, kLP, dyg, (size_t)H * P, nq, P, e_s);
+    tB.store(Bs, kLN);
+    tC.store(Cs, kLN);
+    tx.store(xw, kLP, w_s);
+    tdy.store(dyw, kLP, e_s);
     __syncthreads();
-    const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const size_t NP = (size_t)N * P;
+    const int p0 = tile_col<true>(0);   // this thread's four columns p0 .. p0 + 3
     float acc[8][4];
     zero(acc);
-    contract<8, 4, kQ>(acc, [&](int i, int k) { return Bs[k * kLN + ty + 16 * i]; },
-                       [&](int k, int j) { return xw[k * kLP + tx + 16 * j]; });
+    contract<8, 4, kQ, true, true, true>(acc, Bs, kLN, xw, kLP);
     float *Sd = p.S + ((size_t)bh * (nc + 1) + c) * NP;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = ty + 16 * i, col = tx + 16 * j;
-            if (n < N && col < P)
-                Sd[(size_t)n * P + col] = acc[i][j];
-        }
+    for (int i = 0; i < 8; ++i) {
+        const int n = tile_row<8, true>(i);
+        if (n < N)
+            store4(Sd + (size_t)n * P, p0, P, acc[i]);
+    }
     zero(acc);
-    contract<8, 4, kQ>(acc, [&](int i, int k) { return Cs[k * kLN + ty + 16 * i]; },
-                       [&](int k, int j) { return dyw[k * kLP + tx + 16 * j]; });
+    contract<8, 4, kQ, true, true, true>(acc, Cs, kLN, dyw, kLP);
     float *Rd = p.R + ((size_t)bh * nc + c) * NP;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int n = ty + 16 * i, col = tx + 16 * j;
-            if (n < N && col < P)
-                Rd[(size_t)n * P + col] = acc[i][j];
-        }
+    for (int i = 0; i < 8; ++i) {
+        const int n = tile_row<8, true>(i);
+        if (n < N)
+            store4(Rd + (size_t)n * P, p0, P, acc[i]);
+    }
     if (threadIdx.x == 0)
         p.dec[bh * nc + c] = expf(cs_s[kQ - 1]);
 }
@@ -340,20 +446,82 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_pass_kernel(ChunkBwdParams p
     }
 }
 
-// a [N,P] fp32 state into shared memory, row stride kLP, zero past N, P
+// A [N,P] fp32 state (N <= kNM, P <= kPM) in two steps: load() issues this
+// thread's 16-byte loads (consecutive threads take consecutive rows n), the
+// stores then put it into shared memory straight (row stride kLP) and / or
+// transposed (dst[p * kLN + n]); zero past N, P.  Both store patterns are
+// free of bank conflicts.  Needs P % 4 == 0 (else the scalar fallbacks).
+struct StateTile {
+    static constexpr int IT = kNM * (kPM / 4) / kThreads;
+    float4 v[IT];
+    __device__ __forceinline__ static int row(int it) { return (it * kThreads + (int)threadIdx.x) % kNM; }
+    __device__ __forceinline__ static int cv(int it) { return (it * kThreads + (int)threadIdx.x) / kNM; }
+    __device__ __forceinline__ void load(const float *src, int N, int P)
+    {
+#pragma unroll
+        for (int it = 0; it < IT; ++it)
+            v[it] = (row(it) < N && 4 * cv(it) < P)
+                        ? *reinterpret_cast<const float4 *>(src + (size_t)row(it) * P + 4 * cv(it))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __device__ __forceinline__ void store(float *dst) const
+    {
+#pragma unroll
+        for (int it = 0; it < IT; ++it)
+            *reinterpret_cast<float4 *>(dst + row(it) * kLP + 4 * cv(it)) = v[it];
+    }
+    __device__ __forceinline__ void store_t(float *dst) const
+    {
+#pragma unroll
+        for (int it = 0; it < IT; ++it) {
+            float *d = dst + (4 * cv(it)) * kLN + row(it);
+            d[0] = v[it].x;
+            d[kLN] = v[it].y;
+            d[2 * kLN] = v[it].z;
+            d[3 * kLN] = v[it].w;
+        }
+    }
+    // sum of this thread's elements times the same elements of another state
+    __device__ __forceinline__ float dot(const float *other, int N, int P) const
+    {
+        float s = 0.f;
+        float4 o[IT];
+#pragma unroll
+        for (int it = 0; it < IT; ++it)
+            o[it] = (row(it) < N && 4 * cv(it) < P)
+                        ? *reinterpret_cast<const float4 *>(other + (size_t)row(it) * P + 4 * cv(it))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int it = 0; it < IT; ++it)
+            s = fmaf(v[it].x, o[it].x, fmaf(v[it].y, o[it].y, fmaf(v[it].z, o[it].z, fmaf(v[it].w, o[it].w, s))));
+        return s;
+    }
+};
+
+// scalar fallbacks (P % 4 != 0): straight and transposed
 __device__ __forceinline__ void stage_state(float *dst, const float *src, int N, int P)
 {
     stage<float, kNM, kPM>(dst, kLP, src, (size_t)P, N, P);
+}
+
+// the same state transposed: dst[p * kLN + n], zero past N, P.  Consecutive
+// threads take consecutive n, so the shared-memory stores do not conflict.
+__device__ __forceinline__ void stage_state_t(float *dst, const float *src, int N, int P)
+{
+    for (int i = threadIdx.x; i < kNM * kPM; i += kThreads) {
+        const int n = i % kNM, col = i / kNM;
+        dst[col * kLN + n] = (n < N && col < P) ? src[(size_t)n * P + col] : 0.f;
+    }
 }
 
 // 3. Every gradient of one chunk.  Grid (nc, B*H).
 template <typename T>
 __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p)
 {
-    extern __shared__ float smem[];
+    extern __shared__ __align__(16) float smem[];
     float *xs = smem, *dys = xs + kQ * kLP, *Bs = dys + kQ * kLP, *Cs = Bs + kQ * kLN;
-    float *Mt = Cs + kQ * kLN, *A2 = Mt + kQ * kLQ, *St = A2 + kQ * kLQ;
-    float *rowp = St + kNM * kLP, *colp = rowp + 16 * kQ;
+    float *Mt = Cs + kQ * kLN, *A2 = Mt + kQ * kLQ, *St = A2 + kQ * kLQ, *StT = St + kNM * kLP;
+    float *rowp = StT + kPM * kLN, *colp = rowp + 16 * kQ;
     float *dt_s = colp + 16 * kQ, *z_s = dt_s + kQ, *cs_s = z_s + kQ;
     float *ddir = cs_s + kQ, *vv = ddir + kQ, *uu = vv + kQ, *dcs = uu + kQ;
     float *red = dcs + kQ;   // [32]: per-warp sums (fixed order: deterministic)
@@ -368,22 +536,36 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
     const float *Gout = p.R + ((size_t)bh * nc + c) * NP;
     const float *hin = p.S + ((size_t)bh * (nc + 1) + c) * NP, *hlast = hin + NP;
 
-    chunk_decays(p, b, h, t0, nq, a, dt_s, z_s, cs_s);
+    // every global load of the chunk in flight together, then the stores
     const size_t rowx = (size_t)(b * p.L + t0) * H + h, rowb = (size_t)(b * p.L + t0) * Gg + g;
-    stage<T, kQ, kPM>(xs, kLP, static_cast<const T *>(p.x) + rowx * P, (size_t)H * P, nq, P);
-    stage<T, kQ, kPM>(dys, kLP, static_cast<const T *>(p.dy) + rowx * P, (size_t)H * P, nq, P);
-    stage<T, kQ, kNM>(Bs, kLN, static_cast<const T *>(p.B) + rowb * N, (size_t)Gg * N, nq, N);
-    stage<T, kQ, kNM>(Cs, kLN, static_cast<const T *>(p.C) + rowb * N, (size_t)Gg * N, nq, N);
-    stage_state(St, Gout, N, P);
+    const bool pv = P % 4 == 0;   // 16-byte rows of the states
+    RowTile<T, kQ, kPM> tX, tdy;
+    RowTile<T, kQ, kNM> tB, tC;
+    StateTile sg, sh;
+    tX.load(static_cast<const T *>(p.x) + rowx * P, (size_t)H * P, nq, P);
+    tdy.load(static_cast<const T *>(p.dy) + rowx * P, (size_t)H * P, nq, P);
+    tB.load(static_cast<const T *>(p.B) + rowb * N, (size_t)Gg * N, nq, N);
+    tC.load(static_cast<const T *>(p.C) + rowb * N, (size_t)Gg * N, nq, N);
+    if (pv) {
+        sg.load(Gout, N, P);
+        sh.load(hlast, N, P);
+    }
+    chunk_decays(p, b, h, t0, nq, a, dt_s, z_s, cs_s);
+    tX.store(xs, kLP);
+    tdy.store(dys, kLP);
+    tB.store(Bs, kLN);
+    tC.store(Cs, kLN);
     float gh = 0.f;   // <G_out, h_last>, this thread's share
-    if ((NP & 3) == 0) {
-        const float4 *g4 = reinterpret_cast<const float4 *>(Gout), *h4 = reinterpret_cast<const float4 *>(hlast);
-#pragma unroll 4
-        for (size_t e = tid; e < NP / 4; e += kThreads) {
-            const float4 gv = g4[e], hv = h4[e];
-            gh = fmaf(gv.x, hv.x, fmaf(gv.y, hv.y, fmaf(gv.z, hv.z, fmaf(gv.w, hv.w, gh))));
-        }
+    if (pv) {
+        sg.store(St);
+        sg.store_t(StT);
+#pragma unroll
+        for (int it = 0; it < StateTile::IT; ++it)
+            gh = fmaf(sg.v[it].x, sh.v[it].x,
+                      fmaf(sg.v[it].y, sh.v[it].y, fmaf(sg.v[it].z, sh.v[it].z, fmaf(sg.v[it].w, sh.v[it].w, gh))));
     } else {
+        stage_state(St, Gout, N, P);
+        stage_state_t(StT, Gout, N, P);
         for (size_t e = tid; e < NP; e += kThreads)
             gh = fmaf(Gout[e], hlast[e], gh);
     }
@@ -399,15 +581,14 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
     if (lane == 0)
         red[8 + warp] = dd;
 
-    // CB = C B^T, DX = dy x^T; Mt = E CB, A2 = E DX; row / column sums of W = Mt DX dt_j
+    // CB = C B^T, DX = dy x^T; Mt = E CB, A2 = E DX; row / column sums of W = Mt DX dt_j.
+    // Rows s = ty + 16 i, columns j = tx + 16 jj.
     {
         float cb[4][4], dx[4][4];
         zero(cb);
         zero(dx);
-        contract<4, 4, kNM>(cb, [&](int i, int k) { return Cs[(ty + 16 * i) * kLN + k]; },
-                            [&](int k, int j) { return Bs[(tx + 16 * j) * kLN + k]; });
-        contract<4, 4, kPM>(dx, [&](int i, int k) { return dys[(ty + 16 * i) * kLP + k]; },
-                            [&](int k, int j) { return xs[(tx + 16 * j) * kLP + k]; });
+        contract<4, 4, kNM, false, false, false>(cb, Cs, kLN, Bs, kLN);
+        contract<4, 4, kPM, false, false, false>(dx, dys, kLP, xs, kLP);
         float rp[4] = {0.f, 0.f, 0.f, 0.f}, cp[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -431,31 +612,33 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
     }
     __syncthreads();
 
-    // dx_j = D dy_j + dt_j (Mt^T dy + e^{cs_last - cs_j} B G_out)_j; x . (G^T B) and v
+    // dx_j = D dy_j + dt_j (Mt^T dy + e^{cs_last - cs_j} B G_out)_j; x . (G^T B) and v.
+    // Rows j = 4 ty + i, columns p = 4 tx + q.
+    const int c4 = 4 * tx;
     {
         float in[4][4], out[4][4];
         zero(in);
         zero(out);
-        contract<4, 4, kQ>(in, [&](int i, int k) { return Mt[k * kLQ + ty + 16 * i]; },
-                           [&](int k, int j) { return dys[k * kLP + tx + 16 * j]; });
-        contract<4, 4, kNM>(out, [&](int i, int k) { return Bs[(ty + 16 * i) * kLN + k]; },
-                            [&](int k, int j) { return St[k * kLP + tx + 16 * j]; });
+        contract<4, 4, kQ, true, true, true>(in, Mt, kLQ, dys, kLP);
+        contract<4, 4, kNM, false, true, true>(out, Bs, kLN, St, kLP);
         float *dxg = p.dx + rowx * P;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int j = ty + 16 * i;
+            const int j = tile_row<4, true>(i);
             const float eo = expf(cs_last - cs_s[j]), dtj = dt_s[j];
-            float dsum = 0.f, vsum = 0.f;
+            const float4 x4 = *reinterpret_cast<const float4 *>(xs + j * kLP + c4);
+            const float4 y4 = *reinterpret_cast<const float4 *>(dys + j * kLP + c4);
+            const float xv[4] = {x4.x, x4.y, x4.z, x4.w}, yv[4] = {y4.x, y4.y, y4.z, y4.w};
+            float dsum = 0.f, vsum = 0.f, o[4];
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const int col = tx + 16 * q;
                 const float gx = fmaf(eo, out[i][q], in[i][q]);
-                const float xv = xs[j * kLP + col];
-                dsum = fmaf(xv, gx, dsum);
-                vsum = fmaf(xv, out[i][q], vsum);
-                if (j < nq && col < P)
-                    dxg[(size_t)j * H * P + col] = fmaf(Dh, dys[j * kLP + col], dtj * gx);
+                dsum = fmaf(xv[q], gx, dsum);
+                vsum = fmaf(xv[q], out[i][q], vsum);
+                o[q] = fmaf(Dh, yv[q], dtj * gx);
             }
+            if (j < nq)
+                store4(dxg + (size_t)j * H * P, c4, P, o);
             dsum = half_warp_sum(dsum);
             vsum = half_warp_sum(vsum);
             if (tx == 0) {
@@ -465,54 +648,69 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
         }
     }
 
-    // dB_j = dt_j (A2^T C + e^{cs_last - cs_j} x G_out^T)_j
+    // dB_j = dt_j (A2^T C + e^{cs_last - cs_j} x G_out^T)_j.  Rows j = 4 ty + i,
+    // columns n = 4 tx + q and 64 + 4 tx + q.  The loads of h_in are in flight meanwhile.
+    if (pv)
+        sh.load(hin, N, P);
     {
         float in[4][8], out[4][8];
         zero(in);
         zero(out);
-        contract<4, 8, kQ>(in, [&](int i, int k) { return A2[k * kLQ + ty + 16 * i]; },
-                           [&](int k, int j) { return Cs[k * kLN + tx + 16 * j]; });
-        contract<4, 8, kPM>(out, [&](int i, int k) { return xs[(ty + 16 * i) * kLP + k]; },
-                            [&](int k, int j) { return St[(tx + 16 * j) * kLP + k]; });
+        contract<4, 8, kQ, true, true, true>(in, A2, kLQ, Cs, kLN);
+        contract<4, 8, kPM, false, true, true>(out, xs, kLP, StT, kLN);
         float *dbg = p.dB_head + rowx * N;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int j = ty + 16 * i;
+            const int j = tile_row<4, true>(i);
             const float eo = expf(cs_last - cs_s[j]), dtj = dt_s[j];
+            float o0[4], o1[4];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const int n = tx + 16 * q;
-                if (j < nq && n < N)
-                    dbg[(size_t)j * H * N + n] = dtj * fmaf(eo, out[i][q], in[i][q]);
+            for (int q = 0; q < 4; ++q) {
+                o0[q] = dtj * fmaf(eo, out[i][q], in[i][q]);
+                o1[q] = dtj * fmaf(eo, out[i][q + 4], in[i][q + 4]);
+            }
+            if (j < nq) {
+                store4(dbg + (size_t)j * H * N, c4, N, o0);
+                store4(dbg + (size_t)j * H * N, 64 + c4, N, o1);
             }
         }
     }
     __syncthreads();
-    stage_state(St, hin, N, P);
+    if (pv)
+        sh.store_t(StT);
+    else
+        stage_state_t(StT, hin, N, P);
     __syncthreads();
 
-    // dC_s = (A2 dt) B + e^{cs_s} dy h_in^T; u_s = C_s . (e^{cs_s} h_in dy_s)
+    // dC_s = (A2 dt) B + e^{cs_s} dy h_in^T; u_s = C_s . (e^{cs_s} h_in dy_s).
+    // Rows s = 4 ty + i, columns n = 4 tx + q and 64 + 4 tx + q.
     {
         float in[4][8], out[4][8];
         zero(in);
         zero(out);
-        contract<4, 8, kQ>(in, [&](int i, int k) { return A2[(ty + 16 * i) * kLQ + k] * dt_s[k]; },
-                           [&](int k, int j) { return Bs[k * kLN + tx + 16 * j]; });
-        contract<4, 8, kPM>(out, [&](int i, int k) { return dys[(ty + 16 * i) * kLP + k]; },
-                            [&](int k, int j) { return St[(tx + 16 * j) * kLP + k]; });
+        contract<4, 8, kQ, false, true, true>(in, A2, kLQ, Bs, kLN, dt_s);
+        contract<4, 8, kPM, false, true, true>(out, dys, kLP, StT, kLN);
         float *dcg = p.dC_head + rowx * N;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int s = ty + 16 * i;
+            const int s = tile_row<4, true>(i);
             const float es = expf(cs_s[s]);
-            float usum = 0.f;
+            const float4 ca = *reinterpret_cast<const float4 *>(Cs + s * kLN + c4);
+            const float4 cb = *reinterpret_cast<const float4 *>(Cs + s * kLN + 64 + c4);
+            const float cv[8] = {ca.x, ca.y, ca.z, ca.w, cb.x, cb.y, cb.z, cb.w};
+            float usum = 0.f, o0[4], o1[4];
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const int n = tx + 16 * q;
                 const float inter = es * out[i][q];
-                usum = fmaf(Cs[s * kLN + n], inter, usum);
-                if (s < nq && n < N)
-                    dcg[(size_t)s * H * N + n] = in[i][q] + inter;
+                usum = fmaf(cv[q], inter, usum);
+                if (q < 4)
+                    o0[q] = in[i][q] + inter;
+                else
+                    o1[q - 4] = in[i][q] + inter;
+            }
+            if (s < nq) {
+                store4(dcg + (size_t)s * H * N, c4, N, o0);
+                store4(dcg + (size_t)s * H * N, 64 + c4, N, o1);
             }
             usum = half_warp_sum(usum);
             if (tx == 0)
@@ -581,7 +779,7 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
 
 constexpr size_t kLocalSmem = (size_t)(2 * kQ * kLN + 2 * kQ * kLP + 5 * kQ) * sizeof(float);
 constexpr size_t kGradSmem =
-    (size_t)(2 * kQ * kLP + 2 * kQ * kLN + 2 * kQ * kLQ + kNM * kLP + 32 * kQ + 7 * kQ + 32) * sizeof(float);
+    (size_t)(2 * kQ * kLP + 2 * kQ * kLN + 2 * kQ * kLQ + kNM * kLP + kPM * kLN + 32 * kQ + 7 * kQ + 32) * sizeof(float);
 static_assert(kGradSmem <= 227 * 1024, "grad kernel shared memory");
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }

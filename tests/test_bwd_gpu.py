@@ -4,7 +4,7 @@ which is itself pinned by finite differences of the forward oracle.
 
 Metric: max|g - g_ref| / max|g_ref| per gradient tensor.  The backward's
 arithmetic is fp32 for bf16 and fp32 inputs alike (the inputs are exact in
-both), so one bound serves: 2e-4 (sums over up to a few thousand terms).
+both), so the fp32 bound of the forward serves for both: 1e-4.
 """
 import numpy as np
 import pytest
@@ -15,7 +15,7 @@ from selective_state_space_04_gb300.inputs import Workload, make_inputs
 
 pytestmark = pytest.mark.gpu
 
-TOL = 2e-4
+TOL = 1e-4
 NAMES = ("dx", "ddt_raw", "ddt_bias", "dA_log", "dB", "dC", "dD", "d_init")
 
 
