@@ -140,9 +140,7 @@ template <> __device__ __forceinline__ float silu_out<__nv_bfloat16>(float v)
 }
 
 constexpr int kConvTile = 64;     // time steps per thread
-constexpr int kConvAhead = 8;     // steps whose loads are in flight together
 constexpr int kConvThreads = 128;
-constexpr int kConvVec = 4;       // channels per thread (one 8-byte bf16 vector)
 
 struct ConvParams {
     const void *xbc;            // [B,L,C]
@@ -151,35 +149,66 @@ struct ConvParams {
     void *x, *B, *C;            // [B,L,H*P], [B,L,G*N] x2
     void *state_out;            // [B,K-1,C] or null
     long long L;
-    int Cc, HP, GN, nvec;       // nvec = C / kConvVec
+    int Cc, HP, GN, nvec;       // nvec = C / channels per thread
 };
 
-// thread: 4 consecutive channels (vector v) over kConvTile steps of one batch
-// row; the K-1 inputs before the current step stay in registers
-template <typename T, int K>
-__global__ void __launch_bounds__(kConvThreads, 6) ssd_conv1d_silu_kernel(ConvParams p)
+// Asynchronous 16-byte copies from global into shared memory (cp.async, L1
+// bypassed): the bytes in flight wait in shared memory, not in registers.
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem)
 {
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+constexpr int kConvStages = 16;   // steps of each thread in flight (its own ring of 16-byte slots)
+static_assert((kConvStages & (kConvStages - 1)) == 0, "a power of two (slot = step & (stages - 1))");
+
+template <typename T, int V> struct VecSel;
+template <typename T> struct VecSel<T, 4> { using type = Vec4<T>; };
+template <typename T> struct VecSel<T, 8> { using type = Vec8<T>; };
+
+// a 16-byte vector from its raw bits
+__device__ __forceinline__ void from_raw(Vec8<__nv_bfloat16> &v, const uint4 &r) { v.u = r; }
+__device__ __forceinline__ void from_raw(Vec4<float> &v, const uint4 &r)
+{
+    v.a = make_float4(__uint_as_float(r.x), __uint_as_float(r.y), __uint_as_float(r.z), __uint_as_float(r.w));
+}
+
+// thread: V consecutive channels (one 16-byte vector v) over kConvTile steps
+// of one batch row; the K-1 inputs before the current step stay in registers.
+// Each thread streams its inputs through its own ring of kConvStages 16-byte
+// slots in shared memory (cp.async), so kConvStages steps are in flight per
+// thread; no slot is shared, so no barrier is needed.
+template <typename T, int K, int V>
+__global__ void __launch_bounds__(kConvThreads, 4) ssd_conv1d_silu_kernel(ConvParams p)
+{
+    using Vec = typename VecSel<T, V>::type;
+    static_assert(V * sizeof(T) == 16, "one 16-byte vector per step");
+    __shared__ uint4 ring[kConvStages * kConvThreads];
     const int v = blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= p.nvec)
         return;   // (no barrier in this kernel)
     const long long b = blockIdx.z, L = p.L;
     const long long t0 = (long long)blockIdx.y * kConvTile;
-    const int c0 = kConvVec * v, Cc = p.Cc;
+    const int c0 = V * v, Cc = p.Cc;
     const T *in = static_cast<const T *>(p.xbc) + (size_t)b * L * Cc + c0;
-    float wv[K][kConvVec], bv[kConvVec];
+    float wv[K][V], bv[V];
 #pragma unroll
-    for (int e = 0; e < kConvVec; ++e) {
+    for (int e = 0; e < V; ++e) {
 #pragma unroll
         for (int k = 0; k < K; ++k)
             wv[k][e] = p.w[(size_t)(c0 + e) * K + k];
         bv[e] = p.bias ? p.bias[c0 + e] : 0.f;
     }
     // win[j]: the input at step t - (K-1) + j, j < K-1
-    float win[K - 1][kConvVec];
+    float win[K - 1][V];
 #pragma unroll
     for (int j = 0; j < K - 1; ++j) {
         const long long tt = t0 - (K - 1) + j;
-        Vec4<T> u;
+        Vec u;
         if (tt >= 0) {
             u.load(in + (size_t)tt * Cc);
             u.get(win[j]);
@@ -188,7 +217,7 @@ __global__ void __launch_bounds__(kConvThreads, 6) ssd_conv1d_silu_kernel(ConvPa
             u.get(win[j]);
         } else {
 #pragma unroll
-            for (int e = 0; e < kConvVec; ++e)
+            for (int e = 0; e < V; ++e)
                 win[j][e] = 0.f;
         }
     }
@@ -209,58 +238,79 @@ __global__ void __launch_bounds__(kConvThreads, 6) ssd_conv1d_silu_kernel(ConvPa
         off = c0 - p.HP - p.GN;
     }
     const int nt = (int)min((long long)kConvTile, L - t0);
-    // kConvAhead steps' loads are issued together before the first is used
-    for (int i0 = 0; i0 < nt; i0 += kConvAhead) {
-        Vec4<T> u[kConvAhead];
+    const T *src = in + (size_t)t0 * Cc;
+    T *dst = out + ((size_t)b * L + t0) * stride + off;
+    // one step: the output from the window and the current input, then the window moves on
+    auto step = [&](const Vec &u, T *d) {
+        float cur[V], acc[V];
+        u.get(cur);
 #pragma unroll
-        for (int a = 0; a < kConvAhead; ++a)
-            if (i0 + a < nt)
-                u[a].load_cs(in + (size_t)(t0 + i0 + a) * Cc);
+        for (int e = 0; e < V; ++e) {
+            float s = fmaf(wv[0][e], cur[e], bv[e]);
 #pragma unroll
-        for (int a = 0; a < kConvAhead; ++a) {
-            if (i0 + a >= nt)
-                break;
-            const long long t = t0 + i0 + a;
-            float cur[kConvVec], acc[kConvVec];
-            u[a].get(cur);
-#pragma unroll
-            for (int e = 0; e < kConvVec; ++e) {
-                float s = fmaf(wv[0][e], cur[e], bv[e]);
-#pragma unroll
-                for (int k = 1; k < K; ++k)
-                    s = fmaf(wv[k][e], win[K - 1 - k][e], s);   // the input k steps back
-                acc[e] = silu_out<T>(s);
-            }
-            Vec4<T> o;
-            o.set(acc);
-            o.store(out + ((size_t)b * L + t) * stride + off);
-#pragma unroll
-            for (int j = 0; j + 1 < K - 1; ++j)
-#pragma unroll
-                for (int e = 0; e < kConvVec; ++e)
-                    win[j][e] = win[j + 1][e];
-#pragma unroll
-            for (int e = 0; e < kConvVec; ++e)
-                win[K - 2][e] = cur[e];
+            for (int k = 1; k < K; ++k)
+                s = fmaf(wv[k][e], win[K - 1 - k][e], s);   // the input k steps back
+            acc[e] = silu_out<T>(s);
         }
+        Vec o;
+        o.set(acc);
+        o.store(d);
+#pragma unroll
+        for (int j = 0; j + 1 < K - 1; ++j)
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                win[j][e] = win[j + 1][e];
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            win[K - 2][e] = cur[e];
+    };
+    // the ring: slot s holds step i with i % kConvStages == s; one commit
+    // group per step (empty past the tile's end), so after the wait below at
+    // most kConvStages - 1 groups, the steps after i, are still in flight
+    uint4 *mine = ring + threadIdx.x;
+#pragma unroll
+    for (int s = 0; s < kConvStages; ++s) {
+        if (s < nt)
+            cp_async16(mine + s * kConvThreads, src + (size_t)s * Cc);
+        cp_async_commit();
     }
+    const T *next = src + (size_t)kConvStages * Cc;   // the step kConvStages ahead
+#pragma unroll 4
+    for (int i = 0; i < nt; ++i) {
+        cp_async_wait<kConvStages - 1>();
+        uint4 *slot = mine + (i & (kConvStages - 1)) * kConvThreads;
+        const uint4 raw = *slot;
+        if (i + kConvStages < nt)
+            cp_async16(slot, next);   // after the read of this slot, in program order
+        cp_async_commit();
+        next += Cc;
+        Vec u;
+        from_raw(u, raw);
+        step(u, dst);
+        dst += stride;
+    }
+    cp_async_wait<0>();
     if (p.state_out && t0 + nt == L) {   // the last tile: the last K-1 inputs
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
-            Vec4<T> o;
+            Vec o;
             o.set(win[j]);
             o.store(static_cast<T *>(p.state_out) + ((size_t)b * (K - 1) + j) * Cc + c0);
         }
     }
 }
 
+// bf16: 8 channels (one 16-byte vector) per thread; fp32: 4 (one 16-byte vector)
+template <typename T> constexpr int conv_vec() { return sizeof(T) == 2 ? 8 : 4; }
+
 template <typename T>
 cudaError_t conv_launch_t(int K, const ConvParams &cp, dim3 grid, cudaStream_t st)
 {
+    constexpr int V = conv_vec<T>();
     switch (K) {
-    case 2: ssd_conv1d_silu_kernel<T, 2><<<grid, kConvThreads, 0, st>>>(cp); break;
-    case 3: ssd_conv1d_silu_kernel<T, 3><<<grid, kConvThreads, 0, st>>>(cp); break;
-    case 4: ssd_conv1d_silu_kernel<T, 4><<<grid, kConvThreads, 0, st>>>(cp); break;
+    case 2: ssd_conv1d_silu_kernel<T, 2, V><<<grid, kConvThreads, 0, st>>>(cp); break;
+    case 3: ssd_conv1d_silu_kernel<T, 3, V><<<grid, kConvThreads, 0, st>>>(cp); break;
+    case 4: ssd_conv1d_silu_kernel<T, 4, V><<<grid, kConvThreads, 0, st>>>(cp); break;
     default: return cudaErrorInvalidValue;
     }
     return cudaGetLastError();
@@ -365,7 +415,7 @@ cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t st)
     cp.HP = a.nheads * a.headdim;
     cp.GN = a.ngroups * a.dstate;
     cp.Cc = cp.HP + 2 * cp.GN;
-    cp.nvec = cp.Cc / kConvVec;
+    cp.nvec = cp.Cc / (a.dtype == SSD_DTYPE_BF16 ? conv_vec<__nv_bfloat16>() : conv_vec<float>());
     const dim3 grid((unsigned)((cp.nvec + kConvThreads - 1) / kConvThreads),
                     (unsigned)((a.seqlen + kConvTile - 1) / kConvTile), (unsigned)a.batch);
     const cudaError_t e = a.dtype == SSD_DTYPE_BF16 ? conv_launch_t<__nv_bfloat16>(a.kernel_size, cp, grid, st)
