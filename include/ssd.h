@@ -131,6 +131,11 @@ ssd_status_t ssd_scan_fwd(const void *x, const float *dt_raw, const float *dt_bi
  * buffers stream-ordered, copies the inputs in, runs the scan, copies y (and
  * final_state when non-NULL) back, releases the buffers, and synchronises
  * `stream` before returning, so the host outputs are ready on SSD_OK.
+ * Calls of 32 MiB or more with several batch rows run in up to 8 pieces of
+ * whole rows through three library-owned streams (copies in, scan, copies
+ * out), ordered after and joined back into `stream` by events, so that the
+ * two copy directions and the scan overlap.  Every piece takes the schedule
+ * the whole batch would, and the results are bitwise those of ssd_scan_fwd.
  */
 ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *dt_bias,
                                const float *A_log, const void *B, const void *C,

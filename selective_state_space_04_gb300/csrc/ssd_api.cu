@@ -3,6 +3,7 @@
 // the host-buffer variant, which synchronises it at the end).
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -154,6 +155,34 @@ cudaMemPool_t scratch_pool(int dev)
         pools[dev] = p;
     }
     return pools[dev];
+}
+
+// The host-buffer path pipelines pieces of whole batch rows through three
+// library-owned streams per device (copies in, kernels, copies out).
+constexpr int kHostPieces = 8;                          // most pieces per call
+constexpr int64_t kHostPipelineMinBytes = 32ll << 20;   // smaller calls run as one piece
+
+struct HostStreams {
+    cudaStream_t in = nullptr, comp = nullptr, out = nullptr;
+};
+
+HostStreams host_streams(int dev)
+{
+    static std::mutex mu;
+    static HostStreams streams[64];
+    if (dev < 0 || dev >= 64)
+        return HostStreams{};
+    std::lock_guard<std::mutex> lk(mu);
+    HostStreams &h = streams[dev];
+    if (!h.in) {
+        HostStreams n;
+        if (cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&n.comp, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking) != cudaSuccess)
+            return HostStreams{};
+        h = n;
+    }
+    return h;
 }
 
 // The paths that need no scratch: the sequential scan and the decode step.
@@ -331,44 +360,127 @@ ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *
     if (cudaGetDevice(&dev) != cudaSuccess)
         return SSD_ERR_CUDA;
     cudaMemPool_t pool = scratch_pool(dev);
-    if (!pool)
+    const HostStreams hs = host_streams(dev);
+    if (!pool || !hs.in)
         return SSD_ERR_CUDA;
     char *buf = nullptr;
     if (cudaMallocFromPoolAsync((void **)&buf, (size_t)total, pool, st) != cudaSuccess)
         return SSD_ERR_CUDA;
-    bool ok = true;
+
+    // Pieces of whole batch rows go through three streams: copies in, kernels,
+    // copies out, so the two copy directions and the scan overlap.  All kernels
+    // stay on one stream (the persistent chunked kernel never shares the GPU
+    // with another of its launches).  Each piece takes the schedule the whole
+    // batch would (ranges and pieces give the same bits; a batch that would
+    // take the split schedule runs as one piece), so the result is bitwise the
+    // one ssd_scan_fwd gives.
+    const int64_t Bt = dims->batch;
+    const ScanArgs whole = make_args(buf + off_x, (const float *)(buf + off_dt), (const float *)(buf + off_bias),
+                                     (const float *)(buf + off_alog), buf + off_B, buf + off_C,
+                                     (const float *)(buf + off_D),
+                                     init_state ? (const float *)(buf + off_h0) : nullptr, buf + off_y,
+                                     final_state ? (float *)(buf + off_hf) : nullptr, dims);
+    const uint32_t req = dims->flags & SSD_PATH_MASK;
+    const int32_t path = resolve_path(whole, req, true);
+    if (path < 0) {
+        cudaFreeAsync(buf, st);
+        cudaStreamSynchronize(st);
+        return (ssd_status_t)(-path);
+    }
+    int sched = path == SSD_PATH_CHUNKED ? chunk_schedule(whole) : SSD_SCHEDULE_NONE;
+    int pieces = (int)std::min<int64_t>(Bt, kHostPieces);
+    if (sched == SSD_SCHEDULE_SPLIT || total < kHostPipelineMinBytes)
+        pieces = 1;
+    const int64_t xr = sz.x / Bt, dtr = sz.dt / Bt, bcr = sz.bc / Bt, str = sz.state / Bt;   // bytes per row
+
+    cudaEvent_t start = nullptr, in_done[kHostPieces] = {}, comp_done[kHostPieces] = {}, end_in = nullptr,
+                end_comp = nullptr, end_out = nullptr;
+    bool ok = cudaEventCreateWithFlags(&start, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&end_in, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&end_comp, cudaEventDisableTiming) == cudaSuccess &&
+              cudaEventCreateWithFlags(&end_out, cudaEventDisableTiming) == cudaSuccess;
+    for (int k = 0; ok && k < pieces; ++k)
+        ok = cudaEventCreateWithFlags(&in_done[k], cudaEventDisableTiming) == cudaSuccess &&
+             cudaEventCreateWithFlags(&comp_done[k], cudaEventDisableTiming) == cudaSuccess;
+    ok = ok && cudaEventRecord(start, st) == cudaSuccess && cudaStreamWaitEvent(hs.in, start, 0) == cudaSuccess &&
+         cudaStreamWaitEvent(hs.comp, start, 0) == cudaSuccess && cudaStreamWaitEvent(hs.out, start, 0) == cudaSuccess;
     auto h2d = [&](int64_t off, const void *src, int64_t n) {
         if (ok && src && n > 0)
-            ok = cudaMemcpyAsync(buf + off, src, (size_t)n, cudaMemcpyHostToDevice, st) == cudaSuccess;
+            ok = cudaMemcpyAsync(buf + off, src, (size_t)n, cudaMemcpyHostToDevice, hs.in) == cudaSuccess;
     };
-    h2d(off_x, x, sz.x);
-    h2d(off_dt, dt_raw, sz.dt);
+    auto d2h = [&](void *dst, int64_t off, int64_t n) {
+        if (ok && dst && n > 0)
+            ok = cudaMemcpyAsync(dst, buf + off, (size_t)n, cudaMemcpyDeviceToHost, hs.out) == cudaSuccess;
+    };
     h2d(off_bias, dt_bias, sz.par);
     h2d(off_alog, A_log, sz.par);
-    h2d(off_B, B, sz.bc);
-    h2d(off_C, C, sz.bc);
     h2d(off_D, D, sz.par);
-    h2d(off_h0, init_state, init_state ? sz.state : 0);
-    ssd_status_t rs = SSD_ERR_CUDA;
-    if (ok) {
-        const ScanArgs a = make_args(buf + off_x, (const float *)(buf + off_dt),
+    ssd_status_t rs = ok ? SSD_OK : SSD_ERR_CUDA;
+    int64_t b0 = 0;
+    for (int k = 0; k < pieces && rs == SSD_OK; ++k) {
+        const int64_t rows = Bt / pieces + (k < Bt % pieces ? 1 : 0);
+        const char *hx = static_cast<const char *>(x), *hB = static_cast<const char *>(B);
+        const char *hC = static_cast<const char *>(C);
+        h2d(off_x + b0 * xr, hx + b0 * xr, rows * xr);
+        h2d(off_dt + b0 * dtr, reinterpret_cast<const char *>(dt_raw) + b0 * dtr, rows * dtr);
+        h2d(off_B + b0 * bcr, hB + b0 * bcr, rows * bcr);
+        h2d(off_C + b0 * bcr, hC + b0 * bcr, rows * bcr);
+        if (init_state)
+            h2d(off_h0 + b0 * str, reinterpret_cast<const char *>(init_state) + b0 * str, rows * str);
+        ok = ok && cudaEventRecord(in_done[k], hs.in) == cudaSuccess &&
+             cudaStreamWaitEvent(hs.comp, in_done[k], 0) == cudaSuccess;
+        if (!ok) {
+            rs = SSD_ERR_CUDA;
+            break;
+        }
+        ssd_dims_t pd = *dims;
+        pd.batch = rows;
+        if (pieces > 1 && sched != SSD_SCHEDULE_NONE)
+            pd.flags = (pd.flags & ~SSD_SCHEDULE_REQUEST_MASK) | ((uint32_t)sched << SSD_SCHEDULE_SHIFT);
+        const ScanArgs a = make_args(buf + off_x + b0 * xr, (const float *)(buf + off_dt + b0 * dtr),
                                      (const float *)(buf + off_bias), (const float *)(buf + off_alog),
-                                     buf + off_B, buf + off_C, (const float *)(buf + off_D),
-                                     init_state ? (const float *)(buf + off_h0) : nullptr,
-                                     buf + off_y, final_state ? (float *)(buf + off_hf) : nullptr, dims);
-        rs = run_device(a, dims->flags & SSD_PATH_MASK, st);
-    }
-    if (rs == SSD_OK) {
-        ok = cudaMemcpyAsync(y, buf + off_y, (size_t)sz.x, cudaMemcpyDeviceToHost, st) == cudaSuccess;
-        if (ok && final_state)
-            ok = cudaMemcpyAsync(final_state, buf + off_hf, (size_t)sz.state, cudaMemcpyDeviceToHost,
-                                 st) == cudaSuccess;
+                                     buf + off_B + b0 * bcr, buf + off_C + b0 * bcr, (const float *)(buf + off_D),
+                                     init_state ? (const float *)(buf + off_h0 + b0 * str) : nullptr,
+                                     buf + off_y + b0 * xr,
+                                     final_state ? (float *)(buf + off_hf + b0 * str) : nullptr, &pd);
+        rs = run_device(a, req, hs.comp);
+        if (rs != SSD_OK)
+            break;
+        ok = cudaEventRecord(comp_done[k], hs.comp) == cudaSuccess &&
+             cudaStreamWaitEvent(hs.out, comp_done[k], 0) == cudaSuccess;
+        d2h(static_cast<char *>(y) + b0 * xr, off_y + b0 * xr, rows * xr);
+        if (final_state)
+            d2h(reinterpret_cast<char *>(final_state) + b0 * str, off_hf + b0 * str, rows * str);
         if (!ok)
+            rs = SSD_ERR_CUDA;
+        b0 += rows;
+    }
+    // join the worker streams back into the caller's stream before the buffer goes
+    const bool joined = end_in && end_comp && end_out && cudaEventRecord(end_in, hs.in) == cudaSuccess &&
+                        cudaEventRecord(end_comp, hs.comp) == cudaSuccess &&
+                        cudaEventRecord(end_out, hs.out) == cudaSuccess &&
+                        cudaStreamWaitEvent(st, end_in, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(st, end_comp, 0) == cudaSuccess &&
+                        cudaStreamWaitEvent(st, end_out, 0) == cudaSuccess;
+    if (!joined) {   // fall back to waiting on the host
+        cudaStreamSynchronize(hs.in);
+        cudaStreamSynchronize(hs.comp);
+        cudaStreamSynchronize(hs.out);
+        if (rs == SSD_OK)
             rs = SSD_ERR_CUDA;
     }
     cudaFreeAsync(buf, st);
     if (cudaStreamSynchronize(st) != cudaSuccess && rs == SSD_OK)
         rs = SSD_ERR_CUDA;
+    for (cudaEvent_t e : {start, end_in, end_comp, end_out})
+        if (e)
+            cudaEventDestroy(e);
+    for (int k = 0; k < pieces; ++k) {
+        if (in_done[k])
+            cudaEventDestroy(in_done[k]);
+        if (comp_done[k])
+            cudaEventDestroy(comp_done[k]);
+    }
     return rs;
 }
 

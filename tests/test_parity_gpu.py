@@ -208,6 +208,20 @@ def test_host_entry_point_matches_device(ssd):
     assert torch.equal(yh, yd.cpu()) and torch.equal(fh, fd.cpu())
 
 
+@pytest.mark.parametrize("init", [False, True])
+def test_host_entry_point_pipelined_matches_device(ssd, init):
+    # 55 MB of buffers and 4 batch rows: the host path runs 4 pieces through its
+    # copy-in / compute / copy-out streams; the bits must be the device path's
+    w = Workload("t", 4, 2048, 24, 64, 128, 1, 256, "bf16", init)
+    inp = make_inputs(w, seed=16)
+    yd, fd = run(ssd, inp, w)
+    pinned = {k: (None if v is None else v.contiguous().pin_memory()) for k, v in inp.items()}
+    yh, fh = ssd.ssd_scan_fwd_host(pinned["x"], pinned["dt_raw"], pinned["dt_bias"], pinned["A_log"],
+                                   pinned["B"], pinned["C"], pinned["D"], pinned["init_state"],
+                                   chunk=w.chunk)
+    assert torch.equal(yh, yd.cpu()) and torch.equal(fh, fd.cpu())
+
+
 def test_empty_batch_and_sequence(ssd):
     w = small(batch=0)
     inp = make_inputs(w, seed=14)
