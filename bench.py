@@ -86,6 +86,7 @@ KERNEL_SOURCES = {
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
     "ssd_bwd_kernel": ("ssd_bwd.cu",),
     "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu"),
+    "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh"),
 }
 
 # fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
@@ -102,6 +103,13 @@ def bwd_chunk_flops(w: Workload) -> int:
     nc = (w.seqlen + Q - 1) // Q
     fma = 5 * N * P * Q + 3 * Q * Q * N + 2 * Q * Q * P
     return 2 * fma * w.batch * w.nheads * nc
+
+
+def complex_flops(w: Workload) -> int:
+    """fp32 flops of the complex scan per call: per state float and step, the
+    complex update (2 multiply-adds and 1 multiply per float of a complex
+    pair) and the readout (1 multiply-add), FMA counted as 2."""
+    return 7 * w.dstate * w.headdim * w.seqlen * w.batch * w.nheads
 
 
 def source_digest(kernel: str = "ssd_chunk_fused_kernel") -> str:
@@ -665,7 +673,7 @@ CONV_TAPS = 4
 def neighbor_setup(w: Workload, dev, seed: int):
     """(host inputs, device inputs, device outputs, step function, algorithmic
     bytes, kernel name, oracle function of the first nb batch rows) of the
-    conv1d + SiLU or gated RMSNorm workload ``w``."""
+    conv1d + SiLU, gated RMSNorm, backward or complex-scan workload ``w``."""
     from selective_state_space_04_gb300 import ssd
     from selective_state_space_04_gb300.inputs import make_conv_inputs, make_gnorm_inputs
     import oracle.neighbors as on
@@ -692,6 +700,26 @@ def neighbor_setup(w: Workload, dev, seed: int):
                            None if inp["conv_state"] is None else inp["conv_state"][:nb],
                            w.nheads, w.headdim, w.ngroups, w.dstate)
         return inp, d, outs, step, nbytes, "ssd_conv1d_silu_kernel", ref
+    if w.op == "complex":
+        from selective_state_space_04_gb300.inputs import make_complex_inputs
+        import oracle.complex_scan as ocx
+        inp = make_complex_inputs(w, seed=seed)
+        d = {n: (None if t is None else t.to(dev)) for n, t in inp.items()}
+        outs = {"y": torch.empty_like(d["x"]),
+                "final_state": torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                                           device=dev)}
+
+        def step(stream):
+            ssd.complex_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_polar"], d["B"], d["C"], d["D"],
+                                 d["init_state"], y=outs["y"], final_state=outs["final_state"], stream=stream)
+        state = w.batch * w.nheads * w.headdim * w.dstate * 4
+        nbytes = (2 * BL * HP * es + BL * w.nheads * 4 + 2 * BL * GN * es + 4 * w.nheads * 4
+                  + (state if w.init_state else 0) + state)
+
+        def ref(nb):
+            ocx.complex_fwd(inp["x"][:nb], inp["dt_raw"][:nb], inp["dt_bias"], inp["A_polar"], inp["B"][:nb],
+                            inp["C"][:nb], inp["D"], None if inp["init_state"] is None else inp["init_state"][:nb])
+        return inp, d, outs, step, nbytes, "ssd_complex_seq_kernel", ref
     if w.op == "bwd":
         inp = make_inputs(w, seed=seed)
         rng = np.random.Generator(np.random.PCG64(seed + 1))
@@ -732,6 +760,10 @@ def neighbor_setup(w: Workload, dev, seed: int):
     def ref(nb):
         on.gated_rmsnorm(inp["y"][:nb], inp["z"][:nb], inp["weight"])
     return inp, d, outs, step, 3 * BL * HP * es + HP * 4, "ssd_gated_rmsnorm_kernel", ref
+
+
+NEIGHBOR_NAMES = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward",
+                  "complex": "complex-valued (ET) scan fwd"}
 
 
 def neighbor_oracle_rate(w: Workload, ref, target_s: float, min_seconds: float = 0.0):
@@ -831,7 +863,16 @@ def run_gpu_neighbor(args, w: Workload):
                 "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
                 "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
                 "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
-    name = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward"}[w.op]
+    if w.op == "complex" and w.seqlen > 1:
+        # the state stays in registers over the sequence: fp32 arithmetic bounds it
+        flops = complex_flops(w)
+        tf = flops / avg_launch_s / 1e12
+        roof = {"bound": "alu", "kernel": kernel, "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": tf / FP32_PEAK_TFLOPS, "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
+                "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
+                "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
+    name = NEIGHBOR_NAMES[w.op]
     line = {
         "metric": f"{name} tokens·heads/s at 1 GB300; % of HBM roofline",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -869,7 +910,7 @@ def run_reference_neighbor(args, w: Workload):
         secs += th / v
         th_total += th
     value = th_total / secs
-    name = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward"}[w.op]
+    name = NEIGHBOR_NAMES[w.op]
     line = {
         "impl": "reference", "metric": f"{name} tokens·heads/s at 1 GB300; % of HBM roofline",
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -898,7 +939,7 @@ def main():
     w = WORKLOADS[args.workload]
     if w.op == "trap":
         (run_reference_trap if args.impl == "reference" else run_gpu_trap)(args, w)
-    elif w.op in ("conv", "gnorm", "bwd"):
+    elif w.op in ("conv", "gnorm", "bwd", "complex"):
         (run_reference_neighbor if args.impl == "reference" else run_gpu_neighbor)(args, w)
     elif args.impl == "reference":
         run_reference(args, w)

@@ -299,6 +299,31 @@ ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *we
                                    void *out, const ssd_dims_t *dims, void *stream);
 
 /*
+ * ssd_complex_scan_fwd -- the complex-valued scan with exponential-trapezoidal
+ * (ET) discretisation: the Mamba-3 complex SSD module of the pages, as its
+ * header defines it (complex_ssd.ts).  Per batch row and head, with
+ * A = exp(log|A| + i arg A) and dt_t = softplus(dt_raw_t + dt_bias):
+ *   A_bar_t = exp(dt_t A),  B_bar_t = (A_bar_t - 1) A^-1 B_t  (the exact hold)
+ *   h_t = A_bar_t h_{t-1} + B_bar_t x_t^T,  y_t = Re(C_t^T h_t) + D x_t
+ * (The page's printed kernel exponentiates dt (log|A| + i arg A) and reads out
+ * Re(conj(C) h); its header's statement is the one implemented.)
+ * x, y [B,L,H,P] and B, C [B,L,G,N] in dims->dtype; B and C hold N/2 complex
+ * numbers as (re, im) pairs along N; A_polar [H,2] fp32 = (log|A|, arg A);
+ * dt_raw [B,L,H], dt_bias, D [H] fp32; init_state (NULL: zero) and
+ * final_state (NULL: not written) [B,H,P,N] fp32, complex as (re, im) pairs
+ * along N; final_state may be init_state (in place).  DEVICE pointers, 16-byte
+ * aligned; y overlaps no input.  flags: SSD_PATH_AUTO or SSD_PATH_SEQUENTIAL
+ * (one sequential kernel; seqlen 1 is a decode step).  Supported: N % 4 == 0,
+ * N <= 512; P <= 128 for N <= 128, P <= 64 for N <= 256, P <= 32 for
+ * N <= 512; fp32 or bf16.  seqlen 0 copies the state through.  Errors as
+ * ssd_scan_fwd.
+ */
+ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const float *dt_bias,
+                                  const float *A_polar, const void *B, const void *C, const float *D,
+                                  const float *init_state, void *y, float *final_state,
+                                  const ssd_dims_t *dims, void *stream);
+
+/*
  * ssd_scan_bwd -- the backward of ssd_scan_fwd: the gradients of a loss with
  * respect to every input, given dy = dL/dy and d_final = dL/d final_state.
  * They are the derivatives of the recurrence ssd_scan_fwd evaluates (the

@@ -646,6 +646,71 @@ const char *ssd_status_string(int32_t status)
 
 int32_t ssd_abi_version(void) { return SSD_ABI_VERSION; }
 
+ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const float *dt_bias, const float *A_polar,
+                                  const void *B, const void *C, const float *D, const float *init_state, void *y,
+                                  float *final_state, const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if ((dims->flags & ~SSD_PATH_MASK) != 0)
+        return SSD_ERR_INVALID_DIMS;
+    const uint32_t path = dims->flags & SSD_PATH_MASK;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+        return SSD_ERR_UNSUPPORTED;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!x || !dt_raw || !dt_bias || !A_polar || !B || !C || !D || !y))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {x, dt_raw, dt_bias, A_polar, B, C, D, init_state, y, final_state};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    // outputs overlap no input (the state may be updated in place) and not each other
+    const void *ins[] = {x, dt_raw, dt_bias, A_polar, B, C, D, init_state};
+    const int64_t inb[] = {sz.x, sz.dt, sz.par, 2 * sz.par, sz.bc, sz.bc, sz.par, sz.state};
+    const void *outs[] = {work ? y : nullptr, final_state};
+    const int64_t outb[] = {sz.x, sz.state};
+    for (int o = 0; o < 2; ++o)
+        for (int i = 0; i < 8; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i]) && !(o == 1 && ins[i] == init_state && outs[o] == init_state))
+                return SSD_ERR_ALIASING;
+    if (overlaps(outs[0], outb[0], outs[1], outb[1]))
+        return SSD_ERR_ALIASING;
+    ComplexArgs ca;
+    ca.x = x;
+    ca.B = B;
+    ca.C = C;
+    ca.dt_raw = dt_raw;
+    ca.dt_bias = dt_bias;
+    ca.A_polar = A_polar;
+    ca.D = D;
+    ca.init_state = init_state;
+    ca.y = y;
+    ca.final_state = final_state;
+    ca.batch = dims->batch;
+    ca.seqlen = dims->seqlen;
+    ca.nheads = dims->nheads;
+    ca.headdim = dims->headdim;
+    ca.dstate = dims->dstate;
+    ca.ngroups = dims->ngroups;
+    ca.dtype = dims->dtype;
+    if (!complex_supported(ca))
+        return SSD_ERR_UNSUPPORTED;
+    if (dims->batch == 0)
+        return SSD_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->seqlen == 0) {   // no steps: the state passes through (zero when not given)
+        if (!final_state || final_state == init_state)
+            return SSD_OK;
+        const cudaError_t e = init_state ? cudaMemcpyAsync(final_state, init_state, (size_t)sz.state,
+                                                           cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(final_state, 0, (size_t)sz.state, st);
+        return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    }
+    return complex_launch(ca, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+}
+
 ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, const float *dt, const float *a,
                                const float *trap, const float *D, const float *h0, const void *k0,
                                const void *v0, void *y, float *h_final, void *k_final, void *v_final,

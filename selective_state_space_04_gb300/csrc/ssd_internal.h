@@ -106,6 +106,20 @@ bool bwd_chunk_supported(const BwdArgs &a);
 size_t bwd_chunk_workspace_bytes(const BwdArgs &a);
 cudaError_t bwd_chunk_launch(const BwdArgs &a, void *workspace, cudaStream_t stream);
 
+// ---- complex-valued scan with ET discretisation: ssd_complex.cu
+struct ComplexArgs {
+    const void *x, *B, *C;                      // [B,L,H,P], [B,L,G,N] x2 (dtype; N/2 complex as re, im)
+    const float *dt_raw, *dt_bias, *A_polar, *D; // [B,L,H], [H], [H,2] (log|A|, arg A), [H]
+    const float *init_state;                    // [B,H,P,N] or null
+    void *y;                                    // [B,L,H,P]
+    float *final_state;                         // [B,H,P,N] or null
+    int64_t batch, seqlen;
+    int nheads, headdim, dstate, ngroups;
+    int dtype;
+};
+bool complex_supported(const ComplexArgs &a);
+cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t stream);
+
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream);

@@ -79,6 +79,13 @@ WORKLOADS = {
     # the backward of the scan on the 2.7B layer's heads, 2 sequences of 1024 steps
     # (dy drawn like x, N(0,1); d_final like the initial state, N(0, 0.1^2))
     "bwd_2p7b_2x1024": Workload("bwd_2p7b_2x1024", 2, 1024, 80, 64, 128, 1, 256, "bf16", True, "bwd"),
+    # the complex-valued (ET) scan, N = 128 floats = 64 complex components per
+    # row: many 64-token sequences with the state in and out, and one decode
+    # step of 128 sequences of the 2.7B layer's heads
+    "complex_many_short_seqs": Workload("complex_many_short_seqs", 256, 64, 48, 64, 128, 1, 1, "bf16", True,
+                                        "complex"),
+    "complex_decode_2p7b_128seq": Workload("complex_decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 1, "bf16", True,
+                                           "complex"),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
@@ -152,6 +159,40 @@ def make_trap_inputs(w: Workload, seed: int = 0) -> dict:
     else:
         h0 = k0 = v0 = None
     return dict(v=v, k=k, q=q, dt=dt, a=a, trap=trap, D=D, h0=h0, k0=k0, v0=v0)
+
+
+def make_complex_inputs(w: Workload, seed: int = 0) -> dict:
+    """One seeded input set for the complex-valued (ET) scan of workload ``w``,
+    as CPU torch tensors.
+
+    Keys (draw order): x [B,L,H,P] ~ N(0,1); dt_raw [B,L,H] ~ N(0, 0.1^2);
+    dt_bias [H] = log(expm1(dt0)), dt0 = exp(U[ln 1e-3, ln 1e-1]) (as the SSD
+    inputs); A_polar [H,2] = (log U[1,16], U[0.6 pi, 1.4 pi]) (|A| as the SSD's
+    decay rates, arg A with cos < 0 so every mode decays); B, C [B,L,G,N] ~
+    N(0,1) (re and im parts alike); D [H] ~ N(0,1); when ``w.init_state``
+    init_state [B,H,P,N] ~ N(0, 0.1^2) fp32, else None.
+    """
+    rng = np.random.Generator(np.random.PCG64(seed))
+    Bt, L, H, P, N, G = w.batch, w.seqlen, w.nheads, w.headdim, w.dstate, w.ngroups
+    sd = _TORCH_DTYPE[w.dtype]
+
+    def normal(shape, std=1.0):
+        a = rng.standard_normal(size=shape, dtype=np.float32)
+        if std != 1.0:
+            a *= np.float32(std)
+        return a
+
+    x = torch.from_numpy(normal((Bt, L, H, P))).to(sd)
+    dt_raw = torch.from_numpy(normal((Bt, L, H), 0.1))
+    dt0 = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=H))
+    dt_bias = torch.from_numpy(np.log(np.expm1(dt0)).astype(np.float32))
+    A_polar = torch.from_numpy(np.stack([np.log(rng.uniform(1.0, 16.0, size=H)),
+                                         rng.uniform(0.6 * math.pi, 1.4 * math.pi, size=H)], 1).astype(np.float32))
+    Bm = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    Cm = torch.from_numpy(normal((Bt, L, G, N))).to(sd)
+    D = torch.from_numpy(normal((H,)))
+    init_state = torch.from_numpy(normal((Bt, H, P, N), 0.1)) if w.init_state else None
+    return dict(x=x, dt_raw=dt_raw, dt_bias=dt_bias, A_polar=A_polar, B=Bm, C=Cm, D=D, init_state=init_state)
 
 
 def make_conv_inputs(w: Workload, K: int = 4, seed: int = 0) -> dict:

@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_gated_rmsnorm_fwd.argtypes = [vp, vp, vp, ctypes.c_float, vp, ctypes.POINTER(SsdDims), vp]
     lib.ssd_scan_bwd.restype = ctypes.c_int
     lib.ssd_scan_bwd.argtypes = [vp] * 18 + [ctypes.POINTER(SsdDims), vp]
+    lib.ssd_complex_scan_fwd.restype = ctypes.c_int
+    lib.ssd_complex_scan_fwd.argtypes = [vp] * 10 + [ctypes.POINTER(SsdDims), vp]
     return lib
 
 
@@ -311,6 +313,32 @@ def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, chu
     _check(_lib.ssd_trap_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
                                   ctypes.c_void_p(st.cuda_stream)), "ssd_trap_scan_fwd")
     return y, h_final, k_final, v_final
+
+
+def complex_scan_fwd(x, dt_raw, dt_bias, A_polar, B, C, D, init_state=None, *, path="auto", y=None,
+                     final_state=None, return_state=True, stream=None):
+    """Complex-valued scan with ET discretisation on CUDA tensors.  Returns
+    ``(y, final_state)`` (the state None when not returned).
+
+    ``x [B,L,H,P]`` and ``B, C [B,L,G,N]`` share one dtype (bf16 or fp32); B
+    and C hold N/2 complex numbers as (re, im) pairs along N.  ``A_polar
+    [H,2]`` = (log|A|, arg A), ``dt_raw [B,L,H]``, ``dt_bias, D [H]`` and the
+    states ``[B,H,P,N]`` (complex as (re, im) pairs) are fp32.
+    """
+    Bt, L, H, P = x.shape
+    G, N = B.shape[2], B.shape[3]
+    if y is None:
+        y = torch.empty_like(x)
+    if final_state is None and return_state:
+        final_state = torch.empty((Bt, H, P, N), dtype=torch.float32, device=x.device)
+    named = (("x", x), ("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_polar", A_polar), ("B", B), ("C", C),
+             ("D", D), ("init_state", init_state), ("y", y), ("final_state", final_state))
+    _require_cuda(named)
+    d = make_dims(Bt, L, H, P, N, G, 1, x.dtype, path)
+    st = torch.cuda.current_stream(x.device) if stream is None else stream
+    _check(_lib.ssd_complex_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
+                                     ctypes.c_void_p(st.cuda_stream)), "ssd_complex_scan_fwd")
+    return y, final_state
 
 
 def _require_cuda(named):

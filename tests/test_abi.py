@@ -250,3 +250,24 @@ def test_bwd_entry_validation_before_cuda(libssd):
     assert _bwd_call(libssd, libssd.make_dims(1, 8, 2, 16, 30, 1, 1, "f32", path="sequential")) == 4
     assert _bwd_call(libssd, libssd.make_dims(1, 8, 2, 16, 160, 1, 1, "f32")) == 4
     assert _bwd_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0   # empty: no device access
+
+
+def _complex_call(libssd, dims_, **override):
+    lib = libssd.lib()
+    base = 0x10000000
+    # 10 distinct, 16-byte aligned, widely spaced fake addresses (validation only)
+    names = ["x", "dt_raw", "dt_bias", "A_polar", "B", "C", "D", "init_state", "y", "final_state"]
+    ptrs = {n: ctypes.c_void_p(base + i * 0x1000000) for i, n in enumerate(names)}
+    ptrs.update(override)
+    return lib.ssd_complex_scan_fwd(*(ptrs[n] for n in names), ctypes.byref(dims_), None)
+
+
+def test_complex_entry_validation_before_cuda(libssd):
+    d = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32")
+    assert _complex_call(libssd, d, A_polar=None) == 2                             # SSD_ERR_NULL_PTR
+    assert _complex_call(libssd, d, B=ctypes.c_void_p(0x30000008)) == 3            # SSD_ERR_MISALIGNED
+    assert _complex_call(libssd, d, y=ctypes.c_void_p(0x10000000 + 0x100)) == 7    # y inside x: SSD_ERR_ALIASING
+    assert _complex_call(libssd, libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="chunked")) == 4
+    assert _complex_call(libssd, libssd.make_dims(2, 8, 4, 16, 30, 2, 1, "f32")) == 4   # N % 4 != 0
+    assert _complex_call(libssd, libssd.make_dims(2, 8, 4, 16, 1024, 2, 1, "f32")) == 4  # N > 512
+    assert _complex_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0    # empty: no device access
