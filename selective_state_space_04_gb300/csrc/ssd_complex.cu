@@ -125,6 +125,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             cs[tt * N + 2 * k + 1] = to_f32<T>(Cg[gi + 1]);
         }
         __syncthreads();
+        // unrolled: the readout reductions of a step (shuffle chains, not on the
+        // recurrence) overlap the next steps' state updates
+#pragma unroll 4
         for (int i = 0; i < nt; ++i) {
             const float abr = ab[4 * i], abi = ab[4 * i + 1];
             float4 bt[NV], ct[NV];
@@ -177,6 +180,96 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
     }
 }
 
+// One step (seqlen 1): a stream of the state.  One CTA of 4 warps per (b, h),
+// no shared memory and no barrier; each warp takes blocks of 8 rows, loads all
+// of a block's state before using it, writes the updated rows straight back
+// and reduces each row's readout with shuffles.
+constexpr int kDecWarps = 4, kDecRows = 8;
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kDecWarps * 32, NV == 1 ? 5 : 1) ssd_complex_decode_kernel(CplxParams p)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, P = p.P, N = p.N;
+    const long long bh = blockIdx.x;   // b * H + h (seqlen 1: also the token index)
+    const long long b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / p.G);
+    const float lm = p.A_polar[2 * h], ph = p.A_polar[2 * h + 1];
+    float sph, cph;
+    sincosf(ph, &sph, &cph);
+    const float mag = expf(lm), imag_ = expf(-lm);
+    const float Ar = mag * cph, Ai = mag * sph, Ir = imag_ * cph, Ii = -imag_ * sph;
+    const float dt = softplus_f32(p.dt_raw[bh] + p.dt_bias[h]);
+    float s, c;
+    sincosf(dt * Ai, &s, &c);
+    const float e = expf(dt * Ar);
+    const float abr = e * c, abi = e * s;
+    const float fr = (abr - 1.f) * Ir - abi * Ii, fi = (abr - 1.f) * Ii + abi * Ir;   // (A_bar - 1) A^-1
+    const float Dh = p.D[h];
+    const T *Bg = static_cast<const T *>(p.B) + (b * p.G + g) * (long long)N;
+    const T *Cg = static_cast<const T *>(p.C) + (b * p.G + g) * (long long)N;
+    float bb[NV][4], cv[NV][4];   // this lane's B_bar and C: two complex components per float4
+#pragma unroll
+    for (int q = 0; q < NV; ++q) {
+        const int n = 4 * lane + 128 * q;
+        float bv[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            bv[k] = n < N ? to_f32<T>(Bg[n + k]) : 0.f;
+            cv[q][k] = n < N ? to_f32<T>(Cg[n + k]) : 0.f;
+        }
+        bb[q][0] = fr * bv[0] - fi * bv[1];
+        bb[q][1] = fr * bv[1] + fi * bv[0];
+        bb[q][2] = fr * bv[2] - fi * bv[3];
+        bb[q][3] = fr * bv[3] + fi * bv[2];
+    }
+    const T *xg = static_cast<const T *>(p.x) + bh * P;
+    T *yg = static_cast<T *>(p.y) + bh * P;
+    const size_t sbase = (size_t)bh * P * N;
+    for (int p0 = warp * kDecRows; p0 < P; p0 += kDecWarps * kDecRows) {
+        float4 hv[kDecRows][NV];
+        float xv[kDecRows];
+#pragma unroll
+        for (int i = 0; i < kDecRows; ++i) {
+            const int pr = p0 + i;
+            xv[i] = pr < P ? to_f32<T>(xg[pr]) : 0.f;
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                const int n = 4 * lane + 128 * q;
+                hv[i][q] = (p.h0 && pr < P && n < N)
+                               ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)pr * N + n))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kDecRows; ++i) {
+            const int pr = p0 + i;
+            float acc = 0.f;
+#pragma unroll
+            for (int q = 0; q < NV; ++q) {
+                const float4 z = hv[i][q];
+                const float r0 = fmaf(abr, z.x, fmaf(-abi, z.y, bb[q][0] * xv[i]));
+                const float i0 = fmaf(abr, z.y, fmaf(abi, z.x, bb[q][1] * xv[i]));
+                const float r1 = fmaf(abr, z.z, fmaf(-abi, z.w, bb[q][2] * xv[i]));
+                const float i1 = fmaf(abr, z.w, fmaf(abi, z.z, bb[q][3] * xv[i]));
+                acc = fmaf(cv[q][0], r0, acc);   // Re(C h)
+                acc = fmaf(-cv[q][1], i0, acc);
+                acc = fmaf(cv[q][2], r1, acc);
+                acc = fmaf(-cv[q][3], i1, acc);
+                const int n = 4 * lane + 128 * q;
+                if (p.h_final && pr < P && n < N)
+                    __stcs(reinterpret_cast<float4 *>(p.h_final + sbase + (size_t)pr * N + n),
+                           make_float4(r0, i0, r1, i1));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+                acc += __shfl_xor_sync(0xffffffffu, acc, o);
+            if (lane == 0 && pr < P)
+                yg[pr] = from_f32<T>(fmaf(Dh, xv[i], acc));
+        }
+    }
+}
+
 int complex_nv(int N) { return N <= 128 ? 1 : N <= 256 ? 2 : 4; }
 
 }  // namespace
@@ -218,6 +311,21 @@ cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t st)
     const size_t smem = (size_t)(p.tblk * (2 * a.dstate + a.headdim + 4)) * sizeof(float);
     const dim3 grid((unsigned)(a.batch * a.nheads));
     const bool bf = a.dtype == SSD_DTYPE_BF16;
+    if (a.seqlen == 1) {   // the decode step: the specialised stream of the state
+        if (nv == 1)
+            bf ? ssd_complex_decode_kernel<__nv_bfloat16, 1><<<grid, kDecWarps * 32, 0, st>>>(p)
+               : ssd_complex_decode_kernel<float, 1><<<grid, kDecWarps * 32, 0, st>>>(p);
+        else if (nv == 2)
+            bf ? ssd_complex_decode_kernel<__nv_bfloat16, 2><<<grid, kDecWarps * 32, 0, st>>>(p)
+               : ssd_complex_decode_kernel<float, 2><<<grid, kDecWarps * 32, 0, st>>>(p);
+        else
+            bf ? ssd_complex_decode_kernel<__nv_bfloat16, 4><<<grid, kDecWarps * 32, 0, st>>>(p)
+               : ssd_complex_decode_kernel<float, 4><<<grid, kDecWarps * 32, 0, st>>>(p);
+        const cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess)
+            note_launches(1);
+        return e;
+    }
 #define SSD_CPLX_LAUNCH(NVV)                                                                                    \
     do {                                                                                                         \
         if (bf)                                                                                                  \
