@@ -87,6 +87,7 @@ KERNEL_SOURCES = {
     "ssd_bwd_kernel": ("ssd_bwd.cu",),
     "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu"),
     "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh"),
+    "ssd_complex_decode_kernel": ("ssd_complex.cu", "warp_rows.cuh"),
 }
 
 # fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
@@ -719,7 +720,8 @@ def neighbor_setup(w: Workload, dev, seed: int):
         def ref(nb):
             ocx.complex_fwd(inp["x"][:nb], inp["dt_raw"][:nb], inp["dt_bias"], inp["A_polar"], inp["B"][:nb],
                             inp["C"][:nb], inp["D"], None if inp["init_state"] is None else inp["init_state"][:nb])
-        return inp, d, outs, step, nbytes, "ssd_complex_seq_kernel", ref
+        kernel = "ssd_complex_decode_kernel" if w.seqlen == 1 else "ssd_complex_seq_kernel"
+        return inp, d, outs, step, nbytes, kernel, ref
     if w.op == "bwd":
         inp = make_inputs(w, seed=seed)
         rng = np.random.Generator(np.random.PCG64(seed + 1))
