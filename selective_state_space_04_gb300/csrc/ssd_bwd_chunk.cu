@@ -76,8 +76,11 @@ __device__ __forceinline__ int tile_row(int i) { return RC ? TM * (threadIdx.x >
 template <bool BK>
 __device__ __forceinline__ int tile_col(int j) { return BK ? 4 * (threadIdx.x & 15) + (j & 3) + 64 * (j >> 2) : (threadIdx.x & 15) + 16 * j; }
 
-// acc[i][j] += sum_{k < K} A(row_i, k) B(k, col_j) (times kscale[k] if given),
-// operands in shared memory, rows 16-byte aligned, K % 4 == 0.  A is k-major
+// acc[i][j] += sum_{k_lo <= k < k_hi} A(row_i, k) B(k, col_j) (times kscale[k]
+// if given; k_hi = -1 means K), operands in shared memory, rows 16-byte
+// aligned, K, k_lo and k_hi multiples of 4.  The bounds let a contraction with
+// a causal factor skip the blocks of k where that factor is zero for all of
+// the thread's rows (adding those exact zeros would not change the sums).  A is k-major
 // (A[k * lda + m]; needs RC) when AK, else m-major (A[m * lda + k]); B is
 // k-major (B[k * ldb + n]) when BK, else n-major (B[n * ldb + k]; ldb = 4 mod
 // 32).  Every read is a 16-byte load: along m or n for a k-major operand,
@@ -85,13 +88,14 @@ __device__ __forceinline__ int tile_col(int j) { return BK ? 4 * (threadIdx.x & 
 // B reads 16 distinct 16-byte words in distinct banks: no conflicts.
 template <int TM, int TN, int K, bool AK, bool RC, bool BK>
 __device__ __forceinline__ void contract(float (&acc)[TM][TN], const float *A, int lda, const float *B, int ldb,
-                                         const float *kscale = nullptr)
+                                         const float *kscale = nullptr, int k_lo = 0, int k_hi = -1)
 {
     static_assert(!AK || RC, "a k-major A needs contiguous rows");
     static_assert(TM % 4 == 0 && TN % 4 == 0 && K % 4 == 0, "whole 16-byte words");
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+    const int kend = k_hi < 0 ? K : k_hi;
 #pragma unroll 2
-    for (int k = 0; k < K; k += 4) {
+    for (int k = k_lo; k < kend; k += 4) {
         float av[TM][4], bv[4][TN];
         if constexpr (AK) {
 #pragma unroll
@@ -619,7 +623,7 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
         float in[4][4], out[4][4];
         zero(in);
         zero(out);
-        contract<4, 4, kQ, true, true, true>(in, Mt, kLQ, dys, kLP);
+        contract<4, 4, kQ, true, true, true>(in, Mt, kLQ, dys, kLP, nullptr, 4 * ty);   // Mt[s][j] = 0 for s < j
         contract<4, 4, kNM, false, true, true>(out, Bs, kLN, St, kLP);
         float *dxg = p.dx + rowx * P;
 #pragma unroll
@@ -656,7 +660,7 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
         float in[4][8], out[4][8];
         zero(in);
         zero(out);
-        contract<4, 8, kQ, true, true, true>(in, A2, kLQ, Cs, kLN);
+        contract<4, 8, kQ, true, true, true>(in, A2, kLQ, Cs, kLN, nullptr, 4 * ty);   // A2[s][j] = 0 for s < j
         contract<4, 8, kPM, false, true, true>(out, xs, kLP, StT, kLN);
         float *dbg = p.dB_head + rowx * N;
 #pragma unroll
@@ -688,7 +692,7 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_grad_kernel(ChunkBwdParams p
         float in[4][8], out[4][8];
         zero(in);
         zero(out);
-        contract<4, 8, kQ, false, true, true>(in, A2, kLQ, Bs, kLN, dt_s);
+        contract<4, 8, kQ, false, true, true>(in, A2, kLQ, Bs, kLN, dt_s, 0, 4 * ty + 4);   // A2[s][j] = 0 for j > s
         contract<4, 8, kPM, false, true, true>(out, dys, kLP, StT, kLN);
         float *dcg = p.dC_head + rowx * N;
 #pragma unroll
