@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams 
 //    thread runs one chain over kVec consecutive state elements (n, p) of one
 //    (b, h), loading kBatch chunks ahead so that the loads of a batch are all
 //    in flight together (the stores of a batch go to other addresses).
-constexpr int kVec = 4, kBatch = 8;
+constexpr int kVec = 4, kBatch = 16;
 template <int V>
 __device__ __forceinline__ void chain(float *buf, size_t stride, const float *dec, int nc, bool reverse,
                                       float (&v)[V])

@@ -47,6 +47,9 @@ def run(ssd, inp, init=None, **kw):
     (1, 1, 2, 8, 16, 1, "f32", True),         # one step: a decode step
     (3, 64, 8, 32, 256, 4, "bf16", False),    # two float4 of state per lane
     (1, 40, 2, 32, 512, 1, "f32", True),      # four float4 per lane; smaller time blocks
+    (1, 20, 2, 128, 128, 1, "f32", True),     # the largest headdim: 16 warps of 8 rows
+    (2, 1, 3, 64, 256, 1, "bf16", True),      # decode kernel, two float4 per lane
+    (1, 1, 2, 32, 512, 2, "f32", True),       # decode kernel, four float4 per lane
 ])
 def test_complex_scan_against_oracle(ssd, B, L, H, P, N, G, dtype, init):
     w = Workload("t", B, L, H, P, N, G, 1, dtype, init, "complex")
