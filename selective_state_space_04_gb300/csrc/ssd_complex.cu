@@ -34,6 +34,7 @@ struct CplxParams {
     float *h_final;                   // [B,H,P,N] or null
     long long L;
     int H, P, N, G, tblk;
+    int Pp;                           // staged x row stride: the CTA's rows (warps x rows per warp)
 };
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
@@ -60,8 +61,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
     const long long L = p.L;
     float *bb = sm;                  // [TB][N]: B_bar (interleaved)
     float *cs = bb + TB * N;         // [TB][N]: C
-    float *xs = cs + TB * N;         // [TB][P]
-    float *ab = xs + TB * P;         // [TB][4]: A_bar (re, im), (A_bar - 1) A^-1 (re, im)
+    float *xs = cs + TB * N;         // [TB][Pp], zero past P
+    float *ab = xs + TB * p.Pp;      // [TB][4]: A_bar (re, im), (A_bar - 1) A^-1 (re, im)
+    const int Pp = p.Pp;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
     const long long bh = blockIdx.x;
@@ -108,9 +110,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             ab[4 * i + 2] = (abr - 1.f) * Ir - abi * Ii;   // (A_bar - 1) A^-1
             ab[4 * i + 3] = (abr - 1.f) * Ii + abi * Ir;
         }
-        for (int i = threadIdx.x; i < nt * P; i += nthr) {
-            const int tt = i / P, pp = i - tt * P;
-            xs[i] = to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]);
+        for (int i = threadIdx.x; i < nt * Pp; i += nthr) {
+            const int tt = i / Pp, pp = i - tt * Pp;
+            xs[i] = pp < P ? to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]) : 0.f;
         }
         __syncthreads();
         const int K = N / 2;
@@ -138,11 +140,24 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
                 bt[c] = in ? *reinterpret_cast<const float4 *>(bb + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
                 ct[c] = in ? *reinterpret_cast<const float4 *>(cs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            float acc[RPW];
+            float acc[RPW], xr[RPW];   // this warp's RPW rows of x_t: 16- or 8-byte loads
+            if constexpr (RPW >= 4) {
+#pragma unroll
+                for (int v = 0; v < RPW / 4; ++v) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(xs + i * Pp + p0 + 4 * v);
+                    xr[4 * v] = x4.x;
+                    xr[4 * v + 1] = x4.y;
+                    xr[4 * v + 2] = x4.z;
+                    xr[4 * v + 3] = x4.w;
+                }
+            } else {
+                const float2 x2 = *reinterpret_cast<const float2 *>(xs + i * Pp + p0);
+                xr[0] = x2.x;
+                xr[1] = x2.y;
+            }
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
-                const int pr = p0 + r;
-                const float xv = pr < P ? xs[i * P + pr] : 0.f;
+                const float xv = xr[r];
                 float s = 0.f;
 #pragma unroll
                 for (int c = 0; c < NV; ++c) {
@@ -162,7 +177,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             warp_sum_rows_all<RPW>(acc, lane);
             const int pr = p0 + summed_row<RPW>(lane);
             if ((lane & (32 / RPW - 1)) == 0 && pr < P)
-                yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] = from_f32<T>(fmaf(Dh, xs[i * P + pr], acc[0]));
+                yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] = from_f32<T>(fmaf(Dh, xs[i * Pp + pr], acc[0]));
         }
     }
 
@@ -305,10 +320,11 @@ cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t st)
     p.G = a.ngroups;
     const int nv = complex_nv(a.dstate), rows = kStateFloat4PerLane / nv;
     const int warps = (a.headdim + rows - 1) / rows;
+    p.Pp = warps * rows;
     // steps per staged block: up to 64, within about 200 KB of shared memory
-    const long long per_step = (long long)(2 * a.dstate + a.headdim + 4) * (long long)sizeof(float);
+    const long long per_step = (long long)(2 * a.dstate + p.Pp + 4) * (long long)sizeof(float);
     p.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, a.seqlen, (200LL << 10) / per_step}));
-    const size_t smem = (size_t)(p.tblk * (2 * a.dstate + a.headdim + 4)) * sizeof(float);
+    const size_t smem = (size_t)(p.tblk * (2 * a.dstate + p.Pp + 4)) * sizeof(float);
     const dim3 grid((unsigned)(a.batch * a.nheads));
     const bool bf = a.dtype == SSD_DTYPE_BF16;
     if (a.seqlen == 1) {   // the decode step: the specialised stream of the state
