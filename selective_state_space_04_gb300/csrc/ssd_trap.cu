@@ -37,6 +37,7 @@ struct TrapParams {
     void *k_final, *v_final;
     long long L;
     int H, P, N, G, tblk;
+    int Pp;   // staged v row stride: the CTA's rows (warps x rows per warp)
 };
 
 template <typename T> __device__ __forceinline__ float to_f32(T v);
@@ -103,8 +104,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
     const long long L = p.L;
     float *ks = sm;                  // [TB][N]
     float *qs = ks + TB * N;         // [TB][N]
-    float *vs = qs + TB * N;         // [TB][P]
-    float *cf = vs + TB * P;         // [TB][3]: alpha, beta, gamma
+    float *vs = qs + TB * N;         // [TB][Pp], zero past P
+    float *cf = vs + TB * p.Pp;      // [TB][3]: alpha, beta, gamma
+    const int Pp = p.Pp;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
     const long long bh = blockIdx.x;
@@ -151,9 +153,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
             ks[i] = to_f32<T>(kg[gi]);
             qs[i] = to_f32<T>(qg[gi]);
         }
-        for (int i = threadIdx.x; i < nt * P; i += nthr) {
-            const int tt = i / P, pp = i - tt * P;
-            vs[i] = to_f32<T>(vg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]);
+        for (int i = threadIdx.x; i < nt * Pp; i += nthr) {
+            const int tt = i / Pp, pp = i - tt * Pp;
+            vs[i] = pp < P ? to_f32<T>(vg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]) : 0.f;
         }
         for (int i = threadIdx.x; i < nt; i += nthr) {
             const size_t ci = (size_t)(b * L + t0 + i) * H + h;
@@ -176,11 +178,24 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
                 kt[c][0] = k4.x; kt[c][1] = k4.y; kt[c][2] = k4.z; kt[c][3] = k4.w;
                 qt[c][0] = q4.x; qt[c][1] = q4.y; qt[c][2] = q4.z; qt[c][3] = q4.w;
             }
-            float acc[RPW];
+            float acc[RPW], vr[RPW];   // this warp's RPW rows of v_t: 16- or 8-byte loads
+            if constexpr (RPW >= 4) {
+#pragma unroll
+                for (int u = 0; u < RPW / 4; ++u) {
+                    const float4 v4 = *reinterpret_cast<const float4 *>(vs + i * Pp + p0 + 4 * u);
+                    vr[4 * u] = v4.x;
+                    vr[4 * u + 1] = v4.y;
+                    vr[4 * u + 2] = v4.z;
+                    vr[4 * u + 3] = v4.w;
+                }
+            } else {
+                const float2 v2 = *reinterpret_cast<const float2 *>(vs + i * Pp + p0);
+                vr[0] = v2.x;
+                vr[1] = v2.y;
+            }
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
-                const int pr = p0 + r;
-                const float vt = pr < P ? vs[i * P + pr] : 0.f;
+                const float vt = vr[r];
                 const float bv = beta * vp[r], gv = gamma * vt;
                 float s = 0.f;
 #pragma unroll
@@ -207,7 +222,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
             const int pr = p0 + trap_row<RPW>(lane);
             if ((lane & (32 / RPW - 1)) == 0 && pr < P)
                 yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] =
-                    from_f32<T>(fmaf(p.D[h], vs[i * P + pr], acc[0]));
+                    from_f32<T>(fmaf(p.D[h], vs[i * Pp + pr], acc[0]));
         }
     }
 
@@ -361,14 +376,17 @@ int trap_warps(int P, int N)
     return (P + rpw - 1) / rpw;
 }
 
-// time steps per staged block: k, q (2N), v (P) and three coefficients per step
+// the staged v row stride: the rows of all of the CTA's warps
+int trap_pp(int P, int N) { return trap_warps(P, N) * (kStateFloat4PerLane / trap_nv(N)); }
+
+// time steps per staged block: k, q (2N), v (Pp) and three coefficients per step
 int trap_tblk(int P, int N)
 {
-    const size_t per_step = (size_t)(2 * N + P + 3) * sizeof(float);
+    const size_t per_step = (size_t)(2 * N + trap_pp(P, N) + 3) * sizeof(float);
     return (int)std::max<size_t>(1, std::min<size_t>(64, (48u * 1024u) / per_step));
 }
 
-size_t trap_smem(int P, int N, int tb) { return (size_t)tb * (2 * N + P + 3) * sizeof(float); }
+size_t trap_smem(int P, int N, int tb) { return (size_t)tb * (2 * N + trap_pp(P, N) + 3) * sizeof(float); }
 
 template <typename T, int NV>
 cudaError_t trap_launch_nv(const TrapParams &tp, long long grid, int threads, size_t smem, cudaStream_t st)
@@ -446,6 +464,7 @@ cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream)
     tp.N = a.dstate;
     tp.G = a.ngroups;
     tp.tblk = trap_tblk(a.headdim, a.dstate);
+    tp.Pp = trap_pp(a.headdim, a.dstate);
     const size_t smem = trap_smem(a.headdim, a.dstate, tp.tblk);
     const int threads = 32 * trap_warps(a.headdim, a.dstate);
     const long long grid = a.batch * (long long)a.nheads;
