@@ -80,6 +80,7 @@ KERNEL_SOURCES = {
     "ssd_chunk_fused_kernel": ("ssd_chunk.cu", "ptx.cuh", "tmap.h"),
     "ssd_decode_kernel": ("ssd_decode.cu",),
     "ssd_seq_kernel": ("ssd_seq.cu",),
+    "ssd_seq_rows_kernel": ("ssd_seq.cu", "warp_rows.cuh"),
     "ssd_trap_seq_kernel": ("ssd_trap.cu",),
     "ssd_trap_decode_kernel": ("ssd_trap.cu",),
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
@@ -93,6 +94,14 @@ KERNEL_SOURCES = {
 # fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
 # (the maximum SM clock), for kernels bound by plain fp32 arithmetic
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def seq_kernel_name(w: Workload) -> str:
+    """The sequential path's kernel for these sizes: the row layout where N % 4
+    == 0, N <= 512 and P fits 16 warps of 8 / NV rows, else the slice layout."""
+    nv = 1 if w.dstate <= 128 else (2 if w.dstate <= 256 else 4)
+    rows = w.dstate % 4 == 0 and 4 <= w.dstate <= 512 and w.headdim <= 16 * (8 // nv)
+    return "ssd_seq_rows_kernel" if rows else "ssd_seq_kernel"
 
 
 def bwd_chunk_flops(w: Workload) -> int:
@@ -311,7 +320,7 @@ def run_gpu(args, w: Workload):
     def step():
         ssd.ssd_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"],
                          d["init_state"], chunk=w.chunk, path=args.path, y=y, final_state=fin,
-                         stream=stream)
+                         stream=stream, schedule=args.schedule)
 
     for _ in range(args.warmup):
         step()
@@ -357,7 +366,7 @@ def run_gpu(args, w: Workload):
     def step_host():
         ssd.ssd_scan_fwd_host(pin["x"], pin["dt_raw"], pin["dt_bias"], pin["A_log"], pin["B"],
                               pin["C"], pin["D"], pin["init_state"], chunk=w.chunk, path=args.path,
-                              y=yh, final_state=fh, stream=stream)
+                              y=yh, final_state=fh, stream=stream, schedule=args.schedule)
 
     e2e_steps = max(1, min(args.steps, 5))
     step_host()
@@ -384,7 +393,7 @@ def run_gpu(args, w: Workload):
     t_hbm = alg_bytes / (hbm_peak * 1e9)
     t_tensor = alg_flops / (float(peaks["bf16_tflops"]) * 1e12)
     kernel = {ssd.PATH_CHUNKED: "ssd_chunk_fused_kernel", ssd.PATH_DECODE: "ssd_decode_kernel"}.get(
-        path, "ssd_seq_kernel")
+        path, seq_kernel_name(w))
     traffic = stored_traffic(w.name, kernel)
     clocks = clk.summary()
     line = {
@@ -405,7 +414,7 @@ def run_gpu(args, w: Workload):
                    "chunk": w.chunk, "init_state": w.init_state, "final_state": True,
                    "path": {ssd.PATH_CHUNKED: "chunked", ssd.PATH_DECODE: "decode"}.get(path, "sequential"),
                    "schedule": ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups,
-                                                  w.dstate, w.chunk, w.dtype),
+                                                  w.dstate, w.chunk, w.dtype, schedule=args.schedule),
                    "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
         "roofline": {
             "bound": "hbm" if t_hbm >= t_tensor else "tensor",
@@ -934,6 +943,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="libssd", choices=["libssd", "reference"])
     ap.add_argument("--path", default="auto", choices=["auto", "chunked", "sequential", "decode"])
+    ap.add_argument("--schedule", default="auto", choices=["auto", "ranges", "pieces", "split"],
+                    help="the chunked path's schedule (the forward scan workloads)")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

@@ -23,6 +23,7 @@
 #include <algorithm>
 
 #include "ssd_internal.h"
+#include "warp_rows.cuh"
 
 namespace ssd {
 namespace {
@@ -145,6 +146,188 @@ __global__ void __launch_bounds__(512) ssd_seq_kernel(SeqParams p)
     }
 }
 
+
+// ---- the row layout (N % 4 == 0, N <= 512): one CTA per (b, h), one warp per
+// block of RPW = 8 / NV state rows p, lane l holding n = 4l .. 4l+3 (+128 per
+// further float4) of each row, so the state is read and written as coalesced
+// 512-byte rows and stays in registers.  Per time block (up to 64 steps) the
+// CTA stages B_t, C_t, x_t, dt_t and dA_t in shared memory; each element
+// takes dA h + (dt x) B, the decode step's operations in its order (one decode
+// step equals one step of this scan bit for bit); y_t[p] is a warp butterfly.  The step loop is unrolled so that a step's readout reduction
+// overlaps the next steps' updates, and each warp reads its rows of x_t as
+// 16-byte (8-byte) words from a stride padded to the CTA's rows.
+constexpr int kRowF4PerLane = 8;   // RPW * NV float4 of state per lane
+constexpr int kRowMaxWarps = 16;
+
+struct RowParams {
+    SeqParams s;
+    int Pp;                         // staged x row stride (the CTA's rows)
+};
+
+template <typename T, int NV>
+__global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowParams rp)
+{
+    constexpr int RPW = kRowF4PerLane / NV;
+    const SeqParams &p = rp.s;
+    extern __shared__ float sm[];
+    const int P = p.P, N = p.N, H = p.H, TB = p.tblk, Pp = rp.Pp;
+    const long long L = p.L;
+    float *bs = sm;                  // [TB][N]: B_t
+    float *cs = bs + TB * N;         // [TB][N]: C_t
+    float *xs = cs + TB * N;         // [TB][Pp], zero past P
+    float *da = xs + TB * Pp;        // [TB]: dA_t
+    float *ds = da + TB;             // [TB]: dt_t
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
+    const long long bh = blockIdx.x;
+    const long long b = bh / H;
+    const int h = (int)(bh - b * H);
+    const int g = h / (H / p.G);
+    const int p0 = warp * RPW;
+    const T *xg = static_cast<const T *>(p.x), *Bg = static_cast<const T *>(p.B), *Cg = static_cast<const T *>(p.C);
+    T *yg = static_cast<T *>(p.y);
+    const size_t sbase = (size_t)bh * P * N;
+    const float A = -expf(p.A_log[h]), bias = p.dt_bias[h], Dh = p.D[h];
+
+    float4 hs[RPW][NV];
+#pragma unroll
+    for (int r = 0; r < RPW; ++r) {
+        const int pr = p0 + r;
+#pragma unroll
+        for (int c = 0; c < NV; ++c) {
+            const int n = 4 * lane + 128 * c;
+            hs[r][c] = (p.init_state && pr < P && n < N)
+                           ? __ldcs(reinterpret_cast<const float4 *>(p.init_state + sbase + (size_t)pr * N + n))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+
+    for (long long t0 = 0; t0 < L; t0 += TB) {
+        const int nt = (int)min((long long)TB, L - t0);
+        __syncthreads();   // the previous block is consumed
+        for (int i = threadIdx.x; i < nt; i += nthr) {
+            const float dt = softplus_f32(p.dt_raw[(size_t)(b * L + t0 + i) * H + h] + bias);
+            da[i] = expf(dt * A);
+            ds[i] = dt;
+        }
+        for (int i = threadIdx.x; i < nt * Pp; i += nthr) {
+            const int tt = i / Pp, pp = i - tt * Pp;
+            xs[i] = pp < P ? to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]) : 0.f;
+        }
+        __syncthreads();
+        for (int i = threadIdx.x; i < nt * N; i += nthr) {
+            const int tt = i / N, n = i - tt * N;
+            const size_t gi = ((size_t)(b * L + t0 + tt) * p.G + g) * N + n;
+            bs[i] = to_f32<T>(Bg[gi]);
+            cs[i] = to_f32<T>(Cg[gi]);
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int i = 0; i < nt; ++i) {
+            const float dA = da[i], dt = ds[i];
+            float4 bt[NV], ct[NV];
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const int n = 4 * lane + 128 * c;
+                const bool in = n < N;   // N % 4 == 0: whole float4 chunks
+                bt[c] = in ? *reinterpret_cast<const float4 *>(bs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                ct[c] = in ? *reinterpret_cast<const float4 *>(cs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+            float acc[RPW], xr[RPW];
+            if constexpr (RPW >= 4) {
+#pragma unroll
+                for (int v = 0; v < RPW / 4; ++v) {
+                    const float4 x4 = *reinterpret_cast<const float4 *>(xs + i * Pp + p0 + 4 * v);
+                    xr[4 * v] = x4.x;
+                    xr[4 * v + 1] = x4.y;
+                    xr[4 * v + 2] = x4.z;
+                    xr[4 * v + 3] = x4.w;
+                }
+            } else {
+                const float2 x2 = *reinterpret_cast<const float2 *>(xs + i * Pp + p0);
+                xr[0] = x2.x;
+                xr[1] = x2.y;
+            }
+#pragma unroll
+            for (int r = 0; r < RPW; ++r) {
+                const float dtx = dt * xr[r];
+                float s = 0.f;
+#pragma unroll
+                for (int c = 0; c < NV; ++c) {
+                    float4 &z = hs[r][c];
+                    z.x = fmaf(dA, z.x, dtx * bt[c].x);
+                    z.y = fmaf(dA, z.y, dtx * bt[c].y);
+                    z.z = fmaf(dA, z.z, dtx * bt[c].z);
+                    z.w = fmaf(dA, z.w, dtx * bt[c].w);
+                    s = fmaf(ct[c].x, z.x, s);
+                    s = fmaf(ct[c].y, z.y, s);
+                    s = fmaf(ct[c].z, z.z, s);
+                    s = fmaf(ct[c].w, z.w, s);
+                }
+                acc[r] = s;
+            }
+            warp_sum_rows_all<RPW>(acc, lane);
+            const int pr = p0 + summed_row<RPW>(lane);
+            if ((lane & (32 / RPW - 1)) == 0 && pr < P)
+                yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] = from_f32<T>(fmaf(Dh, xs[i * Pp + pr], acc[0]));
+        }
+    }
+
+    if (p.final_state) {
+#pragma unroll
+        for (int r = 0; r < RPW; ++r) {
+            const int pr = p0 + r;
+#pragma unroll
+            for (int c = 0; c < NV; ++c) {
+                const int n = 4 * lane + 128 * c;
+                if (pr < P && n < N)
+                    __stcs(reinterpret_cast<float4 *>(p.final_state + sbase + (size_t)pr * N + n), hs[r][c]);
+            }
+        }
+    }
+}
+
+int rows_nv(int N) { return N <= 128 ? 1 : N <= 256 ? 2 : 4; }
+
+bool rows_supported(int P, int N)
+{
+    if (N % 4 != 0 || N < 4 || N > 512 || P < 1)
+        return false;
+    return P <= kRowMaxWarps * (kRowF4PerLane / rows_nv(N));
+}
+
+template <typename T, int NV>
+cudaError_t rows_launch_t(const RowParams &rp, int grid, int threads, size_t smem, cudaStream_t st)
+{
+    auto kern = ssd_seq_rows_kernel<T, NV>;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    kern<<<grid, threads, smem, st>>>(rp);
+    return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rows_launch(const SeqParams &sp, int grid, cudaStream_t st)
+{
+    const int nv = rows_nv(sp.N), rpw = kRowF4PerLane / nv;
+    const int warps = (sp.P + rpw - 1) / rpw;
+    RowParams rp;
+    rp.s = sp;
+    rp.Pp = warps * rpw;
+    // steps per staged block: up to 64, within about 200 KB (B, C, x, dA and a dt slot per step)
+    const long long per_step = (long long)(2 * sp.N + rp.Pp + 2) * (long long)sizeof(float);
+    rp.s.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, sp.L, (200LL << 10) / per_step}));
+    const size_t smem = (size_t)rp.s.tblk * (size_t)per_step;
+    switch (nv) {
+    case 1: return rows_launch_t<T, 1>(rp, grid, 32 * warps, smem, st);
+    case 2: return rows_launch_t<T, 2>(rp, grid, 32 * warps, smem, st);
+    default: return rows_launch_t<T, 4>(rp, grid, 32 * warps, smem, st);
+    }
+}
+
 struct SeqShape {
     int slices, npt, tblk;
     size_t smem;
@@ -244,6 +427,13 @@ cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream)
     const long long grid = a.batch * (long long)a.nheads;
     if (grid > 0x7FFFFFFFLL)
         return cudaErrorInvalidValue;
+    if (rows_supported(a.headdim, a.dstate)) {   // the row layout where it applies
+        const cudaError_t e = a.dtype == SSD_DTYPE_BF16 ? rows_launch<__nv_bfloat16>(sp, (int)grid, stream)
+                                                        : rows_launch<float>(sp, (int)grid, stream);
+        if (e == cudaSuccess)
+            note_launches(1);
+        return e;
+    }
     const int threads = s.slices * a.headdim;
     cudaError_t e;
     if (a.dtype == SSD_DTYPE_BF16)
