@@ -76,8 +76,11 @@ def test_tiny_fp32_sequential(ssd):
     check(y, fin, *ref, "f32")
 
 
+# row-layout kernel: one, two and four float4 of state per lane, and 16 warps of
+# 8 rows; slice-layout kernel: N % 4 != 0, or P past the row layout's rows
 @pytest.mark.parametrize("shape", [(1, 1, 2, 8, 16, 1), (2, 37, 4, 8, 16, 2), (1, 200, 3, 5, 7, 1),
-                                   (2, 130, 4, 64, 128, 1), (1, 70, 2, 32, 256, 2)])
+                                   (2, 130, 4, 64, 128, 1), (1, 70, 2, 32, 256, 2), (1, 50, 2, 32, 512, 1),
+                                   (1, 40, 2, 128, 128, 1), (1, 30, 2, 200, 64, 1)])
 def test_sequential_fp32_shapes(ssd, shape):
     Bt, L, H, P, N, G = shape
     w = small(batch=Bt, seqlen=L, nheads=H, headdim=P, dstate=N, ngroups=G, chunk=16, dtype="f32")
