@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 
 #include "ssd_internal.h"
+#include "warp_rows.cuh"
 
 namespace ssd {
 namespace {
@@ -48,42 +49,6 @@ template <> __device__ __forceinline__ float to_f32<float>(float v) { return v; 
 template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 __device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
-
-// sums each of R (a power of two) values over the warp; afterwards vals[0] of
-// lane l holds the total of row bwd_row<R>(l) (each stage halves the rows held)
-template <int R>
-__device__ __forceinline__ void warp_sum_rows(float (&vals)[R], int lane)
-{
-    int cnt = R;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        if (cnt > 1) {
-            const int half = cnt >> 1;
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int j = 0; j < R / 2; ++j)
-                if (j < half) {
-                    const float send = upper ? vals[j] : vals[j + half];
-                    const float keep = upper ? vals[j + half] : vals[j];
-                    vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            cnt = half;
-        } else {
-            vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], o);
-        }
-    }
-}
-
-template <int R>
-__device__ __forceinline__ int bwd_row(int lane)
-{
-    int row = 0, half = R >> 1;
-#pragma unroll
-    for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
-        if (lane & o)
-            row += half;
-    return row;
-}
 
 __device__ __forceinline__ float warp_sum(float v)
 {
@@ -208,9 +173,9 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_bwd_kernel(BwdParams p)
 #pragma unroll
             for (int r = 0; r < kRows; ++r)
                 sx[r] = Gs[r].x * bv[0] + Gs[r].y * bv[1] + Gs[r].z * bv[2] + Gs[r].w * bv[3];
-            warp_sum_rows<kRows>(sx, lane);
+            warp_sum_rows_all<kRows>(sx, lane);
             {
-                const int rr = bwd_row<kRows>(lane);
+                const int rr = summed_row<kRows>(lane);
                 float dv = 0.f;
 #pragma unroll
                 for (int r = 0; r < kRows; ++r)

@@ -23,6 +23,7 @@
 #include <algorithm>
 
 #include "ssd_internal.h"
+#include "warp_rows.cuh"
 
 namespace ssd {
 namespace {
@@ -54,45 +55,6 @@ template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(flo
 // and a CTA has at most 16 warps (so at most 128 registers per thread)
 constexpr int kStateFloat4PerLane = 8;
 constexpr int kMaxWarps = 16;
-
-// Sums each of the R values over the warp's 32 lanes at once (R a power of two
-// <= 32): each butterfly stage exchanges half of the values still held, so R
-// rows take R - 1 + log2(32 / R) shuffles instead of 5 R.  Afterwards vals[0]
-// of lane l is the total of row trap_row<R>(l).
-template <int R>
-__device__ __forceinline__ void warp_sum_rows(float (&vals)[R], int lane)
-{
-    int cnt = R;
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        if (cnt > 1) {
-            const int half = cnt >> 1;
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int j = 0; j < R / 2; ++j) {
-                if (j < half) {
-                    const float send = upper ? vals[j] : vals[j + half];
-                    const float keep = upper ? vals[j + half] : vals[j];
-                    vals[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                }
-            }
-            cnt = half;
-        } else {
-            vals[0] += __shfl_xor_sync(0xffffffffu, vals[0], o);
-        }
-    }
-}
-
-template <int R>
-__device__ __forceinline__ int trap_row(int lane)
-{
-    int row = 0, half = R >> 1;
-#pragma unroll
-    for (int o = 16; o >= 1 && half >= 1; o >>= 1, half >>= 1)
-        if (lane & o)
-            row += half;
-    return row;
-}
 
 // NV: float4 chunks of a state row per lane (N <= 128 NV); RPW: rows per warp
 template <typename T, int NV>
@@ -218,8 +180,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_trap_seq_kernel(TrapParams
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     kp[c][e] = kt[c][e];
-            warp_sum_rows<RPW>(acc, lane);
-            const int pr = p0 + trap_row<RPW>(lane);
+            warp_sum_rows_all<RPW>(acc, lane);
+            const int pr = p0 + summed_row<RPW>(lane);
             if ((lane & (32 / RPW - 1)) == 0 && pr < P)
                 yg[((size_t)(b * L + t0 + i) * H + h) * P + pr] =
                     from_f32<T>(fmaf(p.D[h], vs[i * Pp + pr], acc[0]));
