@@ -916,6 +916,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // initial state)
                 // all 64 loads of the row are issued before the first use (one round trip)
                 const size_t slot_of = (size_t)unit_slot<kPieces>(cur, p);
+                if constexpr (!kPieces) {
+                    // The initial state of this CTA's next unit, when that unit starts its
+                    // chain, into L2 ahead of its loads (64 KB, contiguous for the head
+                    // pair).  Handoff slots are not prefetched: a chained predecessor may
+                    // still be running, and split pass 3 measured no gain.
+                    if (sw == 0 && lane == 0 && p.init_state && p.mode != kSplitLocal &&
+                        cur.u + (long long)gridDim.x < p.nunits) {
+                        const Unit w2 = decode_unit(cur.u + (int)gridDim.x, p);
+                        if (w2.flags & kFirst) {
+                            const float *nxt_state = p.init_state + ((size_t)w2.b * p.H + w2.h0) * (size_t)(kP * kN);
+                            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(nxt_state),
+                                         "r"((uint32_t)(2 * kP * kN * sizeof(float)))
+                                         : "memory");
+                        }
+                    }
+                }
                 uint32_t v[2][32];
                 if (!cur.first() && p.mode != kSplitLocal) {
                     const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
