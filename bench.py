@@ -368,7 +368,7 @@ def run_gpu(args, w: Workload):
                               pin["C"], pin["D"], pin["init_state"], chunk=w.chunk, path=args.path,
                               y=yh, final_state=fh, stream=stream, schedule=args.schedule)
 
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 20))
     step_host()
     if dist:
         dist.barrier()
@@ -597,7 +597,7 @@ def run_gpu_trap(args, w: Workload):
             hv.copy_(dv, non_blocking=True)
         torch.cuda.synchronize(dev)
 
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 20))
     step_e2e()
     if dist:
         dist.barrier()
@@ -845,7 +845,7 @@ def run_gpu_neighbor(args, w: Workload):
             back[n].copy_(t, non_blocking=True)
         torch.cuda.synchronize(dev)
 
-    e2e_steps = max(1, min(args.steps, 5))
+    e2e_steps = max(1, min(args.steps, 20))
     step_e2e()
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
