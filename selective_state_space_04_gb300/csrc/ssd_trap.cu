@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(kDecWarps * 32, NV == 1 ? 5 : 1) ssd_trap_deco
                 acc += __shfl_xor_sync(0xffffffffu, acc, o);
             if (lane == 0 && pr < P) {
                 yg[pr] = from_f32<T>(fmaf(Dh, vt[i], acc));
-                if (p.v_final)
-                    static_cast<T *>(p.v_final)[bh * P + pr] = vg[pr];
+                if (p.v_final)   // v_t from the register (exact: it was read as T)
+                    static_cast<T *>(p.v_final)[bh * P + pr] = from_f32<T>(vt[i]);
             }
         }
     }
