@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle.neighbors import conv1d_silu, gated_rmsnorm
-from selective_state_space_04_gb300.inputs import Workload, make_conv_inputs, make_gnorm_inputs
+from selective_state_space_04_gb300.inputs import WORKLOADS, Workload, make_conv_inputs, make_gnorm_inputs
 
 pytestmark = pytest.mark.gpu
 
@@ -101,3 +101,25 @@ def test_conv_scan_norm_chain(ssd):
     ry, _ = oracle.ssd_fwd(x.cpu(), dt_raw, dt_bias, A_log, Bm.cpu(), Cm.cpu(), D)
     ref = gated_rmsnorm(torch.from_numpy(ry).to(torch.bfloat16), gi["z"], gi["weight"], eps=1e-6)
     assert relerr(out, ref) <= TOL["bf16"]
+
+
+def test_bench_workloads_sampled(ssd):
+    # the bench's full conv and norm workloads in one call each; the oracle takes
+    # the first two batch rows (rows and tokens run independently)
+    w = WORKLOADS["conv_silu_2p7b"]
+    inp = make_conv_inputs(w, K=4, seed=0)
+    d = _dev(inp)
+    x, Bm, Cm, st = ssd.conv1d_silu_fwd(d["xbc"], d["weight"], d["bias"], d["conv_state"], nheads=w.nheads,
+                                        headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate)
+    torch.cuda.synchronize()
+    sub = dict(inp, xbc=inp["xbc"][:2], conv_state=None if inp["conv_state"] is None else inp["conv_state"][:2])
+    rx, rB, rC, rs = conv1d_silu(**sub, H=w.nheads, P=w.headdim, G=w.ngroups, N=w.dstate)
+    for got, ref in ((x, rx), (Bm, rB), (Cm, rC)):
+        assert relerr(got[:2], ref) <= TOL["bf16"]
+    assert np.array_equal(st[:2].double().cpu().numpy(), rs)
+    w = WORKLOADS["gnorm_2p7b"]
+    gi = make_gnorm_inputs(w, seed=0)
+    out = ssd.gated_rmsnorm_fwd(gi["y"].cuda(), gi["z"].cuda(), gi["weight"].cuda(), 1e-6)
+    torch.cuda.synchronize()
+    ref = gated_rmsnorm(gi["y"][:2], gi["z"][:2], gi["weight"], eps=1e-6)
+    assert relerr(out[:2], ref) <= TOL["bf16"]

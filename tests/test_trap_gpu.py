@@ -191,3 +191,17 @@ def test_trap_one_step_against_oracle(ssd, B, H, P, N, G, dtype, init):
     y, h, k, v = _run(ssd, _dev(inp))
     assert relerr(y, ry) <= TOL[dtype] and relerr(h, rh) <= TOL[dtype]
     assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
+
+
+@pytest.mark.parametrize("name,rows", [("trap_many_short_seqs", 6), ("trap_decode_2p7b_128seq", 128)])
+def test_bench_workloads_sampled(ssd, name, rows):
+    # the bench's full workload in one call on the auto path (as the bench runs it);
+    # the oracle takes the first `rows` batch rows (every batch row runs independently)
+    w = WORKLOADS[name]
+    inp = make_trap_inputs(w, seed=0)
+    y, h, kf, vf = _run(ssd, _dev(inp), path="auto")
+    sub = {k: (None if v is None else v[:rows]) if k not in ("D",) else v for k, v in inp.items()}
+    ry, rh, rk, rv = trap_fwd(**sub)
+    for got, ref in ((y, ry), (h, rh)):
+        assert relerr(got[:rows], ref) <= TOL[w.dtype]
+    assert relerr(kf[:rows], rk) <= TOL[w.dtype] and relerr(vf[:rows], rv) <= TOL[w.dtype]
