@@ -510,6 +510,8 @@ __device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, co
 }
 
 // kPieces: the piece schedule (else the range schedule, or a split pass).
+// kLocal: split pass 1, which computes every unit's end state from zero and
+//   nothing else (no C loads, no M, no Y MMAs, no y); only the state MMA runs.
 // kTrap: the trapezoidal (Mamba-3 SISO) recurrence
 //   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
 // (alpha = exp(a dt), beta = alpha dt (1 - trap), gamma = trap dt) evaluated as
@@ -517,7 +519,7 @@ __device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, co
 // decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
 // alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
 // (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
-template <bool kPieces, bool kTrap>
+template <bool kPieces, bool kTrap, bool kLocal>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
@@ -593,9 +595,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 uint8_t *bc = smem + kOffBC + s * kBCStageBytes;
                 const int gc = (cur.w.h0 / p.hpg) * kN;
-                mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], kBCStageBytes);
-                tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
-                tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
+                // split pass 1 computes end states only: it needs B and x, not C
+                constexpr bool with_c = !kLocal;
+                mbar_arrive_expect_tx(&bars[BAR_BC_FULL + s], with_c ? kBCStageBytes : 2 * kTileBytes);
+                if (with_c) {
+                    tma_load_3d(bc, &maps.C, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
+                    tma_load_3d(bc + kTileBytes, &maps.C, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
+                }
                 tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
                 last_bc[s] = (int)j;
@@ -625,15 +631,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------------ MMA
-        // order per sub-chunk j:  Y_diag(j), Y_off(j), S(j+1), state(j)
+        // order per sub-chunk j:  Y_diag(j), Y_off(j), S(j+1), state(j).  Split pass 1
+        // issues the state MMA alone; the other commits still arrive, so every role
+        // keeps its hand-offs
         if (lane == 0) {
+            constexpr bool with_y = !kLocal;
             const uint32_t id_S = idesc_bf16_f32(128, 128, 0, 0);      // C (K-major) x B (K-major)
             const uint32_t id_Yd = idesc_bf16_f32(128, 64, 0, 1);      // M (TMEM) x x (MN-major)
             const uint32_t id_Yoff = idesc_bf16_f32(128, 128, 0, 1);   // C (K-major) x P (MN-major)
             const uint32_t id_St = idesc_bf16_f32(128, 128, 1, 1);     // B^T (MN-major) x wx (MN-major)
             auto issue_S = [&](int stage) {
                 const uint32_t bc = smem_u32(smem + kOffBC + stage * kBCStageBytes);
-                for (int kk = 0; kk < 8; ++kk) {
+                for (int kk = 0; with_y && kk < 8; ++kk) {
                     const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
                     mma_ss(tmem + kColSM, sdesc_sw128(bc + ko, 16, 1024),
                            sdesc_sw128(bc + 2 * kTileBytes + ko, 16, 1024), id_S, kk > 0);
@@ -665,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p))))
                     break;
                 tc_fence_after();
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; with_y && h < 2; ++h)
                     for (int kk = 0; kk < 8; ++kk)
                         mma_ts(tmem + kColYd + 64 * h, tmem + kColSM + 16 * kk + 8 * h,
                                sdesc_sw128(xs + h * kTileBytes + kk * 2048, kTileBytes, 1024), id_Yd, kk > 0);
@@ -679,7 +688,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t spins = 0;
                     while (!(yo_done && s_done)) {
                         bool progressed = false;
-                        if (!s_done && mbar_poll(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1) &&
+                        // (split pass 1 has no S, so no wait for the next B/C tile here: the
+                        // state MMA waits for its own tile instead, and two loads stay in flight)
+                        if (!s_done &&
+                            (!with_y || mbar_poll(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1)) &&
                             mbar_poll(&bars[BAR_YD_DONE], par)) {
                             tc_fence_after();
                             issue_S(s ^ 1);
@@ -687,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (!yo_done && mbar_poll(&bars[BAR_PB_READY], par)) {
                             tc_fence_after();
-                            for (int kk = 0; kk < 8; ++kk) {
+                            for (int kk = 0; with_y && kk < 8; ++kk) {
                                 const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
                                 mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024),
                                        sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
@@ -715,7 +727,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                 }
                 // P += B^T (w o x)   (P already rescaled by the state group)
-                if (!(ok = wait_bar(&bars[BAR_XS_READY], par, p)))
+                if (!(ok = wait_bar(&bars[BAR_XS_READY], par, p)) ||
+                    (!with_y && !(ok = wait_bar(&bars[BAR_BC_FULL + s], (j >> 1) & 1, p))))
                     break;
                 tc_fence_after();
                 for (int kk = 0; kk < 8; ++kk)
@@ -819,7 +832,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!wait_bar(&bars[BAR_S_DONE], j & 1, p))
                 break;
             tc_fence_after();
-            {
+            if constexpr (!kLocal) {   // split pass 1 has no y, so no M
                 const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
                 const float ct0 = cs2[r], ct1 = cs2[kT + r];
                 const float dc0 = kTrap ? dk[10 * kT + 4 + r] : 0.f, dc1 = kTrap ? dk[11 * kT + 4 + r] : 0.f;
@@ -982,6 +995,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- x <- w o x in place (row r, head hf); P <- dtot P
             if (!(ok = wait_bar(&bars[BAR_M_READY], par, p)) || !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
                 break;
+            // split pass 1 issues no Y_diag MMA to read x first: wait for its load here
+            if (kLocal && !(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)))
+                break;
             tc_fence_after();
             const float *dk = decay_base + (j % 3) * kDecayFloats;
             const float ecs = dk[6 * kT + hf * kT + r];
@@ -1024,7 +1040,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = wait_bar(&bars[BAR_YOFF_DONE], par, p)))
                 break;
             tc_fence_after();
-            {
+            if constexpr (!kLocal) {
                 uint8_t *stg = smem + kOffBC + s * kBCStageBytes + sw * 4096;   // this warp's 32 rows
                 for (int half = 0; half < 2; ++half) {
                     uint32_t yd[32], yo[32];
@@ -1050,10 +1066,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
-                if (lane == 0 && 32 * q < cur.valid() && p.mode != kSplitLocal) {
+                if (lane == 0 && 32 * q < cur.valid()) {
                     tma_store_3d(&maps.y, stg, hh * kP, (int)cur.t0() + 32 * q, cur.w.b);
                     bulk_commit_group();
                 }
+            } else {
+                // split pass 1 has no y: only the hand-off of the TMEM columns
+                tc_fence_before();
+                warp_arrive(&bars[BAR_EPI_DONE]);
             }
             // ---- carried state after sub-chunk j
             if (!(ok = wait_bar(&bars[BAR_STATE_DONE], par, p)))
@@ -1104,7 +1124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 // bf16 copy of P for the next sub-chunk's C P, in this sub-chunk's x stage
                 uint8_t *pb = smem + kOffX + s * kXStageBytes + hf * kTileBytes;
-                for (int half = 0; half < 2; ++half) {
+                for (int half = 0; half < 2 && !kLocal; ++half) {   // pass 1: no C P
                     uint32_t v[32];
                     tmem_ld32(ta + 32 * half, v);
                     tmem_wait_ld();
@@ -1158,13 +1178,32 @@ __global__ void __launch_bounds__(256) ssd_split_combine_kernel(float *slots, co
     }
     float4 *sl = reinterpret_cast<float4 *>(slots);
     float4 S = __ldcg(sl + (size_t)chain * kPerChain + e);   // unit (range 0, chain)
-    for (int k = 0; k + 1 < nranges; ++k) {
-        const size_t u = (size_t)k * nchains + chain;
-        const float lam = unit_decay[u * 2 + hf];
-        E = make_float4(fmaf(lam, E.x, S.x), fmaf(lam, E.y, S.y), fmaf(lam, E.z, S.z), fmaf(lam, E.w, S.w));
-        float4 *dst = sl + (u + nchains) * kPerChain + e;
-        S = __ldcg(dst);   // the next unit's own end state, before it is replaced
-        __stcg(dst, E);
+    // The end states and decays of the next kBatch units are all loaded before the
+    // first of them is replaced, so the chain of ranges costs one memory round trip
+    // per batch rather than one per range.
+    constexpr int kBatch = 8;
+    for (int k0 = 0; k0 + 1 < nranges; k0 += kBatch) {
+        float4 nx[kBatch];
+        float lam[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int k = k0 + i;
+            if (k + 1 < nranges) {
+                const size_t u = (size_t)k * nchains + chain;
+                lam[i] = __ldcg(unit_decay + u * 2 + hf);
+                nx[i] = __ldcg(sl + (u + nchains) * kPerChain + e);   // the next unit's own end state
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int k = k0 + i;
+            if (k + 1 < nranges) {
+                const float l = lam[i];
+                E = make_float4(fmaf(l, E.x, S.x), fmaf(l, E.y, S.y), fmaf(l, E.z, S.z), fmaf(l, E.w, S.w));
+                __stcg(sl + ((size_t)(k + 1) * nchains + chain) * kPerChain + e, E);
+                S = nx[i];
+            }
+        }
     }
 }
 
@@ -1226,11 +1265,12 @@ double chained_estimate(long long R, long long nchunks, long long nchains, int Q
     return std::max(rounds * unit_time, ranges * unit_time);
 }
 
-// Estimated time of the split schedule: two passes over independent units
-// (no handoff wait, about half a sub-chunk to refill the pipeline per unit)
-// plus the combine, which streams every unit's state (64 KB) in and out
-// (about 40 ns per unit and chain at HBM speed, in sub-chunk times of about 3 us)
-// and two more launches.
+// Estimated time of the split schedule: two passes over independent units (no
+// handoff wait, about half a sub-chunk to refill the pipeline per unit), of which
+// pass 1 (end states only: B and x loads and the state MMA) measured about half
+// as long as pass 3; then the combine, whose batched loads stream every unit's
+// state (64 KB) in and out at about 2 ns per unit (in sub-chunk times of about
+// 3 us), and about one sub-chunk for the two extra launches.
 double split_estimate(long long R, long long nchunks, long long nchains, int Q, long long grid)
 {
     const double subs_per_chunk = (double)Q / kT;
@@ -1238,8 +1278,8 @@ double split_estimate(long long R, long long nchunks, long long nchains, int Q, 
     const long long units = ranges * nchains;
     const long long rounds = (units + grid - 1) / grid;
     const double pass = rounds * (R * subs_per_chunk + 0.5);
-    const double combine = units * 0.04 / 3.0 + 2.0;
-    return 2.0 * pass + combine;
+    const double combine = units * 0.002 + 1.0;
+    return 1.5 * pass + combine;
 }
 
 void layout(Geometry &g, long long grid_p, int sms);
@@ -1398,10 +1438,16 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.nchains = (int)geo.nchains;
     p.hpg = a.nheads / a.ngroups;
 
-    auto kernel = a.trap ? (geo.pieces ? ssd_chunk_fused_kernel<true, true> : ssd_chunk_fused_kernel<false, true>)
-                         : (geo.pieces ? ssd_chunk_fused_kernel<true, false> : ssd_chunk_fused_kernel<false, false>);
+    auto kernel = a.trap ? (geo.pieces ? ssd_chunk_fused_kernel<true, true, false>
+                                       : ssd_chunk_fused_kernel<false, true, false>)
+                         : (geo.pieces ? ssd_chunk_fused_kernel<true, false, false>
+                                       : ssd_chunk_fused_kernel<false, false, false>);
+    auto kernel_local = ssd_chunk_fused_kernel<false, false, true>;   // split pass 1
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    if (geo.split && cudaFuncSetAttribute(kernel_local, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                          (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)geo.grid);
@@ -1422,7 +1468,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     // split: pass 1 (end state of every unit from zero), combine (entering state of
     // every unit), pass 3 (the scan itself, all units independent)
     p.mode = kSplitLocal;
-    if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, kernel_local, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     const long long threads = geo.nchains * 2 * 16 * kN;

@@ -36,7 +36,10 @@ def test_stalled_handoff_times_out_and_context_survives(ssd):
     args = (d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"], d["init_state"])
     assert ssd.device_error() == 0
     t0 = time.perf_counter()
-    ssd.ssd_scan_fwd(*args, chunk=w.chunk, path="chunked", diag_stall_handoff=True)
+    # the stalled wait is a chained hand-off between units: the ranges schedule
+    assert ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups, w.dstate, w.chunk,
+                              schedule="ranges") == "ranges"
+    ssd.ssd_scan_fwd(*args, chunk=w.chunk, path="chunked", diag_stall_handoff=True, schedule="ranges")
     code = ssd.device_error()          # synchronises the stream, reads and clears the word
     elapsed = time.perf_counter() - t0
     assert code == TIMEOUT
