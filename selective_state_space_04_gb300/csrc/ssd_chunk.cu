@@ -605,8 +605,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(bc + 2 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc, t0, cur.w.b, pol_keep);
                 tma_load_3d(bc + 3 * kTileBytes, &maps.B, &bars[BAR_BC_FULL + s], gc + 64, t0, cur.w.b, pol_keep);
                 last_bc[s] = (int)j;
-                if (j >= 1 && !(ok = wait_bar(&bars[BAR_X_EMPTY + s], ((j - 1) >> 1) & 1, p)))
-                    break;
+                // the x stage is free once Y_off(j-1) has read the bf16 P staged in it; in
+                // split pass 1 (no P there) once the state MMA of sub-chunk j-2 has read it
+                if constexpr (kLocal) {
+                    if (j >= 2 && !(ok = wait_bar(&bars[BAR_X_EMPTY + s], ((j >> 1) + 1) & 1, p)))
+                        break;
+                } else {
+                    if (j >= 1 && !(ok = wait_bar(&bars[BAR_X_EMPTY + s], ((j - 1) >> 1) & 1, p)))
+                        break;
+                }
                 uint8_t *xs = smem + kOffX + s * kXStageBytes;
                 mbar_arrive_expect_tx(&bars[BAR_X_FULL + s], kXStageBytes);
                 tma_load_3d(xs, &maps.x, &bars[BAR_X_FULL + s], cur.w.h0 * kP, t0, cur.w.b, pol_stream);
@@ -705,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                                        sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
                             }
                             mma_commit(&bars[BAR_YOFF_DONE]);
-                            mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
+                            if constexpr (!kLocal)
+                                mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
                             yo_done = progressed = true;
                         }
                         if (!progressed) {
@@ -736,6 +744,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                            sdesc_sw128(xs + kk * 2048, kTileBytes, 1024), id_St, 1);
                 mma_commit(&bars[BAR_STATE_DONE]);
                 mma_commit(&bars[BAR_BC_EMPTY + s]);
+                if constexpr (kLocal)
+                    mma_commit(&bars[BAR_X_EMPTY + s]);   // (split pass 1: see the producer)
                 cur = nxt;
                 has = has_next;
                 ++j;
@@ -983,9 +993,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int half = 0; half < 2; ++half) {
                     tmem_st32(ta + 32 * half, v[half]);
+                    if constexpr (!kLocal) {   // (split pass 1 has no C P; x(j+1) may be landing there)
 #pragma unroll
-                    for (int c8 = 0; c8 < 4; ++c8)
-                        *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v[half] + 8 * c8);
+                        for (int c8 = 0; c8 < 4; ++c8)
+                            *reinterpret_cast<uint4 *>(pb + sw128(r, 4 * half + c8)) = pack8(v[half] + 8 * c8);
+                    }
                 }
                 tmem_wait_st();
                 fence_proxy_async_smem();
