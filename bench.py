@@ -152,8 +152,59 @@ def stored_traffic(workload: str, kernel: str):
 
 
 # ------------------------------------------------------------ clocks
+# NVML clock-event reason bits (nvml.h, nvmlClocksEventReason*)
+_NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+
+class _Nvml:
+    """Read-only NVML queries through the driver's libnvidia-ml (ctypes; no
+    Python package needed).  Nothing here changes a setting of the GPU."""
+
+    def __init__(self, torch_index: int):
+        import ctypes
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.h = ctypes.c_void_p()
+        bus = None
+        try:
+            pr = torch.cuda.get_device_properties(torch_index)
+            bus = "%08x:%02x:%02x.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        except (AttributeError, RuntimeError):
+            bus = None
+        ok = bus is not None and self.lib.nvmlDeviceGetHandleByPciBusId_v2(
+            bus.encode(), ctypes.byref(self.h)) == 0
+        if not ok and self.lib.nvmlDeviceGetHandleByIndex_v2(torch_index, ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        self.reasons_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+
+    def max_sm(self):
+        v = self.ct.c_uint()
+        return float(v.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, self.ct.byref(v)) == 0 else None
+
+    def sample(self):
+        mhz, rs = self.ct.c_uint(), self.ct.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, self.ct.byref(mhz)) != 0:   # NVML_CLOCK_SM
+            return None
+        self.reasons_fn(self.h, self.ct.byref(rs))
+        return float(mhz.value), int(rs.value)
+
+    def power_w(self):
+        mw = self.ct.c_uint()
+        return mw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.h, self.ct.byref(mw)) == 0 else None
+
+    def close(self):
+        self.lib.nvmlShutdown()
+
+
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons while running."""
+    """Samples the SM clock and the clock-event (throttle) reasons while the
+    timed region runs.  Through NVML every 0.2 ms when the driver's library
+    loads (so that a timed region of a few milliseconds still gets samples),
+    else through an nvidia-smi loop every 50 ms."""
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -163,35 +214,72 @@ class ClockSampler:
         self.index = index
         self.proc = None
         self.lines = []
+        self.samples = []       # (sm MHz, power W, reason bits) from NVML
         self.thread = None
+        self.nvml = None
+        self.stop = threading.Event()
+        self.source = None
 
     def __enter__(self):
+        try:
+            self.nvml = _Nvml(self.index)
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+            return self
+        except (OSError, AttributeError):
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
                  "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except OSError:
             self.proc = None
         return self
 
+    def _poll(self):
+        while True:
+            v = self.nvml.sample()
+            if v is not None:
+                self.samples.append(v)
+            if self.stop.is_set():
+                break
+            time.sleep(0.0002)
+        self.power = self.nvml.power_w()
+
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
     def __exit__(self, *exc):
+        self.stop.set()
         if self.proc:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
-            if self.thread:
-                self.thread.join(timeout=2)
+        if self.thread:
+            self.thread.join(timeout=2)
 
     def summary(self):
+        if self.nvml is not None:
+            mx = self.nvml.max_sm()
+            self.nvml.close()
+            reasons = set()
+            for _, bits in self.samples:
+                for bit, name in _NVML_REASONS.items():
+                    if bits & bit:
+                        reasons.add(name)
+            sm = [v[0] for v in self.samples]
+            return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                    "reasons": sorted(reasons), "samples": len(sm),
+                    "power_w_end": getattr(self, "power", None),
+                    "source": "nvml: SM clock and clock-event reasons polled through the timed region"}
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in self.lines:
@@ -207,9 +295,71 @@ class ClockSampler:
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0, "source": self.source}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi, every 50 ms"}
+
+
+# ------------------------------------------------------------ config and L2
+L2_BYTES = 129 * 2**20          # GB300 L2
+FLUSH_BYTES = 256 * 2**20       # a write this large leaves none of a step's inputs in L2
+
+
+def flushes_l2(step_bytes: int) -> bool:
+    """Whether timed steps that move `step_bytes` (their algorithmic bytes) are
+    separated by an L2 flush: when those bytes do not exceed twice the L2, the
+    next step would otherwise find much of its input still there."""
+    return step_bytes <= 2 * L2_BYTES
+
+
+def workload_config(w: Workload, seed: int, flush: bool) -> dict:
+    """The `config` object of a bench line: the workload, identical for the
+    libssd arm and the reference arm (the run's own choices, such as the
+    kernel path, go elsewhere in the line)."""
+    c = {"workload": w.name}
+    if w.op != "ssd":
+        c["op"] = w.op
+    c.update({"batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads, "headdim": w.headdim,
+              "dstate": w.dstate, "ngroups": w.ngroups, "chunk": w.chunk, "dtype": w.dtype,
+              "init_state": w.init_state, "final_state": True,
+              "l2": ("flushed between timed steps (a 256 MB write outside the step's events)"
+                     if flush else "inputs larger than L2 (no flush)"),
+              "seed": seed})
+    return c
+
+
+def timed_region(ssd, step, steps, stream, dev, dist, local, flush):
+    """K steps between a barrier and a synchronize on both sides, each step
+    bracketed by CUDA events on the launching stream, with the clocks sampled
+    throughout.  With `flush`, a 256 MB write between steps (outside their
+    events) evicts the workload from L2, and the region's time is the sum of
+    the steps' own times.  Returns (max-over-ranks total ms, per-step ms,
+    clock summary, library launches)."""
+    scrub = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev) if flush else None
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    launches0 = ssd.launch_count()
+    with ClockSampler(local) as clk:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(steps):
+            if flush:
+                scrub.fill_(float(i))
+            evs[i][0].record(stream)
+            step()
+            evs[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        if dist:
+            dist.barrier()
+    launches = ssd.launch_count() - launches0
+    per = [a.elapsed_time(b) for a, b in evs]
+    total = sum(per) if flush else t_start.elapsed_time(t_end)
+    return max_over_ranks(dist, total, dev), per, clk.summary(), launches
 
 
 # ------------------------------------------------------------ distributed
@@ -328,31 +478,26 @@ def run_gpu(args, w: Workload):
     if ssd.device_error() != 0:
         raise SystemExit("device error during warm-up")
 
-    # timed region: K back-to-back steps, per-step CUDA events on the launching stream
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    launches0 = ssd.launch_count()
-    with ClockSampler(local) as clk:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-    launches = ssd.launch_count() - launches0
+    # timed region: K steps, per-step CUDA events on the launching stream; a
+    # workload that L2 could hold gets an L2 flush between steps, outside the
+    # step's events, and its time is the sum of the steps' own times
+    flush = flushes_l2(algorithmic_bytes(w))
+    total_ms, per_launch_ms, clocks, launches = timed_region(ssd, step, args.steps, stream, dev, dist,
+                                                             local, flush)
     if ssd.device_error() != 0:
         raise SystemExit("device error during the timed region")
-    total_ms = t_start.elapsed_time(t_end)
-    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
-    total_ms = max_over_ranks(dist, total_ms, dev)
+    warm = None
+    if flush:
+        # the same steps back to back with no flush (the workload stays in L2)
+        ws, we = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ws.record(stream)
+        for _ in range(args.steps):
+            step()
+        we.record(stream)
+        torch.cuda.synchronize(dev)
+        wms = ws.elapsed_time(we) / args.steps
+        warm = {"value": w.token_heads / (wms / 1e3), "ms_per_step": wms,
+                "note": "L2-warm: the same steps back to back, no flush"}
     ms_per_step = total_ms / args.steps
     th = w.token_heads
     value = world * th * args.steps / (total_ms / 1e3)
@@ -395,7 +540,6 @@ def run_gpu(args, w: Workload):
     kernel = {ssd.PATH_CHUNKED: "ssd_chunk_fused_kernel", ssd.PATH_DECODE: "ssd_decode_kernel"}.get(
         path, seq_kernel_name(w))
     traffic = stored_traffic(w.name, kernel)
-    clocks = clk.summary()
     line = {
         "metric": METRIC,
         "value": value,
@@ -409,13 +553,11 @@ def run_gpu(args, w: Workload):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "chunk": w.chunk, "init_state": w.init_state, "final_state": True,
-                   "path": {ssd.PATH_CHUNKED: "chunked", ssd.PATH_DECODE: "decode"}.get(path, "sequential"),
-                   "schedule": ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups,
-                                                  w.dstate, w.chunk, w.dtype, schedule=args.schedule),
-                   "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "config": workload_config(w, args.seed, flush),
+        "run": {"path": {ssd.PATH_CHUNKED: "chunked", ssd.PATH_DECODE: "decode"}.get(path, "sequential"),
+                "schedule": ssd.chunk_schedule((w.batch, w.seqlen, w.nheads, w.headdim), w.ngroups,
+                                               w.dstate, w.chunk, w.dtype, schedule=args.schedule),
+                "launches_per_step": int(launches) // max(1, args.steps)},
         "roofline": {
             "bound": "hbm" if t_hbm >= t_tensor else "tensor",
             "kernel": kernel,
@@ -437,6 +579,8 @@ def run_gpu(args, w: Workload):
         "gpu_launches": int(launches),
         "clocks": clocks,
     }
+    if warm is not None:
+        line["warm_l2"] = warm
     if not args.no_cpu_baseline and world == 1:
         shape = size_oracle_sample(w, inp, 10.0)
         v, cores, sample = cpu_oracle_sample(w, inp, shape, min_seconds=10.0)
@@ -480,9 +624,7 @@ def run_reference(args, w: Workload):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": w.name, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "chunk": w.chunk, "init_state": w.init_state, "seed": args.seed},
+        "config": workload_config(w, args.seed, flushes_l2(algorithmic_bytes(w))),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": "per step: " + sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -554,29 +696,11 @@ def run_gpu_trap(args, w: Workload):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    launches0 = ssd.launch_count()
-    with ClockSampler(local) as clk:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            evs[i][0].record(stream)
-            step()
-            evs[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-    launches = ssd.launch_count() - launches0
+    flush = flushes_l2(trap_algorithmic_bytes(w))
+    total_ms, per_launch_ms, clocks, launches = timed_region(ssd, step, args.steps, stream, dev, dist,
+                                                             local, flush)
     # the chunked kernel in its trapezoidal mode takes one more launch (the carried k, v)
     chunked = launches == 2 * args.steps
-    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
-    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
     th = w.token_heads
     value = world * th * args.steps / (total_ms / 1e3)
 
@@ -621,10 +745,8 @@ def run_gpu_trap(args, w: Workload):
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "op": "trap", "batch": w.batch, "seqlen": w.seqlen,
-                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "init_state": w.init_state, "path": "chunked" if chunked else "sequential",
-                   "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "config": workload_config(w, args.seed, flush),
+        "run": {"path": "chunked" if chunked else "sequential"},
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,
@@ -636,7 +758,7 @@ def run_gpu_trap(args, w: Workload):
                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                 "api": "ssd_trap_scan_fwd with pinned host copies in and out"},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
         nb = trap_sample_rows(w, inp, 10.0)
@@ -667,9 +789,7 @@ def run_reference_trap(args, w: Workload):
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "op": "trap", "batch": w.batch, "seqlen": w.seqlen,
-                   "nheads": w.nheads, "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "init_state": w.init_state, "seed": args.seed},
+        "config": workload_config(w, args.seed, flushes_l2(trap_algorithmic_bytes(w))),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "per step: " + sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -809,27 +929,9 @@ def run_gpu_neighbor(args, w: Workload):
     for _ in range(args.warmup):
         step(stream)
     torch.cuda.synchronize(dev)
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(args.steps)]
-    launches0 = ssd.launch_count()
-    with ClockSampler(local) as clk:
-        if dist:
-            dist.barrier()
-        torch.cuda.synchronize(dev)
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            evs[i][0].record(stream)
-            step(stream)
-            evs[i][1].record(stream)
-        t_end.record(stream)
-        torch.cuda.synchronize(dev)
-        if dist:
-            dist.barrier()
-    launches = ssd.launch_count() - launches0
-    total_ms = max_over_ranks(dist, t_start.elapsed_time(t_end), dev)
-    per_launch_ms = [a.elapsed_time(b) for a, b in evs]
+    flush = flushes_l2(alg_bytes)
+    total_ms, per_launch_ms, clocks, launches = timed_region(ssd, lambda: step(stream), args.steps, stream,
+                                                             dev, dist, local, flush)
     th = w.token_heads
     value = world * th * args.steps / (total_ms / 1e3)
     # end to end: pinned host copies of the inputs in and of the outputs back, every step
@@ -889,16 +991,14 @@ def run_gpu_neighbor(args, w: Workload):
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": {"workload": w.name, "op": w.op, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups,
-                   "init_state": w.init_state, "l2": "inputs larger than L2 (no flush)", "seed": args.seed},
+        "config": workload_config(w, args.seed, flush),
         "roofline": roof,
         "e2e": {"value": world * th * e2e_steps / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in pin.values() if t is not None),
                 "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in back.values()),
                 "steps": e2e_steps, "api": "the public call with pinned host copies in and out"},
         "gpu_launches": launches,
-        "clocks": clk.summary(),
+        "clocks": clocks,
     }
     if not args.no_cpu_baseline and world == 1:
         v, sample = neighbor_oracle_rate(w, ref, 10.0, min_seconds=10.0)
@@ -910,7 +1010,7 @@ def run_reference_neighbor(args, w: Workload):
     world, rank, _ = dist_env()
     if rank != 0:
         return
-    _, _, _, _, _, _, ref = neighbor_setup(w, torch.device("cpu"), args.seed)
+    _, _, _, _, nbytes, _, ref = neighbor_setup(w, torch.device("cpu"), args.seed)
     per_step = min(10.0, max(0.02, 120.0 / (args.steps + args.warmup)))
     for _ in range(args.warmup):
         neighbor_oracle_rate(w, ref, per_step)
@@ -927,8 +1027,7 @@ def run_reference_neighbor(args, w: Workload):
         "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "op": w.op, "batch": w.batch, "seqlen": w.seqlen, "nheads": w.nheads,
-                   "headdim": w.headdim, "dstate": w.dstate, "ngroups": w.ngroups, "seed": args.seed},
+        "config": workload_config(w, args.seed, flushes_l2(nbytes)),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "per step: " + sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

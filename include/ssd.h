@@ -38,7 +38,7 @@
 extern "C" {
 #endif
 
-#define SSD_ABI_VERSION 1
+#define SSD_ABI_VERSION 2
 
 typedef enum ssd_dtype {
     SSD_DTYPE_F32 = 0,   /* x, B, C, y are fp32 */
@@ -50,12 +50,15 @@ typedef enum ssd_status {
     SSD_ERR_INVALID_DIMS = 1,   /* a size is negative/zero where it may not be, H % G != 0, overflow */
     SSD_ERR_NULL_PTR = 2,       /* a required pointer is NULL */
     SSD_ERR_MISALIGNED = 3,     /* a pointer is not 16-byte aligned */
-    SSD_ERR_UNSUPPORTED = 4,    /* dtype, shape or requested path not supported */
+    SSD_ERR_UNSUPPORTED = 4,    /* shape or requested path not supported */
     SSD_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed; nothing further enqueued */
     SSD_ERR_TIMEOUT = 6,        /* a kernel gave up a bounded wait (read via ssd_get_device_error) */
     SSD_ERR_ALIASING = 7,       /* y overlaps an input, or the two states overlap partially */
-    SSD_ERR_SCRATCH_LIMIT = 8   /* the scratch needed exceeds the buffer the call may use (the fixed
+    SSD_ERR_SCRATCH_LIMIT = 8,  /* the scratch needed exceeds the buffer the call may use (the fixed
                                    array of ssd_scan_fwd_noalloc, the workspace of ssd_scan_fwd_ws) */
+    SSD_ERR_UNSUPPORTED_DTYPE = 9   /* dims->dtype is not an ssd_dtype_t, or the path requested (or,
+                                       for ssd_scan_fwd_noalloc, the only path it has) does not take it:
+                                       the chunked tcgen05 path takes bf16 only */
 } ssd_status_t;
 
 /* Kernel path selection, in ssd_dims_t.flags (low 4 bits). */
@@ -186,11 +189,17 @@ ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt
  *
  * Arguments, layouts and ownership as ssd_scan_fwd.  Runs the same chunked
  * tcgen05 kernel with its scratch in a fixed 32 MiB array that the library
- * module holds per device, whose address is looked up once per device.  The
- * call calls no allocator.
+ * module holds per device.  The array's device address is looked up on the
+ * first call on a device, with that device current, and again after the
+ * device's context has changed (cudaDeviceReset); make that first call before
+ * any stream capture.  The call calls no allocator.
  * Errors as ssd_scan_fwd, plus:
  *   SSD_ERR_UNSUPPORTED    the chunked path does not support these dims, or
- *                          SSD_PATH_SEQUENTIAL was requested in dims->flags;
+ *                          dims->flags requests a path other than
+ *                          SSD_PATH_AUTO or SSD_PATH_CHUNKED (the sequential
+ *                          and decode paths need no scratch: call ssd_scan_fwd),
+ *                          or requests SSD_SCHEDULE_SPLIT;
+ *   SSD_ERR_UNSUPPORTED_DTYPE  dims->dtype is not bf16;
  *   SSD_ERR_SCRATCH_LIMIT  the kernel would need more than 32 MiB of scratch;
  *                          nothing is enqueued.  The call never takes
  *                          SSD_SCHEDULE_SPLIT, and takes SSD_SCHEDULE_PIECES
@@ -212,11 +221,11 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
 /*
  * ssd_trap_scan_fwd -- the trapezoidal (Mamba-3 SISO) scan, forward.
  *
- * The Mamba-3 SISO GPU forward of the pages replaces the exponential
- * recurrence by a trapezoidal one (module header of its forward pass: "Trapezoidal
- * recurrence (alpha/beta/gamma)", "additional persistent state: k_state,
- * v_state"; step F5b: alpha = exp(a dt), beta = alpha dt (1 - trap),
- * gamma = trap dt).  Per batch row b and head h, with v = x, k = B, q = C of
+ * The Mamba-3 SISO GPU forward of the pages (mamba-rs 0.2.1,
+ * mamba3_siso/gpu/mamba3_gpu.rs) replaces the exponential recurrence by a
+ * trapezoidal one in three coefficients and keeps the last step's k and v as
+ * extra carried state (module header of its forward pass; step F5b:
+ * alpha = exp(a dt), beta = alpha dt (1 - trap), gamma = trap dt).  Per batch row b and head h, with v = x, k = B, q = C of
  * the head's group g = h / (H/G):
  *   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
  *   y_t = q_t^T h_t + D_h v_t
@@ -260,10 +269,11 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
 
 /*
  * ssd_conv1d_silu_fwd -- the causal depthwise conv1d + SiLU that precedes the
- * scan in the Mamba blocks of the pages ("causal conv1d over x + B_proj +
- * C_proj (fused, convD channels)"; the conv1d kernel page:
- * y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d], zero before the
- * sequence; "conv1d burnin + fused SiLU" with a carried conv state).  Over
+ * scan in the Mamba blocks of the pages (the builderforce Mamba2Block runs one
+ * causal conv1d over the fused x, B and C projection channels; the conv1d
+ * kernel page: y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d], zero before
+ * the sequence; the mamba-rs 0.4.0 S6 forward applies SiLU in the same
+ * kernel as the conv and carries the conv state from call to call).  Over
  * the fused channels c of xbc = [x (H*P) | B (G*N) | C (G*N)]:
  *   u[b,t,c] = SiLU(bias[c] + sum_{k<K} weight[c,k] xbc[b,t-k,c])
  * with xbc before t = 0 taken from conv_state (zero when NULL), and u written
@@ -395,8 +405,9 @@ uint64_t ssd_launch_count(void);
  * SSD_ERR_TIMEOUT).  Returns SSD_OK, or SSD_ERR_CUDA if the read failed. */
 ssd_status_t ssd_get_device_error(void *stream, uint32_t *code);
 
-/* Static description of a status code.  Never NULL. */
-const char *ssd_status_string(int32_t status);
+/* Static description of a status code.  Never NULL (an unknown value gives
+ * "unknown status"). */
+const char *ssd_status_string(ssd_status_t status);
 
 /* SSD_ABI_VERSION of the loaded library. */
 int32_t ssd_abi_version(void);

@@ -4,11 +4,12 @@ Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may use it; the product library never imports it.
 
 * :func:`conv1d_silu` -- the causal depthwise convolution over the fused
-  x | B | C channels and its SiLU (the Mamba blocks of the pages: "causal
-  conv1d over x + B_proj + C_proj (fused, convD channels)"; the conv1d kernel
-  page: y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d] with x = 0 before
-  the sequence; "conv1d burnin + fused SiLU" with a carried conv state),
-  split into the scan's x [B,L,H,P], B and C [B,L,G,N].
+  x | B | C channels and its SiLU (the builderforce Mamba2Block runs one
+  causal conv1d over the fused x, B and C projection channels; the conv1d
+  kernel page: y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d] with x = 0
+  before the sequence; the mamba-rs 0.4.0 S6 forward applies SiLU in the
+  conv's own kernel and carries the conv state from call to call), split into
+  the scan's x [B,L,H,P], B and C [B,L,G,N].
 * :func:`gated_rmsnorm` -- the gated output norm of the Mamba-3 forward (step
   F7): RMSNorm(y) * weight * SiLU(z) over the H*P channels of each token.
 """

@@ -3,9 +3,10 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may use it; the product library never imports it.
 
-What is computed (the Mamba-3 SISO GPU forward of the pages: module header,
-"trapezoidal recurrence (alpha/beta/gamma) instead of exponential" and
-"additional persistent state: k_state, v_state"; step F5b for the
+What is computed (the Mamba-3 SISO GPU forward of the pages, mamba-rs 0.2.1
+mamba3_siso/gpu/mamba3_gpu.rs: its module header states a recurrence that is
+trapezoidal in three coefficients where Mamba-2's is exponential, and two
+more carried states holding the last k and v; step F5b gives the
 coefficients), per batch row b and head h, with v = x, k = B, q = C:
 
     alpha_t = exp(a_t * dt_t)

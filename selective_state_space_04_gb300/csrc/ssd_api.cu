@@ -1,6 +1,8 @@
 // ssd_api.cu -- the C ABI of libssd: validation, path choice, scratch memory,
 // launches.  Every entry point only enqueues on the caller's stream (except
 // the host-buffer variant, which synchronises it at the end).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -41,7 +43,7 @@ ssd_status_t check_dims(const ssd_dims_t *d, Sizes *sz)
         d->dstate < 1 || d->ngroups < 1 || d->chunk < 1 || d->nheads % d->ngroups != 0)
         return SSD_ERR_INVALID_DIMS;
     if (d->dtype != SSD_DTYPE_F32 && d->dtype != SSD_DTYPE_BF16)
-        return SSD_ERR_UNSUPPORTED;
+        return SSD_ERR_UNSUPPORTED_DTYPE;
     const uint32_t path = d->flags & SSD_PATH_MASK;
     if ((d->flags & ~(SSD_PATH_MASK | SSD_SCHEDULE_REQUEST_MASK | SSD_DIAG_STALL_HANDOFF)) != 0 ||
         path > SSD_PATH_DECODE)
@@ -111,6 +113,41 @@ bool device_is_gb300_class()
     return major == 10 && minor == 3;
 }
 
+// Why the chunked path refuses dims it does not support: its operands are bf16
+// only, so another dtype is a dtype error; anything else is a shape error.
+ssd_status_t chunk_refusal(const ScanArgs &a)
+{
+    return a.dtype != SSD_DTYPE_BF16 ? SSD_ERR_UNSUPPORTED_DTYPE : SSD_ERR_UNSUPPORTED;
+}
+
+// Unique id of the CUDA context current on this thread, or 0 when there is none
+// or the driver cannot say.  The driver never reuses an id within a process, so
+// the per-device caches below, keyed on it, notice a cudaDeviceReset or a
+// re-created primary context and set themselves up again instead of handing out
+// a pool, stream or address of a context that no longer exists.
+uint64_t current_context_id()
+{
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
 // Resolves the path for validated dims.  Returns SSD_PATH_* or -status.
 int32_t resolve_path(const ScanArgs &a, uint32_t requested, bool probe_device)
 {
@@ -124,7 +161,7 @@ int32_t resolve_path(const ScanArgs &a, uint32_t requested, bool probe_device)
     if (requested == SSD_PATH_SEQUENTIAL)
         return seq_ok ? (int32_t)SSD_PATH_SEQUENTIAL : -(int32_t)SSD_ERR_UNSUPPORTED;
     if (requested == SSD_PATH_CHUNKED)
-        return chunk_ok ? (int32_t)SSD_PATH_CHUNKED : -(int32_t)SSD_ERR_UNSUPPORTED;
+        return chunk_ok ? (int32_t)SSD_PATH_CHUNKED : -(int32_t)chunk_refusal(a);
     if (chunk_ok)
         return SSD_PATH_CHUNKED;
     if (seq_ok)
@@ -133,15 +170,18 @@ int32_t resolve_path(const ScanArgs &a, uint32_t requested, bool probe_device)
 }
 
 // Library-owned stream-ordered memory pool per device (kept cached so that
-// repeated calls do not go back to the driver).
+// repeated calls do not go back to the driver; set up again when the device's
+// context has changed since).
 cudaMemPool_t scratch_pool(int dev)
 {
     static std::mutex mu;
     static cudaMemPool_t pools[64] = {};
+    static uint64_t pool_ctx[64] = {};
     if (dev < 0 || dev >= 64)
         return nullptr;
     std::lock_guard<std::mutex> lk(mu);
-    if (!pools[dev]) {
+    const uint64_t ctx = current_context_id();
+    if (!pools[dev] || ctx == 0 || ctx != pool_ctx[dev]) {
         cudaMemPoolProps props;
         std::memset(&props, 0, sizeof(props));
         props.allocType = cudaMemAllocationTypePinned;
@@ -153,6 +193,7 @@ cudaMemPool_t scratch_pool(int dev)
         uint64_t keep = UINT64_MAX;
         cudaMemPoolSetAttribute(p, cudaMemPoolAttrReleaseThreshold, &keep);
         pools[dev] = p;
+        pool_ctx[dev] = current_context_id();   // the context exists now
     }
     return pools[dev];
 }
@@ -170,17 +211,20 @@ HostStreams host_streams(int dev)
 {
     static std::mutex mu;
     static HostStreams streams[64];
+    static uint64_t streams_ctx[64] = {};
     if (dev < 0 || dev >= 64)
         return HostStreams{};
     std::lock_guard<std::mutex> lk(mu);
     HostStreams &h = streams[dev];
-    if (!h.in) {
+    const uint64_t ctx = current_context_id();
+    if (!h.in || ctx == 0 || ctx != streams_ctx[dev]) {
         HostStreams n;
         if (cudaStreamCreateWithFlags(&n.in, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&n.comp, cudaStreamNonBlocking) != cudaSuccess ||
             cudaStreamCreateWithFlags(&n.out, cudaStreamNonBlocking) != cudaSuccess)
             return HostStreams{};
         h = n;
+        streams_ctx[dev] = current_context_id();
     }
     return h;
 }
@@ -276,20 +320,28 @@ ssd_status_t validate(const void *x, const float *dt_raw, const float *dt_bias, 
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once
-// per device (with that device current) and cached; null on failure.
+// Device address of g_noalloc_scratch on the current device (the host-side name
+// of the array is not a device address).  Looked up with that device current on
+// the first call, and again whenever the device's context has changed since (a
+// cudaDeviceReset unloads the module, and the array may come back elsewhere);
+// cached otherwise.  Null on failure.
 void *noalloc_scratch(int dev)
 {
     static std::mutex mu;
     static void *addr[64] = {};
+    static uint64_t addr_ctx[64] = {};
     if (dev < 0 || dev >= 64)
         return nullptr;
     std::lock_guard<std::mutex> lk(mu);
-    if (!addr[dev]) {
+    const uint64_t ctx = current_context_id();
+    if (!addr[dev] || ctx == 0 || ctx != addr_ctx[dev]) {
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) {
+            addr[dev] = nullptr;
             return nullptr;
+        }
         addr[dev] = p;
+        addr_ctx[dev] = current_context_id();   // the lookup made the context current
     }
     return addr[dev];
 }
@@ -497,7 +549,9 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
     if (dims->batch == 0 || dims->seqlen == 0)
         return ssd_scan_fwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims,
                             stream);
-    if ((dims->flags & SSD_PATH_MASK) == SSD_PATH_SEQUENTIAL)
+    // the chunked kernel is the only path here: another explicit request is refused
+    const uint32_t req = dims->flags & SSD_PATH_MASK;
+    if (req != SSD_PATH_AUTO && req != SSD_PATH_CHUNKED)
         return SSD_ERR_UNSUPPORTED;
     ScanArgs a = make_args(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims);
     if (a.sched_req == SSD_SCHEDULE_SPLIT)
@@ -628,9 +682,9 @@ ssd_status_t ssd_get_device_error(void *stream, uint32_t *code)
     return chunk_read_device_error(static_cast<cudaStream_t>(stream), code);
 }
 
-const char *ssd_status_string(int32_t status)
+const char *ssd_status_string(ssd_status_t status)
 {
-    switch (status) {
+    switch ((int32_t)status) {
     case SSD_OK: return "ok";
     case SSD_ERR_INVALID_DIMS: return "invalid dimensions";
     case SSD_ERR_NULL_PTR: return "required pointer is null";
@@ -640,6 +694,7 @@ const char *ssd_status_string(int32_t status)
     case SSD_ERR_TIMEOUT: return "kernel exceeded a bounded wait";
     case SSD_ERR_ALIASING: return "output overlaps an input";
     case SSD_ERR_SCRATCH_LIMIT: return "scratch needed exceeds the buffer the call may use";
+    case SSD_ERR_UNSUPPORTED_DTYPE: return "dtype not supported";
     default: return "unknown status";
     }
 }
@@ -808,7 +863,7 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     else   // one step is a stream of the state: the sequential kernel
         chunked = chunk_ok && (dims->seqlen > 1 || !seq_ok);
     if (chunked ? !chunk_ok : !seq_ok)
-        return SSD_ERR_UNSUPPORTED;
+        return chunked && dims->dtype != SSD_DTYPE_BF16 ? SSD_ERR_UNSUPPORTED_DTYPE : SSD_ERR_UNSUPPORTED;
     if (!chunked)
         return trap_launch(ta, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
     int dev = 0;

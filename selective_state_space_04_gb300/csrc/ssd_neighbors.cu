@@ -1,11 +1,12 @@
 // ssd_neighbors.cu -- the steps on either side of the scan in the Mamba blocks
 // of the pages.
 //
-// * Causal depthwise conv1d + SiLU over the fused x | B | C channels ("causal
-//   conv1d over x + B_proj + C_proj (fused, convD channels)"; the conv1d
-//   kernel page: y[b,t,d] = sum_k weight[d,k] x[b,t-k,d] + bias[d], zero
-//   before the sequence; "conv1d burnin + fused SiLU" with a carried conv
-//   state), written straight into the scan's x [B,L,H,P], B and C [B,L,G,N].
+// * Causal depthwise conv1d + SiLU over the fused x | B | C channels (the
+//   builderforce Mamba2Block convolves the fused x, B and C projection
+//   channels; the conv1d kernel page: y[b,t,d] = sum_k weight[d,k] x[b,t-k,d]
+//   + bias[d], zero before the sequence; the mamba-rs 0.4.0 S6 forward applies
+//   SiLU in the conv's kernel and carries the conv state between calls),
+//   written straight into the scan's x [B,L,H,P], B and C [B,L,G,N].
 // * Gated RMSNorm of the scan's output (Mamba-3 forward, step F7:
 //   RMSNorm(y) * weight * SiLU(z)) over the H*P channels of each token.
 //

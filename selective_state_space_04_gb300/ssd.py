@@ -25,7 +25,7 @@ DTYPE_BF16 = 1
 
 STATUS = {0: "SSD_OK", 1: "SSD_ERR_INVALID_DIMS", 2: "SSD_ERR_NULL_PTR", 3: "SSD_ERR_MISALIGNED",
           4: "SSD_ERR_UNSUPPORTED", 5: "SSD_ERR_CUDA", 6: "SSD_ERR_TIMEOUT", 7: "SSD_ERR_ALIASING",
-          8: "SSD_ERR_SCRATCH_LIMIT"}
+          8: "SSD_ERR_SCRATCH_LIMIT", 9: "SSD_ERR_UNSUPPORTED_DTYPE"}
 
 
 class SsdError(RuntimeError):
@@ -100,7 +100,10 @@ def make_dims(batch, seqlen, nheads, headdim, dstate, ngroups, chunk, dtype, pat
     d = SsdDims()
     d.batch, d.seqlen, d.nheads, d.headdim = batch, seqlen, nheads, headdim
     d.dstate, d.ngroups, d.chunk = dstate, ngroups, chunk
-    d.dtype = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
+    if isinstance(dtype, int):     # an ssd_dtype_t value, passed through as given
+        d.dtype = dtype
+    else:
+        d.dtype = DTYPE_BF16 if dtype in ("bf16", torch.bfloat16) else DTYPE_F32
     d.flags = (_PATHS[path] if isinstance(path, str) else int(path)) | \
         (_SCHEDULE_REQUESTS[schedule] << SCHEDULE_SHIFT)
     d.reserved = 0

@@ -41,8 +41,8 @@ def test_every_declared_symbol_is_exported(libssd):
 
 def test_abi_version_and_status_strings(libssd):
     lib = libssd.lib()
-    assert lib.ssd_abi_version() == 1
-    for code in range(9):
+    assert lib.ssd_abi_version() == 2
+    for code in range(10):
         s = lib.ssd_status_string(code)
         assert s and s != b"unknown status"
     assert lib.ssd_status_string(99) == b"unknown status"
@@ -99,13 +99,46 @@ def test_output_aliasing_input(libssd):
 def test_chunked_path_needs_bf16_64_128(libssd):
     lib = libssd.lib()
     d = dims(libssd, dtype="f32", path="chunked", headdim=64, dstate=128, chunk=256)
-    assert lib.ssd_select_path(ctypes.byref(d)) == -4
+    assert lib.ssd_select_path(ctypes.byref(d)) == -9      # SSD_ERR_UNSUPPORTED_DTYPE
     d = dims(libssd, path="chunked", headdim=32, dstate=128, chunk=256)
     assert lib.ssd_select_path(ctypes.byref(d)) == -4
     d = dims(libssd, path="chunked", headdim=64, dstate=128, chunk=100)
     assert lib.ssd_select_path(ctypes.byref(d)) == -4
     d = dims(libssd, path="chunked", nheads=3, ngroups=1, headdim=64, dstate=128, chunk=256)
     assert lib.ssd_select_path(ctypes.byref(d)) == -4
+
+
+def test_unknown_dtype_rejected(libssd):
+    # a dtype value outside ssd_dtype_t: SSD_ERR_UNSUPPORTED_DTYPE from every entry
+    # point, before any device access
+    lib = libssd.lib()
+    d = dims(libssd)
+    d.dtype = 7
+    assert call(libssd, d) == 9
+    assert lib.ssd_select_path(ctypes.byref(d)) == -9
+    assert lib.ssd_launches_per_call(ctypes.byref(d)) == -9
+    assert _trap_call(libssd, d) == 9
+    assert _bwd_call(libssd, d) == 9
+    assert _complex_call(libssd, d) == 9
+    with pytest.raises(libssd.SsdError) as e:
+        libssd.workspace_size((1, 64, 2, 64), 1, 128, 256, dtype=7)
+    assert e.value.status == 9
+
+
+def test_noalloc_refuses_other_paths_before_cuda(libssd):
+    # the allocation-free entry point has only the chunked path: an explicit
+    # sequential or decode request, or a split schedule, is refused before any
+    # CUDA call; so is a dtype the chunked path does not take
+    lib = libssd.lib()
+    fake = ctypes.c_void_p(0x10000)
+    args = [fake] * 7 + [None, ctypes.c_void_p(0x90000000), None]
+    for path in ("sequential", "decode"):
+        d = libssd.make_dims(1, 64, 2, 64, 128, 1, 64, "bf16", path=path)
+        assert lib.ssd_scan_fwd_noalloc(*args, ctypes.byref(d), None) == 4
+    d = libssd.make_dims(1, 64, 2, 64, 128, 1, 64, "bf16", schedule="split")
+    assert lib.ssd_scan_fwd_noalloc(*args, ctypes.byref(d), None) == 4
+    d = libssd.make_dims(1, 64, 2, 64, 128, 1, 64, "f32")
+    assert lib.ssd_scan_fwd_noalloc(*args, ctypes.byref(d), None) == 9
 
 
 def test_sequential_path_limits(libssd):
@@ -218,7 +251,7 @@ def test_trap_entry_validation_before_cuda(libssd):
     # h_final overlapping h0 without being it
     assert _trap_call(libssd, d, h_final=ctypes.c_void_p(0x10000000 + 7 * 0x1000000 + 0x10)) == 7
     d2 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="chunked")
-    assert _trap_call(libssd, d2) == 4                                         # SSD_ERR_UNSUPPORTED
+    assert _trap_call(libssd, d2) == 9                                         # SSD_ERR_UNSUPPORTED_DTYPE
     d3 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", schedule="pieces")
     assert _trap_call(libssd, d3) == 1                                         # SSD_ERR_INVALID_DIMS
     d4 = libssd.make_dims(2, 8, 4, 16, 30, 2, 1, "f32")                        # N % 4 != 0

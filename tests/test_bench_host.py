@@ -75,3 +75,26 @@ def test_max_over_ranks_gloo_world_2():
 def test_single_process_needs_no_process_group():
     assert bench.init_dist(1, "gloo") is None
     assert bench.max_over_ranks(None, 3.5, "cpu") == 3.5
+
+
+def test_reference_arm_reports_the_gpu_arms_config():
+    # both arms build `config` from the workload alone, so the driver can pair
+    # them; the reference arm runs the fp64 oracle on the host (no GPU needed)
+    import json
+    import subprocess
+    w = WORKLOADS["tiny_fp32"]
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--workload", "tiny_fp32", "--steps", "2", "--warmup", "3"],
+                         capture_output=True, text=True, timeout=600, check=True).stdout
+    line = json.loads(out.strip().splitlines()[-1])
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.workload_config(w, 0, bench.flushes_l2(bench.algorithmic_bytes(w)))
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_l2_policy():
+    # the 130M layer (58.5 MB) fits in L2 and is flushed between steps; the
+    # 2.7B layer (719 MB) is not
+    assert bench.flushes_l2(bench.algorithmic_bytes(WORKLOADS["mamba2_130m_layer"]))
+    assert not bench.flushes_l2(bench.algorithmic_bytes(WORKLOADS["mamba2_2p7b_layer"]))
+    assert not bench.flushes_l2(bench.algorithmic_bytes(WORKLOADS["many_short_seqs"]))

@@ -243,7 +243,7 @@ def test_rejects_wrong_dtype_for_chunked(ssd):
     inp = make_inputs(w, seed=16)
     with pytest.raises(ssd.SsdError) as ei:
         run(ssd, inp, w, path="chunked")
-    assert ei.value.status == 4
+    assert ei.value.status == 9      # SSD_ERR_UNSUPPORTED_DTYPE: the chunked path takes bf16 only
 
 
 # --------------------------------------------- full size, sampled chains

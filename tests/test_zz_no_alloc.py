@@ -64,3 +64,26 @@ def test_many_chains_fit_the_array(ssd):
     assert ssd.device_error() == 0
     assert torch.equal(y_na, y_ref)
     assert torch.equal(f_na, f_ref)
+
+
+def test_over_the_limit_is_refused_and_launches_nothing(ssd):
+    # batch 16 x 80 heads x 4096 steps on an explicit range-schedule request
+    # needs more scratch than the array holds: SSD_ERR_SCRATCH_LIMIT, with no
+    # launch and nothing enqueued (the output buffer keeps its contents)
+    w = WORKLOADS["mamba2_2p7b_layer"].with_(batch=16)
+    inp = make_inputs(w, 14)
+    d = {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
+    y = torch.full_like(d["x"], 7.0)
+    torch.cuda.synchronize()
+    before = ssd.launch_count()
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_scan_fwd_noalloc(*_args(d), chunk=w.chunk, schedule="ranges", y=y)
+    assert e.value.status == 8
+    torch.cuda.synchronize()
+    assert ssd.launch_count() == before
+    assert bool((y == 7.0).all())
+    # a request for another path is refused the same way, before any launch
+    with pytest.raises(ssd.SsdError) as e:
+        ssd.ssd_scan_fwd_noalloc(*_args(d), chunk=w.chunk, path="sequential", y=y)
+    assert e.value.status == 4
+    assert ssd.launch_count() == before
