@@ -14,8 +14,8 @@
 // inclusive cumulative sum cs_t = sum_{k<=t} dt_k A:
 //
 //   S      = C B^T                                   (T x T, shared by both heads)
-//   M[t,s] = S[t,s] exp(cs_t - cs_s) dt_s  (s <= t),  M[t,t] += D
-//   y_t    = (M x)_t + exp(cs_t) (C P)_t
+//   M[t,s] = S[t,s] exp(cs_t - cs_s) dt_s  (s <= t)
+//   y_t    = (M x)_t + D x_t + exp(cs_t) (C P)_t      (D x added in fp32 to M x)
 //   P     <- exp(cs_{T-1}) P + B^T (w o x),   w_s = exp(cs_{T-1} - cs_s) dt_s
 //
 // This is the quadratic ("dual") form inside a sub-chunk and the linear
@@ -410,6 +410,7 @@ constexpr float kSpanMax = 64.f;
 // One 16-column group of M for both heads: columns s0 .. s0+15 of row t, from
 // the S values sv[0..15], as 8 packed bf16 pairs per head.
 //   M[t,s] = S[t,s] exp(cs_t - cs_s) dt_s  (s <= t, else 0),   M[t,t] += D
+// (the kernel passes D = 0: it adds D x to the fp32 Y_diag accumulator instead)
 // is evaluated as S[t,s] rf colf[s] with the row factor rf = exp(cs_t - cs_e)
 // and the column factor colf[s] = exp(cs_e - cs_s) dt_s, e = s0 + 15 the
 // group's last step (the caller passes rf and colf + s0).  For rows below the
@@ -843,7 +844,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             tc_fence_after();
             if constexpr (!kLocal) {   // split pass 1 has no y, so no M
-                const float D0 = hD[cur.w.h0], D1 = hD[cur.w.h0 + 1];
+                // (D x is added in fp32 to Y_diag by the state group, not through M)
+                const float D0 = 0.f, D1 = 0.f;
                 const float ct0 = cs2[r], ct1 = cs2[kT + r];
                 const float dc0 = kTrap ? dk[10 * kT + 4 + r] : 0.f, dc1 = kTrap ? dk[11 * kT + 4 + r] : 0.f;
 #pragma unroll 1
@@ -1019,12 +1021,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             {
                 uint8_t *xrow = smem + kOffX + s * kXStageBytes + hf * kTileBytes + r * 128;
                 const uint32_t w2 = pack_bf16x2(wsc, wsc);
-                // every chunk of the row gets the same weight, so the chunks are
-                // visited in swizzled order: 8 consecutive rows hit 8 distinct banks
-#pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
+                const float Dh = hD[hh];
+                // The skip term D x goes into the fp32 Y_diag accumulator from the row of x
+                // as loaded (before it is scaled), half a row (32 channels) at a time; then
+                // the row is scaled in place for the state MMA.  Chunks are visited in
+                // swizzled order: 8 consecutive rows hit 8 distinct banks.
+#pragma unroll 1
+                for (int c8 = 0; c8 < 8; ++c8) {   // one 16-byte chunk (8 channels) at a time
                     const int cc = c8 ^ (r & 7);
                     uint4 v4 = *reinterpret_cast<uint4 *>(xrow + cc * 16);
+                    if constexpr (!kLocal) {
+                        const uint32_t tcol = tmem + lane_addr + kColYd + hf * 64 + 8 * c8;
+                        uint32_t yd[8];
+                        tmem_ld8(tcol, yd);
+                        const uint32_t xw[4] = {v4.x, v4.y, v4.z, v4.w};
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float lo = __uint_as_float(xw[e] << 16), hi = __uint_as_float(xw[e] & 0xffff0000u);
+                            yd[2 * e] = __float_as_uint(fmaf(Dh, lo, __uint_as_float(yd[2 * e])));
+                            yd[2 * e + 1] = __float_as_uint(fmaf(Dh, hi, __uint_as_float(yd[2 * e + 1])));
+                        }
+                        tmem_st8(tcol, yd);
+                    }
                     v4.x = mul_bf16x2(v4.x, w2);
                     v4.y = mul_bf16x2(v4.y, w2);
                     v4.z = mul_bf16x2(v4.z, w2);
