@@ -830,6 +830,44 @@ def neighbor_setup(w: Workload, dev, seed: int):
                            None if inp["conv_state"] is None else inp["conv_state"][:nb],
                            w.nheads, w.headdim, w.ngroups, w.dstate)
         return inp, d, outs, step, nbytes, "ssd_conv1d_silu_kernel", ref
+    if w.op == "conv_scan":
+        # the conv1d + SiLU and the scan in one call (the x channels' conv inside the
+        # chunked scan kernel); dt and the head parameters drawn as for the scan
+        inp = make_conv_inputs(w, K=CONV_TAPS, seed=seed)
+        si = make_inputs(w.with_(init_state=False), seed + 1)
+        for n in ("dt_raw", "dt_bias", "A_log", "D"):
+            inp[n] = si[n]
+        d = {n: (None if t is None else t.to(dev)) for n, t in inp.items()}
+        Cc = HP + 2 * GN
+        outs = {"y": torch.empty((w.batch, w.seqlen, w.nheads, w.headdim), dtype=d["xbc"].dtype, device=dev),
+                "final_state": torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
+                                           device=dev),
+                "conv_state_out": torch.empty((w.batch, CONV_TAPS - 1, Cc), dtype=d["xbc"].dtype, device=dev)}
+
+        def step(stream):
+            ssd.conv_scan_fwd(d["xbc"], d["weight"], d["bias"], d["conv_state"], d["dt_raw"], d["dt_bias"],
+                              d["A_log"], d["D"], nheads=w.nheads, headdim=w.headdim, ngroups=w.ngroups,
+                              dstate=w.dstate, chunk=w.chunk, stream=stream, **outs)
+        cstate = w.batch * (CONV_TAPS - 1) * Cc * es
+        sstate = w.batch * w.nheads * w.headdim * w.dstate * 4
+        nbytes = (BL * Cc * es + Cc * (CONV_TAPS + 1) * 4 + (cstate if w.init_state else 0) + cstate   # conv
+                  + BL * w.nheads * 4 + 3 * w.nheads * 4 + BL * HP * es + sstate)                     # scan
+
+        def ref(nb):
+            sub = lambda t: None if t is None else t[:nb]   # noqa: E731
+            rx, rB, rC, _ = on.conv1d_silu(sub(inp["xbc"]), inp["weight"], inp["bias"], sub(inp["conv_state"]),
+                                           w.nheads, w.headdim, w.ngroups, w.dstate)
+            import oracle
+            oracle.ssd_fwd(rx, sub(inp["dt_raw"]), inp["dt_bias"], inp["A_log"], rB, rC, inp["D"])
+
+        def two_calls(stream):   # the same work as ssd_conv1d_silu_fwd, then ssd_scan_fwd
+            x, Bm, Cm, _ = ssd.conv1d_silu_fwd(d["xbc"], d["weight"], d["bias"], d["conv_state"], nheads=w.nheads,
+                                               headdim=w.headdim, ngroups=w.ngroups, dstate=w.dstate,
+                                               conv_state_out=outs["conv_state_out"], stream=stream)
+            ssd.ssd_scan_fwd(x, d["dt_raw"], d["dt_bias"], d["A_log"], Bm, Cm, d["D"], chunk=w.chunk,
+                             y=outs["y"], final_state=outs["final_state"], stream=stream)
+        step.two_calls = two_calls
+        return inp, d, outs, step, nbytes, "ssd_chunk_fused_kernel", ref
     if w.op == "complex":
         from selective_state_space_04_gb300.inputs import make_complex_inputs
         import oracle.complex_scan as ocx
@@ -893,7 +931,7 @@ def neighbor_setup(w: Workload, dev, seed: int):
     return inp, d, outs, step, 3 * BL * HP * es + HP * 4, "ssd_gated_rmsnorm_kernel", ref
 
 
-NEIGHBOR_NAMES = {"conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward",
+NEIGHBOR_NAMES = {"conv_scan": "causal conv1d + SiLU and SSD scan fwd (fused)", "conv": "causal conv1d + SiLU fwd", "gnorm": "gated RMSNorm fwd", "bwd": "SSD scan backward",
                   "complex": "complex-valued (ET) scan fwd"}
 
 
@@ -1000,6 +1038,16 @@ def run_gpu_neighbor(args, w: Workload):
         "gpu_launches": launches,
         "clocks": clocks,
     }
+    if hasattr(step, "two_calls"):
+        # the same work as two library calls (conv, then scan), timed the same way
+        for _ in range(3):
+            step.two_calls(stream)
+        torch.cuda.synchronize(dev)
+        t_ms, _, _, _ = timed_region(ssd, lambda: step.two_calls(stream), args.steps, stream, dev, None, local,
+                                     flush)
+        line["two_call_chain"] = {"ms_per_step": t_ms / args.steps,
+                                  "value": th * args.steps / (t_ms / 1e3),
+                                  "calls": "ssd_conv1d_silu_fwd, then ssd_scan_fwd (x, B, C through device memory)"}
     if not args.no_cpu_baseline and world == 1:
         v, sample = neighbor_oracle_rate(w, ref, 10.0, min_seconds=10.0)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample}
@@ -1051,7 +1099,7 @@ def main():
     w = WORKLOADS[args.workload]
     if w.op == "trap":
         (run_reference_trap if args.impl == "reference" else run_gpu_trap)(args, w)
-    elif w.op in ("conv", "gnorm", "bwd", "complex"):
+    elif w.op in ("conv", "conv_scan", "gnorm", "bwd", "complex"):
         (run_reference_neighbor if args.impl == "reference" else run_gpu_neighbor)(args, w)
     elif args.impl == "reference":
         run_reference(args, w)

@@ -295,6 +295,39 @@ ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const flo
                                  const ssd_dims_t *dims, void *stream);
 
 /*
+ * ssd_conv_scan_fwd -- ssd_conv1d_silu_fwd followed by ssd_scan_fwd, in one call,
+ * with the conv of the x channels done inside the chunked scan kernel (the
+ * builderforce Mamba2Block runs the causal conv1d over the fused x, B, C
+ * projection channels, then the SSD module, on one layer's buffers; the mamba-rs
+ * 0.4.0 S6 forward carries the conv state between calls).  The scan reads the
+ * raw x channels of xbc and applies the conv and SiLU to each tile in shared
+ * memory, so the conv's x never goes through device memory; the B and C
+ * channels (shared by every head of a group) are convolved once by a small
+ * kernel beforehand.
+ *   u = SiLU(conv(xbc)) split into x [B,L,H,P], B and C [B,L,G,N] as
+ *   ssd_conv1d_silu_fwd defines it; then y, final_state as ssd_scan_fwd
+ *   defines them for (x, dt_raw, dt_bias, A_log, B, C, D, init_state).
+ * xbc [B,L,H*P + 2*G*N], conv_state and conv_state_out [B,K-1,H*P + 2*G*N]
+ * (bf16); conv_weight [H*P + 2*G*N, K] and conv_bias (NULL: none) fp32;
+ * kernel_size K in 2..4; the scan's arguments as for ssd_scan_fwd.  Nullable:
+ * conv_bias, conv_state (zero), init_state (zero), final_state and
+ * conv_state_out (not written).  DEVICE pointers of the current device,
+ * caller-owned, 16-byte aligned; outputs overlap no input and each other
+ * (conv_state_out must not overlap conv_state).
+ * Supported: the chunked path's shapes (bf16, P = 64, N = 128, chunk % 64 == 0,
+ * (H/G) even; GB300-class device); flags: SSD_PATH_AUTO or SSD_PATH_CHUNKED,
+ * optionally a schedule request.  Scratch (the convolved B and C, and the
+ * chunked path's) comes stream-ordered from the library pool.  Errors as
+ * ssd_scan_fwd; SSD_ERR_UNSUPPORTED_DTYPE for fp32.  seqlen 0 passes both
+ * states through.  Enqueues on `stream` only; never synchronises.
+ */
+ssd_status_t ssd_conv_scan_fwd(const void *xbc, const float *conv_weight, const float *conv_bias,
+                               const void *conv_state, int32_t kernel_size, const float *dt_raw,
+                               const float *dt_bias, const float *A_log, const float *D,
+                               const float *init_state, void *y, float *final_state,
+                               void *conv_state_out, const ssd_dims_t *dims, void *stream);
+
+/*
  * ssd_gated_rmsnorm_fwd -- the gated output norm after the scan (the Mamba-3
  * forward of the pages, step F7 with its norm: RMSNorm(y) * weight * SiLU(z)),
  * per token over its H*P channels:

@@ -950,6 +950,119 @@ ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const flo
     return conv_launch(na, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
+ssd_status_t ssd_conv_scan_fwd(const void *xbc, const float *conv_weight, const float *conv_bias,
+                               const void *conv_state, int32_t kernel_size, const float *dt_raw,
+                               const float *dt_bias, const float *A_log, const float *D,
+                               const float *init_state, void *y, float *final_state, void *conv_state_out,
+                               const ssd_dims_t *dims, void *stream)
+{
+    Sizes sz;
+    ssd_status_t s = check_dims(dims, &sz);
+    if (s != SSD_OK)
+        return s;
+    if ((dims->flags & ~(SSD_PATH_MASK | SSD_SCHEDULE_REQUEST_MASK)) != 0 || kernel_size < 2 || kernel_size > 4)
+        return SSD_ERR_INVALID_DIMS;
+    const uint32_t path = dims->flags & SSD_PATH_MASK;
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_CHUNKED)
+        return SSD_ERR_UNSUPPORTED;
+    if (dims->dtype != SSD_DTYPE_BF16)
+        return SSD_ERR_UNSUPPORTED_DTYPE;
+    const int64_t HP = (int64_t)dims->nheads * dims->headdim, GN = (int64_t)dims->ngroups * dims->dstate;
+    const int64_t Cc = HP + 2 * GN;
+    if (HP % 8 != 0 || GN % 8 != 0)
+        return SSD_ERR_UNSUPPORTED;
+    int64_t xbcb, stb;
+    if (!mul_ok(dims->batch * dims->seqlen, Cc * 2, &xbcb) || !mul_ok(dims->batch * (kernel_size - 1), Cc * 2, &stb))
+        return SSD_ERR_INVALID_DIMS;
+    const bool work = dims->batch > 0 && dims->seqlen > 0;
+    if (work && (!xbc || !conv_weight || !dt_raw || !dt_bias || !A_log || !D || !y))
+        return SSD_ERR_NULL_PTR;
+    const void *ptrs[] = {xbc, conv_weight, conv_bias, conv_state, dt_raw, dt_bias, A_log, D,
+                          init_state, y, final_state, conv_state_out};
+    for (const void *ptr : ptrs)
+        if (!aligned16(ptr))
+            return SSD_ERR_MISALIGNED;
+    // outputs overlap no input (the scan state may be updated in place) and not each other
+    const void *ins[] = {xbc, conv_weight, conv_bias, conv_state, dt_raw, dt_bias, A_log, D, init_state};
+    const int64_t inb[] = {xbcb, Cc * kernel_size * 4, Cc * 4, stb, sz.dt, sz.par, sz.par, sz.par, sz.state};
+    const void *outs[] = {work ? y : nullptr, final_state, conv_state_out};
+    const int64_t outb[] = {sz.x, sz.state, stb};
+    for (int o = 0; o < 3; ++o) {
+        for (int i = 0; i < 9; ++i)
+            if (overlaps(outs[o], outb[o], ins[i], inb[i]) && !(o == 1 && i == 8 && outs[o] == ins[i]))
+                return SSD_ERR_ALIASING;
+        for (int o2 = o + 1; o2 < 3; ++o2)
+            if (overlaps(outs[o], outb[o], outs[o2], outb[o2]))
+                return SSD_ERR_ALIASING;
+    }
+    ScanArgs a = make_args(nullptr, dt_raw, dt_bias, A_log, nullptr, nullptr, D, init_state, y, final_state, dims);
+    a.conv = true;
+    a.xbc = xbc;
+    a.conv_w = conv_weight;
+    a.conv_b = conv_bias;
+    a.conv_state = conv_state;
+    a.conv_k = kernel_size;
+    a.conv_cc = (int)Cc;
+    if (!chunk_supported(a))
+        return SSD_ERR_UNSUPPORTED;
+    if (dims->batch == 0)
+        return SSD_OK;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (dims->seqlen == 0) {   // no steps: both states pass through (zero when not given)
+        const void *src[] = {init_state, conv_state};
+        void *dst[] = {final_state, conv_state_out};
+        const int64_t nb[] = {sz.state, stb};
+        for (int i = 0; i < 2; ++i) {
+            if (!dst[i] || nb[i] == 0 || src[i] == dst[i])
+                continue;
+            const cudaError_t e = src[i] ? cudaMemcpyAsync(dst[i], src[i], (size_t)nb[i], cudaMemcpyDeviceToDevice, st)
+                                         : cudaMemsetAsync(dst[i], 0, (size_t)nb[i], st);
+            if (e != cudaSuccess)
+                return SSD_ERR_CUDA;
+        }
+        return SSD_OK;
+    }
+    if (!device_is_gb300_class())
+        return SSD_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    cudaMemPool_t pool = scratch_pool(dev);
+    if (!pool)
+        return SSD_ERR_CUDA;
+    // scratch: the convolved B and C, then the chunked path's own
+    const size_t bc_bytes = ((size_t)sz.bc + 255) & ~(size_t)255;
+    const size_t ws_bytes = chunk_workspace_bytes(a);
+    char *buf = nullptr;
+    if (cudaMallocFromPoolAsync((void **)&buf, 2 * bc_bytes + ws_bytes, pool, st) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    NeighborArgs na;
+    na.xbc = xbc;
+    na.w = conv_weight;
+    na.bias = conv_bias;
+    na.state_in = conv_state;
+    na.B = buf;
+    na.C = buf + bc_bytes;
+    na.state_out = conv_state_out;
+    na.kernel_size = kernel_size;
+    na.batch = dims->batch;
+    na.seqlen = dims->seqlen;
+    na.nheads = dims->nheads;
+    na.headdim = dims->headdim;
+    na.dstate = dims->dstate;
+    na.ngroups = dims->ngroups;
+    na.dtype = dims->dtype;
+    ssd_status_t rs = conv_bc_launch(na, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    if (rs == SSD_OK) {
+        a.B = na.B;
+        a.C = na.C;
+        rs = chunk_launch(a, buf + 2 * bc_bytes, st);
+    }
+    if (cudaFreeAsync(buf, st) != cudaSuccess && rs == SSD_OK)
+        rs = SSD_ERR_CUDA;
+    return rs;
+}
+
 ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *weight, float eps, void *out,
                                    const ssd_dims_t *dims, void *stream)
 {

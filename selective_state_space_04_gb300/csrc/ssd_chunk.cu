@@ -86,8 +86,16 @@ constexpr uint32_t kOffDecay = kOffX + 2 * kXStageBytes;
 constexpr uint32_t kOffWsum = kOffDecay + 3 * kDecayFloats * 4;
 constexpr int kMaxHeads = 512;                       // per-head parameters staged in shared memory
 constexpr uint32_t kOffHead = kOffWsum + 64;          // A*log2(e), dt_bias, D  (3 x kMaxHeads floats)
-constexpr uint32_t kOffBars = kOffHead + 3 * kMaxHeads * 4;
-constexpr int kNumBars = 22;
+// conv mode: the conv1d weights of the head pair's 128 x channels, per head and
+// 8-channel chunk c: taps 0..3 (tap k multiplies the input k steps back; zero
+// past the kernel size) then the bias, 8 channels each (40 floats); and the 3
+// raw input rows before the sub-chunk, per head (the halo carried between the
+// sub-chunks of a unit)
+constexpr uint32_t kOffConvW = kOffHead + 3 * kMaxHeads * 4;
+constexpr int kConvWFloats = 2 * 8 * 40;
+constexpr uint32_t kOffHalo = kOffConvW + kConvWFloats * 4;   // [2 heads][3 rows][128 bytes]
+constexpr uint32_t kOffBars = kOffHalo + 2 * 3 * 128;
+constexpr int kNumBars = 24;
 constexpr uint32_t kOffTmemHolder = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffTmemHolder + 16 + 1024;  // + alignment slack
 
@@ -113,6 +121,8 @@ enum {
     BAR_EPI_DONE,
     BAR_DRAIN,
     BAR_MSYNC,   // decay-group barrier (bounded, unlike bar.sync)
+    BAR_X_CONV,  // conv mode: the state group has applied the conv to x(j)
+    BAR_CSYNC,   // conv mode: state-group barrier (bounded)
 };
 
 struct ChunkParams {
@@ -140,6 +150,13 @@ struct ChunkParams {
     const float *tdt, *ta, *ttrap;
     const __nv_bfloat16 *k0, *v0;
     int mode;                         // kChained, kSplitLocal or kSplitEntering
+    // conv mode: raw xbc [B,L,conv_cc] (the x tensor map reads its x channels), the conv
+    // weights [conv_cc, conv_k] and bias [conv_cc] (or null), the carried conv state
+    // [B, conv_k - 1, conv_cc] (or null)
+    const __nv_bfloat16 *xbc;
+    const float *conv_w, *conv_b;
+    const __nv_bfloat16 *conv_state;
+    int conv_k, conv_cc;
 };
 
 // How the units of a chain get their entering state:
@@ -375,6 +392,40 @@ __device__ __forceinline__ int post_row_of(const Cursor &c, const ChunkParams &p
     return kPieces ? (int)blockIdx.x : c.u;
 }
 
+// SiLU for outputs rounded to bf16: SiLU(v) = h + h tanh(h), h = v / 2, with the
+// hardware tanh approximation (the form and the operation order of the library's
+// conv kernel, so that the conv mode's x matches its output bit for bit)
+__device__ __forceinline__ float silu_bf16_out(float v)
+{
+    const float h = 0.5f * v;
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+    return fmaf(h, t, h);
+}
+
+// conv mode: 8 channels (16 bytes) of the raw input at step t of batch row b,
+// channels ch .. ch+7 of xbc: from xbc for t >= 0, else from the carried conv
+// state (its row K-1+t), zero where neither has it
+__device__ __forceinline__ uint4 conv_input_row(const ChunkParams &p, int b, long long t, int ch)
+{
+    if (t >= 0)
+        return __ldg(reinterpret_cast<const uint4 *>(p.xbc + ((size_t)b * p.L + t) * p.conv_cc + ch));
+    const long long rs = p.conv_k - 1 + t;
+    if (p.conv_state && rs >= 0)
+        return __ldg(reinterpret_cast<const uint4 *>(p.conv_state + ((size_t)b * (p.conv_k - 1) + rs) * p.conv_cc + ch));
+    return make_uint4(0u, 0u, 0u, 0u);
+}
+
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
 __device__ __forceinline__ float softplus_f32(float z)
 {
     return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z)));
@@ -520,7 +571,7 @@ __device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, co
 // decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
 // alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
 // (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
-template <bool kPieces, bool kTrap, bool kLocal>
+template <bool kPieces, bool kTrap, bool kLocal, bool kConv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
@@ -563,6 +614,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[BAR_EPI_DONE], kGroupWarps);
         mbar_init(&bars[BAR_DRAIN], 1);
         mbar_init(&bars[BAR_MSYNC], kGroupWarps);
+        mbar_init(&bars[BAR_X_CONV], kGroupWarps);
+        mbar_init(&bars[BAR_CSYNC], kGroupWarps);
         fence_mbar_init();
     }
     if (warp == kMmaWarp) {
@@ -677,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t xs = smem_u32(smem + kOffX + s * kXStageBytes);
                 const uint32_t pb = smem_u32(smem + kOffX + (s ^ 1) * kXStageBytes);
                 // Y_diag[h] = M[h] x[h]
-                if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)) ||
+                if (!(ok = kConv ? wait_bar(&bars[BAR_X_CONV], par, p)
+                                 : wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)) ||
                     !(ok = wait_bar(&bars[BAR_M_READY], par, p)) ||
                     (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p))))
                     break;
@@ -907,6 +961,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t ta = tmem + lane_addr + kColP + hf * 64;
         float unit_decay = 1.f;
+        uint32_t csync = 0;   // conv mode: phase of the state-group barrier
         bool ok = true;
         Cursor cur;
         bool has = cursor_first<kPieces>(cur, p);
@@ -1005,6 +1060,101 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 tc_fence_before();
                 warp_arrive(&bars[BAR_PB_READY]);
+            }
+            if constexpr (kConv) {
+                // ---- causal conv1d + SiLU over the x tile of sub-chunk j, in place (raw xbc
+                //      x channels in, the scan's x out).  Warp sw takes head sw >> 2 and the row
+                //      segments 4 (sw & 3) .. +3 of 8 rows; lane l takes the 8-channel chunk
+                //      l & 7 of segment 4 (sw & 3) + (l >> 3), so that the 8 lanes on one row
+                //      cover its 8 chunks, which the 128-byte swizzle puts in 8 distinct bank
+                //      groups.  The 3 rows before a lane's first row are read before anyone
+                //      writes; the raw rows 125 .. 127 become the next sub-chunk's halo.  The
+                //      weights are read from shared memory row by row.
+                const int hc = sw >> 2, c = lane & 7, r0 = 8 * (4 * (sw & 3) + (lane >> 3));
+                float *cw = reinterpret_cast<float *>(smem + kOffConvW);
+                uint8_t *halo = smem + kOffHalo + hc * (3 * 128);
+                if (cur.k == 0) {   // unit start: this head pair's weights
+                    const int st = threadIdx.x - kStateWarp0 * 32;
+                    for (int i = st; i < kConvWFloats; i += kGroupWarps * 32) {
+                        const int hh2 = i / 320, rem = i % 320, cq = rem / 40, k = (rem % 40) / 8, e = rem % 8;
+                        const int ch = (cur.w.h0 + hh2) * kP + 8 * cq + e;
+                        float v;
+                        if (rem % 40 < 32)
+                            v = k < p.conv_k ? p.conv_w[(size_t)ch * p.conv_k + k] : 0.f;
+                        else
+                            v = p.conv_b ? p.conv_b[ch] : 0.f;
+                        cw[i] = v;
+                    }
+                }
+                if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)))
+                    break;
+                uint8_t *xt = smem + kOffX + s * kXStageBytes + hc * kTileBytes;
+                uint4 hal[3];
+#pragma unroll
+                for (int i = 0; i < 3; ++i) {
+                    const int rr = r0 - 3 + i;
+                    if (rr >= 0)
+                        hal[i] = *reinterpret_cast<const uint4 *>(xt + sw128(rr, c));
+                    else if (cur.k > 0)
+                        hal[i] = *reinterpret_cast<const uint4 *>(halo + (rr + 3) * 128 + 16 * c);
+                    else
+                        hal[i] = conv_input_row(p, cur.w.b, cur.t0() + rr, (cur.w.h0 + hc) * kP + 8 * c);
+                }
+                if (!(ok = group_sync(&bars[BAR_CSYNC], csync, p)))
+                    break;
+                {
+                    const float *wc = cw + (hc * 8 + c) * 40;
+                    float win[3][8];   // win[i]: the input 3 - i steps back
+#pragma unroll
+                    for (int i = 0; i < 3; ++i)
+                        bf16x8_to_f32(hal[i], win[i]);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int rr = r0 + i;
+                        uint4 *cell = reinterpret_cast<uint4 *>(xt + sw128(rr, c));
+                        const uint4 raw = *cell;
+                        if (rr >= 125)   // raw rows 125 .. 127: the next sub-chunk's halo
+                            *reinterpret_cast<uint4 *>(halo + (rr - 125) * 128 + 16 * c) = raw;
+                        float cur8[8], out[8];
+                        bf16x8_to_f32(raw, cur8);
+#pragma unroll
+                        for (int h4 = 0; h4 < 2; ++h4) {   // 4 channels at a time
+                            const float4 w0 = *reinterpret_cast<const float4 *>(wc + 4 * h4);
+                            const float4 w1 = *reinterpret_cast<const float4 *>(wc + 8 + 4 * h4);
+                            const float4 w2 = *reinterpret_cast<const float4 *>(wc + 16 + 4 * h4);
+                            const float4 w3 = *reinterpret_cast<const float4 *>(wc + 24 + 4 * h4);
+                            const float4 bq = *reinterpret_cast<const float4 *>(wc + 32 + 4 * h4);
+                            const float W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
+                            const float W2[4] = {w2.x, w2.y, w2.z, w2.w}, W3[4] = {w3.x, w3.y, w3.z, w3.w};
+                            const float Bq[4] = {bq.x, bq.y, bq.z, bq.w};
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) {
+                                const int e = 4 * h4 + u;
+                                float v = fmaf(W0[u], cur8[e], Bq[u]);
+                                v = fmaf(W1[u], win[2][e], v);
+                                v = fmaf(W2[u], win[1][e], v);
+                                v = fmaf(W3[u], win[0][e], v);
+                                out[e] = silu_bf16_out(v);
+                            }
+                        }
+                        uint4 o;
+                        o.x = pack_bf16x2(out[0], out[1]);
+                        o.y = pack_bf16x2(out[2], out[3]);
+                        o.z = pack_bf16x2(out[4], out[5]);
+                        o.w = pack_bf16x2(out[6], out[7]);
+                        *cell = o;
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            win[0][e] = win[1][e];
+                            win[1][e] = win[2][e];
+                            win[2][e] = cur8[e];
+                        }
+                    }
+                }
+                fence_proxy_async_smem();   // (the MMAs read the tile through the async proxy)
+                if (!(ok = group_sync(&bars[BAR_CSYNC], csync, p)))
+                    break;
+                warp_arrive(&bars[BAR_X_CONV]);
             }
             // ---- x <- w o x in place (row r, head hf); P <- dtot P
             if (!(ok = wait_bar(&bars[BAR_M_READY], par, p)) || !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
@@ -1428,7 +1578,9 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     const Geometry geo = geometry(a);
     Maps maps;
     const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
-    if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
+    // conv mode: x tiles come from the x channels (the first H*P) of the raw xbc rows
+    const uint64_t xrow = a.conv ? (uint64_t)a.conv_cc * 2 : HP * 2;
+    if (!make_tmap_bf16_3d(&maps.x, a.conv ? a.xbc : a.x, HP, L, (uint64_t)a.batch, xrow, xrow * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.y, a.y, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 32))
@@ -1469,11 +1621,20 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.nchains = (int)geo.nchains;
     p.hpg = a.nheads / a.ngroups;
 
-    auto kernel = a.trap ? (geo.pieces ? ssd_chunk_fused_kernel<true, true, false>
+    p.xbc = static_cast<const __nv_bfloat16 *>(a.xbc);
+    p.conv_w = a.conv_w;
+    p.conv_b = a.conv_b;
+    p.conv_state = static_cast<const __nv_bfloat16 *>(a.conv_state);
+    p.conv_k = a.conv_k;
+    p.conv_cc = a.conv_cc;
+    auto kernel = a.conv ? (geo.pieces ? ssd_chunk_fused_kernel<true, false, false, true>
+                                       : ssd_chunk_fused_kernel<false, false, false, true>)
+                : a.trap ? (geo.pieces ? ssd_chunk_fused_kernel<true, true, false>
                                        : ssd_chunk_fused_kernel<false, true, false>)
                          : (geo.pieces ? ssd_chunk_fused_kernel<true, false, false>
                                        : ssd_chunk_fused_kernel<false, false, false>);
-    auto kernel_local = ssd_chunk_fused_kernel<false, false, true>;   // split pass 1
+    auto kernel_local = a.conv ? ssd_chunk_fused_kernel<false, false, true, true>
+                               : ssd_chunk_fused_kernel<false, false, true>;   // split pass 1
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;

@@ -36,6 +36,15 @@ struct ScanArgs {
     size_t scratch_cap = 0;   // nonzero: the chunked path takes no split schedule and, when it
                               // chooses, the piece schedule (at most one state slot per SM)
                               // if the one it would choose needs more scratch than this
+    // conv mode of the chunked path: x is not an input; the kernel reads the x
+    // channels of the fused xbc [B,L,conv_cc] (bf16) and applies the causal conv1d
+    // + SiLU to them itself (weights [conv_cc, conv_k] and bias, fp32; the carried
+    // conv state [B, conv_k - 1, conv_cc] or null).  B and C are the conv's outputs.
+    bool conv = false;
+    const void *xbc = nullptr;
+    const float *conv_w = nullptr, *conv_b = nullptr;
+    const void *conv_state = nullptr;
+    int conv_k = 0, conv_cc = 0;
 };
 
 // The trapezoidal (Mamba-3 SISO) scan, after validation.  Device pointers.
@@ -77,6 +86,10 @@ struct NeighborArgs {
 };
 bool conv_supported(const NeighborArgs &a);
 cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t stream);
+// The conv over the B and C channels only (writing B, C and their part of
+// state_out), and the x channels' part of state_out (the last K-1 inputs):
+// the part of the conv that the chunked path's conv mode does not do itself.
+cudaError_t conv_bc_launch(const NeighborArgs &a, cudaStream_t stream);
 bool gnorm_supported(const NeighborArgs &a);
 cudaError_t gnorm_launch(const NeighborArgs &a, cudaStream_t stream);
 

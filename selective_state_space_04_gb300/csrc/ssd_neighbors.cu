@@ -151,6 +151,7 @@ struct ConvParams {
     void *state_out;            // [B,K-1,C] or null
     long long L;
     int Cc, HP, GN, nvec;       // nvec = C / channels per thread
+    int vbase = 0;              // first vector handled (the launch covers vbase .. nvec-1)
 };
 
 // Asynchronous 16-byte copies from global into shared memory (cp.async, L1
@@ -189,7 +190,7 @@ __global__ void __launch_bounds__(kConvThreads, 4) ssd_conv1d_silu_kernel(ConvPa
     using Vec = typename VecSel<T, V>::type;
     static_assert(V * sizeof(T) == 16, "one 16-byte vector per step");
     __shared__ uint4 ring[kConvStages * kConvThreads];
-    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    const int v = p.vbase + blockIdx.x * blockDim.x + threadIdx.x;
     if (v >= p.nvec)
         return;   // (no barrier in this kernel)
     const long long b = blockIdx.z, L = p.L;
@@ -423,6 +424,66 @@ cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t st)
                                                     : conv_launch_t<float>(a.kernel_size, cp, grid, st);
     if (e == cudaSuccess)
         note_launches(1);
+    return e;
+}
+
+// The x channels' part of the conv state after the sequence: the last K-1
+// inputs (from the carried state when the sequence is shorter than K-1 steps,
+// zero where neither has them).  Thread: one 8-channel bf16 vector of one batch row.
+__global__ void __launch_bounds__(256) ssd_conv_state_tail_kernel(const __nv_bfloat16 *xbc, const __nv_bfloat16 *state_in,
+                                                                  __nv_bfloat16 *state_out, long long L, int Cc,
+                                                                  int nvec, int K)
+{
+    const int v = blockIdx.x * blockDim.x + threadIdx.x;
+    if (v >= nvec)
+        return;
+    const long long b = blockIdx.y;
+    for (int j = 0; j < K - 1; ++j) {
+        const long long tt = L - (K - 1) + j;
+        uint4 u = make_uint4(0u, 0u, 0u, 0u);
+        if (tt >= 0)
+            u = *reinterpret_cast<const uint4 *>(xbc + ((size_t)b * L + tt) * Cc + 8 * v);
+        else if (state_in)
+            u = *reinterpret_cast<const uint4 *>(state_in + ((size_t)b * (K - 1) + (K - 1) + tt) * Cc + 8 * v);
+        *reinterpret_cast<uint4 *>(state_out + ((size_t)b * (K - 1) + j) * Cc + 8 * v) = u;
+    }
+}
+
+cudaError_t conv_bc_launch(const NeighborArgs &a, cudaStream_t st)
+{
+    if (!conv_supported(a) || a.dtype != SSD_DTYPE_BF16)
+        return cudaErrorInvalidValue;
+    ConvParams cp;
+    cp.xbc = a.xbc;
+    cp.w = a.w;
+    cp.bias = a.bias;
+    cp.state_in = a.state_in;
+    cp.x = nullptr;   // (no x channel is handled)
+    cp.B = a.B;
+    cp.C = a.C;
+    cp.state_out = a.state_out;
+    cp.L = a.seqlen;
+    cp.HP = a.nheads * a.headdim;
+    cp.GN = a.ngroups * a.dstate;
+    cp.Cc = cp.HP + 2 * cp.GN;
+    constexpr int V = conv_vec<__nv_bfloat16>();
+    cp.vbase = cp.HP / V;
+    cp.nvec = cp.Cc / V;
+    const dim3 grid((unsigned)((cp.nvec - cp.vbase + kConvThreads - 1) / kConvThreads),
+                    (unsigned)((a.seqlen + kConvTile - 1) / kConvTile), (unsigned)a.batch);
+    cudaError_t e = conv_launch_t<__nv_bfloat16>(a.kernel_size, cp, grid, st);
+    if (e != cudaSuccess)
+        return e;
+    note_launches(1);
+    if (a.state_out) {
+        const int nv = cp.HP / V;
+        ssd_conv_state_tail_kernel<<<dim3((unsigned)((nv + 255) / 256), (unsigned)a.batch), 256, 0, st>>>(
+            static_cast<const __nv_bfloat16 *>(a.xbc), static_cast<const __nv_bfloat16 *>(a.state_in),
+            static_cast<__nv_bfloat16 *>(a.state_out), a.seqlen, cp.Cc, nv, a.kernel_size);
+        e = cudaGetLastError();
+        if (e == cudaSuccess)
+            note_launches(1);
+    }
     return e;
 }
 

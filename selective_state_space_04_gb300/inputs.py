@@ -76,6 +76,9 @@ WORKLOADS = {
     # fused x | B | C channels (with a carried conv state), and the gated RMSNorm
     "conv_silu_2p7b": Workload("conv_silu_2p7b", 8, 4096, 80, 64, 128, 1, 1, "bf16", True, "conv"),
     "gnorm_2p7b": Workload("gnorm_2p7b", 8, 4096, 80, 64, 128, 1, 1, "bf16", False, "gnorm"),
+    # the conv1d + SiLU and the scan of the 2.7B layer in one call (the conv of the x
+    # channels inside the chunked scan kernel), the conv state carried in and out
+    "conv_scan_2p7b": Workload("conv_scan_2p7b", 8, 4096, 80, 64, 128, 1, 256, "bf16", True, "conv_scan"),
     # the backward of the scan on the 2.7B layer's heads, 2 sequences of 1024 steps
     # (dy drawn like x, N(0,1); d_final like the initial state, N(0, 0.1^2))
     "bwd_2p7b_2x1024": Workload("bwd_2p7b_2x1024", 2, 1024, 80, 64, 128, 1, 256, "bf16", True, "bwd"),

@@ -75,6 +75,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssd_trap_scan_fwd.argtypes = [vp] * 14 + [ctypes.POINTER(SsdDims), vp]
     lib.ssd_conv1d_silu_fwd.restype = ctypes.c_int
     lib.ssd_conv1d_silu_fwd.argtypes = [vp] * 8 + [ctypes.c_int32, ctypes.POINTER(SsdDims), vp]
+    lib.ssd_conv_scan_fwd.restype = ctypes.c_int
+    lib.ssd_conv_scan_fwd.argtypes = [vp] * 4 + [ctypes.c_int32] + [vp] * 8 + [ctypes.POINTER(SsdDims), vp]
     lib.ssd_gated_rmsnorm_fwd.restype = ctypes.c_int
     lib.ssd_gated_rmsnorm_fwd.argtypes = [vp, vp, vp, ctypes.c_float, vp, ctypes.POINTER(SsdDims), vp]
     lib.ssd_scan_bwd.restype = ctypes.c_int
@@ -373,6 +375,31 @@ def conv1d_silu_fwd(xbc, weight, bias=None, conv_state=None, *, nheads, headdim,
     _check(_lib.ssd_conv1d_silu_fwd(*(_ptr(t) for _, t in named), ctypes.c_int32(K), ctypes.byref(d),
                                     ctypes.c_void_p(st.cuda_stream)), "ssd_conv1d_silu_fwd")
     return x, B, C, conv_state_out
+
+
+def conv_scan_fwd(xbc, weight, bias, conv_state, dt_raw, dt_bias, A_log, D, init_state=None, *, nheads, headdim,
+                  ngroups, dstate, chunk=256, y=None, final_state=None, conv_state_out=None, return_final_state=True,
+                  return_conv_state=True, stream=None, path="auto", schedule="auto"):
+    """``ssd_conv_scan_fwd``: the causal conv1d + SiLU over ``xbc [B,L,C]`` and the
+    forward scan of its output, with the conv of the x channels inside the chunked
+    scan kernel.  Returns ``(y [B,L,H,P], final_state, conv_state_out)``."""
+    Bt, L, Cc = xbc.shape
+    K = weight.shape[1]
+    if y is None:
+        y = torch.empty((Bt, L, nheads, headdim), dtype=xbc.dtype, device=xbc.device)
+    if final_state is None and return_final_state:
+        final_state = torch.empty((Bt, nheads, headdim, dstate), dtype=torch.float32, device=xbc.device)
+    if conv_state_out is None and return_conv_state:
+        conv_state_out = torch.empty((Bt, K - 1, Cc), dtype=xbc.dtype, device=xbc.device)
+    named = (("xbc", xbc), ("weight", weight), ("bias", bias), ("conv_state", conv_state))
+    rest = (("dt_raw", dt_raw), ("dt_bias", dt_bias), ("A_log", A_log), ("D", D), ("init_state", init_state),
+            ("y", y), ("final_state", final_state), ("conv_state_out", conv_state_out))
+    _require_cuda(named + rest)
+    d = make_dims(Bt, L, nheads, headdim, dstate, ngroups, chunk, xbc.dtype, path, schedule)
+    st = torch.cuda.current_stream(xbc.device) if stream is None else stream
+    _check(_lib.ssd_conv_scan_fwd(*(_ptr(t) for _, t in named), ctypes.c_int32(K), *(_ptr(t) for _, t in rest),
+                                  ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)), "ssd_conv_scan_fwd")
+    return y, final_state, conv_state_out
 
 
 def gated_rmsnorm_fwd(y, z, weight, eps=1e-6, *, out=None, stream=None):

@@ -304,3 +304,29 @@ def test_complex_entry_validation_before_cuda(libssd):
     assert _complex_call(libssd, libssd.make_dims(2, 8, 4, 16, 30, 2, 1, "f32")) == 4   # N % 4 != 0
     assert _complex_call(libssd, libssd.make_dims(2, 8, 4, 16, 1024, 2, 1, "f32")) == 4  # N > 512
     assert _complex_call(libssd, libssd.make_dims(0, 8, 4, 16, 32, 2, 1, "f32")) == 0    # empty: no device access
+
+
+def _conv_scan_call(libssd, dims_, K=4, **override):
+    lib = libssd.lib()
+    base = 0x10000000
+    names = ["xbc", "w", "bias", "state", "dt_raw", "dt_bias", "A_log", "D", "init", "y", "final", "state_out"]
+    ptrs = {n: ctypes.c_void_p(base + i * 0x4000000) for i, n in enumerate(names)}
+    ptrs.update(override)
+    args = [ptrs[n] for n in names[:4]] + [ctypes.c_int32(K)] + [ptrs[n] for n in names[4:]]
+    return lib.ssd_conv_scan_fwd(*args, ctypes.byref(dims_), None)
+
+
+def test_conv_scan_entry_validation_before_cuda(libssd):
+    d = libssd.make_dims(2, 64, 4, 64, 128, 1, 64, "bf16")
+    assert _conv_scan_call(libssd, d, xbc=None) == 2                                   # SSD_ERR_NULL_PTR
+    assert _conv_scan_call(libssd, d, w=ctypes.c_void_p(0x30000008)) == 3             # SSD_ERR_MISALIGNED
+    assert _conv_scan_call(libssd, d, y=ctypes.c_void_p(0x10000000 + 0x100)) == 7     # y inside xbc
+    assert _conv_scan_call(libssd, d, state_out=ctypes.c_void_p(0x10000000 + 3 * 0x4000000)) == 7   # = conv_state
+    assert _conv_scan_call(libssd, d, K=5) == 1                                       # kernel size 2..4
+    assert _conv_scan_call(libssd, d, K=1) == 1
+    assert _conv_scan_call(libssd, libssd.make_dims(2, 64, 4, 64, 128, 1, 64, "f32")) == 9
+    assert _conv_scan_call(libssd, libssd.make_dims(2, 64, 4, 64, 128, 1, 64, "bf16", path="sequential")) == 4
+    d = libssd.make_dims(2, 64, 4, 64, 128, 1, 64, "bf16")
+    d.flags = libssd.DIAG_STALL_HANDOFF
+    assert _conv_scan_call(libssd, d) == 1
+    assert _conv_scan_call(libssd, libssd.make_dims(0, 64, 4, 64, 128, 1, 64, "bf16")) == 0   # empty: no device access
