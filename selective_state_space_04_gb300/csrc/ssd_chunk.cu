@@ -121,8 +121,7 @@ enum {
     BAR_EPI_DONE,
     BAR_DRAIN,
     BAR_MSYNC,   // decay-group barrier (bounded, unlike bar.sync)
-    BAR_X_CONV,  // conv mode: the state group has applied the conv to x(j)
-    BAR_CSYNC,   // conv mode: state-group barrier (bounded)
+    BAR_CSYNC,   // conv mode: decay-group barrier around the conv (bounded)
 };
 
 struct ChunkParams {
@@ -403,27 +402,25 @@ __device__ __forceinline__ float silu_bf16_out(float v)
     return fmaf(h, t, h);
 }
 
-// conv mode: 8 channels (16 bytes) of the raw input at step t of batch row b,
-// channels ch .. ch+7 of xbc: from xbc for t >= 0, else from the carried conv
+// conv mode: 4 channels (8 bytes) of the raw input at step t of batch row b,
+// channels ch .. ch+3 of xbc: from xbc for t >= 0, else from the carried conv
 // state (its row K-1+t), zero where neither has it
-__device__ __forceinline__ uint4 conv_input_row(const ChunkParams &p, int b, long long t, int ch)
+__device__ __forceinline__ uint2 conv_input_row4(const ChunkParams &p, int b, long long t, int ch)
 {
     if (t >= 0)
-        return __ldg(reinterpret_cast<const uint4 *>(p.xbc + ((size_t)b * p.L + t) * p.conv_cc + ch));
+        return __ldg(reinterpret_cast<const uint2 *>(p.xbc + ((size_t)b * p.L + t) * p.conv_cc + ch));
     const long long rs = p.conv_k - 1 + t;
     if (p.conv_state && rs >= 0)
-        return __ldg(reinterpret_cast<const uint4 *>(p.conv_state + ((size_t)b * (p.conv_k - 1) + rs) * p.conv_cc + ch));
-    return make_uint4(0u, 0u, 0u, 0u);
+        return __ldg(reinterpret_cast<const uint2 *>(p.conv_state + ((size_t)b * (p.conv_k - 1) + rs) * p.conv_cc + ch));
+    return make_uint2(0u, 0u);
 }
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8])
+__device__ __forceinline__ void bf16x4_to_f32(const uint2 &u, float (&f)[4])
 {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+    f[0] = __uint_as_float(u.x << 16);
+    f[1] = __uint_as_float(u.x & 0xffff0000u);
+    f[2] = __uint_as_float(u.y << 16);
+    f[3] = __uint_as_float(u.y & 0xffff0000u);
 }
 
 __device__ __forceinline__ float softplus_f32(float z)
@@ -571,6 +568,98 @@ __device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, co
 // decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
 // alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
 // (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
+// conv mode: the causal conv1d + SiLU over the x tile of sub-chunk jj (cursor
+// cur), in place: raw xbc x channels in, the scan's x out.  Run by the 8 warps of
+// the decay group (g: the warp's index in it; csync: the phase of its barrier).
+// Warp g takes head g >> 2 and rows 32 (g & 3) .. +31; lane l takes 4 channels,
+// half (l >> 3) & 1 of the 16-byte chunk l & 7, of the 16 rows from 16 (l >> 4)
+// on.  The 16 lanes on one row then cover its 128 bytes once (8-byte accesses
+// without bank conflicts), and a lane's 4 taps and bias stay in registers for all
+// its rows.  The 3 rows before a lane's first row are read before anyone writes;
+// the raw rows 125 .. 127 become the next sub-chunk's halo.  At a unit start the
+// weights of the unit's head pair are staged first.  False on abort or timeout.
+__device__ __forceinline__ bool conv_x_tile(uint8_t *smem, uint64_t *bars, const ChunkParams &p, const Cursor &cur,
+                                            uint32_t jj, int g, int lane, uint32_t &csync)
+{
+    const int s = jj & 1;
+    const int hc = g >> 2, c = lane & 7, h4 = (lane >> 3) & 1;
+    const int r0 = 32 * (g & 3) + 16 * (lane >> 4);
+    float *cw = reinterpret_cast<float *>(smem + kOffConvW);
+    uint8_t *halo = smem + kOffHalo + hc * (3 * 128) + 16 * c + 8 * h4;
+    if (cur.k == 0) {   // unit start: this head pair's weights
+        for (int i = g * 32 + lane; i < kConvWFloats; i += kGroupWarps * 32) {
+            const int hh2 = i / 320, rem = i % 320, cq = rem / 40, k = (rem % 40) / 8, e = rem % 8;
+            const int ch = (cur.w.h0 + hh2) * kP + 8 * cq + e;
+            float v;
+            if (rem % 40 < 32)
+                v = k < p.conv_k ? p.conv_w[(size_t)ch * p.conv_k + k] : 0.f;
+            else
+                v = p.conv_b ? p.conv_b[ch] : 0.f;
+            cw[i] = v;
+        }
+    }
+    if (!wait_bar(&bars[BAR_X_FULL + s], (jj >> 1) & 1, p))
+        return false;
+    uint8_t *xt = smem + kOffX + s * kXStageBytes + hc * kTileBytes + 8 * h4;
+    uint2 hal[3];
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+        const int rr = r0 - 3 + i;
+        if (rr >= 0)
+            hal[i] = *reinterpret_cast<const uint2 *>(xt + sw128(rr, c));
+        else if (cur.k > 0)
+            hal[i] = *reinterpret_cast<const uint2 *>(halo + (rr + 3) * 128);
+        else
+            hal[i] = conv_input_row4(p, cur.w.b, cur.t0() + rr, (cur.w.h0 + hc) * kP + 8 * c + 4 * h4);
+    }
+    if (!group_sync(&bars[BAR_CSYNC], csync, p))
+        return false;
+    {
+        // (the group barrier's arrive releases and its wait acquires the weights)
+        const float *wc = cw + (hc * 8 + c) * 40 + 4 * h4;
+        const float4 w0 = *reinterpret_cast<const float4 *>(wc);
+        const float4 w1 = *reinterpret_cast<const float4 *>(wc + 8);
+        const float4 w2 = *reinterpret_cast<const float4 *>(wc + 16);
+        const float4 w3 = *reinterpret_cast<const float4 *>(wc + 24);
+        const float4 bq = *reinterpret_cast<const float4 *>(wc + 32);
+        const float W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
+        const float W2[4] = {w2.x, w2.y, w2.z, w2.w}, W3[4] = {w3.x, w3.y, w3.z, w3.w};
+        const float Bq[4] = {bq.x, bq.y, bq.z, bq.w};
+        float win[3][4];   // win[i]: the input 3 - i steps back
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            bf16x4_to_f32(hal[i], win[i]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int rr = r0 + i;
+            uint2 *cell = reinterpret_cast<uint2 *>(xt + sw128(rr, c));
+            const uint2 raw = *cell;
+            if (rr >= 125)   // raw rows 125 .. 127: the next sub-chunk's halo
+                *reinterpret_cast<uint2 *>(halo + (rr - 125) * 128) = raw;
+            float cur4[4], out[4];
+            bf16x4_to_f32(raw, cur4);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float v = fmaf(W0[u], cur4[u], Bq[u]);
+                v = fmaf(W1[u], win[2][u], v);
+                v = fmaf(W2[u], win[1][u], v);
+                v = fmaf(W3[u], win[0][u], v);
+                out[u] = silu_bf16_out(v);
+            }
+            *cell = make_uint2(pack_bf16x2(out[0], out[1]), pack_bf16x2(out[2], out[3]));
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                win[0][u] = win[1][u];
+                win[1][u] = win[2][u];
+                win[2][u] = cur4[u];
+            }
+        }
+    }
+    fence_proxy_async_smem();   // (the MMAs read the tile through the async proxy)
+    // the halo rows and every read of this tile's rows are done before the next tile
+    return group_sync(&bars[BAR_CSYNC], csync, p);
+}
+
 template <bool kPieces, bool kTrap, bool kLocal, bool kConv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
@@ -614,7 +703,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars[BAR_EPI_DONE], kGroupWarps);
         mbar_init(&bars[BAR_DRAIN], 1);
         mbar_init(&bars[BAR_MSYNC], kGroupWarps);
-        mbar_init(&bars[BAR_X_CONV], kGroupWarps);
         mbar_init(&bars[BAR_CSYNC], kGroupWarps);
         fence_mbar_init();
     }
@@ -729,12 +817,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t cA = bc, bB = bc + 2 * kTileBytes;
                 const uint32_t xs = smem_u32(smem + kOffX + s * kXStageBytes);
                 const uint32_t pb = smem_u32(smem + kOffX + (s ^ 1) * kXStageBytes);
+                auto issue_Yoff = [&]() {
+                    tc_fence_after();
+                    for (int kk = 0; with_y && kk < 8; ++kk) {
+                        const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
+                        mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024), sdesc_sw128(pb + kk * 2048, kTileBytes, 1024),
+                               id_Yoff, kk > 0);
+                    }
+                    mma_commit(&bars[BAR_YOFF_DONE]);
+                    if constexpr (!kLocal)
+                        mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
+                };
+                // Bounded poll loop: calls step(progressed) until it returns true, sleeping
+                // after the calls that issued nothing; false on abort or timeout
+                auto poll = [&](auto &&step) -> bool {
+                    const uint64_t tw = globaltimer_ns();
+                    uint32_t spins = 0;
+                    for (;;) {
+                        bool progressed = false;
+                        if (step(progressed))
+                            return true;
+                        if (progressed)
+                            continue;
+                        __nanosleep(32);
+                        if ((++spins & 255u) == 0) {
+                            if (aborted(p))
+                                return false;
+                            if (globaltimer_ns() - tw > p.timeout_ns) {
+                                raise_timeout(p);
+                                return false;
+                            }
+                        }
+                    }
+                };
+                bool yo_done = false;
                 // Y_diag[h] = M[h] x[h]
-                if (!(ok = kConv ? wait_bar(&bars[BAR_X_CONV], par, p)
-                                 : wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)) ||
-                    !(ok = wait_bar(&bars[BAR_M_READY], par, p)) ||
-                    (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p))))
+                if (j >= 1 && !(ok = wait_bar(&bars[BAR_EPI_DONE], (j - 1) & 1, p)))
                     break;
+                if constexpr (kConv) {
+                    // conv mode: Y_off(j) goes ahead of Y_diag(j) when its operand is ready
+                    // first.  The x stage it frees then takes the next raw tile, which the
+                    // decay group convolves once it has published M(j).
+                    // (M_READY(j) also says that the decay group has convolved x(j))
+                    if (!(ok = poll([&](bool &progressed) {
+                              if (!yo_done && mbar_poll(&bars[BAR_PB_READY], par)) {
+                                  issue_Yoff();
+                                  yo_done = progressed = true;
+                              }
+                              return mbar_poll(&bars[BAR_M_READY], par);
+                          })))
+                        break;
+                } else if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)) ||
+                           !(ok = wait_bar(&bars[BAR_M_READY], par, p))) {
+                    break;
+                }
                 tc_fence_after();
                 for (int h = 0; with_y && h < 2; ++h)
                     for (int kk = 0; kk < 8; ++kk)
@@ -745,48 +881,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // M once Y_diag has read it: whichever is ready first goes first, S first
                 // when both are (the next M build waits on it)
                 {
-                    bool yo_done = false, s_done = !has_next;
-                    const uint64_t tw = globaltimer_ns();
-                    uint32_t spins = 0;
-                    while (!(yo_done && s_done)) {
-                        bool progressed = false;
-                        // (split pass 1 has no S, so no wait for the next B/C tile here: the
-                        // state MMA waits for its own tile instead, and two loads stay in flight)
-                        if (!s_done &&
-                            (!with_y || mbar_poll(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1)) &&
-                            mbar_poll(&bars[BAR_YD_DONE], par)) {
-                            tc_fence_after();
-                            issue_S(s ^ 1);
-                            s_done = progressed = true;
-                        }
-                        if (!yo_done && mbar_poll(&bars[BAR_PB_READY], par)) {
-                            tc_fence_after();
-                            for (int kk = 0; with_y && kk < 8; ++kk) {
-                                const uint32_t ko = (kk >> 2) * kTileBytes + (kk & 3) * 32;
-                                mma_ss(tmem + kColYo, sdesc_sw128(cA + ko, 16, 1024),
-                                       sdesc_sw128(pb + kk * 2048, kTileBytes, 1024), id_Yoff, kk > 0);
-                            }
-                            mma_commit(&bars[BAR_YOFF_DONE]);
-                            if constexpr (!kLocal)
-                                mma_commit(&bars[BAR_X_EMPTY + (s ^ 1)]);
-                            yo_done = progressed = true;
-                        }
-                        if (!progressed) {
-                            __nanosleep(32);
-                            if ((++spins & 255u) == 0) {
-                                if (aborted(p)) {
-                                    ok = false;
-                                    break;
-                                }
-                                if (globaltimer_ns() - tw > p.timeout_ns) {
-                                    raise_timeout(p);
-                                    ok = false;
-                                    break;
-                                }
-                            }
-                        }
-                    }
-                    if (!ok)
+                    bool s_done = !has_next;
+                    if (!(ok = poll([&](bool &progressed) {
+                              // (split pass 1 has no S, so no wait for the next B/C tile here: the
+                              // state MMA waits for its own tile instead, and two loads stay in flight)
+                              if (!s_done &&
+                                  (!with_y || mbar_poll(&bars[BAR_BC_FULL + (s ^ 1)], ((j + 1) >> 1) & 1)) &&
+                                  mbar_poll(&bars[BAR_YD_DONE], par)) {
+                                  tc_fence_after();
+                                  issue_S(s ^ 1);
+                                  s_done = progressed = true;
+                              }
+                              if (!yo_done && mbar_poll(&bars[BAR_PB_READY], par)) {
+                                  issue_Yoff();
+                                  yo_done = progressed = true;
+                              }
+                              return yo_done && s_done;
+                          })))
                         break;
                 }
                 // P += B^T (w o x)   (P already rescaled by the state group)
@@ -815,12 +926,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ decay group
         // per sub-chunk j: dt and the local cumulative sum of dt*A (thread: step r,
         // head hd), decay factors for both groups, then M from S (thread: row r,
-        // both heads)
+        // both heads).  Conv mode: once M(j) is published the group computes the
+        // decay factors of sub-chunk j+1 and applies the conv to x(j+1), so that
+        // M_READY(j+1) also says that x(j+1) holds the scan's input.
         const int q = warp & 3;        // TMEM lane quarter
         const int hd = warp >> 2;      // head (decay) / column-group parity (M)
         const int r = q * 32 + lane;
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
-        uint32_t msync = 0;
+        uint32_t msync = 0, csync = 0;
         Cursor cur;
         bool has = cursor_first<kPieces>(cur, p);
         float dt_raw = 0.f;
@@ -831,32 +944,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             else
                 dt_raw = __ldg(p.dt_raw + ((size_t)cur.w.b * p.L + cur.t0() + r) * p.H + cur.w.h0 + hd);
         }
-        for (uint32_t j = 0; has; ++j) {
-            Cursor nxt = cur;
-            const bool has_next = cursor_next<kPieces>(nxt, p);
-            float dt_next = 0.f;   // issued one sub-chunk ahead
-            float tn[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-            if (has_next && r < nxt.valid()) {
-                if constexpr (kTrap)
-                    load_trap_tok(nxt, r, hd, p, tn);
-                else
-                    dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
-            }
-            const int hh = cur.w.h0 + hd;
-            float *dk = decay_base + (j % 3) * kDecayFloats;
-            float *cs2 = dk, *dtv = dk + 2 * kT, *colf = dk + 4 * kT, *ecs = dk + 6 * kT,
-                  *wsc = dk + 8 * kT, *dtot = dk + 10 * kT;
+        // decay factors of sub-chunk jj (cursor c; dt_raw dr, trapezoidal tokens tv) into
+        // buffer jj % 3; false on abort or timeout
+        auto prep = [&](const Cursor &c, uint32_t jj, float dr, const float (&tv)[5]) -> bool {
+            const int hh = c.w.h0 + hd;
+            float *dk = decay_base + (jj % 3) * kDecayFloats;
+            float *cs2 = dk, *dtv = dk + 2 * kT, *colf = dk + 4 * kT, *ecs = dk + 6 * kT, *wsc = dk + 8 * kT,
+                  *dtot = dk + 10 * kT;
             // log2 decay l and input weight wgt of this step; dcv: diagonal weight minus wgt
             float l, wgt, dcv = 0.f;
             if constexpr (kTrap) {
-                const float carried = tq[3] * (1.f - tq[4]);   // dt_{t+1} (1 - trap_{t+1})
-                l = tq[1] * tq[0] * 1.4426950408889634f;
-                wgt = fmaf(tq[2], tq[0], carried);
+                const float carried = tv[3] * (1.f - tv[4]);   // dt_{t+1} (1 - trap_{t+1})
+                l = tv[1] * tv[0] * 1.4426950408889634f;
+                wgt = fmaf(tv[2], tv[0], carried);
                 dcv = -carried;
             } else {
                 float dt = 0.f;
-                if (r < cur.valid())
-                    dt = softplus_f32(dt_raw + hBias[hh]);
+                if (r < c.valid())
+                    dt = softplus_f32(dr + hBias[hh]);
                 l = dt * hA2[hh];
                 wgt = dt;
             }
@@ -869,7 +974,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 31)
                 wsum[hd * 4 + q] = l;
             if (!group_sync(&bars[BAR_MSYNC], msync, p))
-                break;
+                return false;
             float pre = 0.f, tot = 0.f;
 #pragma unroll
             for (int qq = 0; qq < 4; ++qq) {
@@ -888,8 +993,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 dk[10 * kT + 4 + hd * kT + r] = dcv;
             if (r == 0)
                 dtot[hd] = ex2_approx(tot);                   // state decay over the sub-chunk
-            if (!group_sync(&bars[BAR_MSYNC], msync, p))
-                break;
+            return group_sync(&bars[BAR_MSYNC], msync, p);
+        };
+        if constexpr (kConv) {
+            if (has && !(prep(cur, 0, dt_raw, tq) && conv_x_tile(smem, bars, p, cur, 0, warp, lane, csync)))
+                has = false;
+        }
+        for (uint32_t j = 0; has; ++j) {
+            Cursor nxt = cur;
+            const bool has_next = cursor_next<kPieces>(nxt, p);
+            float dt_next = 0.f;   // issued one sub-chunk ahead
+            float tn[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+            if (has_next && r < nxt.valid()) {
+                if constexpr (kTrap)
+                    load_trap_tok(nxt, r, hd, p, tn);
+                else
+                    dt_next = __ldg(p.dt_raw + ((size_t)nxt.w.b * p.L + nxt.t0() + r) * p.H + nxt.w.h0 + hd);
+            }
+            if constexpr (!kConv) {
+                if (!prep(cur, j, dt_raw, tq))
+                    break;
+            }
+            float *dk = decay_base + (j % 3) * kDecayFloats;
+            const float *cs2 = dk, *dtv = dk + 2 * kT, *colf = dk + 4 * kT;
             // ---- M from S, in place, 16 columns at a time (row r, both heads).  The
             //      rows 32q .. 32q+31 of this lane quarter lie below every column
             //      group G < 2q, hold the diagonal in G = 2q, 2q+1 and lie above
@@ -942,6 +1068,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j >= 1 && !wait_bar(&bars[BAR_XS_READY], (j - 1) & 1, p))
                 break;
             warp_arrive(&bars[BAR_M_READY]);
+            if constexpr (kConv) {
+                if (has_next && !(prep(nxt, j + 1, dt_next, tn) &&
+                                  conv_x_tile(smem, bars, p, nxt, j + 1, warp, lane, csync)))
+                    break;
+            }
             cur = nxt;
             has = has_next;
             dt_raw = dt_next;
@@ -961,7 +1092,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_addr = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t ta = tmem + lane_addr + kColP + hf * 64;
         float unit_decay = 1.f;
-        uint32_t csync = 0;   // conv mode: phase of the state-group barrier
         bool ok = true;
         Cursor cur;
         bool has = cursor_first<kPieces>(cur, p);
@@ -1061,101 +1191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 warp_arrive(&bars[BAR_PB_READY]);
             }
-            if constexpr (kConv) {
-                // ---- causal conv1d + SiLU over the x tile of sub-chunk j, in place (raw xbc
-                //      x channels in, the scan's x out).  Warp sw takes head sw >> 2 and the row
-                //      segments 4 (sw & 3) .. +3 of 8 rows; lane l takes the 8-channel chunk
-                //      l & 7 of segment 4 (sw & 3) + (l >> 3), so that the 8 lanes on one row
-                //      cover its 8 chunks, which the 128-byte swizzle puts in 8 distinct bank
-                //      groups.  The 3 rows before a lane's first row are read before anyone
-                //      writes; the raw rows 125 .. 127 become the next sub-chunk's halo.  The
-                //      weights are read from shared memory row by row.
-                const int hc = sw >> 2, c = lane & 7, r0 = 8 * (4 * (sw & 3) + (lane >> 3));
-                float *cw = reinterpret_cast<float *>(smem + kOffConvW);
-                uint8_t *halo = smem + kOffHalo + hc * (3 * 128);
-                if (cur.k == 0) {   // unit start: this head pair's weights
-                    const int st = threadIdx.x - kStateWarp0 * 32;
-                    for (int i = st; i < kConvWFloats; i += kGroupWarps * 32) {
-                        const int hh2 = i / 320, rem = i % 320, cq = rem / 40, k = (rem % 40) / 8, e = rem % 8;
-                        const int ch = (cur.w.h0 + hh2) * kP + 8 * cq + e;
-                        float v;
-                        if (rem % 40 < 32)
-                            v = k < p.conv_k ? p.conv_w[(size_t)ch * p.conv_k + k] : 0.f;
-                        else
-                            v = p.conv_b ? p.conv_b[ch] : 0.f;
-                        cw[i] = v;
-                    }
-                }
-                if (!(ok = wait_bar(&bars[BAR_X_FULL + s], (j >> 1) & 1, p)))
-                    break;
-                uint8_t *xt = smem + kOffX + s * kXStageBytes + hc * kTileBytes;
-                uint4 hal[3];
-#pragma unroll
-                for (int i = 0; i < 3; ++i) {
-                    const int rr = r0 - 3 + i;
-                    if (rr >= 0)
-                        hal[i] = *reinterpret_cast<const uint4 *>(xt + sw128(rr, c));
-                    else if (cur.k > 0)
-                        hal[i] = *reinterpret_cast<const uint4 *>(halo + (rr + 3) * 128 + 16 * c);
-                    else
-                        hal[i] = conv_input_row(p, cur.w.b, cur.t0() + rr, (cur.w.h0 + hc) * kP + 8 * c);
-                }
-                if (!(ok = group_sync(&bars[BAR_CSYNC], csync, p)))
-                    break;
-                {
-                    const float *wc = cw + (hc * 8 + c) * 40;
-                    float win[3][8];   // win[i]: the input 3 - i steps back
-#pragma unroll
-                    for (int i = 0; i < 3; ++i)
-                        bf16x8_to_f32(hal[i], win[i]);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int rr = r0 + i;
-                        uint4 *cell = reinterpret_cast<uint4 *>(xt + sw128(rr, c));
-                        const uint4 raw = *cell;
-                        if (rr >= 125)   // raw rows 125 .. 127: the next sub-chunk's halo
-                            *reinterpret_cast<uint4 *>(halo + (rr - 125) * 128 + 16 * c) = raw;
-                        float cur8[8], out[8];
-                        bf16x8_to_f32(raw, cur8);
-#pragma unroll
-                        for (int h4 = 0; h4 < 2; ++h4) {   // 4 channels at a time
-                            const float4 w0 = *reinterpret_cast<const float4 *>(wc + 4 * h4);
-                            const float4 w1 = *reinterpret_cast<const float4 *>(wc + 8 + 4 * h4);
-                            const float4 w2 = *reinterpret_cast<const float4 *>(wc + 16 + 4 * h4);
-                            const float4 w3 = *reinterpret_cast<const float4 *>(wc + 24 + 4 * h4);
-                            const float4 bq = *reinterpret_cast<const float4 *>(wc + 32 + 4 * h4);
-                            const float W0[4] = {w0.x, w0.y, w0.z, w0.w}, W1[4] = {w1.x, w1.y, w1.z, w1.w};
-                            const float W2[4] = {w2.x, w2.y, w2.z, w2.w}, W3[4] = {w3.x, w3.y, w3.z, w3.w};
-                            const float Bq[4] = {bq.x, bq.y, bq.z, bq.w};
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) {
-                                const int e = 4 * h4 + u;
-                                float v = fmaf(W0[u], cur8[e], Bq[u]);
-                                v = fmaf(W1[u], win[2][e], v);
-                                v = fmaf(W2[u], win[1][e], v);
-                                v = fmaf(W3[u], win[0][e], v);
-                                out[e] = silu_bf16_out(v);
-                            }
-                        }
-                        uint4 o;
-                        o.x = pack_bf16x2(out[0], out[1]);
-                        o.y = pack_bf16x2(out[2], out[3]);
-                        o.z = pack_bf16x2(out[4], out[5]);
-                        o.w = pack_bf16x2(out[6], out[7]);
-                        *cell = o;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            win[0][e] = win[1][e];
-                            win[1][e] = win[2][e];
-                            win[2][e] = cur8[e];
-                        }
-                    }
-                }
-                fence_proxy_async_smem();   // (the MMAs read the tile through the async proxy)
-                if (!(ok = group_sync(&bars[BAR_CSYNC], csync, p)))
-                    break;
-                warp_arrive(&bars[BAR_X_CONV]);
-            }
             // ---- x <- w o x in place (row r, head hf); P <- dtot P
             if (!(ok = wait_bar(&bars[BAR_M_READY], par, p)) || !(ok = wait_bar(&bars[BAR_YD_DONE], par, p)))
                 break;
@@ -1173,32 +1208,42 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t w2 = pack_bf16x2(wsc, wsc);
                 const float Dh = hD[hh];
                 // The skip term D x goes into the fp32 Y_diag accumulator from the row of x
-                // as loaded (before it is scaled), half a row (32 channels) at a time; then
-                // the row is scaled in place for the state MMA.  Chunks are visited in
-                // swizzled order: 8 consecutive rows hit 8 distinct banks.
+                // as loaded (before it is scaled), half a row (32 channels, one TMEM round
+                // trip) at a time; then the row is scaled in place for the state MMA.  Chunks
+                // are visited in swizzled order: 8 consecutive rows hit 8 distinct banks.
 #pragma unroll 1
-                for (int c8 = 0; c8 < 8; ++c8) {   // one 16-byte chunk (8 channels) at a time
-                    const int cc = c8 ^ (r & 7);
-                    uint4 v4 = *reinterpret_cast<uint4 *>(xrow + cc * 16);
+                for (int hx = 0; hx < 2; ++hx) {
+                    uint4 v4[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v4[i] = *reinterpret_cast<const uint4 *>(xrow + ((4 * hx + i) ^ (r & 7)) * 16);
                     if constexpr (!kLocal) {
-                        const uint32_t tcol = tmem + lane_addr + kColYd + hf * 64 + 8 * c8;
-                        uint32_t yd[8];
-                        tmem_ld8(tcol, yd);
-                        const uint32_t xw[4] = {v4.x, v4.y, v4.z, v4.w};
+                        const uint32_t tcol = tmem + lane_addr + kColYd + hf * 64 + 32 * hx;
+                        uint32_t yd[32];
+                        tmem_ld32(tcol, yd);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float lo = __uint_as_float(xw[e] << 16), hi = __uint_as_float(xw[e] & 0xffff0000u);
-                            yd[2 * e] = __float_as_uint(fmaf(Dh, lo, __uint_as_float(yd[2 * e])));
-                            yd[2 * e + 1] = __float_as_uint(fmaf(Dh, hi, __uint_as_float(yd[2 * e + 1])));
+                        for (int i = 0; i < 4; ++i) {
+                            const uint32_t xw[4] = {v4[i].x, v4[i].y, v4[i].z, v4[i].w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float lo = __uint_as_float(xw[e] << 16), hi = __uint_as_float(xw[e] & 0xffff0000u);
+                                yd[8 * i + 2 * e] = __float_as_uint(fmaf(Dh, lo, __uint_as_float(yd[8 * i + 2 * e])));
+                                yd[8 * i + 2 * e + 1] =
+                                    __float_as_uint(fmaf(Dh, hi, __uint_as_float(yd[8 * i + 2 * e + 1])));
+                            }
                         }
-                        tmem_st8(tcol, yd);
+                        tmem_st32(tcol, yd);
                     }
-                    v4.x = mul_bf16x2(v4.x, w2);
-                    v4.y = mul_bf16x2(v4.y, w2);
-                    v4.z = mul_bf16x2(v4.z, w2);
-                    v4.w = mul_bf16x2(v4.w, w2);
-                    *reinterpret_cast<uint4 *>(xrow + cc * 16) = v4;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        uint4 o = v4[i];
+                        o.x = mul_bf16x2(o.x, w2);
+                        o.y = mul_bf16x2(o.y, w2);
+                        o.z = mul_bf16x2(o.z, w2);
+                        o.w = mul_bf16x2(o.w, w2);
+                        *reinterpret_cast<uint4 *>(xrow + ((4 * hx + i) ^ (r & 7)) * 16) = o;
+                    }
                 }
                 for (int half = 0; half < 2; ++half) {
                     uint32_t v[32];
