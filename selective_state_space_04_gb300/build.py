@@ -36,19 +36,39 @@ def _inputs():
     return files
 
 
-def is_stale() -> bool:
+FLAGS_STAMP = os.path.join(BUILD_DIR, "flags")
+
+
+def option_flags() -> list:
+    """Compile-time options chosen by the environment: SSD_NVTX=1 compiles in the
+    NVTX ranges around every entry point and launch function."""
+    return ["-DSSD_NVTX"] if os.environ.get("SSD_NVTX") == "1" else []
+
+
+def _stamp(flags) -> str:
+    return " ".join(flags)
+
+
+def is_stale(flags=()) -> bool:
     if not os.path.exists(LIB_PATH):
+        return True
+    try:
+        with open(FLAGS_STAMP) as f:
+            if f.read() != _stamp(flags):
+                return True
+    except OSError:
         return True
     t = os.path.getmtime(LIB_PATH)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and not is_stale():
+    flags = [*option_flags(), *extra_flags]
+    if not force and not is_stale(flags):
         return LIB_PATH
     os.makedirs(BUILD_DIR, exist_ok=True)
     common = [*ARCH, "-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
-              "-I", INCLUDE, "-I", CSRC, *extra_flags]
+              "-I", INCLUDE, "-I", CSRC, *flags]
     procs = []
     objs = []
     for src in SOURCES:
@@ -71,6 +91,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     tmp = LIB_PATH + f".tmp{os.getpid()}"
     subprocess.run([nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
     os.replace(tmp, LIB_PATH)
+    with open(FLAGS_STAMP, "w") as f:
+        f.write(_stamp(flags))
     return LIB_PATH
 
 

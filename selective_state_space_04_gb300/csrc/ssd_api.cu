@@ -361,6 +361,7 @@ ssd_status_t ssd_scan_fwd(const void *x, const float *dt_raw, const float *dt_bi
                           const float *init_state, void *y, float *final_state,
                           const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_scan_fwd");
     Sizes sz;
     ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
     if (s != SSD_OK)
@@ -388,6 +389,7 @@ ssd_status_t ssd_scan_fwd_host(const void *x, const float *dt_raw, const float *
                                const float *D, const float *init_state, void *y,
                                float *final_state, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_scan_fwd_host");
     Sizes sz;
     ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
     if (s != SSD_OK)
@@ -541,6 +543,7 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
                                   const float *D, const float *init_state, void *y,
                                   float *final_state, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_scan_fwd_noalloc");
     Sizes sz;
     ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
     if (s != SSD_OK)
@@ -597,6 +600,7 @@ ssd_status_t ssd_scan_fwd_ws(const void *x, const float *dt_raw, const float *dt
                              const float *init_state, void *y, float *final_state, void *workspace,
                              uint64_t workspace_bytes, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_scan_fwd_ws");
     Sizes sz;
     ssd_status_t s = validate(x, dt_raw, dt_bias, A_log, B, C, D, init_state, y, final_state, dims, &sz);
     if (s != SSD_OK)
@@ -705,6 +709,7 @@ ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const floa
                                   const void *B, const void *C, const float *D, const float *init_state, void *y,
                                   float *final_state, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_complex_scan_fwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)
@@ -771,6 +776,7 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
                                const void *v0, void *y, float *h_final, void *k_final, void *v_final,
                                const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_trap_scan_fwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)
@@ -887,6 +893,7 @@ ssd_status_t ssd_conv1d_silu_fwd(const void *xbc, const float *weight, const flo
                                  const void *conv_state, void *x, void *B, void *C, void *conv_state_out,
                                  int32_t kernel_size, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_conv1d_silu_fwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)
@@ -956,6 +963,7 @@ ssd_status_t ssd_conv_scan_fwd(const void *xbc, const float *conv_weight, const 
                                const float *init_state, void *y, float *final_state, void *conv_state_out,
                                const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_conv_scan_fwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)
@@ -1066,6 +1074,7 @@ ssd_status_t ssd_conv_scan_fwd(const void *xbc, const float *conv_weight, const 
 ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *weight, float eps, void *out,
                                    const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_gated_rmsnorm_fwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)
@@ -1105,6 +1114,7 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
                           const float *d_final, float *dx, float *ddt_raw, float *ddt_bias, float *dA_log,
                           float *dB, float *dC, float *dD, float *d_init, const ssd_dims_t *dims, void *stream)
 {
+    SSD_NVTX_RANGE("ssd_scan_bwd");
     Sizes sz;
     ssd_status_t s = check_dims(dims, &sz);
     if (s != SSD_OK)

@@ -340,6 +340,7 @@ size_t bwd_workspace_bytes(const BwdArgs &a)
 cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const float *dC_head, const float *part,
                               int nper, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("bwd_finish_launch");
     const long long total = (long long)a.batch * a.seqlen * a.ngroups * a.dstate;
     ssd_bwd_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(dB_head, dC_head, a.dB, a.dC, total,
                                                                           a.nheads, a.ngroups, a.dstate);
@@ -353,6 +354,7 @@ cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const floa
 
 cudaError_t bwd_launch(const BwdArgs &a, void *ws, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("bwd_launch");
     if (!bwd_supported(a))
         return cudaErrorInvalidValue;
     if (a.path == SSD_PATH_CHUNKED)

@@ -808,6 +808,7 @@ size_t bwd_chunk_workspace_bytes(const BwdArgs &a)
 
 cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("bwd_chunk_launch");
     if (!bwd_chunk_supported(a))
         return cudaErrorInvalidValue;
     const size_t BH = (size_t)a.batch * a.nheads, NP = (size_t)a.headdim * a.dstate;

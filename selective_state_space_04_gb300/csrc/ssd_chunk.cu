@@ -1620,6 +1620,7 @@ size_t chunk_workspace_bytes(const ScanArgs &a) { return geometry(a).total; }
 
 ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t stream)
 {
+    SSD_NVTX_RANGE("chunk_launch");
     const Geometry geo = geometry(a);
     Maps maps;
     const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;

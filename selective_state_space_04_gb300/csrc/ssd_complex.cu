@@ -300,6 +300,7 @@ bool complex_supported(const ComplexArgs &a)
 
 cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("complex_launch");
     if (!complex_supported(a))
         return cudaErrorInvalidValue;
     CplxParams p;

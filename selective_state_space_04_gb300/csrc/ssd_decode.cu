@@ -163,6 +163,7 @@ bool decode_supported(const ScanArgs &a)
 
 cudaError_t decode_launch(const ScanArgs &a, cudaStream_t stream)
 {
+    SSD_NVTX_RANGE("decode_launch");
     if (!decode_supported(a))
         return cudaErrorInvalidValue;
     DecodeParams dp;

@@ -8,6 +8,25 @@
 
 #include "ssd.h"
 
+// NVTX ranges, compiled in with -DSSD_NVTX (the build's SSD_NVTX=1): one range per
+// call of a public entry point and one per launch function inside it, named after
+// them, so that a timeline tool shows which call and which kernel family each
+// kernel came from.  Without the flag the macro is empty.
+#ifdef SSD_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace ssd {
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+}  // namespace ssd
+#define SSD_NVTX_RANGE(name) const ::ssd::NvtxRange ssd_nvtx_range_(name)
+#else
+#define SSD_NVTX_RANGE(name) ((void)0)
+#endif
+
 namespace ssd {
 
 // Everything one scan needs, after validation.  Device pointers.

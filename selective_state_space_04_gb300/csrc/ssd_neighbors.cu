@@ -402,6 +402,7 @@ bool conv_supported(const NeighborArgs &a)
 
 cudaError_t conv_launch(const NeighborArgs &a, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("conv_launch");
     if (!conv_supported(a))
         return cudaErrorInvalidValue;
     ConvParams cp;
@@ -451,6 +452,7 @@ __global__ void __launch_bounds__(256) ssd_conv_state_tail_kernel(const __nv_bfl
 
 cudaError_t conv_bc_launch(const NeighborArgs &a, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("conv_bc_launch");
     if (!conv_supported(a) || a.dtype != SSD_DTYPE_BF16)
         return cudaErrorInvalidValue;
     ConvParams cp;
@@ -495,6 +497,7 @@ bool gnorm_supported(const NeighborArgs &a)
 
 cudaError_t gnorm_launch(const NeighborArgs &a, cudaStream_t st)
 {
+    SSD_NVTX_RANGE("gnorm_launch");
     if (!gnorm_supported(a))
         return cudaErrorInvalidValue;
     NormParams np;

@@ -403,6 +403,7 @@ bool seq_supported(int headdim, int dstate)
 
 cudaError_t seq_launch(const ScanArgs &a, cudaStream_t stream)
 {
+    SSD_NVTX_RANGE("seq_launch");
     SeqShape s;
     if (!seq_shape(a.headdim, a.dstate, &s))
         return cudaErrorInvalidValue;

@@ -383,6 +383,7 @@ bool trap_supported(const TrapArgs &a)
 
 cudaError_t trap_carry_launch(const TrapArgs &a, cudaStream_t stream)
 {
+    SSD_NVTX_RANGE("trap_carry_launch");
     if (!a.k_final && !a.v_final)
         return cudaSuccess;
     const long long grid = a.batch * (long long)a.nheads;
@@ -403,6 +404,7 @@ cudaError_t trap_carry_launch(const TrapArgs &a, cudaStream_t stream)
 
 cudaError_t trap_launch(const TrapArgs &a, cudaStream_t stream)
 {
+    SSD_NVTX_RANGE("trap_launch");
     if (!trap_supported(a))
         return cudaErrorInvalidValue;
     TrapParams tp;
