@@ -691,7 +691,7 @@ def run_gpu_trap(args, w: Workload):
 
     def step():
         ssd.ssd_trap_scan_fwd(*(d[n] for n in TRAP_KEYS), y=y, h_final=hf, k_final=kf, v_final=vf,
-                              stream=stream, path=tpath)
+                              stream=stream, path=tpath, schedule=args.schedule)
 
     for _ in range(args.warmup):
         step()
@@ -699,8 +699,10 @@ def run_gpu_trap(args, w: Workload):
     flush = flushes_l2(trap_algorithmic_bytes(w))
     total_ms, per_launch_ms, clocks, launches = timed_region(ssd, step, args.steps, stream, dev, dist,
                                                              local, flush)
-    # the chunked kernel in its trapezoidal mode takes one more launch (the carried k, v)
-    chunked = launches == 2 * args.steps
+    # the chunked kernel in its trapezoidal mode takes one more launch (the carried k,
+    # v): 2 launches per step, 4 on the split schedule; the sequential kernel takes 1
+    per_step = launches // max(1, args.steps)
+    chunked = per_step >= 2
     th = w.token_heads
     value = world * th * args.steps / (total_ms / 1e3)
 
@@ -746,7 +748,9 @@ def run_gpu_trap(args, w: Workload):
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
         "config": workload_config(w, args.seed, flush),
-        "run": {"path": "chunked" if chunked else "sequential"},
+        "run": {"path": "chunked" if chunked else "sequential",
+                "schedule": ("split" if per_step == 4 else "ranges or pieces") if chunked else "none",
+                "launches_per_step": per_step},
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_src,
                      "traffic": stored_traffic(w.name, kernel), "algorithmic_bytes_per_launch": alg_bytes,

@@ -236,10 +236,15 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
  *
  * Arguments are DEVICE pointers of the current device, owned by the caller,
  * contiguous, 16-byte aligned; dims as for ssd_scan_fwd (dtype: x, B, C, y
- * and the k/v states).  flags: a path only.  SSD_PATH_CHUNKED is the chunked
- * tcgen05 kernel in a trapezoidal mode (same limits as for ssd_scan_fwd: bf16,
+ * and the k/v states).  flags: a path and, for the chunked kernel, a schedule
+ * request as for ssd_scan_fwd.  SSD_PATH_CHUNKED is the chunked tcgen05 kernel
+ * in a trapezoidal mode (same limits and schedules as for ssd_scan_fwd: bf16,
  * P = 64, N = 128, chunk % 64 == 0, (H/G) even; scratch from the library pool;
- * one more small launch writes k_final / v_final).  SSD_PATH_SEQUENTIAL is a
+ * one more small launch writes k_final / v_final).  The mode evaluates the
+ * recurrence on the shifted state h~_t = h_t + (beta_{t+1}/alpha_{t+1})
+ * k_t v_t^T, which is linear with decay alpha_t, so the split schedule applies
+ * unchanged; its first pass starts each chain from h0 + dt_0 (1 - trap_0)
+ * k0 v0^T.  SSD_PATH_SEQUENTIAL is a
  * sequential kernel (fp32 arithmetic).  SSD_PATH_AUTO takes the chunked kernel
  * where it applies and seqlen > 1, else the sequential one.
  *   v     [B,L,H,P]   k, q [B,L,G,N]   (dtype)
@@ -257,9 +262,10 @@ ssd_status_t ssd_scan_fwd_noalloc(const void *x, const float *dt_raw, const floa
  * The sequential kernel supports N % 4 == 0, N <= 512; P <= 128 for
  * N <= 128, P <= 64 for N <= 256, P <= 32 for N <= 512; fp32 or bf16.
  * Returns SSD_OK, or an error as ssd_scan_fwd (SSD_ERR_INVALID_DIMS also for
- * flags other than a path; SSD_ERR_UNSUPPORTED for another path or an
- * unsupported shape); nothing is enqueued on error.  seqlen 0 passes the
- * states through.  Enqueues on `stream` only; never synchronises.
+ * flags other than a path or a schedule request; SSD_ERR_UNSUPPORTED for
+ * another path or an unsupported shape); nothing is enqueued on error.
+ * seqlen 0 passes the states through.  Enqueues on `stream` only; never
+ * synchronises.
  */
 ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, const float *dt,
                                const float *a, const float *trap, const float *D,

@@ -782,7 +782,7 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     if (s != SSD_OK)
         return s;
     const uint32_t path = dims->flags & SSD_PATH_MASK;
-    if ((dims->flags & ~SSD_PATH_MASK) != 0)
+    if ((dims->flags & ~(SSD_PATH_MASK | SSD_SCHEDULE_REQUEST_MASK)) != 0)
         return SSD_ERR_INVALID_DIMS;
     if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
         return SSD_ERR_UNSUPPORTED;
@@ -858,7 +858,6 @@ ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, cons
     ca.ttrap = trap;
     ca.k0 = k0;
     ca.v0 = v0;
-    ca.sched_req = 0;
     const bool chunk_ok = chunk_supported(ca) && device_is_gb300_class();
     const bool seq_ok = trap_supported(ta);
     bool chunked;

@@ -558,16 +558,6 @@ __device__ __forceinline__ void load_trap_tok(const Cursor &c, int r, int hd, co
     o[4] = more ? __ldg(p.ttrap + idx + p.H) : 1.f;
 }
 
-// kPieces: the piece schedule (else the range schedule, or a split pass).
-// kLocal: split pass 1, which computes every unit's end state from zero and
-//   nothing else (no C loads, no M, no Y MMAs, no y); only the state MMA runs.
-// kTrap: the trapezoidal (Mamba-3 SISO) recurrence
-//   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
-// (alpha = exp(a dt), beta = alpha dt (1 - trap), gamma = trap dt) evaluated as
-// this kernel's SSD recurrence on h~_t = h_t + (beta_{t+1}/alpha_{t+1}) k_t v_t^T:
-// decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
-// alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
-// (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
 // conv mode: the causal conv1d + SiLU over the x tile of sub-chunk jj (cursor
 // cur), in place: raw xbc x channels in, the scan's x out.  Run by the 8 warps of
 // the decay group (g: the warp's index in it; csync: the phase of its barrier).
@@ -660,6 +650,16 @@ __device__ __forceinline__ bool conv_x_tile(uint8_t *smem, uint64_t *bars, const
     return group_sync(&bars[BAR_CSYNC], csync, p);
 }
 
+// kPieces: the piece schedule (else the range schedule, or a split pass).
+// kLocal: split pass 1, which computes every unit's end state from zero and
+//   nothing else (no C loads, no M, no Y MMAs, no y); only the state MMA runs.
+// kTrap: the trapezoidal (Mamba-3 SISO) recurrence
+//   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
+// (alpha = exp(a dt), beta = alpha dt (1 - trap), gamma = trap dt) evaluated as
+// this kernel's SSD recurrence on h~_t = h_t + (beta_{t+1}/alpha_{t+1}) k_t v_t^T:
+// decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
+// alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
+// (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
 template <bool kPieces, bool kTrap, bool kLocal, bool kConv = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
@@ -1123,9 +1123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *pb = smem + kOffX + (s ^ 1) * kXStageBytes + hf * kTileBytes;
                 // chained: the slot the predecessor filled; split pass 3: this unit's own
                 // slot; split pass 1 starts every unit from zero (the combine adds the
-                // initial state)
+                // initial state), except in the trapezoidal mode, where it starts each
+                // chain's first unit from the chain's entering state (the initial state
+                // and the carried k0 v0^T term) and the combine starts from zero
                 // all 64 loads of the row are issued before the first use (one round trip)
                 const size_t slot_of = (size_t)unit_slot<kPieces>(cur, p);
+                const bool chain_entry = cur.first() && (kTrap || p.mode != kSplitLocal);
                 if constexpr (!kPieces) {
                     // The initial state of this CTA's next unit, when that unit starts its
                     // chain, into L2 ahead of its loads (64 KB, contiguous for the head
@@ -1153,7 +1156,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         v[i >> 3][4 * (i & 7) + 2] = __float_as_uint(f.z);
                         v[i >> 3][4 * (i & 7) + 3] = __float_as_uint(f.w);
                     }
-                } else if (p.init_state && p.mode != kSplitLocal) {
+                } else if (p.init_state && chain_entry) {
                     const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
 #pragma unroll
                     for (int i = 0; i < 64; ++i)
@@ -1166,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (kTrap) {
                     // the chain's first step also takes the carried k0 v0^T, weighted
                     // dt_0 (1 - trap_0) before the decay (see the kernel's comment)
-                    if (cur.first() && p.k0 && p.v0 && p.mode != kSplitLocal) {
+                    if (chain_entry && p.k0 && p.v0) {
                         const size_t i0 = (size_t)cur.w.b * p.L * p.H + hh;   // step 0
                         const float c = __ldg(p.tdt + i0) * (1.f - __ldg(p.ttrap + i0));
                         const float ck = c * __bfloat162float(p.k0[((size_t)cur.w.b * p.H + hh) * kN + r]);
@@ -1541,10 +1544,7 @@ Geometry geometry(const ScanArgs &a)
     if (pieces_ok && a.sched_req == SSD_SCHEDULE_PIECES)
         g.pieces = true;
     g.split = false;
-    // (the trapezoidal mode has no split schedule: its combine would need the
-    // entering-state correction too)
-    const bool split_allowed =
-        !a.trap && (a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0));
+    const bool split_allowed = a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0);
     if (split_allowed && g.nchunks > 1) {
         double best_split = 1e300;
         long long r_split = 1;
@@ -1679,8 +1679,9 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
                                        : ssd_chunk_fused_kernel<false, true, false>)
                          : (geo.pieces ? ssd_chunk_fused_kernel<true, false, false>
                                        : ssd_chunk_fused_kernel<false, false, false>);
-    auto kernel_local = a.conv ? ssd_chunk_fused_kernel<false, false, true, true>
-                               : ssd_chunk_fused_kernel<false, false, true>;   // split pass 1
+    auto kernel_local = a.conv   ? ssd_chunk_fused_kernel<false, false, true, true>
+                        : a.trap ? ssd_chunk_fused_kernel<false, true, true>
+                                 : ssd_chunk_fused_kernel<false, false, true>;   // split pass 1
     if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes) != cudaSuccess)
         return SSD_ERR_CUDA;
@@ -1710,8 +1711,10 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
         return SSD_ERR_CUDA;
     note_launches(1);
     const long long threads = geo.nchains * 2 * 16 * kN;
+    // (the trapezoidal pass 1 has put each chain's entering state into its first unit)
     ssd_split_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
-        p.slots, p.unit_decay, a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2, a.nheads);
+        p.slots, p.unit_decay, a.trap ? nullptr : a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2,
+        a.nheads);
     if (cudaGetLastError() != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);

@@ -72,6 +72,9 @@ WORKLOADS = {
     "trap_many_short_seqs": Workload("trap_many_short_seqs", 256, 64, 48, 64, 128, 1, 1, "bf16", True, "trap"),
     "trap_decode_2p7b_128seq": Workload("trap_decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 1, "bf16", True,
                                         "trap"),
+    # the trapezoidal scan over one 64k-token sequence (the long-context shape):
+    # few chains, so the chunked kernel takes its split schedule
+    "trap_long_context_64k": Workload("trap_long_context_64k", 1, 65536, 32, 64, 128, 8, 256, "bf16", True, "trap"),
     # the steps around the 2.7B layer's scan: the 4-tap conv1d + SiLU over its
     # fused x | B | C channels (with a carried conv state), and the gated RMSNorm
     "conv_silu_2p7b": Workload("conv_silu_2p7b", 8, 4096, 80, 64, 128, 1, 1, "bf16", True, "conv"),

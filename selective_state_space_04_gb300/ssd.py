@@ -289,9 +289,10 @@ def ssd_scan_fwd_ws(x, dt_raw, dt_bias, A_log, B, C, D, init_state=None, *, work
 
 
 def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, chunk=256, path="auto", y=None,
-                      h_final=None, k_final=None, v_final=None, return_states=True, stream=None):
+                      h_final=None, k_final=None, v_final=None, return_states=True, stream=None, schedule="auto"):
     """Trapezoidal (Mamba-3 SISO) scan on CUDA tensors.  Returns
     ``(y, h_final, k_final, v_final)`` (the states None when not returned).
+    ``schedule`` requests a schedule of the chunked kernel, as for ``ssd_scan_fwd``.
 
     ``v [B,L,H,P]``, ``k, q [B,L,G,N]``, ``k0/k_final [B,H,N]`` and
     ``v0/v_final [B,H,P]`` share one dtype (bf16 or fp32); ``dt, a, trap
@@ -313,7 +314,7 @@ def ssd_trap_scan_fwd(v, k, q, dt, a, trap, D, h0=None, k0=None, v0=None, *, chu
     for name, t in named:
         if t is not None and (not t.is_cuda or not t.is_contiguous()):
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
-    d = make_dims(Bt, L, H, P, N, G, chunk, v.dtype, path)
+    d = make_dims(Bt, L, H, P, N, G, chunk, v.dtype, path, schedule)
     st = torch.cuda.current_stream(v.device) if stream is None else stream
     _check(_lib.ssd_trap_scan_fwd(*(_ptr(t) for _, t in named), ctypes.byref(d),
                                   ctypes.c_void_p(st.cuda_stream)), "ssd_trap_scan_fwd")

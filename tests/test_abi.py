@@ -252,8 +252,12 @@ def test_trap_entry_validation_before_cuda(libssd):
     assert _trap_call(libssd, d, h_final=ctypes.c_void_p(0x10000000 + 7 * 0x1000000 + 0x10)) == 7
     d2 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="chunked")
     assert _trap_call(libssd, d2) == 9                                         # SSD_ERR_UNSUPPORTED_DTYPE
-    d3 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", schedule="pieces")
+    d3 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32")
+    d3.flags = 0x40                                                            # beyond the schedule field
     assert _trap_call(libssd, d3) == 1                                         # SSD_ERR_INVALID_DIMS
+    # a schedule request passes the flag check (then fp32 on the chunked kernel is refused)
+    d5 = libssd.make_dims(2, 8, 4, 16, 32, 2, 1, "f32", path="chunked", schedule="split")
+    assert _trap_call(libssd, d5) == 9
     d4 = libssd.make_dims(2, 8, 4, 16, 30, 2, 1, "f32")                        # N % 4 != 0
     assert _trap_call(libssd, d4) == 4
     # empty batch: nothing to do, no device access

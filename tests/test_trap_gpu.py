@@ -205,3 +205,76 @@ def test_bench_workloads_sampled(ssd, name, rows):
     for got, ref in ((y, ry), (h, rh)):
         assert relerr(got[:rows], ref) <= TOL[w.dtype]
     assert relerr(kf[:rows], rk) <= TOL[w.dtype] and relerr(vf[:rows], rv) <= TOL[w.dtype]
+
+
+# ------------------------------------------------ split schedule of the trapezoidal mode
+# The mode runs the recurrence on the shifted state h~ (linear, decay alpha), so
+# the split schedule's pass 1 / combine / pass 3 apply unchanged; pass 1 starts
+# each chain from h0 + dt_0 (1 - trap_0) k0 v0^T.  Weak decay makes the state
+# carried between units matter; without h0, k0, v0 the combine starts from zero.
+@pytest.mark.parametrize("B,L,H,G,init,weak", [
+    (1, 3000, 2, 1, True, True),     # many units per chain, long-range state
+    (2, 1000, 4, 2, True, False),    # ragged tail, head groups
+    (1, 700, 4, 1, False, True),     # no carried states
+    (1, 257, 2, 1, True, True),      # one step past a chunk: a one-step last unit
+])
+def test_trap_split_against_oracle(ssd, B, L, H, G, init, weak):
+    w = Workload("t", B, L, H, 64, 128, G, 256, "bf16", init, "trap")
+    inp = make_trap_inputs(w, seed=170 + L + H)
+    if weak:
+        inp = _weak(inp)
+    ry, rh, rk, rv = trap_fwd(**inp)
+    d = _dev(inp)
+    launches = ssd.launch_count()
+    y, h, k, v = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS), path="chunked", schedule="split")
+    torch.cuda.synchronize()
+    assert ssd.device_error() == 0
+    assert ssd.launch_count() - launches == 4          # pass 1, combine, pass 3, k/v carry
+    ey, eh = relerr(y, ry), relerr(h, rh)
+    print(f"trap split rel err y {ey:.3e} state {eh:.3e}")
+    assert ey <= TOL["bf16"] and eh <= TOL["bf16"]
+    assert np.array_equal(k.double().cpu().numpy(), rk) and np.array_equal(v.double().cpu().numpy(), rv)
+    if weak and init:
+        # the carried-in states matter: without them the output is far off
+        d0 = dict(d, h0=None, k0=None, v0=None)
+        y0, _, _, _ = ssd.ssd_trap_scan_fwd(*(d0[n] for n in KEYS), path="chunked", schedule="split")
+        torch.cuda.synchronize()
+        assert relerr(y0, ry) > 10 * TOL["bf16"]
+
+
+def test_trap_split_agrees_with_ranges(ssd):
+    # two schedules of the same scan: each within the bar of the oracle, and close
+    # to each other (they differ only in where the state crosses unit boundaries)
+    w = Workload("t", 2, 2000, 4, 64, 128, 1, 256, "bf16", True, "trap")
+    inp = _weak(make_trap_inputs(w, seed=180))
+    ry, rh, _, _ = trap_fwd(**inp)
+    d = _dev(inp)
+    outs = {}
+    for sched in ("split", "ranges", "pieces"):
+        outs[sched] = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS), path="chunked", schedule=sched)
+        torch.cuda.synchronize()
+        assert ssd.device_error() == 0
+        assert relerr(outs[sched][0], ry) <= TOL["bf16"] and relerr(outs[sched][1], rh) <= TOL["bf16"]
+    assert relerr(outs["split"][0], outs["ranges"][0].double().cpu().numpy()) <= TOL["bf16"]
+
+
+def test_trap_long_context_takes_split_sampled(ssd):
+    # the 64k-token bench workload on the auto path: one sequence of 8 chains, so
+    # the library chooses the split schedule (3 launches + the k/v carry); the
+    # oracle takes the 4 heads of group 0
+    w = WORKLOADS["trap_long_context_64k"]
+    inp = make_trap_inputs(w, seed=0)
+    d = _dev(inp)
+    launches = ssd.launch_count()
+    y, h, kf, vf = ssd.ssd_trap_scan_fwd(*(d[n] for n in KEYS))
+    torch.cuda.synchronize()
+    assert ssd.device_error() == 0
+    assert ssd.launch_count() - launches == 4
+    hp = w.nheads // w.ngroups
+    sub = {"v": inp["v"][:, :, :hp], "k": inp["k"][:, :, :1], "q": inp["q"][:, :, :1], "dt": inp["dt"][:, :, :hp],
+           "a": inp["a"][:, :, :hp], "trap": inp["trap"][:, :, :hp], "D": inp["D"][:hp], "h0": inp["h0"][:, :hp],
+           "k0": inp["k0"][:, :hp], "v0": inp["v0"][:, :hp]}
+    ry, rh, rk, rv = trap_fwd(**sub)
+    assert relerr(y[:, :, :hp], ry) <= TOL["bf16"] and relerr(h[:, :hp], rh) <= TOL["bf16"]
+    assert np.array_equal(kf[:, :hp].double().cpu().numpy(), rk)
+    assert np.array_equal(vf[:, :hp].double().cpu().numpy(), rv)
