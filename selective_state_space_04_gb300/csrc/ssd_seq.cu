@@ -151,34 +151,93 @@ __global__ void __launch_bounds__(512) ssd_seq_kernel(SeqParams p)
 // block of RPW = 8 / NV state rows p, lane l holding n = 4l .. 4l+3 (+128 per
 // further float4) of each row, so the state is read and written as coalesced
 // 512-byte rows and stays in registers.  Per time block (up to 64 steps) the
-// CTA stages B_t, C_t, x_t, dt_t and dA_t in shared memory; each element
-// takes dA h + (dt x) B, the decode step's operations in its order (one decode
-// step equals one step of this scan bit for bit); y_t[p] is a warp butterfly.  The step loop is unrolled so that a step's readout reduction
-// overlaps the next steps' updates, and each warp reads its rows of x_t as
-// 16-byte (8-byte) words from a stride padded to the CTA's rows.
+// CTA stages B_t and C_t as stored (bf16 stays bf16: half the shared memory, so
+// more CTAs overlap their loads with the others' steps), x_t as fp32 and dt_t,
+// dA_t, with vector copies and no index division.  Each element takes
+// dA h + (dt x) B, the decode step's operations in its order (one decode step
+// equals one step of this scan bit for bit), two elements per instruction with
+// the packed fp32 multiply and FMA; y_t[p] is a warp butterfly over the
+// per-lane readouts (each an fp32 pair, summed at the end).  The step loop is
+// unrolled so that a step's readout reduction overlaps the next steps'
+// updates, and each warp reads its rows of x_t as 16-byte (8-byte) words from a
+// stride padded to the CTA's rows.
 constexpr int kRowF4PerLane = 8;   // RPW * NV float4 of state per lane
 constexpr int kRowMaxWarps = 16;
+constexpr int kRowSmallWarps = 8;  // CTAs of up to 8 warps: 2 or 3 per SM
+// x elements a thread stages per block: steps x rows / threads <= 64 * (8 warps' RPW rows) / 32
+constexpr int kXPerThread = 64 * kRowF4PerLane / 32;
 
 struct RowParams {
     SeqParams s;
     int Pp;                         // staged x row stride (the CTA's rows)
 };
 
-template <typename T, int NV>
-__global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowParams rp)
+typedef unsigned long long f32x2;   // two fp32 lanes (lo, hi) in one 64-bit register pair
+
+__device__ __forceinline__ f32x2 pk2(float lo, float hi)
+{
+    return ((f32x2)__float_as_uint(hi) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float((unsigned)v); }
+__device__ __forceinline__ float hi2(f32x2 v) { return __uint_as_float((unsigned)(v >> 32)); }
+// elementwise a * b + c and a * b, each lane rounded as fmaf / __fmul_rn
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
+{
+    f32x2 d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
+{
+    f32x2 d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// 4 staged values of B or C as two fp32 pairs
+__device__ __forceinline__ void load4(const float *src, f32x2 (&o)[2])
+{
+    const float4 v = *reinterpret_cast<const float4 *>(src);
+    o[0] = pk2(v.x, v.y);
+    o[1] = pk2(v.z, v.w);
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16 *src, f32x2 (&o)[2])
+{
+    const uint2 v = *reinterpret_cast<const uint2 *>(src);
+    o[0] = pk2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u));
+    o[1] = pk2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+}
+// asynchronous 16- and 8-byte copies of B or C into the staging area (the
+// 16-byte ones bypass L1); completed by cp.async.wait_all
+template <typename T>
+__device__ __forceinline__ void cp_async16(T *dst, const T *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void cp_async8(T *dst, const T *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+template <typename T, int NV, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) ssd_seq_rows_kernel(RowParams rp)
 {
     constexpr int RPW = kRowF4PerLane / NV;
     const SeqParams &p = rp.s;
     extern __shared__ float sm[];
     const int P = p.P, N = p.N, H = p.H, TB = p.tblk, Pp = rp.Pp;
     const long long L = p.L;
-    float *bs = sm;                  // [TB][N]: B_t
-    float *cs = bs + TB * N;         // [TB][N]: C_t
-    float *xs = cs + TB * N;         // [TB][Pp], zero past P
+    float *xs = sm;                  // [TB][Pp], zero past P
     float *da = xs + TB * Pp;        // [TB]: dA_t
     float *ds = da + TB;             // [TB]: dt_t
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
+    T *bs = reinterpret_cast<T *>(sm + ((TB * (Pp + 2) + 3) & ~3));   // [TB][N]: B_t as stored (16-byte aligned)
+    T *cs = bs + (size_t)TB * N;     // [TB][N]: C_t
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x, nwarps = nthr >> 5;
     const long long bh = blockIdx.x;
     const long long b = bh / H;
     const int h = (int)(bh - b * H);
@@ -188,17 +247,20 @@ __global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowPara
     T *yg = static_cast<T *>(p.y);
     const size_t sbase = (size_t)bh * P * N;
     const float A = -expf(p.A_log[h]), bias = p.dt_bias[h], Dh = p.D[h];
+    const bool wide16 = (N * (int)sizeof(T)) % 16 == 0;   // staged rows in 16-byte copies
 
-    float4 hs[RPW][NV];
+    f32x2 hs[RPW][NV][2];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         const int pr = p0 + r;
 #pragma unroll
         for (int c = 0; c < NV; ++c) {
             const int n = 4 * lane + 128 * c;
-            hs[r][c] = (p.init_state && pr < P && n < N)
-                           ? __ldcs(reinterpret_cast<const float4 *>(p.init_state + sbase + (size_t)pr * N + n))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = (p.init_state && pr < P && n < N)
+                                 ? __ldcs(reinterpret_cast<const float4 *>(p.init_state + sbase + (size_t)pr * N + n))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            hs[r][c][0] = pk2(v.x, v.y);
+            hs[r][c][1] = pk2(v.z, v.w);
         }
     }
 
@@ -210,28 +272,67 @@ __global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowPara
             da[i] = expf(dt * A);
             ds[i] = dt;
         }
-        for (int i = threadIdx.x; i < nt * Pp; i += nthr) {
-            const int tt = i / Pp, pp = i - tt * Pp;
-            xs[i] = pp < P ? to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]) : 0.f;
+        // B_t and C_t by asynchronous copies (all in flight at once), x_t converted to
+        // fp32 on the way, so that a block costs few memory round trips
+        if (wide16) {   // 16-byte copies: 8 bf16 or 4 fp32 elements
+            constexpr int E = 16 / (int)sizeof(T);
+            for (int i = threadIdx.x; i < nt * (N / E); i += nthr) {
+                const int tt = i / (N / E), q = E * (i - tt * (N / E));
+                const size_t row = ((size_t)(b * L + t0 + tt) * p.G + g) * N;
+                cp_async16(bs + (size_t)tt * N + q, Bg + row + q);
+                cp_async16(cs + (size_t)tt * N + q, Cg + row + q);
+            }
+        } else {        // bf16 rows of N % 8 == 4 elements: 8-byte copies
+            for (int i = threadIdx.x; i < nt * (N / 4); i += nthr) {
+                const int tt = i / (N / 4), q = 4 * (i - tt * (N / 4));
+                const size_t row = ((size_t)(b * L + t0 + tt) * p.G + g) * N;
+                cp_async8(bs + (size_t)tt * N + q, Bg + row + q);
+                cp_async8(cs + (size_t)tt * N + q, Cg + row + q);
+            }
         }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nt * N; i += nthr) {
-            const int tt = i / N, n = i - tt * N;
-            const size_t gi = ((size_t)(b * L + t0 + tt) * p.G + g) * N + n;
-            bs[i] = to_f32<T>(Bg[gi]);
-            cs[i] = to_f32<T>(Cg[gi]);
+        if (nwarps <= 2) {
+            // few warps (small P): each thread's x loads all issued before its first store
+            float xv[kXPerThread];
+#pragma unroll
+            for (int k = 0; k < kXPerThread; ++k) {
+                const int i = threadIdx.x + k * nthr;
+                xv[k] = 0.f;
+                if (i < nt * Pp) {
+                    const int tt = i / Pp, pp = i - tt * Pp;
+                    if (pp < P)
+                        xv[k] = to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kXPerThread; ++k) {
+                const int i = threadIdx.x + k * nthr;
+                if (i < nt * Pp)
+                    xs[i] = xv[k];
+            }
+        } else {
+            // a warp per step row (measured faster than the batch above with 8 warps)
+            for (int tt = warp; tt < nt; tt += nwarps) {
+                const size_t row = (size_t)(b * L + t0 + tt);
+                for (int pp = lane; pp < Pp; pp += 32)
+                    xs[tt * Pp + pp] = pp < P ? to_f32<T>(xg[(row * H + h) * P + pp]) : 0.f;
+            }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
 #pragma unroll 4
         for (int i = 0; i < nt; ++i) {
-            const float dA = da[i], dt = ds[i];
-            float4 bt[NV], ct[NV];
+            const float dt = ds[i];
+            const f32x2 dA2 = pk2(da[i], da[i]);
+            f32x2 bt[NV][2], ct[NV][2];
 #pragma unroll
             for (int c = 0; c < NV; ++c) {
                 const int n = 4 * lane + 128 * c;
-                const bool in = n < N;   // N % 4 == 0: whole float4 chunks
-                bt[c] = in ? *reinterpret_cast<const float4 *>(bs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
-                ct[c] = in ? *reinterpret_cast<const float4 *>(cs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (n < N) {   // N % 4 == 0: whole 4-element chunks
+                    load4(bs + (size_t)i * N + n, bt[c]);
+                    load4(cs + (size_t)i * N + n, ct[c]);
+                } else {
+                    bt[c][0] = bt[c][1] = ct[c][0] = ct[c][1] = 0ull;
+                }
             }
             float acc[RPW], xr[RPW];
             if constexpr (RPW >= 4) {
@@ -251,20 +352,18 @@ __global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowPara
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
                 const float dtx = dt * xr[r];
-                float s = 0.f;
+                const f32x2 dtx2 = pk2(dtx, dtx);
+                f32x2 s = 0ull;
 #pragma unroll
                 for (int c = 0; c < NV; ++c) {
-                    float4 &z = hs[r][c];
-                    z.x = fmaf(dA, z.x, dtx * bt[c].x);
-                    z.y = fmaf(dA, z.y, dtx * bt[c].y);
-                    z.z = fmaf(dA, z.z, dtx * bt[c].z);
-                    z.w = fmaf(dA, z.w, dtx * bt[c].w);
-                    s = fmaf(ct[c].x, z.x, s);
-                    s = fmaf(ct[c].y, z.y, s);
-                    s = fmaf(ct[c].z, z.z, s);
-                    s = fmaf(ct[c].w, z.w, s);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        f32x2 &z = hs[r][c][e];
+                        z = fma2(dA2, z, mul2(dtx2, bt[c][e]));
+                        s = fma2(ct[c][e], z, s);
+                    }
                 }
-                acc[r] = s;
+                acc[r] = lo2(s) + hi2(s);
             }
             warp_sum_rows_all<RPW>(acc, lane);
             const int pr = p0 + summed_row<RPW>(lane);
@@ -281,7 +380,8 @@ __global__ void __launch_bounds__(kRowMaxWarps * 32) ssd_seq_rows_kernel(RowPara
             for (int c = 0; c < NV; ++c) {
                 const int n = 4 * lane + 128 * c;
                 if (pr < P && n < N)
-                    __stcs(reinterpret_cast<float4 *>(p.final_state + sbase + (size_t)pr * N + n), hs[r][c]);
+                    __stcs(reinterpret_cast<float4 *>(p.final_state + sbase + (size_t)pr * N + n),
+                           make_float4(lo2(hs[r][c][0]), hi2(hs[r][c][0]), lo2(hs[r][c][1]), hi2(hs[r][c][1])));
             }
         }
     }
@@ -296,10 +396,10 @@ bool rows_supported(int P, int N)
     return P <= kRowMaxWarps * (kRowF4PerLane / rows_nv(N));
 }
 
-template <typename T, int NV>
+template <typename T, int NV, int MAXT, int MINB>
 cudaError_t rows_launch_t(const RowParams &rp, int grid, int threads, size_t smem, cudaStream_t st)
 {
-    auto kern = ssd_seq_rows_kernel<T, NV>;
+    auto kern = ssd_seq_rows_kernel<T, NV, MAXT, MINB>;
     if (smem > 48 * 1024) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess)
@@ -309,23 +409,39 @@ cudaError_t rows_launch_t(const RowParams &rp, int grid, int threads, size_t sme
     return cudaGetLastError();
 }
 
+template <typename T, int MAXT, int MINB>
+cudaError_t rows_launch_nv(int nv, const RowParams &rp, int grid, int threads, size_t smem, cudaStream_t st)
+{
+    switch (nv) {
+    case 1: return rows_launch_t<T, 1, MAXT, MINB>(rp, grid, threads, smem, st);
+    case 2: return rows_launch_t<T, 2, MAXT, MINB>(rp, grid, threads, smem, st);
+    default: return rows_launch_t<T, 4, MAXT, MINB>(rp, grid, threads, smem, st);
+    }
+}
+
 template <typename T>
 cudaError_t rows_launch(const SeqParams &sp, int grid, cudaStream_t st)
 {
     const int nv = rows_nv(sp.N), rpw = kRowF4PerLane / nv;
     const int warps = (sp.P + rpw - 1) / rpw;
+    const bool small = warps <= kRowSmallWarps;   // 3 CTAs per SM
     RowParams rp;
     rp.s = sp;
     rp.Pp = warps * rpw;
-    // steps per staged block: up to 64, within about 200 KB (B, C, x, dA and a dt slot per step)
-    const long long per_step = (long long)(2 * sp.N + rp.Pp + 2) * (long long)sizeof(float);
-    rp.s.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, sp.L, (200LL << 10) / per_step}));
-    const size_t smem = (size_t)rp.s.tblk * (size_t)per_step;
-    switch (nv) {
-    case 1: return rows_launch_t<T, 1>(rp, grid, 32 * warps, smem, st);
-    case 2: return rows_launch_t<T, 2>(rp, grid, 32 * warps, smem, st);
-    default: return rows_launch_t<T, 4>(rp, grid, 32 * warps, smem, st);
-    }
+    // steps per staged block: up to 64, within a third of the SM's shared memory for
+    // the small CTAs (3 per SM) and about 200 KB otherwise (x as fp32, B and C as
+    // stored, dA and dt per step)
+    const long long per_step =
+        (long long)(rp.Pp + 2) * (long long)sizeof(float) + 2LL * sp.N * (long long)sizeof(T);
+    const long long budget = small ? (72LL << 10) : (200LL << 10);
+    rp.s.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, sp.L, (budget - 16) / per_step}));
+    const size_t smem = (size_t)rp.s.tblk * (size_t)per_step + 16;   // (+ the B_t area's alignment)
+    // (3 CTAs per SM where one float4 of each state row per lane leaves the registers
+    // for it; 2 for the wider states, which would spill at 3)
+    if (small && nv == 1)
+        return rows_launch_t<T, 1, kRowSmallWarps * 32, 3>(rp, grid, 32 * warps, smem, st);
+    return small ? rows_launch_nv<T, kRowSmallWarps * 32, 2>(nv, rp, grid, 32 * warps, smem, st)
+                 : rows_launch_nv<T, kRowMaxWarps * 32, 1>(nv, rp, grid, 32 * warps, smem, st);
 }
 
 struct SeqShape {
