@@ -1146,6 +1146,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 uint32_t v[2][32];
+                // split pass 3 is launched as a programmatic dependent of the combine:
+                // its other roles start on the inputs, and this group waits for the
+                // combined entering states here (a no-op once passed)
+                if (p.mode == kSplitEntering)
+                    asm volatile("griddepcontrol.wait;" ::: "memory");
                 if (!cur.first() && p.mode != kSplitLocal) {
                     const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
 #pragma unroll
@@ -1393,6 +1398,10 @@ __global__ void __launch_bounds__(256) ssd_split_combine_kernel(float *slots, co
                                                                 int nranges, int nhp, int H)
 {
     constexpr int kPerChain = 2 * 16 * kN;   // float4 per slot
+    // launched as a programmatic dependent of pass 1: its slots and decays are
+    // complete and visible after this wait.  (No early trigger for pass 3: its
+    // CTAs, resident beside this grid's, measured slower on the 64k sequences.)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (tid >= (long long)nchains * kPerChain)
         return;
@@ -1710,16 +1719,30 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     if (cudaLaunchKernelEx(&cfg, kernel_local, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
+    // The combine and pass 3 are programmatic dependents of the launch before them
+    // (each waits with griddepcontrol.wait before it reads what that launch wrote),
+    // so their launch and setup overlap the previous kernel's tail.
     const long long threads = geo.nchains * 2 * 16 * kN;
+    cudaLaunchConfig_t ccfg = {};
+    ccfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+    ccfg.blockDim = dim3(256);
+    ccfg.stream = stream;
+    cudaLaunchAttribute pdl[2];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    ccfg.attrs = pdl;
+    ccfg.numAttrs = 1;
     // (the trapezoidal pass 1 has put each chain's entering state into its first unit)
-    ssd_split_combine_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, stream>>>(
-        p.slots, p.unit_decay, a.trap ? nullptr : a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2,
-        a.nheads);
-    if (cudaGetLastError() != cudaSuccess)
+    if (cudaLaunchKernelEx(&ccfg, ssd_split_combine_kernel, p.slots, (const float *)p.unit_decay,
+                           a.trap ? nullptr : a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2,
+                           a.nheads) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     p.mode = kSplitEntering;
     p.epoch = next_epoch();
+    pdl[1] = attr[0];   // cooperative
+    cfg.attrs = pdl;
+    cfg.numAttrs = 2;
     if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
