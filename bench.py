@@ -79,16 +79,16 @@ def load_peaks():
 KERNEL_SOURCES = {
     "ssd_chunk_fused_kernel": ("ssd_chunk.cu", "ptx.cuh", "tmap.h"),
     "ssd_decode_kernel": ("ssd_decode.cu",),
-    "ssd_seq_kernel": ("ssd_seq.cu", "warp_rows.cuh"),
-    "ssd_seq_rows_kernel": ("ssd_seq.cu", "warp_rows.cuh"),
+    "ssd_seq_kernel": ("ssd_seq.cu", "warp_rows.cuh", "f32x2.cuh"),
+    "ssd_seq_rows_kernel": ("ssd_seq.cu", "warp_rows.cuh", "f32x2.cuh"),
     "ssd_trap_seq_kernel": ("ssd_trap.cu", "warp_rows.cuh"),
     "ssd_trap_decode_kernel": ("ssd_trap.cu", "warp_rows.cuh"),
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
     "ssd_bwd_kernel": ("ssd_bwd.cu", "warp_rows.cuh"),
-    "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu", "warp_rows.cuh"),
-    "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh"),
-    "ssd_complex_decode_kernel": ("ssd_complex.cu", "warp_rows.cuh"),
+    "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu", "warp_rows.cuh", "f32x2.cuh"),
+    "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
+    "ssd_complex_decode_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
 }
 
 # fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz

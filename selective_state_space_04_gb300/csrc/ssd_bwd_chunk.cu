@@ -35,6 +35,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "f32x2.cuh"
 #include "ssd_internal.h"
 
 namespace ssd {
@@ -94,6 +95,21 @@ __device__ __forceinline__ void contract(float (&acc)[TM][TN], const float *A, i
     static_assert(TM % 4 == 0 && TN % 4 == 0 && K % 4 == 0, "whole 16-byte words");
     const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
     const int kend = k_hi < 0 ? K : k_hi;
+    // packed accumulators (f32x2): along j for a k-major B (starting from acc), else
+    // along k (starting from zero, added to acc at the end)
+    f32x2 accj[TM][BK ? TN / 2 : 1], acck[TM][BK ? 1 : TN];
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        if constexpr (BK) {
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j)
+                accj[i][j] = pk2(acc[i][2 * j], acc[i][2 * j + 1]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                acck[i][j] = pk2(0.f, 0.f);
+        }
+    }
 #pragma unroll 2
     for (int k = k_lo; k < kend; k += 4) {
         float av[TM][4], bv[4][TN];
@@ -149,13 +165,44 @@ __device__ __forceinline__ void contract(float (&acc)[TM][TN], const float *A, i
                 bv[3][j] = t.w;
             }
         }
+        if constexpr (BK) {
+            // B's 16-byte words hold neighbouring columns: pairs along j, the
+            // operations of acc[i][j] += A B unchanged
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
+            for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-            for (int i = 0; i < TM; ++i)
+                for (int i = 0; i < TM; ++i) {
+                    const f32x2 a2 = pk2(av[i][kk], av[i][kk]);
 #pragma unroll
-                for (int j = 0; j < TN; ++j)
-                    acc[i][j] = fmaf(av[i][kk], bv[kk][j], acc[i][j]);
+                    for (int j = 0; j < TN / 2; ++j)
+                        accj[i][j] = fma2(a2, pk2(bv[kk][2 * j], bv[kk][2 * j + 1]), accj[i][j]);
+                }
+        } else {
+            // both operands' words run along k: pairs along k, two partial sums
+#pragma unroll
+            for (int kk = 0; kk < 4; kk += 2)
+#pragma unroll
+                for (int i = 0; i < TM; ++i) {
+                    const f32x2 a2 = pk2(av[i][kk], av[i][kk + 1]);
+#pragma unroll
+                    for (int j = 0; j < TN; ++j)
+                        acck[i][j] = fma2(a2, pk2(bv[kk][j], bv[kk + 1][j]), acck[i][j]);
+                }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < TM; ++i) {
+        if constexpr (BK) {
+#pragma unroll
+            for (int j = 0; j < TN / 2; ++j) {
+                acc[i][2 * j] = lo2(accj[i][j]);
+                acc[i][2 * j + 1] = hi2(accj[i][j]);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < TN; ++j)
+                acc[i][j] += lo2(acck[i][j]) + hi2(acck[i][j]);
+        }
     }
 }
 

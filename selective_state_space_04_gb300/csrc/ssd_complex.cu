@@ -20,6 +20,7 @@
 
 #include <algorithm>
 
+#include "f32x2.cuh"
 #include "ssd_internal.h"
 #include "warp_rows.cuh"
 
@@ -59,8 +60,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
     extern __shared__ float sm[];
     const int P = p.P, N = p.N, H = p.H, TB = p.tblk;
     const long long L = p.L;
-    float *bb = sm;                  // [TB][N]: B_bar (interleaved)
-    float *cs = bb + TB * N;         // [TB][N]: C
+    // B_bar and C staged per 4-float group of two components k, k+1 as
+    // (re_k, re_k+1, im_k, im_k+1), C's imaginary parts negated: the packed
+    // arithmetic below then takes pairs straight from the 16-byte loads
+    float *bb = sm;                  // [TB][N]: B_bar
+    float *cs = bb + TB * N;         // [TB][N]: C (re, re, -im, -im)
     float *xs = cs + TB * N;         // [TB][Pp], zero past P
     float *ab = xs + TB * p.Pp;      // [TB][4]: A_bar (re, im), (A_bar - 1) A^-1 (re, im)
     const int Pp = p.Pp;
@@ -83,16 +87,19 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
     const float Ar = mag * cph, Ai = mag * sph, Ir = imag_ * cph, Ii = -imag_ * sph;
     const float Dh = p.D[h];
 
-    float4 hs[RPW][NV];   // (re, im, re, im) of components n/2, n/2 + 1
+    // (re, re) and (im, im) of components n/2, n/2 + 1 (the state is stored (re, im, re, im))
+    f32x2 hre[RPW][NV], him[RPW][NV];
 #pragma unroll
     for (int r = 0; r < RPW; ++r) {
         const int pr = p0 + r;
 #pragma unroll
         for (int c = 0; c < NV; ++c) {
             const int n = 4 * lane + 128 * c;
-            hs[r][c] = (p.h0 && pr < P && n < N)
-                           ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)pr * N + n))
-                           : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 v = (p.h0 && pr < P && n < N)
+                                 ? __ldcs(reinterpret_cast<const float4 *>(p.h0 + sbase + (size_t)pr * N + n))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            hre[r][c] = pk2(v.x, v.z);
+            him[r][c] = pk2(v.y, v.w);
         }
     }
 
@@ -121,10 +128,11 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             const size_t gi = ((size_t)(b * L + t0 + tt) * p.G + g) * N + 2 * k;
             const float br = to_f32<T>(Bg[gi]), bi = to_f32<T>(Bg[gi + 1]);
             const float fr = ab[4 * tt + 2], fi = ab[4 * tt + 3];
-            bb[tt * N + 2 * k] = fr * br - fi * bi;
-            bb[tt * N + 2 * k + 1] = fr * bi + fi * br;
-            cs[tt * N + 2 * k] = to_f32<T>(Cg[gi]);
-            cs[tt * N + 2 * k + 1] = to_f32<T>(Cg[gi + 1]);
+            const int o = tt * N + 4 * (k >> 1) + (k & 1);   // re at o, im at o + 2
+            bb[o] = fr * br - fi * bi;
+            bb[o + 2] = fr * bi + fi * br;
+            cs[o] = to_f32<T>(Cg[gi]);
+            cs[o + 2] = -to_f32<T>(Cg[gi + 1]);
         }
         __syncthreads();
         // unrolled: the readout reductions of a step (shuffle chains, not on the
@@ -132,6 +140,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
 #pragma unroll 4
         for (int i = 0; i < nt; ++i) {
             const float abr = ab[4 * i], abi = ab[4 * i + 1];
+            const f32x2 abr2 = pk2(abr, abr), abi2 = pk2(abi, abi), nabi2 = pk2(-abi, -abi);
             float4 bt[NV], ct[NV];
 #pragma unroll
             for (int c = 0; c < NV; ++c) {
@@ -157,22 +166,21 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             }
 #pragma unroll
             for (int r = 0; r < RPW; ++r) {
-                const float xv = xr[r];
-                float s = 0.f;
+                const f32x2 x2 = pk2(xr[r], xr[r]);
+                f32x2 s = pk2(0.f, 0.f);
 #pragma unroll
                 for (int c = 0; c < NV; ++c) {
-                    float4 &z = hs[r][c];
-                    const float r0 = fmaf(abr, z.x, fmaf(-abi, z.y, bt[c].x * xv));
-                    const float i0 = fmaf(abr, z.y, fmaf(abi, z.x, bt[c].y * xv));
-                    const float r1 = fmaf(abr, z.z, fmaf(-abi, z.w, bt[c].z * xv));
-                    const float i1 = fmaf(abr, z.w, fmaf(abi, z.z, bt[c].w * xv));
-                    z = make_float4(r0, i0, r1, i1);
-                    s = fmaf(ct[c].x, r0, s);    // Re(C h) = Cr hr - Ci hi
-                    s = fmaf(-ct[c].y, i0, s);
-                    s = fmaf(ct[c].z, r1, s);
-                    s = fmaf(-ct[c].w, i1, s);
+                    // h <- A_bar h + B_bar x, per component in the order
+                    // re = abr re + (-abi im + Br x), im = abr im + (abi re + Bi x)
+                    const f32x2 re = hre[r][c], im = him[r][c];
+                    const f32x2 nre = fma2(abr2, re, fma2(nabi2, im, mul2(pk2(bt[c].x, bt[c].y), x2)));
+                    const f32x2 nim = fma2(abr2, im, fma2(abi2, re, mul2(pk2(bt[c].z, bt[c].w), x2)));
+                    hre[r][c] = nre;
+                    him[r][c] = nim;
+                    s = fma2(pk2(ct[c].x, ct[c].y), nre, s);   // Re(C h) = Cr hr - Ci hi
+                    s = fma2(pk2(ct[c].z, ct[c].w), nim, s);
                 }
-                acc[r] = s;
+                acc[r] = lo2(s) + hi2(s);
             }
             warp_sum_rows_all<RPW>(acc, lane);
             const int pr = p0 + summed_row<RPW>(lane);
@@ -189,7 +197,8 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             for (int c = 0; c < NV; ++c) {
                 const int n = 4 * lane + 128 * c;
                 if (pr < P && n < N)
-                    __stcs(reinterpret_cast<float4 *>(p.h_final + sbase + (size_t)pr * N + n), hs[r][c]);
+                    __stcs(reinterpret_cast<float4 *>(p.h_final + sbase + (size_t)pr * N + n),
+                           make_float4(lo2(hre[r][c]), lo2(him[r][c]), hi2(hre[r][c]), hi2(him[r][c])));
             }
         }
     }

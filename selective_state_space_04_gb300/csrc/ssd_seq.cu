@@ -22,6 +22,7 @@
 
 #include <algorithm>
 
+#include "f32x2.cuh"
 #include "ssd_internal.h"
 #include "warp_rows.cuh"
 
@@ -171,28 +172,6 @@ struct RowParams {
     SeqParams s;
     int Pp;                         // staged x row stride (the CTA's rows)
 };
-
-typedef unsigned long long f32x2;   // two fp32 lanes (lo, hi) in one 64-bit register pair
-
-__device__ __forceinline__ f32x2 pk2(float lo, float hi)
-{
-    return ((f32x2)__float_as_uint(hi) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ float lo2(f32x2 v) { return __uint_as_float((unsigned)v); }
-__device__ __forceinline__ float hi2(f32x2 v) { return __uint_as_float((unsigned)(v >> 32)); }
-// elementwise a * b + c and a * b, each lane rounded as fmaf / __fmul_rn
-__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c)
-{
-    f32x2 d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ f32x2 mul2(f32x2 a, f32x2 b)
-{
-    f32x2 d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
 
 // 4 staged values of B or C as two fp32 pairs
 __device__ __forceinline__ void load4(const float *src, f32x2 (&o)[2])
