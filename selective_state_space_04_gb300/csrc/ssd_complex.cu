@@ -53,23 +53,57 @@ __device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.f) + 
 constexpr int kStateFloat4PerLane = 8;   // RPW * NV float4 of state per lane
 constexpr int kMaxWarps = 16;
 
-template <typename T, int NV>
-__global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxParams p)
+// staged x elements per thread and block for CTAs of one or two warps:
+// 64 steps x (2 warps x RPW rows) / 64 threads
+constexpr int kXPerThread = 64 * kStateFloat4PerLane / 32;
+constexpr int kSmallWarps = 8;   // CTAs of up to 8 warps: 3 (N <= 128) or 2 per SM
+
+// asynchronous 16- and 8-byte copies of B or C rows into the staging area
+// (completed by cp.async.wait_all)
+template <typename T>
+__device__ __forceinline__ void cp_async16(T *dst, const T *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+template <typename T>
+__device__ __forceinline__ void cp_async8(T *dst, const T *src)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"((unsigned)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+// 4 staged values (two components as re, im, re, im) as floats
+__device__ __forceinline__ float4 load4f(const float *src) { return *reinterpret_cast<const float4 *>(src); }
+__device__ __forceinline__ float4 load4f(const __nv_bfloat16 *src)
+{
+    const uint2 v = *reinterpret_cast<const uint2 *>(src);
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u), __uint_as_float(v.y << 16),
+                       __uint_as_float(v.y & 0xffff0000u));
+}
+
+// One CTA per (b, h), one warp per block of RPW state rows p, lane l holding
+// the components n/2, n/2 + 1 of n = 4l (+128 per further float4) of each row,
+// kept in registers as (re, re) and (im, im) pairs.  Per time block (up to 64
+// steps) the CTA stages B_t and C_t as stored (bf16 stays bf16) by cp.async
+// copies, x_t as fp32 and the step's coefficients A_bar_t and (A_bar_t - 1) A^-1;
+// each lane forms B_bar = ((A_bar - 1) A^-1) B for its two components at use,
+// once per step for all of its rows.
+template <typename T, int NV, int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) ssd_complex_seq_kernel(CplxParams p)
 {
     constexpr int RPW = kStateFloat4PerLane / NV;
     extern __shared__ float sm[];
     const int P = p.P, N = p.N, H = p.H, TB = p.tblk;
     const long long L = p.L;
-    // B_bar and C staged per 4-float group of two components k, k+1 as
-    // (re_k, re_k+1, im_k, im_k+1), C's imaginary parts negated: the packed
-    // arithmetic below then takes pairs straight from the 16-byte loads
-    float *bb = sm;                  // [TB][N]: B_bar
-    float *cs = bb + TB * N;         // [TB][N]: C (re, re, -im, -im)
-    float *xs = cs + TB * N;         // [TB][Pp], zero past P
-    float *ab = xs + TB * p.Pp;      // [TB][4]: A_bar (re, im), (A_bar - 1) A^-1 (re, im)
     const int Pp = p.Pp;
+    float *xs = sm;                  // [TB][Pp], zero past P
+    float *ab = xs + TB * Pp;        // [TB][4]: A_bar (re, im), (A_bar - 1) A^-1 (re, im)
+    T *bs = reinterpret_cast<T *>(sm + ((TB * (Pp + 4) + 3) & ~3));   // [TB][N]: B_t as stored (16-byte aligned)
+    T *cs = bs + (size_t)TB * N;     // [TB][N]: C_t as stored
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nthr = blockDim.x, nwarps = nthr >> 5;
     const long long bh = blockIdx.x;
     const long long b = bh / H;
     const int h = (int)(bh - b * H);
@@ -78,6 +112,7 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
     const T *xg = static_cast<const T *>(p.x), *Bg = static_cast<const T *>(p.B), *Cg = static_cast<const T *>(p.C);
     T *yg = static_cast<T *>(p.y);
     const size_t sbase = (size_t)bh * P * N;
+    const bool wide16 = (N * (int)sizeof(T)) % 16 == 0;   // staged rows in 16-byte copies
 
     // A = |A| (cos arg, sin arg); A^-1 = (cos arg, -sin arg) / |A|
     const float lm = p.A_polar[2 * h], ph = p.A_polar[2 * h + 1];
@@ -117,37 +152,70 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
             ab[4 * i + 2] = (abr - 1.f) * Ir - abi * Ii;   // (A_bar - 1) A^-1
             ab[4 * i + 3] = (abr - 1.f) * Ii + abi * Ir;
         }
-        for (int i = threadIdx.x; i < nt * Pp; i += nthr) {
-            const int tt = i / Pp, pp = i - tt * Pp;
-            xs[i] = pp < P ? to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]) : 0.f;
+        // B_t and C_t by asynchronous copies (all in flight at once)
+        if (wide16) {   // 16-byte copies: 8 bf16 or 4 fp32 elements
+            constexpr int E = 16 / (int)sizeof(T);
+            for (int i = threadIdx.x; i < nt * (N / E); i += nthr) {
+                const int tt = i / (N / E), q = E * (i - tt * (N / E));
+                const size_t row = ((size_t)(b * L + t0 + tt) * p.G + g) * N;
+                cp_async16(bs + (size_t)tt * N + q, Bg + row + q);
+                cp_async16(cs + (size_t)tt * N + q, Cg + row + q);
+            }
+        } else {        // bf16 rows of N % 8 == 4 elements: 8-byte copies
+            for (int i = threadIdx.x; i < nt * (N / 4); i += nthr) {
+                const int tt = i / (N / 4), q = 4 * (i - tt * (N / 4));
+                const size_t row = ((size_t)(b * L + t0 + tt) * p.G + g) * N;
+                cp_async8(bs + (size_t)tt * N + q, Bg + row + q);
+                cp_async8(cs + (size_t)tt * N + q, Cg + row + q);
+            }
         }
-        __syncthreads();
-        const int K = N / 2;
-        for (int i = threadIdx.x; i < nt * K; i += nthr) {
-            const int tt = i / K, k = i - tt * K;
-            const size_t gi = ((size_t)(b * L + t0 + tt) * p.G + g) * N + 2 * k;
-            const float br = to_f32<T>(Bg[gi]), bi = to_f32<T>(Bg[gi + 1]);
-            const float fr = ab[4 * tt + 2], fi = ab[4 * tt + 3];
-            const int o = tt * N + 4 * (k >> 1) + (k & 1);   // re at o, im at o + 2
-            bb[o] = fr * br - fi * bi;
-            bb[o + 2] = fr * bi + fi * br;
-            cs[o] = to_f32<T>(Cg[gi]);
-            cs[o + 2] = -to_f32<T>(Cg[gi + 1]);
+        if (nwarps <= 2) {
+            // few warps (small P): each thread's x loads all issued before its first store
+            float xv[kXPerThread];
+#pragma unroll
+            for (int k = 0; k < kXPerThread; ++k) {
+                const int i = threadIdx.x + k * nthr;
+                xv[k] = 0.f;
+                if (i < nt * Pp) {
+                    const int tt = i / Pp, pp = i - tt * Pp;
+                    if (pp < P)
+                        xv[k] = to_f32<T>(xg[((size_t)(b * L + t0 + tt) * H + h) * P + pp]);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kXPerThread; ++k) {
+                const int i = threadIdx.x + k * nthr;
+                if (i < nt * Pp)
+                    xs[i] = xv[k];
+            }
+        } else {
+            for (int tt = warp; tt < nt; tt += nwarps) {
+                const size_t row = (size_t)(b * L + t0 + tt);
+                for (int pp = lane; pp < Pp; pp += 32)
+                    xs[tt * Pp + pp] = pp < P ? to_f32<T>(xg[(row * H + h) * P + pp]) : 0.f;
+            }
         }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         __syncthreads();
         // unrolled: the readout reductions of a step (shuffle chains, not on the
         // recurrence) overlap the next steps' state updates
 #pragma unroll 4
         for (int i = 0; i < nt; ++i) {
-            const float abr = ab[4 * i], abi = ab[4 * i + 1];
+            const float abr = ab[4 * i], abi = ab[4 * i + 1], fr = ab[4 * i + 2], fi = ab[4 * i + 3];
             const f32x2 abr2 = pk2(abr, abr), abi2 = pk2(abi, abi), nabi2 = pk2(-abi, -abi);
-            float4 bt[NV], ct[NV];
+            f32x2 bre[NV], bim[NV], cre[NV], ncim[NV];   // B_bar (re, re), (im, im); C (re, re), (-im, -im)
 #pragma unroll
             for (int c = 0; c < NV; ++c) {
                 const int n = 4 * lane + 128 * c;
-                const bool in = n < N;   // N % 4 == 0: whole float4 chunks
-                bt[c] = in ? *reinterpret_cast<const float4 *>(bb + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
-                ct[c] = in ? *reinterpret_cast<const float4 *>(cs + i * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+                if (n < N) {   // N % 4 == 0: whole float4 chunks
+                    const float4 bv = load4f(bs + (size_t)i * N + n), cv = load4f(cs + (size_t)i * N + n);
+                    bre[c] = pk2(fr * bv.x - fi * bv.y, fr * bv.z - fi * bv.w);
+                    bim[c] = pk2(fr * bv.y + fi * bv.x, fr * bv.w + fi * bv.z);
+                    cre[c] = pk2(cv.x, cv.z);
+                    ncim[c] = pk2(-cv.y, -cv.w);
+                } else {
+                    bre[c] = bim[c] = cre[c] = ncim[c] = pk2(0.f, 0.f);
+                }
             }
             float acc[RPW], xr[RPW];   // this warp's RPW rows of x_t: 16- or 8-byte loads
             if constexpr (RPW >= 4) {
@@ -173,12 +241,12 @@ __global__ void __launch_bounds__(kMaxWarps * 32) ssd_complex_seq_kernel(CplxPar
                     // h <- A_bar h + B_bar x, per component in the order
                     // re = abr re + (-abi im + Br x), im = abr im + (abi re + Bi x)
                     const f32x2 re = hre[r][c], im = him[r][c];
-                    const f32x2 nre = fma2(abr2, re, fma2(nabi2, im, mul2(pk2(bt[c].x, bt[c].y), x2)));
-                    const f32x2 nim = fma2(abr2, im, fma2(abi2, re, mul2(pk2(bt[c].z, bt[c].w), x2)));
+                    const f32x2 nre = fma2(abr2, re, fma2(nabi2, im, mul2(bre[c], x2)));
+                    const f32x2 nim = fma2(abr2, im, fma2(abi2, re, mul2(bim[c], x2)));
                     hre[r][c] = nre;
                     him[r][c] = nim;
-                    s = fma2(pk2(ct[c].x, ct[c].y), nre, s);   // Re(C h) = Cr hr - Ci hi
-                    s = fma2(pk2(ct[c].z, ct[c].w), nim, s);
+                    s = fma2(cre[c], nre, s);    // Re(C h) = Cr hr - Ci hi
+                    s = fma2(ncim[c], nim, s);
                 }
                 acc[r] = lo2(s) + hi2(s);
             }
@@ -296,6 +364,30 @@ __global__ void __launch_bounds__(kDecWarps * 32, NV == 1 ? 5 : 1) ssd_complex_d
 
 int complex_nv(int N) { return N <= 128 ? 1 : N <= 256 ? 2 : 4; }
 
+template <typename T, int NV, int MAXT, int MINB>
+cudaError_t seq_launch_t(const CplxParams &p, dim3 grid, int warps, size_t smem, cudaStream_t st)
+{
+    auto kern = ssd_complex_seq_kernel<T, NV, MAXT, MINB>;
+    if (smem > 48 * 1024) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess)
+            return e;
+    }
+    kern<<<grid, 32 * warps, smem, st>>>(p);
+    return cudaSuccess;
+}
+
+template <typename T, int MAXT, int MINB>
+cudaError_t seq_launch_nv(int nv, const CplxParams &p, dim3 grid, int warps, size_t smem, cudaStream_t st)
+{
+    switch (nv) {
+    case 1: return seq_launch_t<T, 1, MAXT, MINB>(p, grid, warps, smem, st);
+    case 2: return seq_launch_t<T, 2, MAXT, MINB>(p, grid, warps, smem, st);
+    default: return seq_launch_t<T, 4, MAXT, MINB>(p, grid, warps, smem, st);
+    }
+}
+
+
 }  // namespace
 
 bool complex_supported(const ComplexArgs &a)
@@ -331,12 +423,17 @@ cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t st)
     const int nv = complex_nv(a.dstate), rows = kStateFloat4PerLane / nv;
     const int warps = (a.headdim + rows - 1) / rows;
     p.Pp = warps * rows;
-    // steps per staged block: up to 64, within about 200 KB of shared memory
-    const long long per_step = (long long)(2 * a.dstate + p.Pp + 4) * (long long)sizeof(float);
-    p.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, a.seqlen, (200LL << 10) / per_step}));
-    const size_t smem = (size_t)(p.tblk * (2 * a.dstate + p.Pp + 4)) * sizeof(float);
-    const dim3 grid((unsigned)(a.batch * a.nheads));
     const bool bf = a.dtype == SSD_DTYPE_BF16;
+    const dim3 grid((unsigned)(a.batch * a.nheads));
+    // steps per staged block: up to 64, within a third of the SM's shared memory for
+    // CTAs of up to 8 warps (3 per SM) and about 200 KB otherwise (x and the step's
+    // coefficients as fp32, B and C as stored)
+    const bool small = warps <= kSmallWarps;
+    const long long per_step = (long long)(p.Pp + 4) * (long long)sizeof(float) +
+                               2LL * a.dstate * (long long)(bf ? sizeof(__nv_bfloat16) : sizeof(float));
+    const long long budget = small ? (72LL << 10) : (200LL << 10);
+    p.tblk = (int)std::max<long long>(1, std::min<long long>({64LL, a.seqlen, (budget - 16) / per_step}));
+    const size_t smem = (size_t)p.tblk * (size_t)per_step + 16;   // (+ the B_t area's alignment)
     if (a.seqlen == 1) {   // the decode step: the specialised stream of the state
         if (nv == 1)
             bf ? ssd_complex_decode_kernel<__nv_bfloat16, 1><<<grid, kDecWarps * 32, 0, st>>>(p)
@@ -352,31 +449,17 @@ cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t st)
             note_launches(1);
         return e;
     }
-#define SSD_CPLX_LAUNCH(NVV)                                                                                    \
-    do {                                                                                                         \
-        if (bf)                                                                                                  \
-            ssd_complex_seq_kernel<__nv_bfloat16, NVV><<<grid, 32 * warps, smem, st>>>(p);                       \
-        else                                                                                                     \
-            ssd_complex_seq_kernel<float, NVV><<<grid, 32 * warps, smem, st>>>(p);                               \
-    } while (0)
-    if (smem > 48 * 1024) {
-        const cudaError_t e =
-            nv == 1 ? (bf ? cudaFuncSetAttribute(ssd_complex_seq_kernel<__nv_bfloat16, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                          : cudaFuncSetAttribute(ssd_complex_seq_kernel<float, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-            : nv == 2 ? (bf ? cudaFuncSetAttribute(ssd_complex_seq_kernel<__nv_bfloat16, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                            : cudaFuncSetAttribute(ssd_complex_seq_kernel<float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem))
-                      : (bf ? cudaFuncSetAttribute(ssd_complex_seq_kernel<__nv_bfloat16, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-                            : cudaFuncSetAttribute(ssd_complex_seq_kernel<float, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-        if (e != cudaSuccess)
-            return e;
-    }
-    if (nv == 1)
-        SSD_CPLX_LAUNCH(1);
-    else if (nv == 2)
-        SSD_CPLX_LAUNCH(2);
-    else
-        SSD_CPLX_LAUNCH(4);
-#undef SSD_CPLX_LAUNCH
+    // (3 CTAs per SM where one float4 of each state row per lane leaves the
+    // registers for it; 2 for the wider states)
+    const cudaError_t le =
+        bf ? (small ? (nv == 1 ? seq_launch_t<__nv_bfloat16, 1, kSmallWarps * 32, 3>(p, grid, warps, smem, st)
+                               : seq_launch_nv<__nv_bfloat16, kSmallWarps * 32, 2>(nv, p, grid, warps, smem, st))
+                    : seq_launch_nv<__nv_bfloat16, kMaxWarps * 32, 1>(nv, p, grid, warps, smem, st))
+           : (small ? (nv == 1 ? seq_launch_t<float, 1, kSmallWarps * 32, 3>(p, grid, warps, smem, st)
+                               : seq_launch_nv<float, kSmallWarps * 32, 2>(nv, p, grid, warps, smem, st))
+                    : seq_launch_nv<float, kMaxWarps * 32, 1>(nv, p, grid, warps, smem, st));
+    if (le != cudaSuccess)
+        return le;
     const cudaError_t e = cudaGetLastError();
     if (e == cudaSuccess)
         note_launches(1);
