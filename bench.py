@@ -86,7 +86,7 @@ KERNEL_SOURCES = {
     "ssd_conv1d_silu_kernel": ("ssd_neighbors.cu",),
     "ssd_gated_rmsnorm_kernel": ("ssd_neighbors.cu",),
     "ssd_bwd_kernel": ("ssd_bwd.cu", "warp_rows.cuh"),
-    "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu", "warp_rows.cuh", "f32x2.cuh"),
+    "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu", "ssd_bwd_tc.cu", "warp_rows.cuh", "f32x2.cuh", "ptx.cuh", "tmap.h"),
     "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
     "ssd_complex_decode_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
 }

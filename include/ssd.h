@@ -76,6 +76,11 @@ typedef enum ssd_status {
  * returns; y and final_state are undefined.  It exercises the failure path
  * without faulting the GPU.  Ignored by the sequential path. */
 #define SSD_DIAG_STALL_HANDOFF 0x100u
+/* In ssd_dims_t.flags of ssd_scan_bwd only: run the chunk form's fp32
+ * contractions even where its tensor-core gradient pass applies (bf16 inputs,
+ * P = 64, N = 128).  The tensor-core pass rounds the masked decay products
+ * and the chunk states to bf16 operands; the fp32 form does not. */
+#define SSD_BWD_FP32_FORM 0x200u
 
 /* Schedules of the chunked path (see ssd_chunk_schedule).  One may be requested
  * in ssd_dims_t.flags as (SSD_SCHEDULE_x << SSD_SCHEDULE_SHIFT); 0 there lets

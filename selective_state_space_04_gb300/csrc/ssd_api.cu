@@ -683,7 +683,16 @@ ssd_status_t ssd_get_device_error(void *stream, uint32_t *code)
 {
     if (!code)
         return SSD_ERR_NULL_PTR;
-    return chunk_read_device_error(static_cast<cudaStream_t>(stream), code);
+    const ssd_status_t s = chunk_read_device_error(static_cast<cudaStream_t>(stream), code);
+    if (s != SSD_OK)
+        return s;
+    uint32_t bwd = 0;   // the tensor-core gradient pass of the backward keeps its own word
+    const ssd_status_t s2 = bwd_tc_read_device_error(&bwd);
+    if (s2 != SSD_OK)
+        return s2;
+    if (*code == 0)
+        *code = bwd;
+    return SSD_OK;
 }
 
 const char *ssd_status_string(ssd_status_t status)
@@ -1115,10 +1124,14 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
 {
     SSD_NVTX_RANGE("ssd_scan_bwd");
     Sizes sz;
-    ssd_status_t s = check_dims(dims, &sz);
+    if (!dims)
+        return SSD_ERR_NULL_PTR;
+    ssd_dims_t dchk = *dims;   // (the backward's own flag is checked here, the rest by check_dims)
+    dchk.flags &= ~SSD_BWD_FP32_FORM;
+    ssd_status_t s = check_dims(&dchk, &sz);
     if (s != SSD_OK)
         return s;
-    if ((dims->flags & ~SSD_PATH_MASK) != 0)
+    if ((dims->flags & ~(SSD_PATH_MASK | SSD_BWD_FP32_FORM)) != 0)
         return SSD_ERR_INVALID_DIMS;
     const uint32_t path = dims->flags & SSD_PATH_MASK;
     if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
@@ -1175,6 +1188,7 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
     ba.ngroups = dims->ngroups;
     ba.dtype = dims->dtype;
     ba.path = path;
+    ba.fp32_form = (dims->flags & SSD_BWD_FP32_FORM) != 0;
     if (path == SSD_PATH_AUTO)
         ba.path = bwd_chunk_supported(ba) ? SSD_PATH_CHUNKED : SSD_PATH_SEQUENTIAL;
     if (!bwd_supported(ba))

@@ -920,11 +920,37 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
                                     0, st>>>(p);
     else
         ssd_bwd_pass_kernel<1><<<dim3((unsigned)((NP + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
-    if (bf)
+    if (bf && !a.fp32_form && bwd_tc_supported(a.dtype, a.headdim, a.dstate)) {
+        // the gradient pass on the tensor cores (ssd_bwd_tc.cu)
+        BwdTcArgs t;
+        t.x = a.x;
+        t.B = a.B;
+        t.C = a.C;
+        t.dy = a.dy;
+        t.dt_raw = a.dt_raw;
+        t.dt_bias = a.dt_bias;
+        t.A_log = a.A_log;
+        t.D = a.D;
+        t.S = p.S;
+        t.R = p.R;
+        t.dx = a.dx;
+        t.ddt_raw = a.ddt_raw;
+        t.dB_head = p.dB_head;
+        t.dC_head = p.dC_head;
+        t.part = p.part;
+        t.batch = a.batch;
+        t.seqlen = a.seqlen;
+        t.nheads = a.nheads;
+        t.ngroups = a.ngroups;
+        t.nc = nc;
+        e = bwd_tc_grad_launch(t, st);
+    } else if (bf) {
         ssd_bwd_grad_kernel<__nv_bfloat16><<<grid, kThreads, kGradSmem, st>>>(p);
-    else
+    } else {
         ssd_bwd_grad_kernel<float><<<grid, kThreads, kGradSmem, st>>>(p);
-    e = cudaGetLastError();
+    }
+    if (e == cudaSuccess)
+        e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     note_launches(3);

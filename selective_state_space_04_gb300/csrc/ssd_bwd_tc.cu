@@ -1,0 +1,741 @@
+// ssd_bwd_tc.cu -- the gradient pass of the chunk-form backward (the third of
+// ssd_bwd_chunk.cu's launches) on the tensor cores, for bf16 inputs with
+// P = 64 and N = 128.
+//
+// The chunk form's per-chunk gradients (see ssd_bwd_chunk.cu for their
+// derivation from the forward's chunk algebra), with CB = C B^T, DX = dy x^T,
+// E = causal e^{cs_s - cs_j} within a chunk, Mt = E o CB, A2 = E o DX:
+//   dx_j = D dy_j + dt_j ((Mt^T dy)_j + e^{cs_last - cs_j} (B G_out)_j)
+//   dB_j = dt_j ((A2^T C)_j + e^{cs_last - cs_j} (x G_out^T)_j)
+//   dC_s = (A2 (dt o B))_s + e^{cs_s} (dy h_in^T)_s
+// and d log dA from the row and column sums of W = Mt o DX o dt_j, plus
+// u_s = C_s . e^{cs_s} (dy h_in^T)_s, minus v_j = dt_j e^{cs_last - cs_j}
+// x_j . (B G_out)_j, plus <G_out, h_last> at the chunk's last step.
+//
+// One CTA takes two consecutive 64-step chunks of one (b, h), stacked as the
+// 128 rows of every tcgen05 MMA (kind::f16, bf16 operands in shared memory with
+// the 128-byte swizzle, fp32 accumulators in TMEM; lanes are rows).  E is zero
+// across the two chunks, so CB and DX are block diagonal after the mask and
+// the products with Mt and A2 need nothing more.  The products with a chunk's
+// own state (G_out, h_in) are issued once per chunk over all 128 rows, and each
+// row keeps its own chunk's half.
+//
+// The chunk states enter as two bf16 terms, hi = bf16(v) and lo = bf16(v - hi)
+// (about 16 significant bits), each product with a state issued once per term
+// into the same accumulator: the state terms feed d log dA, whose sums over
+// every step cancel heavily and would carry a single bf16 rounding of the
+// states far past the bf16 bar.
+//
+// Phases (one mbarrier hand-off each, all waits bounded):
+//   MMA 1: CB, DX.
+//   rows: Mt, A2 (bf16, zero outside the row's chunk block), W's sums.
+//   MMA 2: Mt^T dy, B G_out, x G_out^T (the hi terms, both chunks).
+//   rows: G_out's lo terms into its tiles.   MMA 2b: the lo terms.
+//   rows: dx; B scaled in place by dt (for dC); h_in's hi terms into Mt's space.
+//   MMA 3: A2^T C, A2 (dt o B).
+//   rows: dB.
+//   MMA 4: dy h_in^T (hi).   rows: h_in's lo terms.   MMA 4b: the lo terms.
+//   rows: dC, then d log dA's suffix sums, ddt_raw and the chunks' partials.
+// Operands rounded to bf16 once (Mt, A2, dt o B) bound the result's precision
+// as bf16 inputs bound the forward's: the bar is the forward's bf16 bar, not
+// fp32's.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "ptx.cuh"
+#include "ssd_internal.h"
+#include "tmap.h"
+#include "warp_rows.cuh"
+
+namespace ssd {
+
+__device__ unsigned int g_bwd_tc_error;
+
+namespace {
+
+using namespace ssd::ptx;
+
+constexpr int kR = 128;              // rows: two chunks of 64 steps
+constexpr int kCq = 64;              // steps per chunk
+constexpr int kP = 64, kN = 128;
+constexpr int kRowWarps = 4;         // warps 0-3: TMEM lane quarters, one row each per thread
+constexpr int kIssueWarp = 4;        // TMA and MMA issue, TMEM owner
+constexpr int kThreads = 5 * 32;
+constexpr uint32_t kT16 = 16384;     // one [128 rows][64 bf16] tile with the 128-byte swizzle
+
+// shared memory (from a 1024-aligned base)
+constexpr uint32_t kOffC = 0;                    // C [s][n]: tiles n 0-63, 64-127
+constexpr uint32_t kOffB = kOffC + 2 * kT16;     // B [j][n]; later dt_j B_j
+constexpr uint32_t kOffX = kOffB + 2 * kT16;     // x [j][p]
+constexpr uint32_t kOffDY = kOffX + kT16;        // dy [s][p]
+constexpr uint32_t kOffG = kOffDY + kT16;        // G_out of chunk 0, 1: [n][p]
+constexpr uint32_t kOffMT = kOffG + 2 * kT16;    // Mt [s][j]: tiles j 0-63, 64-127; later h_in of chunk 0, 1
+constexpr uint32_t kOffA2 = kOffMT + 2 * kT16;   // A2 [s][j]
+constexpr uint32_t kOffArr = kOffA2 + 2 * kT16;
+// per-row float arrays of 128
+enum { A_DT = 0, A_Z, A_CS2, A_ROWP, A_COLP0, A_DDIR = A_COLP0 + 4, A_VV, A_UU, A_DCS, A_NUM };   // COLP: 4 warps
+constexpr uint32_t kOffRed = kOffArr + A_NUM * kR * 4;   // 64 floats: per-warp sums
+constexpr uint32_t kOffBars = kOffRed + 64 * 4;
+enum {
+    BAR_FULL = 0, BAR_ROWS0, BAR_MMA1, BAR_ROWS1, BAR_MMA2, BAR_ROWS2A, BAR_MMA2B, BAR_ROWS2, BAR_MMA3, BAR_ROWS3,
+    BAR_MMA4, BAR_ROWS4A, BAR_MMA4B, BAR_DRAIN, BAR_RSYNC, kNumBars
+};
+constexpr uint32_t kOffHolder = kOffBars + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kOffHolder + 16 + 1024;
+
+// TMEM columns
+constexpr uint32_t kColCB = 0, kColDX = 128;                  // MMA 1
+constexpr uint32_t kColMTDY = 0, kColBG = 64, kColXG = 256;   // MMA 2 (BG of chunk k at +64k, XG at +128k)
+constexpr uint32_t kColA2C = 0, kColA2B = 128;                // MMA 3 (XG kept until the dB epilogue)
+constexpr uint32_t kColDYH = 256;                             // MMA 4 (chunk k at +128k)
+
+constexpr uint64_t kTimeoutNs = 2000000000ull;
+
+struct TcParams {
+    const float *dt_raw, *dt_bias, *A_log, *D;
+    const float *S, *R;          // [B*H][nc+1][N][P] entering states (slot nc: final); [B*H][nc][N][P] G_out
+    float *dx, *ddt_raw, *dB_head, *dC_head, *part;
+    long long L;
+    int H, G, nc;
+};
+
+struct TcMaps {
+    CUtensorMap x, dy, B, C;
+};
+
+__device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+__device__ void raise_error()
+{
+    atomicCAS(&g_bwd_tc_error, 0u, (unsigned)SSD_ERR_TIMEOUT);
+}
+
+// bounded wait (each probe suspends up to 1 ms); false after kTimeoutNs
+__device__ bool wait_bar(uint64_t *bar, uint32_t parity)
+{
+    if (mbar_wait_for(bar, parity, 1000000u))
+        return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (globaltimer_ns() - t0 < kTimeoutNs)
+        if (mbar_wait_for(bar, parity, 1000000u))
+            return true;
+    raise_error();
+    return false;
+}
+
+__device__ __forceinline__ void warp_arrive(uint64_t *bar)
+{
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0)
+        mbar_arrive(bar);
+}
+
+// bounded barrier of the 4 row warps on an mbarrier (phase: this thread's copy)
+__device__ __forceinline__ bool rsync(uint64_t *bar, uint32_t &phase)
+{
+    warp_arrive(bar);
+    const bool ok = wait_bar(bar, phase);
+    phase ^= 1u;
+    return ok;
+}
+
+__device__ __forceinline__ float softplus_f32(float z) { return fmaxf(z, 0.f) + log1pf(expf(-fabsf(z))); }
+
+// 8 bf16 of a swizzled tile row as floats
+__device__ __forceinline__ void ld8(const uint8_t *tile, int r, int c, float (&v)[8])
+{
+    const uint4 u = *reinterpret_cast<const uint4 *>(tile + sw128(r, c));
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+__device__ __forceinline__ void st8(uint8_t *tile, int r, int c, const float (&v)[8])
+{
+    *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
+                                                                pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// a chunk's fp32 state [n][p] (row n of this thread) into a bf16 tile, zero when
+// absent: its hi term bf16(v) (lo false) or its lo term bf16(v - hi) (lo true)
+__device__ __forceinline__ void stage_state(uint8_t *tile, const float *src, int n, bool lo)
+{
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        float v[8];
+        if (src) {
+            const float4 a = __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 8 * c));
+            const float4 b = __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 8 * c + 4));
+            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+            if (lo) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                v[e] = 0.f;
+        }
+        st8(tile, n, c, v);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+    uint32_t *holder = reinterpret_cast<uint32_t *>(smem + kOffHolder);
+    float *arr = reinterpret_cast<float *>(smem + kOffArr);
+    float *red = reinterpret_cast<float *>(smem + kOffRed);
+    float *dt_s = arr + A_DT * kR, *z_s = arr + A_Z * kR, *cs_s = arr + A_CS2 * kR, *rowp = arr + A_ROWP * kR;
+    float *colp = arr + A_COLP0 * kR;   // [4 warps][128]
+    float *ddir = arr + A_DDIR * kR, *vv = arr + A_VV * kR, *uu = arr + A_UU * kR, *dcs = arr + A_DCS * kR;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int H = p.H, nc = p.nc;
+    const long long bh = blockIdx.y, b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / p.G);
+    const int c0 = 2 * (int)blockIdx.x;                  // first chunk of the pair
+    const long long t0 = (long long)c0 * kCq;
+    const int nq = (int)min((long long)kR, p.L - t0);    // valid rows of the pair
+    const float a = -expf(p.A_log[h]);
+    const size_t NP = (size_t)kN * kP;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i)
+            mbar_init(&bars[i], (i == BAR_ROWS0 || i == BAR_ROWS1 || i == BAR_ROWS2A || i == BAR_ROWS2 ||
+                                 i == BAR_ROWS3 || i == BAR_ROWS4A || i == BAR_RSYNC)
+                                    ? kRowWarps
+                                    : 1);
+        fence_mbar_init();
+    }
+    if (warp == kIssueWarp) {
+        tmem_alloc(holder, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    bool ok = true;
+
+    if (warp == kIssueWarp) {
+        if (lane == 0) {
+            // ---- TMA: C, B (two 64-column tiles each), x, dy
+            const uint64_t pol = policy_evict_first();
+            mbar_arrive_expect_tx(&bars[BAR_FULL], 6 * kT16);
+            tma_load_3d(smem + kOffC, &maps.C, &bars[BAR_FULL], g * kN, (int)t0, (int)b, pol);
+            tma_load_3d(smem + kOffC + kT16, &maps.C, &bars[BAR_FULL], g * kN + 64, (int)t0, (int)b, pol);
+            tma_load_3d(smem + kOffB, &maps.B, &bars[BAR_FULL], g * kN, (int)t0, (int)b, pol);
+            tma_load_3d(smem + kOffB + kT16, &maps.B, &bars[BAR_FULL], g * kN + 64, (int)t0, (int)b, pol);
+            tma_load_3d(smem + kOffX, &maps.x, &bars[BAR_FULL], h * kP, (int)t0, (int)b, pol);
+            tma_load_3d(smem + kOffDY, &maps.dy, &bars[BAR_FULL], h * kP, (int)t0, (int)b, pol);
+            const uint32_t sC = smem_u32(smem + kOffC), sB = smem_u32(smem + kOffB), sX = smem_u32(smem + kOffX);
+            const uint32_t sDY = smem_u32(smem + kOffDY), sG = smem_u32(smem + kOffG);
+            const uint32_t sMT = smem_u32(smem + kOffMT), sA2 = smem_u32(smem + kOffA2);
+            // K-major operand: 8 k-steps of 16 over two 64-column tiles (K = 128) or 4 in one (K = 64)
+            auto kmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + (kk >> 2) * kT16 + (kk & 3) * 32, 16, 1024); };
+            // MN-major operand: k-step kk = rows 16 kk .. +15; the 64-element MN blocks kT16 apart
+            auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kT16, 1024); };
+            const uint32_t i128kk = idesc_bf16_f32(128, 128, 0, 0), i64kn = idesc_bf16_f32(128, 64, 0, 1);
+            const uint32_t i64nn = idesc_bf16_f32(128, 64, 1, 1), i128nn = idesc_bf16_f32(128, 128, 1, 1);
+            const uint32_t i128kn = idesc_bf16_f32(128, 128, 0, 1);
+            do {
+                // ---- MMA 1: CB = C B^T, DX = dy x^T
+                if (!(ok = wait_bar(&bars[BAR_FULL], 0)) || !(ok = wait_bar(&bars[BAR_ROWS0], 0)))
+                    break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColCB, kmaj(sC, kk), kmaj(sB, kk), i128kk, kk > 0);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem + kColDX, kmaj(sDY, kk), kmaj(sX, kk), i128kk, kk > 0);
+                mma_commit(&bars[BAR_MMA1]);
+                // ---- MMA 2: Mt^T dy; B G_out and x G_out^T, G_out's hi terms (each chunk's
+                //      state over all rows)
+                if (!(ok = wait_bar(&bars[BAR_ROWS1], 0)))
+                    break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColMTDY, mnmaj(sMT, kk), mnmaj(sDY, kk), i64nn, kk > 0);
+                auto issue_state_g = [&](bool acc) {
+                    for (int k = 0; k < 2; ++k) {
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_ss(tmem + kColBG + 64 * k, kmaj(sB, kk), mnmaj(sG + k * kT16, kk), i64kn, acc || kk > 0);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + kColXG + 128 * k, kmaj(sX, kk), kmaj(sG + k * kT16, kk), i128kk, acc || kk > 0);
+                    }
+                };
+                issue_state_g(false);
+                mma_commit(&bars[BAR_MMA2]);
+                // ---- MMA 2b: G_out's lo terms, into the same accumulators
+                if (!(ok = wait_bar(&bars[BAR_ROWS2A], 0)))
+                    break;
+                tc_fence_after();
+                issue_state_g(true);
+                mma_commit(&bars[BAR_MMA2B]);
+                // ---- MMA 3: A2^T C, A2 (dt o B)
+                if (!(ok = wait_bar(&bars[BAR_ROWS2], 0)))
+                    break;
+                tc_fence_after();
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColA2C, mnmaj(sA2, kk), mnmaj(sC, kk), i128nn, kk > 0);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColA2B, kmaj(sA2, kk), mnmaj(sB, kk), i128kn, kk > 0);
+                mma_commit(&bars[BAR_MMA3]);
+                // ---- MMA 4: dy h_in^T, h_in's hi terms, then its lo terms, into the
+                //      columns of x G_out^T once the dB epilogue has read them
+                auto issue_state_h = [&](bool acc) {
+                    for (int k = 0; k < 2; ++k)
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss(tmem + kColDYH + 128 * k, kmaj(sDY, kk), kmaj(sMT + k * kT16, kk), i128kk,
+                                   acc || kk > 0);
+                };
+                if (!(ok = wait_bar(&bars[BAR_ROWS3], 0)))
+                    break;
+                tc_fence_after();
+                issue_state_h(false);
+                mma_commit(&bars[BAR_MMA4]);
+                if (!(ok = wait_bar(&bars[BAR_ROWS4A], 0)))
+                    break;
+                tc_fence_after();
+                issue_state_h(true);
+                mma_commit(&bars[BAR_MMA4B]);
+            } while (false);
+            // no MMA may be in flight when tensor memory is released, nor a TMA load
+            // when the CTA exits
+            mma_commit(&bars[BAR_DRAIN]);
+            const uint64_t tw = globaltimer_ns();
+            while (!mbar_wait_for(&bars[BAR_DRAIN], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+            }
+            while (!mbar_wait_for(&bars[BAR_FULL], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ rows
+        const int q = warp;                     // TMEM lane quarter
+        const int r = 32 * q + lane;            // this thread's row: step t0 + r
+        const int k = r >> 6;                   // its chunk (0, 1)
+        const int c = c0 + k;
+        const bool cvalid = c < nc;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
+        const uint32_t trow = tmem + lane_addr;
+        uint8_t *tC = smem + kOffC, *tB = smem + kOffB, *tX = smem + kOffX, *tDY = smem + kOffDY;
+        uint8_t *tG = smem + kOffG, *tMT = smem + kOffMT, *tA2 = smem + kOffA2;
+        uint32_t rphase = 0;
+        do {
+            // ---- per step: dt, z and the cumulative sum of dt a within the chunk (log2 units)
+            {
+                float dt = 0.f, z = 0.f;
+                if (r < nq) {
+                    z = p.dt_raw[(size_t)(b * p.L + t0 + r) * H + h] + p.dt_bias[h];
+                    dt = softplus_f32(z);
+                }
+                dt_s[r] = dt;
+                z_s[r] = z;
+                float v = dt * a * 1.4426950408889634f;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, v, o);
+                    if (lane >= o)
+                        v += u;
+                }
+                cs_s[r] = v;
+            }
+            // both chunks' G_out (row n = r of each) into bf16 tiles, and this row's
+            // share of <G_out, h_last> per chunk (summed per warp; over the warps below)
+#pragma unroll 1
+            for (int kk = 0; kk < 2; ++kk) {
+                const bool v = c0 + kk < nc;
+                const float *G2 = v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr;
+                stage_state(tG + kk * kT16, G2, r, false);
+                float s = 0.f;
+                if (v) {
+                    const float *Gr = G2 + (size_t)r * kP;
+                    const float *Hr = p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP + (size_t)r * kP;
+                    for (int e = 0; e < kP; e += 4) {
+                        const float4 ga = __ldg(reinterpret_cast<const float4 *>(Gr + e));
+                        const float4 ha = __ldg(reinterpret_cast<const float4 *>(Hr + e));
+                        s = fmaf(ga.x, ha.x, fmaf(ga.y, ha.y, fmaf(ga.z, ha.z, fmaf(ga.w, ha.w, s))));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0)
+                    red[8 * kk + q] = s;
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&bars[BAR_ROWS0]);
+            // chunk cumsums: the second warp of each chunk adds the first's total
+            if (!(ok = wait_bar(&bars[BAR_FULL], 0)))
+                break;
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            const float cs_pre = (q & 1) ? cs_s[32 * (q - 1) + 31] : 0.f;
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            cs_s[r] += cs_pre;
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            // sum over the chunk of dy . x (this row)
+            {
+                float d = 0.f;
+                for (int cc = 0; cc < 8; ++cc) {
+                    float xv[8], yv[8];
+                    ld8(tX, r, cc, xv);
+                    ld8(tDY, r, cc, yv);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        d = fmaf(xv[e], yv[e], d);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1)
+                    d += __shfl_xor_sync(0xffffffffu, d, o);
+                if (lane == 0)
+                    red[16 + q] = d;
+            }
+            const float cs_r = cs_s[r];
+            const float cs_last = cs_s[64 * k + 63];
+            const float dt_r = dt_s[r];
+            // ---- rows 1: Mt, A2 from CB, DX (this row's chunk block), W's sums
+            if (!(ok = wait_bar(&bars[BAR_MMA1], 0)))
+                break;
+            tc_fence_after();
+            {
+                float rsum = 0.f;
+                const int jb = 64 * k;   // the block of this row's chunk
+#pragma unroll 1
+                for (int g16 = 0; g16 < 4; ++g16) {
+                    uint32_t cb[16], dx[16];
+                    tmem_ld16(trow + kColCB + jb + 16 * g16, cb);
+                    tmem_ld16(trow + kColDX + jb + 16 * g16, dx);
+                    tmem_wait_ld();
+                    float mt[16], a2[16], w[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const int j = jb + 16 * g16 + e;
+                        const float E = (j <= r && r < nq) ? ex2_approx(cs_r - cs_s[j]) : 0.f;
+                        mt[e] = E * __uint_as_float(cb[e]);
+                        a2[e] = E * __uint_as_float(dx[e]);
+                        w[e] = mt[e] * dt_s[j] * __uint_as_float(dx[e]);
+                        rsum += w[e];
+                    }
+                    // Mt, A2 as bf16: columns j = jb + 16 g16 .. +15 are chunks 2 g16, 2 g16 + 1 of tile k
+                    {
+                        float v0[8], v1[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            v0[e] = mt[e];
+                            v1[e] = mt[8 + e];
+                        }
+                        st8(tMT + k * kT16, r, 2 * g16, v0);
+                        st8(tMT + k * kT16, r, 2 * g16 + 1, v1);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            v0[e] = a2[e];
+                            v1[e] = a2[8 + e];
+                        }
+                        st8(tA2 + k * kT16, r, 2 * g16, v0);
+                        st8(tA2 + k * kT16, r, 2 * g16 + 1, v1);
+                    }
+                    // column sums over this warp's 32 rows
+                    warp_sum_rows_all<16>(w, lane);
+                    if ((lane & 1) == 0)
+                        colp[q * kR + jb + 16 * g16 + summed_row<16>(lane)] = w[0];
+                }
+                rowp[r] = rsum;
+                // zero the other chunk's block of this row
+                float zz[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    zz[e] = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc) {
+                    st8(tMT + (1 - k) * kT16, r, cc, zz);
+                    st8(tA2 + (1 - k) * kT16, r, cc, zz);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bars[BAR_ROWS1]);
+            // ---- rows 2a: G_out's lo terms (row n = r) into its tiles, once MMA 2 has read the hi
+            if (!(ok = wait_bar(&bars[BAR_MMA2], 0)))
+                break;
+            for (int kk = 0; kk < 2; ++kk)
+                stage_state(tG + kk * kT16, c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, true);
+            fence_proxy_async_smem();
+            warp_arrive(&bars[BAR_ROWS2A]);
+            // ---- rows 2: dx_j = D dy_j + dt_j (in + eo out); dt o B in place; h_in's hi terms
+            if (!(ok = wait_bar(&bars[BAR_MMA2B], 0)))
+                break;
+            tc_fence_after();
+            {
+                const float eo = ex2_approx(cs_last - cs_r), Dh = p.D[h];
+                float dsum = 0.f, vsum = 0.f;
+                float *dxg = p.dx + ((size_t)(b * p.L + t0 + r) * H + h) * kP;
+#pragma unroll 1
+                for (int g16 = 0; g16 < 4; ++g16) {
+                    uint32_t in[16], out[16];
+                    tmem_ld16(trow + kColMTDY + 16 * g16, in);
+                    tmem_ld16(trow + kColBG + 64 * k + 16 * g16, out);
+                    tmem_wait_ld();
+                    float xv[16], yv[16], o[16];
+                    {
+                        float t8[8];
+                        ld8(tX, r, 2 * g16, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            xv[e] = t8[e];
+                        ld8(tX, r, 2 * g16 + 1, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            xv[8 + e] = t8[e];
+                        ld8(tDY, r, 2 * g16, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            yv[e] = t8[e];
+                        ld8(tDY, r, 2 * g16 + 1, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            yv[8 + e] = t8[e];
+                    }
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float ov = __uint_as_float(out[e]);
+                        const float gx = fmaf(eo, ov, __uint_as_float(in[e]));
+                        dsum = fmaf(xv[e], gx, dsum);
+                        vsum = fmaf(xv[e], ov, vsum);
+                        o[e] = fmaf(Dh, yv[e], dt_r * gx);
+                    }
+                    if (r < nq) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(dxg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    }
+                }
+                ddir[r] = dsum;
+                vv[r] = dt_r * eo * vsum;
+                // B_j <- dt_j B_j (row j = r), for A2 (dt o B) in MMA 3
+#pragma unroll 1
+                for (int tt = 0; tt < 2; ++tt)
+                    for (int cc = 0; cc < 8; ++cc) {
+                        float v[8];
+                        ld8(tB + tt * kT16, r, cc, v);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            v[e] *= dt_r;
+                        st8(tB + tt * kT16, r, cc, v);
+                    }
+                // h_in of both chunks (row n = r), its hi terms, into Mt's space, for MMA 4
+                for (int kk = 0; kk < 2; ++kk) {
+                    const bool v = c0 + kk < nc;
+                    stage_state(tMT + kk * kT16, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r, false);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            warp_arrive(&bars[BAR_ROWS2]);
+            // ---- rows 3: dB_j = dt_j (in + eo out)
+            if (!(ok = wait_bar(&bars[BAR_MMA3], 0)))
+                break;
+            tc_fence_after();
+            {
+                const float eo = ex2_approx(cs_last - cs_r);
+                float *dbg = p.dB_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
+#pragma unroll 1
+                for (int g16 = 0; g16 < 8; ++g16) {
+                    uint32_t in[16], out[16];
+                    tmem_ld16(trow + kColA2C + 16 * g16, in);
+                    tmem_ld16(trow + kColXG + 128 * k + 16 * g16, out);
+                    tmem_wait_ld();
+                    if (r < nq) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4) {
+                            float o[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u)
+                                o[u] = dt_r * fmaf(eo, __uint_as_float(out[e + u]), __uint_as_float(in[e + u]));
+                            *reinterpret_cast<float4 *>(dbg + 16 * g16 + e) = make_float4(o[0], o[1], o[2], o[3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            warp_arrive(&bars[BAR_ROWS3]);
+            // ---- rows 4a: h_in's lo terms into Mt's space, once MMA 4 has read the hi
+            if (!(ok = wait_bar(&bars[BAR_MMA4], 0)))
+                break;
+            for (int kk = 0; kk < 2; ++kk)
+                stage_state(tMT + kk * kT16, c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r,
+                            true);
+            fence_proxy_async_smem();
+            warp_arrive(&bars[BAR_ROWS4A]);
+            // ---- rows 4: dC_s = in + e^{cs_s} out, u_s = C_s . e^{cs_s} out
+            if (!(ok = wait_bar(&bars[BAR_MMA4B], 0)))
+                break;
+            tc_fence_after();
+            {
+                const float es = ex2_approx(cs_r);
+                float usum = 0.f;
+                float *dcg = p.dC_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
+#pragma unroll 1
+                for (int g16 = 0; g16 < 8; ++g16) {
+                    uint32_t in[16], out[16];
+                    tmem_ld16(trow + kColA2B + 16 * g16, in);
+                    tmem_ld16(trow + kColDYH + 128 * k + 16 * g16, out);
+                    tmem_wait_ld();
+                    float cv[16];
+                    {
+                        float t8[8];
+                        ld8(tC + (g16 >> 2) * kT16, r, 2 * (g16 & 3), t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            cv[e] = t8[e];
+                        ld8(tC + (g16 >> 2) * kT16, r, 2 * (g16 & 3) + 1, t8);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            cv[8 + e] = t8[e];
+                    }
+                    float o[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        const float inter = es * __uint_as_float(out[e]);
+                        usum = fmaf(cv[e], inter, usum);
+                        o[e] = __uint_as_float(in[e]) + inter;
+                    }
+                    if (r < nq) {
+#pragma unroll
+                        for (int e = 0; e < 16; e += 4)
+                            *reinterpret_cast<float4 *>(dcg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
+                    }
+                }
+                uu[r] = usum;
+            }
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            // ---- dL/dcs_t = row sum - column sum + u - v; suffix sums within each chunk,
+            //      <G_out, h_last> entering at the chunk's last step
+            {
+                const float cl = colp[(2 * k) * kR + r] + colp[(2 * k + 1) * kR + r];
+                dcs[r] = rowp[r] - cl + uu[r] - vv[r];
+            }
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            if ((q & 1) == 0) {   // warp 2k: chunk k's 64 steps, two per lane
+                const float ghs = red[8 * k] + red[8 * k + 1] + red[8 * k + 2] + red[8 * k + 3];
+                const int base = 64 * k;
+                const float v0 = dcs[base + 2 * lane], v1 = dcs[base + 2 * lane + 1];
+                float s = v0 + v1;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float t = __shfl_down_sync(0xffffffffu, s, o);
+                    if (lane + o < 32)
+                        s += t;
+                }
+                float after = __shfl_down_sync(0xffffffffu, s, 1);
+                if (lane == 31)
+                    after = 0.f;
+                const float s1 = ghs + after + v1;
+                dcs[base + 2 * lane + 1] = s1;
+                dcs[base + 2 * lane] = s1 + v0;
+            }
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            // ddt_raw; the chunk's partials: a sum dt dlogdA, sum ddt_raw, sum dy . x
+            {
+                float cda = 0.f, cdb = 0.f;
+                if (r < nq) {
+                    const float ddt = fmaf(a, dcs[r], ddir[r]);
+                    cdb = ddt / (1.f + expf(-z_s[r]));
+                    p.ddt_raw[(size_t)(b * p.L + t0 + r) * H + h] = cdb;
+                    cda = dt_r * dcs[r];
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    cda += __shfl_xor_sync(0xffffffffu, cda, o);
+                    cdb += __shfl_xor_sync(0xffffffffu, cdb, o);
+                }
+                if (lane == 0) {
+                    red[24 + q] = cda;
+                    red[28 + q] = cdb;
+                }
+            }
+            if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
+                break;
+            if (lane == 0 && (q & 1) == 0 && cvalid) {
+                const size_t BHC = (size_t)gridDim.y * nc, i = (size_t)bh * nc + c;
+                p.part[i] = a * (red[24 + q] + red[24 + q + 1]);
+                p.part[BHC + i] = red[28 + q] + red[28 + q + 1];
+                p.part[2 * BHC + i] = red[16 + q] + red[16 + q + 1];
+            }
+        } while (false);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kIssueWarp)
+        tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(int dtype, int headdim, int dstate)
+{
+    return dtype == SSD_DTYPE_BF16 && headdim == kP && dstate == kN;
+}
+
+cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t st)
+{
+    SSD_NVTX_RANGE("bwd_tc_grad_launch");
+    TcMaps maps;
+    const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
+    if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
+        !make_tmap_bf16_3d(&maps.dy, a.dy, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
+        !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
+        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128))
+        return cudaErrorInvalidValue;
+    TcParams p;
+    p.dt_raw = a.dt_raw;
+    p.dt_bias = a.dt_bias;
+    p.A_log = a.A_log;
+    p.D = a.D;
+    p.S = a.S;
+    p.R = a.R;
+    p.dx = a.dx;
+    p.ddt_raw = a.ddt_raw;
+    p.dB_head = a.dB_head;
+    p.dC_head = a.dC_head;
+    p.part = a.part;
+    p.L = a.seqlen;
+    p.H = a.nheads;
+    p.G = a.ngroups;
+    p.nc = a.nc;
+    const cudaError_t e =
+        cudaFuncSetAttribute(ssd_bwd_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    const dim3 grid((unsigned)((a.nc + 1) / 2), (unsigned)(a.batch * a.nheads));
+    ssd_bwd_tc_grad_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
+    return cudaGetLastError();
+}
+
+ssd_status_t bwd_tc_read_device_error(uint32_t *code)
+{
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_bwd_tc_error, sizeof(v)) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_bwd_tc_error, &zero, sizeof(zero)) != cudaSuccess)
+        return SSD_ERR_CUDA;
+    *code = v;
+    return SSD_OK;
+}
+
+}  // namespace ssd

@@ -124,6 +124,8 @@ struct BwdArgs {
     int nheads, headdim, dstate, ngroups;
     int dtype;
     uint32_t path;                              // SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED (resolved)
+    bool fp32_form = false;                     // the chunk form's fp32 contractions even where the
+                                                // tensor-core gradient pass applies (SSD_BWD_FP32_FORM)
 };
 // ssd_bwd.cu: dispatch, the sequential kernel and the fixed-order reductions
 bool bwd_seq_supported(const BwdArgs &a);
@@ -133,6 +135,19 @@ cudaError_t bwd_launch(const BwdArgs &a, void *workspace, cudaStream_t stream);
 // dB, dC from the per-head buffers; dA_log, ddt_bias, dD from nper partials per (b, h)
 cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const float *dC_head, const float *part,
                               int nper, cudaStream_t stream);
+// ssd_bwd_tc.cu: the chunk form's gradient pass on the tensor cores (bf16, P = 64,
+// N = 128), from the chunk states and state gradients the first two launches left
+struct BwdTcArgs {
+    const void *x, *B, *C, *dy;                 // bf16
+    const float *dt_raw, *dt_bias, *A_log, *D;
+    const float *S, *R;                         // [B*H][nc+1][N][P] entering states; [B*H][nc][N][P] G_out
+    float *dx, *ddt_raw, *dB_head, *dC_head, *part;
+    int64_t batch, seqlen;
+    int nheads, ngroups, nc;
+};
+bool bwd_tc_supported(int dtype, int headdim, int dstate);
+cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t stream);
+ssd_status_t bwd_tc_read_device_error(uint32_t *code);
 // ssd_bwd_chunk.cu: the chunk-parallel backward (P <= 64, N <= 128)
 bool bwd_chunk_supported(const BwdArgs &a);
 size_t bwd_chunk_workspace_bytes(const BwdArgs &a);

@@ -14,6 +14,7 @@ from .build import LIB_PATH
 
 PATH_AUTO = 0
 DIAG_STALL_HANDOFF = 0x100
+BWD_FP32_FORM = 0x200   # ssd_scan_bwd: the chunk form's fp32 contractions even where the tensor-core pass applies
 PATH_SEQUENTIAL = 1
 PATH_CHUNKED = 2
 PATH_DECODE = 3
@@ -419,9 +420,11 @@ def gated_rmsnorm_fwd(y, z, weight, eps=1e-6, *, out=None, stream=None):
 
 
 def ssd_scan_bwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final=None, *, path="auto",
-                 stream=None):
+                 stream=None, fp32_form=False):
     """Gradients of ``ssd_scan_fwd`` given ``dy`` (and ``d_final``).  Returns a
-    dict of fp32 CUDA tensors: dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init."""
+    dict of fp32 CUDA tensors: dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init.
+    ``fp32_form`` keeps the chunk form's fp32 contractions where its tensor-core
+    gradient pass would apply (bf16, P = 64, N = 128)."""
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     f32 = dict(dtype=torch.float32, device=x.device)
@@ -433,6 +436,8 @@ def ssd_scan_bwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final=Non
              ("init_state", init_state), ("dy", dy), ("d_final", d_final)) + tuple(out.items())
     _require_cuda(named)
     d = make_dims(Bt, L, H, P, N, G, 1, x.dtype, path)
+    if fp32_form:
+        d.flags |= BWD_FP32_FORM
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     _check(_lib.ssd_scan_bwd(*(_ptr(t) for _, t in named), ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)),
            "ssd_scan_bwd")
