@@ -163,27 +163,34 @@ __device__ __forceinline__ void st8(uint8_t *tile, int r, int c, const float (&v
 
 // a chunk's fp32 state [n][p] (row n of this thread) into a bf16 tile, zero when
 // absent: its hi term bf16(v) (lo false) or its lo term bf16(v - hi) (lo true)
-__device__ __forceinline__ void stage_state(uint8_t *tile, const float *src, int n, bool lo)
+// (all 16 loads of the row are issued before the first store); with dot, also
+// returns the row's dot product with the same row of another state (0 when absent)
+__device__ __forceinline__ float stage_state(uint8_t *tile, const float *src, int n, bool lo,
+                                             const float *dot = nullptr)
 {
+    float4 a[16], o[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = src ? __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[i] = (src && dot) ? __ldg(reinterpret_cast<const float4 *>(dot + (size_t)n * kP + 4 * i))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float d = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        d = fmaf(a[i].x, o[i].x, fmaf(a[i].y, o[i].y, fmaf(a[i].z, o[i].z, fmaf(a[i].w, o[i].w, d))));
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
-        float v[8];
-        if (src) {
-            const float4 a = __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 8 * c));
-            const float4 b = __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 8 * c + 4));
-            v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-            if (lo) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
-            }
-        } else {
+        float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w, a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z,
+                      a[2 * c + 1].w};
+        if (lo) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                v[e] = 0.f;
+                v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
         }
         st8(tile, n, c, v);
     }
+    return d;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
@@ -229,6 +236,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
 
     if (warp == kIssueWarp) {
         if (lane == 0) {
+            // the state blocks this CTA reads (G_out and h_in of both chunks, and the
+            // state after the pair) into L2 now: the row warps stage them in several passes
+            for (int kk = 0; kk < 2; ++kk)
+                if (c0 + kk < nc) {
+                    const float *blocks[2] = {p.R + ((size_t)bh * nc + c0 + kk) * NP,
+                                              p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP};
+                    for (const float *blk : blocks)
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(blk), "r"((uint32_t)(NP * 4))
+                                     : "memory");
+                }
+            {
+                const int cl = min(c0 + 2, nc);   // h_last of the pair's last chunk
+                const float *blk = p.S + ((size_t)bh * (nc + 1) + cl) * NP;
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(blk), "r"((uint32_t)(NP * 4)) : "memory");
+            }
             // ---- TMA: C, B (two 64-column tiles each), x, dy
             const uint64_t pol = policy_evict_first();
             mbar_arrive_expect_tx(&bars[BAR_FULL], 6 * kT16);
@@ -349,28 +371,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 }
                 cs_s[r] = v;
             }
-            // both chunks' G_out (row n = r of each) into bf16 tiles, and this row's
-            // share of <G_out, h_last> per chunk (summed per warp; over the warps below)
-#pragma unroll 1
+            // both chunks' G_out (row n = r of each), its hi terms, into bf16 tiles, and
+            // this row's share of <G_out, h_last> per chunk (summed per warp here; over
+            // the warps at the end)
+#pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const bool v = c0 + kk < nc;
-                const float *G2 = v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr;
-                stage_state(tG + kk * kT16, G2, r, false);
-                float s = 0.f;
-                if (v) {
-                    const float *Gr = G2 + (size_t)r * kP;
-                    const float *Hr = p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP + (size_t)r * kP;
-                    for (int e = 0; e < kP; e += 4) {
-                        const float4 ga = __ldg(reinterpret_cast<const float4 *>(Gr + e));
-                        const float4 ha = __ldg(reinterpret_cast<const float4 *>(Hr + e));
-                        s = fmaf(ga.x, ha.x, fmaf(ga.y, ha.y, fmaf(ga.z, ha.z, fmaf(ga.w, ha.w, s))));
-                    }
-                }
+                float s2 = stage_state(tG + kk * kT16, v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, false,
+                                       v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP : nullptr);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
-                    s += __shfl_xor_sync(0xffffffffu, s, o);
+                    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
                 if (lane == 0)
-                    red[8 * kk + q] = s;
+                    red[8 * kk + q] = s2;
             }
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS0]);
@@ -469,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             // ---- rows 2a: G_out's lo terms (row n = r) into its tiles, once MMA 2 has read the hi
             if (!(ok = wait_bar(&bars[BAR_MMA2], 0)))
                 break;
+#pragma unroll
             for (int kk = 0; kk < 2; ++kk)
                 stage_state(tG + kk * kT16, c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, true);
             fence_proxy_async_smem();
@@ -535,6 +549,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                         st8(tB + tt * kT16, r, cc, v);
                     }
                 // h_in of both chunks (row n = r), its hi terms, into Mt's space, for MMA 4
+#pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const bool v = c0 + kk < nc;
                     stage_state(tMT + kk * kT16, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r, false);
@@ -573,6 +588,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             // ---- rows 4a: h_in's lo terms into Mt's space, once MMA 4 has read the hi
             if (!(ok = wait_bar(&bars[BAR_MMA4], 0)))
                 break;
+#pragma unroll
             for (int kk = 0; kk < 2; ++kk)
                 stage_state(tMT + kk * kT16, c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r,
                             true);
