@@ -61,9 +61,10 @@ using namespace ssd::ptx;
 constexpr int kR = 128;              // rows: two chunks of 64 steps
 constexpr int kCq = 64;              // steps per chunk
 constexpr int kP = 64, kN = 128;
-constexpr int kRowWarps = 4;         // warps 0-3: TMEM lane quarters, one row each per thread
-constexpr int kIssueWarp = 4;        // TMA and MMA issue, TMEM owner
-constexpr int kThreads = 5 * 32;
+constexpr int kRowWarps = 8;         // warps 0-7: warp w reads TMEM lane quarter w & 3 (one row per
+                                     // thread) and takes column half w >> 2 of that row's work
+constexpr int kIssueWarp = 8;        // TMA and MMA issue, TMEM owner
+constexpr int kThreads = 9 * 32;
 constexpr uint32_t kT16 = 16384;     // one [128 rows][64 bf16] tile with the 128-byte swizzle
 
 // shared memory (from a 1024-aligned base)
@@ -75,8 +76,9 @@ constexpr uint32_t kOffG = kOffDY + kT16;        // G_out of chunk 0, 1: [n][p]
 constexpr uint32_t kOffMT = kOffG + 2 * kT16;    // Mt [s][j]: tiles j 0-63, 64-127; later h_in of chunk 0, 1
 constexpr uint32_t kOffA2 = kOffMT + 2 * kT16;   // A2 [s][j]
 constexpr uint32_t kOffArr = kOffA2 + 2 * kT16;
-// per-row float arrays of 128
-enum { A_DT = 0, A_Z, A_CS2, A_ROWP, A_COLP0, A_DDIR = A_COLP0 + 4, A_VV, A_UU, A_DCS, A_NUM };   // COLP: 4 warps
+// per-row float arrays of 128 (ROWP, DDIR, VV, UU: one per column half; COLP: one per lane quarter)
+enum { A_DT = 0, A_Z, A_CS2, A_ROWP, A_COLP0 = A_ROWP + 2, A_DDIR = A_COLP0 + 4, A_VV = A_DDIR + 2, A_UU = A_VV + 2,
+       A_DCS = A_UU + 2, A_NUM };
 constexpr uint32_t kOffRed = kOffArr + A_NUM * kR * 4;   // 64 floats: per-warp sums
 constexpr uint32_t kOffBars = kOffRed + 64 * 4;
 enum {
@@ -133,7 +135,7 @@ __device__ __forceinline__ void warp_arrive(uint64_t *bar)
         mbar_arrive(bar);
 }
 
-// bounded barrier of the 4 row warps on an mbarrier (phase: this thread's copy)
+// bounded barrier of the row warps on an mbarrier (phase: this thread's copy)
 __device__ __forceinline__ bool rsync(uint64_t *bar, uint32_t &phase)
 {
     warp_arrive(bar);
@@ -161,26 +163,28 @@ __device__ __forceinline__ void st8(uint8_t *tile, int r, int c, const float (&v
                                                                 pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
 }
 
-// a chunk's fp32 state [n][p] (row n of this thread) into a bf16 tile, zero when
-// absent: its hi term bf16(v) (lo false) or its lo term bf16(v - hi) (lo true)
-// (all 16 loads of the row are issued before the first store); with dot, also
-// returns the row's dot product with the same row of another state (0 when absent)
-__device__ __forceinline__ float stage_state(uint8_t *tile, const float *src, int n, bool lo,
+// columns 32 hf .. 32 hf + 31 of a chunk's fp32 state [n][p] (row n of this
+// thread) into a bf16 tile, zero when absent: its hi term bf16(v) (lo false) or
+// its lo term bf16(v - hi) (lo true) (all loads issued before the first store);
+// with dot, also returns the dot product of those columns with the same ones of
+// another state (0 when absent)
+__device__ __forceinline__ float stage_state(uint8_t *tile, const float *src, int n, int hf, bool lo,
                                              const float *dot = nullptr)
 {
-    float4 a[16], o[16];
+    float4 a[8], o[8];
+    const size_t base = (size_t)n * kP + 32 * hf;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        a[i] = src ? __ldg(reinterpret_cast<const float4 *>(src + (size_t)n * kP + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        o[i] = (src && dot) ? __ldg(reinterpret_cast<const float4 *>(dot + (size_t)n * kP + 4 * i))
+    for (int i = 0; i < 8; ++i) {
+        a[i] = src ? __ldg(reinterpret_cast<const float4 *>(src + base + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        o[i] = (src && dot) ? __ldg(reinterpret_cast<const float4 *>(dot + base + 4 * i))
                             : make_float4(0.f, 0.f, 0.f, 0.f);
     }
     float d = 0.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
+    for (int i = 0; i < 8; ++i)
         d = fmaf(a[i].x, o[i].x, fmaf(a[i].y, o[i].y, fmaf(a[i].z, o[i].z, fmaf(a[i].w, o[i].w, d))));
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
+    for (int c = 0; c < 4; ++c) {
         float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w, a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z,
                       a[2 * c + 1].w};
         if (lo) {
@@ -188,7 +192,7 @@ __device__ __forceinline__ float stage_state(uint8_t *tile, const float *src, in
             for (int e = 0; e < 8; ++e)
                 v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
         }
-        st8(tile, n, c, v);
+        st8(tile, n, 4 * hf + c, v);
     }
     return d;
 }
@@ -203,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
     float *arr = reinterpret_cast<float *>(smem + kOffArr);
     float *red = reinterpret_cast<float *>(smem + kOffRed);
     float *dt_s = arr + A_DT * kR, *z_s = arr + A_Z * kR, *cs_s = arr + A_CS2 * kR, *rowp = arr + A_ROWP * kR;
-    float *colp = arr + A_COLP0 * kR;   // [4 warps][128]
+    float *colp = arr + A_COLP0 * kR;   // [4 lane quarters][128]
     float *ddir = arr + A_DDIR * kR, *vv = arr + A_VV * kR, *uu = arr + A_UU * kR, *dcs = arr + A_DCS * kR;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -342,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
         }
     } else {
         // ------------------------------------------------------------ rows
-        const int q = warp;                     // TMEM lane quarter
+        const int q = warp & 3;                 // TMEM lane quarter
+        const int hf = warp >> 2;               // column half
         const int r = 32 * q + lane;            // this thread's row: step t0 + r
         const int k = r >> 6;                   // its chunk (0, 1)
         const int c = c0 + k;
@@ -354,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
         uint32_t rphase = 0;
         do {
             // ---- per step: dt, z and the cumulative sum of dt a within the chunk (log2 units)
-            {
+            if (hf == 0) {
                 float dt = 0.f, z = 0.f;
                 if (r < nq) {
                     z = p.dt_raw[(size_t)(b * p.L + t0 + r) * H + h] + p.dt_bias[h];
@@ -371,19 +376,19 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 }
                 cs_s[r] = v;
             }
-            // both chunks' G_out (row n = r of each), its hi terms, into bf16 tiles, and
-            // this row's share of <G_out, h_last> per chunk (summed per warp here; over
-            // the warps at the end)
+            // both chunks' G_out (row n = r of each, this half's columns), its hi terms,
+            // into bf16 tiles, and their share of <G_out, h_last> per chunk (summed per
+            // warp here; over the warps at the end)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const bool v = c0 + kk < nc;
-                float s2 = stage_state(tG + kk * kT16, v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, false,
-                                       v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP : nullptr);
+                float s2 = stage_state(tG + kk * kT16, v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, hf,
+                                       false, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP : nullptr);
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1)
                     s2 += __shfl_xor_sync(0xffffffffu, s2, o);
                 if (lane == 0)
-                    red[8 * kk + q] = s2;
+                    red[8 * kk + warp] = s2;
             }
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS0]);
@@ -395,13 +400,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             const float cs_pre = (q & 1) ? cs_s[32 * (q - 1) + 31] : 0.f;
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
-            cs_s[r] += cs_pre;
+            if (hf == 0)
+                cs_s[r] += cs_pre;
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
-            // sum over the chunk of dy . x (this row)
+            // sum over the chunk of dy . x (this row, this half's columns)
             {
                 float d = 0.f;
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
                     float xv[8], yv[8];
                     ld8(tX, r, cc, xv);
                     ld8(tDY, r, cc, yv);
@@ -413,12 +419,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 for (int o = 16; o > 0; o >>= 1)
                     d += __shfl_xor_sync(0xffffffffu, d, o);
                 if (lane == 0)
-                    red[16 + q] = d;
+                    red[16 + warp] = d;
             }
             const float cs_r = cs_s[r];
             const float cs_last = cs_s[64 * k + 63];
             const float dt_r = dt_s[r];
-            // ---- rows 1: Mt, A2 from CB, DX (this row's chunk block), W's sums
+            // ---- rows 1: Mt, A2 from CB, DX (this half of this row's chunk block), W's sums
             if (!(ok = wait_bar(&bars[BAR_MMA1], 0)))
                 break;
             tc_fence_after();
@@ -426,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 float rsum = 0.f;
                 const int jb = 64 * k;   // the block of this row's chunk
 #pragma unroll 1
-                for (int g16 = 0; g16 < 4; ++g16) {
+                for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
                     uint32_t cb[16], dx[16];
                     tmem_ld16(trow + kColCB + jb + 16 * g16, cb);
                     tmem_ld16(trow + kColDX + jb + 16 * g16, dx);
@@ -464,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                     if ((lane & 1) == 0)
                         colp[q * kR + jb + 16 * g16 + summed_row<16>(lane)] = w[0];
                 }
-                rowp[r] = rsum;
-                // zero the other chunk's block of this row
+                rowp[hf * kR + r] = rsum;
+                // zero the other chunk's block of this row (this half's columns)
                 float zz[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     zz[e] = 0.f;
 #pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
+                for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
                     st8(tMT + (1 - k) * kT16, r, cc, zz);
                     st8(tA2 + (1 - k) * kT16, r, cc, zz);
                 }
@@ -484,7 +490,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 break;
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
-                stage_state(tG + kk * kT16, c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, true);
+                stage_state(tG + kk * kT16, c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, hf,
+                            true);
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS2A]);
             // ---- rows 2: dx_j = D dy_j + dt_j (in + eo out); dt o B in place; h_in's hi terms
@@ -496,7 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 float dsum = 0.f, vsum = 0.f;
                 float *dxg = p.dx + ((size_t)(b * p.L + t0 + r) * H + h) * kP;
 #pragma unroll 1
-                for (int g16 = 0; g16 < 4; ++g16) {
+                for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
                     uint32_t in[16], out[16];
                     tmem_ld16(trow + kColMTDY + 16 * g16, in);
                     tmem_ld16(trow + kColBG + 64 * k + 16 * g16, out);
@@ -535,24 +542,24 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                             *reinterpret_cast<float4 *>(dxg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
                     }
                 }
-                ddir[r] = dsum;
-                vv[r] = dt_r * eo * vsum;
-                // B_j <- dt_j B_j (row j = r), for A2 (dt o B) in MMA 3
+                ddir[hf * kR + r] = dsum;
+                vv[hf * kR + r] = dt_r * eo * vsum;
+                // B_j <- dt_j B_j (row j = r; this half: B's tile hf), for A2 (dt o B) in MMA 3
 #pragma unroll 1
-                for (int tt = 0; tt < 2; ++tt)
-                    for (int cc = 0; cc < 8; ++cc) {
-                        float v[8];
-                        ld8(tB + tt * kT16, r, cc, v);
+                for (int cc = 0; cc < 8; ++cc) {
+                    float v[8];
+                    ld8(tB + hf * kT16, r, cc, v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            v[e] *= dt_r;
-                        st8(tB + tt * kT16, r, cc, v);
-                    }
+                    for (int e = 0; e < 8; ++e)
+                        v[e] *= dt_r;
+                    st8(tB + hf * kT16, r, cc, v);
+                }
                 // h_in of both chunks (row n = r), its hi terms, into Mt's space, for MMA 4
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk) {
                     const bool v = c0 + kk < nc;
-                    stage_state(tMT + kk * kT16, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r, false);
+                    stage_state(tMT + kk * kT16, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r, hf,
+                                false);
                 }
             }
             fence_proxy_async_smem();
@@ -566,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 const float eo = ex2_approx(cs_last - cs_r);
                 float *dbg = p.dB_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
 #pragma unroll 1
-                for (int g16 = 0; g16 < 8; ++g16) {
+                for (int g16 = 4 * hf; g16 < 4 * hf + 4; ++g16) {
                     uint32_t in[16], out[16];
                     tmem_ld16(trow + kColA2C + 16 * g16, in);
                     tmem_ld16(trow + kColXG + 128 * k + 16 * g16, out);
@@ -591,7 +598,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk)
                 stage_state(tMT + kk * kT16, c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r,
-                            true);
+                            hf, true);
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS4A]);
             // ---- rows 4: dC_s = in + e^{cs_s} out, u_s = C_s . e^{cs_s} out
@@ -603,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 float usum = 0.f;
                 float *dcg = p.dC_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
 #pragma unroll 1
-                for (int g16 = 0; g16 < 8; ++g16) {
+                for (int g16 = 4 * hf; g16 < 4 * hf + 4; ++g16) {
                     uint32_t in[16], out[16];
                     tmem_ld16(trow + kColA2B + 16 * g16, in);
                     tmem_ld16(trow + kColDYH + 128 * k + 16 * g16, out);
@@ -633,20 +640,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                             *reinterpret_cast<float4 *>(dcg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
                     }
                 }
-                uu[r] = usum;
+                uu[hf * kR + r] = usum;
             }
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
             // ---- dL/dcs_t = row sum - column sum + u - v; suffix sums within each chunk,
             //      <G_out, h_last> entering at the chunk's last step
-            {
+            if (hf == 0) {
                 const float cl = colp[(2 * k) * kR + r] + colp[(2 * k + 1) * kR + r];
-                dcs[r] = rowp[r] - cl + uu[r] - vv[r];
+                dcs[r] = (rowp[r] + rowp[kR + r]) - cl + (uu[r] + uu[kR + r]) - (vv[r] + vv[kR + r]);
             }
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
-            if ((q & 1) == 0) {   // warp 2k: chunk k's 64 steps, two per lane
-                const float ghs = red[8 * k] + red[8 * k + 1] + red[8 * k + 2] + red[8 * k + 3];
+            if (warp == 2 * k) {   // warp 2k: chunk k's 64 steps, two per lane
+                float ghs = 0.f;
+#pragma unroll
+                for (int w = 0; w < kRowWarps; ++w)
+                    ghs += red[8 * k + w];
                 const int base = 64 * k;
                 const float v0 = dcs[base + 2 * lane], v1 = dcs[base + 2 * lane + 1];
                 float s = v0 + v1;
@@ -666,10 +676,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
             // ddt_raw; the chunk's partials: a sum dt dlogdA, sum ddt_raw, sum dy . x
-            {
+            if (hf == 0) {
                 float cda = 0.f, cdb = 0.f;
                 if (r < nq) {
-                    const float ddt = fmaf(a, dcs[r], ddir[r]);
+                    const float ddt = fmaf(a, dcs[r], ddir[r] + ddir[kR + r]);
                     cdb = ddt / (1.f + expf(-z_s[r]));
                     p.ddt_raw[(size_t)(b * p.L + t0 + r) * H + h] = cdb;
                     cda = dt_r * dcs[r];
@@ -686,11 +696,11 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             }
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
-            if (lane == 0 && (q & 1) == 0 && cvalid) {
+            if (lane == 0 && hf == 0 && (q & 1) == 0 && cvalid) {
                 const size_t BHC = (size_t)gridDim.y * nc, i = (size_t)bh * nc + c;
                 p.part[i] = a * (red[24 + q] + red[24 + q + 1]);
                 p.part[BHC + i] = red[28 + q] + red[28 + q + 1];
-                p.part[2 * BHC + i] = red[16 + q] + red[16 + q + 1];
+                p.part[2 * BHC + i] = (red[16 + q] + red[16 + q + 1]) + (red[20 + q] + red[20 + q + 1]);
             }
         } while (false);
     }
