@@ -1007,17 +1007,31 @@ def run_gpu_neighbor(args, w: Workload):
             "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
             "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3}
     if w.op == "bwd" and w.headdim <= 64 and w.dstate <= 128:
-        # the chunk-form backward: fp32 FFMA contractions dominate its time, so
-        # its roofline is the fp32 pipe; the whole call (5 launches) is timed
+        # the chunk-form backward, whole call (5 launches) timed.  Its contractions
+        # run on the tensor cores for bf16 with P = 64, N = 128 (the chunk states
+        # and the gradient pass), else as fp32 FFMA: the roofline is that pipe.
         flops = bwd_chunk_flops(w)
         tf = flops / avg_launch_s / 1e12
-        roof = {"bound": "alu", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_local_kernel, ssd_bwd_pass_kernel, "
-                                          "ssd_bwd_grad_kernel, ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
-                "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_PEAK_TFLOPS,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
-                "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
-                "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
-                "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
+        if w.dtype == "bf16" and w.headdim == 64 and w.dstate == 128:
+            tc_peak = float(peaks["bf16_tflops"])
+            roof = {"bound": "tensor", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_tc_local_kernel, "
+                                                  "ssd_bwd_pass_kernel, ssd_bwd_tc_grad_kernel, "
+                                                  "ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
+                    "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
+                    "peak_source": peak_src + " (bf16 dense, burst)",
+                    "traffic": stored_traffic(w.name, kernel), "contraction_flops_per_launch": flops,
+                    "fp32_pipe_frac": tf / FP32_PEAK_TFLOPS,
+                    "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
+                    "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (tc_peak * 1e12) * 1e3,
+                    "note": "latency-bound: neither the tensor pipe nor HBM is busy (see its profile)"}
+        else:
+            roof = {"bound": "alu", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_local_kernel, ssd_bwd_pass_kernel, "
+                                              "ssd_bwd_grad_kernel, ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
+                    "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_PEAK_TFLOPS,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
+                    "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
+                    "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
+                    "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
     if w.op == "complex" and w.seqlen > 1:
         # the state stays in registers over the sequence: fp32 arithmetic bounds it
         flops = complex_flops(w)

@@ -895,6 +895,8 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     p.nc = nc;
     const dim3 grid((unsigned)nc, (unsigned)BH);
     const bool bf = a.dtype == SSD_DTYPE_BF16;
+    // the tensor-core form (ssd_bwd_tc.cu) of the chunk states and of the gradient pass
+    const bool tc = bf && !a.fp32_form && bwd_tc_supported(a.dtype, a.headdim, a.dstate);
     cudaError_t e;
     if (bf) {
         e = cudaFuncSetAttribute(ssd_bwd_local_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -911,17 +913,38 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     }
     if (e != cudaSuccess)
         return e;
-    if (bf)
+    if (tc) {
+        BwdTcLocalArgs t;
+        t.x = a.x;
+        t.B = a.B;
+        t.C = a.C;
+        t.dy = a.dy;
+        t.dt_raw = a.dt_raw;
+        t.dt_bias = a.dt_bias;
+        t.A_log = a.A_log;
+        t.S = p.S;
+        t.R = p.R;
+        t.dec = p.dec;
+        t.batch = a.batch;
+        t.seqlen = a.seqlen;
+        t.nheads = a.nheads;
+        t.ngroups = a.ngroups;
+        t.nc = nc;
+        e = bwd_tc_local_launch(t, st);
+        if (e != cudaSuccess)
+            return e;
+    } else if (bf) {
         ssd_bwd_local_kernel<__nv_bfloat16><<<grid, kThreads, kLocalSmem, st>>>(p);
-    else
+    } else {
         ssd_bwd_local_kernel<float><<<grid, kThreads, kLocalSmem, st>>>(p);
+    }
     if (NP % kVec == 0)
         ssd_bwd_pass_kernel<kVec><<<dim3((unsigned)((NP / kVec + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads,
                                     0, st>>>(p);
     else
         ssd_bwd_pass_kernel<1><<<dim3((unsigned)((NP + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
-    if (bf && !a.fp32_form && bwd_tc_supported(a.dtype, a.headdim, a.dstate)) {
-        // the gradient pass on the tensor cores (ssd_bwd_tc.cu)
+    if (tc) {
+        // the gradient pass on the tensor cores
         BwdTcArgs t;
         t.x = a.x;
         t.B = a.B;

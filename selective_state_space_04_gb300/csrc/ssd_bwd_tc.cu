@@ -712,6 +712,199 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
         tmem_dealloc(tmem, 512);
 }
 
+
+// ---------------------------------------------------------------- chunk states
+// The chunk form's first launch on the tensor cores: for one 64-step chunk,
+//   S(c) = sum_j e^{cs_last - cs_j} dt_j B_j x_j^T,   R(c) = sum_s e^{cs_s} C_s dy_s^T
+// ([N][P] each, rows n) and e^{cs_last(c)}.  Both are M = 128 (n) x N = 64 (p)
+// x K = 64 (steps) products with MN-major operands: B (C) as the TMA loads it,
+// and x (dy) scaled per step by w_j = e^{cs_last - cs_j} dt_j (e^{cs_s}) in place.
+// The scaled operand enters as hi = bf16(v) and lo = bf16(v - hi), two products
+// into one accumulator, so the states keep about 16 significant bits of the
+// scaled inputs (B, C, x and dy themselves are exact in bf16).  The results
+// leave through shared memory (128-byte swizzle: a thread writing its own row
+// meets no bank conflict) by tensor stores.
+constexpr int kLq = 64;                       // steps per chunk
+constexpr int kLThreads = 128;                // 4 warps: rows, then TMEM lane quarters; thread 0 issues
+constexpr uint32_t kLT = 8192;                // one [64 rows][64 bf16] tile with the 128-byte swizzle
+constexpr uint32_t kLOffB = 0, kLOffC = 2 * kLT, kLOffX = 4 * kLT, kLOffDY = 5 * kLT, kLOffXL = 6 * kLT,
+                   kLOffDYL = 7 * kLT;
+constexpr uint32_t kLOut = 16384;             // one [128 n][32 p] fp32 box; the four boxes reuse the inputs
+constexpr uint32_t kLOffArr = 8 * kLT;        // dt, cs (raw two-warp scans), w, e: 64 floats each
+constexpr uint32_t kLOffBars = kLOffArr + 4 * kLq * 4;
+constexpr uint32_t kLOffHolder = kLOffBars + 16;
+constexpr uint32_t kLSmemBytes = kLOffHolder + 16 + 1024;
+static_assert(4 * kLOut <= kLOffArr, "the output boxes must fit in the input tiles");
+
+struct TcLocalParams {
+    const float *dt_raw, *dt_bias, *A_log;
+    float *dec;   // [B*H][nc]: e^{cs_last(c)}
+    long long L;
+    int H, G, nc;
+};
+
+struct TcLocalMaps {
+    CUtensorMap x, dy, B, C;   // bf16, boxes of 64 x 64
+    CUtensorMap S, R;          // fp32 [slot][n][p], boxes of 32 p x 128 n
+};
+
+__global__ void __launch_bounds__(kLThreads) ssd_bwd_tc_local_kernel(const __grid_constant__ TcLocalMaps maps,
+                                                                       const TcLocalParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kLOffBars);   // 0: tiles landed, 1: products done
+    uint32_t *holder = reinterpret_cast<uint32_t *>(smem + kLOffHolder);
+    float *dt_s = reinterpret_cast<float *>(smem + kLOffArr), *cs_s = dt_s + kLq, *w_s = cs_s + kLq,
+          *e_s = w_s + kLq;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, nc = p.nc, c = (int)blockIdx.x;
+    const long long bh = blockIdx.y, b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / p.G);
+    const long long t0 = (long long)c * kLq;
+    const int nq = (int)min((long long)kLq, p.L - t0);
+    const float a = -expf(p.A_log[h]);
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(holder, 128);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    if (tid == 0) {
+        // x, dy are read once; B, C again by the group's other heads
+        const uint64_t once = policy_evict_first(), shared = policy_evict_last();
+        mbar_arrive_expect_tx(&bars[0], 6 * kLT);
+        tma_load_3d(smem + kLOffB, &maps.B, &bars[0], g * kN, (int)t0, (int)b, shared);
+        tma_load_3d(smem + kLOffB + kLT, &maps.B, &bars[0], g * kN + 64, (int)t0, (int)b, shared);
+        tma_load_3d(smem + kLOffC, &maps.C, &bars[0], g * kN, (int)t0, (int)b, shared);
+        tma_load_3d(smem + kLOffC + kLT, &maps.C, &bars[0], g * kN + 64, (int)t0, (int)b, shared);
+        tma_load_3d(smem + kLOffX, &maps.x, &bars[0], h * kP, (int)t0, (int)b, once);
+        tma_load_3d(smem + kLOffDY, &maps.dy, &bars[0], h * kP, (int)t0, (int)b, once);
+    }
+    // dt and the inclusive cumsum of dt a within each warp of the chunk's 64 steps
+    if (tid < kLq) {
+        float dt = 0.f;
+        if (tid < nq)
+            dt = softplus_f32(p.dt_raw[(size_t)(b * p.L + t0 + tid) * H + h] + p.dt_bias[h]);
+        dt_s[tid] = dt;
+        float v = dt * a;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o)
+                v += u;
+        }
+        cs_s[tid] = v;
+    }
+    __syncthreads();
+    // the step weights (the second warp's cumsums continue the first's)
+    if (tid < kLq) {
+        const float c31 = cs_s[31];
+        const float cs = cs_s[tid] + (tid >= 32 ? c31 : 0.f), cl = cs_s[kLq - 1] + c31;
+        w_s[tid] = expf(cl - cs) * dt_s[tid];
+        e_s[tid] = expf(cs);
+        if (tid == 0)
+            p.dec[bh * nc + c] = expf(cl);
+    }
+    __syncthreads();
+    bool ok = wait_bar(&bars[0], 0);
+    if (ok) {
+        // row j of x (threads 0-63) or of dy (64-127), scaled: hi in place, lo beside
+        const int j = tid & (kLq - 1);
+        const bool isx = tid < kLq;
+        uint8_t *hi = smem + (isx ? kLOffX : kLOffDY), *lo = smem + (isx ? kLOffXL : kLOffDYL);
+        const float sc = isx ? w_s[j] : e_s[j];
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+            float v[8], l[8];
+            ld8(hi, j, cc, v);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                v[e] *= sc;
+                l[e] = v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+            }
+            st8(hi, j, cc, v);
+            st8(lo, j, cc, l);
+        }
+        fence_proxy_async_smem();
+    }
+    ok = __syncthreads_and(ok);
+    const bool issued = ok;
+    if (tid == 0 && ok) {
+        tc_fence_after();
+        const uint32_t i64nn = idesc_bf16_f32(128, 64, 1, 1);
+        // MN-major operand, k-step kk = steps 16 kk .. +15; the two 64-element n blocks kLT apart
+        auto mn = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kLT, 1024); };
+        const uint32_t sB = smem_u32(smem + kLOffB), sC = smem_u32(smem + kLOffC);
+        const uint32_t sX = smem_u32(smem + kLOffX), sXL = smem_u32(smem + kLOffXL);
+        const uint32_t sDY = smem_u32(smem + kLOffDY), sDYL = smem_u32(smem + kLOffDYL);
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem, mn(sB, kk), mn(sX, kk), i64nn, kk > 0);
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem, mn(sB, kk), mn(sXL, kk), i64nn, 1);
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + 64, mn(sC, kk), mn(sDY, kk), i64nn, kk > 0);
+        for (int kk = 0; kk < 4; ++kk)
+            mma_ss(tmem + 64, mn(sC, kk), mn(sDYL, kk), i64nn, 1);
+        mma_commit(&bars[1]);
+    }
+    if (ok)
+        ok = wait_bar(&bars[1], 0);
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    if (ok) {
+        // thread n: row n of S (columns 0-63) and of R (64-127), 32 columns per box
+        const int n = tid;
+        const uint32_t trow = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+#pragma unroll 1
+        for (int q = 0; q < 4; ++q) {
+            uint32_t v[32];
+            tmem_ld32(trow + 32 * q, v);
+            tmem_wait_ld();
+            uint8_t *box = smem + q * kLOut + n * 128;
+#pragma unroll
+            for (int cc = 0; cc < 8; ++cc)
+                *reinterpret_cast<uint4 *>(box + ((cc ^ (n & 7)) << 4)) =
+                    make_uint4(v[4 * cc], v[4 * cc + 1], v[4 * cc + 2], v[4 * cc + 3]);
+        }
+        fence_proxy_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+        if (ok) {
+            const int slot_s = (int)(bh * (nc + 1) + c), slot_r = (int)(bh * nc + c);
+            tma_store_3d(&maps.S, smem, 0, 0, slot_s);
+            tma_store_3d(&maps.S, smem + kLOut, 32, 0, slot_s);
+            tma_store_3d(&maps.R, smem + 2 * kLOut, 0, 0, slot_r);
+            tma_store_3d(&maps.R, smem + 3 * kLOut, 32, 0, slot_r);
+            bulk_commit_group();
+            bulk_wait_all();
+        } else {
+            // after a timeout: no TMA load or product may still be in flight at exit
+            const uint64_t tw = globaltimer_ns();
+            while (!mbar_wait_for(&bars[0], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+            }
+            if (issued)
+                while (!mbar_wait_for(&bars[1], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+                }
+        }
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        tmem_dealloc(tmem, 128);
+}
+
 }  // namespace
 
 bool bwd_tc_supported(int dtype, int headdim, int dstate)
@@ -751,6 +944,36 @@ cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t st)
         return e;
     const dim3 grid((unsigned)((a.nc + 1) / 2), (unsigned)(a.batch * a.nheads));
     ssd_bwd_tc_grad_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
+    return cudaGetLastError();
+}
+
+cudaError_t bwd_tc_local_launch(const BwdTcLocalArgs &a, cudaStream_t st)
+{
+    SSD_NVTX_RANGE("bwd_tc_local_launch");
+    TcLocalMaps maps;
+    const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
+    const uint64_t BH = (uint64_t)a.batch * a.nheads, NP4 = (uint64_t)kN * kP * 4;
+    if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.dy, a.dy, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, kLq) ||
+        !make_tmap_f32_3d(&maps.S, a.S, kP, kN, BH * (a.nc + 1), kP * 4, NP4, 32, kN) ||
+        !make_tmap_f32_3d(&maps.R, a.R, kP, kN, BH * a.nc, kP * 4, NP4, 32, kN))
+        return cudaErrorInvalidValue;
+    TcLocalParams p;
+    p.dt_raw = a.dt_raw;
+    p.dt_bias = a.dt_bias;
+    p.A_log = a.A_log;
+    p.dec = a.dec;
+    p.L = a.seqlen;
+    p.H = a.nheads;
+    p.G = a.ngroups;
+    p.nc = a.nc;
+    const cudaError_t e = cudaFuncSetAttribute(ssd_bwd_tc_local_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kLSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    ssd_bwd_tc_local_kernel<<<dim3((unsigned)a.nc, (unsigned)BH), kLThreads, kLSmemBytes, st>>>(maps, p);
     return cudaGetLastError();
 }
 

@@ -145,7 +145,15 @@ struct BwdTcArgs {
     int64_t batch, seqlen;
     int nheads, ngroups, nc;
 };
+struct BwdTcLocalArgs {
+    const void *x, *B, *C, *dy;                 // bf16
+    const float *dt_raw, *dt_bias, *A_log;
+    float *S, *R, *dec;                         // [B*H][nc+1][N][P] (slots 0 .. nc-1 written), [B*H][nc][N][P], [B*H][nc]
+    int64_t batch, seqlen;
+    int nheads, ngroups, nc;
+};
 bool bwd_tc_supported(int dtype, int headdim, int dstate);
+cudaError_t bwd_tc_local_launch(const BwdTcLocalArgs &a, cudaStream_t stream);
 cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t stream);
 ssd_status_t bwd_tc_read_device_error(uint32_t *code);
 // ssd_bwd_chunk.cu: the chunk-parallel backward (P <= 64, N <= 128)

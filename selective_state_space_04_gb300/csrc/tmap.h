@@ -43,4 +43,22 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
     return r == CUDA_SUCCESS;
 }
 
+// The same for an fp32 tensor (box0 x 4 bytes must be at most 128: the
+// swizzle span).
+inline bool make_tmap_f32_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                             uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1)
+{
+    auto enc = tensor_map_encoder();
+    if (!enc)
+        return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {s1, s2};
+    cuuint32_t box[3] = {box0, box1, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace ssd
