@@ -896,7 +896,10 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     const dim3 grid((unsigned)nc, (unsigned)BH);
     const bool bf = a.dtype == SSD_DTYPE_BF16;
     // the tensor-core form (ssd_bwd_tc.cu) of the chunk states and of the gradient pass
-    const bool tc = bf && !a.fp32_form && bwd_tc_supported(a.dtype, a.headdim, a.dstate);
+    // (its tensor maps need 16-byte aligned bases)
+    auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const bool tc = bf && !a.fp32_form && bwd_tc_supported(a.dtype, a.headdim, a.dstate) && aligned16(a.x) &&
+                    aligned16(a.B) && aligned16(a.C) && aligned16(a.dy) && aligned16(a.dx);
     cudaError_t e;
     if (bf) {
         e = cudaFuncSetAttribute(ssd_bwd_local_kernel<__nv_bfloat16>, cudaFuncAttributeMaxDynamicSharedMemorySize,

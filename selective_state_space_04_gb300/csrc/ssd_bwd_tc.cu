@@ -36,6 +36,12 @@
 //   rows: dB.
 //   MMA 4: dy h_in^T (hi).   rows: h_in's lo terms.   MMA 4b: the lo terms.
 //   rows: dC, then d log dA's suffix sums, ddt_raw and the chunks' partials.
+// dx, dB and dC leave by tensor stores: each warp stages its 32 rows x 32
+// columns (128-byte swizzle, so a thread writing its own row meets no bank
+// conflict) in a tile whose last reader has finished -- dx in G_out's, dB in
+// B's and A2's, dC in x's, dy's and G_out's -- and one lane issues the store.
+// A warp drains its older store groups before its next hand-off, so no staging
+// area is rewritten while a store still reads it.
 // Operands rounded to bf16 once (Mt, A2, dt o B) bound the result's precision
 // as bf16 inputs bound the forward's: the bar is the forward's bf16 bar, not
 // fp32's.
@@ -105,7 +111,8 @@ struct TcParams {
 };
 
 struct TcMaps {
-    CUtensorMap x, dy, B, C;
+    CUtensorMap x, dy, B, C;       // bf16 loads, boxes of 64 x 128
+    CUtensorMap dx, dB, dC;        // fp32 stores, boxes of 32 x 32
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
@@ -161,6 +168,16 @@ __device__ __forceinline__ void st8(uint8_t *tile, int r, int c, const float (&v
 {
     *reinterpret_cast<uint4 *>(tile + sw128(r, c)) = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]),
                                                                 pack_bf16x2(v[4], v[5]), pack_bf16x2(v[6], v[7]));
+}
+
+// 16 fp32 values (columns 16 g .. 16 g + 15 of a 32-column box) of row r of a
+// [rows][32 fp32] staging box with the 128-byte swizzle (box 1024-byte aligned)
+__device__ __forceinline__ void stage16(uint8_t *box, int r, int g, const float (&o)[16])
+{
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4 *>(box + r * 128 + (((4 * g + i) ^ (r & 7)) << 4)) =
+            make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
 // columns 32 hf .. 32 hf + 31 of a chunk's fp32 state [n][p] (row n of this
@@ -501,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             {
                 const float eo = ex2_approx(cs_last - cs_r), Dh = p.D[h];
                 float dsum = 0.f, vsum = 0.f;
-                float *dxg = p.dx + ((size_t)(b * p.L + t0 + r) * H + h) * kP;
+                uint8_t *stg = smem + kOffG + hf * 16384 + 32 * q * 128;   // this warp's dx box
 #pragma unroll 1
                 for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
                     uint32_t in[16], out[16];
@@ -536,11 +553,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                         vsum = fmaf(xv[e], ov, vsum);
                         o[e] = fmaf(Dh, yv[e], dt_r * gx);
                     }
-                    if (r < nq) {
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(dxg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                    }
+                    stage16(stg, lane, g16 & 1, o);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (32 * q < nq)
+                        tma_store_3d(&maps.dx, stg, h * kP + 32 * hf, (int)t0 + 32 * q, (int)b);
+                    bulk_commit_group();
                 }
                 ddir[hf * kR + r] = dsum;
                 vv[hf * kR + r] = dt_r * eo * vsum;
@@ -571,24 +591,31 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             tc_fence_after();
             {
                 const float eo = ex2_approx(cs_last - cs_r);
-                float *dbg = p.dB_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
+                // this warp's two dB boxes (columns 64 hf .. +63): B's tiles for hf 0, A2's for hf 1
+                uint8_t *stg = smem + (hf ? kOffA2 : kOffB) + 32 * q * 128;
 #pragma unroll 1
                 for (int g16 = 4 * hf; g16 < 4 * hf + 4; ++g16) {
                     uint32_t in[16], out[16];
                     tmem_ld16(trow + kColA2C + 16 * g16, in);
                     tmem_ld16(trow + kColXG + 128 * k + 16 * g16, out);
                     tmem_wait_ld();
-                    if (r < nq) {
+                    float o[16];
 #pragma unroll
-                        for (int e = 0; e < 16; e += 4) {
-                            float o[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u)
-                                o[u] = dt_r * fmaf(eo, __uint_as_float(out[e + u]), __uint_as_float(in[e + u]));
-                            *reinterpret_cast<float4 *>(dbg + 16 * g16 + e) = make_float4(o[0], o[1], o[2], o[3]);
-                        }
-                    }
+                    for (int e = 0; e < 16; ++e)
+                        o[e] = dt_r * fmaf(eo, __uint_as_float(out[e]), __uint_as_float(in[e]));
+                    stage16(stg + ((g16 >> 1) & 1) * 16384, lane, g16 & 1, o);
                 }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (32 * q < nq) {
+                        tma_store_3d(&maps.dB, stg, h * kN + 64 * hf, (int)t0 + 32 * q, (int)b);
+                        tma_store_3d(&maps.dB, stg + 16384, h * kN + 64 * hf + 32, (int)t0 + 32 * q, (int)b);
+                    }
+                    bulk_commit_group();
+                    bulk_wait_read_but_last();   // the dx store has read its box (reused for dC)
+                }
+                __syncwarp();
             }
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS3]);
@@ -608,7 +635,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             {
                 const float es = ex2_approx(cs_r);
                 float usum = 0.f;
-                float *dcg = p.dC_head + ((size_t)(b * p.L + t0 + r) * H + h) * kN;
+                // this warp's two dC boxes (columns 64 hf .. +63) in x's, dy's and G_out's tiles
+                uint8_t *stg = smem + kOffX + hf * 32768 + 32 * q * 128;
 #pragma unroll 1
                 for (int g16 = 4 * hf; g16 < 4 * hf + 4; ++g16) {
                     uint32_t in[16], out[16];
@@ -634,13 +662,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                         usum = fmaf(cv[e], inter, usum);
                         o[e] = __uint_as_float(in[e]) + inter;
                     }
-                    if (r < nq) {
-#pragma unroll
-                        for (int e = 0; e < 16; e += 4)
-                            *reinterpret_cast<float4 *>(dcg + 16 * g16 + e) = make_float4(o[e], o[e + 1], o[e + 2], o[e + 3]);
-                    }
+                    stage16(stg + ((g16 >> 1) & 1) * 16384, lane, g16 & 1, o);
                 }
                 uu[hf * kR + r] = usum;
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    if (32 * q < nq) {
+                        tma_store_3d(&maps.dC, stg, h * kN + 64 * hf, (int)t0 + 32 * q, (int)b);
+                        tma_store_3d(&maps.dC, stg + 16384, h * kN + 64 * hf + 32, (int)t0 + 32 * q, (int)b);
+                    }
+                    bulk_commit_group();
+                }
             }
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
@@ -703,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 p.part[2 * BHC + i] = (red[16 + q] + red[16 + q + 1]) + (red[20 + q] + red[20 + q + 1]);
             }
         } while (false);
+        if (lane == 0)
+            bulk_wait_all();   // every store of this warp done before the CTA exits
     }
 
     tc_fence_before();
@@ -921,6 +956,11 @@ cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t st)
         !make_tmap_bf16_3d(&maps.dy, a.dy, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128) ||
         !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, 128))
+        return cudaErrorInvalidValue;
+    const uint64_t HN = (uint64_t)a.nheads * kN;
+    if (!make_tmap_f32_3d(&maps.dx, a.dx, HP, L, (uint64_t)a.batch, HP * 4, HP * 4 * L, 32, 32) ||
+        !make_tmap_f32_3d(&maps.dB, a.dB_head, HN, L, (uint64_t)a.batch, HN * 4, HN * 4 * L, 32, 32) ||
+        !make_tmap_f32_3d(&maps.dC, a.dC_head, HN, L, (uint64_t)a.batch, HN * 4, HN * 4 * L, 32, 32))
         return cudaErrorInvalidValue;
     TcParams p;
     p.dt_raw = a.dt_raw;
