@@ -180,38 +180,53 @@ __device__ __forceinline__ void stage16(uint8_t *box, int r, int g, const float 
             make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
 }
 
-// columns 32 hf .. 32 hf + 31 of a chunk's fp32 state [n][p] (row n of this
-// thread) into a bf16 tile, zero when absent: its hi term bf16(v) (lo false) or
-// its lo term bf16(v - hi) (lo true) (all loads issued before the first store);
-// with dot, also returns the dot product of those columns with the same ones of
-// another state (0 when absent)
-__device__ __forceinline__ float stage_state(uint8_t *tile, const float *src, int n, int hf, bool lo,
-                                             const float *dot = nullptr)
+// Rows 32 q .. 32 q + 31 and columns 32 hf .. 32 hf + 31 of both chunks' fp32
+// states [n][p] (src[k], null when absent) into the bf16 tiles tile + k kT16,
+// zero when absent: their hi terms bf16(v) (lo false) or lo terms bf16(v - hi)
+// (lo true).  The loads are coalesced (load i of lane l: row 32 q + 4 i + l / 8,
+// columns 32 hf + 4 (l % 8) .. +3, so a warp reads four whole 128-byte
+// segments at a time), all issued before the first store.  With kDot, also
+// this lane's share of the dot products of those elements with the same ones
+// of other states (dot[k]; 0 when absent) in d[k].
+template <bool kDot>
+__device__ __forceinline__ void stage_states(uint8_t *tile, const float *const (&src)[2], int q, int hf, int lane,
+                                             bool lo, const float *const (&dot)[2], float (&d)[2])
 {
-    float4 a[8], o[8];
-    const size_t base = (size_t)n * kP + 32 * hf;
+    const int rr = lane >> 3, c4 = lane & 7;
+    float4 a[2][8], o[2][kDot ? 8 : 1];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        a[i] = src ? __ldg(reinterpret_cast<const float4 *>(src + base + 4 * i)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        o[i] = (src && dot) ? __ldg(reinterpret_cast<const float4 *>(dot + base + 4 * i))
-                            : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float d = 0.f;
+    for (int k = 0; k < 2; ++k)
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        d = fmaf(a[i].x, o[i].x, fmaf(a[i].y, o[i].y, fmaf(a[i].z, o[i].z, fmaf(a[i].w, o[i].w, d))));
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        float v[8] = {a[2 * c].x, a[2 * c].y, a[2 * c].z, a[2 * c].w, a[2 * c + 1].x, a[2 * c + 1].y, a[2 * c + 1].z,
-                      a[2 * c + 1].w};
-        if (lo) {
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-                v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
+        for (int i = 0; i < 8; ++i) {
+            const size_t off = (size_t)(32 * q + 4 * i + rr) * kP + 32 * hf + 4 * c4;
+            a[k][i] = src[k] ? __ldg(reinterpret_cast<const float4 *>(src[k] + off)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if constexpr (kDot)
+                o[k][i] = (src[k] && dot[k]) ? __ldg(reinterpret_cast<const float4 *>(dot[k] + off))
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
         }
-        st8(tile, n, 4 * hf + c, v);
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float dk = 0.f;
+        if constexpr (kDot) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                dk = fmaf(a[k][i].x, o[k][i].x, fmaf(a[k][i].y, o[k][i].y, fmaf(a[k][i].z, o[k][i].z, fmaf(a[k][i].w, o[k][i].w, dk))));
+        }
+        d[k] = dk;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float v[4] = {a[k][i].x, a[k][i].y, a[k][i].z, a[k][i].w};
+            if (lo) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    v[e] -= __bfloat162float(__float2bfloat16_rn(v[e]));
+            }
+            // 4 bf16 = half of the 16-byte chunk 4 hf + c4 / 2 of row n
+            const int n = 32 * q + 4 * i + rr;
+            *reinterpret_cast<uint2 *>(tile + k * kT16 + sw128(n, 4 * hf + (c4 >> 1)) + 8 * (c4 & 1)) =
+                make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        }
     }
-    return d;
 }
 
 __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __grid_constant__ TcMaps maps, const TcParams p)
@@ -374,6 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
         uint8_t *tC = smem + kOffC, *tB = smem + kOffB, *tX = smem + kOffX, *tDY = smem + kOffDY;
         uint8_t *tG = smem + kOffG, *tMT = smem + kOffMT, *tA2 = smem + kOffA2;
         uint32_t rphase = 0;
+        // G_out of chunk c0 + kk, the state entering it and the state after it;
+        // null past the sequence's chunks
+        auto gout = [&](int kk) -> const float * {
+            return c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr;
+        };
+        auto hin = [&](int kk) -> const float * {
+            return c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr;
+        };
+        auto hout = [&](int kk) -> const float * {
+            return c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP : nullptr;
+        };
         do {
             // ---- per step: dt, z and the cumulative sum of dt a within the chunk (log2 units)
             if (hf == 0) {
@@ -396,16 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             // both chunks' G_out (row n = r of each, this half's columns), its hi terms,
             // into bf16 tiles, and their share of <G_out, h_last> per chunk (summed per
             // warp here; over the warps at the end)
+            {
+                float s2[2];
+                stage_states<true>(tG, {gout(0), gout(1)}, q, hf, lane, false, {hout(0), hout(1)}, s2);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk) {
-                const bool v = c0 + kk < nc;
-                float s2 = stage_state(tG + kk * kT16, v ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, hf,
-                                       false, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk + 1) * NP : nullptr);
+                for (int kk = 0; kk < 2; ++kk) {
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
-                if (lane == 0)
-                    red[8 * kk + warp] = s2;
+                    for (int o = 16; o > 0; o >>= 1)
+                        s2[kk] += __shfl_xor_sync(0xffffffffu, s2[kk], o);
+                    if (lane == 0)
+                        red[8 * kk + warp] = s2[kk];
+                }
             }
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS0]);
@@ -505,10 +532,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             // ---- rows 2a: G_out's lo terms (row n = r) into its tiles, once MMA 2 has read the hi
             if (!(ok = wait_bar(&bars[BAR_MMA2], 0)))
                 break;
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-                stage_state(tG + kk * kT16, c0 + kk < nc ? p.R + ((size_t)bh * nc + c0 + kk) * NP : nullptr, r, hf,
-                            true);
+            {
+                float unused[2];
+                stage_states<false>(tG, {gout(0), gout(1)}, q, hf, lane, true, {nullptr, nullptr}, unused);
+            }
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS2A]);
             // ---- rows 2: dx_j = D dy_j + dt_j (in + eo out); dt o B in place; h_in's hi terms
@@ -575,11 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                     st8(tB + hf * kT16, r, cc, v);
                 }
                 // h_in of both chunks (row n = r), its hi terms, into Mt's space, for MMA 4
-#pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const bool v = c0 + kk < nc;
-                    stage_state(tMT + kk * kT16, v ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r, hf,
-                                false);
+                {
+                    float unused[2];
+                    stage_states<false>(tMT, {hin(0), hin(1)}, q, hf, lane, false, {nullptr, nullptr}, unused);
                 }
             }
             fence_proxy_async_smem();
@@ -622,10 +647,10 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             // ---- rows 4a: h_in's lo terms into Mt's space, once MMA 4 has read the hi
             if (!(ok = wait_bar(&bars[BAR_MMA4], 0)))
                 break;
-#pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-                stage_state(tMT + kk * kT16, c0 + kk < nc ? p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP : nullptr, r,
-                            hf, true);
+            {
+                float unused[2];
+                stage_states<false>(tMT, {hin(0), hin(1)}, q, hf, lane, true, {nullptr, nullptr}, unused);
+            }
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS4A]);
             // ---- rows 4: dC_s = in + e^{cs_s} out, u_s = C_s . e^{cs_s} out
