@@ -424,7 +424,10 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams 
 //    final state); blockIdx.z = 1: R(c) <- G_out(c), d init <- G_out(-1).  Each
 //    thread runs one chain over kVec consecutive state elements (n, p) of one
 //    (b, h), loading kBatch chunks ahead so that the loads of a batch are all
-//    in flight together (the stores of a batch go to other addresses).
+//    in flight together (the stores of a batch go to other addresses).  Two
+//    blocks per SM (128 registers): one block per SM at 142 registers left the
+//    loads of 8 warps per SM in flight (78 us on 2 x 1024 steps, 80 heads, against
+//    70 us capped); batches of 8 at three blocks per SM measured slower.
 constexpr int kVec = 4, kBatch = 16;
 template <int V>
 __device__ __forceinline__ void chain(float *buf, size_t stride, const float *dec, int nc, bool reverse,
@@ -461,22 +464,45 @@ __device__ __forceinline__ void chain(float *buf, size_t stride, const float *de
     }
 }
 
-template <int V>
-__global__ void __launch_bounds__(kThreads) ssd_bwd_pass_kernel(ChunkBwdParams p)
+// kTr (P = 64, N % 16 == 0, V = 4, 16-byte aligned [B,H,P,N] tensors): a block's
+// 1024 elements are 16 whole rows n, and the [P][N] tensors (the initial state
+// or d final in, d init out) pass through a shared-memory transpose, so their
+// loads and stores are 64-byte segments rather than 4-byte pieces 4 N bytes
+// apart.
+constexpr int kTrLd = 17;   // transpose row stride (floats)
+template <int V, bool kTr>
+__global__ void __launch_bounds__(kThreads, 2) ssd_bwd_pass_kernel(ChunkBwdParams p)
 {
     const int P = p.P, N = p.N, nc = p.nc;
     const long long bh = blockIdx.y;
     const int NP = N * P, e0 = (blockIdx.x * kThreads + threadIdx.x) * V;
-    if (e0 >= NP)
+    __shared__ float tr[kTr ? kPM * kTrLd : 1];
+    if (!kTr && e0 >= NP)
         return;
     const float *dec = p.dec + bh * nc;
     const bool fwd = blockIdx.z == 0;
     const float *in = fwd ? p.init_state : p.d_final;   // [B,H,P,N] or null
+    const int nb = (int)blockIdx.x * (kThreads * V / kPM);   // kTr: the block's first row n
     float v[V];
+    if constexpr (kTr) {
+        const int t = threadIdx.x, pr = t >> 2, n4 = 4 * (t & 3);
+        const float4 f = in ? *reinterpret_cast<const float4 *>(in + (size_t)bh * NP + (size_t)pr * N + nb + n4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+        tr[pr * kTrLd + n4] = f.x;
+        tr[pr * kTrLd + n4 + 1] = f.y;
+        tr[pr * kTrLd + n4 + 2] = f.z;
+        tr[pr * kTrLd + n4 + 3] = f.w;
+        __syncthreads();
+        const int nn = e0 / P - nb, col = e0 % P;
 #pragma unroll
-    for (int e = 0; e < V; ++e) {
-        const int n = (e0 + e) / P, col = (e0 + e) - n * P;
-        v[e] = in ? in[(size_t)bh * NP + (size_t)col * N + n] : 0.f;
+        for (int e = 0; e < V; ++e)
+            v[e] = tr[(col + e) * kTrLd + nn];
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            const int n = (e0 + e) / P, col = (e0 + e) - n * P;
+            v[e] = in ? in[(size_t)bh * NP + (size_t)col * N + n] : 0.f;
+        }
     }
     if (fwd) {
         float *S = p.S + (size_t)bh * (nc + 1) * NP + e0;
@@ -488,10 +514,23 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_pass_kernel(ChunkBwdParams p
     } else {
         chain<V>(p.R + (size_t)bh * nc * NP + e0, (size_t)NP, dec, nc, true, v);
         if (p.d_init) {
+            if constexpr (kTr) {
+                const int nn = e0 / P - nb, col = e0 % P;
+                __syncthreads();   // every thread has read its initial values
 #pragma unroll
-            for (int e = 0; e < V; ++e) {
-                const int n = (e0 + e) / P, col = (e0 + e) - n * P;
-                p.d_init[(size_t)bh * NP + (size_t)col * N + n] = v[e];
+                for (int e = 0; e < V; ++e)
+                    tr[(col + e) * kTrLd + nn] = v[e];
+                __syncthreads();
+                const int t = threadIdx.x, pr = t >> 2, n4 = 4 * (t & 3);
+                *reinterpret_cast<float4 *>(p.d_init + (size_t)bh * NP + (size_t)pr * N + nb + n4) =
+                    make_float4(tr[pr * kTrLd + n4], tr[pr * kTrLd + n4 + 1], tr[pr * kTrLd + n4 + 2],
+                                tr[pr * kTrLd + n4 + 3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) {
+                    const int n = (e0 + e) / P, col = (e0 + e) - n * P;
+                    p.d_init[(size_t)bh * NP + (size_t)col * N + n] = v[e];
+                }
             }
         }
     }
@@ -941,11 +980,16 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     } else {
         ssd_bwd_local_kernel<float><<<grid, kThreads, kLocalSmem, st>>>(p);
     }
-    if (NP % kVec == 0)
-        ssd_bwd_pass_kernel<kVec><<<dim3((unsigned)((NP / kVec + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads,
-                                    0, st>>>(p);
+    const bool tr = a.headdim == kPM && a.dstate % 16 == 0 && aligned16(a.init_state) && aligned16(a.d_final) &&
+                    aligned16(a.d_init);
+    if (tr)
+        ssd_bwd_pass_kernel<kVec, true><<<dim3((unsigned)(NP / kVec / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
+    else if (NP % kVec == 0)
+        ssd_bwd_pass_kernel<kVec, false><<<dim3((unsigned)((NP / kVec + kThreads - 1) / kThreads), (unsigned)BH, 2),
+                                           kThreads, 0, st>>>(p);
     else
-        ssd_bwd_pass_kernel<1><<<dim3((unsigned)((NP + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
+        ssd_bwd_pass_kernel<1, false><<<dim3((unsigned)((NP + kThreads - 1) / kThreads), (unsigned)BH, 2), kThreads, 0,
+                                        st>>>(p);
     if (tc) {
         // the gradient pass on the tensor cores
         BwdTcArgs t;
