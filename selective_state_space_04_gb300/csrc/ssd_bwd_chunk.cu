@@ -426,8 +426,9 @@ __global__ void __launch_bounds__(kThreads) ssd_bwd_local_kernel(ChunkBwdParams 
 //    (b, h), loading kBatch chunks ahead so that the loads of a batch are all
 //    in flight together (the stores of a batch go to other addresses).  Two
 //    blocks per SM (128 registers): one block per SM at 142 registers left the
-//    loads of 8 warps per SM in flight (78 us on 2 x 1024 steps, 80 heads, against
-//    70 us capped); batches of 8 at three blocks per SM measured slower.
+//    loads of only 8 warps per SM in flight (the whole backward on 2 x 1024
+//    steps, 80 heads: 0.370 ms, against 0.344 ms capped); batches of 8 at three
+//    blocks per SM measured 0.375 ms.
 constexpr int kVec = 4, kBatch = 16;
 template <int V>
 __device__ __forceinline__ void chain(float *buf, size_t stride, const float *dec, int nc, bool reverse,
