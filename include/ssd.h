@@ -81,6 +81,13 @@ typedef enum ssd_status {
  * P = 64, N = 128).  The tensor-core pass rounds the masked decay products
  * and the chunk states to bf16 operands; the fp32 form does not. */
 #define SSD_BWD_FP32_FORM 0x200u
+/* In ssd_dims_t.flags of ssd_scan_bwd only: where the tensor-core form applies,
+ * compute the chunk states and link them in two launches (every chunk at once,
+ * then the chains) rather than in one launch that walks each (b, h) through its
+ * chunks with the running state in TMEM.  The library takes the one-launch walk
+ * when 2 B H fills the GPU's SMs or the sequence has at most 8 chunks of 64
+ * steps.  Both give the same chunk states up to the order of fp32 additions. */
+#define SSD_BWD_SPLIT_STATES 0x400u
 
 /* Schedules of the chunked path (see ssd_chunk_schedule).  One may be requested
  * in ssd_dims_t.flags as (SSD_SCHEDULE_x << SSD_SCHEDULE_SHIFT); 0 there lets

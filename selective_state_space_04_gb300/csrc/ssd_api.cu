@@ -1126,12 +1126,12 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
     Sizes sz;
     if (!dims)
         return SSD_ERR_NULL_PTR;
-    ssd_dims_t dchk = *dims;   // (the backward's own flag is checked here, the rest by check_dims)
-    dchk.flags &= ~SSD_BWD_FP32_FORM;
+    ssd_dims_t dchk = *dims;   // (the backward's own flags are checked here, the rest by check_dims)
+    dchk.flags &= ~(SSD_BWD_FP32_FORM | SSD_BWD_SPLIT_STATES);
     ssd_status_t s = check_dims(&dchk, &sz);
     if (s != SSD_OK)
         return s;
-    if ((dims->flags & ~(SSD_PATH_MASK | SSD_BWD_FP32_FORM)) != 0)
+    if ((dims->flags & ~(SSD_PATH_MASK | SSD_BWD_FP32_FORM | SSD_BWD_SPLIT_STATES)) != 0)
         return SSD_ERR_INVALID_DIMS;
     const uint32_t path = dims->flags & SSD_PATH_MASK;
     if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
@@ -1189,6 +1189,7 @@ ssd_status_t ssd_scan_bwd(const void *x, const float *dt_raw, const float *dt_bi
     ba.dtype = dims->dtype;
     ba.path = path;
     ba.fp32_form = (dims->flags & SSD_BWD_FP32_FORM) != 0;
+    ba.split_states = (dims->flags & SSD_BWD_SPLIT_STATES) != 0;
     if (path == SSD_PATH_AUTO)
         ba.path = bwd_chunk_supported(ba) ? SSD_PATH_CHUNKED : SSD_PATH_SEQUENTIAL;
     if (!bwd_supported(ba))

@@ -956,7 +956,40 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     }
     if (e != cudaSuccess)
         return e;
+    // the tensor-core form's chunk states: one launch walking each (b, h) through its
+    // chunks (the state in TMEM) when 2 B H CTAs fill the SMs or the walk is short,
+    // else every chunk at once and then the chains
+    int sms = 0;
     if (tc) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+    }
+    const bool walk = tc && !a.split_states && (2 * (long long)BH >= sms || nc <= 8);
+    if (walk) {
+        BwdTcChainArgs t;
+        t.x = a.x;
+        t.B = a.B;
+        t.C = a.C;
+        t.dy = a.dy;
+        t.dt_raw = a.dt_raw;
+        t.dt_bias = a.dt_bias;
+        t.A_log = a.A_log;
+        t.init_state = a.init_state;
+        t.d_final = a.d_final;
+        t.S = p.S;
+        t.R = p.R;
+        t.d_init = a.d_init;
+        t.batch = a.batch;
+        t.seqlen = a.seqlen;
+        t.nheads = a.nheads;
+        t.ngroups = a.ngroups;
+        t.nc = nc;
+        e = bwd_tc_chain_launch(t, st);
+        if (e != cudaSuccess)
+            return e;
+    } else if (tc) {
         BwdTcLocalArgs t;
         t.x = a.x;
         t.B = a.B;
@@ -983,7 +1016,9 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
     }
     const bool tr = a.headdim == kPM && a.dstate % 16 == 0 && aligned16(a.init_state) && aligned16(a.d_final) &&
                     aligned16(a.d_init);
-    if (tr)
+    if (walk)
+        ;   // the walk has linked the chunks
+    else if (tr)
         ssd_bwd_pass_kernel<kVec, true><<<dim3((unsigned)(NP / kVec / kThreads), (unsigned)BH, 2), kThreads, 0, st>>>(p);
     else if (NP % kVec == 0)
         ssd_bwd_pass_kernel<kVec, false><<<dim3((unsigned)((NP / kVec + kThreads - 1) / kThreads), (unsigned)BH, 2),
@@ -1024,7 +1059,7 @@ cudaError_t bwd_chunk_launch(const BwdArgs &a, void *ws, cudaStream_t st)
         e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
-    note_launches(3);
+    note_launches(walk ? 2 : 3);
     return bwd_finish_launch(a, p.dB_head, p.dC_head, p.part, nc, st);
 }
 

@@ -965,6 +965,247 @@ __global__ void __launch_bounds__(kLThreads) ssd_bwd_tc_local_kernel(const __gri
         tmem_dealloc(tmem, 128);
 }
 
+
+// ---------------------------------------------------------------- chunk chains
+// The chunk states and the chains linking them in one launch: one CTA per
+// (b, h) and direction walks the chunks in order with the running state in
+// TMEM ([n lanes][p columns], fp32).  Forward (blockIdx.y = 0), from the
+// initial state: h_in(c) out to slot c, then h <- e^{cs_last(c)} h + S(c);
+// the final state to slot nc.  Reverse (blockIdx.y = 1), from d final: G_out(c)
+// out to slot c, then G <- e^{cs_last(c)} G + R(c); d init at the end.  S(c) and
+// R(c) are the products of ssd_bwd_tc_local_kernel, accumulated straight into
+// the running state (hi and lo terms of the scaled operand); the decay is
+// applied to the state in TMEM before the chunk's products.
+constexpr uint32_t kCOffA = 0;                    // B or C: two [64 rows][64 bf16] tiles
+constexpr uint32_t kCOffV = 2 * kLT;              // x or dy, scaled in place (hi terms)
+constexpr uint32_t kCOffVL = 3 * kLT;             // the lo terms
+constexpr uint32_t kCOffOut = 4 * kLT;            // the state out: two [128 n][32 p] fp32 boxes
+constexpr uint32_t kCOffArr = kCOffOut + 2 * kLOut;   // raw cumsums, step weights: 64 floats each; the decay
+constexpr uint32_t kCOffBars = kCOffArr + (2 * kLq + 4) * 4;
+constexpr uint32_t kCOffHolder = kCOffBars + 16;
+constexpr uint32_t kCSmemBytes = kCOffHolder + 16 + 1024;
+
+struct TcChainParams {
+    const float *dt_raw, *dt_bias, *A_log;
+    const float *init_state, *d_final;   // [B,H,P,N] or null
+    float *d_init;                       // [B,H,P,N] or null
+    long long L;
+    int H, G, nc;
+};
+
+struct TcChainMaps {
+    CUtensorMap x, dy, B, C;   // bf16, boxes of 64 x 64
+    CUtensorMap S, R;          // fp32 [slot][n][p], boxes of 32 p x 128 n
+};
+
+__global__ void __launch_bounds__(kLThreads) ssd_bwd_tc_chain_kernel(const __grid_constant__ TcChainMaps maps,
+                                                                       const TcChainParams p)
+{
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                ~static_cast<uintptr_t>(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kCOffBars);   // 0: tiles landed, 1: products done
+    uint32_t *holder = reinterpret_cast<uint32_t *>(smem + kCOffHolder);
+    float *cs_s = reinterpret_cast<float *>(smem + kCOffArr), *w_s = cs_s + kLq, *dec_s = w_s + kLq;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = p.H, nc = p.nc;
+    const bool fwd = blockIdx.y == 0;
+    const long long bh = blockIdx.x, b = bh / H;
+    const int h = (int)(bh - b * H), g = h / (H / p.G);
+    const float a = -expf(p.A_log[h]), bias = p.dt_bias[h];
+    const size_t NP = (size_t)kN * kP;
+    const CUtensorMap *mA = fwd ? &maps.B : &maps.C, *mV = fwd ? &maps.x : &maps.dy, *mO = fwd ? &maps.S : &maps.R;
+
+    if (tid == 0) {
+        mbar_init(&bars[0], 1);
+        mbar_init(&bars[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(holder, 64);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *holder;
+    const uint32_t trow = tmem + (static_cast<uint32_t>(32 * warp) << 16);   // this thread's state row n = tid
+    auto chunk_of = [&](int it) { return fwd ? it : nc - 1 - it; };
+    auto load_tiles = [&](int c) {   // thread 0: chunk c's operand tiles
+        const uint64_t once = policy_evict_first(), shared = policy_evict_last();
+        const int t0 = c * kLq;
+        mbar_arrive_expect_tx(&bars[0], 3 * kLT);
+        tma_load_3d(smem + kCOffA, mA, &bars[0], g * kN, t0, (int)b, shared);
+        tma_load_3d(smem + kCOffA + kLT, mA, &bars[0], g * kN + 64, t0, (int)b, shared);
+        tma_load_3d(smem + kCOffV, mV, &bars[0], h * kP, t0, (int)b, once);
+    };
+    auto load_dt = [&](int c) {   // row tid < 64 of chunk c: dt_raw + bias (0 past the sequence)
+        const long long t = (long long)c * kLq + tid;
+        return (tid < kLq && t < p.L) ? p.dt_raw[(size_t)(b * p.L + t) * H + h] + bias : 0.f;
+    };
+    if (tid == 0 && nc > 0)
+        load_tiles(chunk_of(0));
+    // the entering state: the initial state (forward) or d final (reverse), [P][N]
+    {
+        const float *in = fwd ? p.init_state : p.d_final;
+        uint32_t v[2][32];
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            v[i >> 5][i & 31] = __float_as_uint(in ? __ldg(in + (size_t)bh * NP + (size_t)i * kN + tid) : 0.f);
+        tmem_st32(trow, v[0]);
+        tmem_st32(trow + 32, v[1]);
+        tmem_wait_st();
+    }
+    float zn = nc > 0 ? load_dt(chunk_of(0)) : 0.f;
+    bool ok = true;
+    uint32_t par = 0;
+    for (int it = 0; it < nc && ok; ++it, par ^= 1u) {
+        const int c = chunk_of(it);
+        const long long t0 = (long long)c * kLq;
+        // dt, the chunk's cumsum of dt a (two warps) and the step weights
+        float dt = 0.f;
+        if (tid < kLq) {
+            dt = t0 + tid < p.L ? softplus_f32(zn) : 0.f;
+            float v = dt * a;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o)
+                    v += u;
+            }
+            cs_s[tid] = v;
+        }
+        __syncthreads();
+        if (tid < kLq) {
+            const float c31 = cs_s[31];
+            const float cs = cs_s[tid] + (tid >= 32 ? c31 : 0.f), cl = cs_s[kLq - 1] + c31;
+            w_s[tid] = fwd ? expf(cl - cs) * dt : expf(cs);
+            if (tid == 0)
+                dec_s[0] = expf(cl);
+            if (it + 1 < nc)
+                zn = load_dt(chunk_of(it + 1));   // in flight through the rest of the chunk
+        }
+        if (tid == 0)
+            bulk_wait_read_all();   // the previous state store has read its boxes
+        __syncthreads();
+        ok = wait_bar(&bars[0], par);
+        if (ok) {
+            // the scaled operand: row j = tid % 64, columns 32 (tid / 64) .. +31; hi in place, lo beside
+            const int j = tid & (kLq - 1), hf = tid >> 6;
+            const float sc = w_s[j];
+            uint8_t *hi = smem + kCOffV, *lo = smem + kCOffVL;
+#pragma unroll
+            for (int cc = 4 * hf; cc < 4 * hf + 4; ++cc) {
+                float v[8], l[8];
+                ld8(hi, j, cc, v);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    v[e] *= sc;
+                    l[e] = v[e] - __bfloat162float(__float2bfloat16_rn(v[e]));
+                }
+                st8(hi, j, cc, v);
+                st8(lo, j, cc, l);
+            }
+            // the state entering the chunk out (row n = tid), then scaled by the chunk's decay
+            uint32_t v[2][32];
+            tmem_ld32(trow, v[0]);
+            tmem_ld32(trow + 32, v[1]);
+            tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint8_t *box = smem + kCOffOut + q * kLOut + tid * 128;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(box + ((cc ^ (tid & 7)) << 4)) =
+                        make_uint4(v[q][4 * cc], v[q][4 * cc + 1], v[q][4 * cc + 2], v[q][4 * cc + 3]);
+            }
+            const float d = dec_s[0];
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    v[q][e] = __float_as_uint(d * __uint_as_float(v[q][e]));
+            tmem_st32(trow, v[0]);
+            tmem_st32(trow + 32, v[1]);
+            tmem_wait_st();
+            fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        ok = __syncthreads_and(ok);
+        if (!ok)
+            break;
+        if (tid == 0) {
+            tc_fence_after();
+            const int slot = fwd ? (int)(bh * (nc + 1) + c) : (int)(bh * nc + c);
+            tma_store_3d(mO, smem + kCOffOut, 0, 0, slot);
+            tma_store_3d(mO, smem + kCOffOut + kLOut, 32, 0, slot);
+            bulk_commit_group();
+            const uint32_t i64nn = idesc_bf16_f32(128, 64, 1, 1);
+            auto mn = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kLT, 1024); };
+            const uint32_t sA = smem_u32(smem + kCOffA), sV = smem_u32(smem + kCOffV), sVL = smem_u32(smem + kCOffVL);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tmem, mn(sA, kk), mn(sV, kk), i64nn, 1);
+            for (int kk = 0; kk < 4; ++kk)
+                mma_ss(tmem, mn(sA, kk), mn(sVL, kk), i64nn, 1);
+            mma_commit(&bars[1]);
+        }
+        // the next state read and the next chunk's tiles both wait for the products
+        ok = wait_bar(&bars[1], par);
+        tc_fence_after();
+        if (ok && tid == 0 && it + 1 < nc)
+            load_tiles(chunk_of(it + 1));
+        ok = __syncthreads_and(ok);
+    }
+    if (ok) {
+        // the final state (forward, slot nc) or d init (reverse, [P][N])
+        uint32_t v[2][32];
+        tmem_ld32(trow, v[0]);
+        tmem_ld32(trow + 32, v[1]);
+        tmem_wait_ld();
+        if (fwd) {
+            if (tid == 0)
+                bulk_wait_read_all();
+            __syncthreads();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint8_t *box = smem + kCOffOut + q * kLOut + tid * 128;
+#pragma unroll
+                for (int cc = 0; cc < 8; ++cc)
+                    *reinterpret_cast<uint4 *>(box + ((cc ^ (tid & 7)) << 4)) =
+                        make_uint4(v[q][4 * cc], v[q][4 * cc + 1], v[q][4 * cc + 2], v[q][4 * cc + 3]);
+            }
+            fence_proxy_async_smem();
+            __syncthreads();
+            if (tid == 0) {
+                const int slot = (int)(bh * (nc + 1) + nc);
+                tma_store_3d(mO, smem + kCOffOut, 0, 0, slot);
+                tma_store_3d(mO, smem + kCOffOut + kLOut, 32, 0, slot);
+                bulk_commit_group();
+            }
+        } else if (p.d_init) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                p.d_init[(size_t)bh * NP + (size_t)i * kN + tid] = __uint_as_float(v[i >> 5][i & 31]);
+        }
+    }
+    if (tid == 0) {
+        bulk_wait_all();
+        if (!ok) {
+            // after a timeout: no TMA load or product may still be in flight at exit
+            const uint64_t tw = globaltimer_ns();
+            while (!mbar_wait_for(&bars[0], par, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+            }
+            while (!mbar_wait_for(&bars[1], par, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+        tmem_dealloc(tmem, 64);
+}
+
 }  // namespace
 
 bool bwd_tc_supported(int dtype, int headdim, int dstate)
@@ -1039,6 +1280,38 @@ cudaError_t bwd_tc_local_launch(const BwdTcLocalArgs &a, cudaStream_t st)
     if (e != cudaSuccess)
         return e;
     ssd_bwd_tc_local_kernel<<<dim3((unsigned)a.nc, (unsigned)BH), kLThreads, kLSmemBytes, st>>>(maps, p);
+    return cudaGetLastError();
+}
+
+cudaError_t bwd_tc_chain_launch(const BwdTcChainArgs &a, cudaStream_t st)
+{
+    SSD_NVTX_RANGE("bwd_tc_chain_launch");
+    TcChainMaps maps;
+    const uint64_t HP = (uint64_t)a.nheads * kP, GN = (uint64_t)a.ngroups * kN, L = (uint64_t)a.seqlen;
+    const uint64_t BH = (uint64_t)a.batch * a.nheads, NP4 = (uint64_t)kN * kP * 4;
+    if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.dy, a.dy, HP, L, (uint64_t)a.batch, HP * 2, HP * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.B, a.B, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, kLq) ||
+        !make_tmap_bf16_3d(&maps.C, a.C, GN, L, (uint64_t)a.batch, GN * 2, GN * 2 * L, 64, kLq) ||
+        !make_tmap_f32_3d(&maps.S, a.S, kP, kN, BH * (a.nc + 1), kP * 4, NP4, 32, kN) ||
+        !make_tmap_f32_3d(&maps.R, a.R, kP, kN, BH * a.nc, kP * 4, NP4, 32, kN))
+        return cudaErrorInvalidValue;
+    TcChainParams p;
+    p.dt_raw = a.dt_raw;
+    p.dt_bias = a.dt_bias;
+    p.A_log = a.A_log;
+    p.init_state = a.init_state;
+    p.d_final = a.d_final;
+    p.d_init = a.d_init;
+    p.L = a.seqlen;
+    p.H = a.nheads;
+    p.G = a.ngroups;
+    p.nc = a.nc;
+    const cudaError_t e = cudaFuncSetAttribute(ssd_bwd_tc_chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kCSmemBytes);
+    if (e != cudaSuccess)
+        return e;
+    ssd_bwd_tc_chain_kernel<<<dim3((unsigned)BH, 2), kLThreads, kCSmemBytes, st>>>(maps, p);
     return cudaGetLastError();
 }
 

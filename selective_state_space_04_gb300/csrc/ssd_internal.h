@@ -126,6 +126,8 @@ struct BwdArgs {
     uint32_t path;                              // SSD_PATH_SEQUENTIAL or SSD_PATH_CHUNKED (resolved)
     bool fp32_form = false;                     // the chunk form's fp32 contractions even where the
                                                 // tensor-core gradient pass applies (SSD_BWD_FP32_FORM)
+    bool split_states = false;                  // the tensor-core form's chunk states and chains as two
+                                                // launches (SSD_BWD_SPLIT_STATES)
 };
 // ssd_bwd.cu: dispatch, the sequential kernel and the fixed-order reductions
 bool bwd_seq_supported(const BwdArgs &a);
@@ -154,6 +156,15 @@ struct BwdTcLocalArgs {
 };
 bool bwd_tc_supported(int dtype, int headdim, int dstate);
 cudaError_t bwd_tc_local_launch(const BwdTcLocalArgs &a, cudaStream_t stream);
+struct BwdTcChainArgs {
+    const void *x, *B, *C, *dy;                 // bf16
+    const float *dt_raw, *dt_bias, *A_log;
+    const float *init_state, *d_final;          // [B,H,P,N] or null
+    float *S, *R, *d_init;                      // [B*H][nc+1][N][P] (all slots), [B*H][nc][N][P], [B,H,P,N] or null
+    int64_t batch, seqlen;
+    int nheads, ngroups, nc;
+};
+cudaError_t bwd_tc_chain_launch(const BwdTcChainArgs &a, cudaStream_t stream);
 cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t stream);
 ssd_status_t bwd_tc_read_device_error(uint32_t *code);
 // ssd_bwd_chunk.cu: the chunk-parallel backward (P <= 64, N <= 128)

@@ -15,6 +15,7 @@ from .build import LIB_PATH
 PATH_AUTO = 0
 DIAG_STALL_HANDOFF = 0x100
 BWD_FP32_FORM = 0x200   # ssd_scan_bwd: the chunk form's fp32 contractions even where the tensor-core pass applies
+BWD_SPLIT_STATES = 0x400   # ssd_scan_bwd: the tensor-core form's chunk states and chains as two launches
 PATH_SEQUENTIAL = 1
 PATH_CHUNKED = 2
 PATH_DECODE = 3
@@ -420,11 +421,12 @@ def gated_rmsnorm_fwd(y, z, weight, eps=1e-6, *, out=None, stream=None):
 
 
 def ssd_scan_bwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final=None, *, path="auto",
-                 stream=None, fp32_form=False):
+                 stream=None, fp32_form=False, split_states=False):
     """Gradients of ``ssd_scan_fwd`` given ``dy`` (and ``d_final``).  Returns a
     dict of fp32 CUDA tensors: dx, ddt_raw, ddt_bias, dA_log, dB, dC, dD, d_init.
     ``fp32_form`` keeps the chunk form's fp32 contractions where its tensor-core
-    gradient pass would apply (bf16, P = 64, N = 128)."""
+    form would apply (bf16, P = 64, N = 128); ``split_states`` computes that
+    form's chunk states and chains in two launches instead of one walk."""
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
     f32 = dict(dtype=torch.float32, device=x.device)
@@ -438,6 +440,8 @@ def ssd_scan_bwd(x, dt_raw, dt_bias, A_log, B, C, D, init_state, dy, d_final=Non
     d = make_dims(Bt, L, H, P, N, G, 1, x.dtype, path)
     if fp32_form:
         d.flags |= BWD_FP32_FORM
+    if split_states:
+        d.flags |= BWD_SPLIT_STATES
     st = torch.cuda.current_stream(x.device) if stream is None else stream
     _check(_lib.ssd_scan_bwd(*(_ptr(t) for _, t in named), ctypes.byref(d), ctypes.c_void_p(st.cuda_stream)),
            "ssd_scan_bwd")

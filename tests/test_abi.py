@@ -336,9 +336,9 @@ def test_conv_scan_entry_validation_before_cuda(libssd):
     assert _conv_scan_call(libssd, libssd.make_dims(0, 64, 4, 64, 128, 1, 64, "bf16")) == 0   # empty: no device access
 
 
-def test_backward_takes_the_fp32_form_flag_only(libssd):
-    # ssd_scan_bwd accepts SSD_BWD_FP32_FORM (0x200) beside a path and nothing else;
-    # an empty batch returns before any device access
+def test_backward_takes_its_own_flags_only(libssd):
+    # ssd_scan_bwd accepts SSD_BWD_FP32_FORM (0x200) and SSD_BWD_SPLIT_STATES (0x400)
+    # beside a path and nothing else; an empty batch returns before any device access
     lib = libssd.lib()
     names = ["x", "dt_raw", "dt_bias", "A_log", "B", "C", "D", "init_state", "dy", "d_final",
              "dx", "ddt_raw", "ddt_bias", "dA_log", "dB", "dC", "dD", "d_init"]
@@ -346,7 +346,9 @@ def test_backward_takes_the_fp32_form_flag_only(libssd):
     d = libssd.make_dims(0, 64, 2, 64, 128, 1, 16, "bf16")
     d.flags = libssd.BWD_FP32_FORM
     assert lib.ssd_scan_bwd(*ptrs, ctypes.byref(d), None) == 0
-    d.flags = 0x400
+    d.flags = libssd.BWD_SPLIT_STATES | libssd.BWD_FP32_FORM
+    assert lib.ssd_scan_bwd(*ptrs, ctypes.byref(d), None) == 0
+    d.flags = 0x800
     assert lib.ssd_scan_bwd(*ptrs, ctypes.byref(d), None) == 1                 # SSD_ERR_INVALID_DIMS
     # the forward entry points do not take it
     d.flags = libssd.BWD_FP32_FORM

@@ -47,10 +47,11 @@ def _grads_in(w, seed):
     return inp, dy, dfin
 
 
-def _run(ssd, inp, dy, dfin, path="auto", fp32_form=False):
+def _run(ssd, inp, dy, dfin, path="auto", fp32_form=False, split_states=False):
     d = {k: (None if v is None else v.cuda().contiguous()) for k, v in inp.items()}
     out = ssd.ssd_scan_bwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_log"], d["B"], d["C"], d["D"], d["init_state"],
-                           dy.cuda(), None if dfin is None else dfin.cuda(), path=path, fp32_form=fp32_form)
+                           dy.cuda(), None if dfin is None else dfin.cuda(), path=path, fp32_form=fp32_form,
+                           split_states=split_states)
     torch.cuda.synchronize()
     return out
 
@@ -92,13 +93,15 @@ def test_backward_against_oracle(ssd, path, B, L, H, P, N, G, dtype, init, dfina
     (3, 64, 2, 2, True, True),       # one chunk
 ])
 def test_backward_tensor_core_pass_against_oracle(ssd, B, L, H, G, init, dfinal):
-    # the tensor-core gradient pass (bf16, P = 64, N = 128) at the bf16 bar, and the
-    # fp32 form of the same call at the fp32 bar
+    # the tensor-core form (bf16, P = 64, N = 128) at the bf16 bar -- its chunk states
+    # as the library picks them (one walk per (b, h) up to 8 chunks here) and as two
+    # launches -- and the fp32 form of the same call at the fp32 bar
     w = Workload("t", B, L, H, 64, 128, G, 16, "bf16", init)
     inp, dy, dfin = _grads_in(w, seed=260 + L + H)
     dfin = dfin if dfinal else None
     ref = ssd_bwd(**inp, dy=dy, d_final=dfin)
     _check(_run(ssd, inp, dy, dfin, "chunked"), ref, tol=TOL_TC)
+    _check(_run(ssd, inp, dy, dfin, "chunked", split_states=True), ref, tol=TOL_TC)
     _check(_run(ssd, inp, dy, dfin, "chunked", fp32_form=True), ref, tol=TOL)
 
 
@@ -165,3 +168,22 @@ def test_backward_full_size_sampled_heads(ssd):
                   dA_log=out["dA_log"][heads], dD=out["dD"][heads], d_init=out["d_init"][:, heads])
     _check(sliced, ref, names=tuple(sliced), tol=TOL_TC)
     _check(_run(ssd, sub, dy_s, dfin_s), ref, names=("dB", "dC"), tol=TOL_TC)
+
+
+def test_backward_state_walk_matches_the_two_launch_states(ssd):
+    # 2 x 1000 steps (16 chunks, ragged tail), 80 heads: the library walks each (b, h)
+    # through its chunks in one launch; forced into two launches, the chunk states
+    # differ only in the order of fp32 additions, so every gradient agrees far below
+    # the bf16 bar.  Both forms are bitwise repeatable.
+    w = Workload("t", 2, 1000, 80, 64, 128, 1, 16, "bf16", True)
+    inp, dy, dfin = _grads_in(w, seed=271)
+    walk = _run(ssd, inp, dy, dfin)
+    split = _run(ssd, inp, dy, dfin, split_states=True)
+    for k in NAMES:
+        a, b = walk[k].double(), split[k].double()
+        err = float((a - b).abs().max() / b.abs().max().clamp_min(1e-30))
+        print(f"{k}: walk vs two launches {err:.2e}")
+        assert err <= 1e-4, k
+    again = _run(ssd, inp, dy, dfin)
+    for k in NAMES:
+        assert torch.equal(walk[k], again[k]), k
