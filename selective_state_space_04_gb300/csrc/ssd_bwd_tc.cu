@@ -1085,8 +1085,15 @@ __global__ void __launch_bounds__(kLThreads) ssd_bwd_tc_chain_kernel(const __gri
             if (it + 1 < nc)
                 zn = load_dt(chunk_of(it + 1));   // in flight through the rest of the chunk
         }
-        if (tid == 0)
+        if (tid == 0) {
             bulk_wait_read_all();   // the previous state store has read its boxes
+            if (it + 1 < nc) {      // the next chunk's tiles into L2: its loads start after this chunk's products
+                const int cn = chunk_of(it + 1) * kLq;
+                tma_prefetch_3d(mA, g * kN, cn, (int)b);
+                tma_prefetch_3d(mA, g * kN + 64, cn, (int)b);
+                tma_prefetch_3d(mV, h * kP, cn, (int)b);
+            }
+        }
         __syncthreads();
         ok = wait_bar(&bars[0], par);
         if (ok) {
