@@ -1,9 +1,9 @@
 // ssd_trap.cu -- the trapezoidal (Mamba-3 SISO) scan, sequential in time.
 //
 // Per batch row b and head h, with v = x, k = B, q = C of the head's group
-// (the Mamba-3 SISO GPU forward of the pages: "trapezoidal recurrence
-// (alpha/beta/gamma) instead of exponential", step F5b for the coefficients,
-// and the persistent k_state / v_state):
+// (the Mamba-3 SISO GPU forward page: its step F5b replaces the exponential
+// update by a trapezoidal one with three coefficients, and the layer keeps
+// the previous step's k and v as persistent state):
 //   alpha_t = exp(a_t dt_t),  beta_t = alpha_t dt_t (1 - trap_t),  gamma_t = trap_t dt_t
 //   h_t = alpha_t h_{t-1} + beta_t k_{t-1} v_{t-1}^T + gamma_t k_t v_t^T
 //   y_t = q_t^T h_t + D v_t
