@@ -401,11 +401,16 @@ ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const floa
  * [B,H,P,N] fp32 (NULL: zero).  Outputs, all fp32, caller-owned, overlapping
  * no input and each other: dx [B,L,H,P], ddt_raw [B,L,H], ddt_bias [H],
  * dA_log [H], dB and dC [B,L,G,N], dD [H], d_init [B,H,P,N] (NULL: not
- * written).  DEVICE pointers, 16-byte aligned.  flags: a path only.
+ * written).  DEVICE pointers, 16-byte aligned.  flags: a path, plus
+ * SSD_BWD_FP32_FORM and SSD_BWD_SPLIT_STATES (above).
  * SSD_PATH_CHUNKED: the chunk form (chunks of 64 steps in parallel: local
  * chunk states and state gradients, a pass over the chunks that links them,
- * then every gradient of a chunk as dense fp32 contractions); supported for
- * P <= 64, N <= 128, B*H <= 65535.  SSD_PATH_SEQUENTIAL: one sequential
+ * then every gradient of a chunk as dense contractions); supported for
+ * P <= 64, N <= 128, B*H <= 65535.  For bf16 with P = 64 and N = 128 its
+ * contractions run on the tensor cores (bf16 operands, fp32 accumulation;
+ * the chunk states enter as two bf16 terms), and the chunk states and their
+ * links may be computed in one walk per (b, h) (SSD_BWD_SPLIT_STATES);
+ * otherwise, or with SSD_BWD_FP32_FORM, as fp32 FFMA.  SSD_PATH_SEQUENTIAL: one sequential
  * kernel per (b, h) that recomputes the forward states segment by segment;
  * supported for N % 4 == 0, N <= 128, P <= 128.  SSD_PATH_AUTO takes the
  * chunk form where it applies, else the sequential kernel.  Scratch (chunk
