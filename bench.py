@@ -89,6 +89,7 @@ KERNEL_SOURCES = {
     "ssd_scan_bwd": ("ssd_bwd.cu", "ssd_bwd_chunk.cu", "ssd_bwd_tc.cu", "warp_rows.cuh", "f32x2.cuh", "ptx.cuh", "tmap.h"),
     "ssd_complex_seq_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
     "ssd_complex_decode_kernel": ("ssd_complex.cu", "warp_rows.cuh", "f32x2.cuh"),
+    "ssd_complex_tc_kernel": ("ssd_complex_tc.cu", "ptx.cuh", "tmap.h"),
 }
 
 # fp32 FFMA peak of one GB300: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz
@@ -804,7 +805,14 @@ def run_reference_trap(args, w: Workload):
 CONV_TAPS = 4
 
 
-def neighbor_setup(w: Workload, dev, seed: int):
+def complex_takes_tc(w: Workload, path: str = "auto") -> bool:
+    """Whether the complex scan runs its chunk form on the tensor cores (the
+    library's rule: bf16, P = 64, N = 128, at least two steps, unless the
+    sequential kernel is asked for)."""
+    return path != "sequential" and w.dtype == "bf16" and w.headdim == 64 and w.dstate == 128 and w.seqlen >= 2
+
+
+def neighbor_setup(w: Workload, dev, seed: int, path: str = "auto"):
     """(host inputs, device inputs, device outputs, step function, algorithmic
     bytes, kernel name, oracle function of the first nb batch rows) of the
     conv1d + SiLU, gated RMSNorm, backward or complex-scan workload ``w``."""
@@ -881,9 +889,12 @@ def neighbor_setup(w: Workload, dev, seed: int):
                 "final_state": torch.empty((w.batch, w.nheads, w.headdim, w.dstate), dtype=torch.float32,
                                            device=dev)}
 
+        cpath = path if path in ("chunked", "sequential") else "auto"
+
         def step(stream):
             ssd.complex_scan_fwd(d["x"], d["dt_raw"], d["dt_bias"], d["A_polar"], d["B"], d["C"], d["D"],
-                                 d["init_state"], y=outs["y"], final_state=outs["final_state"], stream=stream)
+                                 d["init_state"], path=cpath, y=outs["y"], final_state=outs["final_state"],
+                                 stream=stream)
         state = w.batch * w.nheads * w.headdim * w.dstate * 4
         nbytes = (2 * BL * HP * es + BL * w.nheads * 4 + 2 * BL * GN * es + 4 * w.nheads * 4
                   + (state if w.init_state else 0) + state)
@@ -891,7 +902,8 @@ def neighbor_setup(w: Workload, dev, seed: int):
         def ref(nb):
             ocx.complex_fwd(inp["x"][:nb], inp["dt_raw"][:nb], inp["dt_bias"], inp["A_polar"], inp["B"][:nb],
                             inp["C"][:nb], inp["D"], None if inp["init_state"] is None else inp["init_state"][:nb])
-        kernel = "ssd_complex_decode_kernel" if w.seqlen == 1 else "ssd_complex_seq_kernel"
+        kernel = ("ssd_complex_decode_kernel" if w.seqlen == 1 else
+                  "ssd_complex_tc_kernel" if complex_takes_tc(w, cpath) else "ssd_complex_seq_kernel")
         return inp, d, outs, step, nbytes, kernel, ref
     if w.op == "bwd":
         inp = make_inputs(w, seed=seed)
@@ -966,7 +978,7 @@ def run_gpu_neighbor(args, w: Workload):
     from selective_state_space_04_gb300 import build
     build.build()
     from selective_state_space_04_gb300 import ssd
-    inp, d, outs, step, alg_bytes, kernel, ref = neighbor_setup(w, dev, args.seed + rank)
+    inp, d, outs, step, alg_bytes, kernel, ref = neighbor_setup(w, dev, args.seed + rank, args.path)
     stream = torch.cuda.current_stream(dev)
     for _ in range(args.warmup):
         step(stream)
@@ -1032,7 +1044,7 @@ def run_gpu_neighbor(args, w: Workload):
                     "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,
                     "algorithmic_bytes_per_launch": alg_bytes, "hbm_frac": achieved / hbm_peak,
                     "avg_launch_ms": avg_launch_s * 1e3, "roofline_ms": flops / (FP32_PEAK_TFLOPS * 1e12) * 1e3}
-    if w.op == "complex" and w.seqlen > 1:
+    if w.op == "complex" and w.seqlen > 1 and not complex_takes_tc(w, args.path):
         # the state stays in registers over the sequence: fp32 arithmetic bounds it
         flops = complex_flops(w)
         tf = flops / avg_launch_s / 1e12

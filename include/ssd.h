@@ -373,8 +373,12 @@ ssd_status_t ssd_gated_rmsnorm_fwd(const void *y, const void *z, const float *we
  * dt_raw [B,L,H], dt_bias, D [H] fp32; init_state (NULL: zero) and
  * final_state (NULL: not written) [B,H,P,N] fp32, complex as (re, im) pairs
  * along N; final_state may be init_state (in place).  DEVICE pointers, 16-byte
- * aligned; y overlaps no input.  flags: SSD_PATH_AUTO or SSD_PATH_SEQUENTIAL
- * (one sequential kernel; seqlen 1 is a decode step).  Supported: N % 4 == 0,
+ * aligned; y overlaps no input.  flags: SSD_PATH_SEQUENTIAL (one sequential
+ * kernel; seqlen 1 is a decode step), SSD_PATH_CHUNKED (the chunk form on the
+ * tensor cores: chunks of 64 steps, two batch rows per CTA, bf16 operands and
+ * fp32 accumulation; bf16 with P = 64, N = 128 and seqlen >= 2 only, else
+ * SSD_ERR_UNSUPPORTED) or SSD_PATH_AUTO (the chunk form where it applies, else
+ * the sequential kernel).  The sequential kernel supports N % 4 == 0,
  * N <= 512; P <= 128 for N <= 128, P <= 64 for N <= 256, P <= 32 for
  * N <= 512; fp32 or bf16.  seqlen 0 copies the state through.  Errors as
  * ssd_scan_fwd.

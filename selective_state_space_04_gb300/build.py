@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(BUILD_DIR, "libssd.so")
-SOURCES = ["ssd_api.cu", "ssd_seq.cu", "ssd_chunk.cu", "ssd_decode.cu", "ssd_trap.cu", "ssd_neighbors.cu", "ssd_bwd.cu", "ssd_bwd_chunk.cu", "ssd_bwd_tc.cu", "ssd_complex.cu"]
+SOURCES = ["ssd_api.cu", "ssd_seq.cu", "ssd_chunk.cu", "ssd_decode.cu", "ssd_trap.cu", "ssd_neighbors.cu", "ssd_bwd.cu", "ssd_bwd_chunk.cu", "ssd_bwd_tc.cu", "ssd_complex.cu", "ssd_complex_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -686,12 +686,14 @@ ssd_status_t ssd_get_device_error(void *stream, uint32_t *code)
     const ssd_status_t s = chunk_read_device_error(static_cast<cudaStream_t>(stream), code);
     if (s != SSD_OK)
         return s;
-    uint32_t bwd = 0;   // the tensor-core gradient pass of the backward keeps its own word
-    const ssd_status_t s2 = bwd_tc_read_device_error(&bwd);
+    uint32_t bwd = 0, cplx = 0;   // the backward's and the complex chunk form's kernels keep their own words
+    ssd_status_t s2 = bwd_tc_read_device_error(&bwd);
+    if (s2 == SSD_OK)
+        s2 = complex_tc_read_device_error(&cplx);
     if (s2 != SSD_OK)
         return s2;
     if (*code == 0)
-        *code = bwd;
+        *code = bwd ? bwd : cplx;
     return SSD_OK;
 }
 
@@ -726,7 +728,7 @@ ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const floa
     if ((dims->flags & ~SSD_PATH_MASK) != 0)
         return SSD_ERR_INVALID_DIMS;
     const uint32_t path = dims->flags & SSD_PATH_MASK;
-    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL)
+    if (path != SSD_PATH_AUTO && path != SSD_PATH_SEQUENTIAL && path != SSD_PATH_CHUNKED)
         return SSD_ERR_UNSUPPORTED;
     const bool work = dims->batch > 0 && dims->seqlen > 0;
     if (work && (!x || !dt_raw || !dt_bias || !A_polar || !B || !C || !D || !y))
@@ -764,7 +766,11 @@ ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const floa
     ca.dstate = dims->dstate;
     ca.ngroups = dims->ngroups;
     ca.dtype = dims->dtype;
-    if (!complex_supported(ca))
+    // the chunk form on the tensor cores where it applies (auto) or is asked for
+    const bool tc = path != SSD_PATH_SEQUENTIAL && complex_tc_supported(ca);
+    if (path == SSD_PATH_CHUNKED && !tc)
+        return SSD_ERR_UNSUPPORTED;
+    if (!tc && !complex_supported(ca))
         return SSD_ERR_UNSUPPORTED;
     if (dims->batch == 0)
         return SSD_OK;
@@ -777,7 +783,7 @@ ssd_status_t ssd_complex_scan_fwd(const void *x, const float *dt_raw, const floa
                                          : cudaMemsetAsync(final_state, 0, (size_t)sz.state, st);
         return e == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
     }
-    return complex_launch(ca, st) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
+    return (tc ? complex_tc_launch(ca, st) : complex_launch(ca, st)) == cudaSuccess ? SSD_OK : SSD_ERR_CUDA;
 }
 
 ssd_status_t ssd_trap_scan_fwd(const void *v, const void *k, const void *q, const float *dt, const float *a,

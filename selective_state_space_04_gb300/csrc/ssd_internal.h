@@ -185,6 +185,10 @@ struct ComplexArgs {
 };
 bool complex_supported(const ComplexArgs &a);
 cudaError_t complex_launch(const ComplexArgs &a, cudaStream_t stream);
+// ssd_complex_tc.cu: the chunk form on the tensor cores (bf16, P = 64, N = 128, seqlen >= 2)
+bool complex_tc_supported(const ComplexArgs &a);
+cudaError_t complex_tc_launch(const ComplexArgs &a, cudaStream_t stream);
+ssd_status_t complex_tc_read_device_error(uint32_t *code);
 
 // ---- sequential (direct recurrence) path: ssd_seq.cu
 bool seq_supported(int headdim, int dstate);

@@ -1,6 +1,8 @@
 """GPU parity of the complex-valued (ET) scan (ssd_complex_scan_fwd) against
 its fp64 oracle, which the CPU tests pin to an ODE solution of the continuous
-system, the unrolled product form and the real SSD oracle.
+system, the unrolled product form and the real SSD oracle.  Both paths: the
+sequential kernel and, for bf16 with P = 64 and N = 128, the chunk form on the
+tensor cores (two batch rows per CTA, chunks of 64 steps).
 
 Metric: max|out - ref| / max|ref| over the whole tensor, y and the final state
 separately; 1e-4 for fp32 inputs, 2e-2 for bf16 (the forward's bounds).
@@ -42,7 +44,7 @@ def run(ssd, inp, init=None, **kw):
 
 @pytest.mark.parametrize("B,L,H,P,N,G,dtype,init", [
     (2, 100, 4, 64, 128, 1, "f32", True),     # two time blocks, the second ragged
-    (2, 70, 4, 64, 128, 2, "bf16", True),
+    (2, 70, 4, 64, 128, 2, "bf16", True),     # chunk form: two chunks, the second of 6 steps
     (1, 130, 3, 17, 44, 1, "f32", False),     # ragged P, N (11 complex components)
     (1, 1, 2, 8, 16, 1, "f32", True),         # one step: a decode step
     (3, 64, 8, 32, 256, 4, "bf16", False),    # two float4 of state per lane
@@ -61,17 +63,47 @@ def test_complex_scan_against_oracle(ssd, B, L, H, P, N, G, dtype, init):
     assert ey <= TOL[dtype] and ef <= TOL[dtype]
 
 
-def test_split_resume_and_in_place_state_are_bitwise(ssd):
+@pytest.mark.parametrize("path", ["chunked", "sequential"])
+@pytest.mark.parametrize("B,L,H,G,init", [
+    (3, 64, 4, 1, True),      # one chunk; an odd batch: the last CTA holds one row
+    (1, 300, 2, 1, False),    # five chunks, the last of 44 steps; one row, no state in
+    (2, 2, 3, 3, True),       # two steps
+    (4, 200, 6, 2, True),     # four chunks, two CTAs per head
+])
+def test_complex_chunk_form_against_oracle(ssd, path, B, L, H, G, init):
+    w = Workload("t", B, L, H, 64, 128, G, 1, "bf16", init, "complex")
+    inp = make_complex_inputs(w, seed=320 + L + B)
+    ry, rf = complex_fwd(**inp)
+    y, f = run(ssd, inp, path=path)
+    ey, ef = relerr(y, ry), relerr(f, rf)
+    print(f"{path}: y {ey:.2e} final {ef:.2e}")
+    assert ey <= TOL["bf16"] and ef <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("path,cut", [("sequential", 77), ("chunked", 64)])
+def test_split_resume_and_in_place_state_are_bitwise(ssd, path, cut):
+    # the sequential kernel resumes bitwise at any step; the chunk form at a chunk
+    # boundary (its chunks then start at the same steps, and the state passes in fp32)
     w = Workload("t", 2, 150, 4, 64, 128, 1, 1, "bf16", True, "complex")
     inp = make_complex_inputs(w, seed=310)
-    y, f = run(ssd, inp)
-    cut = 77
+    y, f = run(ssd, inp, path=path)
     first = {k: (v[:, :cut].contiguous() if k in ("x", "dt_raw", "B", "C") else v) for k, v in inp.items()}
     second = {k: (v[:, cut:].contiguous() if k in ("x", "dt_raw", "B", "C") else v) for k, v in inp.items()}
-    y1, f1 = run(ssd, first)
+    y1, f1 = run(ssd, first, path=path)
     state = f1.clone()
-    y2, _ = run(ssd, second, init=state, final_state=state)   # the state updated in place
+    y2, _ = run(ssd, second, init=state, final_state=state, path=path)   # the state updated in place
     assert torch.equal(torch.cat([y1, y2], 1), y) and torch.equal(state, f)
+
+
+def test_chunk_form_matches_the_sequential_kernel(ssd):
+    # the two evaluations of the same recurrence agree far below the bf16 bar that
+    # both meet against the oracle (bf16 operands in the chunk form)
+    w = Workload("t", 4, 256, 8, 64, 128, 2, 1, "bf16", True, "complex")
+    inp = make_complex_inputs(w, seed=330)
+    yc, fc = run(ssd, inp, path="chunked")
+    ys, fs = run(ssd, inp, path="sequential")
+    assert relerr(yc, ys.double().cpu().numpy()) <= TOL["bf16"]
+    assert relerr(fc, fs.double().cpu().numpy()) <= TOL["bf16"]
 
 
 def test_no_steps_passes_the_state_through(ssd):
