@@ -58,21 +58,23 @@ using namespace ssd::ptx;
 constexpr int kR = 128;                    // rows: two batch rows' chunks of 64 steps
 constexpr int kQ = 64;                     // steps per chunk
 constexpr int kP = 64, kN = 128;
-constexpr int kRowWarps = 4;               // warps 0-3: TMEM lane quarters, one row per thread
-constexpr int kIssueWarp = 4;              // TMA and MMA issue, TMEM owner
-constexpr int kThreads = 5 * 32;
+constexpr int kRowWarps = 8;               // warps 0-7: warp w reads TMEM lane quarter w & 3 (one row
+                                           // per thread) and takes half w >> 2 of that quarter's work
+constexpr int kIssueWarp = 8;              // TMA and MMA issue, TMEM owner
+constexpr int kThreads = 9 * 32;
 constexpr uint32_t kT16 = 16384;           // one [128 rows][64 bf16] tile, 128-byte swizzle
 
 // shared memory (from a 1024-aligned base)
 constexpr uint32_t kOffC = 0;                      // C [t][n], two tiles (n 0-63, 64-127); then C^
-constexpr uint32_t kOffCT = kOffC + 2 * kT16;      // C~; after S, y staging (tile 0)
+constexpr uint32_t kOffCT = kOffC + 2 * kT16;      // C~; after S, y staging (2 KB per warp)
 constexpr uint32_t kOffCL = kOffCT + 2 * kT16;     // C_L
 constexpr uint32_t kOffB = kOffCL + 2 * kT16;      // B [s][n]
 constexpr uint32_t kOffBT = kOffB + 2 * kT16;      // B~
 constexpr uint32_t kOffX = kOffBT + 2 * kT16;      // x [s][p]
 constexpr uint32_t kOffHB = kOffX + kT16;          // the states entering the chunk, bf16 [n][p], one tile each
 constexpr uint32_t kOffArr = kOffHB + 2 * kT16;
-enum { A_TAU = 0, A_FR, A_FI, A_CR, A_CI, A_NUM };  // per row: tau, f, the column factor of M's blocks
+// per row: tau, f, the column factor of M's blocks, Lambda, g
+enum { A_TAU = 0, A_FR, A_FI, A_CR, A_CI, A_LR, A_LI, A_GR, A_GI, A_NUM };
 constexpr uint32_t kOffRed = kOffArr + A_NUM * kR * 4;   // 8 floats: warp totals of dt
 constexpr uint32_t kOffBars = kOffRed + 8 * 4;
 enum { BAR_FULL = 0, BAR_ROWS_A, BAR_MMA_S, BAR_ROWS_M, BAR_MMA_Y, BAR_EPI, BAR_RSYNC, BAR_DRAIN, kNumBars };
@@ -97,7 +99,7 @@ struct CtcParams {
 
 struct CtcMaps {
     CUtensorMap x, B, C;  // bf16 loads, boxes of 64 x 64
-    CUtensorMap y;        // bf16 stores, boxes of 64 x 32
+    CUtensorMap y;        // bf16 stores, boxes of 32 x 32, no swizzle
 };
 
 __device__ __forceinline__ uint32_t sw128(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
@@ -263,13 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
         }
     } else {
         // ------------------------------------------------------------ rows
-        const int q = warp;                      // TMEM lane quarter
+        const int q = warp & 3;                  // TMEM lane quarter
+        const int hf = warp >> 2;                // half: tile columns 64 hf.., M's blocks of parity hf,
+                                                 // state hf, y columns 32 hf..
         const int t = 32 * q + lane;             // this thread's step row (and state row n = t)
         const int rr = q >> 1, i = t & (kQ - 1); // the step row's batch row (0, 1) and step in the chunk
         const int b = b0 + rr;
         const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
         uint8_t *tC = smem + kOffC, *tCT = smem + kOffCT, *tCL = smem + kOffCL, *tB = smem + kOffB;
         uint8_t *tBT = smem + kOffBT, *tX = smem + kOffX, *tHB = smem + kOffHB;
+        float *lr_s = arr + A_LR * kR, *li_s = arr + A_LI * kR, *gr_s = arr + A_GR * kR, *gi_s = arr + A_GI * kR;
         const float Dh = p.D[h];
         uint32_t rphase = 0;
         // (every wait's result is made warp-uniform: the TMEM loads and stores that
@@ -278,90 +283,103 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
             const long long l = (long long)c * kQ + i;
             return (b < p.Bt && l < p.L) ? p.dt_raw[((size_t)b * p.L + l) * H + h] : 0.f;
         };
-        float zr = nch > 0 ? dt_raw_of(0) : 0.f;
+        float zr = (nch > 0 && hf == 0) ? dt_raw_of(0) : 0.f;
+        // state hf entering the first chunk (row n = t), loaded now: the loads overlap
+        // the first chunk's tiles and factors
+        uint32_t hv[2][32];
+        {
+            const float *src = (p.h0 && b0 + hf < p.Bt) ? p.h0 + ((size_t)(b0 + hf) * H + h) * NP + t : nullptr;
+#pragma unroll
+            for (int k = 0; k < 64; ++k)
+                hv[k >> 5][k & 31] = __float_as_uint(src ? __ldg(src + (size_t)k * kN) : 0.f);
+        }
         for (int c = 0; c < nch && ok; ++c) {
             const uint32_t par = c & 1;
             const long long l = (long long)c * kQ + i;
             const bool valid = b < p.Bt && l < p.L;
-            // ---- dt, tau within the row's chunk (its two warps), the complex factors
-            const float dt = valid ? softplus_f32(zr + p.dt_bias[h]) : 0.f;
-            if (c + 1 < nch)
-                zr = dt_raw_of(c + 1);   // in flight through this chunk
-            float tau = dt;
+            // ---- dt, tau within the row's chunk (its two warps of half 0), the complex factors
+            float dt = 0.f, tau = 0.f;
+            if (hf == 0) {
+                dt = valid ? softplus_f32(zr + p.dt_bias[h]) : 0.f;
+                if (c + 1 < nch)
+                    zr = dt_raw_of(c + 1);   // in flight through this chunk
+                tau = dt;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float u = __shfl_up_sync(0xffffffffu, tau, o);
-                if (lane >= o)
-                    tau += u;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, tau, o);
+                    if (lane >= o)
+                        tau += u;
+                }
+                if (lane == 31)
+                    red[q] = tau;
             }
-            if (lane == 31)
-                red[q] = tau;
             if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))))
                 break;
-            tau += (q & 1) ? red[q - 1] : 0.f;
-            const float tau_end = red[2 * rr] + red[2 * rr + 1];
-            // f = (e^{A dt} - 1) / A, with e^{A dt} - 1 = expm1(a_r dt) cos(a_i dt) - 2 sin^2(a_i dt / 2)
-            //     + i e^{a_r dt} sin(a_i dt)
-            float sd, cd;
-            sincosf(ai * dt, &sd, &cd);
-            const float sh = sinf(0.5f * ai * dt);
-            const float nr = expm1f(ar * dt) * cd - 2.f * sh * sh, ni = expf(ar * dt) * sd;
-            const float2 f = make_float2((nr * ar + ni * ai) * inv, (ni * ar - nr * ai) * inv);
-            const float2 lam = cexp_a(ar, ai, tau);                      // Lambda_t
-            const float2 gw = cmul(cexp_a(ar, ai, tau_end - tau), f);    // g_t
-            const float tau_e = __shfl_sync(0xffffffffu, tau, lane | 15);   // the end of this 16-step block
-            const float2 cf = cmul(cexp_a(ar, ai, tau_e - tau), f);      // column factor of M's blocks
-            tau_s[t] = tau;
-            fr_s[t] = f.x;
-            fi_s[t] = f.y;
-            cr_s[t] = cf.x;
-            ci_s[t] = cf.y;
-            // (the M build reads other rows' entries)
+            if (hf == 0) {
+                tau += (q & 1) ? red[q - 1] : 0.f;
+                const float tau_end = red[2 * rr] + red[2 * rr + 1];
+                // f = (e^{A dt} - 1) / A, with e^{A dt} - 1 = expm1(a_r dt) cos(a_i dt) - 2 sin^2(a_i dt / 2)
+                //     + i e^{a_r dt} sin(a_i dt)
+                float sd, cd;
+                sincosf(ai * dt, &sd, &cd);
+                const float sh = sinf(0.5f * ai * dt);
+                const float nr = expm1f(ar * dt) * cd - 2.f * sh * sh, ni = expf(ar * dt) * sd;
+                const float2 f = make_float2((nr * ar + ni * ai) * inv, (ni * ar - nr * ai) * inv);
+                const float2 lam = cexp_a(ar, ai, tau);                      // Lambda_t
+                const float2 gw = cmul(cexp_a(ar, ai, tau_end - tau), f);    // g_t
+                const float tau_e = __shfl_sync(0xffffffffu, tau, lane | 15);   // the end of this 16-step block
+                const float2 cf = cmul(cexp_a(ar, ai, tau_e - tau), f);      // column factor of M's blocks
+                tau_s[t] = tau;
+                fr_s[t] = f.x;
+                fi_s[t] = f.y;
+                cr_s[t] = cf.x;
+                ci_s[t] = cf.y;
+                lr_s[t] = lam.x;
+                li_s[t] = lam.y;
+                gr_s[t] = gw.x;
+                gi_s[t] = gw.y;
+            }
+            // (every row's entries are read by the other half and by the M build)
             if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))) ||
                 !(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_FULL], par))))
                 break;
-            // ---- C^ (in place), C~, C_L from row t of C; B~ from row t of B
+            // ---- C^ (in place), C~, C_L from row t of C; B~ from row t of B (tile hf)
+            {
+                const float2 lam = make_float2(lr_s[t], li_s[t]), gw = make_float2(gr_s[t], gi_s[t]);
+                uint8_t *c0 = tC + hf * kT16, *b1 = tB + hf * kT16;
 #pragma unroll 1
-            for (int cc = 0; cc < 16; ++cc) {
-                uint8_t *c0 = tC + (cc >> 3) * kT16, *b1 = tB + (cc >> 3) * kT16;
-                const int ch = cc & 7;
-                float v[8], w1[8], w2[8], w3[8];
-                ld8(c0, t, ch, v);
+                for (int ch = 0; ch < 8; ++ch) {
+                    float v[8], w1[8], w2[8], w3[8];
+                    ld8(c0, t, ch, v);
 #pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const float re = v[k], im = v[k + 1];
-                    w1[k] = im;                              // C~ = (C_i, C_r)
-                    w1[k + 1] = re;
-                    w2[k] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
-                    w2[k + 1] = -(lam.x * im + lam.y * re);
-                    w3[k] = re;                              // C^ = (C_r, -C_i)
-                    w3[k + 1] = -im;
-                }
-                st8(tCT + (cc >> 3) * kT16, t, ch, w1);
-                st8(tCL + (cc >> 3) * kT16, t, ch, w2);
-                st8(c0, t, ch, w3);
-                ld8(b1, t, ch, v);
+                    for (int k = 0; k < 8; k += 2) {
+                        const float re = v[k], im = v[k + 1];
+                        w1[k] = im;                              // C~ = (C_i, C_r)
+                        w1[k + 1] = re;
+                        w2[k] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
+                        w2[k + 1] = -(lam.x * im + lam.y * re);
+                        w3[k] = re;                              // C^ = (C_r, -C_i)
+                        w3[k + 1] = -im;
+                    }
+                    st8(tCT + hf * kT16, t, ch, w1);
+                    st8(tCL + hf * kT16, t, ch, w2);
+                    st8(c0, t, ch, w3);
+                    ld8(b1, t, ch, v);
 #pragma unroll
-                for (int k = 0; k < 8; k += 2) {
-                    const float re = v[k], im = v[k + 1];
-                    w1[k] = gw.x * re - gw.y * im;           // B~ = g B
-                    w1[k + 1] = gw.x * im + gw.y * re;
+                    for (int k = 0; k < 8; k += 2) {
+                        const float re = v[k], im = v[k + 1];
+                        w1[k] = gw.x * re - gw.y * im;           // B~ = g B
+                        w1[k + 1] = gw.x * im + gw.y * re;
+                    }
+                    st8(tBT + hf * kT16, t, ch, w1);
                 }
-                st8(tBT + (cc >> 3) * kT16, t, ch, w1);
             }
-            // ---- the states (row n = t): bf16 copies for C_L H, then rotated by Lambda_63
-            //      of their batch row (lanes 2k, 2k+1 hold a component's re, im)
-#pragma unroll 1
-            for (int r = 0; r < 2; ++r) {
-                uint32_t v[2][32];
-                if (c == 0) {
-                    const float *src = (p.h0 && b0 + r < p.Bt) ? p.h0 + ((size_t)(b0 + r) * H + h) * NP + t : nullptr;
-#pragma unroll
-                    for (int k = 0; k < 64; ++k)
-                        v[k >> 5][k & 31] = __float_as_uint(src ? __ldg(src + (size_t)k * kN) : 0.f);
-                } else {
-                    tmem_ld32(trow + kColH + 64 * r, v[0]);
-                    tmem_ld32(trow + kColH + 64 * r + 32, v[1]);
+            // ---- state hf (row n = t): its bf16 copy for C_L H, then rotated by Lambda_63
+            //      of its batch row (lanes 2k, 2k+1 hold a component's re, im)
+            {
+                if (c > 0) {
+                    tmem_ld32(trow + kColH + 64 * hf, hv[0]);
+                    tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
                     tmem_wait_ld();
                 }
 #pragma unroll
@@ -369,35 +387,36 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                     float w[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        w[e] = __uint_as_float(v[cc >> 2][8 * (cc & 3) + e]);
-                    st8(tHB + r * kT16, t, cc, w);
+                        w[e] = __uint_as_float(hv[cc >> 2][8 * (cc & 3) + e]);
+                    st8(tHB + hf * kT16, t, cc, w);
                 }
-                const float te = red[2 * r] + red[2 * r + 1];   // tau at the end of row r's chunk
+                const float te = red[2 * hf] + red[2 * hf + 1];   // tau at the end of row hf's chunk
                 const float2 z = cexp_a(ar, ai, te);
                 const bool odd = lane & 1;
 #pragma unroll
                 for (int k = 0; k < 64; ++k) {
-                    const float mine = __uint_as_float(v[k >> 5][k & 31]);
+                    const float mine = __uint_as_float(hv[k >> 5][k & 31]);
                     const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
                     // even lane: re' = z_r re - z_i im; odd lane: im' = z_r im + z_i re
                     const float out = odd ? fmaf(z.x, mine, z.y * other) : fmaf(z.x, mine, -z.y * other);
-                    v[k >> 5][k & 31] = __float_as_uint(out);
+                    hv[k >> 5][k & 31] = __float_as_uint(out);
                 }
-                tmem_st32(trow + kColH + 64 * r, v[0]);
-                tmem_st32(trow + kColH + 64 * r + 32, v[1]);
+                tmem_st32(trow + kColH + 64 * hf, hv[0]);
+                tmem_st32(trow + kColH + 64 * hf + 32, hv[1]);
             }
             tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS_A]);
-            // ---- M from S_re, S_im in place (row t; blocks of 16 steps)
+            // ---- M from S_re, S_im in place (row t; the blocks of 16 steps of parity hf)
             if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_S], par))))
                 break;
             tc_fence_after();
             {
                 const int gdiag = t >> 4;   // the block holding step t (2q or 2q + 1 within the warp)
+                const float tau_t = tau_s[t];   // (computed by half 0)
 #pragma unroll 1
-                for (int G = 0; G < 8; ++G) {
+                for (int G = hf; G < 8; G += 2) {
                     uint32_t m[8];
                     // warp-uniform: some row of this warp reaches block G (the TMEM loads are
                     // collective); each lane then takes its own case
@@ -409,30 +428,36 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                         uint32_t sr[16], si[16];
                         tmem_ld16(trow + kColS + 16 * G, sr);
                         tmem_ld16(trow + kColSI + 16 * G, si);
+                        const int s0 = 16 * G, se = s0 + 15;
+                        // e^{A (tau_t - tau_e)}: at most 1 in modulus below the diagonal block and
+                        // at most e^{|a_r| span} on it; the factored form there while that stays
+                        // far inside fp32 (the span test is the same for the whole block)
+                        const bool factored = G < gdiag || fabsf(ar) * (tau_s[se] - tau_s[s0]) < 60.f;
+                        const float2 rf = cexp_a(ar, ai, tau_t - tau_s[se]);
                         tmem_wait_ld();
                         float mv[16];
                         if (G > gdiag) {    // above this row's diagonal
 #pragma unroll
                             for (int e = 0; e < 16; ++e)
                                 mv[e] = 0.f;
-                        } else if (G == gdiag) {   // the diagonal block: e^{A (tau_t - tau_s)} f_s, s <= t
+                        } else if (factored) {
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
-                                const int s = 16 * G + e;
+                                const int s = s0 + e;
+                                const float2 E = cmul(rf, make_float2(cr_s[s], ci_s[s]));
+                                const float v = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
+                                mv[e] = s <= t ? v : 0.f;
+                            }
+                        } else {            // the diagonal block, directly: e^{A (tau_t - tau_s)} f_s, s <= t
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                const int s = s0 + e;
                                 float val = 0.f;
                                 if (s <= t) {
-                                    const float2 E = cmul(cexp_a(ar, ai, tau - tau_s[s]), make_float2(fr_s[s], fi_s[s]));
+                                    const float2 E = cmul(cexp_a(ar, ai, tau_t - tau_s[s]), make_float2(fr_s[s], fi_s[s]));
                                     val = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
                                 }
                                 mv[e] = val;
-                            }
-                        } else {            // below: e^{A (tau_t - tau_e)} times the column factor
-                            const float2 rf = cexp_a(ar, ai, tau - tau_s[16 * G + 15]);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int s = 16 * G + e;
-                                const float2 E = cmul(rf, make_float2(cr_s[s], ci_s[s]));
-                                mv[e] = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
                             }
                         }
 #pragma unroll
@@ -445,14 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
             tmem_wait_st();
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS_M]);
-            // ---- y = M x + C_L H_r + D x (row t), by a tensor store per warp
+            // ---- y = M x + C_L H_r + D x (row t, columns 32 hf ..), by a tensor store per warp
             if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_Y], par))))
                 break;
             tc_fence_after();
             {
-                uint8_t *stg = tCT + 32 * q * 128;   // this warp's box (C~ is dead)
+                uint8_t *stg = tCT + warp * 2048;   // this warp's box: 32 rows x 32 bf16, plain (C~ is dead)
 #pragma unroll 1
-                for (int g16 = 0; g16 < 4; ++g16) {
+                for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
                     uint32_t ym[16], yo[16];
                     tmem_ld16(trow + kColY + 16 * g16, ym);
                     tmem_ld16(trow + kColSI + 64 * rr + 16 * g16, yo);
@@ -464,7 +489,9 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             o[e] = fmaf(Dh, xv[e], __uint_as_float(ym[8 * hh + e]) + __uint_as_float(yo[8 * hh + e]));
-                        st8(stg, lane, 2 * g16 + hh, o);
+                        *reinterpret_cast<uint4 *>(stg + lane * 64 + 16 * (2 * (g16 & 1) + hh)) =
+                            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                       pack_bf16x2(o[6], o[7]));
                     }
                 }
                 fence_proxy_async_smem();
@@ -472,28 +499,22 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                 if (lane == 0) {
                     const long long r0 = (long long)c * kQ + 32 * (q & 1);
                     if (b < p.Bt && r0 < p.L)
-                        tma_store_3d(&maps.y, stg, h * kP, (int)r0, b);
+                        tma_store_3d(&maps.y, stg, h * kP + 32 * hf, (int)r0, b);
                     bulk_commit_group();
                     bulk_wait_read_all();   // the box is rewritten next chunk
                 }
             }
             warp_arrive(&bars[BAR_EPI]);
         }
-        // ---- the final states (row n = t), [P][N]
-        if (ok && p.h_final) {
-#pragma unroll 1
-            for (int r = 0; r < 2; ++r) {
-                if (b0 + r >= p.Bt)
-                    break;
-                uint32_t v[2][32];
-                tmem_ld32(trow + kColH + 64 * r, v[0]);
-                tmem_ld32(trow + kColH + 64 * r + 32, v[1]);
-                tmem_wait_ld();
-                float *dst = p.h_final + ((size_t)(b0 + r) * H + h) * NP + t;
+        // ---- the final state hf (row n = t), [P][N]
+        if (ok && p.h_final && b0 + hf < p.Bt) {
+            tmem_ld32(trow + kColH + 64 * hf, hv[0]);
+            tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
+            tmem_wait_ld();
+            float *dst = p.h_final + ((size_t)(b0 + hf) * H + h) * NP + t;
 #pragma unroll
-                for (int k = 0; k < 64; ++k)
-                    dst[(size_t)k * kN] = __uint_as_float(v[k >> 5][k & 31]);
-            }
+            for (int k = 0; k < 64; ++k)
+                dst[(size_t)k * kN] = __uint_as_float(hv[k >> 5][k & 31]);
         }
         if (lane == 0)
             bulk_wait_all();
@@ -536,7 +557,7 @@ cudaError_t complex_tc_launch(const ComplexArgs &a, cudaStream_t st)
     if (!make_tmap_bf16_3d(&maps.x, a.x, HP, L, Bt, HP * 2, HP * 2 * L, 64, kQ) ||
         !make_tmap_bf16_3d(&maps.B, a.B, GN, L, Bt, GN * 2, GN * 2 * L, 64, kQ) ||
         !make_tmap_bf16_3d(&maps.C, a.C, GN, L, Bt, GN * 2, GN * 2 * L, 64, kQ) ||
-        !make_tmap_bf16_3d(&maps.y, a.y, HP, L, Bt, HP * 2, HP * 2 * L, 64, 32))
+        !make_tmap_bf16_3d(&maps.y, a.y, HP, L, Bt, HP * 2, HP * 2 * L, 32, 32, false))
         return cudaErrorInvalidValue;
     CtcParams p;
     p.dt_raw = a.dt_raw;

@@ -25,10 +25,11 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder()
 }
 
 // Row-major bf16 tensor [d2][d1][d0] (d0 contiguous) viewed through boxes of
-// box0 x box1 x 1 elements with 128-byte swizzle; out-of-range elements read
+// box0 x box1 x 1 elements with the 128-byte swizzle (or none); out-of-range elements read
 // as zero.  strides in bytes: s1 = stride of dim 1, s2 = stride of dim 2.
 inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, uint64_t d1,
-                              uint64_t d2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1)
+                              uint64_t d2, uint64_t s1, uint64_t s2, uint32_t box0, uint32_t box1,
+                              bool swizzle = true)
 {
     auto enc = tensor_map_encoder();
     if (!enc)
@@ -38,7 +39,8 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t d0, u
     cuuint32_t box[3] = {box0, box1, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims,
-                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
