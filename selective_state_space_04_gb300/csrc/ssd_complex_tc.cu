@@ -33,8 +33,8 @@
 // Phases per chunk, one mbarrier hand-off each (all waits bounded):
 //   TMA: C, B, x of both rows.    rows: dt, tau and the complex factors; C^, C~,
 //   C_L, B~ from C and B; each state's bf16 copy, then the state rotated by
-//   Lambda_63 in TMEM.    MMA: S_re, S_im.    rows: M in place of S_re.
-//   MMA: Y = M x; C_L H_0, C_L H_1 in place of S_im; H_r += B~^T x (its rows).
+//   Lambda_63 in TMEM.    MMA: S_re, S_im; then H_r += B~^T x (its rows) and
+//   C_L H_0.    rows: M in place of S_re.    MMA: Y = M x; C_L H_1 in place of S_im.
 //   rows: y = Y + C_L H_r + D x by tensor stores.  After the last chunk the
 //   states go out.
 #include <cuda.h>
@@ -83,9 +83,10 @@ constexpr uint32_t kSmemBytes = kOffHolder + 16 + 1024;
 
 // TMEM columns
 constexpr uint32_t kColS = 0;       // S_re; M (bf16 pairs) in the first 8 columns of each 16
-constexpr uint32_t kColSI = 128;    // S_im; then C_L H_0 (+0) and C_L H_1 (+64)
+constexpr uint32_t kColSI = 128;    // S_im; then C_L H_1
 constexpr uint32_t kColY = 256;     // M x
 constexpr uint32_t kColH = 320;     // the states: row r at +64 r
+constexpr uint32_t kColYO0 = 448;   // C_L H_0 (issued with S, before M is built)
 
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 
@@ -240,18 +241,21 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ss(tmem + kColSI, kmaj(sCT, kk), kmaj(sB, kk), i128kk, kk > 0);
                 mma_commit(&bars[BAR_MMA_S]);
-                // ---- Y = M x; C_L H_r (in S_im's columns); H_r += B~^T x over row r's steps
+                // H_r += B~^T x over row r's steps, and C_L H_0: their operands are ready, so
+                // they run while M is built
+                for (int r = 0; r < 2; ++r)
+                    for (int kk = 4 * r; kk < 4 * r + 4; ++kk)
+                        mma_ss(tmem + kColH + 64 * r, mnmaj(sBT, kk), mnmaj(sX, kk), i64nn, 1);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColYO0, kmaj(sCL, kk), mnmaj(sHB, kk), i64kn, kk > 0);
+                // ---- Y = M x; C_L H_1 (in S_im's columns, once M has been built from them)
                 if (!(ok = wait_bar(&bars[BAR_ROWS_M], par)))
                     break;
                 tc_fence_after();
                 for (int kk = 0; kk < 8; ++kk)
                     mma_ts(tmem + kColY, tmem + kColS + 16 * kk, mnmaj(sX, kk), i64kn, kk > 0);
-                for (int r = 0; r < 2; ++r)
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_ss(tmem + kColSI + 64 * r, kmaj(sCL, kk), mnmaj(sHB + r * kT16, kk), i64kn, kk > 0);
-                for (int r = 0; r < 2; ++r)
-                    for (int kk = 4 * r; kk < 4 * r + 4; ++kk)
-                        mma_ss(tmem + kColH + 64 * r, mnmaj(sBT, kk), mnmaj(sX, kk), i64nn, 1);
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_ss(tmem + kColSI, kmaj(sCL, kk), mnmaj(sHB + kT16, kk), i64kn, kk > 0);
                 mma_commit(&bars[BAR_MMA_Y]);
             }
             // no MMA may be in flight when tensor memory is released, nor a TMA load
@@ -480,7 +484,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                 for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
                     uint32_t ym[16], yo[16];
                     tmem_ld16(trow + kColY + 16 * g16, ym);
-                    tmem_ld16(trow + kColSI + 64 * rr + 16 * g16, yo);
+                    tmem_ld16(trow + (rr ? kColSI : kColYO0) + 16 * g16, yo);
                     tmem_wait_ld();
                     float xv[8], o[8];
 #pragma unroll
