@@ -18,10 +18,13 @@
 //   H' = rot(Lambda_63) H + B~^T x, B~[s] = (Re(g_s B_s[k]), Im(g_s B_s[k])),
 // rot(z) multiplying each complex component of H (the lane pair 2k, 2k+1) by z.
 //
-// One CTA takes two batch rows of one head, stacked as the 128 rows of every
+// A work item is two batch rows of one head, stacked as the 128 rows of every
 // tcgen05 MMA (kind::f16, bf16 operands in shared memory with the 128-byte
-// swizzle, fp32 accumulators in TMEM; lane = row), and walks their chunks
-// together with both states in TMEM.  E is zero across the two rows, so M is
+// swizzle, fp32 accumulators in TMEM; lane = row), whose chunks are walked
+// together with both states in TMEM.  One persistent CTA per SM takes items in
+// turn; each step's C and B load once the previous step's S products have read
+// theirs, its x once the previous epilogue has, and an item's entering states
+// are prefetched into L2 an item ahead.  E is zero across the two rows, so M is
 // block diagonal; the products with a row's state are issued once per state
 // over all 128 rows, and each row keeps its own one.  M below the diagonal
 // blocks is factored per 16-step block (ending at step e) as
@@ -41,6 +44,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -180,13 +184,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
     float *red = reinterpret_cast<float *>(smem + kOffRed);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int H = p.H, h = (int)blockIdx.y, g = h / (H / p.G);
-    const int b0 = 2 * (int)blockIdx.x;                       // batch rows b0, b0 + 1
+    const int H = p.H;
     const int nch = (int)((p.L + kQ - 1) / kQ);
-    const float la = p.A_polar[2 * h], th = p.A_polar[2 * h + 1];
-    const float ar = expf(la) * cosf(th), ai = expf(la) * sinf(th);
-    const float inv = 1.f / (ar * ar + ai * ai);            // 1 / |A|^2
     const size_t NP = (size_t)kN * kP;
+    // work items: (pair of batch rows, head), pair-major so that the CTAs running
+    // at once share a group's B and C; CTA i takes items i, i + grid, ...
+    const long long nitems = (long long)((p.Bt + 1) / 2) * H;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i)
@@ -202,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
     tc_fence_after();
     const uint32_t tmem = *holder;
     bool ok = true;
-    uint32_t last_full = 0;   // chunks whose loads were issued (issue lane)
+    uint32_t armed = 0;   // steps whose loads were issued (issue lane)
 
     if (warp == kIssueWarp) {
         if (lane == 0) {
@@ -216,53 +219,96 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
             auto mnmaj = [](uint32_t base, int kk) { return sdesc_sw128(base + kk * 2048, kT16, 1024); };
             const uint32_t i128kk = idesc_bf16_f32(128, 128, 0, 0), i64kn = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t i64nn = idesc_bf16_f32(128, 64, 1, 1);
-            for (int c = 0; c < nch && ok; ++c) {
-                const uint32_t par = c & 1;
-                if (c > 0 && !(ok = wait_bar(&bars[BAR_EPI], par ^ 1u)))
-                    break;
-                // ---- TMA: C, B (two 64-column boxes each) and x of both rows
+            // the loads of one step (item u, chunk c): C and B once the previous step's S
+            // products have read theirs, x once the previous step's epilogue has read
+            // its x; the barrier is armed for all of them with the first
+            auto load_cb = [&](long long u, int c) {
+                const int bp = (int)(u / H), hh = (int)(u - (long long)bp * H), gg = hh / (H / p.G);
                 mbar_arrive_expect_tx(&bars[BAR_FULL], 5 * kT16);
                 for (int r = 0; r < 2; ++r) {
                     const uint32_t ro = r * (kT16 / 2);   // rows 64 r ..
-                    const int t0 = c * kQ, br = b0 + r;
-                    tma_load_3d(smem + kOffC + ro, &maps.C, &bars[BAR_FULL], g * kN, t0, br, shared);
-                    tma_load_3d(smem + kOffC + kT16 + ro, &maps.C, &bars[BAR_FULL], g * kN + 64, t0, br, shared);
-                    tma_load_3d(smem + kOffB + ro, &maps.B, &bars[BAR_FULL], g * kN, t0, br, shared);
-                    tma_load_3d(smem + kOffB + kT16 + ro, &maps.B, &bars[BAR_FULL], g * kN + 64, t0, br, shared);
-                    tma_load_3d(smem + kOffX + ro, &maps.x, &bars[BAR_FULL], h * kP, t0, br, once);
+                    const int t0 = c * kQ, br = 2 * bp + r;
+                    tma_load_3d(smem + kOffC + ro, &maps.C, &bars[BAR_FULL], gg * kN, t0, br, shared);
+                    tma_load_3d(smem + kOffC + kT16 + ro, &maps.C, &bars[BAR_FULL], gg * kN + 64, t0, br, shared);
+                    tma_load_3d(smem + kOffB + ro, &maps.B, &bars[BAR_FULL], gg * kN, t0, br, shared);
+                    tma_load_3d(smem + kOffB + kT16 + ro, &maps.B, &bars[BAR_FULL], gg * kN + 64, t0, br, shared);
                 }
-                last_full = c + 1;
-                // ---- S_re = C^ B^T, S_im = C~ B^T
-                if (!(ok = wait_bar(&bars[BAR_ROWS_A], par)))
-                    break;
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColS, kmaj(sC, kk), kmaj(sB, kk), i128kk, kk > 0);
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColSI, kmaj(sCT, kk), kmaj(sB, kk), i128kk, kk > 0);
-                mma_commit(&bars[BAR_MMA_S]);
-                // H_r += B~^T x over row r's steps, and C_L H_0: their operands are ready, so
-                // they run while M is built
+                ++armed;
+            };
+            auto load_x = [&](long long u, int c) {
+                const int bp = (int)(u / H), hh = (int)(u - (long long)bp * H);
                 for (int r = 0; r < 2; ++r)
-                    for (int kk = 4 * r; kk < 4 * r + 4; ++kk)
-                        mma_ss(tmem + kColH + 64 * r, mnmaj(sBT, kk), mnmaj(sX, kk), i64nn, 1);
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColYO0, kmaj(sCL, kk), mnmaj(sHB, kk), i64kn, kk > 0);
-                // ---- Y = M x; C_L H_1 (in S_im's columns, once M has been built from them)
-                if (!(ok = wait_bar(&bars[BAR_ROWS_M], par)))
-                    break;
-                tc_fence_after();
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ts(tmem + kColY, tmem + kColS + 16 * kk, mnmaj(sX, kk), i64kn, kk > 0);
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_ss(tmem + kColSI, kmaj(sCL, kk), mnmaj(sHB + kT16, kk), i64kn, kk > 0);
-                mma_commit(&bars[BAR_MMA_Y]);
+                    tma_load_3d(smem + kOffX + r * (kT16 / 2), &maps.x, &bars[BAR_FULL], hh * kP, c * kQ, 2 * bp + r,
+                                once);
+            };
+            // an item's entering states into L2 one item ahead (the row warps load them)
+            auto prefetch_states = [&](long long u) {
+                if (!p.h0 || u >= nitems)
+                    return;
+                const int bp = (int)(u / H), hh = (int)(u - (long long)bp * H);
+                for (int r = 0; r < 2; ++r)
+                    if (2 * bp + r < p.Bt)
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                                         p.h0 + ((size_t)(2 * bp + r) * H + hh) * NP),
+                                     "r"((uint32_t)(NP * 4))
+                                     : "memory");
+            };
+            uint32_t k = 0;   // steps so far (the barriers' phases)
+            if ((long long)blockIdx.x < nitems) {
+                load_cb(blockIdx.x, 0);
+                load_x(blockIdx.x, 0);
+            }
+            for (long long u = blockIdx.x; u < nitems && ok; u += gridDim.x) {
+                prefetch_states(u + gridDim.x);
+                for (int c = 0; c < nch && ok; ++c, ++k) {
+                    const uint32_t par = k & 1;
+                    const long long un = c + 1 < nch ? u : u + gridDim.x;   // the next step
+                    const int cn = c + 1 < nch ? c + 1 : 0;
+                    const bool has_next = un < nitems;
+                    // ---- S_re = C^ B^T, S_im = C~ B^T
+                    if (!(ok = wait_bar(&bars[BAR_ROWS_A], par)))
+                        break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColS, kmaj(sC, kk), kmaj(sB, kk), i128kk, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColSI, kmaj(sCT, kk), kmaj(sB, kk), i128kk, kk > 0);
+                    mma_commit(&bars[BAR_MMA_S]);
+                    // H_r += B~^T x over row r's steps, and C_L H_0: their operands are ready,
+                    // so they run while M is built
+                    for (int r = 0; r < 2; ++r)
+                        for (int kk = 4 * r; kk < 4 * r + 4; ++kk)
+                            mma_ss(tmem + kColH + 64 * r, mnmaj(sBT, kk), mnmaj(sX, kk), i64nn, 1);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColYO0, kmaj(sCL, kk), mnmaj(sHB, kk), i64kn, kk > 0);
+                    // the next step's C and B, once S has read this step's
+                    if (has_next) {
+                        if (!(ok = wait_bar(&bars[BAR_MMA_S], par)))
+                            break;
+                        load_cb(un, cn);
+                    }
+                    // ---- Y = M x; C_L H_1 (in S_im's columns, once M has been built from them)
+                    if (!(ok = wait_bar(&bars[BAR_ROWS_M], par)))
+                        break;
+                    tc_fence_after();
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ts(tmem + kColY, tmem + kColS + 16 * kk, mnmaj(sX, kk), i64kn, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_ss(tmem + kColSI, kmaj(sCL, kk), mnmaj(sHB + kT16, kk), i64kn, kk > 0);
+                    mma_commit(&bars[BAR_MMA_Y]);
+                    // the next step's x, once this step's epilogue has read its x
+                    if (has_next) {
+                        if (!(ok = wait_bar(&bars[BAR_EPI], par)))
+                            break;
+                        load_x(un, cn);
+                    }
+                }
             }
             // no MMA may be in flight when tensor memory is released, nor a TMA load
             // when the CTA exits
             const uint64_t tw = globaltimer_ns();
-            if (last_full > 0)
-                while (!mbar_wait_for(&bars[BAR_FULL], (last_full - 1) & 1, 1000000u) &&
+            if (armed > 0)
+                while (!mbar_wait_for(&bars[BAR_FULL], (armed - 1) & 1, 1000000u) &&
                        globaltimer_ns() - tw < kTimeoutNs) {
                 }
             mma_commit(&bars[BAR_DRAIN]);   // (arrives once every MMA issued so far has completed)
@@ -274,31 +320,36 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                                                  // state hf, y columns 32 hf..
         const int t = 32 * q + lane;             // this thread's step row (and state row n = t)
         const int rr = q >> 1, i = t & (kQ - 1); // the step row's batch row (0, 1) and step in the chunk
-        const int b = b0 + rr;
         const uint32_t trow = tmem + (static_cast<uint32_t>(32 * q) << 16);
         uint8_t *tC = smem + kOffC, *tCT = smem + kOffCT, *tCL = smem + kOffCL, *tB = smem + kOffB;
         uint8_t *tBT = smem + kOffBT, *tX = smem + kOffX, *tHB = smem + kOffHB;
         float *lr_s = arr + A_LR * kR, *li_s = arr + A_LI * kR, *gr_s = arr + A_GR * kR, *gi_s = arr + A_GI * kR;
-        const float Dh = p.D[h];
-        uint32_t rphase = 0;
+        uint32_t rphase = 0, k = 0;   // (k: steps so far, the barriers' phases)
         // (every wait's result is made warp-uniform: the TMEM loads and stores that
         // follow are collective)
+        for (long long u = blockIdx.x; u < nitems && ok; u += gridDim.x) {
+        const int bp = (int)(u / H), h = (int)(u - (long long)bp * H);
+        const int b0 = 2 * bp, b = b0 + rr;      // batch rows b0, b0 + 1; this step row's
+        const float la = p.A_polar[2 * h], th = p.A_polar[2 * h + 1];
+        const float ar = expf(la) * cosf(th), ai = expf(la) * sinf(th);
+        const float inv = 1.f / (ar * ar + ai * ai);            // 1 / |A|^2
+        const float Dh = p.D[h];
         auto dt_raw_of = [&](int c) {
             const long long l = (long long)c * kQ + i;
             return (b < p.Bt && l < p.L) ? p.dt_raw[((size_t)b * p.L + l) * H + h] : 0.f;
         };
         float zr = (nch > 0 && hf == 0) ? dt_raw_of(0) : 0.f;
-        // state hf entering the first chunk (row n = t), loaded now: the loads overlap
-        // the first chunk's tiles and factors
+        // state hf entering the item's first chunk (row n = t), loaded now: the loads
+        // overlap the chunk's tiles and factors
         uint32_t hv[2][32];
         {
             const float *src = (p.h0 && b0 + hf < p.Bt) ? p.h0 + ((size_t)(b0 + hf) * H + h) * NP + t : nullptr;
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
-                hv[k >> 5][k & 31] = __float_as_uint(src ? __ldg(src + (size_t)k * kN) : 0.f);
+            for (int kk = 0; kk < 64; ++kk)
+                hv[kk >> 5][kk & 31] = __float_as_uint(src ? __ldg(src + (size_t)kk * kN) : 0.f);
         }
-        for (int c = 0; c < nch && ok; ++c) {
-            const uint32_t par = c & 1;
+        for (int c = 0; c < nch && ok; ++c, ++k) {
+            const uint32_t par = k & 1;
             const long long l = (long long)c * kQ + i;
             const bool valid = b < p.Bt && l < p.L;
             // ---- dt, tau within the row's chunk (its two warps of half 0), the complex factors
@@ -356,24 +407,24 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                     float v[8], w1[8], w2[8], w3[8];
                     ld8(c0, t, ch, v);
 #pragma unroll
-                    for (int k = 0; k < 8; k += 2) {
-                        const float re = v[k], im = v[k + 1];
-                        w1[k] = im;                              // C~ = (C_i, C_r)
-                        w1[k + 1] = re;
-                        w2[k] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
-                        w2[k + 1] = -(lam.x * im + lam.y * re);
-                        w3[k] = re;                              // C^ = (C_r, -C_i)
-                        w3[k + 1] = -im;
+                    for (int j = 0; j < 8; j += 2) {
+                        const float re = v[j], im = v[j + 1];
+                        w1[j] = im;                              // C~ = (C_i, C_r)
+                        w1[j + 1] = re;
+                        w2[j] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
+                        w2[j + 1] = -(lam.x * im + lam.y * re);
+                        w3[j] = re;                              // C^ = (C_r, -C_i)
+                        w3[j + 1] = -im;
                     }
                     st8(tCT + hf * kT16, t, ch, w1);
                     st8(tCL + hf * kT16, t, ch, w2);
                     st8(c0, t, ch, w3);
                     ld8(b1, t, ch, v);
 #pragma unroll
-                    for (int k = 0; k < 8; k += 2) {
-                        const float re = v[k], im = v[k + 1];
-                        w1[k] = gw.x * re - gw.y * im;           // B~ = g B
-                        w1[k + 1] = gw.x * im + gw.y * re;
+                    for (int j = 0; j < 8; j += 2) {
+                        const float re = v[j], im = v[j + 1];
+                        w1[j] = gw.x * re - gw.y * im;           // B~ = g B
+                        w1[j + 1] = gw.x * im + gw.y * re;
                     }
                     st8(tBT + hf * kT16, t, ch, w1);
                 }
@@ -398,12 +449,12 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
                 const float2 z = cexp_a(ar, ai, te);
                 const bool odd = lane & 1;
 #pragma unroll
-                for (int k = 0; k < 64; ++k) {
-                    const float mine = __uint_as_float(hv[k >> 5][k & 31]);
+                for (int j = 0; j < 64; ++j) {
+                    const float mine = __uint_as_float(hv[j >> 5][j & 31]);
                     const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
                     // even lane: re' = z_r re - z_i im; odd lane: im' = z_r im + z_i re
                     const float out = odd ? fmaf(z.x, mine, z.y * other) : fmaf(z.x, mine, -z.y * other);
-                    hv[k >> 5][k & 31] = __float_as_uint(out);
+                    hv[j >> 5][j & 31] = __float_as_uint(out);
                 }
                 tmem_st32(trow + kColH + 64 * hf, hv[0]);
                 tmem_st32(trow + kColH + 64 * hf + 32, hv[1]);
@@ -510,15 +561,16 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
             }
             warp_arrive(&bars[BAR_EPI]);
         }
-        // ---- the final state hf (row n = t), [P][N]
+        // ---- the item's final state hf (row n = t), [P][N]
         if (ok && p.h_final && b0 + hf < p.Bt) {
             tmem_ld32(trow + kColH + 64 * hf, hv[0]);
             tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
             tmem_wait_ld();
             float *dst = p.h_final + ((size_t)(b0 + hf) * H + h) * NP + t;
 #pragma unroll
-            for (int k = 0; k < 64; ++k)
-                dst[(size_t)k * kN] = __uint_as_float(hv[k >> 5][k & 31]);
+            for (int kk = 0; kk < 64; ++kk)
+                dst[(size_t)kk * kN] = __uint_as_float(hv[kk >> 5][kk & 31]);
+        }
         }
         if (lane == 0)
             bulk_wait_all();
@@ -546,8 +598,8 @@ bool complex_tc_supported(const ComplexArgs &a)
 {
     auto al = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     return a.dtype == SSD_DTYPE_BF16 && a.headdim == kP && a.dstate == kN && a.seqlen >= 2 &&
-           a.batch >= 1 && a.nheads <= 65535 && (a.batch + 1) / 2 <= 0x7FFFFFFF && a.seqlen < (1LL << 31) &&
-           al(a.x) && al(a.B) && al(a.C) && al(a.y);
+           a.batch >= 1 && a.batch < (1LL << 30) && a.seqlen < (1LL << 31) &&
+           (long long)((a.batch + 1) / 2) * a.nheads < (1LL << 40) && al(a.x) && al(a.B) && al(a.C) && al(a.y);
 }
 
 cudaError_t complex_tc_launch(const ComplexArgs &a, cudaStream_t st)
@@ -578,7 +630,12 @@ cudaError_t complex_tc_launch(const ComplexArgs &a, cudaStream_t st)
         cudaFuncSetAttribute(ssd_complex_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid((unsigned)((a.batch + 1) / 2), (unsigned)a.nheads);
+    // persistent: one CTA per SM (its shared memory), each walking items
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const long long nitems = (long long)((a.batch + 1) / 2) * a.nheads;
+    const dim3 grid((unsigned)std::min<long long>(nitems, sms));
     ssd_complex_tc_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
     return cudaGetLastError();
 }
