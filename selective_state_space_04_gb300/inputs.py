@@ -92,6 +92,9 @@ WORKLOADS = {
                                         "complex"),
     "complex_decode_2p7b_128seq": Workload("complex_decode_2p7b_128seq", 128, 1, 80, 64, 128, 1, 1, "bf16", True,
                                            "complex"),
+    # long complex sequences: 8 x 4096 tokens, 38 heads (152 pairs of batch rows and
+    # heads, one per SM for the chunk form), the state in and out
+    "complex_long_8x4096": Workload("complex_long_8x4096", 8, 4096, 38, 64, 128, 1, 1, "bf16", True, "complex"),
 }
 
 _TORCH_DTYPE = {"bf16": torch.bfloat16, "f32": torch.float32}
