@@ -328,249 +328,249 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_complex_tc_kernel(const __gri
         // (every wait's result is made warp-uniform: the TMEM loads and stores that
         // follow are collective)
         for (long long u = blockIdx.x; u < nitems && ok; u += gridDim.x) {
-        const int bp = (int)(u / H), h = (int)(u - (long long)bp * H);
-        const int b0 = 2 * bp, b = b0 + rr;      // batch rows b0, b0 + 1; this step row's
-        const float la = p.A_polar[2 * h], th = p.A_polar[2 * h + 1];
-        const float ar = expf(la) * cosf(th), ai = expf(la) * sinf(th);
-        const float inv = 1.f / (ar * ar + ai * ai);            // 1 / |A|^2
-        const float Dh = p.D[h];
-        auto dt_raw_of = [&](int c) {
-            const long long l = (long long)c * kQ + i;
-            return (b < p.Bt && l < p.L) ? p.dt_raw[((size_t)b * p.L + l) * H + h] : 0.f;
-        };
-        float zr = (nch > 0 && hf == 0) ? dt_raw_of(0) : 0.f;
-        // state hf entering the item's first chunk (row n = t), loaded now: the loads
-        // overlap the chunk's tiles and factors
-        uint32_t hv[2][32];
-        {
-            const float *src = (p.h0 && b0 + hf < p.Bt) ? p.h0 + ((size_t)(b0 + hf) * H + h) * NP + t : nullptr;
-#pragma unroll
-            for (int kk = 0; kk < 64; ++kk)
-                hv[kk >> 5][kk & 31] = __float_as_uint(src ? __ldg(src + (size_t)kk * kN) : 0.f);
-        }
-        for (int c = 0; c < nch && ok; ++c, ++k) {
-            const uint32_t par = k & 1;
-            const long long l = (long long)c * kQ + i;
-            const bool valid = b < p.Bt && l < p.L;
-            // ---- dt, tau within the row's chunk (its two warps of half 0), the complex factors
-            float dt = 0.f, tau = 0.f;
-            if (hf == 0) {
-                dt = valid ? softplus_f32(zr + p.dt_bias[h]) : 0.f;
-                if (c + 1 < nch)
-                    zr = dt_raw_of(c + 1);   // in flight through this chunk
-                tau = dt;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, tau, o);
-                    if (lane >= o)
-                        tau += u;
-                }
-                if (lane == 31)
-                    red[q] = tau;
-            }
-            if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))))
-                break;
-            if (hf == 0) {
-                tau += (q & 1) ? red[q - 1] : 0.f;
-                const float tau_end = red[2 * rr] + red[2 * rr + 1];
-                // f = (e^{A dt} - 1) / A, with e^{A dt} - 1 = expm1(a_r dt) cos(a_i dt) - 2 sin^2(a_i dt / 2)
-                //     + i e^{a_r dt} sin(a_i dt)
-                float sd, cd;
-                sincosf(ai * dt, &sd, &cd);
-                const float sh = sinf(0.5f * ai * dt);
-                const float nr = expm1f(ar * dt) * cd - 2.f * sh * sh, ni = expf(ar * dt) * sd;
-                const float2 f = make_float2((nr * ar + ni * ai) * inv, (ni * ar - nr * ai) * inv);
-                const float2 lam = cexp_a(ar, ai, tau);                      // Lambda_t
-                const float2 gw = cmul(cexp_a(ar, ai, tau_end - tau), f);    // g_t
-                const float tau_e = __shfl_sync(0xffffffffu, tau, lane | 15);   // the end of this 16-step block
-                const float2 cf = cmul(cexp_a(ar, ai, tau_e - tau), f);      // column factor of M's blocks
-                tau_s[t] = tau;
-                fr_s[t] = f.x;
-                fi_s[t] = f.y;
-                cr_s[t] = cf.x;
-                ci_s[t] = cf.y;
-                lr_s[t] = lam.x;
-                li_s[t] = lam.y;
-                gr_s[t] = gw.x;
-                gi_s[t] = gw.y;
-            }
-            // (every row's entries are read by the other half and by the M build)
-            if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))) ||
-                !(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_FULL], par))))
-                break;
-            // ---- C^ (in place), C~, C_L from row t of C; B~ from row t of B (tile hf)
+            const int bp = (int)(u / H), h = (int)(u - (long long)bp * H);
+            const int b0 = 2 * bp, b = b0 + rr;      // batch rows b0, b0 + 1; this step row's
+            const float la = p.A_polar[2 * h], th = p.A_polar[2 * h + 1];
+            const float ar = expf(la) * cosf(th), ai = expf(la) * sinf(th);
+            const float inv = 1.f / (ar * ar + ai * ai);            // 1 / |A|^2
+            const float Dh = p.D[h];
+            auto dt_raw_of = [&](int c) {
+                const long long l = (long long)c * kQ + i;
+                return (b < p.Bt && l < p.L) ? p.dt_raw[((size_t)b * p.L + l) * H + h] : 0.f;
+            };
+            float zr = (nch > 0 && hf == 0) ? dt_raw_of(0) : 0.f;
+            // state hf entering the item's first chunk (row n = t), loaded now: the loads
+            // overlap the chunk's tiles and factors
+            uint32_t hv[2][32];
             {
-                const float2 lam = make_float2(lr_s[t], li_s[t]), gw = make_float2(gr_s[t], gi_s[t]);
-                uint8_t *c0 = tC + hf * kT16, *b1 = tB + hf * kT16;
-#pragma unroll 1
-                for (int ch = 0; ch < 8; ++ch) {
-                    float v[8], w1[8], w2[8], w3[8];
-                    ld8(c0, t, ch, v);
+                const float *src = (p.h0 && b0 + hf < p.Bt) ? p.h0 + ((size_t)(b0 + hf) * H + h) * NP + t : nullptr;
 #pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const float re = v[j], im = v[j + 1];
-                        w1[j] = im;                              // C~ = (C_i, C_r)
-                        w1[j + 1] = re;
-                        w2[j] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
-                        w2[j + 1] = -(lam.x * im + lam.y * re);
-                        w3[j] = re;                              // C^ = (C_r, -C_i)
-                        w3[j + 1] = -im;
+                for (int kk = 0; kk < 64; ++kk)
+                    hv[kk >> 5][kk & 31] = __float_as_uint(src ? __ldg(src + (size_t)kk * kN) : 0.f);
+            }
+            for (int c = 0; c < nch && ok; ++c, ++k) {
+                const uint32_t par = k & 1;
+                const long long l = (long long)c * kQ + i;
+                const bool valid = b < p.Bt && l < p.L;
+                // ---- dt, tau within the row's chunk (its two warps of half 0), the complex factors
+                float dt = 0.f, tau = 0.f;
+                if (hf == 0) {
+                    dt = valid ? softplus_f32(zr + p.dt_bias[h]) : 0.f;
+                    if (c + 1 < nch)
+                        zr = dt_raw_of(c + 1);   // in flight through this chunk
+                    tau = dt;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const float u = __shfl_up_sync(0xffffffffu, tau, o);
+                        if (lane >= o)
+                            tau += u;
                     }
-                    st8(tCT + hf * kT16, t, ch, w1);
-                    st8(tCL + hf * kT16, t, ch, w2);
-                    st8(c0, t, ch, w3);
-                    ld8(b1, t, ch, v);
-#pragma unroll
-                    for (int j = 0; j < 8; j += 2) {
-                        const float re = v[j], im = v[j + 1];
-                        w1[j] = gw.x * re - gw.y * im;           // B~ = g B
-                        w1[j + 1] = gw.x * im + gw.y * re;
-                    }
-                    st8(tBT + hf * kT16, t, ch, w1);
+                    if (lane == 31)
+                        red[q] = tau;
                 }
-            }
-            // ---- state hf (row n = t): its bf16 copy for C_L H, then rotated by Lambda_63
-            //      of its batch row (lanes 2k, 2k+1 hold a component's re, im)
-            {
-                if (c > 0) {
-                    tmem_ld32(trow + kColH + 64 * hf, hv[0]);
-                    tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
-                    tmem_wait_ld();
+                if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))))
+                    break;
+                if (hf == 0) {
+                    tau += (q & 1) ? red[q - 1] : 0.f;
+                    const float tau_end = red[2 * rr] + red[2 * rr + 1];
+                    // f = (e^{A dt} - 1) / A, with e^{A dt} - 1 = expm1(a_r dt) cos(a_i dt) - 2 sin^2(a_i dt / 2)
+                    //     + i e^{a_r dt} sin(a_i dt)
+                    float sd, cd;
+                    sincosf(ai * dt, &sd, &cd);
+                    const float sh = sinf(0.5f * ai * dt);
+                    const float nr = expm1f(ar * dt) * cd - 2.f * sh * sh, ni = expf(ar * dt) * sd;
+                    const float2 f = make_float2((nr * ar + ni * ai) * inv, (ni * ar - nr * ai) * inv);
+                    const float2 lam = cexp_a(ar, ai, tau);                      // Lambda_t
+                    const float2 gw = cmul(cexp_a(ar, ai, tau_end - tau), f);    // g_t
+                    const float tau_e = __shfl_sync(0xffffffffu, tau, lane | 15);   // the end of this 16-step block
+                    const float2 cf = cmul(cexp_a(ar, ai, tau_e - tau), f);      // column factor of M's blocks
+                    tau_s[t] = tau;
+                    fr_s[t] = f.x;
+                    fi_s[t] = f.y;
+                    cr_s[t] = cf.x;
+                    ci_s[t] = cf.y;
+                    lr_s[t] = lam.x;
+                    li_s[t] = lam.y;
+                    gr_s[t] = gw.x;
+                    gi_s[t] = gw.y;
                 }
-#pragma unroll
-                for (int cc = 0; cc < 8; ++cc) {
-                    float w[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        w[e] = __uint_as_float(hv[cc >> 2][8 * (cc & 3) + e]);
-                    st8(tHB + hf * kT16, t, cc, w);
-                }
-                const float te = red[2 * hf] + red[2 * hf + 1];   // tau at the end of row hf's chunk
-                const float2 z = cexp_a(ar, ai, te);
-                const bool odd = lane & 1;
-#pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    const float mine = __uint_as_float(hv[j >> 5][j & 31]);
-                    const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
-                    // even lane: re' = z_r re - z_i im; odd lane: im' = z_r im + z_i re
-                    const float out = odd ? fmaf(z.x, mine, z.y * other) : fmaf(z.x, mine, -z.y * other);
-                    hv[j >> 5][j & 31] = __float_as_uint(out);
-                }
-                tmem_st32(trow + kColH + 64 * hf, hv[0]);
-                tmem_st32(trow + kColH + 64 * hf + 32, hv[1]);
-            }
-            tmem_wait_st();
-            fence_proxy_async_smem();
-            tc_fence_before();
-            warp_arrive(&bars[BAR_ROWS_A]);
-            // ---- M from S_re, S_im in place (row t; the blocks of 16 steps of parity hf)
-            if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_S], par))))
-                break;
-            tc_fence_after();
-            {
-                const int gdiag = t >> 4;   // the block holding step t (2q or 2q + 1 within the warp)
-                const float tau_t = tau_s[t];   // (computed by half 0)
+                // (every row's entries are read by the other half and by the M build)
+                if (!(ok = __all_sync(0xffffffffu, rsync(&bars[BAR_RSYNC], rphase))) ||
+                    !(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_FULL], par))))
+                    break;
+                // ---- C^ (in place), C~, C_L from row t of C; B~ from row t of B (tile hf)
+                {
+                    const float2 lam = make_float2(lr_s[t], li_s[t]), gw = make_float2(gr_s[t], gi_s[t]);
+                    uint8_t *c0 = tC + hf * kT16, *b1 = tB + hf * kT16;
 #pragma unroll 1
-                for (int G = hf; G < 8; G += 2) {
-                    uint32_t m[8];
-                    // warp-uniform: some row of this warp reaches block G (the TMEM loads are
-                    // collective); each lane then takes its own case
-                    if ((G >> 2) != rr || G > 2 * q + 1) {
+                    for (int ch = 0; ch < 8; ++ch) {
+                        float v[8], w1[8], w2[8], w3[8];
+                        ld8(c0, t, ch, v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            m[e] = 0u;
-                    } else {
-                        uint32_t sr[16], si[16];
-                        tmem_ld16(trow + kColS + 16 * G, sr);
-                        tmem_ld16(trow + kColSI + 16 * G, si);
-                        const int s0 = 16 * G, se = s0 + 15;
-                        // e^{A (tau_t - tau_e)}: at most 1 in modulus below the diagonal block and
-                        // at most e^{|a_r| span} on it; the factored form there while that stays
-                        // far inside fp32 (the span test is the same for the whole block)
-                        const bool factored = G < gdiag || fabsf(ar) * (tau_s[se] - tau_s[s0]) < 60.f;
-                        const float2 rf = cexp_a(ar, ai, tau_t - tau_s[se]);
-                        tmem_wait_ld();
-                        float mv[16];
-                        if (G > gdiag) {    // above this row's diagonal
-#pragma unroll
-                            for (int e = 0; e < 16; ++e)
-                                mv[e] = 0.f;
-                        } else if (factored) {
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int s = s0 + e;
-                                const float2 E = cmul(rf, make_float2(cr_s[s], ci_s[s]));
-                                const float v = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
-                                mv[e] = s <= t ? v : 0.f;
-                            }
-                        } else {            // the diagonal block, directly: e^{A (tau_t - tau_s)} f_s, s <= t
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const int s = s0 + e;
-                                float val = 0.f;
-                                if (s <= t) {
-                                    const float2 E = cmul(cexp_a(ar, ai, tau_t - tau_s[s]), make_float2(fr_s[s], fi_s[s]));
-                                    val = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
-                                }
-                                mv[e] = val;
-                            }
+                        for (int j = 0; j < 8; j += 2) {
+                            const float re = v[j], im = v[j + 1];
+                            w1[j] = im;                              // C~ = (C_i, C_r)
+                            w1[j + 1] = re;
+                            w2[j] = lam.x * re - lam.y * im;         // C_L = (Re(Lambda C), -Im(Lambda C))
+                            w2[j + 1] = -(lam.x * im + lam.y * re);
+                            w3[j] = re;                              // C^ = (C_r, -C_i)
+                            w3[j + 1] = -im;
                         }
+                        st8(tCT + hf * kT16, t, ch, w1);
+                        st8(tCL + hf * kT16, t, ch, w2);
+                        st8(c0, t, ch, w3);
+                        ld8(b1, t, ch, v);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
-                    }
-                    tmem_st8(trow + kColS + 16 * G, m);
-                }
-            }
-            tmem_wait_st();
-            tc_fence_before();
-            warp_arrive(&bars[BAR_ROWS_M]);
-            // ---- y = M x + C_L H_r + D x (row t, columns 32 hf ..), by a tensor store per warp
-            if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_Y], par))))
-                break;
-            tc_fence_after();
-            {
-                uint8_t *stg = tCT + warp * 2048;   // this warp's box: 32 rows x 32 bf16, plain (C~ is dead)
-#pragma unroll 1
-                for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
-                    uint32_t ym[16], yo[16];
-                    tmem_ld16(trow + kColY + 16 * g16, ym);
-                    tmem_ld16(trow + (rr ? kColSI : kColYO0) + 16 * g16, yo);
-                    tmem_wait_ld();
-                    float xv[8], o[8];
-#pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
-                        ld8(tX, t, 2 * g16 + hh, xv);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            o[e] = fmaf(Dh, xv[e], __uint_as_float(ym[8 * hh + e]) + __uint_as_float(yo[8 * hh + e]));
-                        *reinterpret_cast<uint4 *>(stg + lane * 64 + 16 * (2 * (g16 & 1) + hh)) =
-                            make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
-                                       pack_bf16x2(o[6], o[7]));
+                        for (int j = 0; j < 8; j += 2) {
+                            const float re = v[j], im = v[j + 1];
+                            w1[j] = gw.x * re - gw.y * im;           // B~ = g B
+                            w1[j + 1] = gw.x * im + gw.y * re;
+                        }
+                        st8(tBT + hf * kT16, t, ch, w1);
                     }
                 }
+                // ---- state hf (row n = t): its bf16 copy for C_L H, then rotated by Lambda_63
+                //      of its batch row (lanes 2k, 2k+1 hold a component's re, im)
+                {
+                    if (c > 0) {
+                        tmem_ld32(trow + kColH + 64 * hf, hv[0]);
+                        tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
+                        tmem_wait_ld();
+                    }
+#pragma unroll
+                    for (int cc = 0; cc < 8; ++cc) {
+                        float w[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            w[e] = __uint_as_float(hv[cc >> 2][8 * (cc & 3) + e]);
+                        st8(tHB + hf * kT16, t, cc, w);
+                    }
+                    const float te = red[2 * hf] + red[2 * hf + 1];   // tau at the end of row hf's chunk
+                    const float2 z = cexp_a(ar, ai, te);
+                    const bool odd = lane & 1;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        const float mine = __uint_as_float(hv[j >> 5][j & 31]);
+                        const float other = __shfl_xor_sync(0xffffffffu, mine, 1);
+                        // even lane: re' = z_r re - z_i im; odd lane: im' = z_r im + z_i re
+                        const float out = odd ? fmaf(z.x, mine, z.y * other) : fmaf(z.x, mine, -z.y * other);
+                        hv[j >> 5][j & 31] = __float_as_uint(out);
+                    }
+                    tmem_st32(trow + kColH + 64 * hf, hv[0]);
+                    tmem_st32(trow + kColH + 64 * hf + 32, hv[1]);
+                }
+                tmem_wait_st();
                 fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    const long long r0 = (long long)c * kQ + 32 * (q & 1);
-                    if (b < p.Bt && r0 < p.L)
-                        tma_store_3d(&maps.y, stg, h * kP + 32 * hf, (int)r0, b);
-                    bulk_commit_group();
-                    bulk_wait_read_all();   // the box is rewritten next chunk
-                }
-            }
-            warp_arrive(&bars[BAR_EPI]);
-        }
-        // ---- the item's final state hf (row n = t), [P][N]
-        if (ok && p.h_final && b0 + hf < p.Bt) {
-            tmem_ld32(trow + kColH + 64 * hf, hv[0]);
-            tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
-            tmem_wait_ld();
-            float *dst = p.h_final + ((size_t)(b0 + hf) * H + h) * NP + t;
+                tc_fence_before();
+                warp_arrive(&bars[BAR_ROWS_A]);
+                // ---- M from S_re, S_im in place (row t; the blocks of 16 steps of parity hf)
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_S], par))))
+                    break;
+                tc_fence_after();
+                {
+                    const int gdiag = t >> 4;   // the block holding step t (2q or 2q + 1 within the warp)
+                    const float tau_t = tau_s[t];   // (computed by half 0)
+#pragma unroll 1
+                    for (int G = hf; G < 8; G += 2) {
+                        uint32_t m[8];
+                        // warp-uniform: some row of this warp reaches block G (the TMEM loads are
+                        // collective); each lane then takes its own case
+                        if ((G >> 2) != rr || G > 2 * q + 1) {
 #pragma unroll
-            for (int kk = 0; kk < 64; ++kk)
-                dst[(size_t)kk * kN] = __uint_as_float(hv[kk >> 5][kk & 31]);
-        }
+                            for (int e = 0; e < 8; ++e)
+                                m[e] = 0u;
+                        } else {
+                            uint32_t sr[16], si[16];
+                            tmem_ld16(trow + kColS + 16 * G, sr);
+                            tmem_ld16(trow + kColSI + 16 * G, si);
+                            const int s0 = 16 * G, se = s0 + 15;
+                            // e^{A (tau_t - tau_e)}: at most 1 in modulus below the diagonal block and
+                            // at most e^{|a_r| span} on it; the factored form there while that stays
+                            // far inside fp32 (the span test is the same for the whole block)
+                            const bool factored = G < gdiag || fabsf(ar) * (tau_s[se] - tau_s[s0]) < 60.f;
+                            const float2 rf = cexp_a(ar, ai, tau_t - tau_s[se]);
+                            tmem_wait_ld();
+                            float mv[16];
+                            if (G > gdiag) {    // above this row's diagonal
+#pragma unroll
+                                for (int e = 0; e < 16; ++e)
+                                    mv[e] = 0.f;
+                            } else if (factored) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    const int s = s0 + e;
+                                    const float2 E = cmul(rf, make_float2(cr_s[s], ci_s[s]));
+                                    const float v = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
+                                    mv[e] = s <= t ? v : 0.f;
+                                }
+                            } else {            // the diagonal block, directly: e^{A (tau_t - tau_s)} f_s, s <= t
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) {
+                                    const int s = s0 + e;
+                                    float val = 0.f;
+                                    if (s <= t) {
+                                        const float2 E = cmul(cexp_a(ar, ai, tau_t - tau_s[s]), make_float2(fr_s[s], fi_s[s]));
+                                        val = E.x * __uint_as_float(sr[e]) - E.y * __uint_as_float(si[e]);
+                                    }
+                                    mv[e] = val;
+                                }
+                            }
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                m[e] = pack_bf16x2(mv[2 * e], mv[2 * e + 1]);
+                        }
+                        tmem_st8(trow + kColS + 16 * G, m);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                warp_arrive(&bars[BAR_ROWS_M]);
+                // ---- y = M x + C_L H_r + D x (row t, columns 32 hf ..), by a tensor store per warp
+                if (!(ok = __all_sync(0xffffffffu, wait_bar(&bars[BAR_MMA_Y], par))))
+                    break;
+                tc_fence_after();
+                {
+                    uint8_t *stg = tCT + warp * 2048;   // this warp's box: 32 rows x 32 bf16, plain (C~ is dead)
+#pragma unroll 1
+                    for (int g16 = 2 * hf; g16 < 2 * hf + 2; ++g16) {
+                        uint32_t ym[16], yo[16];
+                        tmem_ld16(trow + kColY + 16 * g16, ym);
+                        tmem_ld16(trow + (rr ? kColSI : kColYO0) + 16 * g16, yo);
+                        tmem_wait_ld();
+                        float xv[8], o[8];
+#pragma unroll
+                        for (int hh = 0; hh < 2; ++hh) {
+                            ld8(tX, t, 2 * g16 + hh, xv);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                o[e] = fmaf(Dh, xv[e], __uint_as_float(ym[8 * hh + e]) + __uint_as_float(yo[8 * hh + e]));
+                            *reinterpret_cast<uint4 *>(stg + lane * 64 + 16 * (2 * (g16 & 1) + hh)) =
+                                make_uint4(pack_bf16x2(o[0], o[1]), pack_bf16x2(o[2], o[3]), pack_bf16x2(o[4], o[5]),
+                                           pack_bf16x2(o[6], o[7]));
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        const long long r0 = (long long)c * kQ + 32 * (q & 1);
+                        if (b < p.Bt && r0 < p.L)
+                            tma_store_3d(&maps.y, stg, h * kP + 32 * hf, (int)r0, b);
+                        bulk_commit_group();
+                        bulk_wait_read_all();   // the box is rewritten next chunk
+                    }
+                }
+                warp_arrive(&bars[BAR_EPI]);
+            }
+            // ---- the item's final state hf (row n = t), [P][N]
+            if (ok && p.h_final && b0 + hf < p.Bt) {
+                tmem_ld32(trow + kColH + 64 * hf, hv[0]);
+                tmem_ld32(trow + kColH + 64 * hf + 32, hv[1]);
+                tmem_wait_ld();
+                float *dst = p.h_final + ((size_t)(b0 + hf) * H + h) * NP + t;
+#pragma unroll
+                for (int kk = 0; kk < 64; ++kk)
+                    dst[(size_t)kk * kN] = __uint_as_float(hv[kk >> 5][kk & 31]);
+            }
         }
         if (lane == 0)
             bulk_wait_all();
