@@ -49,6 +49,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "ptx.cuh"
@@ -89,7 +90,7 @@ constexpr uint32_t kOffRed = kOffArr + A_NUM * kR * 4;   // 64 floats: per-warp 
 constexpr uint32_t kOffBars = kOffRed + 64 * 4;
 enum {
     BAR_FULL = 0, BAR_ROWS0, BAR_MMA1, BAR_ROWS1, BAR_MMA2, BAR_ROWS2A, BAR_MMA2B, BAR_ROWS2, BAR_MMA3, BAR_ROWS3,
-    BAR_MMA4, BAR_ROWS4A, BAR_MMA4B, BAR_DRAIN, BAR_RSYNC, kNumBars
+    BAR_MMA4, BAR_ROWS4A, BAR_MMA4B, BAR_DRAIN, BAR_RSYNC, BAR_DONE, kNumBars
 };
 constexpr uint32_t kOffHolder = kOffBars + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kOffHolder + 16 + 1024;
@@ -108,6 +109,7 @@ struct TcParams {
     float *dx, *ddt_raw, *dB_head, *dC_head, *part;
     long long L;
     int H, G, nc;
+    long long BH;                // batch rows x heads
 };
 
 struct TcMaps {
@@ -244,18 +246,33 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int H = p.H, nc = p.nc;
-    const long long bh = blockIdx.y, b = bh / H;
-    const int h = (int)(bh - b * H), g = h / (H / p.G);
-    const int c0 = 2 * (int)blockIdx.x;                  // first chunk of the pair
-    const long long t0 = (long long)c0 * kCq;
-    const int nq = (int)min((long long)kR, p.L - t0);    // valid rows of the pair
-    const float a = -expf(p.A_log[h]);
     const size_t NP = (size_t)kN * kP;
+    // work items: a pair of chunks of one (b, h), u = bh * npairs + pair; CTA i takes
+    // items i, i + grid, ... (one persistent CTA per SM)
+    const int npairs = (nc + 1) / 2;
+    const long long nitems = (long long)npairs * p.BH;
+    struct Item {
+        long long bh, b, t0;
+        int h, g, c0, nq;   // head, group, first chunk of the pair, valid rows of the pair
+        float a;
+    };
+    auto item = [&](long long u) {
+        Item it;
+        it.bh = u / npairs;
+        it.c0 = 2 * (int)(u - it.bh * npairs);
+        it.b = it.bh / H;
+        it.h = (int)(it.bh - it.b * H);
+        it.g = it.h / (H / p.G);
+        it.t0 = (long long)it.c0 * kCq;
+        it.nq = (int)min((long long)kR, p.L - it.t0);
+        it.a = -expf(p.A_log[it.h]);
+        return it;
+    };
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i)
             mbar_init(&bars[i], (i == BAR_ROWS0 || i == BAR_ROWS1 || i == BAR_ROWS2A || i == BAR_ROWS2 ||
-                                 i == BAR_ROWS3 || i == BAR_ROWS4A || i == BAR_RSYNC)
+                                 i == BAR_ROWS3 || i == BAR_ROWS4A || i == BAR_RSYNC || i == BAR_DONE)
                                     ? kRowWarps
                                     : 1);
         fence_mbar_init();
@@ -272,30 +289,43 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
 
     if (warp == kIssueWarp) {
         if (lane == 0) {
-            // the state blocks this CTA reads (G_out and h_in of both chunks, and the
-            // state after the pair) into L2 now: the row warps stage them in several passes
-            for (int kk = 0; kk < 2; ++kk)
-                if (c0 + kk < nc) {
-                    const float *blocks[2] = {p.R + ((size_t)bh * nc + c0 + kk) * NP,
-                                              p.S + ((size_t)bh * (nc + 1) + c0 + kk) * NP};
-                    for (const float *blk : blocks)
-                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(blk), "r"((uint32_t)(NP * 4))
-                                     : "memory");
-                }
-            {
-                const int cl = min(c0 + 2, nc);   // h_last of the pair's last chunk
-                const float *blk = p.S + ((size_t)bh * (nc + 1) + cl) * NP;
+            // the state blocks an item reads (G_out and h_in of both chunks, and the
+            // state after the pair: the row warps stage them in several passes) and its
+            // tiles into L2, one item ahead
+            auto prefetch_item = [&](long long u) {
+                if (u >= nitems)
+                    return;
+                const Item it = item(u);
+                for (int kk = 0; kk < 2; ++kk)
+                    if (it.c0 + kk < nc) {
+                        const float *blocks[2] = {p.R + ((size_t)it.bh * nc + it.c0 + kk) * NP,
+                                                  p.S + ((size_t)it.bh * (nc + 1) + it.c0 + kk) * NP};
+                        for (const float *blk : blocks)
+                            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(blk),
+                                         "r"((uint32_t)(NP * 4))
+                                         : "memory");
+                    }
+                const float *blk = p.S + ((size_t)it.bh * (nc + 1) + min(it.c0 + 2, nc)) * NP;
                 asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(blk), "r"((uint32_t)(NP * 4)) : "memory");
-            }
+                tma_prefetch_3d(&maps.C, it.g * kN, (int)it.t0, (int)it.b);
+                tma_prefetch_3d(&maps.C, it.g * kN + 64, (int)it.t0, (int)it.b);
+                tma_prefetch_3d(&maps.B, it.g * kN, (int)it.t0, (int)it.b);
+                tma_prefetch_3d(&maps.B, it.g * kN + 64, (int)it.t0, (int)it.b);
+                tma_prefetch_3d(&maps.x, it.h * kP, (int)it.t0, (int)it.b);
+                tma_prefetch_3d(&maps.dy, it.h * kP, (int)it.t0, (int)it.b);
+            };
             // ---- TMA: C, B (two 64-column tiles each), x, dy
             const uint64_t pol = policy_evict_first();
-            mbar_arrive_expect_tx(&bars[BAR_FULL], 6 * kT16);
-            tma_load_3d(smem + kOffC, &maps.C, &bars[BAR_FULL], g * kN, (int)t0, (int)b, pol);
-            tma_load_3d(smem + kOffC + kT16, &maps.C, &bars[BAR_FULL], g * kN + 64, (int)t0, (int)b, pol);
-            tma_load_3d(smem + kOffB, &maps.B, &bars[BAR_FULL], g * kN, (int)t0, (int)b, pol);
-            tma_load_3d(smem + kOffB + kT16, &maps.B, &bars[BAR_FULL], g * kN + 64, (int)t0, (int)b, pol);
-            tma_load_3d(smem + kOffX, &maps.x, &bars[BAR_FULL], h * kP, (int)t0, (int)b, pol);
-            tma_load_3d(smem + kOffDY, &maps.dy, &bars[BAR_FULL], h * kP, (int)t0, (int)b, pol);
+            auto load_tiles = [&](const Item &it) {
+                mbar_arrive_expect_tx(&bars[BAR_FULL], 6 * kT16);
+                tma_load_3d(smem + kOffC, &maps.C, &bars[BAR_FULL], it.g * kN, (int)it.t0, (int)it.b, pol);
+                tma_load_3d(smem + kOffC + kT16, &maps.C, &bars[BAR_FULL], it.g * kN + 64, (int)it.t0, (int)it.b, pol);
+                tma_load_3d(smem + kOffB, &maps.B, &bars[BAR_FULL], it.g * kN, (int)it.t0, (int)it.b, pol);
+                tma_load_3d(smem + kOffB + kT16, &maps.B, &bars[BAR_FULL], it.g * kN + 64, (int)it.t0, (int)it.b, pol);
+                tma_load_3d(smem + kOffX, &maps.x, &bars[BAR_FULL], it.h * kP, (int)it.t0, (int)it.b, pol);
+                tma_load_3d(smem + kOffDY, &maps.dy, &bars[BAR_FULL], it.h * kP, (int)it.t0, (int)it.b, pol);
+            };
+            uint32_t armed = 0;
             const uint32_t sC = smem_u32(smem + kOffC), sB = smem_u32(smem + kOffB), sX = smem_u32(smem + kOffX);
             const uint32_t sDY = smem_u32(smem + kOffDY), sG = smem_u32(smem + kOffG);
             const uint32_t sMT = smem_u32(smem + kOffMT), sA2 = smem_u32(smem + kOffA2);
@@ -306,9 +336,18 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             const uint32_t i128kk = idesc_bf16_f32(128, 128, 0, 0), i64kn = idesc_bf16_f32(128, 64, 0, 1);
             const uint32_t i64nn = idesc_bf16_f32(128, 64, 1, 1), i128nn = idesc_bf16_f32(128, 128, 1, 1);
             const uint32_t i128kn = idesc_bf16_f32(128, 128, 0, 1);
+            uint32_t ik = 0;   // items so far (the barriers' phases)
+            for (long long u = blockIdx.x; u < nitems && ok; u += gridDim.x, ++ik) {
+            const uint32_t par = ik & 1;
+            // the tiles, once the row warps are done with the previous item's
+            if (ik > 0 && !(ok = wait_bar(&bars[BAR_DONE], par ^ 1u)))
+                break;
+            prefetch_item(u);   // this item's states, staged in several passes
+            load_tiles(item(u));
+            ++armed;
             do {
                 // ---- MMA 1: CB = C B^T, DX = dy x^T
-                if (!(ok = wait_bar(&bars[BAR_FULL], 0)) || !(ok = wait_bar(&bars[BAR_ROWS0], 0)))
+                if (!(ok = wait_bar(&bars[BAR_FULL], par)) || !(ok = wait_bar(&bars[BAR_ROWS0], par)))
                     break;
                 tc_fence_after();
                 for (int kk = 0; kk < 8; ++kk)
@@ -318,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 mma_commit(&bars[BAR_MMA1]);
                 // ---- MMA 2: Mt^T dy; B G_out and x G_out^T, G_out's hi terms (each chunk's
                 //      state over all rows)
-                if (!(ok = wait_bar(&bars[BAR_ROWS1], 0)))
+                if (!(ok = wait_bar(&bars[BAR_ROWS1], par)))
                     break;
                 tc_fence_after();
                 for (int kk = 0; kk < 8; ++kk)
@@ -334,13 +373,13 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                 issue_state_g(false);
                 mma_commit(&bars[BAR_MMA2]);
                 // ---- MMA 2b: G_out's lo terms, into the same accumulators
-                if (!(ok = wait_bar(&bars[BAR_ROWS2A], 0)))
+                if (!(ok = wait_bar(&bars[BAR_ROWS2A], par)))
                     break;
                 tc_fence_after();
                 issue_state_g(true);
                 mma_commit(&bars[BAR_MMA2B]);
                 // ---- MMA 3: A2^T C, A2 (dt o B)
-                if (!(ok = wait_bar(&bars[BAR_ROWS2], 0)))
+                if (!(ok = wait_bar(&bars[BAR_ROWS2], par)))
                     break;
                 tc_fence_after();
                 for (int kk = 0; kk < 8; ++kk)
@@ -356,25 +395,28 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
                             mma_ss(tmem + kColDYH + 128 * k, kmaj(sDY, kk), kmaj(sMT + k * kT16, kk), i128kk,
                                    acc || kk > 0);
                 };
-                if (!(ok = wait_bar(&bars[BAR_ROWS3], 0)))
+                if (!(ok = wait_bar(&bars[BAR_ROWS3], par)))
                     break;
                 tc_fence_after();
                 issue_state_h(false);
                 mma_commit(&bars[BAR_MMA4]);
-                if (!(ok = wait_bar(&bars[BAR_ROWS4A], 0)))
+                if (!(ok = wait_bar(&bars[BAR_ROWS4A], par)))
                     break;
                 tc_fence_after();
                 issue_state_h(true);
                 mma_commit(&bars[BAR_MMA4B]);
             } while (false);
+            }
             // no MMA may be in flight when tensor memory is released, nor a TMA load
             // when the CTA exits
             mma_commit(&bars[BAR_DRAIN]);
             const uint64_t tw = globaltimer_ns();
             while (!mbar_wait_for(&bars[BAR_DRAIN], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
             }
-            while (!mbar_wait_for(&bars[BAR_FULL], 0, 1000000u) && globaltimer_ns() - tw < kTimeoutNs) {
-            }
+            if (armed > 0)
+                while (!mbar_wait_for(&bars[BAR_FULL], (armed - 1) & 1, 1000000u) &&
+                       globaltimer_ns() - tw < kTimeoutNs) {
+                }
         }
     } else {
         // ------------------------------------------------------------ rows
@@ -382,13 +424,23 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
         const int hf = warp >> 2;               // column half
         const int r = 32 * q + lane;            // this thread's row: step t0 + r
         const int k = r >> 6;                   // its chunk (0, 1)
-        const int c = c0 + k;
-        const bool cvalid = c < nc;
         const uint32_t lane_addr = static_cast<uint32_t>(32 * q) << 16;
         const uint32_t trow = tmem + lane_addr;
         uint8_t *tC = smem + kOffC, *tB = smem + kOffB, *tX = smem + kOffX, *tDY = smem + kOffDY;
         uint8_t *tG = smem + kOffG, *tMT = smem + kOffMT, *tA2 = smem + kOffA2;
-        uint32_t rphase = 0;
+        uint32_t rphase = 0, ik = 0;   // (ik: items so far, the barriers' phases)
+        for (long long u = blockIdx.x; u < nitems && ok; u += gridDim.x, ++ik) {
+        const uint32_t par = ik & 1;
+        const Item it = item(u);
+        const long long bh = it.bh, b = it.b, t0 = it.t0;
+        const int h = it.h, c0 = it.c0, nq = it.nq;
+        const float a = it.a;
+        const int c = c0 + k;
+        const bool cvalid = c < nc;
+        // every warp's stores of the previous item have read their staging boxes
+        // (G_out's, x's, dy's, B's and A2's tiles), which this item refills
+        if (ik > 0 && !(ok = wait_bar(&bars[BAR_DONE], par ^ 1u)))
+            break;
         // G_out of chunk c0 + kk, the state entering it and the state after it;
         // null past the sequence's chunks
         auto gout = [&](int kk) -> const float * {
@@ -437,7 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS0]);
             // chunk cumsums: the second warp of each chunk adds the first's total
-            if (!(ok = wait_bar(&bars[BAR_FULL], 0)))
+            if (!(ok = wait_bar(&bars[BAR_FULL], par)))
                 break;
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
@@ -469,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             const float cs_last = cs_s[64 * k + 63];
             const float dt_r = dt_s[r];
             // ---- rows 1: Mt, A2 from CB, DX (this half of this row's chunk block), W's sums
-            if (!(ok = wait_bar(&bars[BAR_MMA1], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA1], par)))
                 break;
             tc_fence_after();
             {
@@ -530,7 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS1]);
             // ---- rows 2a: G_out's lo terms (row n = r) into its tiles, once MMA 2 has read the hi
-            if (!(ok = wait_bar(&bars[BAR_MMA2], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA2], par)))
                 break;
             {
                 float unused[2];
@@ -539,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS2A]);
             // ---- rows 2: dx_j = D dy_j + dt_j (in + eo out); dt o B in place; h_in's hi terms
-            if (!(ok = wait_bar(&bars[BAR_MMA2B], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA2B], par)))
                 break;
             tc_fence_after();
             {
@@ -611,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS2]);
             // ---- rows 3: dB_j = dt_j (in + eo out)
-            if (!(ok = wait_bar(&bars[BAR_MMA3], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA3], par)))
                 break;
             tc_fence_after();
             {
@@ -645,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             tc_fence_before();
             warp_arrive(&bars[BAR_ROWS3]);
             // ---- rows 4a: h_in's lo terms into Mt's space, once MMA 4 has read the hi
-            if (!(ok = wait_bar(&bars[BAR_MMA4], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA4], par)))
                 break;
             {
                 float unused[2];
@@ -654,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             fence_proxy_async_smem();
             warp_arrive(&bars[BAR_ROWS4A]);
             // ---- rows 4: dC_s = in + e^{cs_s} out, u_s = C_s . e^{cs_s} out
-            if (!(ok = wait_bar(&bars[BAR_MMA4B], 0)))
+            if (!(ok = wait_bar(&bars[BAR_MMA4B], par)))
                 break;
             tc_fence_after();
             {
@@ -755,12 +807,17 @@ __global__ void __launch_bounds__(kThreads, 1) ssd_bwd_tc_grad_kernel(const __gr
             if (!(ok = rsync(&bars[BAR_RSYNC], rphase)))
                 break;
             if (lane == 0 && hf == 0 && (q & 1) == 0 && cvalid) {
-                const size_t BHC = (size_t)gridDim.y * nc, i = (size_t)bh * nc + c;
+                const size_t BHC = (size_t)p.BH * nc, i = (size_t)bh * nc + c;
                 p.part[i] = a * (red[24 + q] + red[24 + q + 1]);
                 p.part[BHC + i] = red[28 + q] + red[28 + q + 1];
                 p.part[2 * BHC + i] = (red[16 + q] + red[16 + q + 1]) + (red[20 + q] + red[20 + q + 1]);
             }
         } while (false);
+        // the item's staging boxes read by their stores, before the next item refills them
+        if (lane == 0)
+            bulk_wait_read_all();
+        warp_arrive(&bars[BAR_DONE]);
+        }
         if (lane == 0)
             bulk_wait_all();   // every store of this warp done before the CTA exits
     }
@@ -1251,11 +1308,17 @@ cudaError_t bwd_tc_grad_launch(const BwdTcArgs &a, cudaStream_t st)
     p.H = a.nheads;
     p.G = a.ngroups;
     p.nc = a.nc;
+    p.BH = (long long)a.batch * a.nheads;
     const cudaError_t e =
         cudaFuncSetAttribute(ssd_bwd_tc_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess)
         return e;
-    const dim3 grid((unsigned)((a.nc + 1) / 2), (unsigned)(a.batch * a.nheads));
+    // persistent: one CTA per SM (its shared memory and TMEM), each walking items
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cudaErrorInvalidValue;
+    const long long nitems = (long long)((a.nc + 1) / 2) * p.BH;
+    const dim3 grid((unsigned)std::min<long long>(nitems, sms));
     ssd_bwd_tc_grad_kernel<<<grid, kThreads, kSmemBytes, st>>>(maps, p);
     return cudaGetLastError();
 }
