@@ -26,12 +26,15 @@
 // theirs, its x once the previous epilogue has, and an item's entering states
 // are prefetched into L2 an item ahead.  E is zero across the two rows, so M is
 // block diagonal; the products with a row's state are issued once per state
-// over all 128 rows, and each row keeps its own one.  M below the diagonal
-// blocks is factored per 16-step block (ending at step e) as
-// e^{A (tau_t - tau_e)} . e^{A (tau_e - tau_s)} f_s, both factors of modulus at
-// most 1 for decaying modes; the diagonal blocks take e^{A (tau_t - tau_s)} f_s
-// directly.  M, C_L, B~ and H enter as single bf16 operands, as the real
-// chunked scan rounds its M, its state copy and its scaled inputs.
+// over all 128 rows, and each row keeps its own one.  M is factored per 16-step
+// block (ending at step e) as e^{A (tau_t - tau_e)} . e^{A (tau_e - tau_s)} f_s:
+// below a row's diagonal block both factors have modulus at most 1 for decaying
+// modes; on it the row factor is at most e^{|a_r| span}, so the factored form
+// (masked to s <= t) is taken while that stays far inside fp32, and
+// e^{A (tau_t - tau_s)} f_s per element otherwise.  M, C_L, B~ and H enter as
+// single bf16 operands, as the real chunked scan rounds its M, its state copy
+// and its scaled inputs.  Eight row warps: the two warps of a TMEM lane quarter
+// split the tile columns, M's blocks, the two states and the y columns.
 //
 // Phases per chunk, one mbarrier hand-off each (all waits bounded):
 //   TMA: C, B, x of both rows.    rows: dt, tau and the complex factors; C^, C~,
