@@ -1019,16 +1019,15 @@ def run_gpu_neighbor(args, w: Workload):
             "algorithmic_tensor_flops_per_launch": 0, "avg_launch_ms": avg_launch_s * 1e3,
             "roofline_ms": alg_bytes / (hbm_peak * 1e9) * 1e3}
     if w.op == "bwd" and w.headdim <= 64 and w.dstate <= 128:
-        # the chunk-form backward, whole call (5 launches) timed.  Its contractions
-        # run on the tensor cores for bf16 with P = 64, N = 128 (the chunk states
-        # and the gradient pass), else as fp32 FFMA: the roofline is that pipe.
+        # the chunk-form backward, whole call timed.  Its contractions run on the
+        # tensor cores for bf16 with P = 64, N = 128 (the chunk states and the
+        # gradient pass), else as fp32 FFMA: the roofline is that pipe.
         flops = bwd_chunk_flops(w)
         tf = flops / avg_launch_s / 1e12
         if w.dtype == "bf16" and w.headdim == 64 and w.dstate == 128:
             tc_peak = float(peaks["bf16_tflops"])
-            roof = {"bound": "tensor", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_tc_local_kernel, "
-                                                  "ssd_bwd_pass_kernel, ssd_bwd_tc_grad_kernel, "
-                                                  "ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
+            roof = {"bound": "tensor", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_tc_chain_kernel, "
+                                                  "ssd_bwd_tc_grad_kernel, ssd_bwd_finish4_kernel)",
                     "achieved": tf, "peak": tc_peak, "unit": "TFLOP/s", "frac": tf / tc_peak,
                     "peak_source": peak_src + " (bf16 dense, burst)",
                     "traffic": stored_traffic(w.name, kernel), "contraction_flops_per_launch": flops,
@@ -1038,7 +1037,7 @@ def run_gpu_neighbor(args, w: Workload):
                     "note": "latency-bound: neither the tensor pipe nor HBM is busy (see its profile)"}
         else:
             roof = {"bound": "alu", "kernel": "ssd_scan_bwd (whole call: ssd_bwd_local_kernel, ssd_bwd_pass_kernel, "
-                                              "ssd_bwd_grad_kernel, ssd_bwd_reduce_kernel, ssd_bwd_heads_kernel)",
+                                              "ssd_bwd_grad_kernel, ssd_bwd_finish4_kernel)",
                     "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s", "frac": tf / FP32_PEAK_TFLOPS,
                     "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2070 MHz",
                     "traffic": stored_traffic(w.name, kernel), "fp32_flops_per_launch": flops,

@@ -289,15 +289,69 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce_kernel(const float *dB_hea
     dC[i] = sc;
 }
 
-// The same with four consecutive n per thread (16-byte loads; N % 4 == 0 and
-// 16-byte aligned tensors) and the loads of 8 heads in flight at once; each
-// element is still summed over the heads in order, so the results are those
-// of the scalar form bit for bit.
-__global__ void __launch_bounds__(256) ssd_bwd_reduce4_kernel(const float4 *dB_head, const float4 *dC_head,
-                                                               float4 *dB, float4 *dC, long long total4, int H, int G,
-                                                               int N4)
+// dA_log, d dt_bias, dD [H]: the partials of (b, h) (nper of them, one per
+// chunk or one per sequence) summed over batch rows and partials in order (b,
+// then c).  They are loaded kBatch at a time so that those loads are in flight
+// together; the sums and their order are those of the plain loop.
+__device__ __forceinline__ void heads_sum(const float *part, float *dA_log, float *ddt_bias, float *dD, int Bt, int H,
+                                          int nper, int h)
 {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;   // (row, g, n / 4)
+    const size_t BHC = (size_t)Bt * H * nper;
+    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
+    constexpr int kBatch = 16;
+    const long long n = (long long)Bt * nper;
+    for (long long j0 = 0; j0 < n; j0 += kBatch) {
+        float v0[kBatch], v1[kBatch], v2[kBatch];
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+            if (j0 + k < n) {
+                const long long j = j0 + k, b = j / nper, c = j - b * nper;
+                const size_t i = ((size_t)b * H + h) * nper + c;
+                v0[k] = part[i];
+                v1[k] = part[BHC + i];
+                v2[k] = part[2 * BHC + i];
+            }
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k)
+            if (j0 + k < n) {
+                s0 += v0[k];
+                s1 += v1[k];
+                s2 += v2[k];
+            }
+    }
+    dA_log[h] = s0;
+    ddt_bias[h] = s1;
+    dD[h] = s2;
+}
+
+__global__ void ssd_bwd_heads_kernel(const float *part, float *dA_log, float *ddt_bias, float *dD, int Bt, int H,
+                                     int nper)
+{
+    const int h = blockIdx.x * blockDim.x + threadIdx.x;
+    if (h < H)
+        heads_sum(part, dA_log, ddt_bias, dD, Bt, H, nper, h);
+}
+
+// Both reductions in one launch.  The first hblocks CTAs sum the per-head
+// partials (one thread per head).  The others take dB and dC with four
+// consecutive n per thread (16-byte loads; N % 4 == 0 and 16-byte aligned
+// tensors) and the loads of 8 heads in flight at once; each element is still
+// summed over the heads in order, so the results are those of the scalar form
+// bit for bit.  The two parts read what the launch before wrote and share
+// nothing.
+__global__ void __launch_bounds__(256) ssd_bwd_finish4_kernel(const float4 *dB_head, const float4 *dC_head,
+                                                               float4 *dB, float4 *dC, long long total4, int H, int G,
+                                                               int N4, const float *part, float *dA_log,
+                                                               float *ddt_bias, float *dD, int Bt, int nper,
+                                                               int hblocks)
+{
+    if ((int)blockIdx.x < hblocks) {
+        const int h = blockIdx.x * blockDim.x + threadIdx.x;
+        if (h < H)
+            heads_sum(part, dA_log, ddt_bias, dD, Bt, H, nper, h);
+        return;
+    }
+    const long long i = (long long)(blockIdx.x - hblocks) * blockDim.x + threadIdx.x;   // (row, g, n / 4)
     if (i >= total4)
         return;
     const int n4 = (int)(i % N4);
@@ -326,28 +380,6 @@ __global__ void __launch_bounds__(256) ssd_bwd_reduce4_kernel(const float4 *dB_h
     }
     dB[i] = sb;
     dC[i] = sc;
-}
-
-// dA_log, d dt_bias, dD [H]: the partials of each (b, h) (nper of them, one
-// per chunk or one per sequence) summed over batch rows and partials in order
-__global__ void ssd_bwd_heads_kernel(const float *part, float *dA_log, float *ddt_bias, float *dD, int Bt, int H,
-                                     int nper)
-{
-    const int h = blockIdx.x * blockDim.x + threadIdx.x;
-    if (h >= H)
-        return;
-    const size_t BHC = (size_t)Bt * H * nper;
-    float s0 = 0.f, s1 = 0.f, s2 = 0.f;
-    for (int b = 0; b < Bt; ++b)
-        for (int c = 0; c < nper; ++c) {
-            const size_t i = ((size_t)b * H + h) * nper + c;
-            s0 += part[i];
-            s1 += part[BHC + i];
-            s2 += part[2 * BHC + i];
-        }
-    dA_log[h] = s0;
-    ddt_bias[h] = s1;
-    dD[h] = s2;
 }
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
@@ -382,14 +414,19 @@ cudaError_t bwd_finish_launch(const BwdArgs &a, const float *dB_head, const floa
     SSD_NVTX_RANGE("bwd_finish_launch");
     const long long total = (long long)a.batch * a.seqlen * a.ngroups * a.dstate;
     auto aligned16 = [](const void *q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
-    if (a.dstate % 4 == 0 && aligned16(dB_head) && aligned16(dC_head) && aligned16(a.dB) && aligned16(a.dC))
-        ssd_bwd_reduce4_kernel<<<(unsigned)((total / 4 + 255) / 256), 256, 0, st>>>(
+    if (a.dstate % 4 == 0 && aligned16(dB_head) && aligned16(dC_head) && aligned16(a.dB) && aligned16(a.dC)) {
+        const int hblocks = (a.nheads + 255) / 256;
+        ssd_bwd_finish4_kernel<<<(unsigned)(hblocks + (total / 4 + 255) / 256), 256, 0, st>>>(
             reinterpret_cast<const float4 *>(dB_head), reinterpret_cast<const float4 *>(dC_head),
             reinterpret_cast<float4 *>(a.dB), reinterpret_cast<float4 *>(a.dC), total / 4, a.nheads, a.ngroups,
-            a.dstate / 4);
-    else
-        ssd_bwd_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(dB_head, dC_head, a.dB, a.dC, total,
-                                                                              a.nheads, a.ngroups, a.dstate);
+            a.dstate / 4, part, a.dA_log, a.ddt_bias, a.dD, (int)a.batch, nper, hblocks);
+        const cudaError_t e = cudaGetLastError();
+        if (e == cudaSuccess)
+            note_launches(1);
+        return e;
+    }
+    ssd_bwd_reduce_kernel<<<(unsigned)((total + 255) / 256), 256, 0, st>>>(dB_head, dC_head, a.dB, a.dC, total,
+                                                                          a.nheads, a.ngroups, a.dstate);
     ssd_bwd_heads_kernel<<<(a.nheads + 127) / 128, 128, 0, st>>>(part, a.dA_log, a.ddt_bias, a.dD, (int)a.batch,
                                                                  a.nheads, nper);
     const cudaError_t e = cudaGetLastError();
