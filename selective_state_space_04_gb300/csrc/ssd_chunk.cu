@@ -1474,6 +1474,7 @@ int sm_count()
 
 struct Geometry {
     long long nchunks, nchains, chunks_per_unit, nranges, nunits, grid;
+    long long seqlen, span;   // steps per unit: chunks_per_unit chunks, or (split) whole sub-chunks
     bool split;    // two passes with a combine in between, instead of chained units
     bool pieces;   // chained, one run of equal length per CTA (see decode_piece)
     long long nsub_chain, total_subs;
@@ -1503,19 +1504,20 @@ double chained_estimate(long long R, long long nchunks, long long nchains, int Q
     return std::max(rounds * unit_time, ranges * unit_time);
 }
 
-// Estimated time of the split schedule: two passes over independent units (no
-// handoff wait, about half a sub-chunk to refill the pipeline per unit), of which
-// pass 1 (end states only: B and x loads and the state MMA) measured about half
-// as long as pass 3; then the combine, whose batched loads stream every unit's
-// state (64 KB) in and out at about 2 ns per unit (in sub-chunk times of about
-// 3 us), and about one sub-chunk for the two extra launches.
-double split_estimate(long long R, long long nchunks, long long nchains, int Q, long long grid)
+// Estimated time of the split schedule with units of `len` blocks of
+// `subs_per_block` sub-chunks each (nblocks blocks per chain): two passes over
+// independent units (no handoff wait, about half a sub-chunk to refill the
+// pipeline per unit), of which pass 1 (end states only: B and x loads and the
+// state MMA) measured about half as long as pass 3; then the combine, whose
+// batched loads stream every unit's state (64 KB) in and out at about 2 ns per
+// unit (in sub-chunk times of about 3 us), and about one sub-chunk for the two
+// extra launches.
+double split_estimate(long long len, long long nblocks, long long nchains, double subs_per_block, long long grid)
 {
-    const double subs_per_chunk = (double)Q / kT;
-    const long long ranges = (nchunks + R - 1) / R;
+    const long long ranges = (nblocks + len - 1) / len;
     const long long units = ranges * nchains;
     const long long rounds = (units + grid - 1) / grid;
-    const double pass = rounds * (R * subs_per_chunk + 0.5);
+    const double pass = rounds * (len * subs_per_block + 0.5);
     const double combine = units * 0.002 + 1.0;
     return 1.5 * pass + combine;
 }
@@ -1525,6 +1527,7 @@ void layout(Geometry &g, long long grid_p, int sms);
 Geometry geometry(const ScanArgs &a)
 {
     Geometry g;
+    g.seqlen = a.seqlen;
     g.nchunks = (a.seqlen + a.chunk - 1) / a.chunk;
     g.nchains = a.batch * (a.nheads / 2);
     g.nsub_chain = (a.seqlen + kT - 1) / kT;
@@ -1554,20 +1557,37 @@ Geometry geometry(const ScanArgs &a)
         g.pieces = true;
     g.split = false;
     const bool split_allowed = a.sched_req == SSD_SCHEDULE_SPLIT || (a.sched_req == 0 && a.scratch_cap == 0);
+    g.span = g.chunks_per_unit * a.chunk;
     if (split_allowed && g.nchunks > 1) {
         double best_split = 1e300;
-        long long r_split = 1;
+        long long span_split = a.chunk;
         for (int i = 0; i + 1 < nc; ++i) {   // at least two ranges
-            const double est = split_estimate(cand[i], g.nchunks, g.nchains, a.chunk, sms);
+            const double est = split_estimate(cand[i], g.nchunks, g.nchains, (double)a.chunk / kT, sms);
             if (est < best_split * 0.999) {
                 best_split = est;
-                r_split = cand[i];
+                span_split = cand[i] * a.chunk;
             }
         }
         if (best_split < 0.8 * best || a.sched_req == SSD_SCHEDULE_SPLIT) {
             g.split = true;
             g.pieces = false;
-            g.chunks_per_unit = r_split;
+            // Once split, where a chunk is a whole number of the kernel's 128-step
+            // sub-chunks, a unit may be any whole number of sub-chunks (the sub-chunk
+            // grid of every chain stays where it is): the lengths that make the units
+            // fill whole rounds of the grid.  Units stay fewer than 2^31.
+            if (a.chunk % kT == 0) {
+                const long long smax = std::min<long long>(g.nsub_chain - 1, 4096);
+                for (long long S = 1; S <= smax; ++S) {
+                    if ((g.nsub_chain + S - 1) / S > ((1LL << 31) - 1) / std::max<long long>(1, g.nchains))
+                        continue;
+                    const double est = split_estimate(S, g.nsub_chain, g.nchains, 1.0, sms);
+                    if (est < best_split * 0.99) {
+                        best_split = est;
+                        span_split = S * kT;
+                    }
+                }
+            }
+            g.span = span_split;
         }
     }
     layout(g, grid_p, sms);
@@ -1585,13 +1605,14 @@ void layout(Geometry &g, long long grid_p, int sms)
     size_t flag_rows, slot_bytes;
     if (g.pieces) {
         g.chunks_per_unit = g.nchunks;
+        g.span = g.seqlen;
         g.nranges = 1;
         g.grid = grid_p;
         g.nunits = 0;
         flag_rows = (size_t)g.grid;   // one per boundary between CTAs
         slot_bytes = g.grid > 1 ? (size_t)g.grid * slot_state : 0;
     } else {
-        g.nranges = (g.nchunks + g.chunks_per_unit - 1) / g.chunks_per_unit;
+        g.nranges = (g.seqlen + g.span - 1) / g.span;
         g.nunits = g.nranges * g.nchains;
         g.grid = std::min<long long>(sms, g.nunits);
         flag_rows = (size_t)g.nunits;
@@ -1668,7 +1689,7 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     p.L = a.seqlen;
     p.nunits = geo.nunits;
     p.H = a.nheads;
-    p.span = (int)(geo.chunks_per_unit * a.chunk);
+    p.span = (int)geo.span;
     p.nranges = (int)geo.nranges;
     p.nsub_chain = (int)geo.nsub_chain;
     p.total_subs = geo.total_subs;
