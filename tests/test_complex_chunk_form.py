@@ -34,7 +34,7 @@ def _interleave(z):
     return out
 
 
-def chunk_form(x, dt_raw, dt_bias, A_polar, B, C, D, init_state, Q, block=16):
+def chunk_form(x, dt_raw, dt_bias, A_polar, B, C, D, init_state, Q, block=16, slip=None):
     """y [Bt,L,H,P] and the final state [Bt,H,P,N] by the chunk form above."""
     Bt, L, H, P = x.shape
     G, N = B.shape[2], B.shape[3]
@@ -58,6 +58,8 @@ def chunk_form(x, dt_raw, dt_bias, A_polar, B, C, D, init_state, Q, block=16):
                 Chat[:, 1::2] *= -1.0
                 Ctil = np.empty_like(Cr)
                 Ctil[:, 0::2], Ctil[:, 1::2] = Cr[:, 1::2], Cr[:, 0::2]
+                if slip == "sign_in_Ctil":
+                    Ctil[:, 0::2] *= -1.0
                 S_re, S_im = Chat @ Br.T, Ctil @ Br.T                   # [t][s]
                 M = np.zeros((n, n))
                 for s0 in range(0, n, block):
@@ -73,11 +75,13 @@ def chunk_form(x, dt_raw, dt_bias, A_polar, B, C, D, init_state, Q, block=16):
                 LC = lam[:, None] * Cc
                 CL = np.empty_like(Cr)
                 CL[:, 0::2], CL[:, 1::2] = LC.real, -LC.imag
+                if slip == "sign_in_CL":
+                    CL[:, 1::2] *= -1.0
                 xs = x[b, st, h]
-                y[b, st, h] = M @ xs + CL @ Hs + D[h] * xs
+                y[b, st, h] = M @ xs + (0.0 if slip == "no_state_term" else CL @ Hs) + D[h] * xs
                 gs = np.exp(a * (tau[-1] - tau)) * f
                 Bt_ = _interleave(gs[:, None] * (Br[:, 0::2] + 1j * Br[:, 1::2]))   # B~ [n][N]
-                Hc = (Hs[0::2] + 1j * Hs[1::2]) * lam[-1]                         # rot(Lambda_last) H
+                Hc = (Hs[0::2] + 1j * Hs[1::2]) * (1.0 if slip == "no_rotation" else lam[-1])   # rot(Lambda_last) H
                 Hs = np.empty_like(Hs)
                 Hs[0::2], Hs[1::2] = Hc.real, Hc.imag
                 Hs = Hs + Bt_.T @ xs
@@ -123,4 +127,12 @@ def test_a_conjugated_product_is_caught():
     Cb = c["C"].copy()
     Cb[..., 1::2] *= -1.0              # C_i -> -C_i everywhere: the readout of conj(C)
     y1, _ = chunk_form(**bad | {"C": Cb}, Q=64)
+    assert _rel(y1, y0) > 1e-2
+
+
+@pytest.mark.parametrize("slip", ["sign_in_Ctil", "sign_in_CL", "no_state_term", "no_rotation"])
+def test_planted_slips_are_caught(slip):
+    c = _case(13, Bt=2, L=200, H=3, P=5, N=8, G=1, init=True)
+    y0, _ = complex_fwd(**c)
+    y1, _ = chunk_form(**c, Q=64, slip=slip)
     assert _rel(y1, y0) > 1e-2
