@@ -660,10 +660,15 @@ __device__ __forceinline__ bool conv_x_tile(uint8_t *smem, uint64_t *bars, const
 // decay alpha_t, input weight w_t = gamma_t + dt_{t+1} (1 - trap_{t+1}) (gamma
 // alone at the last step), y_t = q_t h~_t + (D - dt_{t+1} (1 - trap_{t+1}) q_t.k_t) v_t
 // (a correction on the diagonal of M), entering state h0 + dt_0 (1 - trap_0) k0 v0^T.
-template <bool kPieces, bool kTrap, bool kLocal, bool kConv = false>
+// kFold: split pass 3 with the combine folded in, for few ranges: a unit's
+//   entering state is formed at its start from the initial state and the end
+//   states and decays its predecessors left in pass 1, by the combine's
+//   arithmetic (E_0 = h0 or 0, E_{j+1} = Lambda_j E_j + S_j, in range order).
+template <bool kPieces, bool kTrap, bool kLocal, bool kConv = false, bool kFold = false>
 __global__ void __launch_bounds__(kThreads, 1)
     ssd_chunk_fused_kernel(const __grid_constant__ Maps maps, const ChunkParams p)
 {
+    static_assert(!kFold || (!kPieces && !kTrap && !kLocal && !kConv), "the folded combine is split pass 3 only");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                 ~static_cast<uintptr_t>(1023));
@@ -1146,12 +1151,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 uint32_t v[2][32];
-                // split pass 3 is launched as a programmatic dependent of the combine:
-                // its other roles start on the inputs, and this group waits for the
-                // combined entering states here (a no-op once passed)
+                // split pass 3 is launched as a programmatic dependent of the combine
+                // (of pass 1 with the combine folded in): its other roles start on the
+                // inputs, and this group waits for the launch before it here (a no-op
+                // once passed)
                 if (p.mode == kSplitEntering)
                     asm volatile("griddepcontrol.wait;" ::: "memory");
-                if (!cur.first() && p.mode != kSplitLocal) {
+                if (kFold && !cur.first()) {
+                    // E_0: the initial state (or 0), then each predecessor's end state S_j and
+                    // decay Lambda_j from pass 1, half a row (8 float4) of S_j at a time
+                    if (p.init_state) {
+                        const float *src = p.init_state + ((size_t)cur.w.b * p.H + hh) * (size_t)(kP * kN) + r;
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            v[i >> 5][i & 31] = __float_as_uint(__ldg(src + (size_t)i * kN));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 64; ++i)
+                            v[i >> 5][i & 31] = 0u;
+                    }
+                    const int rg = cur.u / p.nchains, chain = cur.u - rg * p.nchains;
+                    for (int jj = 0; jj < rg; ++jj) {
+                        const size_t uj = (size_t)jj * p.nchains + chain;
+                        const float lam = __ldcg(p.unit_decay + uj * 2 + hf);
+                        const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (uj * 2 + hf) * 16 * kN + r;
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            float4 sv[8];
+#pragma unroll
+                            for (int i = 0; i < 8; ++i)
+                                sv[i] = __ldcg(src + (size_t)(8 * half + i) * kN);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                uint32_t *e = &v[half][4 * i];
+                                e[0] = __float_as_uint(fmaf(lam, __uint_as_float(e[0]), sv[i].x));
+                                e[1] = __float_as_uint(fmaf(lam, __uint_as_float(e[1]), sv[i].y));
+                                e[2] = __float_as_uint(fmaf(lam, __uint_as_float(e[2]), sv[i].z));
+                                e[3] = __float_as_uint(fmaf(lam, __uint_as_float(e[3]), sv[i].w));
+                            }
+                        }
+                    }
+                } else if (!cur.first() && p.mode != kSplitLocal) {
                     const float4 *src = reinterpret_cast<const float4 *>(p.slots) + (slot_of * 2 + hf) * 16 * kN + r;
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -1598,6 +1638,16 @@ Geometry geometry(const ScanArgs &a)
     return g;
 }
 
+// Split evaluations of at most this many ranges per chain fold the combine into
+// pass 3 (ssd_chunk_fused_kernel's kFold): each unit then reads at most three
+// predecessors' end states at its start, in place of one combine launch.
+constexpr long long kFoldMaxRanges = 4;
+
+bool split_folds(const ScanArgs &a, const Geometry &g)
+{
+    return g.split && !a.conv && !a.trap && g.nranges <= kFoldMaxRanges;
+}
+
 // Grid and scratch layout of the chosen schedule.
 void layout(Geometry &g, long long grid_p, int sms)
 {
@@ -1735,7 +1785,13 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
         return SSD_OK;
     }
     // split: pass 1 (end state of every unit from zero), combine (entering state of
-    // every unit), pass 3 (the scan itself, all units independent)
+    // every unit), pass 3 (the scan itself, all units independent); with few ranges
+    // the combine is folded into pass 3
+    const bool fold = split_folds(a, geo);
+    auto kernel_fold = ssd_chunk_fused_kernel<false, false, false, false, true>;
+    if (fold && cudaFuncSetAttribute(kernel_fold, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+                    cudaSuccess)
+        return SSD_ERR_CUDA;
     p.mode = kSplitLocal;
     if (cudaLaunchKernelEx(&cfg, kernel_local, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
@@ -1743,34 +1799,40 @@ ssd_status_t chunk_launch(const ScanArgs &a, void *workspace, cudaStream_t strea
     // The combine and pass 3 are programmatic dependents of the launch before them
     // (each waits with griddepcontrol.wait before it reads what that launch wrote),
     // so their launch and setup overlap the previous kernel's tail.
-    const long long threads = geo.nchains * 2 * 16 * kN;
-    cudaLaunchConfig_t ccfg = {};
-    ccfg.gridDim = dim3((unsigned)((threads + 255) / 256));
-    ccfg.blockDim = dim3(256);
-    ccfg.stream = stream;
     cudaLaunchAttribute pdl[2];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
-    ccfg.attrs = pdl;
-    ccfg.numAttrs = 1;
-    // (the trapezoidal pass 1 has put each chain's entering state into its first unit)
-    if (cudaLaunchKernelEx(&ccfg, ssd_split_combine_kernel, p.slots, (const float *)p.unit_decay,
-                           a.trap ? nullptr : a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2,
-                           a.nheads) != cudaSuccess)
-        return SSD_ERR_CUDA;
-    note_launches(1);
+    if (!fold) {
+        const long long threads = geo.nchains * 2 * 16 * kN;
+        cudaLaunchConfig_t ccfg = {};
+        ccfg.gridDim = dim3((unsigned)((threads + 255) / 256));
+        ccfg.blockDim = dim3(256);
+        ccfg.stream = stream;
+        ccfg.attrs = pdl;
+        ccfg.numAttrs = 1;
+        // (the trapezoidal pass 1 has put each chain's entering state into its first unit)
+        if (cudaLaunchKernelEx(&ccfg, ssd_split_combine_kernel, p.slots, (const float *)p.unit_decay,
+                               a.trap ? nullptr : a.init_state, (int)geo.nchains, (int)geo.nranges, a.nheads / 2,
+                               a.nheads) != cudaSuccess)
+            return SSD_ERR_CUDA;
+        note_launches(1);
+    }
     p.mode = kSplitEntering;
     p.epoch = next_epoch();
     pdl[1] = attr[0];   // cooperative
     cfg.attrs = pdl;
     cfg.numAttrs = 2;
-    if (cudaLaunchKernelEx(&cfg, kernel, maps, p) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, fold ? kernel_fold : kernel, maps, p) != cudaSuccess)
         return SSD_ERR_CUDA;
     note_launches(1);
     return SSD_OK;
 }
 
-int chunk_launches(const ScanArgs &a) { return geometry(a).split ? 3 : 1; }
+int chunk_launches(const ScanArgs &a)
+{
+    const Geometry g = geometry(a);
+    return g.split ? (split_folds(a, g) ? 2 : 3) : 1;
+}
 
 int chunk_schedule(const ScanArgs &a)
 {

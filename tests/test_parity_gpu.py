@@ -338,6 +338,39 @@ def test_weak_decay_state_passing(ssd, seqlen, H):
     assert relerr(y0, ref_y) > 10 * 2e-2
 
 
+@pytest.mark.parametrize("init", [True, False])
+def test_split_with_folded_combine_weak_decay(ssd, init):
+    # few ranges per chain (the 130M layer's shape: 48 chains of 3 ranges): pass 3
+    # forms each unit's entering state from its predecessors' end states (two
+    # launches, no combine); weak decay makes those states matter
+    w = WORKLOADS["mamba2_130m_layer"].with_(init_state=init)
+    shape = (w.batch, w.seqlen, w.nheads, w.headdim)
+    assert ssd.chunk_schedule(shape, w.ngroups, w.dstate, w.chunk) == "split"
+    assert ssd.launches_per_call(shape, w.ngroups, w.dstate, w.chunk) == 2
+    inp = _weak_decay(make_inputs(w, seed=90 + init), w.nheads)
+    launches = ssd.launch_count()
+    y, fin = run(ssd, inp, w, init=init)
+    assert ssd.launch_count() - launches == 2
+    yc, fc = y.cpu(), fin.cpu()
+    num_y = den_y = num_f = den_f = 0.0
+    for b, h in sample_pairs(w, 8, seed=3):
+        ry, rf = oracle_pair(inp, w, b, h)
+        num_y = max(num_y, float(np.max(np.abs(yc[b, :, h].double().numpy() - ry))))
+        den_y = max(den_y, float(np.max(np.abs(ry))))
+        num_f = max(num_f, float(np.max(np.abs(fc[b, h].double().numpy() - rf))))
+        den_f = max(den_f, float(np.max(np.abs(rf))))
+    print(f"rel err y {num_y / den_y:.3e}  final state {num_f / den_f:.3e}")
+    assert num_y / den_y <= TOL["bf16"] and num_f / den_f <= TOL["bf16"]
+    # the state entering the second range matters: restarting there from zero moves y far
+    ry, _ = oracle_pair(inp, w, 0, 0)
+    t0 = 768
+    tail = dict(x=inp["x"][0:1, t0:, 0:1], dt_raw=inp["dt_raw"][0:1, t0:, 0:1], dt_bias=inp["dt_bias"][0:1],
+                A_log=inp["A_log"][0:1], B=inp["B"][0:1, t0:, 0:1], C=inp["C"][0:1, t0:, 0:1], D=inp["D"][0:1],
+                init_state=None)
+    rt, _ = oracle.ssd_fwd(**tail)
+    assert relerr(rt[0, :, 0], ry[t0:]) > 10 * TOL["bf16"]
+
+
 # ----------------------------------------------------------- piece schedule
 # On request: each CTA takes one run of equal length over the chains' sub-chunks
 # laid end to end; with more chains than SMs some chains are cut between two
