@@ -448,9 +448,14 @@ int32_t ssd_launches_per_call(const ssd_dims_t *dims);
  *   SSD_SCHEDULE_PIECES  the chains' 128-step sub-chunks, chain after chain, cut
  *                        into one run of equal length per CTA; a chain cut
  *                        between two CTAs hands its state across (one launch);
- *   SSD_SCHEDULE_SPLIT   every unit's end state from zero, a combine of those
+ *   SSD_SCHEDULE_SPLIT   units of whole chunks or (where a chunk is a whole
+ *                        number of 128-step sub-chunks) of whole sub-chunks:
+ *                        every unit's end state from zero, a combine of those
  *                        states along each chain, then every unit from its
- *                        combined entering state (three launches).
+ *                        combined entering state (three launches; two where a
+ *                        chain has at most 4 units and the scan has no conv or
+ *                        trapezoidal mode: each unit then combines its
+ *                        predecessors' end states itself).
  * All three evaluate the chunked recurrence with the state carried from chunk
  * to chunk; they differ only in which CTA computes what, and when.
  * ssd_scan_fwd_noalloc may choose differently (see there).  Returns -(ssd_status_t)
